@@ -1,0 +1,9 @@
+"""CPU oracle of the sparse-decode KV offload step (test infrastructure only).
+
+Only the tests, the smoke check and the benchmark's CPU-baseline leg may use
+this package; the library path never imports it.
+"""
+from .oracle import (  # noqa: F401
+    OK, EINVAL, ENOMEM, ERANGE, ECAPACITY, PAD_PAYLOAD, DIM, OracleUnit, StepResult, build,
+    lib, score, step_many, threads,
+)

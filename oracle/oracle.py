@@ -1,0 +1,204 @@
+"""ctypes wrapper of the CPU oracle (kvo_oracle.c).
+
+TEST INFRASTRUCTURE ONLY: the tests, the smoke check and the benchmark's
+CPU-baseline leg use it; the library path never does.
+"""
+import ctypes
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+OK = 0
+EINVAL = -1
+ENOMEM = -2
+ERANGE = -3
+ECAPACITY = -6
+PAD_PAYLOAD = -(2 ** 31)
+DIM = 128
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "kvo_oracle.c")
+_SO = os.path.join(_HERE, "libkvo_oracle.so")
+_lock = threading.Lock()
+_lib = None
+
+
+def build(force=False):
+    """Compile the oracle with plain gcc: no fast-math, no FP contraction."""
+    if not force and os.path.exists(_SO) and os.path.getmtime(_SO) >= os.path.getmtime(_SRC):
+        return _SO
+    tmp = _SO + ".tmp%d" % os.getpid()
+    cmd = ["gcc", "-O2", "-std=c11", "-fPIC", "-shared", "-fopenmp", "-ffp-contract=off",
+           "-fno-fast-math", _SRC, "-o", tmp, "-lm"]
+    subprocess.run(cmd, check=True)
+    os.replace(tmp, _SO)
+    return _SO
+
+
+def lib():
+    global _lib
+    with _lock:
+        if _lib is None:
+            build()
+            L = ctypes.CDLL(_SO)
+            vp, i32, i64 = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64
+            L.oracle_unit_new.restype = vp
+            L.oracle_unit_new.argtypes = [i64, i32, i32, i32, i32, i32, i32]
+            L.oracle_unit_free.restype = None
+            L.oracle_unit_free.argtypes = [vp]
+            L.oracle_append.restype = i32
+            L.oracle_append.argtypes = [vp, i32, vp, vp]
+            L.oracle_step.restype = i32
+            L.oracle_step.argtypes = [vp] + [vp] * 9
+            L.oracle_step_many.restype = i32
+            L.oracle_step_many.argtypes = [vp, i32] + [vp] * 9
+            L.oracle_score.restype = ctypes.c_float
+            L.oracle_score.argtypes = [vp, vp]
+            L.oracle_scores.restype = None
+            L.oracle_scores.argtypes = [vp, vp, i64, vp]
+            L.oracle_threads.restype = i32
+            L.oracle_threads.argtypes = []
+            L.oracle_len.restype = i64
+            L.oracle_len.argtypes = [vp]
+            L.oracle_stamp.restype = ctypes.c_uint32
+            L.oracle_stamp.argtypes = [vp]
+            for name in ("oracle_cache_slots", "oracle_slot_token", "oracle_last_use",
+                         "oracle_hot", "oracle_rows", "oracle_keys"):
+                getattr(L, name).restype = vp
+                getattr(L, name).argtypes = [vp]
+            _lib = L
+    return _lib
+
+
+def score(q, k):
+    """Canonical fp32 score of one 128-element bf16 query/key pair (uint16 arrays)."""
+    q = np.ascontiguousarray(q, dtype=np.uint16)
+    k = np.ascontiguousarray(k, dtype=np.uint16)
+    assert q.size == DIM and k.size == DIM
+    return np.float32(lib().oracle_score(q.ctypes.data, k.ctypes.data))
+
+
+class StepResult:
+    __slots__ = ("tok", "score", "pay", "slot", "status", "miss_tok", "miss_slot", "n_miss")
+
+    def misses(self):
+        return list(zip(self.miss_tok[: self.n_miss].tolist(), self.miss_slot[: self.n_miss].tolist()))
+
+
+class OracleUnit:
+    """One (request, layer) unit: host rows, indexer keys, hot shelf, LRU table."""
+
+    def __init__(self, max_tokens, topk, capacity, n_pos, row_elems=576, keep_rows=True):
+        self.L = lib()
+        self.max_tokens, self.topk, self.capacity, self.n_pos = max_tokens, topk, capacity, n_pos
+        self.row_elems, self.keep_rows = row_elems, keep_rows
+        self.h = self.L.oracle_unit_new(max_tokens, DIM, row_elems, topk, capacity, n_pos,
+                                        1 if keep_rows else 0)
+        if not self.h:
+            raise MemoryError("oracle_unit_new failed")
+
+    def __del__(self):
+        h = getattr(self, "h", None)
+        if h:
+            self.L.oracle_unit_free(h)
+            self.h = None
+
+    def append(self, keys, rows=None):
+        keys = np.ascontiguousarray(keys, dtype=np.uint16).reshape(-1, DIM)
+        n = keys.shape[0]
+        rp = None
+        if rows is not None:
+            rows = np.ascontiguousarray(rows, dtype=np.uint16).reshape(n, self.row_elems)
+            rp = rows.ctypes.data
+        return self.L.oracle_append(self.h, n, rp, keys.ctypes.data)
+
+    def step(self, queries):
+        q = np.ascontiguousarray(queries, dtype=np.uint16).reshape(self.n_pos, DIM)
+        P, K = self.n_pos, self.topk
+        r = StepResult()
+        r.tok = np.empty((P, K), np.int32)
+        r.score = np.empty((P, K), np.float32)
+        r.pay = np.empty((P, K), np.int32)
+        r.slot = np.empty((P, K), np.int32)
+        st = np.zeros(1, np.int32)
+        r.miss_tok = np.full(P * K, -1, np.int32)
+        r.miss_slot = np.full(P * K, -1, np.int32)
+        nm = np.zeros(1, np.int32)
+        rc = self.L.oracle_step(self.h, q.ctypes.data, r.tok.ctypes.data, r.score.ctypes.data,
+                                r.pay.ctypes.data, r.slot.ctypes.data, st.ctypes.data,
+                                r.miss_tok.ctypes.data, r.miss_slot.ctypes.data, nm.ctypes.data)
+        if rc != OK:
+            raise RuntimeError("oracle_step failed: %d" % rc)
+        r.status = int(st[0])
+        r.n_miss = int(nm[0])
+        return r
+
+    def scores(self, query, n=None):
+        n = self.length if n is None else n
+        q = np.ascontiguousarray(query, dtype=np.uint16).reshape(DIM)
+        out = np.empty(n, np.float32)
+        self.L.oracle_scores(self.h, q.ctypes.data, n, out.ctypes.data)
+        return out
+
+    def _view(self, fn, n, dtype):
+        p = getattr(self.L, fn)(self.h)
+        if not p or n == 0:
+            return np.empty(0, dtype)
+        buf = (ctypes.c_char * (n * np.dtype(dtype).itemsize)).from_address(p)
+        return np.frombuffer(buf, dtype=dtype, count=n).copy()
+
+    @property
+    def length(self):
+        return int(self.L.oracle_len(self.h))
+
+    @property
+    def stamp(self):
+        return int(self.L.oracle_stamp(self.h))
+
+    def cache_slots(self):
+        return self._view("oracle_cache_slots", self.max_tokens, np.int32)
+
+    def slot_token(self):
+        return self._view("oracle_slot_token", self.capacity, np.int32)
+
+    def last_use(self):
+        return self._view("oracle_last_use", self.capacity, np.uint32)
+
+    def hot(self):
+        assert self.keep_rows
+        return self._view("oracle_hot", self.capacity * self.row_elems, np.uint16).reshape(
+            self.capacity, self.row_elems)
+
+    def rows(self):
+        assert self.keep_rows
+        return self._view("oracle_rows", self.max_tokens * self.row_elems, np.uint16).reshape(
+            self.max_tokens, self.row_elems)
+
+
+def step_many(units, queries):
+    """One step of many units in parallel (OpenMP).  queries: [n][P][128] uint16."""
+    L = lib()
+    n = len(units)
+    P, K = units[0].n_pos, units[0].topk
+    q = np.ascontiguousarray(queries, dtype=np.uint16).reshape(n, P, DIM)
+    hs = (ctypes.c_void_p * n)(*[u.h for u in units])
+    tok = np.empty((n, P, K), np.int32)
+    sc = np.empty((n, P, K), np.float32)
+    pay = np.empty((n, P, K), np.int32)
+    sl = np.empty((n, P, K), np.int32)
+    st = np.zeros(n, np.int32)
+    mt = np.empty((n, P * K), np.int32)
+    ms = np.empty((n, P * K), np.int32)
+    nm = np.zeros(n, np.int32)
+    rc = L.oracle_step_many(hs, n, q.ctypes.data, tok.ctypes.data, sc.ctypes.data,
+                            pay.ctypes.data, sl.ctypes.data, st.ctypes.data, mt.ctypes.data,
+                            ms.ctypes.data, nm.ctypes.data)
+    if rc != OK:
+        raise RuntimeError("oracle_step_many failed: %d" % rc)
+    return tok, sc, pay, sl, st, nm
+
+
+def threads():
+    return int(lib().oracle_threads())
