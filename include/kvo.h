@@ -1,0 +1,216 @@
+/*
+ * kvo.h -- C ABI of the GB300-native sparse-decode KV offload hot path.
+ *
+ * The operation follows two web pages:
+ *  [LS] "Layerwise and Sparse KV Cache Offloading Design", section 4 "Sparse
+ *       Decode Offload": "Memory layout" (full main KV in a pinned host pool;
+ *       indexer cache and per-layer hot K/V buffers in device memory) and
+ *       "Decode step" (steps 1-6: new-token rows to their logical host slots,
+ *       indexer top-k, LRU residency table, miss-row copy host -> device,
+ *       logical -> physical remap).  Section 2 "Transfer granularity": token
+ *       rows device -> host, top-k miss rows host -> device.
+ *  [FO] "FlashOffloading offloads all KV cache ... What does it mean?", the
+ *       decode paragraphs: fixed-size hot shelf, MTP3 per-position miss lists
+ *       merged and deduplicated, the cache_slots reverse index (-1 when
+ *       absent), token index and slot packed into one int32 before selection.
+ *
+ * Units.  A unit is one (request r, layer l) pair, u = r * n_layers + l.
+ * Every unit owns: a host row pool [max_tokens][row_elems] bf16 (pinned,
+ * mapped), an indexer cache [max_tokens][128] bf16 and a hot buffer
+ * [hot_capacity][row_elems] bf16 in device memory, cache_slots[max_tokens]
+ * (token -> hot slot, -1 absent), slot_token[hot_capacity] (slot -> token,
+ * -1 free), last_use[hot_capacity] (stamp of the last step that used the
+ * slot) and a step stamp.  Units never interact.
+ *
+ * Semantics fixed by this library where the pages are silent (the CPU oracle
+ * shipped with the tests states the same rules):
+ *  - score: single-head fp32 dot product of bf16 query and key, summed as 16
+ *    FMA chains over d = 8j..8j+7 followed by the tree c_j += c_{j+w},
+ *    w = 8, 4, 2, 1; zero returned as +0.
+ *  - selection order: score descending, then token ascending; outputs keep
+ *    that order.  Position p (of P) sees tokens t < len - (P - 1 - p).
+ *  - payload: cache_slots[t] when >= 0 (hit: the slot), else -(t + 1)
+ *    (miss: the token); read before the step's update.  Padding entries (a
+ *    position sees fewer than k tokens): token -1, score -inf, payload
+ *    KVO_PAD_PAYLOAD, slot -1.
+ *  - merge: the step's wanted set W is the distinct tokens of all P lists;
+ *    misses are filled in token order.
+ *  - LRU: the unit's stamp grows by one per successful step; victims are the
+ *    slots not holding a token of W, in (last_use asc, slot asc) order
+ *    (free slots have last_use 0); every slot of W gets last_use = stamp.
+ *  - capacity: |W| > hot_capacity -> unit status KVO_ECAPACITY, the unit's
+ *    state and hot rows stay unchanged, its slots are -1.
+ *
+ * Conventions.  Every call returns 0 (KVO_OK) or a negative KVO_E* code;
+ * kvo_last_error() gives a thread-local message.  kvo_append and kvo_step
+ * are asynchronous on the caller's CUDA stream (a cudaStream_t passed as
+ * void*, NULL = legacy default stream) and never synchronise the device;
+ * they return only argument and launch errors.  Per-unit results go to the
+ * device array unit_status.  The caller owns queries, inputs, outputs and
+ * the stream; the library owns the host pool, the indexer cache, the hot
+ * buffers and the residency metadata.  A handle is not thread-safe, and calls
+ * on one handle must be ordered (same stream, or synchronised by the caller).
+ * Device pointers are plain CUDA device addresses (any allocator).
+ */
+#ifndef KVO_H
+#define KVO_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define KVO_OK 0
+#define KVO_EINVAL (-1)    /* bad argument or configuration */
+#define KVO_ENOMEM (-2)    /* host or device allocation failed */
+#define KVO_ERANGE (-3)    /* append past max_tokens, unit index out of range */
+#define KVO_ECUDA (-4)     /* CUDA runtime error (no device, launch failure) */
+#define KVO_ETIMEOUT (-5)  /* a bounded device-side wait expired (unit status) */
+#define KVO_ECAPACITY (-6) /* |W| > hot_capacity (unit status only) */
+
+#define KVO_PAD_PAYLOAD INT32_MIN
+
+typedef struct kvo_handle kvo_handle;
+
+typedef struct kvo_config {
+  int32_t n_requests;   /* >= 1 */
+  int32_t n_layers;     /* >= 1; units = n_requests * n_layers */
+  int64_t max_tokens;   /* cached tokens per unit, upper bound, >= 1, < 2^31 */
+  int32_t idx_dim;      /* indexer dimension: must be 128 */
+  int32_t row_elems;    /* bf16 elements of one main-KV row (576 for MLA), multiple of 8 */
+  int32_t topk;         /* k, 1..4096, <= hot_capacity */
+  int32_t hot_capacity; /* hot slots per unit, 1..2^24 */
+  int32_t n_positions;  /* P query positions per step, 1..8 (4 = MTP3) */
+  int32_t device;       /* CUDA device ordinal */
+} kvo_config;
+
+typedef struct kvo_stats {
+  uint64_t steps;           /* kvo_step calls */
+  uint64_t unit_steps;      /* unit steps that ended KVO_OK */
+  uint64_t capacity_errors; /* unit steps that ended KVO_ECAPACITY */
+  uint64_t hits;            /* distinct selected tokens already resident */
+  uint64_t misses;          /* distinct selected tokens filled from host */
+  uint64_t rows_h2d;        /* rows copied host pool -> hot buffer (counted by the copy kernel) */
+  uint64_t bytes_h2d;
+  uint64_t rows_d2h;        /* rows appended device -> host pool (counted by the copy kernel) */
+  uint64_t bytes_d2h;
+  uint64_t timeouts;        /* bounded device waits that expired */
+} kvo_stats;
+
+/* Options for kvo_set_option. */
+#define KVO_OPT_GATHER_MODE 1 /* value: KVO_GATHER_LDG (default) | KVO_GATHER_BULK */
+#define KVO_OPT_WAIT_LIMIT_NS 2 /* bound of every device-side wait, ns (default 2e9) */
+#define KVO_GATHER_LDG 0  /* miss rows read by 16-byte loads from the mapped host pool */
+#define KVO_GATHER_BULK 1 /* miss rows moved by bulk async copies through shared memory */
+
+/*
+ * kvo_create: allocate one handle ([LS] "Memory layout").  cfg is read, not
+ * kept.  Allocates the pinned mapped host pool (units * max_tokens *
+ * row_elems * 2 bytes), the device indexer cache, hot buffers, metadata and
+ * step scratch; initialises cache_slots and slot_token to -1, last_use, stamps
+ * and lengths to 0.  Synchronous.  Errors: KVO_EINVAL (cfg out of range),
+ * KVO_ECUDA (no such device), KVO_ENOMEM.  On error *out is NULL.
+ */
+int kvo_create(const kvo_config* cfg, kvo_handle** out);
+
+/* kvo_destroy: synchronise the device and free everything.  NULL is a no-op. */
+int kvo_destroy(kvo_handle* h);
+
+/*
+ * kvo_host_rows: host address of row 0 of unit's pool; rows are contiguous,
+ * row_elems bf16 each, max_tokens rows.  The caller may write rows [0, n)
+ * before kvo_prefill(unit, n) (bulk load of a prefilled context; untimed
+ * set-up, outside the decode step).  NULL if unit is out of range.
+ */
+void* kvo_host_rows(kvo_handle* h, int32_t unit);
+
+/*
+ * kvo_prefill: set an empty unit's context to n_tokens tokens whose rows are
+ * already in the host pool; copies idx_keys (bf16 [n_tokens][128], host or
+ * device memory) into the indexer cache on the given stream.  Errors:
+ * KVO_EINVAL (unit not empty), KVO_ERANGE (unit or n_tokens out of range).
+ */
+int kvo_prefill(kvo_handle* h, int32_t unit, int64_t n_tokens, const void* idx_keys,
+                void* stream);
+
+/*
+ * kvo_append ([LS] Decode step 1-2; "Transfer granularity": token rows
+ * device -> host): for each listed unit, copy its n_tokens new rows to host
+ * pool rows len..len+n_tokens-1 and their indexer keys to the indexer cache,
+ * then len += n_tokens.  New tokens are not resident (cache_slots -1).
+ *   units     : host array [n_units] of distinct unit ids, or NULL = all units
+ *               in order (then n_units must equal the unit count).
+ *   main_rows : device bf16 [n_units][n_tokens][row_elems]
+ *   idx_keys  : device bf16 [n_units][n_tokens][128]
+ * Errors (nothing launched): KVO_EINVAL (bad pointer, duplicate unit),
+ * KVO_ERANGE (unit id out of range or len + n_tokens > max_tokens).
+ */
+int kvo_append(kvo_handle* h, const int32_t* units, int32_t n_units, int32_t n_tokens,
+               const void* main_rows, const void* idx_keys, void* stream);
+
+/*
+ * kvo_step ([LS] Decode step 3-6, [FO] decode paragraphs): one decode step
+ * of every listed unit: indexer scoring of every cached token, fused top-k
+ * carrying the packed payload, MTP merge and dedup, LRU residency update,
+ * miss-row copy from the host pool into the hot buffer, remap to slots.
+ *   units        : host array [n_units] of distinct unit ids, or NULL = all.
+ *   queries      : device bf16 [n_units][P][128]
+ *   topk_tokens  : device int32 [n_units][P][k] (out)
+ *   topk_slots   : device int32 [n_units][P][k] (out) hot slot of each token
+ *   topk_scores  : device float [n_units][P][k] (out, nullable)
+ *   topk_payload : device int32 [n_units][P][k] (out, nullable) packed payload
+ *   unit_status  : device int32 [n_units] (out) KVO_OK | KVO_ECAPACITY |
+ *                  KVO_ETIMEOUT
+ * Outputs are unspecified until the stream reaches the end of the step.
+ */
+int kvo_step(kvo_handle* h, const int32_t* units, int32_t n_units, const void* queries,
+             int32_t* topk_tokens, int32_t* topk_slots, float* topk_scores,
+             int32_t* topk_payload, int32_t* unit_status, void* stream);
+
+/*
+ * kvo_select ([LS] Decode step 3, [FO] packed-payload top-k): the scoring
+ * and fused top-k of kvo_step alone, on caller buffers, stateless.
+ *   keys        : device bf16; key of token t of unit i at
+ *                 keys + (i * unit_stride + t) * 128 elements
+ *   cache_slots : device int32, entry of token t of unit i at
+ *                 cache_slots[i * unit_stride + t]; NULL = nothing resident
+ *   lengths     : host int64 [n_units] cached tokens per unit (<= unit_stride)
+ *   queries     : device bf16 [n_units][n_pos][128]
+ *   tokens, scores, payload: device [n_units][n_pos][k] (scores, payload
+ *                 nullable), same order and padding rules as kvo_step
+ *   workspace   : device scratch of at least kvo_select_workspace_size()
+ *                 bytes, 256-byte aligned, owned by the caller; its contents
+ *                 need no initialisation and are not preserved
+ * Errors: KVO_EINVAL, KVO_ECUDA.  Asynchronous on stream.
+ */
+size_t kvo_select_workspace_size(int32_t n_units, int32_t n_pos, int32_t k, int32_t device);
+int kvo_select(const void* keys, int64_t unit_stride, const int32_t* cache_slots,
+               const int64_t* lengths, int32_t n_units, int32_t n_pos, int32_t k,
+               const void* queries, int32_t* tokens, float* scores, int32_t* payload,
+               void* workspace, size_t workspace_bytes, void* stream);
+
+/* kvo_set_option: KVO_OPT_* above.  KVO_EINVAL on unknown key or value. */
+int kvo_set_option(kvo_handle* h, int32_t key, int64_t value);
+
+/* kvo_get_stats: synchronises the device, then copies the counters. */
+int kvo_get_stats(kvo_handle* h, kvo_stats* out);
+
+/*
+ * kvo_export_state: synchronises the device and copies one unit's state to
+ * host buffers (any may be NULL): cache_slots [max_tokens] int32,
+ * slot_token [hot_capacity] int32, last_use [hot_capacity] uint32, length
+ * and stamp scalars, hot_rows [hot_capacity][row_elems] bf16.
+ */
+int kvo_export_state(kvo_handle* h, int32_t unit, int32_t* cache_slots, int32_t* slot_token,
+                     uint32_t* last_use, int64_t* length, uint32_t* stamp, void* hot_rows);
+
+/* kvo_last_error: message of the last failing call on this thread ("" if none). */
+const char* kvo_last_error(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* KVO_H */

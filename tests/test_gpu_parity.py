@@ -1,0 +1,262 @@
+"""CUDA path vs CPU oracle, element by element, through the C ABI.
+
+Reduced sizes check every unit at every step (tokens, payloads, slots, status
+bit-exact; scores within 1e-5 relative and, by construction, bit-identical;
+exported residency state and hot rows bit-exact).  The full-size workloads
+run in the launch configuration the benchmark times and check sampled units,
+which the oracle replays one by one.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import workload as W
+from tests.gpu_harness import Runner
+from tests.helpers import int_bf16
+from top_cache_gb300 import kvo as K
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    from top_cache_gb300 import build
+    build.build()
+    yield
+
+
+def _run(wl, steps=None, check_state=True, count_rows=True, **kw):
+    r = Runner(wl, steps=steps, **kw)
+    try:
+        before = r.kv.stats()
+        n_miss = 0
+        for s in range(r.steps):
+            r.append(wl.n_new)
+            res = r.step(s)
+            r.compare(res, state=check_state)
+            n_miss += sum(v[0].n_miss for v in res.values())
+        st = r.kv.stats()
+        if count_rows and len(r.check) == r.U:
+            # transferred rows == deduplicated miss count, counted by the copy kernel
+            assert st["rows_h2d"] - before["rows_h2d"] == n_miss
+            assert st["misses"] - before["misses"] == n_miss
+        return st, n_miss
+    finally:
+        r.close()
+
+
+# ---------------------------------------------------------------- reduced sizes
+def test_single_4k_full_size():
+    st, n_miss = _run(W.WORKLOADS["single_4k"])
+    assert st["unit_steps"] == 20 and 0 < n_miss < 20 * 256
+
+
+def test_batch16x8_mtp3_reduced():
+    wl = W.reduced(W.WORKLOADS["batch16x8_32k_mtp3"], n_requests=2, n_layers=2, context=4001,
+                   topk=256, hot_capacity=512, steps=8)
+    _run(wl)
+
+
+def test_batch32x16_reduced_ragged():
+    wl = W.reduced(W.WORKLOADS["batch32x16_64k"], n_requests=2, n_layers=3, context=6003,
+                   topk=300, hot_capacity=1200, steps=6)
+    _run(wl)
+
+
+def test_long_context_reduced_multi_piece():
+    # two units of ~150k tokens: each unit spans dozens of score CTAs and the
+    # candidate union exceeds the select kernel's shared-memory buffer
+    wl = W.reduced(W.WORKLOADS["long_1m_mtp3"], n_requests=1, n_layers=2, context=150001,
+                   topk=512, hot_capacity=4096, steps=3)
+    _run(wl)
+
+
+@pytest.mark.parametrize("drift", W.SWEEP_DRIFTS)
+def test_sweep_reduced(drift):
+    wl = W.reduced(W.WORKLOADS["sweep64x4_16k_mtp3"], n_requests=4, n_layers=2, context=3000,
+                   topk=128, hot_capacity=256, steps=6, drift=drift)
+    _run(wl)
+
+
+def test_bulk_gather_mode():
+    wl = W.reduced(W.WORKLOADS["batch16x8_32k_mtp3"], n_requests=2, n_layers=2, context=3000,
+                   topk=256, hot_capacity=600, steps=5)
+    _run(wl, gather_mode=K.KVO_GATHER_BULK)
+
+
+def test_positions_1_to_8():
+    for P in (2, 3, 5, 8):
+        wl = W.Workload("p%d" % P, 1, 2, 2500, P, P, 64, 64 * P, 4, 0.5, 77)
+        _run(wl, distinct=True)
+
+
+def test_capacity_overflow_transactional():
+    # distinct per-position queries with P*k > C overflow on some steps
+    wl = W.Workload("cap", 2, 2, 2000, 4, 4, 64, 160, 6, 0.3, 78)
+    r = Runner(wl, distinct=True)
+    try:
+        seen = 0
+        for s in range(r.steps):
+            r.append(wl.n_new)
+            res = r.step(s)
+            r.compare(res)
+            seen += sum(1 for v in res.values() if v[0].status == oracle.ECAPACITY)
+        assert seen > 0
+    finally:
+        r.close()
+
+
+def test_forced_ties_and_zero_query():
+    # integer keys in {-1, 0, 1}, each row repeated three times: many equal scores
+    def keys_fn(units_rl, t0, n):
+        out = np.empty((len(units_rl), n, 128), np.uint16)
+        for i, rl in enumerate(units_rl):
+            base = W.token_rows(5, W.KIND_KEYS, [rl], t0 // 3, (t0 + n + 2) // 3 - t0 // 3 + 1, 128)[0]
+            f = np.clip(np.rint(W.bf16_to_f32(base)), -1, 1)
+            idx = np.arange(t0, t0 + n) // 3 - t0 // 3
+            out[i] = int_bf16(f[idx])
+        return out
+
+    wl = W.Workload("ties", 1, 3, 1500, 2, 2, 100, 300, 5, 0.9, 79)
+    q = W.unit_queries(wl.seed, wl.units_rl(), wl.drift, wl.steps, wl.n_pos, distinct=True)
+    qf = np.clip(np.rint(W.bf16_to_f32(q)), -1, 1)
+    q = int_bf16(qf)
+    q[1, :, 0, :] = 0  # step 1, position 0: all scores are +0, order by token alone
+    _run(wl, keys_fn=keys_fn, queries=q)
+
+
+def test_units_subset_ragged_lengths_and_repeat():
+    wl = W.Workload("subset", 2, 3, 2048, 2, 2, 128, 400, 6, 0.8, 80)
+    r = Runner(wl)
+    try:
+        # append to every unit, then step a changing subset; lengths diverge
+        for s in range(r.steps):
+            sub = [u for u in range(r.U) if (u + s) % 3 != 0]
+            r.append(wl.n_new, units=sub)
+            res = r.step(s, units=sub)
+            r.compare(res)
+        # a repeated step with the same queries and no append is all hits
+        last = [u for u in range(r.U) if (u + r.steps - 1) % 3 != 0]
+        before = r.kv.stats()
+        res = r.step(r.steps - 1, units=last[:2])
+        r.compare(res)
+        assert all(v[0].n_miss == 0 for v in res.values())
+        after = r.kv.stats()
+        assert after["rows_h2d"] == before["rows_h2d"]
+        assert after["bytes_h2d"] == before["bytes_h2d"]
+    finally:
+        r.close()
+
+
+def test_empty_and_short_units():
+    # context 0: the first steps see fewer tokens than k (and than P)
+    wl = W.Workload("short", 1, 2, 0, 3, 3, 16, 64, 8, 0.9, 81)
+    _run(wl)
+
+
+def test_append_past_max_tokens_rejected():
+    wl = W.Workload("range", 1, 1, 64, 1, 1, 8, 16, 2, 0.9, 82)
+    r = Runner(wl)
+    try:
+        r.append(1)
+        r.append(1)
+        with pytest.raises(K.KvoError) as e:
+            r.append(1)
+        assert e.value.code == K.KVO_ERANGE
+        assert r.kv.export_state(0)["length"] == 66
+    finally:
+        r.close()
+
+
+def test_bad_arguments():
+    with pytest.raises(K.KvoError) as e:
+        K.kvo_create(1, 1, 100, 64, 32, 1)  # capacity < k
+    assert e.value.code == K.KVO_EINVAL
+    kv = K.Kvo(1, 2, 100, 8, 16, 1)
+    try:
+        q = torch.zeros((2, 1, 128), dtype=torch.bfloat16, device="cuda")
+        with pytest.raises(K.KvoError) as e:
+            kv.step(q, units=[1, 1])
+        assert e.value.code == K.KVO_EINVAL
+        with pytest.raises(K.KvoError) as e:
+            kv.step(q, units=[0, 5])
+        assert e.value.code == K.KVO_ERANGE
+        with pytest.raises(K.KvoError):
+            kv.set_option(99, 0)
+    finally:
+        kv.close()
+
+
+def test_select_stateless():
+    n, P, k = 5, 3, 200
+    lengths = [0, 150, 3000, 12345, 777]
+    stride = 12352
+    keys = np.zeros((n, stride, 128), np.uint16)
+    for i in range(n):
+        keys[i, : lengths[i]] = W.token_rows(83, W.KIND_KEYS, [(i, 0)], 0, lengths[i], 128)[0]
+    q = W.unit_queries(83, [(i, 0) for i in range(n)], 0.9, 1, P, distinct=True)[0]
+    rng = np.random.default_rng(83)
+    cs = np.full((n, stride), -1, np.int32)
+    for i in range(n):
+        res = rng.choice(max(1, lengths[i]), size=min(lengths[i], 400), replace=False)
+        cs[i, res] = rng.permutation(len(res)).astype(np.int32)
+    dev = lambda a: torch.from_numpy(a).cuda()
+    kd, qd, csd = dev(keys), dev(np.ascontiguousarray(q)), dev(cs)
+    tok = torch.empty((n, P, k), dtype=torch.int32, device="cuda")
+    sc = torch.empty((n, P, k), dtype=torch.float32, device="cuda")
+    pay = torch.empty((n, P, k), dtype=torch.int32, device="cuda")
+    wsb = K.kvo_select_workspace_size(n, P, k, 0)
+    ws = torch.empty(wsb, dtype=torch.uint8, device="cuda")
+    K.kvo_select(kd, stride, csd, lengths, n, P, k, qd, tok, sc, pay, ws, wsb)
+    torch.cuda.synchronize()
+    tok, sc, pay = tok.cpu().numpy(), sc.cpu().numpy(), pay.cpu().numpy()
+    for i in range(n):
+        o = oracle.OracleUnit(max(1, lengths[i]), k, k * P, P, row_elems=8, keep_rows=False)
+        o.append(keys[i, : lengths[i]])
+        r = o.step(q[i])
+        assert np.array_equal(tok[i], r.tok)
+        fin = np.isfinite(r.score)
+        assert np.array_equal(sc[i][fin].view(np.uint32), r.score[fin].view(np.uint32))
+        # payload rule applied to the caller's cache_slots
+        exp = np.where(r.tok >= 0, np.where(cs[i][np.maximum(r.tok, 0)] >= 0,
+                                            cs[i][np.maximum(r.tok, 0)], -(r.tok + 1)),
+                       K.KVO_PAD_PAYLOAD)
+        assert np.array_equal(pay[i], exp)
+
+
+# ---------------------------------------------------------------- full sizes
+def _meminfo_gb():
+    try:
+        with open("/proc/meminfo") as f:
+            for line in f:
+                if line.startswith("MemAvailable:"):
+                    return int(line.split()[1]) / 1e6
+    except OSError:
+        pass
+    return 0.0
+
+
+def test_full_batch16x8_mtp3_sampled():
+    wl = W.WORKLOADS["batch16x8_32k_mtp3"]
+    _run(wl, check_units=[0, 61, 127], count_rows=False)
+
+
+def test_full_long_1m_mtp3_sampled():
+    wl = W.WORKLOADS["long_1m_mtp3"]
+    _run(wl, steps=5, check_units=[3], count_rows=False)
+
+
+def test_full_sweep_sampled():
+    base = W.WORKLOADS["sweep64x4_16k_mtp3"]
+    for drift in W.SWEEP_DRIFTS:
+        wl = W.reduced(base, drift=drift)
+        _run(wl, steps=10, check_units=[0, 255], count_rows=False)
+
+
+def test_full_batch32x16_sampled():
+    wl = W.WORKLOADS["batch32x16_64k"]
+    need = wl.n_units * wl.max_tokens() * wl.row_elems * 2 / 1e9
+    if _meminfo_gb() < need * 1.3 + 16:
+        pytest.skip("host memory below %.0f GB for the pinned pool" % (need * 1.3 + 16))
+    _run(wl, steps=12, check_units=[5, 400], count_rows=False)

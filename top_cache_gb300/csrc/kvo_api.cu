@@ -1,0 +1,548 @@
+// C ABI of libkvo: argument checks, allocation, launch order.
+//
+// Memory layout ("Layerwise and Sparse KV Cache Offloading Design", section 4
+// "Memory layout"): the full main-KV history lives in one pinned, mapped host
+// allocation [units][stride][row_elems] bf16 that kernels read and write in
+// place over the host link; the indexer cache [units][stride][128] bf16, the
+// hot buffers [units][C][row_elems] bf16 and the residency metadata live in
+// device memory.  A decode step is five launches on the caller's stream:
+// plan -> score -> select -> residency -> gather.
+#include <cuda_runtime.h>
+#include <stdint.h>
+#include <string.h>
+
+#include <string>
+#include <vector>
+
+#include "kvo_internal.cuh"
+
+using kvo::DevStats;
+
+struct kvo_handle {
+  kvo_config cfg{};
+  int device = 0, n_sm = 0;
+  int U = 0, C = 0, P = 0, k = 0, R = 0, cap = 0;
+  int64_t stride = 0;
+  int G_max = 0;
+  uint16_t* host_pool = nullptr;      // host address
+  uint16_t* host_pool_dev = nullptr;  // device-visible address of the same memory
+  uint16_t* idx = nullptr;
+  uint16_t* hot = nullptr;
+  int32_t* cache_slots = nullptr;
+  int32_t* slot_token = nullptr;
+  uint32_t* last_use = nullptr;
+  uint32_t* stamp = nullptr;
+  int32_t* len = nullptr;
+  std::vector<int64_t> len_host;
+  int32_t* all_units = nullptr;  // identity list
+  int32_t* units_dev = nullptr;  // last uploaded explicit list
+  std::vector<int32_t> units_cached;
+  int64_t* off = nullptr;
+  uint64_t* seg_keys = nullptr;
+  int32_t* seg_cnt = nullptr;
+  int32_t* sel_pay = nullptr;
+  int32_t* miss_tok = nullptr;
+  int32_t* miss_slot = nullptr;
+  int32_t* miss_cnt = nullptr;
+  int64_t* miss_off = nullptr;
+  uint32_t* done_ctr = nullptr;
+  uint32_t* err = nullptr;
+  DevStats* stats = nullptr;
+  uint64_t host_steps = 0;
+  int gather_mode = KVO_GATHER_LDG;
+  uint64_t wait_ns = 2000000000ull;
+};
+
+namespace {
+
+thread_local std::string g_err;
+
+int fail(int code, const std::string& msg) {
+  g_err = msg;
+  return code;
+}
+
+int cuda_fail(cudaError_t e, const char* what) {
+  g_err = std::string(what) + ": " + cudaGetErrorString(e);
+  return KVO_ECUDA;
+}
+
+// Makes the handle's device current for the duration of a call.
+struct DeviceGuard {
+  int prev = -1;
+  bool ok = true;
+  explicit DeviceGuard(int dev) {
+    if (cudaGetDevice(&prev) != cudaSuccess) prev = -1;
+    if (prev != dev) ok = cudaSetDevice(dev) == cudaSuccess;
+  }
+  ~DeviceGuard() {
+    if (prev >= 0) cudaSetDevice(prev);
+  }
+};
+
+template <class T>
+cudaError_t dalloc(T** p, size_t count) {
+  return cudaMalloc(reinterpret_cast<void**>(p), count * sizeof(T) > 0 ? count * sizeof(T) : 16);
+}
+
+void free_all(kvo_handle* h) {
+  void* dev[] = {h->idx, h->hot, h->cache_slots, h->slot_token, h->last_use, h->stamp, h->len,
+                 h->all_units, h->units_dev, h->off, h->seg_keys, h->seg_cnt, h->sel_pay,
+                 h->miss_tok, h->miss_slot, h->miss_cnt, h->miss_off, h->done_ctr, h->err,
+                 h->stats};
+  for (void* p : dev)
+    if (p) cudaFree(p);
+  if (h->host_pool) cudaFreeHost(h->host_pool);
+}
+
+size_t residency_smem_bytes(int C, int P, int k) {
+  int n2 = 1;
+  while (n2 < P * k) n2 <<= 1;
+  const int nwords = (C + 31) / 32;
+  return (size_t)((nwords + 3) & ~3) * 4 + (size_t)n2 * 16;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// Resolve the unit list of a call: NULL = all; else validate and upload.
+int resolve_units(kvo_handle* h, const int32_t* units, int32_t n_units, cudaStream_t s,
+                  const int32_t** dev_units) {
+  if (units == nullptr) {
+    if (n_units != h->U) return fail(KVO_EINVAL, "units == NULL requires n_units == unit count");
+    *dev_units = h->all_units;
+    return KVO_OK;
+  }
+  if (n_units < 1 || n_units > h->U) return fail(KVO_EINVAL, "n_units out of range");
+  std::vector<uint8_t> seen((size_t)h->U, 0);
+  for (int32_t i = 0; i < n_units; ++i) {
+    const int32_t u = units[i];
+    if (u < 0 || u >= h->U) return fail(KVO_ERANGE, "unit id out of range");
+    if (seen[(size_t)u]) return fail(KVO_EINVAL, "duplicate unit id in list");
+    seen[(size_t)u] = 1;
+  }
+  bool same = (int32_t)h->units_cached.size() == n_units &&
+              memcmp(h->units_cached.data(), units, (size_t)n_units * 4) == 0;
+  if (!same) {
+    h->units_cached.assign(units, units + n_units);
+    cudaError_t e = cudaMemcpyAsync(h->units_dev, h->units_cached.data(), (size_t)n_units * 4,
+                                    cudaMemcpyHostToDevice, s);
+    if (e != cudaSuccess) return cuda_fail(e, "unit list upload");
+  }
+  *dev_units = h->units_dev;
+  return KVO_OK;
+}
+
+int grid_for(int64_t T, int G_max) {
+  const int64_t per = 4096;  // fewest tokens worth a CTA
+  int64_t g = (T + per - 1) / per;
+  if (g < 1) g = 1;
+  if (g > G_max) g = G_max;
+  return (int)g;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* kvo_last_error(void) { return g_err.c_str(); }
+
+int kvo_create(const kvo_config* cfg, kvo_handle** out) {
+  if (!out) return fail(KVO_EINVAL, "out is NULL");
+  *out = nullptr;
+  if (!cfg) return fail(KVO_EINVAL, "cfg is NULL");
+  const kvo_config c = *cfg;
+  if (c.n_requests < 1 || c.n_layers < 1 || (int64_t)c.n_requests * c.n_layers > (1 << 20))
+    return fail(KVO_EINVAL, "n_requests * n_layers must be in [1, 2^20]");
+  if (c.max_tokens < 1 || c.max_tokens >= (int64_t)1 << 31) return fail(KVO_EINVAL, "max_tokens out of range");
+  if (c.idx_dim != kvo::kDim) return fail(KVO_EINVAL, "idx_dim must be 128");
+  if (c.row_elems < 8 || c.row_elems > 4096 || c.row_elems % 8)
+    return fail(KVO_EINVAL, "row_elems must be a multiple of 8 in [8, 4096]");
+  if (c.topk < 1 || c.topk > 4096) return fail(KVO_EINVAL, "topk must be in [1, 4096]");
+  if (c.hot_capacity < c.topk || c.hot_capacity > (1 << 24))
+    return fail(KVO_EINVAL, "hot_capacity must be in [topk, 2^24]");
+  if (c.n_positions < 1 || c.n_positions > 8) return fail(KVO_EINVAL, "n_positions must be in [1, 8]");
+  const int cap = kvo::score_cap_for(c.n_positions, c.topk);
+  if (cap == 0) return fail(KVO_EINVAL, "topk too large for n_positions (shared-memory candidate buffer)");
+  if (residency_smem_bytes(c.hot_capacity, c.n_positions, c.topk) > 224 * 1024)
+    return fail(KVO_EINVAL, "hot_capacity / n_positions * topk too large for the residency kernel");
+
+  int ndev = 0;
+  if (cudaGetDeviceCount(&ndev) != cudaSuccess || ndev == 0) return fail(KVO_ECUDA, "no CUDA device");
+  if (c.device < 0 || c.device >= ndev) return fail(KVO_ECUDA, "device ordinal out of range");
+  DeviceGuard guard(c.device);
+  if (!guard.ok) return fail(KVO_ECUDA, "cudaSetDevice failed");
+
+  kvo_handle* h = new (std::nothrow) kvo_handle();
+  if (!h) return fail(KVO_ENOMEM, "handle");
+  h->cfg = c;
+  h->device = c.device;
+  cudaDeviceGetAttribute(&h->n_sm, cudaDevAttrMultiProcessorCount, c.device);
+  h->U = c.n_requests * c.n_layers;
+  h->C = c.hot_capacity;
+  h->P = c.n_positions;
+  h->k = c.topk;
+  h->R = c.row_elems;
+  h->cap = cap;
+  h->stride = (c.max_tokens + 7) & ~(int64_t)7;
+  h->G_max = h->n_sm;
+  h->len_host.assign((size_t)h->U, 0);
+
+  const size_t U = (size_t)h->U, S = (size_t)h->stride, C = (size_t)h->C, PK = (size_t)h->P * h->k;
+  cudaError_t e = cudaHostAlloc(reinterpret_cast<void**>(&h->host_pool), U * S * h->R * 2,
+                                cudaHostAllocMapped | cudaHostAllocPortable);
+  if (e != cudaSuccess) {
+    h->host_pool = nullptr;
+    delete h;
+    return fail(KVO_ENOMEM, std::string("pinned host pool: ") + cudaGetErrorString(e));
+  }
+  e = cudaHostGetDevicePointer(reinterpret_cast<void**>(&h->host_pool_dev), h->host_pool, 0);
+  const size_t segs = (size_t)h->G_max + U;
+  if (e == cudaSuccess) e = dalloc(&h->idx, U * S * kvo::kDim);
+  if (e == cudaSuccess) e = dalloc(&h->hot, U * C * h->R);
+  if (e == cudaSuccess) e = dalloc(&h->cache_slots, U * S);
+  if (e == cudaSuccess) e = dalloc(&h->slot_token, U * C);
+  if (e == cudaSuccess) e = dalloc(&h->last_use, U * C);
+  if (e == cudaSuccess) e = dalloc(&h->stamp, U);
+  if (e == cudaSuccess) e = dalloc(&h->len, U);
+  if (e == cudaSuccess) e = dalloc(&h->all_units, U);
+  if (e == cudaSuccess) e = dalloc(&h->units_dev, U);
+  if (e == cudaSuccess) e = dalloc(&h->off, U + 1);
+  if (e == cudaSuccess) e = dalloc(&h->seg_keys, segs * PK);
+  if (e == cudaSuccess) e = dalloc(&h->seg_cnt, segs * h->P);
+  if (e == cudaSuccess) e = dalloc(&h->sel_pay, U * PK);
+  if (e == cudaSuccess) e = dalloc(&h->miss_tok, U * PK);
+  if (e == cudaSuccess) e = dalloc(&h->miss_slot, U * PK);
+  if (e == cudaSuccess) e = dalloc(&h->miss_cnt, U);
+  if (e == cudaSuccess) e = dalloc(&h->miss_off, U + 1);
+  if (e == cudaSuccess) e = dalloc(&h->done_ctr, 1);
+  if (e == cudaSuccess) e = dalloc(&h->err, 1);
+  if (e == cudaSuccess) e = dalloc(&h->stats, 1);
+  if (e != cudaSuccess) {
+    free_all(h);
+    delete h;
+    return fail(KVO_ENOMEM, std::string("device allocation: ") + cudaGetErrorString(e));
+  }
+  // initial state: nothing resident, every slot free, stamps and lengths 0
+  e = kvo::launch_fill_i32(h->cache_slots, -1, U * S, 0);
+  if (e == cudaSuccess) e = kvo::launch_fill_i32(h->slot_token, -1, U * C, 0);
+  if (e == cudaSuccess) e = cudaMemset(h->last_use, 0, U * C * 4);
+  if (e == cudaSuccess) e = cudaMemset(h->stamp, 0, U * 4);
+  if (e == cudaSuccess) e = cudaMemset(h->len, 0, U * 4);
+  if (e == cudaSuccess) e = cudaMemset(h->miss_cnt, 0, U * 4);
+  if (e == cudaSuccess) e = cudaMemset(h->miss_off, 0, (U + 1) * 8);
+  if (e == cudaSuccess) e = cudaMemset(h->done_ctr, 0, 4);
+  if (e == cudaSuccess) e = cudaMemset(h->err, 0, 4);
+  if (e == cudaSuccess) e = cudaMemset(h->stats, 0, sizeof(DevStats));
+  if (e == cudaSuccess) {
+    std::vector<int32_t> ident(U);
+    for (size_t u = 0; u < U; ++u) ident[u] = (int32_t)u;
+    e = cudaMemcpy(h->all_units, ident.data(), U * 4, cudaMemcpyHostToDevice);
+  }
+  if (e == cudaSuccess) e = cudaDeviceSynchronize();
+  if (e != cudaSuccess) {
+    free_all(h);
+    delete h;
+    return cuda_fail(e, "initialisation");
+  }
+  *out = h;
+  g_err.clear();
+  return KVO_OK;
+}
+
+int kvo_destroy(kvo_handle* h) {
+  if (!h) return KVO_OK;
+  DeviceGuard guard(h->device);
+  cudaDeviceSynchronize();
+  free_all(h);
+  delete h;
+  return KVO_OK;
+}
+
+void* kvo_host_rows(kvo_handle* h, int32_t unit) {
+  if (!h || unit < 0 || unit >= h->U) return nullptr;
+  return h->host_pool + (size_t)unit * h->stride * h->R;
+}
+
+int kvo_prefill(kvo_handle* h, int32_t unit, int64_t n_tokens, const void* idx_keys, void* stream) {
+  if (!h) return fail(KVO_EINVAL, "handle is NULL");
+  if (unit < 0 || unit >= h->U) return fail(KVO_ERANGE, "unit out of range");
+  if (n_tokens < 0 || n_tokens > h->cfg.max_tokens) return fail(KVO_ERANGE, "n_tokens out of range");
+  if (h->len_host[(size_t)unit] != 0) return fail(KVO_EINVAL, "prefill needs an empty unit");
+  if (n_tokens > 0 && !idx_keys) return fail(KVO_EINVAL, "idx_keys is NULL");
+  DeviceGuard guard(h->device);
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  cudaError_t e = cudaSuccess;
+  if (n_tokens > 0)
+    e = cudaMemcpyAsync(h->idx + (size_t)unit * h->stride * kvo::kDim, idx_keys,
+                        (size_t)n_tokens * kvo::kKeyBytes, cudaMemcpyDefault, s);
+  if (e == cudaSuccess) e = kvo::launch_set_len(h->len, unit, (int32_t)n_tokens, s);
+  if (e != cudaSuccess) return cuda_fail(e, "prefill");
+  h->len_host[(size_t)unit] = n_tokens;
+  return KVO_OK;
+}
+
+int kvo_append(kvo_handle* h, const int32_t* units, int32_t n_units, int32_t n_tokens,
+               const void* main_rows, const void* idx_keys, void* stream) {
+  if (!h) return fail(KVO_EINVAL, "handle is NULL");
+  if (n_tokens < 0) return fail(KVO_EINVAL, "n_tokens < 0");
+  if (n_tokens > 0 && (!main_rows || !idx_keys)) return fail(KVO_EINVAL, "NULL rows or keys");
+  if (!aligned16(main_rows) || !aligned16(idx_keys)) return fail(KVO_EINVAL, "rows/keys not 16-byte aligned");
+  DeviceGuard guard(h->device);
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  // range check before anything is launched
+  for (int32_t i = 0; i < n_units; ++i) {
+    const int32_t u = units ? units[i] : i;
+    if (u < 0 || u >= h->U) return fail(KVO_ERANGE, "unit id out of range");
+    if (h->len_host[(size_t)u] + n_tokens > h->cfg.max_tokens)
+      return fail(KVO_ERANGE, "append past max_tokens");
+  }
+  const int32_t* du = nullptr;
+  int rc = resolve_units(h, units, n_units, s, &du);
+  if (rc != KVO_OK) return rc;
+  if (n_tokens == 0) return KVO_OK;
+  kvo::AppendArgs a{};
+  a.units = du;
+  a.n = n_units;
+  a.n_tok = n_tokens;
+  a.row_elems = h->R;
+  a.stride = h->stride;
+  a.rows = static_cast<const uint16_t*>(main_rows);
+  a.keys = static_cast<const uint16_t*>(idx_keys);
+  a.host_pool = h->host_pool_dev;
+  a.idx = h->idx;
+  a.len = h->len;
+  a.stats = h->stats;
+  cudaError_t e = kvo::launch_append(a, s);
+  if (e != cudaSuccess) return cuda_fail(e, "append launch");
+  for (int32_t i = 0; i < n_units; ++i) h->len_host[(size_t)(units ? units[i] : i)] += n_tokens;
+  return KVO_OK;
+}
+
+int kvo_step(kvo_handle* h, const int32_t* units, int32_t n_units, const void* queries,
+             int32_t* topk_tokens, int32_t* topk_slots, float* topk_scores, int32_t* topk_payload,
+             int32_t* unit_status, void* stream) {
+  if (!h) return fail(KVO_EINVAL, "handle is NULL");
+  if (!queries || !topk_tokens || !topk_slots || !unit_status) return fail(KVO_EINVAL, "NULL argument");
+  if (!aligned16(queries)) return fail(KVO_EINVAL, "queries not 16-byte aligned");
+  DeviceGuard guard(h->device);
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const int32_t* du = nullptr;
+  int rc = resolve_units(h, units, n_units, s, &du);
+  if (rc != KVO_OK) return rc;
+  int64_t T = 0;
+  for (int32_t i = 0; i < n_units; ++i) T += h->len_host[(size_t)(units ? units[i] : i)];
+
+  kvo::SelectArgs sa{};
+  sa.keys = h->idx;
+  sa.stride = h->stride;
+  sa.units = du;
+  sa.len = h->len;
+  sa.queries = static_cast<const uint16_t*>(queries);
+  sa.cache_slots = h->cache_slots;
+  sa.n = n_units;
+  sa.P = h->P;
+  sa.k = h->k;
+  sa.cap = h->cap;
+  sa.T = T;
+  sa.G = grid_for(T, h->G_max);
+  sa.off = h->off;
+  sa.seg_keys = h->seg_keys;
+  sa.seg_cnt = h->seg_cnt;
+  sa.out_tok = topk_tokens;
+  sa.out_score = topk_scores;
+  sa.out_pay = h->sel_pay;
+  sa.out_pay_user = topk_payload;
+  sa.err = h->err;
+  sa.stats = h->stats;
+  sa.wait_ns = h->wait_ns;
+  cudaError_t e = kvo::launch_plan(sa, s);
+  if (e == cudaSuccess) e = kvo::launch_score(sa, s);
+  if (e == cudaSuccess) e = kvo::launch_select(sa, s);
+
+  kvo::ResidencyArgs ra{};
+  ra.units = du;
+  ra.n = n_units;
+  ra.P = h->P;
+  ra.k = h->k;
+  ra.C = h->C;
+  ra.stride = h->stride;
+  ra.tok = topk_tokens;
+  ra.pay = h->sel_pay;
+  ra.cache_slots = h->cache_slots;
+  ra.slot_token = h->slot_token;
+  ra.last_use = h->last_use;
+  ra.stamp = h->stamp;
+  ra.out_slot = topk_slots;
+  ra.status = unit_status;
+  ra.miss_tok = h->miss_tok;
+  ra.miss_slot = h->miss_slot;
+  ra.miss_cnt = h->miss_cnt;
+  ra.miss_off = h->miss_off;
+  ra.done_ctr = h->done_ctr;
+  ra.err = h->err;
+  ra.stats = h->stats;
+  if (e == cudaSuccess) e = kvo::launch_residency(ra, s);
+
+  kvo::GatherArgs ga{};
+  ga.units = du;
+  ga.n = n_units;
+  ga.row_elems = h->R;
+  ga.C = h->C;
+  ga.mode = h->gather_mode;
+  ga.stride = h->stride;
+  ga.host_pool = h->host_pool_dev;
+  ga.hot = h->hot;
+  ga.miss_tok = h->miss_tok;
+  ga.miss_slot = h->miss_slot;
+  ga.miss_off = h->miss_off;
+  ga.pk = h->P * h->k;
+  ga.stats = h->stats;
+  ga.err = h->err;
+  ga.wait_ns = h->wait_ns;
+  if (e == cudaSuccess) e = kvo::launch_gather(ga, h->n_sm, s);
+  if (e != cudaSuccess) return cuda_fail(e, "step launch");
+  ++h->host_steps;
+  return KVO_OK;
+}
+
+size_t kvo_select_workspace_size(int32_t n_units, int32_t n_pos, int32_t k, int32_t device) {
+  int n_sm = 0;
+  if (n_units < 1 || n_pos < 1 || k < 1) return 0;
+  if (cudaDeviceGetAttribute(&n_sm, cudaDevAttrMultiProcessorCount, device) != cudaSuccess) return 0;
+  auto up = [](size_t x) { return (x + 255) & ~(size_t)255; };
+  const size_t n = (size_t)n_units, PK = (size_t)n_pos * k, segs = (size_t)n_sm + n;
+  return up(n * 4) * 2 + up((n + 1) * 8) + up(segs * PK * 8) + up(segs * n_pos * 4) + up(n * PK * 4) + up(4);
+}
+
+int kvo_select(const void* keys, int64_t unit_stride, const int32_t* cache_slots,
+               const int64_t* lengths, int32_t n_units, int32_t n_pos, int32_t k,
+               const void* queries, int32_t* tokens, float* scores, int32_t* payload,
+               void* workspace, size_t workspace_bytes, void* stream) {
+  if (!keys || !lengths || !queries || !tokens || !workspace) return fail(KVO_EINVAL, "NULL argument");
+  if (n_units < 1 || n_pos < 1 || n_pos > 8 || k < 1 || k > 4096) return fail(KVO_EINVAL, "size out of range");
+  if (unit_stride < 1 || unit_stride >= (int64_t)1 << 31) return fail(KVO_EINVAL, "unit_stride out of range");
+  if (!aligned16(keys) || !aligned16(queries)) return fail(KVO_EINVAL, "keys/queries not 16-byte aligned");
+  if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return fail(KVO_EINVAL, "workspace not 256-byte aligned");
+  const int cap = kvo::score_cap_for(n_pos, k);
+  if (cap == 0) return fail(KVO_EINVAL, "k too large for n_pos");
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return fail(KVO_ECUDA, "no current device");
+  const size_t need = kvo_select_workspace_size(n_units, n_pos, k, dev);
+  if (need == 0 || workspace_bytes < need) return fail(KVO_EINVAL, "workspace too small");
+  std::vector<int32_t> host(2 * (size_t)n_units);
+  int64_t T = 0;
+  for (int32_t i = 0; i < n_units; ++i) {
+    if (lengths[i] < 0 || lengths[i] > unit_stride) return fail(KVO_EINVAL, "length out of range");
+    host[i] = i;
+    host[n_units + i] = (int32_t)lengths[i];
+    T += lengths[i];
+  }
+  int n_sm = 0;
+  cudaDeviceGetAttribute(&n_sm, cudaDevAttrMultiProcessorCount, dev);
+  auto up = [](size_t x) { return (x + 255) & ~(size_t)255; };
+  const size_t n = (size_t)n_units, PK = (size_t)n_pos * k, segs = (size_t)n_sm + n;
+  uint8_t* w = static_cast<uint8_t*>(workspace);
+  int32_t* d_units = reinterpret_cast<int32_t*>(w); w += up(n * 4);
+  int32_t* d_len = reinterpret_cast<int32_t*>(w); w += up(n * 4);
+  int64_t* d_off = reinterpret_cast<int64_t*>(w); w += up((n + 1) * 8);
+  uint64_t* d_seg_keys = reinterpret_cast<uint64_t*>(w); w += up(segs * PK * 8);
+  int32_t* d_seg_cnt = reinterpret_cast<int32_t*>(w); w += up(segs * n_pos * 4);
+  int32_t* d_pay = reinterpret_cast<int32_t*>(w); w += up(n * PK * 4);
+  uint32_t* d_err = reinterpret_cast<uint32_t*>(w);
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  cudaError_t e = cudaMemcpyAsync(d_units, host.data(), n * 4, cudaMemcpyHostToDevice, s);
+  if (e == cudaSuccess) e = cudaMemcpyAsync(d_len, host.data() + n, n * 4, cudaMemcpyHostToDevice, s);
+  if (e == cudaSuccess) e = cudaMemsetAsync(d_err, 0, 4, s);
+  if (e != cudaSuccess) return cuda_fail(e, "select set-up");
+  kvo::SelectArgs sa{};
+  sa.keys = static_cast<const uint16_t*>(keys);
+  sa.stride = unit_stride;
+  sa.units = d_units;
+  sa.len = d_len;
+  sa.queries = static_cast<const uint16_t*>(queries);
+  sa.cache_slots = cache_slots;
+  sa.n = n_units;
+  sa.P = n_pos;
+  sa.k = k;
+  sa.cap = cap;
+  sa.T = T;
+  sa.G = grid_for(T, n_sm);
+  sa.off = d_off;
+  sa.seg_keys = d_seg_keys;
+  sa.seg_cnt = d_seg_cnt;
+  sa.out_tok = tokens;
+  sa.out_score = scores;
+  sa.out_pay = payload ? payload : d_pay;
+  sa.out_pay_user = nullptr;
+  sa.err = d_err;
+  sa.stats = nullptr;
+  sa.wait_ns = 2000000000ull;
+  e = kvo::launch_plan(sa, s);
+  if (e == cudaSuccess) e = kvo::launch_score(sa, s);
+  if (e == cudaSuccess) e = kvo::launch_select(sa, s);
+  if (e != cudaSuccess) return cuda_fail(e, "select launch");
+  return KVO_OK;
+}
+
+int kvo_set_option(kvo_handle* h, int32_t key, int64_t value) {
+  if (!h) return fail(KVO_EINVAL, "handle is NULL");
+  switch (key) {
+    case KVO_OPT_GATHER_MODE:
+      if (value != KVO_GATHER_LDG && value != KVO_GATHER_BULK) return fail(KVO_EINVAL, "bad gather mode");
+      h->gather_mode = (int)value;
+      return KVO_OK;
+    case KVO_OPT_WAIT_LIMIT_NS:
+      if (value < 1000) return fail(KVO_EINVAL, "wait limit below 1 us");
+      h->wait_ns = (uint64_t)value;
+      return KVO_OK;
+    default:
+      return fail(KVO_EINVAL, "unknown option");
+  }
+}
+
+int kvo_get_stats(kvo_handle* h, kvo_stats* out) {
+  if (!h || !out) return fail(KVO_EINVAL, "NULL argument");
+  DeviceGuard guard(h->device);
+  cudaError_t e = cudaDeviceSynchronize();
+  DevStats d{};
+  uint32_t err = 0;
+  if (e == cudaSuccess) e = cudaMemcpy(&d, h->stats, sizeof(d), cudaMemcpyDeviceToHost);
+  if (e == cudaSuccess) e = cudaMemcpy(&err, h->err, 4, cudaMemcpyDeviceToHost);
+  if (e != cudaSuccess) return cuda_fail(e, "stats");
+  out->steps = h->host_steps;
+  out->unit_steps = d.unit_steps;
+  out->capacity_errors = d.capacity_errors;
+  out->hits = d.hits;
+  out->misses = d.misses;
+  out->rows_h2d = d.rows_h2d;
+  out->bytes_h2d = d.bytes_h2d;
+  out->rows_d2h = d.rows_d2h;
+  out->bytes_d2h = d.bytes_d2h;
+  out->timeouts = (err & kvo::kErrTimeout) ? 1 : 0;
+  return KVO_OK;
+}
+
+int kvo_export_state(kvo_handle* h, int32_t unit, int32_t* cache_slots, int32_t* slot_token,
+                     uint32_t* last_use, int64_t* length, uint32_t* stamp, void* hot_rows) {
+  if (!h) return fail(KVO_EINVAL, "handle is NULL");
+  if (unit < 0 || unit >= h->U) return fail(KVO_ERANGE, "unit out of range");
+  DeviceGuard guard(h->device);
+  cudaError_t e = cudaDeviceSynchronize();
+  const size_t S = (size_t)h->stride, C = (size_t)h->C;
+  if (e == cudaSuccess && cache_slots)
+    e = cudaMemcpy(cache_slots, h->cache_slots + unit * S, (size_t)h->cfg.max_tokens * 4, cudaMemcpyDeviceToHost);
+  if (e == cudaSuccess && slot_token)
+    e = cudaMemcpy(slot_token, h->slot_token + unit * C, C * 4, cudaMemcpyDeviceToHost);
+  if (e == cudaSuccess && last_use)
+    e = cudaMemcpy(last_use, h->last_use + unit * C, C * 4, cudaMemcpyDeviceToHost);
+  if (e == cudaSuccess && stamp) e = cudaMemcpy(stamp, h->stamp + unit, 4, cudaMemcpyDeviceToHost);
+  if (e == cudaSuccess && hot_rows)
+    e = cudaMemcpy(hot_rows, h->hot + unit * C * h->R, C * h->R * 2, cudaMemcpyDeviceToHost);
+  int32_t dlen = 0;
+  if (e == cudaSuccess) e = cudaMemcpy(&dlen, h->len + unit, 4, cudaMemcpyDeviceToHost);
+  if (e != cudaSuccess) return cuda_fail(e, "export");
+  if (length) *length = dlen;
+  return KVO_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,229 @@
+// Internal declarations shared by the kernels of libkvo (sm_103a only).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/kvo.h"
+
+namespace kvo {
+
+constexpr int kDim = 128;            // indexer dimension
+constexpr int kKeyBytes = kDim * 2;  // one indexer key row
+constexpr uint32_t kFull = 0xffffffffu;
+
+// Error bits of the sticky device error word.
+constexpr uint32_t kErrTimeout = 1u;
+constexpr uint32_t kErrPlan = 2u;
+
+// Device-side counters (mirrors kvo_stats).
+struct DevStats {
+  unsigned long long steps, unit_steps, capacity_errors, hits, misses, rows_h2d, bytes_h2d,
+      rows_d2h, bytes_d2h, timeouts;
+};
+
+// ---------------------------------------------------------------------------
+// Ordering keys.  A selection key is larger for a better candidate: the fp32
+// score mapped to an order-preserving unsigned word in the high half, the
+// bitwise complement of the token in the low half (lower token wins a tie).
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ uint32_t order_bits(float f) {
+  uint32_t b = __float_as_uint(f);
+  return (b & 0x80000000u) ? ~b : (b | 0x80000000u);
+}
+__device__ __forceinline__ float unorder_bits(uint32_t k) {
+  uint32_t b = (k & 0x80000000u) ? (k & 0x7fffffffu) : ~k;
+  return __uint_as_float(b);
+}
+__device__ __forceinline__ uint64_t sel_key(float s, uint32_t t) {
+  return ((uint64_t)order_bits(s) << 32) | (uint64_t)(~t);
+}
+__device__ __forceinline__ uint32_t key_token(uint64_t key) { return ~(uint32_t)key; }
+__device__ __forceinline__ float key_score(uint64_t key) { return unorder_bits((uint32_t)(key >> 32)); }
+
+// bf16 pair (packed in a 32-bit word) -> two exact fp32 values.
+__device__ __forceinline__ float bf_lo(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf_hi(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
+
+// ---------------------------------------------------------------------------
+// mbarrier + bulk async copy (inline PTX)
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+  return (uint32_t)__cvta_generic_to_shared(p);
+}
+__device__ __forceinline__ uint64_t global_ns() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count) : "memory");
+}
+__device__ __forceinline__ void fence_mbar_init() {
+  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)),
+               "r"(bytes)
+               : "memory");
+}
+__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+// Bounded wait on a phase parity.  Returns false when limit_ns elapsed.
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, uint64_t limit_ns) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = global_ns();
+  for (uint32_t it = 1;; ++it) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if ((it & 31u) == 0 && global_ns() - t0 > limit_ns) return false;
+  }
+}
+// 1-D bulk copy global -> shared; completion counted in bytes on bar.
+// dst, src 16-byte aligned; bytes a multiple of 16.
+__device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+          smem_u32(dst)),
+      "l"(src), "r"(bytes), "r"(smem_u32(bar))
+      : "memory");
+}
+// 1-D bulk copy shared -> global, tracked by the issuing thread's bulk group.
+__device__ __forceinline__ void bulk_s2g(void* dst, const void* src, uint32_t bytes) {
+  asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(dst),
+               "r"(smem_u32(src)), "r"(bytes)
+               : "memory");
+}
+__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+__device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
+__device__ __forceinline__ void bulk_wait_read_all() {
+  asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+}
+__device__ __forceinline__ void fence_proxy_async_smem() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+// Named barrier among the first n_threads threads of the block (id 1..15).
+__device__ __forceinline__ void named_sync(uint32_t id, uint32_t n_threads) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(n_threads) : "memory");
+}
+
+__device__ __forceinline__ uint32_t lanemask_lt() {
+  uint32_t m;
+  asm("mov.u32 %0, %%lanemask_lt;" : "=r"(m));
+  return m;
+}
+
+// Upper bound search: largest i in [0, n) with off[i] <= x (off non-decreasing).
+__device__ __forceinline__ int find_segment(const int64_t* off, int n, int64_t x) {
+  int lo = 0, hi = n - 1;
+  while (lo < hi) {
+    int mid = (lo + hi + 1) >> 1;
+    if (off[mid] <= x) lo = mid; else hi = mid - 1;
+  }
+  return lo;
+}
+
+// CTA of the flat partition [floor(c*T/G), floor((c+1)*T/G)) holding token x.
+__device__ __forceinline__ int cta_of(int64_t x, int64_t T, int G) {
+  return (int)(((x + 1) * (int64_t)G - 1) / T);
+}
+__device__ __forceinline__ int64_t cta_start(int c, int64_t T, int G) {
+  return ((int64_t)c * T) / G;
+}
+
+// ---------------------------------------------------------------------------
+// Launch-side structures
+// ---------------------------------------------------------------------------
+struct SelectArgs {
+  const uint16_t* keys;        // bf16 [.][stride][128], unit id major
+  int64_t stride;              // token stride between units
+  const int32_t* units;        // [n] unit ids (device)
+  const int32_t* len;          // device lengths indexed by unit id
+  const uint16_t* queries;     // [n][P][128]
+  const int32_t* cache_slots;  // [.][stride] or nullptr
+  int32_t n, P, k, cap;        // cap: candidate buffer entries per position
+  int64_t T;                   // total cached tokens of the listed units
+  int32_t G;                   // score CTAs
+  int64_t* off;                // [n+1] flat offsets (scratch, written by plan)
+  uint64_t* seg_keys;          // [(G+n)][P][k] candidates per segment
+  int32_t* seg_cnt;            // [(G+n)][P]
+  int32_t* out_tok;            // [n][P][k]
+  float* out_score;            // nullable
+  int32_t* out_pay;            // [n][P][k] (internal copy, may equal user payload)
+  int32_t* out_pay_user;       // nullable, second destination
+  uint32_t* err;               // sticky error word
+  DevStats* stats;             // nullable
+  uint64_t wait_ns;
+};
+
+struct ResidencyArgs {
+  const int32_t* units;
+  int32_t n, P, k, C;
+  int64_t stride;              // cache_slots stride per unit
+  const int32_t* tok;          // [n][P][k]
+  const int32_t* pay;          // [n][P][k]
+  int32_t* cache_slots;        // [U][stride]
+  int32_t* slot_token;         // [U][C]
+  uint32_t* last_use;          // [U][C]
+  uint32_t* stamp;             // [U]
+  int32_t* out_slot;           // [n][P][k]
+  int32_t* status;             // [n]
+  int32_t* miss_tok;           // [n][P*k]
+  int32_t* miss_slot;          // [n][P*k]
+  int32_t* miss_cnt;           // [n]
+  int64_t* miss_off;           // [n+1]
+  uint32_t* done_ctr;          // last-block counter (self-resetting)
+  uint32_t* err;
+  DevStats* stats;
+};
+
+struct GatherArgs {
+  const int32_t* units;
+  int32_t n, row_elems, C, mode;
+  int64_t stride;              // host pool rows per unit
+  const uint16_t* host_pool;   // device-visible address of the pinned pool
+  uint16_t* hot;               // [U][C][row_elems]
+  const int32_t* miss_tok;
+  const int32_t* miss_slot;
+  const int64_t* miss_off;     // [n+1]
+  int32_t pk;                  // stride of the miss lists
+  DevStats* stats;
+  uint32_t* err;
+  uint64_t wait_ns;
+};
+
+struct AppendArgs {
+  const int32_t* units;
+  int32_t n, n_tok, row_elems;
+  int64_t stride;
+  const uint16_t* rows;        // [n][n_tok][row_elems]
+  const uint16_t* keys;        // [n][n_tok][128]
+  uint16_t* host_pool;         // device-visible address
+  uint16_t* idx;               // [U][stride][128]
+  int32_t* len;                // [U]
+  DevStats* stats;
+};
+
+// Host-side launchers (return cudaError_t of the launch).
+int score_cap_for(int P, int k);
+cudaError_t launch_plan(const SelectArgs& a, cudaStream_t s);
+cudaError_t launch_score(const SelectArgs& a, cudaStream_t s);
+cudaError_t launch_select(const SelectArgs& a, cudaStream_t s);
+cudaError_t launch_residency(const ResidencyArgs& a, cudaStream_t s);
+cudaError_t launch_gather(const GatherArgs& a, int n_sm, cudaStream_t s);
+cudaError_t launch_append(const AppendArgs& a, cudaStream_t s);
+cudaError_t launch_set_len(int32_t* len, int32_t unit, int32_t value, cudaStream_t s);
+cudaError_t launch_fill_i32(int32_t* p, int32_t v, size_t n, cudaStream_t s);
+
+}  // namespace kvo

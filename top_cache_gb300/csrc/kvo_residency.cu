@@ -1,0 +1,541 @@
+// Residency update, miss-row fill and new-token append.
+//
+// "Layerwise and Sparse KV Cache Offloading Design", section 4 "Sparse Decode
+// Offload", Decode step: (2) new K/V rows copied to their logical slots in the
+// host pool, (4) the per-layer LRU residency table identifies hits, assigns
+// hot slots to misses and selects eviction slots, (5) only miss rows are
+// copied host -> device, (6) logical top-k positions remapped to physical
+// slots.  "FlashOffloading ... What does it mean?", decode paragraphs: the
+// shelf size stays fixed, the MTP3 per-position miss lists are merged and
+// deduplicated before loading, cache_slots maps a token to its slot or -1.
+//
+//  residency_kernel : one CTA per unit; merge + dedup of the P lists, LRU
+//                     victims in (last_use, slot) order, reverse-index
+//                     updates, remap; the last CTA to finish writes the
+//                     prefix sums of the per-unit miss counts.
+//  gather_ldg_kernel / gather_bulk_kernel : persistent copy of every miss row
+//                     from the mapped pinned host pool into the hot buffers.
+//  append_kernel    : one CTA per unit; new rows to the host pool, new keys
+//                     to the indexer cache, len += n.
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "kvo_internal.cuh"
+
+namespace kvo {
+
+namespace {
+
+constexpr int kResThreads = 1024;
+constexpr int kGatherThreads = 256;
+constexpr int kGatherRows = 32;     // rows per batch (LDG gather)
+constexpr int kBulkDepth = 4;       // rows in flight per warp (bulk gather)
+
+__device__ __forceinline__ uint32_t block_sum_u32(uint32_t v, uint32_t* wsum) {
+  const int lane = threadIdx.x & 31, w = threadIdx.x >> 5, nw = blockDim.x >> 5;
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(kFull, v, o);
+  if (lane == 0) wsum[w] = v;
+  __syncthreads();
+  uint32_t t = 0;
+  for (int x = 0; x < nw; ++x) t += wsum[x];
+  __syncthreads();
+  return t;
+}
+
+__device__ __forceinline__ uint32_t block_max_u32(uint32_t v, uint32_t* wsum) {
+  const int lane = threadIdx.x & 31, w = threadIdx.x >> 5, nw = blockDim.x >> 5;
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v = max(v, __shfl_xor_sync(kFull, v, o));
+  if (lane == 0) wsum[w] = v;
+  __syncthreads();
+  uint32_t t = 0;
+  for (int x = 0; x < nw; ++x) t = max(t, wsum[x]);
+  __syncthreads();
+  return t;
+}
+
+// Exclusive block scan of v; *total gets the block sum.
+__device__ __forceinline__ uint32_t block_excl_scan(uint32_t v, uint32_t* wsum, uint32_t* total) {
+  const int lane = threadIdx.x & 31, w = threadIdx.x >> 5, nw = blockDim.x >> 5;
+  uint32_t incl = v;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const uint32_t y = __shfl_up_sync(kFull, incl, o);
+    if (lane >= o) incl += y;
+  }
+  if (lane == 31) wsum[w] = incl;
+  __syncthreads();
+  if (w == 0) {
+    uint32_t s = lane < nw ? wsum[lane] : 0;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const uint32_t y = __shfl_up_sync(kFull, s, o);
+      if (lane >= o) s += y;
+    }
+    if (lane < nw) wsum[lane] = s;
+  }
+  __syncthreads();
+  const uint32_t excl = (w ? wsum[w - 1] : 0) + incl - v;
+  *total = wsum[nw - 1];
+  __syncthreads();
+  return excl;
+}
+
+// Warp 0: the bin (counting from the bottom) holding the need-th smallest.
+__device__ __forceinline__ void scan_bins_asc(const uint32_t* hist, uint32_t need, uint32_t* rx,
+                                              int lane) {
+  uint32_t v[8], sum = 0;
+#pragma unroll
+  for (int e = 0; e < 8; ++e) {
+    v[e] = hist[8 * lane + e];
+    sum += v[e];
+  }
+  uint32_t incl = sum;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const uint32_t y = __shfl_up_sync(kFull, incl, o);
+    if (lane >= o) incl += y;
+  }
+  uint32_t below = incl - sum;
+#pragma unroll
+  for (int e = 0; e < 8; ++e) {
+    if (below < need && need <= below + v[e]) {
+      rx[0] = 8 * lane + e;
+      rx[1] = below;
+      rx[2] = v[e];
+    }
+    below += v[e];
+  }
+}
+
+template <class T>
+__device__ __forceinline__ void bitonic_asc(T* buf, int n) {
+  for (int size = 2; size <= n; size <<= 1) {
+    for (int stride = size >> 1; stride > 0; stride >>= 1) {
+      for (int i = threadIdx.x; i < (n >> 1); i += blockDim.x) {
+        const int lo = 2 * i - (i & (stride - 1));
+        const int hi = lo + stride;
+        const T x = buf[lo], y = buf[hi];
+        const bool asc = (lo & size) == 0;
+        if (asc ? (x > y) : (x < y)) {
+          buf[lo] = y;
+          buf[hi] = x;
+        }
+      }
+      __syncthreads();
+    }
+  }
+}
+
+__device__ __forceinline__ int pow2_at_least(int x) {
+  int p = 1;
+  while (p < x) p <<= 1;
+  return p;
+}
+
+}  // namespace
+
+// ---------------------------------------------------------------------------
+// residency: merge/dedup, LRU, reverse index, remap (one CTA per unit)
+// ---------------------------------------------------------------------------
+__global__ void __launch_bounds__(kResThreads) residency_kernel(ResidencyArgs a) {
+  extern __shared__ __align__(128) uint8_t smem[];
+  const int C = a.C, PK = a.P * a.k;
+  const int n2 = pow2_at_least(PK);
+  const int nwords = (C + 31) >> 5;
+  const int nwords_pad = (nwords + 3) & ~3;
+  uint32_t* bitmap = reinterpret_cast<uint32_t*>(smem);        // [nwords_pad] hit slots
+  int32_t* raw = reinterpret_cast<int32_t*>(bitmap + nwords_pad);  // [n2] miss tokens with dups
+  int32_t* M = raw + n2;                                        // [n2] distinct misses, ascending
+  uint64_t* vic = reinterpret_cast<uint64_t*>(M + n2);          // [n2] victim keys
+  __shared__ uint32_t hist[256];
+  __shared__ uint32_t rx[8];
+  __shared__ uint32_t wsum[32];
+  __shared__ uint32_t sc[8];
+
+  const int tid = threadIdx.x;
+  const int i = blockIdx.x;
+  const int u = a.units[i];
+  const int32_t* tok = a.tok + (int64_t)i * PK;
+  const int32_t* pay = a.pay + (int64_t)i * PK;
+  int32_t* out_slot = a.out_slot + (int64_t)i * PK;
+  int32_t* cs = a.cache_slots + (int64_t)u * a.stride;
+  int32_t* st = a.slot_token + (int64_t)u * C;
+  uint32_t* lu = a.last_use + (int64_t)u * C;
+
+  int32_t status = KVO_OK;
+  uint32_t m = 0, hits = 0;
+  if (*((volatile uint32_t*)a.err) != 0) status = KVO_ETIMEOUT;
+
+  if (status == KVO_OK) {
+    for (int w = tid; w < nwords; w += kResThreads) bitmap[w] = 0;
+    if (tid == 0) sc[0] = 0;
+    __syncthreads();
+    // payload says hit (slot) or miss (token): mark hit slots, list misses
+    for (int e = tid; e < PK; e += kResThreads) {
+      const int32_t t = tok[e];
+      if (t < 0) continue;
+      const int32_t p = pay[e];
+      if (p >= 0) {
+        if (p < C) atomicOr(&bitmap[p >> 5], 1u << (p & 31));
+      } else {
+        const uint32_t dst = atomicAdd(&sc[0], 1u);
+        if (dst < (uint32_t)n2) raw[dst] = t;
+      }
+    }
+    __syncthreads();
+    const int nraw = (int)min(sc[0], (uint32_t)n2);
+    const int np = pow2_at_least(nraw > 0 ? nraw : 1);
+    for (int e = nraw + tid; e < np; e += kResThreads) raw[e] = INT32_MAX;
+    __syncthreads();
+    bitonic_asc(raw, np);
+    // distinct misses in token order
+    for (int base = 0; base < np; base += kResThreads) {
+      const int e = base + tid;
+      const int32_t v = e < nraw ? raw[e] : 0;
+      const uint32_t flag = (e < nraw && (e == 0 || raw[e - 1] != v)) ? 1u : 0u;
+      uint32_t total;
+      const uint32_t pos = block_excl_scan(flag, wsum, &total);
+      if (flag) M[m + pos] = v;
+      m += total;
+    }
+    uint32_t hc = 0;
+    for (int w = tid; w < nwords; w += kResThreads) hc += __popc(bitmap[w]);
+    hits = block_sum_u32(hc, wsum);
+    if (hits + m > (uint32_t)C) status = KVO_ECAPACITY;
+  }
+
+  if (status == KVO_OK) {
+    const uint32_t stamp = a.stamp[u] + 1;
+    __syncthreads();
+    if (tid == 0) a.stamp[u] = stamp;
+    // hits: refresh their stamps
+    for (int w = tid; w < nwords; w += kResThreads) {
+      uint32_t bits = bitmap[w];
+      while (bits) {
+        const int b = __ffs(bits) - 1;
+        bits &= bits - 1;
+        lu[w * 32 + b] = stamp;
+      }
+    }
+    if (m > 0) {
+      // victims: the m smallest (last_use, slot) among slots not hit
+      auto eligible = [&](int s) { return ((bitmap[s >> 5] >> (s & 31)) & 1u) == 0; };
+      uint32_t mx = 0;
+      for (int s = tid; s < C; s += kResThreads)
+        if (eligible(s)) mx = max(mx, lu[s]);
+      mx = block_max_u32(mx, wsum);
+      const int bits_s = C > 1 ? 32 - __clz(C - 1) : 0;
+      const int bits_lu = mx ? 32 - __clz(mx) : 0;
+      const int B = bits_s + bits_lu;
+      const uint64_t smask = (1ull << bits_s) - 1;
+      uint64_t prefix = 0, mask = 0;
+      uint32_t need = m;
+      for (int shift = B > 0 ? ((B - 1) / 8) * 8 : 0; shift >= 0; shift -= 8) {
+        for (int b = tid; b < 256; b += kResThreads) hist[b] = 0;
+        __syncthreads();
+        for (int s = tid; s < C; s += kResThreads) {
+          if (!eligible(s)) continue;
+          const uint64_t key = ((uint64_t)lu[s] << bits_s) | (uint64_t)s;
+          if ((key & mask) == prefix) atomicAdd(&hist[(uint32_t)(key >> shift) & 255u], 1u);
+        }
+        __syncthreads();
+        if (tid < 32) scan_bins_asc(hist, need, rx, tid);
+        __syncthreads();
+        const uint32_t bin = rx[0], below = rx[1], inbin = rx[2];
+        need -= below;
+        prefix |= (uint64_t)bin << shift;
+        mask |= 0xffull << shift;
+        __syncthreads();
+        if (inbin == need) break;
+      }
+      if (tid == 0) sc[1] = 0;
+      __syncthreads();
+      for (int s = tid; s < C; s += kResThreads) {
+        if (!eligible(s)) continue;
+        const uint64_t key = ((uint64_t)lu[s] << bits_s) | (uint64_t)s;
+        if ((key & mask) <= prefix) {
+          const uint32_t dst = atomicAdd(&sc[1], 1u);
+          if (dst < (uint32_t)n2) vic[dst] = key;
+        }
+      }
+      __syncthreads();
+      const int nv = pow2_at_least((int)m);
+      for (int e = (int)m + tid; e < nv; e += kResThreads) vic[e] = ~0ull;
+      __syncthreads();
+      bitonic_asc(vic, nv);
+      // i-th miss (token order) takes the i-th victim
+      for (uint32_t r = tid; r < m; r += kResThreads) {
+        const int s = (int)(vic[r] & smask);
+        const int32_t t = M[r];
+        const int32_t old = st[s];
+        if (old >= 0) cs[old] = -1;
+        st[s] = t;
+        cs[t] = s;
+        lu[s] = stamp;
+        a.miss_tok[(int64_t)i * PK + r] = t;
+        a.miss_slot[(int64_t)i * PK + r] = s;
+      }
+    }
+    __syncthreads();
+    // remap logical top-k positions to physical slots
+    for (int e = tid; e < PK; e += kResThreads) {
+      const int32_t t = tok[e];
+      out_slot[e] = t >= 0 ? cs[t] : -1;
+    }
+  } else {
+    m = 0;
+    for (int e = tid; e < PK; e += kResThreads) out_slot[e] = -1;
+  }
+
+  if (tid == 0) {
+    a.status[i] = status;
+    a.miss_cnt[i] = (int32_t)m;
+    if (a.stats) {
+      if (status == KVO_OK) {
+        atomicAdd(&a.stats->unit_steps, 1ull);
+        atomicAdd(&a.stats->hits, (unsigned long long)hits);
+        atomicAdd(&a.stats->misses, (unsigned long long)m);
+      } else if (status == KVO_ECAPACITY) {
+        atomicAdd(&a.stats->capacity_errors, 1ull);
+      }
+    }
+  }
+
+  // the last CTA writes the prefix sums of the miss counts
+  __threadfence();
+  __syncthreads();
+  if (tid == 0) sc[2] = (atomicAdd(a.done_ctr, 1u) == (uint32_t)(a.n - 1)) ? 1u : 0u;
+  __syncthreads();
+  if (sc[2]) {
+    __threadfence();
+    int64_t carry = 0;
+    for (int base = 0; base < a.n; base += kResThreads) {
+      const int e = base + tid;
+      const uint32_t v = e < a.n ? (uint32_t)__ldcg(&a.miss_cnt[e]) : 0u;
+      uint32_t total;
+      const uint32_t pos = block_excl_scan(v, wsum, &total);
+      if (e < a.n) a.miss_off[e] = carry + pos;
+      carry += total;
+    }
+    if (tid == 0) {
+      a.miss_off[a.n] = carry;
+      *a.done_ctr = 0;
+    }
+  }
+}
+
+// ---------------------------------------------------------------------------
+// gather, 16-byte loads from the mapped host pool (zero copy)
+// ---------------------------------------------------------------------------
+__global__ void __launch_bounds__(kGatherThreads) gather_ldg_kernel(GatherArgs a) {
+  __shared__ int64_t src_off[kGatherRows];
+  __shared__ int64_t dst_off[kGatherRows];
+  const int tid = threadIdx.x;
+  const int64_t R = a.miss_off[a.n];
+  const int cpr = a.row_elems / 8;  // 16-byte chunks per row
+  int64_t moved = 0;
+  for (int64_t b0 = (int64_t)blockIdx.x * kGatherRows; b0 < R; b0 += (int64_t)gridDim.x * kGatherRows) {
+    const int nrow = (int)((R - b0) < kGatherRows ? (R - b0) : kGatherRows);
+    if (tid < nrow) {
+      const int64_t r = b0 + tid;
+      const int i = find_segment(a.miss_off, a.n, r);
+      const int64_t loc = r - a.miss_off[i];
+      const int u = a.units[i];
+      const int32_t t = a.miss_tok[(int64_t)i * a.pk + loc];
+      const int32_t s = a.miss_slot[(int64_t)i * a.pk + loc];
+      src_off[tid] = ((int64_t)u * a.stride + t) * a.row_elems;
+      dst_off[tid] = ((int64_t)u * a.C + s) * a.row_elems;
+    }
+    __syncthreads();
+    const int total = nrow * cpr;
+    constexpr int U = 8;
+    for (int q0 = tid; q0 < total; q0 += kGatherThreads * U) {
+      uint4 v[U];
+#pragma unroll
+      for (int x = 0; x < U; ++x) {
+        const int q = q0 + x * kGatherThreads;
+        if (q < total) {
+          const int row = q / cpr, c = q - row * cpr;
+          v[x] = *reinterpret_cast<const uint4*>(a.host_pool + src_off[row] + c * 8);
+        }
+      }
+#pragma unroll
+      for (int x = 0; x < U; ++x) {
+        const int q = q0 + x * kGatherThreads;
+        if (q < total) {
+          const int row = q / cpr, c = q - row * cpr;
+          *reinterpret_cast<uint4*>(a.hot + dst_off[row] + c * 8) = v[x];
+        }
+      }
+    }
+    moved += nrow;
+    __syncthreads();
+  }
+  if (tid == 0 && moved && a.stats) {
+    atomicAdd(&a.stats->rows_h2d, (unsigned long long)moved);
+    atomicAdd(&a.stats->bytes_h2d, (unsigned long long)moved * a.row_elems * 2ull);
+  }
+}
+
+// ---------------------------------------------------------------------------
+// gather, bulk async copies host -> shared -> hot (one elected lane per warp,
+// kBulkDepth rows in flight per warp)
+// ---------------------------------------------------------------------------
+__global__ void __launch_bounds__(kGatherThreads) gather_bulk_kernel(GatherArgs a) {
+  extern __shared__ __align__(128) uint8_t smem[];
+  constexpr int kWarps = kGatherThreads / 32;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const uint32_t row_bytes = (uint32_t)a.row_elems * 2u;
+  const uint32_t slot_bytes = (row_bytes + 127u) & ~127u;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem);  // [kWarps][kBulkDepth]
+  uint8_t* stage = smem + 128 * ((kWarps * kBulkDepth * 8 + 127) / 128);
+  uint64_t* mybar = bars + warp * kBulkDepth;
+  uint8_t* mybuf = stage + (size_t)warp * kBulkDepth * slot_bytes;
+  if (lane == 0) {
+    for (int d = 0; d < kBulkDepth; ++d) mbar_init(&mybar[d], 1);
+    fence_mbar_init();
+  }
+  __syncwarp();
+  if (lane != 0) return;
+  const int64_t R = a.miss_off[a.n];
+  const int64_t gw = (int64_t)blockIdx.x * kWarps + warp;
+  const int64_t nw = (int64_t)gridDim.x * kWarps;
+  // rows handled by this warp: r = gw + q * nw, q = 0, 1, ...
+  const int64_t nq = R > gw ? (R - gw + nw - 1) / nw : 0;
+  auto addr = [&](int64_t q, const uint16_t** src, uint16_t** dst) {
+    const int64_t r = gw + q * nw;
+    const int i = find_segment(a.miss_off, a.n, r);
+    const int64_t loc = r - a.miss_off[i];
+    const int u = a.units[i];
+    const int32_t t = a.miss_tok[(int64_t)i * a.pk + loc];
+    const int32_t s = a.miss_slot[(int64_t)i * a.pk + loc];
+    *src = a.host_pool + ((int64_t)u * a.stride + t) * a.row_elems;
+    *dst = a.hot + ((int64_t)u * a.C + s) * a.row_elems;
+  };
+  bool timed_out = false;
+  const int64_t pro = nq < kBulkDepth ? nq : kBulkDepth;
+  for (int64_t q = 0; q < pro; ++q) {
+    const uint16_t* src;
+    uint16_t* dst;
+    addr(q, &src, &dst);
+    mbar_arrive_expect_tx(&mybar[q], row_bytes);
+    bulk_g2s(mybuf + q * slot_bytes, src, row_bytes, &mybar[q]);
+  }
+  for (int64_t q = 0; q < nq; ++q) {
+    const int d = (int)(q % kBulkDepth);
+    const uint32_t parity = (uint32_t)((q / kBulkDepth) & 1);
+    if (!mbar_wait(&mybar[d], parity, a.wait_ns)) timed_out = true;
+    const uint16_t* src;
+    uint16_t* dst;
+    addr(q, &src, &dst);
+    bulk_s2g(dst, mybuf + d * slot_bytes, row_bytes);
+    bulk_commit();
+    if (q + kBulkDepth < nq) {
+      bulk_wait_read_all();  // staging slot d is free again
+      addr(q + kBulkDepth, &src, &dst);
+      mbar_arrive_expect_tx(&mybar[d], row_bytes);
+      bulk_g2s(mybuf + d * slot_bytes, src, row_bytes, &mybar[d]);
+    }
+  }
+  bulk_wait_all();
+  if (timed_out) atomicOr(a.err, kErrTimeout);
+  if (nq && a.stats) {
+    atomicAdd(&a.stats->rows_h2d, (unsigned long long)nq);
+    atomicAdd(&a.stats->bytes_h2d, (unsigned long long)nq * row_bytes);
+  }
+}
+
+// ---------------------------------------------------------------------------
+// append: one CTA per listed unit
+// ---------------------------------------------------------------------------
+__global__ void __launch_bounds__(256) append_kernel(AppendArgs a) {
+  __shared__ int32_t base;
+  const int i = blockIdx.x, tid = threadIdx.x;
+  const int u = a.units[i];
+  if (tid == 0) base = a.len[u];
+  __syncthreads();
+  const int cpr = a.row_elems / 8;
+  const int64_t nrow_chunks = (int64_t)a.n_tok * cpr;
+  const uint4* src = reinterpret_cast<const uint4*>(a.rows + (int64_t)i * a.n_tok * a.row_elems);
+  for (int64_t q = tid; q < nrow_chunks; q += blockDim.x) {
+    const int64_t tj = q / cpr, c = q - tj * cpr;
+    *reinterpret_cast<uint4*>(a.host_pool + ((int64_t)u * a.stride + base + tj) * a.row_elems + c * 8) =
+        src[q];
+  }
+  const int64_t nkey_chunks = (int64_t)a.n_tok * (kDim / 8);
+  const uint4* ksrc = reinterpret_cast<const uint4*>(a.keys + (int64_t)i * a.n_tok * kDim);
+  for (int64_t q = tid; q < nkey_chunks; q += blockDim.x) {
+    const int64_t tj = q / (kDim / 8), c = q - tj * (kDim / 8);
+    *reinterpret_cast<uint4*>(a.idx + ((int64_t)u * a.stride + base + tj) * kDim + c * 8) = ksrc[q];
+  }
+  __syncthreads();
+  if (tid == 0) {
+    a.len[u] = base + a.n_tok;
+    if (a.stats) {
+      atomicAdd(&a.stats->rows_d2h, (unsigned long long)a.n_tok);
+      atomicAdd(&a.stats->bytes_d2h, (unsigned long long)a.n_tok * a.row_elems * 2ull);
+    }
+  }
+}
+
+__global__ void set_len_kernel(int32_t* len, int32_t unit, int32_t value) { len[unit] = value; }
+
+__global__ void fill_i32_kernel(int32_t* p, int32_t v, size_t n) {
+  for (size_t e = blockIdx.x * (size_t)blockDim.x + threadIdx.x; e < n; e += (size_t)gridDim.x * blockDim.x)
+    p[e] = v;
+}
+
+// ---------------------------------------------------------------------------
+// host launchers
+// ---------------------------------------------------------------------------
+size_t residency_smem(int C, int P, int k) {
+  int n2 = 1;
+  while (n2 < P * k) n2 <<= 1;
+  const int nwords = (C + 31) / 32;
+  const int nwords_pad = (nwords + 3) & ~3;
+  return (size_t)nwords_pad * 4 + (size_t)n2 * 4 * 2 + (size_t)n2 * 8;
+}
+
+cudaError_t launch_residency(const ResidencyArgs& a, cudaStream_t s) {
+  const size_t smem = residency_smem(a.C, a.P, a.k);
+  cudaError_t e = cudaFuncSetAttribute(residency_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return e;
+  residency_kernel<<<a.n, kResThreads, smem, s>>>(a);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_gather(const GatherArgs& a, int n_sm, cudaStream_t s) {
+  if (a.mode == KVO_GATHER_BULK) {
+    const uint32_t slot_bytes = ((uint32_t)a.row_elems * 2u + 127u) & ~127u;
+    const size_t smem = 128 * ((kGatherThreads / 32 * kBulkDepth * 8 + 127) / 128) +
+                        (size_t)(kGatherThreads / 32) * kBulkDepth * slot_bytes;
+    cudaError_t e = cudaFuncSetAttribute(gather_bulk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    gather_bulk_kernel<<<n_sm * 4, kGatherThreads, smem, s>>>(a);
+  } else {
+    gather_ldg_kernel<<<n_sm * 4, kGatherThreads, 0, s>>>(a);
+  }
+  return cudaGetLastError();
+}
+
+cudaError_t launch_append(const AppendArgs& a, cudaStream_t s) {
+  append_kernel<<<a.n, 256, 0, s>>>(a);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_set_len(int32_t* len, int32_t unit, int32_t value, cudaStream_t s) {
+  set_len_kernel<<<1, 1, 0, s>>>(len, unit, value);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_fill_i32(int32_t* p, int32_t v, size_t n, cudaStream_t s) {
+  if (n == 0) return cudaSuccess;
+  size_t blocks = (n + 255) / 256;
+  if (blocks > 65535) blocks = 65535;
+  fill_i32_kernel<<<(unsigned)blocks, 256, 0, s>>>(p, v, n);
+  return cudaGetLastError();
+}
+
+}  // namespace kvo

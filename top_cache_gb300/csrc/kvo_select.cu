@@ -1,0 +1,616 @@
+// Indexer scoring and the fused top-k ("Layerwise and Sparse KV Cache
+// Offloading Design", section 4, Decode step 3; "FlashOffloading ... What does
+// it mean?", the LIM paragraph: index and slot packed into one int32 so the
+// winners already say hit or miss).
+//
+// Three kernels, all on the caller's stream:
+//  plan_kernel   : flat token offsets of the listed units (one block).
+//  score_kernel  : persistent, one CTA per SM.  The listed units' cached
+//                  tokens form one flat range that is cut into G equal
+//                  pieces; each CTA streams its piece's indexer keys through
+//                  a bulk-copy ring in shared memory, scores every token
+//                  against the P queries (CUDA-core fp32, the canonical
+//                  order), and keeps, per (unit, position), the tokens that
+//                  can still be in the top-k in a shared-memory candidate
+//                  buffer filtered by a rising threshold.  At the end of each
+//                  unit piece it writes at most k candidates per position.
+//  select_kernel : one CTA per (unit, position): exact radix select of the k
+//                  best candidates over the unit's pieces, bitonic sort into
+//                  (score desc, token asc) order, payload packed from
+//                  cache_slots for the winners.
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "kvo_internal.cuh"
+
+namespace kvo {
+
+namespace {
+
+constexpr int kTile = 128;                  // tokens per ring stage
+constexpr int kTileBytes = kTile * kKeyBytes;
+constexpr int kStages = 3;
+constexpr int kCW = 16;                     // consumer warps
+constexpr int kCT = kCW * 32;               // consumer threads
+constexpr int kScoreThreads = kCT + 32;     // + one producer warp
+constexpr int kSmemMax = 227 * 1024;
+constexpr int kSmemFixed = kStages * kTileBytes + 2 * kStages * 8 + 8 * 4 + 8 * 8 + 256 * 4 + 8 * 4;
+constexpr int kSelThreads = 512;
+constexpr int kSelSmemKeys = 8192;          // candidates held in shared memory by select
+constexpr int kMaxK = 4096;
+
+// ---------------------------------------------------------------------------
+// 16-lane tree reduction of chunk sums.  Lane j (of a half warp) holds chunk
+// j's partial sums for V (token, position) pairs.  Levels pair lanes j and
+// j^8, then j^4, j^2, j^1: exactly the tree c_j += c_{j+w}, w = 8, 4, 2, 1
+// (fp32 addition is commutative, so both lanes of a pair hold the same sum).
+// While more than one value is left per lane, a level also transposes: each
+// lane keeps half of the values and receives the partner's partial of that
+// half, so V values cost V-1 shuffles instead of 4V.
+// ---------------------------------------------------------------------------
+template <int CUR, int V>
+__device__ __forceinline__ void tree_level(float (&a)[V], int lane, int m) {
+  if constexpr (CUR > 1) {
+    const bool up = (lane & m) != 0;
+#pragma unroll
+    for (int i = 0; i < CUR / 2; ++i) {
+      const float send = up ? a[i] : a[i + CUR / 2];
+      const float keep = up ? a[i + CUR / 2] : a[i];
+      a[i] = keep + __shfl_xor_sync(kFull, send, m);
+    }
+  } else {
+    a[0] = a[0] + __shfl_xor_sync(kFull, a[0], m);
+  }
+}
+
+template <int V>
+__device__ __forceinline__ void tree16(float (&a)[V], int lane) {
+  tree_level<V, V>(a, lane, 8);
+  tree_level<(V >= 2 ? V / 2 : 1), V>(a, lane, 4);
+  tree_level<(V >= 4 ? V / 4 : 1), V>(a, lane, 2);
+  tree_level<(V >= 8 ? V / 8 : 1), V>(a, lane, 1);
+}
+
+// Index (into the original V values) of the first value a lane holds after
+// tree16, and whether the lane is the one that reports it.
+template <int V>
+__device__ __forceinline__ int tree_offset(int lane) {
+  int off = 0, cur = V;
+#pragma unroll
+  for (int m = 8; m >= 1; m >>= 1) {
+    if (cur > 1) {
+      if (lane & m) off += cur / 2;
+      cur /= 2;
+    }
+  }
+  return off;
+}
+template <int V>
+__device__ __forceinline__ bool tree_owner(int lane) {
+  constexpr int dup = V >= 16 ? 0 : (16 / V - 1);
+  return (lane & dup) == 0;
+}
+
+// Warp 0 of the block: find the histogram bin (counting from the top) that
+// holds the need-th largest element.  rx[0] = bin, rx[1] = count above it,
+// rx[2] = count in it.
+__device__ __forceinline__ void scan_bins_desc(const uint32_t* hist, uint32_t need, uint32_t* rx,
+                                               int lane) {
+  uint32_t v[8], sum = 0;
+#pragma unroll
+  for (int e = 0; e < 8; ++e) {
+    v[e] = hist[255 - 8 * lane - e];
+    sum += v[e];
+  }
+  uint32_t incl = sum;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const uint32_t y = __shfl_up_sync(kFull, incl, o);
+    if (lane >= o) incl += y;
+  }
+  uint32_t above = incl - sum;
+#pragma unroll
+  for (int e = 0; e < 8; ++e) {
+    if (above < need && need <= above + v[e]) {
+      rx[0] = 255 - 8 * lane - e;
+      rx[1] = above;
+      rx[2] = v[e];
+    }
+    above += v[e];
+  }
+}
+
+// Exact radix select over unique 64-bit keys: returns the smallest value
+// 'thr' such that exactly 'need' keys are >= thr.  for_each(f) must call f on
+// every key once (strided over the NT participating threads); sync() is the
+// barrier of those threads.  Requires need <= number of keys.
+template <int NT, class ForEach, class Sync>
+__device__ __forceinline__ uint64_t radix_threshold_desc(ForEach for_each, uint32_t need,
+                                                         uint32_t* hist, uint32_t* rx, int tid,
+                                                         Sync sync) {
+  uint64_t prefix = 0, mask = 0;
+  for (int shift = 56; shift >= 0; shift -= 8) {
+    for (int b = tid; b < 256; b += NT) hist[b] = 0;
+    sync();
+    for_each([&](uint64_t key) {
+      if ((key & mask) == prefix) atomicAdd(&hist[(uint32_t)(key >> shift) & 255u], 1u);
+    });
+    sync();
+    if (tid < 32) scan_bins_desc(hist, need, rx, tid);
+    sync();
+    const uint32_t bin = rx[0], above = rx[1], inbin = rx[2];
+    need -= above;
+    prefix |= (uint64_t)bin << shift;
+    mask |= 0xffull << shift;
+    if (inbin == need) break;
+  }
+  return prefix;
+}
+
+// In-place bitonic sort, descending, of n (power of two) keys in shared memory.
+template <int NT, class Sync>
+__device__ __forceinline__ void bitonic_desc(uint64_t* buf, int n, int tid, Sync sync) {
+  for (int size = 2; size <= n; size <<= 1) {
+    for (int stride = size >> 1; stride > 0; stride >>= 1) {
+      for (int i = tid; i < (n >> 1); i += NT) {
+        const int lo = 2 * i - (i & (stride - 1));
+        const int hi = lo + stride;
+        const uint64_t x = buf[lo], y = buf[hi];
+        const bool desc = (lo & size) == 0;
+        if (desc ? (x < y) : (x > y)) {
+          buf[lo] = y;
+          buf[hi] = x;
+        }
+      }
+      sync();
+    }
+  }
+}
+
+__device__ __forceinline__ void consumer_sync() { named_sync(1, kCT); }
+
+// Shrink candidate buffer p to exactly k entries (the k largest keys) and
+// raise its threshold.  All consumer threads call it; cnt[p] > k.
+__device__ __forceinline__ void compact_candidates(uint64_t* cand, uint32_t* cnt, uint64_t* thr,
+                                                   uint64_t* scratch, uint32_t* hist, uint32_t* rx,
+                                                   int k, int ctid) {
+  const uint32_t n = *cnt;
+  auto for_each = [&](auto f) {
+    for (uint32_t i = ctid; i < n; i += kCT) f(cand[i]);
+  };
+  const uint64_t t = radix_threshold_desc<kCT>(for_each, (uint32_t)k, hist, rx, ctid, consumer_sync);
+  if (ctid == 0) rx[3] = 0;
+  consumer_sync();
+  const int lane = ctid & 31;
+  for (uint32_t i0 = 0; i0 < n; i0 += kCT) {
+    const uint32_t i = i0 + ctid;
+    const uint64_t key = i < n ? cand[i] : 0;
+    const bool keep = i < n && key >= t;
+    const uint32_t m = __ballot_sync(kFull, keep);
+    if (m) {
+      uint32_t base = 0;
+      if (lane == 0) base = atomicAdd(&rx[3], __popc(m));
+      base = __shfl_sync(kFull, base, 0);
+      const uint32_t dst = base + __popc(m & lanemask_lt());
+      if (keep && dst < (uint32_t)k) scratch[dst] = key;
+    }
+  }
+  consumer_sync();
+  for (int i = ctid; i < k; i += kCT) cand[i] = scratch[i];
+  if (ctid == 0) {
+    *cnt = (uint32_t)k;
+    *thr = t;
+  }
+  consumer_sync();
+}
+
+struct Piece {
+  int i;          // index into the listed units
+  int64_t t0, t1; // local token range
+  int64_t len;    // unit length
+};
+
+// The pieces of CTA c's flat range, in order.  Returns false when done.
+struct PieceIter {
+  const int64_t* off;
+  int n;
+  int64_t g0, g1;
+  int i;
+  __device__ void begin(const int64_t* o, int n_, int64_t a, int64_t b) {
+    off = o;
+    n = n_;
+    g0 = a;
+    g1 = b;
+    i = (a < b) ? find_segment(o, n_, a) : n_;
+  }
+  __device__ bool next(Piece& pc) {
+    while (i < n) {
+      const int64_t s = off[i], e = off[i + 1];
+      if (s >= g1) {
+        i = n;
+        return false;
+      }
+      const int cur = i++;
+      const int64_t a = s > g0 ? s : g0, b = e < g1 ? e : g1;
+      if (a < b) {
+        pc.i = cur;
+        pc.t0 = a - s;
+        pc.t1 = b - s;
+        pc.len = e - s;
+        return true;
+      }
+    }
+    return false;
+  }
+};
+
+}  // namespace
+
+// ---------------------------------------------------------------------------
+// plan: off[i] = sum of len[units[j]] for j < i; check off[n] == T.
+// ---------------------------------------------------------------------------
+__global__ void __launch_bounds__(1024) plan_kernel(SelectArgs a) {
+  __shared__ int64_t warp_sums[32];
+  __shared__ int64_t carry;
+  const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
+  if (tid == 0) carry = 0;
+  __syncthreads();
+  for (int base = 0; base < a.n; base += 1024) {
+    const int i = base + tid;
+    const int64_t v = i < a.n ? (int64_t)a.len[a.units[i]] : 0;
+    int64_t incl = v;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int64_t y = __shfl_up_sync(kFull, incl, o);
+      if (lane >= o) incl += y;
+    }
+    if (lane == 31) warp_sums[w] = incl;
+    __syncthreads();
+    if (w == 0) {
+      int64_t s = warp_sums[lane];
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int64_t y = __shfl_up_sync(kFull, s, o);
+        if (lane >= o) s += y;
+      }
+      warp_sums[lane] = s;
+    }
+    __syncthreads();
+    const int64_t excl = carry + (w ? warp_sums[w - 1] : 0) + incl - v;
+    if (i < a.n) a.off[i] = excl;
+    __syncthreads();
+    if (tid == 1023) carry = excl + v;
+    __syncthreads();
+  }
+  if (tid == 0) {
+    a.off[a.n] = carry;
+    if (carry != a.T) atomicOr(a.err, kErrPlan);
+  }
+}
+
+// ---------------------------------------------------------------------------
+// score: one persistent CTA per flat piece of the token range.
+// ---------------------------------------------------------------------------
+template <int PP>
+__global__ void __launch_bounds__(kScoreThreads, 1) score_kernel(SelectArgs a) {
+  extern __shared__ __align__(128) uint8_t smem[];
+  uint8_t* ring = smem;
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + kStages * kTileBytes);
+  uint64_t* empty = full + kStages;
+  uint32_t* cnt = reinterpret_cast<uint32_t*>(empty + kStages);  // [8]
+  uint64_t* thr = reinterpret_cast<uint64_t*>(cnt + 8);           // [8]
+  uint32_t* hist = reinterpret_cast<uint32_t*>(thr + 8);          // [256]
+  uint32_t* rx = hist + 256;                                      // [8]
+  uint64_t* cand = reinterpret_cast<uint64_t*>(rx + 8);           // [P][cap]
+  uint64_t* scratch = cand + (size_t)a.P * a.cap;                 // [k]
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int c = blockIdx.x;
+  const int64_t g0 = cta_start(c, a.T, a.G), g1 = cta_start(c + 1, a.T, a.G);
+  if (tid == 0) {
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], kCW);
+    }
+    fence_mbar_init();
+  }
+  __syncthreads();
+  if (g0 >= g1) return;
+
+  if (warp == kCW) {
+    // ---------------- producer: stream every tile of every piece ----------
+    if (lane == 0) {
+      PieceIter it;
+      it.begin(a.off, a.n, g0, g1);
+      Piece pc;
+      uint32_t seq = 0;
+      while (it.next(pc)) {
+        const int u = a.units[pc.i];
+        const uint16_t* kb = a.keys + ((int64_t)u * a.stride) * kDim;
+        for (int64_t t = pc.t0; t < pc.t1; t += kTile, ++seq) {
+          const int stage = seq % kStages;
+          const uint32_t round = seq / kStages;
+          if (round > 0 && !mbar_wait(&empty[stage], (round - 1) & 1u, a.wait_ns))
+            atomicOr(a.err, kErrTimeout);
+          const int64_t nt = (pc.t1 - t) < kTile ? (pc.t1 - t) : kTile;
+          const uint32_t bytes = (uint32_t)nt * kKeyBytes;
+          mbar_arrive_expect_tx(&full[stage], bytes);
+          bulk_g2s(ring + stage * kTileBytes, kb + t * kDim, bytes, &full[stage]);
+        }
+      }
+    }
+    return;
+  }
+
+  // ---------------- consumers ----------------------------------------------
+  constexpr int V = 4 * PP;                 // (token, position) pairs per lane
+  constexpr int VL = V >= 16 ? V / 16 : 1;  // values left per lane after the tree
+  const int ctid = tid;                     // consumers are threads 0..kCT-1
+  const int h = lane >> 4, j = lane & 15;
+  const int toff = tree_offset<V>(lane);
+  const bool owner = tree_owner<V>(lane);
+  const int P = a.P, k = a.k, cap = a.cap;
+
+  PieceIter it;
+  it.begin(a.off, a.n, g0, g1);
+  Piece pc;
+  uint32_t seq = 0;
+  while (it.next(pc)) {
+    const int i = pc.i;
+    // this lane's chunk of every query (fp32, exact)
+    float qf[PP][8];
+#pragma unroll
+    for (int p = 0; p < PP; ++p) {
+      if (p < P) {
+        const uint4 v = *reinterpret_cast<const uint4*>(a.queries + ((int64_t)i * P + p) * kDim + j * 8);
+        qf[p][0] = bf_lo(v.x); qf[p][1] = bf_hi(v.x);
+        qf[p][2] = bf_lo(v.y); qf[p][3] = bf_hi(v.y);
+        qf[p][4] = bf_lo(v.z); qf[p][5] = bf_hi(v.z);
+        qf[p][6] = bf_lo(v.w); qf[p][7] = bf_hi(v.w);
+      } else {
+#pragma unroll
+        for (int e = 0; e < 8; ++e) qf[p][e] = 0.f;
+      }
+    }
+    if (ctid < P) {
+      cnt[ctid] = 0;
+      thr[ctid] = 0;
+    }
+    consumer_sync();
+
+    for (int64_t t = pc.t0; t < pc.t1; t += kTile, ++seq) {
+      const int stage = seq % kStages;
+      const uint32_t round = seq / kStages;
+      if (!mbar_wait(&full[stage], round & 1u, a.wait_ns) && lane == 0) atomicOr(a.err, kErrTimeout);
+      const int nt = (int)((pc.t1 - t) < kTile ? (pc.t1 - t) : kTile);
+      const uint8_t* tile = ring + stage * kTileBytes;
+
+      float acc[V];
+#pragma unroll
+      for (int tau = 0; tau < 4; ++tau) {
+        const int row = warp * 8 + h * 4 + tau;
+        const uint4 kv = *reinterpret_cast<const uint4*>(tile + row * kKeyBytes + j * 16);
+        const float kf[8] = {bf_lo(kv.x), bf_hi(kv.x), bf_lo(kv.y), bf_hi(kv.y),
+                             bf_lo(kv.z), bf_hi(kv.z), bf_lo(kv.w), bf_hi(kv.w)};
+#pragma unroll
+        for (int p = 0; p < PP; ++p) {
+          float s = 0.f;
+#pragma unroll
+          for (int e = 0; e < 8; ++e) s = __fmaf_rn(qf[p][e], kf[e], s);
+          acc[tau * PP + p] = s;
+        }
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&empty[stage]);
+      tree16<V>(acc, lane);
+
+#pragma unroll
+      for (int r = 0; r < VL; ++r) {
+        const int v = toff + r;
+        const int tau = v / PP, p = v % PP;
+        const int row = warp * 8 + h * 4 + tau;
+        const int64_t tok = t + row;
+        float s = acc[r];
+        if (s == 0.f) s = 0.f;  // +0 for a zero score
+        bool pass = false;
+        uint64_t key = 0;
+        if (owner && row < nt && p < P && tok < pc.len - (P - 1 - p)) {
+          key = sel_key(s, (uint32_t)tok);
+          pass = key >= thr[p];
+        }
+        if (__ballot_sync(kFull, pass)) {
+          for (int pp = 0; pp < P; ++pp) {
+            const bool mine = pass && p == pp;
+            const uint32_t m = __ballot_sync(kFull, mine);
+            if (m) {
+              const int leader = __ffs(m) - 1;
+              uint32_t base = 0;
+              if (lane == leader) base = atomicAdd(&cnt[pp], __popc(m));
+              base = __shfl_sync(kFull, base, leader);
+              const uint32_t dst = base + __popc(m & lanemask_lt());
+              if (mine && dst < (uint32_t)cap) cand[(size_t)pp * cap + dst] = key;
+            }
+          }
+        }
+      }
+      consumer_sync();
+      bool need = false;
+      for (int p = 0; p < P; ++p) need |= cnt[p] > (uint32_t)(cap - kTile);
+      if (need) {
+        for (int p = 0; p < P; ++p)
+          if (cnt[p] > (uint32_t)(cap - kTile))
+            compact_candidates(cand + (size_t)p * cap, &cnt[p], &thr[p], scratch, hist, rx, k, ctid);
+      }
+    }
+
+    // piece done: at most k candidates per position go out
+    for (int p = 0; p < P; ++p)
+      if (cnt[p] > (uint32_t)k)
+        compact_candidates(cand + (size_t)p * cap, &cnt[p], &thr[p], scratch, hist, rx, k, ctid);
+    const int64_t seg = (int64_t)c + i;
+    for (int p = 0; p < P; ++p) {
+      const uint32_t np = cnt[p];
+      uint64_t* dst = a.seg_keys + (seg * P + p) * (int64_t)k;
+      for (uint32_t e = ctid; e < np; e += kCT) dst[e] = cand[(size_t)p * cap + e];
+      if (ctid == 0) a.seg_cnt[seg * P + p] = (int32_t)np;
+    }
+    consumer_sync();
+  }
+}
+
+// ---------------------------------------------------------------------------
+// select: exact top-k of one (unit, position) over its pieces' candidates.
+// ---------------------------------------------------------------------------
+__global__ void __launch_bounds__(kSelThreads) select_kernel(SelectArgs a) {
+  extern __shared__ __align__(128) uint8_t smem[];
+  uint64_t* keys = reinterpret_cast<uint64_t*>(smem);          // [kSelSmemKeys]
+  uint64_t* sorted = keys + kSelSmemKeys;                       // [kpad]
+  __shared__ uint32_t hist[256];
+  __shared__ uint32_t rx[8];
+
+  const int tid = threadIdx.x;
+  const int P = a.P, k = a.k;
+  const int i = blockIdx.x / P, p = blockIdx.x % P;
+  const int64_t s0 = a.off[i], s1 = a.off[i + 1];
+  int c0 = 0, c1 = -1;
+  if (s1 > s0) {
+    c0 = cta_of(s0, a.T, a.G);
+    c1 = cta_of(s1 - 1, a.T, a.G);
+  }
+  uint32_t n = 0;
+  for (int c = c0; c <= c1; ++c) n += (uint32_t)a.seg_cnt[((int64_t)c + i) * P + p];
+  const bool in_smem = n <= (uint32_t)kSelSmemKeys;
+  auto sync = [] { __syncthreads(); };
+
+  if (in_smem) {
+    uint32_t base = 0;
+    for (int c = c0; c <= c1; ++c) {
+      const int64_t seg = (int64_t)c + i;
+      const uint32_t m = (uint32_t)a.seg_cnt[seg * P + p];
+      const uint64_t* src = a.seg_keys + (seg * P + p) * (int64_t)k;
+      for (uint32_t e = tid; e < m; e += kSelThreads) keys[base + e] = src[e];
+      base += m;
+    }
+    __syncthreads();
+  }
+  auto for_each = [&](auto f) {
+    if (in_smem) {
+      for (uint32_t e = tid; e < n; e += kSelThreads) f(keys[e]);
+    } else {
+      for (int c = c0; c <= c1; ++c) {
+        const int64_t seg = (int64_t)c + i;
+        const uint32_t m = (uint32_t)a.seg_cnt[seg * P + p];
+        const uint64_t* src = a.seg_keys + (seg * P + p) * (int64_t)k;
+        for (uint32_t e = tid; e < m; e += kSelThreads) f(src[e]);
+      }
+    }
+  };
+  uint64_t thr = 0;
+  if (n > (uint32_t)k) thr = radix_threshold_desc<kSelThreads>(for_each, (uint32_t)k, hist, rx, tid, sync);
+  const uint32_t count = n < (uint32_t)k ? n : (uint32_t)k;
+  int kpad = 1;
+  while (kpad < k) kpad <<= 1;
+  if (tid == 0) rx[4] = 0;
+  __syncthreads();
+  const int lane = tid & 31;
+  // keys >= thr go to the sort buffer (uniform trip counts: full-warp ballots)
+  auto keep_from = [&](const uint64_t* src, uint32_t m) {
+    for (uint32_t b = 0; b < m; b += kSelThreads) {
+      const uint32_t e = b + tid;
+      const uint64_t key = e < m ? src[e] : 0;
+      const bool keep = e < m && key >= thr;
+      const uint32_t msk = __ballot_sync(kFull, keep);
+      if (msk) {
+        uint32_t base = 0;
+        if (lane == 0) base = atomicAdd(&rx[4], __popc(msk));
+        base = __shfl_sync(kFull, base, 0);
+        const uint32_t dst = base + __popc(msk & lanemask_lt());
+        if (keep && dst < (uint32_t)kpad) sorted[dst] = key;
+      }
+    }
+  };
+  if (in_smem) {
+    keep_from(keys, n);
+  } else {
+    for (int c = c0; c <= c1; ++c) {
+      const int64_t seg = (int64_t)c + i;
+      keep_from(a.seg_keys + (seg * P + p) * (int64_t)k, (uint32_t)a.seg_cnt[seg * P + p]);
+    }
+  }
+  __syncthreads();
+  for (int e = count + tid; e < kpad; e += kSelThreads) sorted[e] = 0;
+  __syncthreads();
+  bitonic_desc<kSelThreads>(sorted, kpad, tid, sync);
+
+  const int u = a.units[i];
+  const int64_t obase = ((int64_t)i * P + p) * k;
+  for (int r = tid; r < k; r += kSelThreads) {
+    int32_t tok = -1, pay = KVO_PAD_PAYLOAD;
+    float sc = __uint_as_float(0xff800000u);
+    if (r < (int)count) {
+      const uint64_t key = sorted[r];
+      tok = (int32_t)key_token(key);
+      sc = key_score(key);
+      const int32_t cs = a.cache_slots ? a.cache_slots[(int64_t)u * a.stride + tok] : -1;
+      pay = cs >= 0 ? cs : -(tok + 1);
+    }
+    a.out_tok[obase + r] = tok;
+    if (a.out_score) a.out_score[obase + r] = sc;
+    a.out_pay[obase + r] = pay;
+    if (a.out_pay_user && a.out_pay_user != a.out_pay) a.out_pay_user[obase + r] = pay;
+  }
+}
+
+// ---------------------------------------------------------------------------
+// host launchers
+// ---------------------------------------------------------------------------
+int score_cap_for(int P, int k) {
+  const long avail = (long)kSmemMax - kSmemFixed - (long)k * 8 - 256;
+  if (avail <= 0) return 0;
+  long cap = avail / ((long)P * 8);
+  long target = 3L * k;
+  if (target < k + 4L * kTile) target = k + 4L * kTile;
+  if (cap > target) cap = target;
+  cap &= ~63L;
+  if (cap < (long)k + kTile) return 0;
+  return (int)cap;
+}
+
+static size_t score_smem(const SelectArgs& a) {
+  return (size_t)kSmemFixed + (size_t)a.P * a.cap * 8 + (size_t)a.k * 8;
+}
+
+cudaError_t launch_plan(const SelectArgs& a, cudaStream_t s) {
+  plan_kernel<<<1, 1024, 0, s>>>(a);
+  return cudaGetLastError();
+}
+
+template <int PP>
+static cudaError_t launch_score_pp(const SelectArgs& a, cudaStream_t s) {
+  const size_t smem = score_smem(a);
+  cudaError_t e = cudaFuncSetAttribute(score_kernel<PP>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       (int)smem);
+  if (e != cudaSuccess) return e;
+  score_kernel<PP><<<a.G, kScoreThreads, smem, s>>>(a);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_score(const SelectArgs& a, cudaStream_t s) {
+  if (a.P <= 1) return launch_score_pp<1>(a, s);
+  if (a.P <= 2) return launch_score_pp<2>(a, s);
+  if (a.P <= 4) return launch_score_pp<4>(a, s);
+  return launch_score_pp<8>(a, s);
+}
+
+cudaError_t launch_select(const SelectArgs& a, cudaStream_t s) {
+  if (a.k > kMaxK) return cudaErrorInvalidValue;
+  int kpad = 1;
+  while (kpad < a.k) kpad <<= 1;
+  const size_t smem = (size_t)kSelSmemKeys * 8 + (size_t)kpad * 8;
+  cudaError_t e = cudaFuncSetAttribute(select_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return e;
+  select_kernel<<<a.n * a.P, kSelThreads, smem, s>>>(a);
+  return cudaGetLastError();
+}
+
+}  // namespace kvo

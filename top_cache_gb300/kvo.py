@@ -1,0 +1,270 @@
+"""Python binding of libkvo (the C ABI declared in include/kvo.h).
+
+Argument marshalling only: every step of the decode path runs in the CUDA
+kernels of libkvo.so.  PyTorch is used for device memory and streams.  There
+is no CPU fallback: if the library is missing or cannot be loaded, every call
+raises.
+"""
+import ctypes
+import os
+import threading
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SO = os.path.join(_HERE, "libkvo.so")
+
+KVO_OK = 0
+KVO_EINVAL = -1
+KVO_ENOMEM = -2
+KVO_ERANGE = -3
+KVO_ECUDA = -4
+KVO_ETIMEOUT = -5
+KVO_ECAPACITY = -6
+KVO_PAD_PAYLOAD = -(2 ** 31)
+
+KVO_OPT_GATHER_MODE = 1
+KVO_OPT_WAIT_LIMIT_NS = 2
+KVO_GATHER_LDG = 0
+KVO_GATHER_BULK = 1
+
+EXPORTED = ("kvo_create", "kvo_destroy", "kvo_host_rows", "kvo_prefill", "kvo_append", "kvo_step",
+            "kvo_select_workspace_size", "kvo_select", "kvo_set_option", "kvo_get_stats",
+            "kvo_export_state", "kvo_last_error")
+
+
+class KvoConfig(ctypes.Structure):
+    _fields_ = [("n_requests", ctypes.c_int32), ("n_layers", ctypes.c_int32),
+                ("max_tokens", ctypes.c_int64), ("idx_dim", ctypes.c_int32),
+                ("row_elems", ctypes.c_int32), ("topk", ctypes.c_int32),
+                ("hot_capacity", ctypes.c_int32), ("n_positions", ctypes.c_int32),
+                ("device", ctypes.c_int32)]
+
+
+class KvoStats(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_uint64) for n in
+                ("steps", "unit_steps", "capacity_errors", "hits", "misses", "rows_h2d",
+                 "bytes_h2d", "rows_d2h", "bytes_d2h", "timeouts")]
+
+
+class KvoError(RuntimeError):
+    def __init__(self, code, msg):
+        super().__init__("kvo error %d: %s" % (code, msg))
+        self.code = code
+
+
+_lock = threading.Lock()
+_lib = None
+
+
+def library_path():
+    return _SO
+
+
+def lib():
+    """Load libkvo.so (built by top_cache_gb300.build / __graft_entry__.build)."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            if not os.path.exists(_SO):
+                raise ImportError("libkvo.so is not built (run top_cache_gb300.build.build()); "
+                                  "there is no fallback path")
+            L = ctypes.CDLL(_SO)
+            vp, i32, i64 = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64
+            L.kvo_create.restype = ctypes.c_int
+            L.kvo_create.argtypes = [ctypes.POINTER(KvoConfig), ctypes.POINTER(vp)]
+            L.kvo_destroy.restype = ctypes.c_int
+            L.kvo_destroy.argtypes = [vp]
+            L.kvo_host_rows.restype = vp
+            L.kvo_host_rows.argtypes = [vp, i32]
+            L.kvo_prefill.restype = ctypes.c_int
+            L.kvo_prefill.argtypes = [vp, i32, i64, vp, vp]
+            L.kvo_append.restype = ctypes.c_int
+            L.kvo_append.argtypes = [vp, vp, i32, i32, vp, vp, vp]
+            L.kvo_step.restype = ctypes.c_int
+            L.kvo_step.argtypes = [vp, vp, i32, vp, vp, vp, vp, vp, vp, vp]
+            L.kvo_select_workspace_size.restype = ctypes.c_size_t
+            L.kvo_select_workspace_size.argtypes = [i32, i32, i32, i32]
+            L.kvo_select.restype = ctypes.c_int
+            L.kvo_select.argtypes = [vp, i64, vp, vp, i32, i32, i32, vp, vp, vp, vp, vp,
+                                     ctypes.c_size_t, vp]
+            L.kvo_set_option.restype = ctypes.c_int
+            L.kvo_set_option.argtypes = [vp, i32, i64]
+            L.kvo_get_stats.restype = ctypes.c_int
+            L.kvo_get_stats.argtypes = [vp, ctypes.POINTER(KvoStats)]
+            L.kvo_export_state.restype = ctypes.c_int
+            L.kvo_export_state.argtypes = [vp, i32, vp, vp, vp, vp, vp, vp]
+            L.kvo_last_error.restype = ctypes.c_char_p
+            L.kvo_last_error.argtypes = []
+            _lib = L
+    return _lib
+
+
+def _check(rc):
+    if rc != KVO_OK:
+        raise KvoError(rc, lib().kvo_last_error().decode())
+    return rc
+
+
+def _ptr(t):
+    """Device/host address of a tensor or array, or None."""
+    if t is None:
+        return None
+    if isinstance(t, int):
+        return t
+    if isinstance(t, np.ndarray):
+        return t.ctypes.data
+    return t.data_ptr()
+
+
+def _stream(stream):
+    if stream is None:
+        import torch
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, int):
+        return stream
+    return stream.cuda_stream
+
+
+def _units(units):
+    if units is None:
+        return None, None
+    arr = np.ascontiguousarray(units, dtype=np.int32)
+    return arr, arr.ctypes.data
+
+
+def kvo_create(n_requests, n_layers, max_tokens, topk, hot_capacity, n_positions=1,
+               row_elems=576, idx_dim=128, device=0):
+    cfg = KvoConfig(n_requests, n_layers, max_tokens, idx_dim, row_elems, topk, hot_capacity,
+                    n_positions, device)
+    h = ctypes.c_void_p()
+    _check(lib().kvo_create(ctypes.byref(cfg), ctypes.byref(h)))
+    return h.value
+
+
+def kvo_destroy(h):
+    return _check(lib().kvo_destroy(h))
+
+
+def kvo_host_rows(h, unit):
+    """Integer host address of unit's row 0 in the pinned host pool."""
+    p = lib().kvo_host_rows(h, unit)
+    if not p:
+        raise KvoError(KVO_ERANGE, "unit out of range")
+    return p
+
+
+def kvo_prefill(h, unit, n_tokens, idx_keys, stream=None):
+    return _check(lib().kvo_prefill(h, unit, n_tokens, _ptr(idx_keys), _stream(stream)))
+
+
+def kvo_append(h, units, n_units, n_tokens, main_rows, idx_keys, stream=None):
+    arr, up = _units(units)
+    return _check(lib().kvo_append(h, up, n_units, n_tokens, _ptr(main_rows), _ptr(idx_keys),
+                                   _stream(stream)))
+
+
+def kvo_step(h, units, n_units, queries, topk_tokens, topk_slots, topk_scores, topk_payload,
+             unit_status, stream=None):
+    arr, up = _units(units)
+    return _check(lib().kvo_step(h, up, n_units, _ptr(queries), _ptr(topk_tokens),
+                                 _ptr(topk_slots), _ptr(topk_scores), _ptr(topk_payload),
+                                 _ptr(unit_status), _stream(stream)))
+
+
+def kvo_select_workspace_size(n_units, n_pos, k, device=0):
+    return int(lib().kvo_select_workspace_size(n_units, n_pos, k, device))
+
+
+def kvo_select(keys, unit_stride, cache_slots, lengths, n_units, n_pos, k, queries, tokens,
+               scores, payload, workspace, workspace_bytes, stream=None):
+    ln = np.ascontiguousarray(lengths, dtype=np.int64)
+    return _check(lib().kvo_select(_ptr(keys), unit_stride, _ptr(cache_slots), ln.ctypes.data,
+                                   n_units, n_pos, k, _ptr(queries), _ptr(tokens), _ptr(scores),
+                                   _ptr(payload), _ptr(workspace), workspace_bytes,
+                                   _stream(stream)))
+
+
+def kvo_set_option(h, key, value):
+    return _check(lib().kvo_set_option(h, key, value))
+
+
+def kvo_get_stats(h):
+    s = KvoStats()
+    _check(lib().kvo_get_stats(h, ctypes.byref(s)))
+    return {n: int(getattr(s, n)) for n, _ in KvoStats._fields_}
+
+
+def kvo_export_state(h, unit, max_tokens, capacity, row_elems=576, with_rows=False):
+    cs = np.empty(max_tokens, np.int32)
+    st = np.empty(capacity, np.int32)
+    lu = np.empty(capacity, np.uint32)
+    ln = ctypes.c_int64()
+    sp = ctypes.c_uint32()
+    hot = np.empty((capacity, row_elems), np.uint16) if with_rows else None
+    _check(lib().kvo_export_state(h, unit, cs.ctypes.data, st.ctypes.data, lu.ctypes.data,
+                                  ctypes.addressof(ln), ctypes.addressof(sp),
+                                  hot.ctypes.data if with_rows else None))
+    return {"cache_slots": cs, "slot_token": st, "last_use": lu, "length": ln.value,
+            "stamp": sp.value, "hot": hot}
+
+
+class Kvo:
+    """A handle plus output buffers for all units (plumbing around the C ABI)."""
+
+    def __init__(self, n_requests, n_layers, max_tokens, topk, hot_capacity, n_positions=1,
+                 row_elems=576, device=0):
+        import torch
+        self.n_requests, self.n_layers = n_requests, n_layers
+        self.U = n_requests * n_layers
+        self.max_tokens, self.topk, self.C = max_tokens, topk, hot_capacity
+        self.P, self.R, self.device = n_positions, row_elems, device
+        self.h = kvo_create(n_requests, n_layers, max_tokens, topk, hot_capacity, n_positions,
+                            row_elems, 128, device)
+        dev = torch.device("cuda", device)
+        shape = (self.U, self.P, self.topk)
+        self.tokens = torch.empty(shape, dtype=torch.int32, device=dev)
+        self.slots = torch.empty(shape, dtype=torch.int32, device=dev)
+        self.scores = torch.empty(shape, dtype=torch.float32, device=dev)
+        self.payload = torch.empty(shape, dtype=torch.int32, device=dev)
+        self.status = torch.empty(self.U, dtype=torch.int32, device=dev)
+
+    def close(self):
+        if self.h:
+            kvo_destroy(self.h)
+            self.h = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+    def host_rows(self, unit):
+        return kvo_host_rows(self.h, unit)
+
+    def prefill(self, unit, n_tokens, idx_keys, stream=None):
+        return kvo_prefill(self.h, unit, n_tokens, idx_keys, stream)
+
+    def append(self, main_rows, idx_keys, units=None, stream=None):
+        n_units = self.U if units is None else len(units)
+        n_tok = int(idx_keys.shape[-2])
+        return kvo_append(self.h, units, n_units, n_tok, main_rows, idx_keys, stream)
+
+    def step(self, queries, units=None, stream=None, out=None):
+        n = self.U if units is None else len(units)
+        if out is None:
+            out = (self.tokens[:n], self.slots[:n], self.scores[:n], self.payload[:n],
+                   self.status[:n])
+        tok, sl, sc, pay, st = out
+        kvo_step(self.h, units, n, queries, tok, sl, sc, pay, st, stream)
+        return out
+
+    def set_option(self, key, value):
+        return kvo_set_option(self.h, key, value)
+
+    def stats(self):
+        return kvo_get_stats(self.h)
+
+    def export_state(self, unit, with_rows=False):
+        return kvo_export_state(self.h, unit, self.max_tokens, self.C, self.R, with_rows)

@@ -8,4 +8,4 @@ from .gen import (  # noqa: F401
     KIND_KEYS, KIND_ROWS, KIND_QINIT, KIND_QNOISE, build, lib, normal_bf16, normal_f64,
     token_rows, token_rows_into, query_walk, unit_queries, bf16_to_f32, f32_to_bf16_np,
 )
-from .configs import WORKLOADS, Workload, reduced  # noqa: F401
+from .configs import SWEEP_DRIFTS, WORKLOADS, Workload, reduced  # noqa: F401
