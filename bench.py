@@ -1,0 +1,599 @@
+#!/usr/bin/env python
+"""Benchmark of the sparse-decode KV offload step on GB300.
+
+One step = one pass of the whole hot path over the batch: append the new
+tokens (rows to the pinned host pool, keys to the indexer cache), then
+kvo_step (score every cached token, fused top-k with packed payload, MTP
+merge/dedup, LRU residency update, miss-row fill from host, remap).
+
+Workload (default): 16 requests x 8 layers, 32,768-token context, MTP3 (4
+positions, 4 new tokens per step), top-2048 of a 4,096-slot hot shelf, random
+walk queries with drift 0.9, a 50-step decode sequence.  The timed loop
+replays that sequence: after step 49 every unit is returned to its 32,768
+prefilled tokens with an empty shelf (kvo_reset, inside the timed region) and
+the sequence starts again, so cold and warm steps appear in the sequence's
+own mix.  The 1.07 GB of indexer keys read per step exceed the 129 MB L2.
+
+Prints one JSON line (rank 0).  --impl reference times the CPU oracle instead.
+"""
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "decode steps/s (layer·request selections/s) + miss-fill GB/s vs roofline"
+UNIT = "selections/s"
+DEFAULT_WORKLOAD = "batch16x8_32k_mtp3"
+PEAKS_FILE = os.path.join(ROOT, "MEASURED_PEAKS.json")
+TRAFFIC_FILE = os.path.join(ROOT, "profiles", "traffic.json")
+FALLBACK_HBM_GBS = 6800.0
+
+
+# --------------------------------------------------------------------------- distributed
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def dist_init(backend):
+    import torch.distributed as dist
+    world, rank, _ = dist_env()
+    if world > 1 and not dist.is_initialized():
+        os.environ.setdefault("MASTER_ADDR", "127.0.0.1")
+        dist.init_process_group(backend=backend)
+    return world, rank
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def reduce_max(x, world, device=None):
+    """Max of a float over ranks (identity when world == 1)."""
+    if world == 1:
+        return float(x)
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_rate(units_per_rank, steps, max_ms, world):
+    """Selections per second of all ranks: every rank processes units_per_rank x steps."""
+    return units_per_rank * steps * world / (max_ms / 1e3)
+
+
+# --------------------------------------------------------------------------- helpers
+def load_peaks():
+    try:
+        with open(PEAKS_FILE) as f:
+            p = json.load(f)
+        return float(p["hbm_gbs"]), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def kernel_source_hash():
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "top_cache_gb300", "csrc")
+    for name in sorted(os.listdir(csrc)):
+        with open(os.path.join(csrc, name), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def load_traffic(kernel, workload):
+    """Per-launch DRAM bytes of kernel from the committed ncu summary, if it is current."""
+    try:
+        with open(TRAFFIC_FILE) as f:
+            t = json.load(f)
+        e = t[kernel]
+        if e.get("source_hash") != kernel_source_hash() or e.get("workload") != workload:
+            return None
+        return float(e["bytes_per_launch"])
+    except Exception:
+        return None
+
+
+class ClockSampler:
+    """nvidia-smi samples (host-timestamped) while the GPU runs the timed steps."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index, period_ms=100):
+        self.samples = []
+        self.proc = None
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(gpu_index), "--query-gpu=" + self.FIELDS,
+                 "--format=csv,noheader,nounits", "-lms", str(period_ms)],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) >= 9:
+                self.samples.append((time.time(), parts))
+
+    def stop(self):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self, t0, t1):
+        def num(x):
+            try:
+                return float(x)
+            except ValueError:
+                return None
+        win = [p for (t, p) in self.samples if t0 <= t <= t1]
+        used = "timed region"
+        if len(win) < 3:
+            win = [p for (_, p) in self.samples]
+            used = "timed region and the clock window right after it"
+        if not win:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"], "samples": 0}
+        sm = [num(p[1]) for p in win if num(p[1]) is not None]
+        mx = [num(p[2]) for p in win if num(p[2]) is not None]
+        pw = [num(p[3]) for p in win if num(p[3]) is not None]
+        names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+        reasons = sorted({names[i] for p in win for i in range(4) if p[5 + i].lower() == "active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(mx) if mx else None,
+                "power_w_max": max(pw) if pw else None,
+                "reasons": reasons, "samples": len(win), "window": used}
+
+
+def measure_host_link(torch, device, nbytes=1 << 30, reps=5):
+    """Copy-engine bandwidth pinned host <-> device (GB/s), best of reps."""
+    h = torch.empty(nbytes, dtype=torch.uint8, pin_memory=True)
+    d = torch.empty(nbytes, dtype=torch.uint8, device=device)
+    h.fill_(1)
+    out = {}
+    for name, fn in (("h2d", lambda: d.copy_(h, non_blocking=True)),
+                     ("d2h", lambda: h.copy_(d, non_blocking=True))):
+        best = 0.0
+        for _ in range(reps):
+            s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            torch.cuda.synchronize()
+            s.record()
+            fn()
+            e.record()
+            torch.cuda.synchronize()
+            best = max(best, nbytes / (s.elapsed_time(e) / 1e3) / 1e9)
+        out[name] = best
+    del h, d
+    torch.cuda.empty_cache()
+    return out
+
+
+# --------------------------------------------------------------------------- workload set-up
+def make_workload(args):
+    import workload as W
+    wl = W.WORKLOADS[args.workload]
+    kw = {}
+    if args.requests:
+        kw["n_requests"] = args.requests
+    if args.layers:
+        kw["n_layers"] = args.layers
+    if args.context:
+        kw["context"] = args.context
+    if kw:
+        wl = W.reduced(wl, **kw)
+    return wl
+
+
+def prepare(wl, rank, device, log):
+    """Handle with the prefilled context, plus per-sequence-step inputs on the device."""
+    import numpy as np
+    import torch
+    import workload as W
+    from top_cache_gb300 import kvo as K
+
+    units = [(rank * wl.n_requests + r, l) for r in range(wl.n_requests) for l in range(wl.n_layers)]
+    U = len(units)
+    S = wl.steps
+    tmax = wl.max_tokens(S)
+    t0 = time.time()
+    kv = K.Kvo(wl.n_requests, wl.n_layers, tmax, wl.topk, wl.hot_capacity, wl.n_pos, wl.row_elems,
+               device=device.index or 0)
+    unit_stride = (kv.host_rows(1) - kv.host_rows(0)) // 2 if U > 1 else 0
+    W.token_rows_into(kv.host_rows(0), unit_stride, wl.seed, W.KIND_ROWS, units, 0, wl.context,
+                      wl.row_elems)
+    chunk = max(1, (256 << 20) // max(1, wl.context * 256))
+    for b in range(0, U, chunk):
+        ids = list(range(b, min(U, b + chunk)))
+        keys = torch.from_numpy(W.token_rows(wl.seed, W.KIND_KEYS, [units[u] for u in ids], 0,
+                                             wl.context, 128)).to(device)
+        for j, u in enumerate(ids):
+            kv.prefill(u, wl.context, keys[j])
+        torch.cuda.synchronize(device)
+        del keys
+    # inputs of every step of the sequence (untimed set-up)
+    rows = np.empty((S, U, wl.n_new, wl.row_elems), np.uint16)
+    keys = np.empty((S, U, wl.n_new, 128), np.uint16)
+    for s in range(S):
+        t = wl.context + s * wl.n_new
+        rows[s] = W.token_rows(wl.seed, W.KIND_ROWS, units, t, wl.n_new, wl.row_elems)
+        keys[s] = W.token_rows(wl.seed, W.KIND_KEYS, units, t, wl.n_new, 128)
+    q = W.unit_queries(wl.seed, units, wl.drift, S, wl.n_pos)
+    inp = {"rows_h": rows, "keys_h": keys, "q_h": q,
+           "rows": torch.from_numpy(rows).to(device), "keys": torch.from_numpy(keys).to(device),
+           "q": torch.from_numpy(q).to(device)}
+    log("set-up %.1f s (host pool %.2f GB pinned)" % (time.time() - t0,
+                                                        U * tmax * wl.row_elems * 2 / 1e9))
+    return kv, inp, units
+
+
+class Sequence:
+    """Replays the workload's decode sequence: reset to the prefill every S steps."""
+
+    def __init__(self, kv, inp, wl):
+        self.kv, self.inp, self.wl = kv, inp, wl
+        self.g = 0
+
+    def pos(self):
+        return self.g % self.wl.steps
+
+    def step(self, out=None):
+        p = self.pos()
+        if p == 0 and self.g > 0:
+            self.kv.reset(self.wl.context)
+        self.kv.append(self.inp["rows"][p], self.inp["keys"][p])
+        self.kv.step(self.inp["q"][p], out=out)
+        self.g += 1
+        return p
+
+
+# --------------------------------------------------------------------------- GPU arm
+def run_kvo(args, log):
+    import numpy as np
+    import torch
+    from top_cache_gb300 import kvo as K
+
+    world, rank = dist_init("nccl")
+    _, _, local = dist_env()
+    torch.cuda.set_device(local)
+    device = torch.device("cuda", local)
+    wl = make_workload(args)
+    hbm_peak, hbm_src = load_peaks()
+    link = measure_host_link(torch, device)
+    kv, inp, units = prepare(wl, rank, device, log)
+    U, P, k, R = len(units), wl.n_pos, wl.topk, wl.row_elems
+    kv.set_option(K.KVO_OPT_GATHER_MODE, K.KVO_GATHER_BULK if args.gather == "bulk" else K.KVO_GATHER_LDG)
+    seq = Sequence(kv, inp, wl)
+    stream = torch.cuda.current_stream(device)
+
+    # warm-up (the first step of the sequence is the cold, all-miss step)
+    for _ in range(args.warmup):
+        seq.step()
+    torch.cuda.synchronize(device)
+    kv.profile_read()
+    kv.set_option(K.KVO_OPT_PROFILE, 1)
+    st0 = kv.stats()
+    sampler = ClockSampler(local)
+    time.sleep(0.3)
+
+    # ---------------- timed region
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps + 1)]
+    positions = []
+    barrier(world)
+    torch.cuda.synchronize(device)
+    t_wall0 = time.time()
+    ev[0].record(stream)
+    for i in range(args.steps):
+        positions.append(seq.step())
+        ev[i + 1].record(stream)
+    torch.cuda.synchronize(device)
+    t_wall1 = time.time()
+    barrier(world)
+    step_ms = [ev[i].elapsed_time(ev[i + 1]) for i in range(args.steps)]
+    total_ms = ev[0].elapsed_time(ev[args.steps])
+    prof = kv.profile_read()
+    kv.set_option(K.KVO_OPT_PROFILE, 0)
+    st1 = kv.stats()
+    # keep the GPU busy a little longer so the clock sampler sees the load
+    t_c0 = time.time()
+    while time.time() - t_c0 < 1.0:
+        seq.step()
+        torch.cuda.synchronize(device)
+    sampler.stop()
+    clocks = sampler.summary(t_wall0, t_wall1)
+
+    max_ms = reduce_max(total_ms, world, device)
+    value = whole_job_rate(U, args.steps, max_ms, world)
+
+    # ---------------- per-kernel roofline
+    rows_h2d = st1["rows_h2d"] - st0["rows_h2d"]
+    bytes_h2d = st1["bytes_h2d"] - st0["bytes_h2d"]
+    lens = [wl.context + (p + 1) * wl.n_new for p in positions]  # tokens per unit after append
+    score_bytes = sum(256.0 * U * L for L in lens)
+    append_bytes = args.steps * U * wl.n_new * (R * 2 + 256)
+    kernels = {}
+    for name, (ms, n) in prof.items():
+        if n == 0:
+            continue
+        kernels[name] = {"launches": n, "ms_total": round(ms, 4), "ms_per_launch": round(ms / n, 5),
+                         "share": round(ms / max(1e-9, sum(v[0] for v in prof.values())), 4)}
+    if "score" in kernels:
+        a = score_bytes / (prof["score"][0] / 1e3) / 1e9
+        kernels["score"].update(bound="hbm", bytes_per_launch=score_bytes / prof["score"][1],
+                                achieved_gbs=round(a, 1), peak_gbs=hbm_peak,
+                                frac=round(a / hbm_peak, 4), peak_source=hbm_src)
+    if "gather" in kernels and bytes_h2d:
+        a = bytes_h2d / (prof["gather"][0] / 1e3) / 1e9
+        kernels["gather"].update(bound="host-link", bytes_per_launch=bytes_h2d / prof["gather"][1],
+                                 achieved_gbs=round(a, 1), peak_gbs=round(link["h2d"], 1),
+                                 frac=round(a / link["h2d"], 4),
+                                 peak_source="measured pinned host->device copy, this run")
+    if "append" in kernels:
+        a = append_bytes / (prof["append"][0] / 1e3) / 1e9
+        kernels["append"].update(achieved_gbs=round(a, 1))
+    dom = max(kernels, key=lambda n: kernels[n]["ms_total"])
+    d = kernels[dom]
+    roof = {"kernel": dom, "bound": d.get("bound", "latency"),
+            "achieved": d.get("achieved_gbs"), "peak": d.get("peak_gbs"), "unit": "GB/s",
+            "frac": d.get("frac"), "traffic": load_traffic(dom, wl.name),
+            "peak_source": d.get("peak_source")}
+
+    # step roofline: slower of HBM bytes at peak and host-link bytes at measured bandwidth
+    n_steps = args.steps
+    hbm_step = (score_bytes + U * n_steps * (wl.n_new * 256 + 8 * wl.hot_capacity + 16 * P * k)
+                + bytes_h2d) / n_steps
+    host_step = (bytes_h2d + args.steps * U * wl.n_new * R * 2) / n_steps
+    t_roof = max(hbm_step / (hbm_peak * 1e9), host_step / (link["h2d"] * 1e9)) * 1e3
+    t_meas = total_ms / n_steps
+    cold = [m for m, p in zip(step_ms, positions) if p == 0]
+    warm = [m for m, p in zip(step_ms, positions) if p != 0]
+
+    # ---------------- end to end through the public API with host buffers
+    e2e = None
+    if not args.no_e2e:
+        e2e = run_e2e(args, kv, inp, wl, U, device, world, torch)
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        cpu = run_cpu_baseline(wl, args.cpu_units, args.cpu_steps, log)
+
+    launches = sum(v[1] for v in prof.values())
+    line = {
+        "metric": METRIC, "value": round(value, 1), "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(max_ms / args.steps, 4),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+        "data": "synthetic (seeded N(0,1) bf16 keys and rows, random-walk queries)",
+        "config": {"workload": wl.name, "n_requests": wl.n_requests, "n_layers": wl.n_layers,
+                   "context": wl.context, "n_pos": P, "n_new": wl.n_new, "topk": k,
+                   "hot_capacity": wl.hot_capacity, "drift": wl.drift,
+                   "steps_per_sequence": wl.steps, "gather": args.gather,
+                   "parallelism": "replicas%d" % world,
+                   "l2": "inputs larger than L2: %.2f GB of indexer keys read per step"
+                         % (score_bytes / n_steps / 1e9)},
+        "roofline": roof,
+        "miss_fill": {"gbs": kernels.get("gather", {}).get("achieved_gbs"),
+                      "peak_gbs": round(link["h2d"], 1), "rows_per_step": rows_h2d / n_steps,
+                      "frac": kernels.get("gather", {}).get("frac")},
+        "step_roofline": {"hbm_bytes": round(hbm_step), "host_link_bytes": round(host_step),
+                          "t_roofline_ms": round(t_roof, 4), "t_measured_ms": round(t_meas, 4),
+                          "frac": round(t_roof / t_meas, 4)},
+        "steps_ms": {"median": round(statistics.median(step_ms), 4),
+                     "p90": round(sorted(step_ms)[int(0.9 * (len(step_ms) - 1))], 4),
+                     "warm_median": round(statistics.median(warm), 4) if warm else None,
+                     "cold_median": round(statistics.median(cold), 4) if cold else None},
+        "kernels": kernels,
+        "host_link_gbs": {k_: round(v, 1) for k_, v in link.items()},
+        "hits_per_step": (st1["hits"] - st0["hits"]) / n_steps,
+        "misses_per_step": (st1["misses"] - st0["misses"]) / n_steps,
+        "clocks": clocks,
+        "e2e": e2e,
+        "gpu_launches": launches,
+        "cpu_baseline": cpu,
+    }
+    kv.close()
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+def run_e2e(args, kv, inp, wl, U, device, world, torch):
+    """Same steps through the public API with pinned host inputs and outputs."""
+    P, k = wl.n_pos, wl.topk
+    pin = lambda a: torch.from_numpy(a).pin_memory()
+    rows_h, keys_h, q_h = pin(inp["rows_h"]), pin(inp["keys_h"]), pin(inp["q_h"])
+    rows_d = torch.empty_like(inp["rows"][0])
+    keys_d = torch.empty_like(inp["keys"][0])
+    q_d = torch.empty_like(inp["q"][0])
+    out_d = (torch.empty((U, P, k), dtype=torch.int32, device=device),
+             torch.empty((U, P, k), dtype=torch.int32, device=device),
+             torch.empty((U, P, k), dtype=torch.float32, device=device),
+             torch.empty((U, P, k), dtype=torch.int32, device=device),
+             torch.empty(U, dtype=torch.int32, device=device))
+    out_h = [torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for t in out_d]
+    read = (0, 1, 2, 4)  # tokens, slots, scores, status come back every step
+    kv.reset(wl.context)
+    g = 0
+    n = args.steps
+    h2d = (rows_d.numel() + keys_d.numel() + q_d.numel()) * 2
+    d2h = sum(out_d[i].numel() * out_d[i].element_size() for i in read)
+    for warm in (True, False):
+        steps = min(args.warmup, n) if warm else n
+        barrier(world)
+        torch.cuda.synchronize(device)
+        t0 = time.perf_counter()
+        for _ in range(steps):
+            p = g % wl.steps
+            if p == 0 and g > 0:
+                kv.reset(wl.context)
+            rows_d.copy_(rows_h[p], non_blocking=True)
+            keys_d.copy_(keys_h[p], non_blocking=True)
+            q_d.copy_(q_h[p], non_blocking=True)
+            kv.append(rows_d, keys_d)
+            kv.step(q_d, out=out_d)
+            for i in read:
+                out_h[i].copy_(out_d[i], non_blocking=True)
+            torch.cuda.current_stream(device).synchronize()
+            g += 1
+        t1 = time.perf_counter()
+    ms = reduce_max((t1 - t0) * 1e3, world, device)
+    return {"value": round(whole_job_rate(U, n, ms, world), 1), "unit": UNIT,
+            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+            "ms_per_step": round(ms / n, 4)}
+
+
+# --------------------------------------------------------------------------- CPU oracle
+def run_cpu_baseline(wl, n_units, n_steps, log, units_offset=0):
+    """The CPU oracle, as it stands, on a bounded sample of the same workload."""
+    import numpy as np
+    import oracle
+    import workload as W
+
+    units = wl.units_rl()[units_offset:units_offset + n_units]
+    tmax = wl.max_tokens(n_steps)
+    keys = W.token_rows(wl.seed, W.KIND_KEYS, units, 0, tmax, 128)
+    rows = W.token_rows(wl.seed, W.KIND_ROWS, units, 0, tmax, wl.row_elems)
+    q = W.unit_queries(wl.seed, units, wl.drift, n_steps, wl.n_pos)
+    ors = []
+    for i in range(len(units)):
+        o = oracle.OracleUnit(tmax, wl.topk, wl.hot_capacity, wl.n_pos, wl.row_elems, keep_rows=True)
+        o.append(keys[i, :wl.context], rows[i, :wl.context])
+        ors.append(o)
+    timed = 0.0
+    L = wl.context
+    for s in range(n_steps):
+        t0 = time.perf_counter()
+        for i, o in enumerate(ors):
+            o.append(keys[i, L:L + wl.n_new], rows[i, L:L + wl.n_new])
+        oracle.step_many(ors, q[s])
+        dt = time.perf_counter() - t0
+        L += wl.n_new
+        if s > 0:
+            timed += dt
+    n = len(units) * (n_steps - 1)
+    log("cpu oracle: %d unit-steps in %.2f s" % (n, timed))
+    return {"value": round(n / timed, 2), "unit": UNIT, "cores": oracle.threads(), "kind": "oracle",
+            "sample": "%d of %d units (%s), %d warm steps after one cold step, context %d"
+                      % (len(units), wl.n_units, wl.name, n_steps - 1, wl.context)}
+
+
+def run_reference(args, log):
+    """Reference arm: the CPU oracle timed on this machine's host cores."""
+    world, rank, _ = dist_env()
+    if rank != 0:
+        return
+    import numpy as np
+    import oracle
+    import workload as W
+
+    wl = make_workload(args)
+    # size the per-step sample so that the whole run ends within a few minutes
+    probe = run_cpu_baseline(wl, min(16, wl.n_units), 2, log)
+    per_unit_s = 1.0 / probe["value"]
+    budget_s = 90.0
+    n_units = int(max(1, min(wl.n_units, budget_s / max(1, args.steps + args.warmup) / per_unit_s)))
+    units = wl.units_rl()[:n_units]
+    S = wl.steps
+    tmax = wl.max_tokens(S)
+    keys = W.token_rows(wl.seed, W.KIND_KEYS, units, 0, tmax, 128)
+    rows = W.token_rows(wl.seed, W.KIND_ROWS, units, 0, tmax, wl.row_elems)
+    q = W.unit_queries(wl.seed, units, wl.drift, S, wl.n_pos)
+
+    def fresh():
+        ors = []
+        for i in range(n_units):
+            o = oracle.OracleUnit(tmax, wl.topk, wl.hot_capacity, wl.n_pos, wl.row_elems, True)
+            o.append(keys[i, :wl.context], rows[i, :wl.context])
+            ors.append(o)
+        return ors
+
+    ors = fresh()
+    g = 0
+    timed = 0.0
+    for i in range(args.warmup + args.steps):
+        p = g % S
+        if p == 0 and g > 0:
+            ors = fresh()  # the sequence starts again from the prefill (untimed)
+        L = wl.context + p * wl.n_new
+        t0 = time.perf_counter()
+        for j, o in enumerate(ors):
+            o.append(keys[j, L:L + wl.n_new], rows[j, L:L + wl.n_new])
+        oracle.step_many(ors, q[p])
+        dt = time.perf_counter() - t0
+        if i >= args.warmup:
+            timed += dt
+        g += 1
+    value = n_units * args.steps / timed
+    line = {
+        "impl": "reference", "metric": METRIC, "value": round(value, 2), "unit": UNIT,
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(timed * 1e3 / args.steps, 3), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+        "data": "synthetic (seeded N(0,1) bf16 keys and rows, random-walk queries)",
+        "config": {"workload": wl.name, "n_requests": wl.n_requests, "n_layers": wl.n_layers,
+                   "context": wl.context, "n_pos": wl.n_pos, "n_new": wl.n_new,
+                   "topk": wl.topk, "hot_capacity": wl.hot_capacity, "drift": wl.drift,
+                   "steps_per_sequence": S, "parallelism": "replicas%d" % world},
+        "cpu_baseline": {"value": round(value, 2), "unit": UNIT, "cores": oracle.threads(),
+                         "kind": "oracle",
+                         "sample": "%d of %d units per step (%s), context %d"
+                                   % (n_units, wl.n_units, wl.name, wl.context)},
+        "e2e": {"value": round(value, 2), "unit": UNIT, "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2495)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=("kvo", "reference"), default="kvo")
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
+    ap.add_argument("--requests", type=int, default=0)
+    ap.add_argument("--layers", type=int, default=0)
+    ap.add_argument("--context", type=int, default=0)
+    ap.add_argument("--gather", choices=("ldg", "bulk"), default="ldg")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-units", type=int, default=32)
+    ap.add_argument("--cpu-steps", type=int, default=4)
+    ap.add_argument("--quiet", action="store_true")
+    args = ap.parse_args(argv)
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    log = (lambda *a: None) if args.quiet else (lambda m: print("[bench] " + m, file=sys.stderr, flush=True))
+    if args.impl == "reference":
+        run_reference(args, log)
+    else:
+        import __graft_entry__
+        __graft_entry__.build()
+        run_kvo(args, log)
+
+
+if __name__ == "__main__":
+    main()

@@ -102,6 +102,7 @@ typedef struct kvo_stats {
 /* Options for kvo_set_option. */
 #define KVO_OPT_GATHER_MODE 1 /* value: KVO_GATHER_LDG (default) | KVO_GATHER_BULK */
 #define KVO_OPT_WAIT_LIMIT_NS 2 /* bound of every device-side wait, ns (default 2e9) */
+#define KVO_OPT_PROFILE 3       /* 1: bracket every launch with CUDA events (kvo_profile_read) */
 #define KVO_GATHER_LDG 0  /* miss rows read by 16-byte loads from the mapped host pool */
 #define KVO_GATHER_BULK 1 /* miss rows moved by bulk async copies through shared memory */
 
@@ -190,6 +191,34 @@ int kvo_select(const void* keys, int64_t unit_stride, const int32_t* cache_slots
                const int64_t* lengths, int32_t n_units, int32_t n_pos, int32_t k,
                const void* queries, int32_t* tokens, float* scores, int32_t* payload,
                void* workspace, size_t workspace_bytes, void* stream);
+
+/*
+ * kvo_reset: return every listed unit to its first keep_tokens cached tokens
+ * with an empty hot shelf (cache_slots and slot_token -1, last_use and stamp
+ * 0), as when a finished request's unit is reused for a new request whose
+ * prefilled context is already in place.  keep_tokens must not exceed any
+ * listed unit's length.  Asynchronous on stream.  Errors: KVO_EINVAL,
+ * KVO_ERANGE.
+ */
+int kvo_reset(kvo_handle* h, const int32_t* units, int32_t n_units, int64_t keep_tokens,
+              void* stream);
+
+/*
+ * Per-kernel device time, recorded when KVO_OPT_PROFILE is 1: CUDA events on
+ * the launching stream bracket every kernel the library launches.
+ * kvo_profile_read synchronises those events, adds their durations into
+ * ms[kind] and the launch counts into launches[kind] for kind <
+ * min(n_kinds, KVO_PROF_KINDS), and forgets them.
+ */
+#define KVO_PROF_APPEND 0
+#define KVO_PROF_PLAN 1
+#define KVO_PROF_SCORE 2
+#define KVO_PROF_SELECT 3
+#define KVO_PROF_RESIDENCY 4
+#define KVO_PROF_GATHER 5
+#define KVO_PROF_RESET 6
+#define KVO_PROF_KINDS 7
+int kvo_profile_read(kvo_handle* h, double* ms, uint64_t* launches, int32_t n_kinds);
 
 /* kvo_set_option: KVO_OPT_* above.  KVO_EINVAL on unknown key or value. */
 int kvo_set_option(kvo_handle* h, int32_t key, int64_t value);

@@ -51,6 +51,14 @@ struct kvo_handle {
   uint64_t host_steps = 0;
   int gather_mode = KVO_GATHER_LDG;
   uint64_t wait_ns = 2000000000ull;
+  // opt-in launch profiling
+  bool profile = false;
+  struct Rec {
+    int kind;
+    cudaEvent_t e0, e1;
+  };
+  std::vector<Rec> recs;
+  std::vector<cudaEvent_t> free_events;
 };
 
 namespace {
@@ -86,6 +94,13 @@ cudaError_t dalloc(T** p, size_t count) {
 }
 
 void free_all(kvo_handle* h) {
+  for (auto& r : h->recs) {
+    cudaEventDestroy(r.e0);
+    cudaEventDestroy(r.e1);
+  }
+  for (auto e : h->free_events) cudaEventDestroy(e);
+  h->recs.clear();
+  h->free_events.clear();
   void* dev[] = {h->idx, h->hot, h->cache_slots, h->slot_token, h->last_use, h->stamp, h->len,
                  h->all_units, h->units_dev, h->off, h->seg_keys, h->seg_cnt, h->sel_pay,
                  h->miss_tok, h->miss_slot, h->miss_cnt, h->miss_off, h->done_ctr, h->err,
@@ -130,6 +145,29 @@ int resolve_units(kvo_handle* h, const int32_t* units, int32_t n_units, cudaStre
   }
   *dev_units = h->units_dev;
   return KVO_OK;
+}
+
+cudaEvent_t take_event(kvo_handle* h) {
+  if (!h->free_events.empty()) {
+    cudaEvent_t e = h->free_events.back();
+    h->free_events.pop_back();
+    return e;
+  }
+  cudaEvent_t e = nullptr;
+  if (cudaEventCreate(&e) != cudaSuccess) return nullptr;
+  return e;
+}
+
+// Runs one launch, bracketed by events when profiling is on.
+template <class F>
+cudaError_t timed(kvo_handle* h, int kind, cudaStream_t s, F launch) {
+  if (!h->profile) return launch();
+  cudaEvent_t e0 = take_event(h), e1 = take_event(h);
+  if (e0) cudaEventRecord(e0, s);
+  cudaError_t e = launch();
+  if (e1) cudaEventRecord(e1, s);
+  if (e0 && e1) h->recs.push_back({kind, e0, e1});
+  return e;
 }
 
 int grid_for(int64_t T, int G_max) {
@@ -312,7 +350,7 @@ int kvo_append(kvo_handle* h, const int32_t* units, int32_t n_units, int32_t n_t
   a.idx = h->idx;
   a.len = h->len;
   a.stats = h->stats;
-  cudaError_t e = kvo::launch_append(a, s);
+  cudaError_t e = timed(h, KVO_PROF_APPEND, s, [&] { return kvo::launch_append(a, s); });
   if (e != cudaSuccess) return cuda_fail(e, "append launch");
   for (int32_t i = 0; i < n_units; ++i) h->len_host[(size_t)(units ? units[i] : i)] += n_tokens;
   return KVO_OK;
@@ -355,9 +393,9 @@ int kvo_step(kvo_handle* h, const int32_t* units, int32_t n_units, const void* q
   sa.err = h->err;
   sa.stats = h->stats;
   sa.wait_ns = h->wait_ns;
-  cudaError_t e = kvo::launch_plan(sa, s);
-  if (e == cudaSuccess) e = kvo::launch_score(sa, s);
-  if (e == cudaSuccess) e = kvo::launch_select(sa, s);
+  cudaError_t e = timed(h, KVO_PROF_PLAN, s, [&] { return kvo::launch_plan(sa, s); });
+  if (e == cudaSuccess) e = timed(h, KVO_PROF_SCORE, s, [&] { return kvo::launch_score(sa, s); });
+  if (e == cudaSuccess) e = timed(h, KVO_PROF_SELECT, s, [&] { return kvo::launch_select(sa, s); });
 
   kvo::ResidencyArgs ra{};
   ra.units = du;
@@ -381,7 +419,7 @@ int kvo_step(kvo_handle* h, const int32_t* units, int32_t n_units, const void* q
   ra.done_ctr = h->done_ctr;
   ra.err = h->err;
   ra.stats = h->stats;
-  if (e == cudaSuccess) e = kvo::launch_residency(ra, s);
+  if (e == cudaSuccess) e = timed(h, KVO_PROF_RESIDENCY, s, [&] { return kvo::launch_residency(ra, s); });
 
   kvo::GatherArgs ga{};
   ga.units = du;
@@ -399,7 +437,7 @@ int kvo_step(kvo_handle* h, const int32_t* units, int32_t n_units, const void* q
   ga.stats = h->stats;
   ga.err = h->err;
   ga.wait_ns = h->wait_ns;
-  if (e == cudaSuccess) e = kvo::launch_gather(ga, h->n_sm, s);
+  if (e == cudaSuccess) e = timed(h, KVO_PROF_GATHER, s, [&] { return kvo::launch_gather(ga, h->n_sm, s); });
   if (e != cudaSuccess) return cuda_fail(e, "step launch");
   ++h->host_steps;
   return KVO_OK;
@@ -491,6 +529,10 @@ int kvo_set_option(kvo_handle* h, int32_t key, int64_t value) {
       if (value != KVO_GATHER_LDG && value != KVO_GATHER_BULK) return fail(KVO_EINVAL, "bad gather mode");
       h->gather_mode = (int)value;
       return KVO_OK;
+    case KVO_OPT_PROFILE:
+      if (value != 0 && value != 1) return fail(KVO_EINVAL, "profile is 0 or 1");
+      h->profile = value == 1;
+      return KVO_OK;
     case KVO_OPT_WAIT_LIMIT_NS:
       if (value < 1000) return fail(KVO_EINVAL, "wait limit below 1 us");
       h->wait_ns = (uint64_t)value;
@@ -498,6 +540,55 @@ int kvo_set_option(kvo_handle* h, int32_t key, int64_t value) {
     default:
       return fail(KVO_EINVAL, "unknown option");
   }
+}
+
+int kvo_reset(kvo_handle* h, const int32_t* units, int32_t n_units, int64_t keep_tokens, void* stream) {
+  if (!h) return fail(KVO_EINVAL, "handle is NULL");
+  if (keep_tokens < 0) return fail(KVO_EINVAL, "keep_tokens < 0");
+  DeviceGuard guard(h->device);
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  for (int32_t i = 0; i < n_units; ++i) {
+    const int32_t u = units ? units[i] : i;
+    if (u < 0 || u >= h->U) return fail(KVO_ERANGE, "unit id out of range");
+    if (h->len_host[(size_t)u] < keep_tokens) return fail(KVO_ERANGE, "keep_tokens beyond a unit's length");
+  }
+  const int32_t* du = nullptr;
+  int rc = resolve_units(h, units, n_units, s, &du);
+  if (rc != KVO_OK) return rc;
+  kvo::ResetArgs a{};
+  a.units = du;
+  a.n = n_units;
+  a.keep = (int32_t)keep_tokens;
+  a.stride = h->stride;
+  a.C = h->C;
+  a.cache_slots = h->cache_slots;
+  a.slot_token = h->slot_token;
+  a.last_use = h->last_use;
+  a.stamp = h->stamp;
+  a.len = h->len;
+  cudaError_t e = timed(h, KVO_PROF_RESET, s, [&] { return kvo::launch_reset(a, s); });
+  if (e != cudaSuccess) return cuda_fail(e, "reset launch");
+  for (int32_t i = 0; i < n_units; ++i) h->len_host[(size_t)(units ? units[i] : i)] = keep_tokens;
+  return KVO_OK;
+}
+
+int kvo_profile_read(kvo_handle* h, double* ms, uint64_t* launches, int32_t n_kinds) {
+  if (!h || !ms || !launches || n_kinds < 0) return fail(KVO_EINVAL, "NULL argument");
+  DeviceGuard guard(h->device);
+  for (auto& r : h->recs) {
+    float t = 0.f;
+    cudaError_t e = cudaEventSynchronize(r.e1);
+    if (e == cudaSuccess) e = cudaEventElapsedTime(&t, r.e0, r.e1);
+    if (e != cudaSuccess) return cuda_fail(e, "profile events");
+    if (r.kind < n_kinds && r.kind < KVO_PROF_KINDS) {
+      ms[r.kind] += t;
+      launches[r.kind] += 1;
+    }
+    h->free_events.push_back(r.e0);
+    h->free_events.push_back(r.e1);
+  }
+  h->recs.clear();
+  return KVO_OK;
 }
 
 int kvo_get_stats(kvo_handle* h, kvo_stats* out) {

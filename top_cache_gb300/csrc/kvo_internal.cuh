@@ -215,6 +215,17 @@ struct AppendArgs {
   DevStats* stats;
 };
 
+struct ResetArgs {
+  const int32_t* units;
+  int32_t n, keep, C;
+  int64_t stride;
+  int32_t* cache_slots;
+  int32_t* slot_token;
+  uint32_t* last_use;
+  uint32_t* stamp;
+  int32_t* len;
+};
+
 // Host-side launchers (return cudaError_t of the launch).
 int score_cap_for(int P, int k);
 cudaError_t launch_plan(const SelectArgs& a, cudaStream_t s);
@@ -223,6 +234,7 @@ cudaError_t launch_select(const SelectArgs& a, cudaStream_t s);
 cudaError_t launch_residency(const ResidencyArgs& a, cudaStream_t s);
 cudaError_t launch_gather(const GatherArgs& a, int n_sm, cudaStream_t s);
 cudaError_t launch_append(const AppendArgs& a, cudaStream_t s);
+cudaError_t launch_reset(const ResetArgs& a, cudaStream_t s);
 cudaError_t launch_set_len(int32_t* len, int32_t unit, int32_t value, cudaStream_t s);
 cudaError_t launch_fill_i32(int32_t* p, int32_t v, size_t n, cudaStream_t s);
 

@@ -480,6 +480,23 @@ __global__ void __launch_bounds__(256) append_kernel(AppendArgs a) {
   }
 }
 
+// reset: one CTA per listed unit; residency cleared, length cut back.
+__global__ void __launch_bounds__(256) reset_kernel(ResetArgs a) {
+  const int i = blockIdx.x, u = a.units[i];
+  int32_t* cs = a.cache_slots + (int64_t)u * a.stride;
+  const int32_t len = a.len[u];
+  for (int32_t t = threadIdx.x; t < len; t += blockDim.x) cs[t] = -1;
+  for (int s = threadIdx.x; s < a.C; s += blockDim.x) {
+    a.slot_token[(int64_t)u * a.C + s] = -1;
+    a.last_use[(int64_t)u * a.C + s] = 0;
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    a.stamp[u] = 0;
+    a.len[u] = a.keep;
+  }
+}
+
 __global__ void set_len_kernel(int32_t* len, int32_t unit, int32_t value) { len[unit] = value; }
 
 __global__ void fill_i32_kernel(int32_t* p, int32_t v, size_t n) {
@@ -522,6 +539,11 @@ cudaError_t launch_gather(const GatherArgs& a, int n_sm, cudaStream_t s) {
 
 cudaError_t launch_append(const AppendArgs& a, cudaStream_t s) {
   append_kernel<<<a.n, 256, 0, s>>>(a);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_reset(const ResetArgs& a, cudaStream_t s) {
+  reset_kernel<<<a.n, 256, 0, s>>>(a);
   return cudaGetLastError();
 }
 

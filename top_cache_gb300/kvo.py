@@ -25,12 +25,14 @@ KVO_PAD_PAYLOAD = -(2 ** 31)
 
 KVO_OPT_GATHER_MODE = 1
 KVO_OPT_WAIT_LIMIT_NS = 2
+KVO_OPT_PROFILE = 3
+PROF_KINDS = ("append", "plan", "score", "select", "residency", "gather", "reset")
 KVO_GATHER_LDG = 0
 KVO_GATHER_BULK = 1
 
 EXPORTED = ("kvo_create", "kvo_destroy", "kvo_host_rows", "kvo_prefill", "kvo_append", "kvo_step",
-            "kvo_select_workspace_size", "kvo_select", "kvo_set_option", "kvo_get_stats",
-            "kvo_export_state", "kvo_last_error")
+            "kvo_select_workspace_size", "kvo_select", "kvo_reset", "kvo_profile_read",
+            "kvo_set_option", "kvo_get_stats", "kvo_export_state", "kvo_last_error")
 
 
 class KvoConfig(ctypes.Structure):
@@ -88,6 +90,10 @@ def lib():
             L.kvo_select.restype = ctypes.c_int
             L.kvo_select.argtypes = [vp, i64, vp, vp, i32, i32, i32, vp, vp, vp, vp, vp,
                                      ctypes.c_size_t, vp]
+            L.kvo_reset.restype = ctypes.c_int
+            L.kvo_reset.argtypes = [vp, vp, i32, i64, vp]
+            L.kvo_profile_read.restype = ctypes.c_int
+            L.kvo_profile_read.argtypes = [vp, vp, vp, i32]
             L.kvo_set_option.restype = ctypes.c_int
             L.kvo_set_option.argtypes = [vp, i32, i64]
             L.kvo_get_stats.restype = ctypes.c_int
@@ -185,6 +191,20 @@ def kvo_select(keys, unit_stride, cache_slots, lengths, n_units, n_pos, k, queri
                                    _stream(stream)))
 
 
+def kvo_reset(h, units, n_units, keep_tokens, stream=None):
+    arr, up = _units(units)
+    return _check(lib().kvo_reset(h, up, n_units, keep_tokens, _stream(stream)))
+
+
+def kvo_profile_read(h):
+    """{kind: (ms, launches)} accumulated since the last read (profiling option on)."""
+    n = len(PROF_KINDS)
+    ms = np.zeros(n, np.float64)
+    cnt = np.zeros(n, np.uint64)
+    _check(lib().kvo_profile_read(h, ms.ctypes.data, cnt.ctypes.data, n))
+    return {k: (float(ms[i]), int(cnt[i])) for i, k in enumerate(PROF_KINDS)}
+
+
 def kvo_set_option(h, key, value):
     return _check(lib().kvo_set_option(h, key, value))
 
@@ -259,6 +279,13 @@ class Kvo:
         tok, sl, sc, pay, st = out
         kvo_step(self.h, units, n, queries, tok, sl, sc, pay, st, stream)
         return out
+
+    def reset(self, keep_tokens, units=None, stream=None):
+        n_units = self.U if units is None else len(units)
+        return kvo_reset(self.h, units, n_units, keep_tokens, stream)
+
+    def profile_read(self):
+        return kvo_profile_read(self.h)
 
     def set_option(self, key, value):
         return kvo_set_option(self.h, key, value)
