@@ -285,6 +285,8 @@ def run_kvo(args, log):
     kv, inp, units = prepare(wl, rank, device, log)
     U, P, k, R = len(units), wl.n_pos, wl.topk, wl.row_elems
     kv.set_option(K.KVO_OPT_GATHER_MODE, K.KVO_GATHER_BULK if args.gather == "bulk" else K.KVO_GATHER_LDG)
+    kv.set_option(K.KVO_OPT_GROUPS, args.groups)
+    kv.set_option(K.KVO_OPT_SCORE_CTAS, args.score_ctas)
     seq = Sequence(kv, inp, wl)
     stream = torch.cuda.current_stream(device)
 
@@ -388,7 +390,7 @@ def run_kvo(args, log):
         "config": {"workload": wl.name, "n_requests": wl.n_requests, "n_layers": wl.n_layers,
                    "context": wl.context, "n_pos": P, "n_new": wl.n_new, "topk": k,
                    "hot_capacity": wl.hot_capacity, "drift": wl.drift,
-                   "steps_per_sequence": wl.steps, "gather": args.gather,
+                   "steps_per_sequence": wl.steps, "gather": args.gather, "groups": args.groups,
                    "parallelism": "replicas%d" % world,
                    "l2": "inputs larger than L2: %.2f GB of indexer keys read per step"
                          % (score_bytes / n_steps / 1e9)},
@@ -578,6 +580,9 @@ def main(argv=None):
     ap.add_argument("--layers", type=int, default=0)
     ap.add_argument("--context", type=int, default=0)
     ap.add_argument("--gather", choices=("ldg", "bulk"), default="ldg")
+    ap.add_argument("--groups", type=int, default=1,
+                    help="unit groups per step; miss-row copies overlap the next group's scoring")
+    ap.add_argument("--score-ctas", type=int, default=0, help="cap on scoring CTAs (0 = one per SM)")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-units", type=int, default=32)

@@ -103,6 +103,9 @@ typedef struct kvo_stats {
 #define KVO_OPT_GATHER_MODE 1 /* value: KVO_GATHER_LDG (default) | KVO_GATHER_BULK */
 #define KVO_OPT_WAIT_LIMIT_NS 2 /* bound of every device-side wait, ns (default 2e9) */
 #define KVO_OPT_PROFILE 3       /* 1: bracket every launch with CUDA events (kvo_profile_read) */
+#define KVO_OPT_GROUPS 4        /* 1..16 unit groups per kvo_step: the miss-row copy of group g runs
+                                   on a library stream while group g+1 is scored (default 1) */
+#define KVO_OPT_SCORE_CTAS 5    /* upper bound on scoring CTAs per launch, 0 = one per SM */
 #define KVO_GATHER_LDG 0  /* miss rows read by 16-byte loads from the mapped host pool */
 #define KVO_GATHER_BULK 1 /* miss rows moved by bulk async copies through shared memory */
 

@@ -30,7 +30,8 @@ class Runner:
     """One workload run: GPU handle + oracle replicas of the checked units."""
 
     def __init__(self, wl, check_units=None, distinct=False, rows_for=None, steps=None,
-                 gather_mode=K.KVO_GATHER_LDG, keys_fn=None, queries=None, max_tokens=None):
+                 gather_mode=K.KVO_GATHER_LDG, keys_fn=None, queries=None, max_tokens=None,
+                 options=None):
         self.wl = wl
         self.steps = wl.steps if steps is None else steps
         self.units_rl = wl.units_rl()
@@ -41,6 +42,8 @@ class Runner:
         self.kv = K.Kvo(wl.n_requests, wl.n_layers, self.tmax, wl.topk, wl.hot_capacity,
                         wl.n_pos, wl.row_elems)
         self.kv.set_option(K.KVO_OPT_GATHER_MODE, gather_mode)
+        for key, value in (options or {}).items():
+            self.kv.set_option(key, value)
         self.keys_fn = keys_fn
         # prefill: rows into the pinned pool, keys into the indexer cache
         _fill_host_rows(self.kv, wl, self.units_rl, rows_for, 0, wl.context)

@@ -85,6 +85,21 @@ def test_bulk_gather_mode():
     _run(wl, gather_mode=K.KVO_GATHER_BULK)
 
 
+@pytest.mark.parametrize("groups", [2, 3, 5])
+def test_unit_groups_two_streams(groups):
+    # the miss-row copy of each group overlaps the next group's scoring
+    wl = W.reduced(W.WORKLOADS["batch16x8_32k_mtp3"], n_requests=3, n_layers=2, context=3001,
+                   topk=256, hot_capacity=600, steps=5)
+    _run(wl, options={K.KVO_OPT_GROUPS: groups})
+
+
+def test_few_score_ctas_long_pieces():
+    # a cap on scoring CTAs makes each CTA stream long pieces (many compactions)
+    wl = W.reduced(W.WORKLOADS["batch16x8_32k_mtp3"], n_requests=1, n_layers=3, context=40000,
+                   topk=512, hot_capacity=1024, steps=3)
+    _run(wl, options={K.KVO_OPT_SCORE_CTAS: 2})
+
+
 def test_positions_1_to_8():
     for P in (2, 3, 5, 8):
         wl = W.Workload("p%d" % P, 1, 2, 2500, P, P, 64, 64 * P, 4, 0.5, 77)
@@ -240,6 +255,11 @@ def _meminfo_gb():
 def test_full_batch16x8_mtp3_sampled():
     wl = W.WORKLOADS["batch16x8_32k_mtp3"]
     _run(wl, check_units=[0, 61, 127], count_rows=False)
+
+
+def test_full_batch16x8_mtp3_grouped_sampled():
+    wl = W.WORKLOADS["batch16x8_32k_mtp3"]
+    _run(wl, steps=20, check_units=[0, 40, 127], count_rows=False, options={K.KVO_OPT_GROUPS: 4})
 
 
 def test_full_long_1m_mtp3_sampled():

@@ -38,6 +38,7 @@ struct kvo_handle {
   int32_t* units_dev = nullptr;  // last uploaded explicit list
   std::vector<int32_t> units_cached;
   int64_t* off = nullptr;
+  uint64_t* gthr = nullptr;
   uint64_t* seg_keys = nullptr;
   int32_t* seg_cnt = nullptr;
   int32_t* sel_pay = nullptr;
@@ -51,6 +52,12 @@ struct kvo_handle {
   uint64_t host_steps = 0;
   int gather_mode = KVO_GATHER_LDG;
   uint64_t wait_ns = 2000000000ull;
+  // unit groups: miss-row copies overlap the next group's scoring
+  int groups = 1;
+  int score_ctas = 0;
+  cudaStream_t side = nullptr;
+  cudaEvent_t ev_fork = nullptr, ev_join = nullptr;
+  cudaEvent_t ev_group[16] = {};
   // opt-in launch profiling
   bool profile = false;
   struct Rec {
@@ -101,8 +108,13 @@ void free_all(kvo_handle* h) {
   for (auto e : h->free_events) cudaEventDestroy(e);
   h->recs.clear();
   h->free_events.clear();
+  if (h->side) cudaStreamDestroy(h->side);
+  if (h->ev_fork) cudaEventDestroy(h->ev_fork);
+  if (h->ev_join) cudaEventDestroy(h->ev_join);
+  for (auto& ev : h->ev_group)
+    if (ev) cudaEventDestroy(ev);
   void* dev[] = {h->idx, h->hot, h->cache_slots, h->slot_token, h->last_use, h->stamp, h->len,
-                 h->all_units, h->units_dev, h->off, h->seg_keys, h->seg_cnt, h->sel_pay,
+                 h->all_units, h->units_dev, h->off, h->gthr, h->seg_keys, h->seg_cnt, h->sel_pay,
                  h->miss_tok, h->miss_slot, h->miss_cnt, h->miss_off, h->done_ctr, h->err,
                  h->stats};
   for (void* p : dev)
@@ -245,14 +257,19 @@ int kvo_create(const kvo_config* cfg, kvo_handle** out) {
   if (e == cudaSuccess) e = dalloc(&h->all_units, U);
   if (e == cudaSuccess) e = dalloc(&h->units_dev, U);
   if (e == cudaSuccess) e = dalloc(&h->off, U + 1);
+  if (e == cudaSuccess) e = dalloc(&h->gthr, U * h->P);
   if (e == cudaSuccess) e = dalloc(&h->seg_keys, segs * PK);
   if (e == cudaSuccess) e = dalloc(&h->seg_cnt, segs * h->P);
   if (e == cudaSuccess) e = dalloc(&h->sel_pay, U * PK);
   if (e == cudaSuccess) e = dalloc(&h->miss_tok, U * PK);
   if (e == cudaSuccess) e = dalloc(&h->miss_slot, U * PK);
   if (e == cudaSuccess) e = dalloc(&h->miss_cnt, U);
-  if (e == cudaSuccess) e = dalloc(&h->miss_off, U + 1);
-  if (e == cudaSuccess) e = dalloc(&h->done_ctr, 1);
+  if (e == cudaSuccess) e = dalloc(&h->miss_off, U + 16);
+  if (e == cudaSuccess) e = dalloc(&h->done_ctr, 16);
+  if (e == cudaSuccess) e = cudaStreamCreateWithFlags(&h->side, cudaStreamNonBlocking);
+  if (e == cudaSuccess) e = cudaEventCreateWithFlags(&h->ev_fork, cudaEventDisableTiming);
+  if (e == cudaSuccess) e = cudaEventCreateWithFlags(&h->ev_join, cudaEventDisableTiming);
+  for (int g = 0; g < 16 && e == cudaSuccess; ++g) e = cudaEventCreateWithFlags(&h->ev_group[g], cudaEventDisableTiming);
   if (e == cudaSuccess) e = dalloc(&h->err, 1);
   if (e == cudaSuccess) e = dalloc(&h->stats, 1);
   if (e != cudaSuccess) {
@@ -267,8 +284,8 @@ int kvo_create(const kvo_config* cfg, kvo_handle** out) {
   if (e == cudaSuccess) e = cudaMemset(h->stamp, 0, U * 4);
   if (e == cudaSuccess) e = cudaMemset(h->len, 0, U * 4);
   if (e == cudaSuccess) e = cudaMemset(h->miss_cnt, 0, U * 4);
-  if (e == cudaSuccess) e = cudaMemset(h->miss_off, 0, (U + 1) * 8);
-  if (e == cudaSuccess) e = cudaMemset(h->done_ctr, 0, 4);
+  if (e == cudaSuccess) e = cudaMemset(h->miss_off, 0, (U + 16) * 8);
+  if (e == cudaSuccess) e = cudaMemset(h->done_ctr, 0, 16 * 4);
   if (e == cudaSuccess) e = cudaMemset(h->err, 0, 4);
   if (e == cudaSuccess) e = cudaMemset(h->stats, 0, sizeof(DevStats));
   if (e == cudaSuccess) {
@@ -367,77 +384,104 @@ int kvo_step(kvo_handle* h, const int32_t* units, int32_t n_units, const void* q
   const int32_t* du = nullptr;
   int rc = resolve_units(h, units, n_units, s, &du);
   if (rc != KVO_OK) return rc;
-  int64_t T = 0;
-  for (int32_t i = 0; i < n_units; ++i) T += h->len_host[(size_t)(units ? units[i] : i)];
+  const int PK = h->P * h->k;
+  int NG = h->groups < n_units ? h->groups : n_units;
+  if (NG < 1) NG = 1;
+  const int g_max = h->score_ctas > 0 && h->score_ctas < h->G_max ? h->score_ctas : h->G_max;
+  cudaError_t e = cudaSuccess;
+  if (NG > 1) {
+    e = cudaEventRecord(h->ev_fork, s);
+    if (e == cudaSuccess) e = cudaStreamWaitEvent(h->side, h->ev_fork, 0);
+  }
+  for (int g = 0; g < NG && e == cudaSuccess; ++g) {
+    const int b = (int)((int64_t)n_units * g / NG), en = (int)((int64_t)n_units * (g + 1) / NG);
+    const int ng = en - b;
+    if (ng <= 0) continue;
+    int64_t T = 0;
+    for (int32_t i = b; i < en; ++i) T += h->len_host[(size_t)(units ? units[i] : i)];
+    const size_t ob = (size_t)b * PK;
 
-  kvo::SelectArgs sa{};
-  sa.keys = h->idx;
-  sa.stride = h->stride;
-  sa.units = du;
-  sa.len = h->len;
-  sa.queries = static_cast<const uint16_t*>(queries);
-  sa.cache_slots = h->cache_slots;
-  sa.n = n_units;
-  sa.P = h->P;
-  sa.k = h->k;
-  sa.cap = h->cap;
-  sa.T = T;
-  sa.G = grid_for(T, h->G_max);
-  sa.off = h->off;
-  sa.seg_keys = h->seg_keys;
-  sa.seg_cnt = h->seg_cnt;
-  sa.out_tok = topk_tokens;
-  sa.out_score = topk_scores;
-  sa.out_pay = h->sel_pay;
-  sa.out_pay_user = topk_payload;
-  sa.err = h->err;
-  sa.stats = h->stats;
-  sa.wait_ns = h->wait_ns;
-  cudaError_t e = timed(h, KVO_PROF_PLAN, s, [&] { return kvo::launch_plan(sa, s); });
-  if (e == cudaSuccess) e = timed(h, KVO_PROF_SCORE, s, [&] { return kvo::launch_score(sa, s); });
-  if (e == cudaSuccess) e = timed(h, KVO_PROF_SELECT, s, [&] { return kvo::launch_select(sa, s); });
+    kvo::SelectArgs sa{};
+    sa.keys = h->idx;
+    sa.stride = h->stride;
+    sa.units = du + b;
+    sa.len = h->len;
+    sa.queries = static_cast<const uint16_t*>(queries) + (size_t)b * h->P * kvo::kDim;
+    sa.cache_slots = h->cache_slots;
+    sa.n = ng;
+    sa.P = h->P;
+    sa.k = h->k;
+    sa.cap = h->cap;
+    sa.T = T;
+    sa.G = grid_for(T, g_max);
+    sa.off = h->off;
+    sa.gthr = h->gthr;
+    sa.seg_keys = h->seg_keys;
+    sa.seg_cnt = h->seg_cnt;
+    sa.out_tok = topk_tokens + ob;
+    sa.out_score = topk_scores ? topk_scores + ob : nullptr;
+    sa.out_pay = h->sel_pay + ob;
+    sa.out_pay_user = topk_payload ? topk_payload + ob : nullptr;
+    sa.err = h->err;
+    sa.stats = h->stats;
+    sa.wait_ns = h->wait_ns;
+    e = timed(h, KVO_PROF_PLAN, s, [&] { return kvo::launch_plan(sa, s); });
+    if (e == cudaSuccess) e = timed(h, KVO_PROF_SCORE, s, [&] { return kvo::launch_score(sa, s); });
+    if (e == cudaSuccess) e = timed(h, KVO_PROF_SELECT, s, [&] { return kvo::launch_select(sa, s); });
 
-  kvo::ResidencyArgs ra{};
-  ra.units = du;
-  ra.n = n_units;
-  ra.P = h->P;
-  ra.k = h->k;
-  ra.C = h->C;
-  ra.stride = h->stride;
-  ra.tok = topk_tokens;
-  ra.pay = h->sel_pay;
-  ra.cache_slots = h->cache_slots;
-  ra.slot_token = h->slot_token;
-  ra.last_use = h->last_use;
-  ra.stamp = h->stamp;
-  ra.out_slot = topk_slots;
-  ra.status = unit_status;
-  ra.miss_tok = h->miss_tok;
-  ra.miss_slot = h->miss_slot;
-  ra.miss_cnt = h->miss_cnt;
-  ra.miss_off = h->miss_off;
-  ra.done_ctr = h->done_ctr;
-  ra.err = h->err;
-  ra.stats = h->stats;
-  if (e == cudaSuccess) e = timed(h, KVO_PROF_RESIDENCY, s, [&] { return kvo::launch_residency(ra, s); });
+    kvo::ResidencyArgs ra{};
+    ra.units = du + b;
+    ra.n = ng;
+    ra.P = h->P;
+    ra.k = h->k;
+    ra.C = h->C;
+    ra.stride = h->stride;
+    ra.tok = topk_tokens + ob;
+    ra.pay = h->sel_pay + ob;
+    ra.cache_slots = h->cache_slots;
+    ra.slot_token = h->slot_token;
+    ra.last_use = h->last_use;
+    ra.stamp = h->stamp;
+    ra.out_slot = topk_slots + ob;
+    ra.status = unit_status + b;
+    ra.miss_tok = h->miss_tok + ob;
+    ra.miss_slot = h->miss_slot + ob;
+    ra.miss_cnt = h->miss_cnt + b;
+    ra.miss_off = h->miss_off + b + g;
+    ra.done_ctr = h->done_ctr + g;
+    ra.err = h->err;
+    ra.stats = h->stats;
+    if (e == cudaSuccess) e = timed(h, KVO_PROF_RESIDENCY, s, [&] { return kvo::launch_residency(ra, s); });
 
-  kvo::GatherArgs ga{};
-  ga.units = du;
-  ga.n = n_units;
-  ga.row_elems = h->R;
-  ga.C = h->C;
-  ga.mode = h->gather_mode;
-  ga.stride = h->stride;
-  ga.host_pool = h->host_pool_dev;
-  ga.hot = h->hot;
-  ga.miss_tok = h->miss_tok;
-  ga.miss_slot = h->miss_slot;
-  ga.miss_off = h->miss_off;
-  ga.pk = h->P * h->k;
-  ga.stats = h->stats;
-  ga.err = h->err;
-  ga.wait_ns = h->wait_ns;
-  if (e == cudaSuccess) e = timed(h, KVO_PROF_GATHER, s, [&] { return kvo::launch_gather(ga, h->n_sm, s); });
+    kvo::GatherArgs ga{};
+    ga.units = du + b;
+    ga.n = ng;
+    ga.row_elems = h->R;
+    ga.C = h->C;
+    ga.mode = h->gather_mode;
+    ga.stride = h->stride;
+    ga.host_pool = h->host_pool_dev;
+    ga.hot = h->hot;
+    ga.miss_tok = h->miss_tok + ob;
+    ga.miss_slot = h->miss_slot + ob;
+    ga.miss_off = h->miss_off + b + g;
+    ga.pk = PK;
+    ga.stats = h->stats;
+    ga.err = h->err;
+    ga.wait_ns = h->wait_ns;
+    if (NG > 1) {
+      if (e == cudaSuccess) e = cudaEventRecord(h->ev_group[g], s);
+      if (e == cudaSuccess) e = cudaStreamWaitEvent(h->side, h->ev_group[g], 0);
+      if (e == cudaSuccess)
+        e = timed(h, KVO_PROF_GATHER, h->side, [&] { return kvo::launch_gather(ga, h->n_sm, h->side); });
+    } else if (e == cudaSuccess) {
+      e = timed(h, KVO_PROF_GATHER, s, [&] { return kvo::launch_gather(ga, h->n_sm, s); });
+    }
+  }
+  if (NG > 1 && e == cudaSuccess) {
+    e = cudaEventRecord(h->ev_join, h->side);
+    if (e == cudaSuccess) e = cudaStreamWaitEvent(s, h->ev_join, 0);
+  }
   if (e != cudaSuccess) return cuda_fail(e, "step launch");
   ++h->host_steps;
   return KVO_OK;
@@ -449,7 +493,8 @@ size_t kvo_select_workspace_size(int32_t n_units, int32_t n_pos, int32_t k, int3
   if (cudaDeviceGetAttribute(&n_sm, cudaDevAttrMultiProcessorCount, device) != cudaSuccess) return 0;
   auto up = [](size_t x) { return (x + 255) & ~(size_t)255; };
   const size_t n = (size_t)n_units, PK = (size_t)n_pos * k, segs = (size_t)n_sm + n;
-  return up(n * 4) * 2 + up((n + 1) * 8) + up(segs * PK * 8) + up(segs * n_pos * 4) + up(n * PK * 4) + up(4);
+  return up(n * 4) * 2 + up((n + 1) * 8) + up(n * n_pos * 8) + up(segs * PK * 8) + up(segs * n_pos * 4) +
+         up(n * PK * 4) + up(4);
 }
 
 int kvo_select(const void* keys, int64_t unit_stride, const int32_t* cache_slots,
@@ -483,6 +528,7 @@ int kvo_select(const void* keys, int64_t unit_stride, const int32_t* cache_slots
   int32_t* d_units = reinterpret_cast<int32_t*>(w); w += up(n * 4);
   int32_t* d_len = reinterpret_cast<int32_t*>(w); w += up(n * 4);
   int64_t* d_off = reinterpret_cast<int64_t*>(w); w += up((n + 1) * 8);
+  uint64_t* d_gthr = reinterpret_cast<uint64_t*>(w); w += up(n * n_pos * 8);
   uint64_t* d_seg_keys = reinterpret_cast<uint64_t*>(w); w += up(segs * PK * 8);
   int32_t* d_seg_cnt = reinterpret_cast<int32_t*>(w); w += up(segs * n_pos * 4);
   int32_t* d_pay = reinterpret_cast<int32_t*>(w); w += up(n * PK * 4);
@@ -506,6 +552,7 @@ int kvo_select(const void* keys, int64_t unit_stride, const int32_t* cache_slots
   sa.T = T;
   sa.G = grid_for(T, n_sm);
   sa.off = d_off;
+  sa.gthr = d_gthr;
   sa.seg_keys = d_seg_keys;
   sa.seg_cnt = d_seg_cnt;
   sa.out_tok = tokens;
@@ -532,6 +579,14 @@ int kvo_set_option(kvo_handle* h, int32_t key, int64_t value) {
     case KVO_OPT_PROFILE:
       if (value != 0 && value != 1) return fail(KVO_EINVAL, "profile is 0 or 1");
       h->profile = value == 1;
+      return KVO_OK;
+    case KVO_OPT_GROUPS:
+      if (value < 1 || value > 16) return fail(KVO_EINVAL, "groups must be in [1, 16]");
+      h->groups = (int)value;
+      return KVO_OK;
+    case KVO_OPT_SCORE_CTAS:
+      if (value < 0 || value > 1 << 20) return fail(KVO_EINVAL, "score_ctas out of range");
+      h->score_ctas = (int)value;
       return KVO_OK;
     case KVO_OPT_WAIT_LIMIT_NS:
       if (value < 1000) return fail(KVO_EINVAL, "wait limit below 1 us");

@@ -156,6 +156,7 @@ struct SelectArgs {
   int64_t T;                   // total cached tokens of the listed units
   int32_t G;                   // score CTAs
   int64_t* off;                // [n+1] flat offsets (scratch, written by plan)
+  uint64_t* gthr;              // [n][P] shared lower bounds of each k-th best key (zeroed by plan)
   uint64_t* seg_keys;          // [(G+n)][P][k] candidates per segment
   int32_t* seg_cnt;            // [(G+n)][P]
   int32_t* out_tok;            // [n][P][k]

@@ -33,8 +33,9 @@ constexpr int kStages = 3;
 constexpr int kCW = 16;                     // consumer warps
 constexpr int kCT = kCW * 32;               // consumer threads
 constexpr int kScoreThreads = kCT + 32;     // + one producer warp
-constexpr int kSmemMax = 227 * 1024;
-constexpr int kSmemFixed = kStages * kTileBytes + 2 * kStages * 8 + 8 * 4 + 8 * 8 + 256 * 4 + 8 * 4;
+constexpr int kCheckTiles = 4;            // tiles between candidate-buffer checks
+constexpr int kSmemMax = 222 * 1024;        // leaves room for a co-resident copy CTA
+constexpr int kSmemFixed = kStages * kTileBytes + 2 * kStages * 8 + 8 * 4 + 8 * 8 + 256 * 4 + 8 * 4 + 8;
 constexpr int kSelThreads = 512;
 constexpr int kSelSmemKeys = 8192;          // candidates held in shared memory by select
 constexpr int kMaxK = 4096;
@@ -43,48 +44,46 @@ constexpr int kMaxK = 4096;
 // 16-lane tree reduction of chunk sums.  Lane j (of a half warp) holds chunk
 // j's partial sums for V (token, position) pairs.  Levels pair lanes j and
 // j^8, then j^4, j^2, j^1: exactly the tree c_j += c_{j+w}, w = 8, 4, 2, 1
-// (fp32 addition is commutative, so both lanes of a pair hold the same sum).
-// While more than one value is left per lane, a level also transposes: each
-// lane keeps half of the values and receives the partner's partial of that
-// half, so V values cost V-1 shuffles instead of 4V.
+// (fp32 addition is commutative, so either lane of a pair may add).  While
+// more than one value is left per lane a level also transposes: each lane
+// keeps the lower half of its slots and receives the partner's upper half, so
+// V values cost V-1 shuffles and no selects.  That works because slot i of
+// lane l holds pair (i ^ X_l), X_l = tree_perm<V>(l): partners differ in
+// exactly the bit of X that the level splits on.
 // ---------------------------------------------------------------------------
 template <int CUR, int V>
-__device__ __forceinline__ void tree_level(float (&a)[V], int lane, int m) {
+__device__ __forceinline__ void tree_level(float (&a)[V], int m) {
   if constexpr (CUR > 1) {
-    const bool up = (lane & m) != 0;
 #pragma unroll
-    for (int i = 0; i < CUR / 2; ++i) {
-      const float send = up ? a[i] : a[i + CUR / 2];
-      const float keep = up ? a[i + CUR / 2] : a[i];
-      a[i] = keep + __shfl_xor_sync(kFull, send, m);
-    }
+    for (int i = 0; i < CUR / 2; ++i) a[i] = a[i] + __shfl_xor_sync(kFull, a[i + CUR / 2], m);
   } else {
     a[0] = a[0] + __shfl_xor_sync(kFull, a[0], m);
   }
 }
 
 template <int V>
-__device__ __forceinline__ void tree16(float (&a)[V], int lane) {
-  tree_level<V, V>(a, lane, 8);
-  tree_level<(V >= 2 ? V / 2 : 1), V>(a, lane, 4);
-  tree_level<(V >= 4 ? V / 4 : 1), V>(a, lane, 2);
-  tree_level<(V >= 8 ? V / 8 : 1), V>(a, lane, 1);
+__device__ __forceinline__ void tree16(float (&a)[V]) {
+  tree_level<V, V>(a, 8);
+  tree_level<(V >= 2 ? V / 2 : 1), V>(a, 4);
+  tree_level<(V >= 4 ? V / 4 : 1), V>(a, 2);
+  tree_level<(V >= 8 ? V / 8 : 1), V>(a, 1);
 }
 
-// Index (into the original V values) of the first value a lane holds after
-// tree16, and whether the lane is the one that reports it.
+// X_l: the lane's slot permutation (slot i holds pair i ^ X_l), which is also
+// the pair held in slot 0 after tree16.
 template <int V>
-__device__ __forceinline__ int tree_offset(int lane) {
-  int off = 0, cur = V;
+__device__ __forceinline__ int tree_perm(int lane) {
+  int x = 0, cur = V;
 #pragma unroll
   for (int m = 8; m >= 1; m >>= 1) {
     if (cur > 1) {
-      if (lane & m) off += cur / 2;
+      if (lane & m) x += cur / 2;
       cur /= 2;
     }
   }
-  return off;
+  return x;
 }
+// After tree16 with V < 16 several lanes hold the same sum; one reports it.
 template <int V>
 __device__ __forceinline__ bool tree_owner(int lane) {
   constexpr int dup = V >= 16 ? 0 : (16 / V - 1);
@@ -169,19 +168,43 @@ __device__ __forceinline__ void bitonic_desc(uint64_t* buf, int n, int tid, Sync
 
 __device__ __forceinline__ void consumer_sync() { named_sync(1, kCT); }
 
-// Shrink candidate buffer p to exactly k entries (the k largest keys) and
-// raise its threshold.  All consumer threads call it; cnt[p] > k.
+// Shrink one candidate buffer to at most k keys, all >= floor, that include
+// every key of the buffer which can still be among the unit's k best:
+// floor = max(local threshold, the unit's shared threshold gth), then, if
+// more than k keys reach it, the k-th largest of them.  A threshold found by
+// the radix select is a lower bound of the unit's k-th best (k keys of this
+// piece reach it) and is published to gth.  All consumer threads call it.
 __device__ __forceinline__ void compact_candidates(uint64_t* cand, uint32_t* cnt, uint64_t* thr,
-                                                   uint64_t* scratch, uint32_t* hist, uint32_t* rx,
-                                                   int k, int ctid) {
-  const uint32_t n = *cnt;
-  auto for_each = [&](auto f) {
-    for (uint32_t i = ctid; i < n; i += kCT) f(cand[i]);
-  };
-  const uint64_t t = radix_threshold_desc<kCT>(for_each, (uint32_t)k, hist, rx, ctid, consumer_sync);
-  if (ctid == 0) rx[3] = 0;
-  consumer_sync();
+                                                   uint64_t* gth, uint64_t* fl, uint64_t* scratch,
+                                                   uint32_t* hist, uint32_t* rx, int k, int ctid) {
   const int lane = ctid & 31;
+  if (ctid == 0) {
+    uint64_t f = *thr;
+    const uint64_t g = __ldcg(reinterpret_cast<const unsigned long long*>(gth));
+    *fl = g > f ? g : f;
+    rx[3] = 0;
+    rx[5] = 0;
+  }
+  consumer_sync();
+  const uint64_t floor = *fl;
+  const uint32_t n = *cnt;
+  uint32_t c = 0;
+  for (uint32_t i = ctid; i < n; i += kCT) c += cand[i] >= floor ? 1u : 0u;
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) c += __shfl_xor_sync(kFull, c, o);
+  if (lane == 0 && c) atomicAdd(&rx[5], c);
+  consumer_sync();
+  const uint32_t nge = rx[5];
+  uint64_t t = floor;
+  if (nge > (uint32_t)k) {
+    auto for_each = [&](auto f) {
+      for (uint32_t i = ctid; i < n; i += kCT) {
+        const uint64_t key = cand[i];
+        if (key >= floor) f(key);
+      }
+    };
+    t = radix_threshold_desc<kCT>(for_each, (uint32_t)k, hist, rx, ctid, consumer_sync);
+  }
   for (uint32_t i0 = 0; i0 < n; i0 += kCT) {
     const uint32_t i = i0 + ctid;
     const uint64_t key = i < n ? cand[i] : 0;
@@ -196,10 +219,12 @@ __device__ __forceinline__ void compact_candidates(uint64_t* cand, uint32_t* cnt
     }
   }
   consumer_sync();
-  for (int i = ctid; i < k; i += kCT) cand[i] = scratch[i];
+  const uint32_t kept = rx[3] < (uint32_t)k ? rx[3] : (uint32_t)k;
+  for (uint32_t i = ctid; i < kept; i += kCT) cand[i] = scratch[i];
   if (ctid == 0) {
-    *cnt = (uint32_t)k;
+    *cnt = kept;
     *thr = t;
+    if (nge > (uint32_t)k) atomicMax(reinterpret_cast<unsigned long long*>(gth), (unsigned long long)t);
   }
   consumer_sync();
 }
@@ -282,6 +307,7 @@ __global__ void __launch_bounds__(1024) plan_kernel(SelectArgs a) {
     if (tid == 1023) carry = excl + v;
     __syncthreads();
   }
+  for (int e = tid; e < a.n * a.P; e += 1024) a.gthr[e] = 0;
   if (tid == 0) {
     a.off[a.n] = carry;
     if (carry != a.T) atomicOr(a.err, kErrPlan);
@@ -301,7 +327,8 @@ __global__ void __launch_bounds__(kScoreThreads, 1) score_kernel(SelectArgs a) {
   uint64_t* thr = reinterpret_cast<uint64_t*>(cnt + 8);           // [8]
   uint32_t* hist = reinterpret_cast<uint32_t*>(thr + 8);          // [256]
   uint32_t* rx = hist + 256;                                      // [8]
-  uint64_t* cand = reinterpret_cast<uint64_t*>(rx + 8);           // [P][cap]
+  uint64_t* fl = reinterpret_cast<uint64_t*>(rx + 8);             // [1]
+  uint64_t* cand = fl + 1;                                        // [P][cap]
   uint64_t* scratch = cand + (size_t)a.P * a.cap;                 // [k]
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -345,11 +372,18 @@ __global__ void __launch_bounds__(kScoreThreads, 1) score_kernel(SelectArgs a) {
   // ---------------- consumers ----------------------------------------------
   constexpr int V = 4 * PP;                 // (token, position) pairs per lane
   constexpr int VL = V >= 16 ? V / 16 : 1;  // values left per lane after the tree
+  constexpr int LPP = PP == 1 ? 0 : PP == 2 ? 1 : PP == 4 ? 2 : 3;
   const int ctid = tid;                     // consumers are threads 0..kCT-1
   const int h = lane >> 4, j = lane & 15;
-  const int toff = tree_offset<V>(lane);
+  // slot (tau, p) of this lane scores token row tau ^ tx against position p ^ px
+  const int X = tree_perm<V>(lane);
+  const int tx = X >> LPP, px = X & (PP - 1);
   const bool owner = tree_owner<V>(lane);
   const int P = a.P, k = a.k, cap = a.cap;
+  const uint32_t trigger = (uint32_t)(cap - kCheckTiles * kTile);
+  int rowoff[4];
+#pragma unroll
+  for (int tau = 0; tau < 4; ++tau) rowoff[tau] = (warp * 8 + h * 4 + (tau ^ tx)) * kKeyBytes + j * 16;
 
   PieceIter it;
   it.begin(a.off, a.n, g0, g1);
@@ -357,12 +391,14 @@ __global__ void __launch_bounds__(kScoreThreads, 1) score_kernel(SelectArgs a) {
   uint32_t seq = 0;
   while (it.next(pc)) {
     const int i = pc.i;
-    // this lane's chunk of every query (fp32, exact)
+    uint64_t* gth = a.gthr + (int64_t)i * P;
+    // this lane's chunk of the queries, in slot order (fp32, exact)
     float qf[PP][8];
 #pragma unroll
     for (int p = 0; p < PP; ++p) {
-      if (p < P) {
-        const uint4 v = *reinterpret_cast<const uint4*>(a.queries + ((int64_t)i * P + p) * kDim + j * 8);
+      const int pq = p ^ px;
+      if (pq < P) {
+        const uint4 v = *reinterpret_cast<const uint4*>(a.queries + ((int64_t)i * P + pq) * kDim + j * 8);
         qf[p][0] = bf_lo(v.x); qf[p][1] = bf_hi(v.x);
         qf[p][2] = bf_lo(v.y); qf[p][3] = bf_hi(v.y);
         qf[p][4] = bf_lo(v.z); qf[p][5] = bf_hi(v.z);
@@ -378,7 +414,8 @@ __global__ void __launch_bounds__(kScoreThreads, 1) score_kernel(SelectArgs a) {
     }
     consumer_sync();
 
-    for (int64_t t = pc.t0; t < pc.t1; t += kTile, ++seq) {
+    int ti = 0;
+    for (int64_t t = pc.t0; t < pc.t1; t += kTile, ++seq, ++ti) {
       const int stage = seq % kStages;
       const uint32_t round = seq / kStages;
       if (!mbar_wait(&full[stage], round & 1u, a.wait_ns) && lane == 0) atomicOr(a.err, kErrTimeout);
@@ -388,8 +425,7 @@ __global__ void __launch_bounds__(kScoreThreads, 1) score_kernel(SelectArgs a) {
       float acc[V];
 #pragma unroll
       for (int tau = 0; tau < 4; ++tau) {
-        const int row = warp * 8 + h * 4 + tau;
-        const uint4 kv = *reinterpret_cast<const uint4*>(tile + row * kKeyBytes + j * 16);
+        const uint4 kv = *reinterpret_cast<const uint4*>(tile + rowoff[tau]);
         const float kf[8] = {bf_lo(kv.x), bf_hi(kv.x), bf_lo(kv.y), bf_hi(kv.y),
                              bf_lo(kv.z), bf_hi(kv.z), bf_lo(kv.w), bf_hi(kv.w)};
 #pragma unroll
@@ -402,12 +438,12 @@ __global__ void __launch_bounds__(kScoreThreads, 1) score_kernel(SelectArgs a) {
       }
       __syncwarp();
       if (lane == 0) mbar_arrive(&empty[stage]);
-      tree16<V>(acc, lane);
+      tree16<V>(acc);
 
 #pragma unroll
       for (int r = 0; r < VL; ++r) {
-        const int v = toff + r;
-        const int tau = v / PP, p = v % PP;
+        const int cmb = r ^ X;
+        const int tau = cmb >> LPP, p = cmb & (PP - 1);
         const int row = warp * 8 + h * 4 + tau;
         const int64_t tok = t + row;
         float s = acc[r];
@@ -433,20 +469,30 @@ __global__ void __launch_bounds__(kScoreThreads, 1) score_kernel(SelectArgs a) {
           }
         }
       }
-      consumer_sync();
-      bool need = false;
-      for (int p = 0; p < P; ++p) need |= cnt[p] > (uint32_t)(cap - kTile);
-      if (need) {
-        for (int p = 0; p < P; ++p)
-          if (cnt[p] > (uint32_t)(cap - kTile))
-            compact_candidates(cand + (size_t)p * cap, &cnt[p], &thr[p], scratch, hist, rx, k, ctid);
+      // every kCheckTiles tiles: adopt the unit's shared thresholds and
+      // compact the buffers that could overflow within the next tiles
+      if (t + kTile < pc.t1 && (ti + 1) % kCheckTiles == 0) {
+        consumer_sync();
+        bool need = false;
+        for (int p = 0; p < P; ++p) need |= cnt[p] > trigger;
+        if (ctid < P) {
+          const uint64_t g = __ldcg(reinterpret_cast<const unsigned long long*>(gth + ctid));
+          if (g > thr[ctid]) thr[ctid] = g;
+        }
+        if (need) {
+          for (int p = 0; p < P; ++p)
+            if (cnt[p] > trigger)
+              compact_candidates(cand + (size_t)p * cap, &cnt[p], &thr[p], gth + p, fl, scratch, hist,
+                                 rx, k, ctid);
+        }
       }
     }
 
-    // piece done: at most k candidates per position go out
+    // piece done: at most k candidates per position, all above the shared threshold
+    consumer_sync();
     for (int p = 0; p < P; ++p)
-      if (cnt[p] > (uint32_t)k)
-        compact_candidates(cand + (size_t)p * cap, &cnt[p], &thr[p], scratch, hist, rx, k, ctid);
+      compact_candidates(cand + (size_t)p * cap, &cnt[p], &thr[p], gth + p, fl, scratch, hist, rx, k,
+                         ctid);
     const int64_t seg = (int64_t)c + i;
     for (int p = 0; p < P; ++p) {
       const uint32_t np = cnt[p];
@@ -569,10 +615,10 @@ int score_cap_for(int P, int k) {
   if (avail <= 0) return 0;
   long cap = avail / ((long)P * 8);
   long target = 3L * k;
-  if (target < k + 4L * kTile) target = k + 4L * kTile;
+  if (target < k + 2L * kCheckTiles * kTile) target = k + 2L * kCheckTiles * kTile;
   if (cap > target) cap = target;
   cap &= ~63L;
-  if (cap < (long)k + kTile) return 0;
+  if (cap < (long)k + (long)kCheckTiles * kTile) return 0;
   return (int)cap;
 }
 

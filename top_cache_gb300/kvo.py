@@ -26,6 +26,8 @@ KVO_PAD_PAYLOAD = -(2 ** 31)
 KVO_OPT_GATHER_MODE = 1
 KVO_OPT_WAIT_LIMIT_NS = 2
 KVO_OPT_PROFILE = 3
+KVO_OPT_GROUPS = 4
+KVO_OPT_SCORE_CTAS = 5
 PROF_KINDS = ("append", "plan", "score", "select", "residency", "gather", "reset")
 KVO_GATHER_LDG = 0
 KVO_GATHER_BULK = 1
