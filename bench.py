@@ -409,6 +409,7 @@ def run_kvo(args, log):
         "host_link_gbs": {k_: round(v, 1) for k_, v in link.items()},
         "hits_per_step": (st1["hits"] - st0["hits"]) / n_steps,
         "misses_per_step": (st1["misses"] - st0["misses"]) / n_steps,
+        "rescored_units_per_step": (st1["rescored"] - st0["rescored"]) / n_steps,
         "clocks": clocks,
         "e2e": e2e,
         "gpu_launches": launches,

@@ -97,6 +97,7 @@ typedef struct kvo_stats {
   uint64_t rows_d2h;        /* rows appended device -> host pool (counted by the copy kernel) */
   uint64_t bytes_d2h;
   uint64_t timeouts;        /* bounded device waits that expired */
+  uint64_t rescored;        /* units rescored because a speculative threshold was too high */
 } kvo_stats;
 
 /* Options for kvo_set_option. */
@@ -106,6 +107,10 @@ typedef struct kvo_stats {
 #define KVO_OPT_GROUPS 4        /* 1..16 unit groups per kvo_step: the miss-row copy of group g runs
                                    on a library stream while group g+1 is scored (default 1) */
 #define KVO_OPT_SCORE_CTAS 5    /* upper bound on scoring CTAs per launch, 0 = one per SM */
+#define KVO_OPT_SPECULATE 6     /* 0: off; v in 1..1000: each (unit, position) starts its scan
+                                   with threshold (previous step's k-th score) x (query norm
+                                   ratio) x v/1000, and a unit whose candidates fall short is
+                                   rescored exactly in the same call (default 900) */
 #define KVO_GATHER_LDG 0  /* miss rows read by 16-byte loads from the mapped host pool */
 #define KVO_GATHER_BULK 1 /* miss rows moved by bulk async copies through shared memory */
 
@@ -220,7 +225,9 @@ int kvo_reset(kvo_handle* h, const int32_t* units, int32_t n_units, int64_t keep
 #define KVO_PROF_RESIDENCY 4
 #define KVO_PROF_GATHER 5
 #define KVO_PROF_RESET 6
-#define KVO_PROF_KINDS 7
+#define KVO_PROF_RESCORE 7   /* rescoring pass of units whose speculative threshold was too high */
+#define KVO_PROF_RESELECT 8
+#define KVO_PROF_KINDS 9
 int kvo_profile_read(kvo_handle* h, double* ms, uint64_t* launches, int32_t n_kinds);
 
 /* kvo_set_option: KVO_OPT_* above.  KVO_EINVAL on unknown key or value. */

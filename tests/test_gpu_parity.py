@@ -85,6 +85,25 @@ def test_bulk_gather_mode():
     _run(wl, gather_mode=K.KVO_GATHER_BULK)
 
 
+@pytest.mark.parametrize("spec", [0, 500, 900])
+def test_speculation_settings_agree(spec):
+    # 0: every scan starts from an empty threshold; otherwise from the last
+    # step's k-th score scaled by spec/1000
+    wl = W.reduced(W.WORKLOADS["batch16x8_32k_mtp3"], n_requests=2, n_layers=2, context=5000,
+                   topk=256, hot_capacity=600, steps=6)
+    _run(wl, options={K.KVO_OPT_SPECULATE: spec})
+
+
+@pytest.mark.parametrize("drift", [0.0, 0.9])
+def test_speculation_without_margin_falls_back_exactly(drift):
+    # no margin and fresh queries: the previous k-th score is often too high;
+    # those units must be rescored and the results must stay exact
+    wl = W.Workload("nomargin", 3, 2, 4000, 4, 4, 200, 900, 8, drift, 84)
+    st, _ = _run(wl, distinct=True, options={K.KVO_OPT_SPECULATE: 1000})
+    if drift == 0.0:
+        assert st["rescored"] > 0
+
+
 @pytest.mark.parametrize("groups", [2, 3, 5])
 def test_unit_groups_two_streams(groups):
     # the miss-row copy of each group overlaps the next group's scoring

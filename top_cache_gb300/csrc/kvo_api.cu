@@ -39,6 +39,13 @@ struct kvo_handle {
   std::vector<int32_t> units_cached;
   int64_t* off = nullptr;
   uint64_t* gthr = nullptr;
+  uint64_t* spec = nullptr;     // [U][P] persistent: k-th best key of each unit's last step
+  float* qn_prev = nullptr;     // [U][P] persistent: that step's squared query norms
+  float* qn_cur = nullptr;      // [U][P] scratch
+  uint64_t* tspec = nullptr;    // [U][P] scratch
+  int32_t* fb = nullptr;        // [U] scratch
+  uint32_t* fb_any = nullptr;   // scratch
+  int speculate = 900;          // permille, 0 = off
   uint64_t* seg_keys = nullptr;
   int32_t* seg_cnt = nullptr;
   int32_t* sel_pay = nullptr;
@@ -114,7 +121,8 @@ void free_all(kvo_handle* h) {
   for (auto& ev : h->ev_group)
     if (ev) cudaEventDestroy(ev);
   void* dev[] = {h->idx, h->hot, h->cache_slots, h->slot_token, h->last_use, h->stamp, h->len,
-                 h->all_units, h->units_dev, h->off, h->gthr, h->seg_keys, h->seg_cnt, h->sel_pay,
+                 h->all_units, h->units_dev, h->off, h->gthr, h->spec, h->qn_prev, h->qn_cur,
+                 h->tspec, h->fb, h->fb_any, h->seg_keys, h->seg_cnt, h->sel_pay,
                  h->miss_tok, h->miss_slot, h->miss_cnt, h->miss_off, h->done_ctr, h->err,
                  h->stats};
   for (void* p : dev)
@@ -258,6 +266,12 @@ int kvo_create(const kvo_config* cfg, kvo_handle** out) {
   if (e == cudaSuccess) e = dalloc(&h->units_dev, U);
   if (e == cudaSuccess) e = dalloc(&h->off, U + 1);
   if (e == cudaSuccess) e = dalloc(&h->gthr, U * h->P);
+  if (e == cudaSuccess) e = dalloc(&h->spec, U * h->P);
+  if (e == cudaSuccess) e = dalloc(&h->qn_prev, U * h->P);
+  if (e == cudaSuccess) e = dalloc(&h->qn_cur, U * h->P);
+  if (e == cudaSuccess) e = dalloc(&h->tspec, U * h->P);
+  if (e == cudaSuccess) e = dalloc(&h->fb, U);
+  if (e == cudaSuccess) e = dalloc(&h->fb_any, 1);
   if (e == cudaSuccess) e = dalloc(&h->seg_keys, segs * PK);
   if (e == cudaSuccess) e = dalloc(&h->seg_cnt, segs * h->P);
   if (e == cudaSuccess) e = dalloc(&h->sel_pay, U * PK);
@@ -282,6 +296,10 @@ int kvo_create(const kvo_config* cfg, kvo_handle** out) {
   if (e == cudaSuccess) e = kvo::launch_fill_i32(h->slot_token, -1, U * C, 0);
   if (e == cudaSuccess) e = cudaMemset(h->last_use, 0, U * C * 4);
   if (e == cudaSuccess) e = cudaMemset(h->stamp, 0, U * 4);
+  if (e == cudaSuccess) e = cudaMemset(h->spec, 0, U * h->P * 8);
+  if (e == cudaSuccess) e = cudaMemset(h->qn_prev, 0, U * h->P * 4);
+  if (e == cudaSuccess) e = cudaMemset(h->fb, 0, U * 4);
+  if (e == cudaSuccess) e = cudaMemset(h->fb_any, 0, 4);
   if (e == cudaSuccess) e = cudaMemset(h->len, 0, U * 4);
   if (e == cudaSuccess) e = cudaMemset(h->miss_cnt, 0, U * 4);
   if (e == cudaSuccess) e = cudaMemset(h->miss_off, 0, (U + 16) * 8);
@@ -425,9 +443,25 @@ int kvo_step(kvo_handle* h, const int32_t* units, int32_t n_units, const void* q
     sa.err = h->err;
     sa.stats = h->stats;
     sa.wait_ns = h->wait_ns;
+    const bool spec_on = h->speculate > 0;
+    sa.spec = h->spec;
+    sa.qn_prev = h->qn_prev;
+    sa.qn_cur = h->qn_cur + (size_t)b * h->P;
+    sa.tspec = h->tspec + (size_t)b * h->P;
+    sa.fb = h->fb + b;
+    sa.fb_any = h->fb_any;
+    sa.spec_scale = spec_on ? (float)h->speculate / 1000.f : 0.f;
+    sa.fallback = 0;
     e = timed(h, KVO_PROF_PLAN, s, [&] { return kvo::launch_plan(sa, s); });
     if (e == cudaSuccess) e = timed(h, KVO_PROF_SCORE, s, [&] { return kvo::launch_score(sa, s); });
     if (e == cudaSuccess) e = timed(h, KVO_PROF_SELECT, s, [&] { return kvo::launch_select(sa, s); });
+    if (spec_on) {
+      // units whose speculative threshold was too high are rescored exactly
+      kvo::SelectArgs fa = sa;
+      fa.fallback = 1;
+      if (e == cudaSuccess) e = timed(h, KVO_PROF_RESCORE, s, [&] { return kvo::launch_score(fa, s); });
+      if (e == cudaSuccess) e = timed(h, KVO_PROF_RESELECT, s, [&] { return kvo::launch_select(fa, s); });
+    }
 
     kvo::ResidencyArgs ra{};
     ra.units = du + b;
@@ -588,6 +622,10 @@ int kvo_set_option(kvo_handle* h, int32_t key, int64_t value) {
       if (value < 0 || value > 1 << 20) return fail(KVO_EINVAL, "score_ctas out of range");
       h->score_ctas = (int)value;
       return KVO_OK;
+    case KVO_OPT_SPECULATE:
+      if (value < 0 || value > 1000) return fail(KVO_EINVAL, "speculate must be in [0, 1000]");
+      h->speculate = (int)value;
+      return KVO_OK;
     case KVO_OPT_WAIT_LIMIT_NS:
       if (value < 1000) return fail(KVO_EINVAL, "wait limit below 1 us");
       h->wait_ns = (uint64_t)value;
@@ -621,6 +659,9 @@ int kvo_reset(kvo_handle* h, const int32_t* units, int32_t n_units, int64_t keep
   a.last_use = h->last_use;
   a.stamp = h->stamp;
   a.len = h->len;
+  a.P = h->P;
+  a.spec = h->spec;
+  a.qn_prev = h->qn_prev;
   cudaError_t e = timed(h, KVO_PROF_RESET, s, [&] { return kvo::launch_reset(a, s); });
   if (e != cudaSuccess) return cuda_fail(e, "reset launch");
   for (int32_t i = 0; i < n_units; ++i) h->len_host[(size_t)(units ? units[i] : i)] = keep_tokens;
@@ -665,6 +706,7 @@ int kvo_get_stats(kvo_handle* h, kvo_stats* out) {
   out->rows_d2h = d.rows_d2h;
   out->bytes_d2h = d.bytes_d2h;
   out->timeouts = (err & kvo::kErrTimeout) ? 1 : 0;
+  out->rescored = d.rescored;
   return KVO_OK;
 }
 

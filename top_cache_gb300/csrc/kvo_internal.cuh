@@ -19,7 +19,7 @@ constexpr uint32_t kErrPlan = 2u;
 // Device-side counters (mirrors kvo_stats).
 struct DevStats {
   unsigned long long steps, unit_steps, capacity_errors, hits, misses, rows_h2d, bytes_h2d,
-      rows_d2h, bytes_d2h, timeouts;
+      rows_d2h, bytes_d2h, timeouts, rescored;
 };
 
 // ---------------------------------------------------------------------------
@@ -166,6 +166,18 @@ struct SelectArgs {
   uint32_t* err;               // sticky error word
   DevStats* stats;             // nullable
   uint64_t wait_ns;
+  // Speculative thresholds (all nullable: off).  spec[u][p] is the k-th best
+  // key of unit u's last step and qn_prev[u][p] that step's squared query
+  // norm; plan turns them into tspec[i][p] for this step, select verifies the
+  // result is exact and flags units to rescore (fb, fb_any) otherwise.
+  uint64_t* spec;
+  float* qn_prev;
+  float* qn_cur;
+  uint64_t* tspec;
+  int32_t* fb;
+  uint32_t* fb_any;
+  float spec_scale;            // threshold = previous k-th score * norm ratio * spec_scale
+  int32_t fallback;            // 1: rescoring pass over the flagged units, no speculation
 };
 
 struct ResidencyArgs {
@@ -218,7 +230,9 @@ struct AppendArgs {
 
 struct ResetArgs {
   const int32_t* units;
-  int32_t n, keep, C;
+  int32_t n, keep, C, P;
+  uint64_t* spec;              // [U][P] cleared
+  float* qn_prev;              // [U][P] cleared
   int64_t stride;
   int32_t* cache_slots;
   int32_t* slot_token;

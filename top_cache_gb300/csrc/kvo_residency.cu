@@ -490,6 +490,10 @@ __global__ void __launch_bounds__(256) reset_kernel(ResetArgs a) {
     a.slot_token[(int64_t)u * a.C + s] = -1;
     a.last_use[(int64_t)u * a.C + s] = 0;
   }
+  for (int p = threadIdx.x; p < a.P; p += blockDim.x) {
+    a.spec[(int64_t)u * a.P + p] = 0;
+    a.qn_prev[(int64_t)u * a.P + p] = 0.f;
+  }
   __syncthreads();
   if (threadIdx.x == 0) {
     a.stamp[u] = 0;

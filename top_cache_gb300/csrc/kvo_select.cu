@@ -33,9 +33,9 @@ constexpr int kStages = 3;
 constexpr int kCW = 16;                     // consumer warps
 constexpr int kCT = kCW * 32;               // consumer threads
 constexpr int kScoreThreads = kCT + 32;     // + one producer warp
-constexpr int kCheckTiles = 4;            // tiles between candidate-buffer checks
+constexpr int kCheckTiles = 8;            // tiles between candidate-buffer checks
 constexpr int kSmemMax = 222 * 1024;        // leaves room for a co-resident copy CTA
-constexpr int kSmemFixed = kStages * kTileBytes + 2 * kStages * 8 + 8 * 4 + 8 * 8 + 256 * 4 + 8 * 4 + 8;
+constexpr int kSmemFixed = kStages * kTileBytes + 2 * kStages * 8 + 8 * 4 + 8 * 8 + 256 * 4 + 10 * 4 + 8;
 constexpr int kSelThreads = 512;
 constexpr int kSelSmemKeys = 8192;          // candidates held in shared memory by select
 constexpr int kMaxK = 4096;
@@ -127,8 +127,37 @@ template <int NT, class ForEach, class Sync>
 __device__ __forceinline__ uint64_t radix_threshold_desc(ForEach for_each, uint32_t need,
                                                          uint32_t* hist, uint32_t* rx, int tid,
                                                          Sync sync) {
-  uint64_t prefix = 0, mask = 0;
-  for (int shift = 56; shift >= 0; shift -= 8) {
+  // the bytes every key shares need no histogram pass
+  unsigned long long* mm = reinterpret_cast<unsigned long long*>(rx + 4);  // rx[4..7]: min, max
+  if (tid == 0) {
+    mm[0] = ~0ull;
+    mm[1] = 0ull;
+  }
+  sync();
+  unsigned long long lo = ~0ull, hi = 0ull;
+  for_each([&](uint64_t key) {
+    lo = key < lo ? key : lo;
+    hi = key > hi ? key : hi;
+  });
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    const unsigned long long l2 = __shfl_xor_sync(kFull, lo, o), h2 = __shfl_xor_sync(kFull, hi, o);
+    lo = l2 < lo ? l2 : lo;
+    hi = h2 > hi ? h2 : hi;
+  }
+  if ((tid & 31) == 0) {
+    atomicMin(&mm[0], lo);
+    atomicMax(&mm[1], hi);
+  }
+  sync();
+  const unsigned long long kmin = mm[0], kmax = mm[1];
+  sync();
+  const int common = kmin == kmax ? 64 : __clzll((long long)(kmin ^ kmax));
+  const int top = 56 - 8 * (common / 8);  // first byte that differs
+  if (top < 0) return kmin;               // all keys equal (cannot happen: keys are unique)
+  const uint64_t cmask = top >= 56 ? 0ull : ~((1ull << (top + 8)) - 1);
+  uint64_t prefix = kmin & cmask, mask = cmask;
+  for (int shift = top; shift >= 0; shift -= 8) {
     for (int b = tid; b < 256; b += NT) hist[b] = 0;
     sync();
     for_each([&](uint64_t key) {
@@ -183,7 +212,7 @@ __device__ __forceinline__ void compact_candidates(uint64_t* cand, uint32_t* cnt
     const uint64_t g = __ldcg(reinterpret_cast<const unsigned long long*>(gth));
     *fl = g > f ? g : f;
     rx[3] = 0;
-    rx[5] = 0;
+    rx[8] = 0;
   }
   consumer_sync();
   const uint64_t floor = *fl;
@@ -192,9 +221,9 @@ __device__ __forceinline__ void compact_candidates(uint64_t* cand, uint32_t* cnt
   for (uint32_t i = ctid; i < n; i += kCT) c += cand[i] >= floor ? 1u : 0u;
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) c += __shfl_xor_sync(kFull, c, o);
-  if (lane == 0 && c) atomicAdd(&rx[5], c);
+  if (lane == 0 && c) atomicAdd(&rx[8], c);
   consumer_sync();
-  const uint32_t nge = rx[5];
+  const uint32_t nge = rx[8];
   uint64_t t = floor;
   if (nge > (uint32_t)k) {
     auto for_each = [&](auto f) {
@@ -238,11 +267,13 @@ struct Piece {
 // The pieces of CTA c's flat range, in order.  Returns false when done.
 struct PieceIter {
   const int64_t* off;
+  const int32_t* only;  // if set, pieces of units with only[i] == 0 are skipped
   int n;
   int64_t g0, g1;
   int i;
-  __device__ void begin(const int64_t* o, int n_, int64_t a, int64_t b) {
+  __device__ void begin(const int64_t* o, int n_, int64_t a, int64_t b, const int32_t* only_ = nullptr) {
     off = o;
+    only = only_;
     n = n_;
     g0 = a;
     g1 = b;
@@ -257,7 +288,7 @@ struct PieceIter {
       }
       const int cur = i++;
       const int64_t a = s > g0 ? s : g0, b = e < g1 ? e : g1;
-      if (a < b) {
+      if (a < b && (!only || only[cur] != 0)) {
         pc.i = cur;
         pc.t0 = a - s;
         pc.t1 = b - s;
@@ -307,7 +338,39 @@ __global__ void __launch_bounds__(1024) plan_kernel(SelectArgs a) {
     if (tid == 1023) carry = excl + v;
     __syncthreads();
   }
-  for (int e = tid; e < a.n * a.P; e += 1024) a.gthr[e] = 0;
+  for (int e = tid; e < a.n * a.P; e += 1024) {
+    a.gthr[e] = 0;
+    if (!a.tspec) continue;
+    const int i = e / a.P, p = e - (e / a.P) * a.P;
+    const int u = a.units[i];
+    // squared query norm (fp32; only steers the speculative threshold)
+    const uint4* q = reinterpret_cast<const uint4*>(a.queries + (int64_t)e * kDim);
+    float s2 = 0.f;
+#pragma unroll 4
+    for (int c = 0; c < kDim / 8; ++c) {
+      const uint4 v = q[c];
+      const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+      for (int x = 0; x < 4; ++x) s2 += bf_lo(w[x]) * bf_lo(w[x]) + bf_hi(w[x]) * bf_hi(w[x]);
+    }
+    if (a.qn_cur) a.qn_cur[e] = s2;
+    uint64_t t = 0;
+    if (a.spec && a.qn_prev && a.spec_scale > 0.f) {
+      const uint64_t kth = a.spec[(int64_t)u * a.P + p];
+      const float sk = key_score(kth);
+      const float prev = a.qn_prev[(int64_t)u * a.P + p];
+      const int64_t vis = (int64_t)a.len[u] - (a.P - 1 - p);
+      if (kth != 0 && sk > 0.f && prev > 0.f && s2 > 0.f && vis > a.k) {
+        const float ts = sk * sqrtf(s2 / prev) * a.spec_scale;
+        if (ts > 0.f) t = (uint64_t)order_bits(ts) << 32;
+      }
+    }
+    a.tspec[e] = t;
+  }
+  if (a.fb) {
+    for (int i = tid; i < a.n; i += 1024) a.fb[i] = 0;
+    if (tid == 0) *a.fb_any = 0;
+  }
   if (tid == 0) {
     a.off[a.n] = carry;
     if (carry != a.T) atomicOr(a.err, kErrPlan);
@@ -326,14 +389,16 @@ __global__ void __launch_bounds__(kScoreThreads, 1) score_kernel(SelectArgs a) {
   uint32_t* cnt = reinterpret_cast<uint32_t*>(empty + kStages);  // [8]
   uint64_t* thr = reinterpret_cast<uint64_t*>(cnt + 8);           // [8]
   uint32_t* hist = reinterpret_cast<uint32_t*>(thr + 8);          // [256]
-  uint32_t* rx = hist + 256;                                      // [8]
-  uint64_t* fl = reinterpret_cast<uint64_t*>(rx + 8);             // [1]
+  uint32_t* rx = hist + 256;                                      // [10]
+  uint64_t* fl = reinterpret_cast<uint64_t*>(rx + 10);            // [1]
   uint64_t* cand = fl + 1;                                        // [P][cap]
   uint64_t* scratch = cand + (size_t)a.P * a.cap;                 // [k]
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int c = blockIdx.x;
+  if (a.fallback && *reinterpret_cast<volatile uint32_t*>(a.fb_any) == 0) return;
   const int64_t g0 = cta_start(c, a.T, a.G), g1 = cta_start(c + 1, a.T, a.G);
+  const int32_t* only = a.fallback ? a.fb : nullptr;  // rescoring pass: flagged units only
   if (tid == 0) {
     for (int s = 0; s < kStages; ++s) {
       mbar_init(&full[s], 1);
@@ -348,7 +413,7 @@ __global__ void __launch_bounds__(kScoreThreads, 1) score_kernel(SelectArgs a) {
     // ---------------- producer: stream every tile of every piece ----------
     if (lane == 0) {
       PieceIter it;
-      it.begin(a.off, a.n, g0, g1);
+      it.begin(a.off, a.n, g0, g1, only);
       Piece pc;
       uint32_t seq = 0;
       while (it.next(pc)) {
@@ -373,6 +438,7 @@ __global__ void __launch_bounds__(kScoreThreads, 1) score_kernel(SelectArgs a) {
   constexpr int V = 4 * PP;                 // (token, position) pairs per lane
   constexpr int VL = V >= 16 ? V / 16 : 1;  // values left per lane after the tree
   constexpr int LPP = PP == 1 ? 0 : PP == 2 ? 1 : PP == 4 ? 2 : 3;
+  constexpr int PH = PP >= 2 ? PP / 2 : 1;  // position pairs (packed fp32x2 FMA)
   const int ctid = tid;                     // consumers are threads 0..kCT-1
   const int h = lane >> 4, j = lane & 15;
   // slot (tau, p) of this lane scores token row tau ^ tx against position p ^ px
@@ -384,15 +450,34 @@ __global__ void __launch_bounds__(kScoreThreads, 1) score_kernel(SelectArgs a) {
   int rowoff[4];
 #pragma unroll
   for (int tau = 0; tau < 4; ++tau) rowoff[tau] = (warp * 8 + h * 4 + (tau ^ tx)) * kKeyBytes + j * 16;
+  // Result r of this lane is (row rrow[r], position rpos[r]).  For insertion,
+  // lane q < P is the leader of position q: lead[r] = lanes reporting
+  // position q; same[r] = lanes reporting this lane's position.
+  int rrow[VL], rpos[VL];
+  uint32_t lead[VL], same[VL];
+#pragma unroll
+  for (int r = 0; r < VL; ++r) {
+    const int cmb = r ^ X;
+    rrow[r] = warp * 8 + h * 4 + (cmb >> LPP);
+    rpos[r] = cmb & (PP - 1);
+    lead[r] = 0;
+    same[r] = 0;
+    for (int q = 0; q < PP; ++q) {
+      const uint32_t m = __ballot_sync(kFull, owner && rpos[r] == q);
+      if (lane == q) lead[r] = m;
+      if (rpos[r] == q) same[r] = m;
+    }
+  }
 
   PieceIter it;
-  it.begin(a.off, a.n, g0, g1);
+  it.begin(a.off, a.n, g0, g1, only);
   Piece pc;
   uint32_t seq = 0;
   while (it.next(pc)) {
     const int i = pc.i;
     uint64_t* gth = a.gthr + (int64_t)i * P;
-    // this lane's chunk of the queries, in slot order (fp32, exact)
+    // this lane's chunk of the queries, in slot order (fp32, exact); with
+    // several positions, slots 2m and 2m+1 are packed for fp32x2 FMAs
     float qf[PP][8];
 #pragma unroll
     for (int p = 0; p < PP; ++p) {
@@ -408,11 +493,18 @@ __global__ void __launch_bounds__(kScoreThreads, 1) score_kernel(SelectArgs a) {
         for (int e = 0; e < 8; ++e) qf[p][e] = 0.f;
       }
     }
+    float2 qp[PH][8];
+#pragma unroll
+    for (int m = 0; m < PH; ++m)
+#pragma unroll
+      for (int e = 0; e < 8; ++e) qp[m][e] = make_float2(qf[2 * m][e], PP >= 2 ? qf[(2 * m + 1) % PP][e] : 0.f);
     if (ctid < P) {
       cnt[ctid] = 0;
-      thr[ctid] = 0;
+      thr[ctid] = (!a.fallback && a.tspec) ? a.tspec[(int64_t)i * P + ctid] : 0ull;
     }
     consumer_sync();
+    // tokens before this index are visible to every position
+    const int64_t all_visible = pc.len - (P - 1);
 
     int ti = 0;
     for (int64_t t = pc.t0; t < pc.t1; t += kTile, ++seq, ++ti) {
@@ -428,44 +520,57 @@ __global__ void __launch_bounds__(kScoreThreads, 1) score_kernel(SelectArgs a) {
         const uint4 kv = *reinterpret_cast<const uint4*>(tile + rowoff[tau]);
         const float kf[8] = {bf_lo(kv.x), bf_hi(kv.x), bf_lo(kv.y), bf_hi(kv.y),
                              bf_lo(kv.z), bf_hi(kv.z), bf_lo(kv.w), bf_hi(kv.w)};
+        if constexpr (PP >= 2) {
+          // positions 2m and 2m+1 at once; each lane of the pair is the
+          // position's own FMA chain in element order
+          float2 s2[PH];
 #pragma unroll
-        for (int p = 0; p < PP; ++p) {
+          for (int m = 0; m < PH; ++m) s2[m] = make_float2(0.f, 0.f);
+#pragma unroll
+          for (int e = 0; e < 8; ++e) {
+            const float2 kk = make_float2(kf[e], kf[e]);
+#pragma unroll
+            for (int m = 0; m < PH; ++m) s2[m] = __ffma2_rn(qp[m][e], kk, s2[m]);
+          }
+#pragma unroll
+          for (int m = 0; m < PH; ++m) {
+            acc[tau * PP + 2 * m] = s2[m].x;
+            acc[tau * PP + 2 * m + 1] = s2[m].y;
+          }
+        } else {
           float s = 0.f;
 #pragma unroll
-          for (int e = 0; e < 8; ++e) s = __fmaf_rn(qf[p][e], kf[e], s);
-          acc[tau * PP + p] = s;
+          for (int e = 0; e < 8; ++e) s = __fmaf_rn(qf[0][e], kf[e], s);
+          acc[tau] = s;
         }
       }
       __syncwarp();
       if (lane == 0) mbar_arrive(&empty[stage]);
       tree16<V>(acc);
 
+      // full tiles whose tokens every position sees need no per-result tests
+      const bool interior = nt == kTile && t + kTile <= all_visible;
 #pragma unroll
       for (int r = 0; r < VL; ++r) {
-        const int cmb = r ^ X;
-        const int tau = cmb >> LPP, p = cmb & (PP - 1);
-        const int row = warp * 8 + h * 4 + tau;
-        const int64_t tok = t + row;
+        const int p = rpos[r];
+        const int64_t tok = t + rrow[r];
         float s = acc[r];
         if (s == 0.f) s = 0.f;  // +0 for a zero score
-        bool pass = false;
-        uint64_t key = 0;
-        if (owner && row < nt && p < P && tok < pc.len - (P - 1 - p)) {
-          key = sel_key(s, (uint32_t)tok);
-          pass = key >= thr[p];
-        }
-        if (__ballot_sync(kFull, pass)) {
-          for (int pp = 0; pp < P; ++pp) {
-            const bool mine = pass && p == pp;
-            const uint32_t m = __ballot_sync(kFull, mine);
-            if (m) {
-              const int leader = __ffs(m) - 1;
-              uint32_t base = 0;
-              if (lane == leader) base = atomicAdd(&cnt[pp], __popc(m));
-              base = __shfl_sync(kFull, base, leader);
-              const uint32_t dst = base + __popc(m & lanemask_lt());
-              if (mine && dst < (uint32_t)cap) cand[(size_t)pp * cap + dst] = key;
-            }
+        const uint64_t key = sel_key(s, (uint32_t)tok);
+        bool ok = owner && p < P;
+        if (!interior) ok = ok && rrow[r] < nt && tok < pc.len - (P - 1 - p);
+        const bool pass = ok && key >= thr[p];
+        const uint32_t mall = __ballot_sync(kFull, pass);
+        if (mall) {
+          uint32_t base = 0;
+          if (lane < P) {
+            const uint32_t n_here = __popc(mall & lead[r]);
+            if (n_here) base = atomicAdd(&cnt[lane], n_here);
+          }
+          base = __shfl_sync(kFull, base, p);
+          if (pass) {
+            const uint32_t dst = base + __popc(mall & same[r] & lanemask_lt());
+            if (dst < (uint32_t)cap) cand[(size_t)p * cap + dst] = key;
           }
         }
       }
@@ -512,11 +617,13 @@ __global__ void __launch_bounds__(kSelThreads) select_kernel(SelectArgs a) {
   uint64_t* keys = reinterpret_cast<uint64_t*>(smem);          // [kSelSmemKeys]
   uint64_t* sorted = keys + kSelSmemKeys;                       // [kpad]
   __shared__ uint32_t hist[256];
-  __shared__ uint32_t rx[8];
+  __shared__ __align__(8) uint32_t rx[10];
 
   const int tid = threadIdx.x;
   const int P = a.P, k = a.k;
   const int i = blockIdx.x / P, p = blockIdx.x % P;
+  if (a.fallback && a.fb[i] == 0) return;  // rescoring pass: only flagged units
+  if (a.fallback && p == 0 && threadIdx.x == 0 && a.stats) atomicAdd(&a.stats->rescored, 1ull);
   const int64_t s0 = a.off[i], s1 = a.off[i + 1];
   int c0 = 0, c1 = -1;
   if (s1 > s0) {
@@ -525,6 +632,20 @@ __global__ void __launch_bounds__(kSelThreads) select_kernel(SelectArgs a) {
   }
   uint32_t n = 0;
   for (int c = c0; c <= c1; ++c) n += (uint32_t)a.seg_cnt[((int64_t)c + i) * P + p];
+  // A speculative threshold is exact when at least min(k, visible) keys
+  // reached it: then every key of the top k did.  Otherwise the unit is
+  // rescored without speculation.
+  if (!a.fallback && a.tspec && a.tspec[(int64_t)i * P + p] != 0) {
+    const int64_t vis = (s1 - s0) - (P - 1 - p);
+    const uint32_t need = (uint32_t)(vis < k ? (vis > 0 ? vis : 0) : k);
+    if (n < need) {
+      if (tid == 0) {
+        a.fb[i] = 1;
+        atomicExch(a.fb_any, 1u);
+      }
+      return;
+    }
+  }
   const bool in_smem = n <= (uint32_t)kSelSmemKeys;
   auto sync = [] { __syncthreads(); };
 
@@ -556,7 +677,7 @@ __global__ void __launch_bounds__(kSelThreads) select_kernel(SelectArgs a) {
   const uint32_t count = n < (uint32_t)k ? n : (uint32_t)k;
   int kpad = 1;
   while (kpad < k) kpad <<= 1;
-  if (tid == 0) rx[4] = 0;
+  if (tid == 0) rx[9] = 0;
   __syncthreads();
   const int lane = tid & 31;
   // keys >= thr go to the sort buffer (uniform trip counts: full-warp ballots)
@@ -568,7 +689,7 @@ __global__ void __launch_bounds__(kSelThreads) select_kernel(SelectArgs a) {
       const uint32_t msk = __ballot_sync(kFull, keep);
       if (msk) {
         uint32_t base = 0;
-        if (lane == 0) base = atomicAdd(&rx[4], __popc(msk));
+        if (lane == 0) base = atomicAdd(&rx[9], __popc(msk));
         base = __shfl_sync(kFull, base, 0);
         const uint32_t dst = base + __popc(msk & lanemask_lt());
         if (keep && dst < (uint32_t)kpad) sorted[dst] = key;
@@ -604,6 +725,10 @@ __global__ void __launch_bounds__(kSelThreads) select_kernel(SelectArgs a) {
     if (a.out_score) a.out_score[obase + r] = sc;
     a.out_pay[obase + r] = pay;
     if (a.out_pay_user && a.out_pay_user != a.out_pay) a.out_pay_user[obase + r] = pay;
+  }
+  if (a.spec && tid == 0) {
+    a.spec[(int64_t)u * P + p] = count >= (uint32_t)k ? sorted[k - 1] : 0ull;
+    if (a.qn_prev && a.qn_cur) a.qn_prev[(int64_t)u * P + p] = a.qn_cur[(int64_t)i * P + p];
   }
 }
 

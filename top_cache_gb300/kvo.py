@@ -28,7 +28,9 @@ KVO_OPT_WAIT_LIMIT_NS = 2
 KVO_OPT_PROFILE = 3
 KVO_OPT_GROUPS = 4
 KVO_OPT_SCORE_CTAS = 5
-PROF_KINDS = ("append", "plan", "score", "select", "residency", "gather", "reset")
+KVO_OPT_SPECULATE = 6
+PROF_KINDS = ("append", "plan", "score", "select", "residency", "gather", "reset", "rescore",
+              "reselect")
 KVO_GATHER_LDG = 0
 KVO_GATHER_BULK = 1
 
@@ -48,7 +50,7 @@ class KvoConfig(ctypes.Structure):
 class KvoStats(ctypes.Structure):
     _fields_ = [(n, ctypes.c_uint64) for n in
                 ("steps", "unit_steps", "capacity_errors", "hits", "misses", "rows_h2d",
-                 "bytes_h2d", "rows_d2h", "bytes_d2h", "timeouts")]
+                 "bytes_h2d", "rows_d2h", "bytes_d2h", "timeouts", "rescored")]
 
 
 class KvoError(RuntimeError):
