@@ -39,6 +39,10 @@ struct kvo_handle {
   std::vector<int32_t> units_cached;
   int64_t* off = nullptr;
   uint64_t* gthr = nullptr;
+  uint32_t* tok_bits = nullptr; // [U][tok_words] scratch, kept all zero
+  int64_t tok_words = 0;
+  int32_t* order = nullptr;     // [2][U][C] LRU lists
+  int32_t* order_par = nullptr; // [U]
   uint64_t* spec = nullptr;     // [U][P] persistent: k-th best key of each unit's last step
   float* qn_prev = nullptr;     // [U][P] persistent: that step's squared query norms
   float* qn_cur = nullptr;      // [U][P] scratch
@@ -122,7 +126,7 @@ void free_all(kvo_handle* h) {
     if (ev) cudaEventDestroy(ev);
   void* dev[] = {h->idx, h->hot, h->cache_slots, h->slot_token, h->last_use, h->stamp, h->len,
                  h->all_units, h->units_dev, h->off, h->gthr, h->spec, h->qn_prev, h->qn_cur,
-                 h->tspec, h->fb, h->fb_any, h->seg_keys, h->seg_cnt, h->sel_pay,
+                 h->tspec, h->fb, h->fb_any, h->tok_bits, h->order, h->order_par, h->seg_keys, h->seg_cnt, h->sel_pay,
                  h->miss_tok, h->miss_slot, h->miss_cnt, h->miss_off, h->done_ctr, h->err,
                  h->stats};
   for (void* p : dev)
@@ -131,10 +135,8 @@ void free_all(kvo_handle* h) {
 }
 
 size_t residency_smem_bytes(int C, int P, int k) {
-  int n2 = 1;
-  while (n2 < P * k) n2 <<= 1;
   const int nwords = (C + 31) / 32;
-  return (size_t)((nwords + 3) & ~3) * 4 + (size_t)n2 * 16;
+  return (size_t)((nwords + 3) & ~3) * 4 + (size_t)P * k * 8;
 }
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
@@ -266,6 +268,10 @@ int kvo_create(const kvo_config* cfg, kvo_handle** out) {
   if (e == cudaSuccess) e = dalloc(&h->units_dev, U);
   if (e == cudaSuccess) e = dalloc(&h->off, U + 1);
   if (e == cudaSuccess) e = dalloc(&h->gthr, U * h->P);
+  h->tok_words = (h->stride + 31) / 32;
+  if (e == cudaSuccess) e = dalloc(&h->tok_bits, U * (size_t)h->tok_words);
+  if (e == cudaSuccess) e = dalloc(&h->order, 2 * U * C);
+  if (e == cudaSuccess) e = dalloc(&h->order_par, U);
   if (e == cudaSuccess) e = dalloc(&h->spec, U * h->P);
   if (e == cudaSuccess) e = dalloc(&h->qn_prev, U * h->P);
   if (e == cudaSuccess) e = dalloc(&h->qn_cur, U * h->P);
@@ -296,6 +302,8 @@ int kvo_create(const kvo_config* cfg, kvo_handle** out) {
   if (e == cudaSuccess) e = kvo::launch_fill_i32(h->slot_token, -1, U * C, 0);
   if (e == cudaSuccess) e = cudaMemset(h->last_use, 0, U * C * 4);
   if (e == cudaSuccess) e = cudaMemset(h->stamp, 0, U * 4);
+  if (e == cudaSuccess) e = cudaMemset(h->tok_bits, 0, U * (size_t)h->tok_words * 4);
+  if (e == cudaSuccess) e = kvo::launch_order_init(h->order, h->order_par, h->U, h->C, 0);
   if (e == cudaSuccess) e = cudaMemset(h->spec, 0, U * h->P * 8);
   if (e == cudaSuccess) e = cudaMemset(h->qn_prev, 0, U * h->P * 4);
   if (e == cudaSuccess) e = cudaMemset(h->fb, 0, U * 4);
@@ -485,6 +493,12 @@ int kvo_step(kvo_handle* h, const int32_t* units, int32_t n_units, const void* q
     ra.done_ctr = h->done_ctr + g;
     ra.err = h->err;
     ra.stats = h->stats;
+    ra.len = h->len;
+    ra.tok_bits = h->tok_bits;
+    ra.tok_words = h->tok_words;
+    ra.order = h->order;
+    ra.order_par = h->order_par;
+    ra.U = h->U;
     if (e == cudaSuccess) e = timed(h, KVO_PROF_RESIDENCY, s, [&] { return kvo::launch_residency(ra, s); });
 
     kvo::GatherArgs ga{};
@@ -662,6 +676,8 @@ int kvo_reset(kvo_handle* h, const int32_t* units, int32_t n_units, int64_t keep
   a.P = h->P;
   a.spec = h->spec;
   a.qn_prev = h->qn_prev;
+  a.order = h->order;
+  a.order_par = h->order_par;
   cudaError_t e = timed(h, KVO_PROF_RESET, s, [&] { return kvo::launch_reset(a, s); });
   if (e != cudaSuccess) return cuda_fail(e, "reset launch");
   for (int32_t i = 0; i < n_units; ++i) h->len_host[(size_t)(units ? units[i] : i)] = keep_tokens;

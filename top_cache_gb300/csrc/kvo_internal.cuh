@@ -199,6 +199,12 @@ struct ResidencyArgs {
   uint32_t* done_ctr;          // last-block counter (self-resetting)
   uint32_t* err;
   DevStats* stats;
+  const int32_t* len;          // [U] cached tokens
+  uint32_t* tok_bits;          // [U][tok_words] token bitmap scratch (all zero between calls)
+  int64_t tok_words;
+  int32_t* order;              // [2][U][C] LRU lists (double buffered)
+  int32_t* order_par;          // [U] which buffer is current
+  int32_t U;
 };
 
 struct GatherArgs {
@@ -233,6 +239,8 @@ struct ResetArgs {
   int32_t n, keep, C, P;
   uint64_t* spec;              // [U][P] cleared
   float* qn_prev;              // [U][P] cleared
+  int32_t* order;              // [U][C] first LRU buffer set to 0..C-1
+  int32_t* order_par;          // [U] set to 0
   int64_t stride;
   int32_t* cache_slots;
   int32_t* slot_token;
@@ -250,6 +258,7 @@ cudaError_t launch_residency(const ResidencyArgs& a, cudaStream_t s);
 cudaError_t launch_gather(const GatherArgs& a, int n_sm, cudaStream_t s);
 cudaError_t launch_append(const AppendArgs& a, cudaStream_t s);
 cudaError_t launch_reset(const ResetArgs& a, cudaStream_t s);
+cudaError_t launch_order_init(int32_t* order, int32_t* par, int U, int C, cudaStream_t s);
 cudaError_t launch_set_len(int32_t* len, int32_t unit, int32_t value, cudaStream_t s);
 cudaError_t launch_fill_i32(int32_t* p, int32_t v, size_t n, cudaStream_t s);
 

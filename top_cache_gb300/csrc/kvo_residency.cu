@@ -43,18 +43,6 @@ __device__ __forceinline__ uint32_t block_sum_u32(uint32_t v, uint32_t* wsum) {
   return t;
 }
 
-__device__ __forceinline__ uint32_t block_max_u32(uint32_t v, uint32_t* wsum) {
-  const int lane = threadIdx.x & 31, w = threadIdx.x >> 5, nw = blockDim.x >> 5;
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) v = max(v, __shfl_xor_sync(kFull, v, o));
-  if (lane == 0) wsum[w] = v;
-  __syncthreads();
-  uint32_t t = 0;
-  for (int x = 0; x < nw; ++x) t = max(t, wsum[x]);
-  __syncthreads();
-  return t;
-}
-
 // Exclusive block scan of v; *total gets the block sum.
 __device__ __forceinline__ uint32_t block_excl_scan(uint32_t v, uint32_t* wsum, uint32_t* total) {
   const int lane = threadIdx.x & 31, w = threadIdx.x >> 5, nw = blockDim.x >> 5;
@@ -82,75 +70,27 @@ __device__ __forceinline__ uint32_t block_excl_scan(uint32_t v, uint32_t* wsum, 
   return excl;
 }
 
-// Warp 0: the bin (counting from the bottom) holding the need-th smallest.
-__device__ __forceinline__ void scan_bins_asc(const uint32_t* hist, uint32_t need, uint32_t* rx,
-                                              int lane) {
-  uint32_t v[8], sum = 0;
-#pragma unroll
-  for (int e = 0; e < 8; ++e) {
-    v[e] = hist[8 * lane + e];
-    sum += v[e];
-  }
-  uint32_t incl = sum;
-#pragma unroll
-  for (int o = 1; o < 32; o <<= 1) {
-    const uint32_t y = __shfl_up_sync(kFull, incl, o);
-    if (lane >= o) incl += y;
-  }
-  uint32_t below = incl - sum;
-#pragma unroll
-  for (int e = 0; e < 8; ++e) {
-    if (below < need && need <= below + v[e]) {
-      rx[0] = 8 * lane + e;
-      rx[1] = below;
-      rx[2] = v[e];
-    }
-    below += v[e];
-  }
-}
-
-template <class T>
-__device__ __forceinline__ void bitonic_asc(T* buf, int n) {
-  for (int size = 2; size <= n; size <<= 1) {
-    for (int stride = size >> 1; stride > 0; stride >>= 1) {
-      for (int i = threadIdx.x; i < (n >> 1); i += blockDim.x) {
-        const int lo = 2 * i - (i & (stride - 1));
-        const int hi = lo + stride;
-        const T x = buf[lo], y = buf[hi];
-        const bool asc = (lo & size) == 0;
-        if (asc ? (x > y) : (x < y)) {
-          buf[lo] = y;
-          buf[hi] = x;
-        }
-      }
-      __syncthreads();
-    }
-  }
-}
-
-__device__ __forceinline__ int pow2_at_least(int x) {
-  int p = 1;
-  while (p < x) p <<= 1;
-  return p;
-}
-
 }  // namespace
 
 // ---------------------------------------------------------------------------
 // residency: merge/dedup, LRU, reverse index, remap (one CTA per unit)
+//
+// No sorting: the distinct misses come out in token order from a token
+// bitmap (each thread owns a contiguous run of words; one block scan), and
+// the LRU order is an explicit list of the unit's slots kept in (last_use,
+// slot) order: victims are the first m entries not hit this step, and the
+// step's touched slots (hits and filled misses, all with the new stamp) move
+// to the end in slot order.  Every slot starts free with last_use 0, so the
+// initial list 0..C-1 is in that order, and the update preserves it.
 // ---------------------------------------------------------------------------
 __global__ void __launch_bounds__(kResThreads) residency_kernel(ResidencyArgs a) {
   extern __shared__ __align__(128) uint8_t smem[];
   const int C = a.C, PK = a.P * a.k;
-  const int n2 = pow2_at_least(PK);
   const int nwords = (C + 31) >> 5;
   const int nwords_pad = (nwords + 3) & ~3;
-  uint32_t* bitmap = reinterpret_cast<uint32_t*>(smem);        // [nwords_pad] hit slots
-  int32_t* raw = reinterpret_cast<int32_t*>(bitmap + nwords_pad);  // [n2] miss tokens with dups
-  int32_t* M = raw + n2;                                        // [n2] distinct misses, ascending
-  uint64_t* vic = reinterpret_cast<uint64_t*>(M + n2);          // [n2] victim keys
-  __shared__ uint32_t hist[256];
-  __shared__ uint32_t rx[8];
+  uint32_t* bitmap = reinterpret_cast<uint32_t*>(smem);        // [nwords_pad] hit, then touched slots
+  int32_t* M = reinterpret_cast<int32_t*>(bitmap + nwords_pad);  // [PK] distinct misses, ascending
+  int32_t* V = M + PK;                                          // [PK] victims in LRU order
   __shared__ uint32_t wsum[32];
   __shared__ uint32_t sc[8];
 
@@ -163,6 +103,10 @@ __global__ void __launch_bounds__(kResThreads) residency_kernel(ResidencyArgs a)
   int32_t* cs = a.cache_slots + (int64_t)u * a.stride;
   int32_t* st = a.slot_token + (int64_t)u * C;
   uint32_t* lu = a.last_use + (int64_t)u * C;
+  uint32_t* tbm = a.tok_bits + (int64_t)u * a.tok_words;
+  const int par = a.order_par[u];
+  const int32_t* cur = a.order + ((int64_t)par * a.U + u) * C;
+  int32_t* nxt = a.order + ((int64_t)(par ^ 1) * a.U + u) * C;
 
   int32_t status = KVO_OK;
   uint32_t m = 0, hits = 0;
@@ -170,9 +114,8 @@ __global__ void __launch_bounds__(kResThreads) residency_kernel(ResidencyArgs a)
 
   if (status == KVO_OK) {
     for (int w = tid; w < nwords; w += kResThreads) bitmap[w] = 0;
-    if (tid == 0) sc[0] = 0;
     __syncthreads();
-    // payload says hit (slot) or miss (token): mark hit slots, list misses
+    // payload says hit (slot) or miss (token): mark hit slots and miss tokens
     for (int e = tid; e < PK; e += kResThreads) {
       const int32_t t = tok[e];
       if (t < 0) continue;
@@ -180,25 +123,29 @@ __global__ void __launch_bounds__(kResThreads) residency_kernel(ResidencyArgs a)
       if (p >= 0) {
         if (p < C) atomicOr(&bitmap[p >> 5], 1u << (p & 31));
       } else {
-        const uint32_t dst = atomicAdd(&sc[0], 1u);
-        if (dst < (uint32_t)n2) raw[dst] = t;
+        atomicOr(&tbm[t >> 5], 1u << (t & 31));
       }
     }
     __syncthreads();
-    const int nraw = (int)min(sc[0], (uint32_t)n2);
-    const int np = pow2_at_least(nraw > 0 ? nraw : 1);
-    for (int e = nraw + tid; e < np; e += kResThreads) raw[e] = INT32_MAX;
-    __syncthreads();
-    bitonic_asc(raw, np);
-    // distinct misses in token order
-    for (int base = 0; base < np; base += kResThreads) {
-      const int e = base + tid;
-      const int32_t v = e < nraw ? raw[e] : 0;
-      const uint32_t flag = (e < nraw && (e == 0 || raw[e - 1] != v)) ? 1u : 0u;
-      uint32_t total;
-      const uint32_t pos = block_excl_scan(flag, wsum, &total);
-      if (flag) M[m + pos] = v;
-      m += total;
+    // distinct misses in token order; the bitmap words are cleared behind
+    const int tw = (int)((a.len[u] + 31) >> 5);
+    const int per = (tw + kResThreads - 1) / kResThreads;
+    const int w0 = tid * per, w1 = min(tw, w0 + per);
+    uint32_t c = 0;
+    for (int w = w0; w < w1; ++w) c += __popc(__ldcg(&tbm[w]));
+    uint32_t total;
+    uint32_t pos = block_excl_scan(c, wsum, &total);
+    m = total;
+    for (int w = w0; w < w1; ++w) {
+      uint32_t bits = __ldcg(&tbm[w]);
+      if (!bits) continue;
+      tbm[w] = 0;
+      while (bits) {
+        const int b = __ffs(bits) - 1;
+        bits &= bits - 1;
+        if (pos < (uint32_t)PK) M[pos] = w * 32 + b;
+        ++pos;
+      }
     }
     uint32_t hc = 0;
     for (int w = tid; w < nwords; w += kResThreads) hc += __popc(bitmap[w]);
@@ -210,7 +157,6 @@ __global__ void __launch_bounds__(kResThreads) residency_kernel(ResidencyArgs a)
     const uint32_t stamp = a.stamp[u] + 1;
     __syncthreads();
     if (tid == 0) a.stamp[u] = stamp;
-    // hits: refresh their stamps
     for (int w = tid; w < nwords; w += kResThreads) {
       uint32_t bits = bitmap[w];
       while (bits) {
@@ -219,55 +165,23 @@ __global__ void __launch_bounds__(kResThreads) residency_kernel(ResidencyArgs a)
         lu[w * 32 + b] = stamp;
       }
     }
+    const int per = (C + kResThreads - 1) / kResThreads;
+    const int j0 = tid * per, j1 = min(C, j0 + per);
+    auto hit = [&](int s) { return ((bitmap[s >> 5] >> (s & 31)) & 1u) != 0; };
     if (m > 0) {
-      // victims: the m smallest (last_use, slot) among slots not hit
-      auto eligible = [&](int s) { return ((bitmap[s >> 5] >> (s & 31)) & 1u) == 0; };
-      uint32_t mx = 0;
-      for (int s = tid; s < C; s += kResThreads)
-        if (eligible(s)) mx = max(mx, lu[s]);
-      mx = block_max_u32(mx, wsum);
-      const int bits_s = C > 1 ? 32 - __clz(C - 1) : 0;
-      const int bits_lu = mx ? 32 - __clz(mx) : 0;
-      const int B = bits_s + bits_lu;
-      const uint64_t smask = (1ull << bits_s) - 1;
-      uint64_t prefix = 0, mask = 0;
-      uint32_t need = m;
-      for (int shift = B > 0 ? ((B - 1) / 8) * 8 : 0; shift >= 0; shift -= 8) {
-        for (int b = tid; b < 256; b += kResThreads) hist[b] = 0;
-        __syncthreads();
-        for (int s = tid; s < C; s += kResThreads) {
-          if (!eligible(s)) continue;
-          const uint64_t key = ((uint64_t)lu[s] << bits_s) | (uint64_t)s;
-          if ((key & mask) == prefix) atomicAdd(&hist[(uint32_t)(key >> shift) & 255u], 1u);
-        }
-        __syncthreads();
-        if (tid < 32) scan_bins_asc(hist, need, rx, tid);
-        __syncthreads();
-        const uint32_t bin = rx[0], below = rx[1], inbin = rx[2];
-        need -= below;
-        prefix |= (uint64_t)bin << shift;
-        mask |= 0xffull << shift;
-        __syncthreads();
-        if (inbin == need) break;
-      }
-      if (tid == 0) sc[1] = 0;
-      __syncthreads();
-      for (int s = tid; s < C; s += kResThreads) {
-        if (!eligible(s)) continue;
-        const uint64_t key = ((uint64_t)lu[s] << bits_s) | (uint64_t)s;
-        if ((key & mask) <= prefix) {
-          const uint32_t dst = atomicAdd(&sc[1], 1u);
-          if (dst < (uint32_t)n2) vic[dst] = key;
-        }
+      // victims: the first m slots of the LRU list that were not hit
+      uint32_t c = 0;
+      for (int j = j0; j < j1; ++j) c += hit(cur[j]) ? 0u : 1u;
+      uint32_t total;
+      uint32_t rank = block_excl_scan(c, wsum, &total);
+      for (int j = j0; j < j1 && rank < m; ++j) {
+        const int s = cur[j];
+        if (!hit(s)) V[rank++] = s;
       }
       __syncthreads();
-      const int nv = pow2_at_least((int)m);
-      for (int e = (int)m + tid; e < nv; e += kResThreads) vic[e] = ~0ull;
-      __syncthreads();
-      bitonic_asc(vic, nv);
       // i-th miss (token order) takes the i-th victim
       for (uint32_t r = tid; r < m; r += kResThreads) {
-        const int s = (int)(vic[r] & smask);
+        const int s = V[r];
         const int32_t t = M[r];
         const int32_t old = st[s];
         if (old >= 0) cs[old] = -1;
@@ -277,6 +191,35 @@ __global__ void __launch_bounds__(kResThreads) residency_kernel(ResidencyArgs a)
         a.miss_tok[(int64_t)i * PK + r] = t;
         a.miss_slot[(int64_t)i * PK + r] = s;
       }
+      __syncthreads();
+      for (uint32_t r = tid; r < m; r += kResThreads) atomicOr(&bitmap[V[r] >> 5], 1u << (V[r] & 31));
+    }
+    __syncthreads();
+    if (hits + m > 0) {
+      // new list: untouched slots in their order, then the touched ones in slot order
+      uint32_t c = 0;
+      for (int j = j0; j < j1; ++j) c += hit(cur[j]) ? 0u : 1u;
+      uint32_t kept;
+      uint32_t q = block_excl_scan(c, wsum, &kept);
+      for (int j = j0; j < j1; ++j) {
+        const int s = cur[j];
+        if (!hit(s)) nxt[q++] = s;
+      }
+      const int wper = (nwords + kResThreads - 1) / kResThreads;
+      const int v0 = tid * wper, v1 = min(nwords, v0 + wper);
+      uint32_t tc = 0;
+      for (int w = v0; w < v1; ++w) tc += __popc(bitmap[w]);
+      uint32_t tt;
+      uint32_t o = kept + block_excl_scan(tc, wsum, &tt);
+      for (int w = v0; w < v1; ++w) {
+        uint32_t bits = bitmap[w];
+        while (bits) {
+          const int b = __ffs(bits) - 1;
+          bits &= bits - 1;
+          nxt[o++] = w * 32 + b;
+        }
+      }
+      if (tid == 0) a.order_par[u] = par ^ 1;
     }
     __syncthreads();
     // remap logical top-k positions to physical slots
@@ -489,7 +432,9 @@ __global__ void __launch_bounds__(256) reset_kernel(ResetArgs a) {
   for (int s = threadIdx.x; s < a.C; s += blockDim.x) {
     a.slot_token[(int64_t)u * a.C + s] = -1;
     a.last_use[(int64_t)u * a.C + s] = 0;
+    a.order[(int64_t)u * a.C + s] = s;
   }
+  if (threadIdx.x == 0) a.order_par[u] = 0;
   for (int p = threadIdx.x; p < a.P; p += blockDim.x) {
     a.spec[(int64_t)u * a.P + p] = 0;
     a.qn_prev[(int64_t)u * a.P + p] = 0.f;
@@ -499,6 +444,14 @@ __global__ void __launch_bounds__(256) reset_kernel(ResetArgs a) {
     a.stamp[u] = 0;
     a.len[u] = a.keep;
   }
+}
+
+__global__ void order_init_kernel(int32_t* order, int32_t* par, int U, int C) {
+  const size_t n = (size_t)U * C;
+  for (size_t e = blockIdx.x * (size_t)blockDim.x + threadIdx.x; e < n; e += (size_t)gridDim.x * blockDim.x)
+    order[e] = (int32_t)(e % (size_t)C);
+  for (size_t e = blockIdx.x * (size_t)blockDim.x + threadIdx.x; e < (size_t)U; e += (size_t)gridDim.x * blockDim.x)
+    par[e] = 0;
 }
 
 __global__ void set_len_kernel(int32_t* len, int32_t unit, int32_t value) { len[unit] = value; }
@@ -512,11 +465,9 @@ __global__ void fill_i32_kernel(int32_t* p, int32_t v, size_t n) {
 // host launchers
 // ---------------------------------------------------------------------------
 size_t residency_smem(int C, int P, int k) {
-  int n2 = 1;
-  while (n2 < P * k) n2 <<= 1;
   const int nwords = (C + 31) / 32;
   const int nwords_pad = (nwords + 3) & ~3;
-  return (size_t)nwords_pad * 4 + (size_t)n2 * 4 * 2 + (size_t)n2 * 8;
+  return (size_t)nwords_pad * 4 + (size_t)P * k * 4 * 2;
 }
 
 cudaError_t launch_residency(const ResidencyArgs& a, cudaStream_t s) {
@@ -534,9 +485,9 @@ cudaError_t launch_gather(const GatherArgs& a, int n_sm, cudaStream_t s) {
                         (size_t)(kGatherThreads / 32) * kBulkDepth * slot_bytes;
     cudaError_t e = cudaFuncSetAttribute(gather_bulk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
-    gather_bulk_kernel<<<n_sm * 4, kGatherThreads, smem, s>>>(a);
+    gather_bulk_kernel<<<n_sm, kGatherThreads, smem, s>>>(a);
   } else {
-    gather_ldg_kernel<<<n_sm * 4, kGatherThreads, 0, s>>>(a);
+    gather_ldg_kernel<<<n_sm, kGatherThreads, 0, s>>>(a);
   }
   return cudaGetLastError();
 }
@@ -548,6 +499,11 @@ cudaError_t launch_append(const AppendArgs& a, cudaStream_t s) {
 
 cudaError_t launch_reset(const ResetArgs& a, cudaStream_t s) {
   reset_kernel<<<a.n, 256, 0, s>>>(a);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_order_init(int32_t* order, int32_t* par, int U, int C, cudaStream_t s) {
+  order_init_kernel<<<1024, 256, 0, s>>>(order, par, U, C);
   return cudaGetLastError();
 }
 

@@ -21,6 +21,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <type_traits>
+
 #include "kvo_internal.cuh"
 
 namespace kvo {
@@ -175,24 +177,84 @@ __device__ __forceinline__ uint64_t radix_threshold_desc(ForEach for_each, uint3
   return prefix;
 }
 
-// In-place bitonic sort, descending, of n (power of two) keys in shared memory.
-template <int NT, class Sync>
-__device__ __forceinline__ void bitonic_desc(uint64_t* buf, int n, int tid, Sync sync) {
+// Bitonic sort, descending, of n = E * NT keys (n a power of two) held in
+// registers, E consecutive keys per thread; buf (n keys of shared memory) is
+// only the exchange area of strides that cross warps.  Strides below E stay
+// in a thread, strides below 32 E use warp shuffles.
+template <int E, int NT>
+__device__ __forceinline__ void bitonic_regs_desc(uint64_t (&v)[E], uint64_t* buf, int n, int tid) {
+  const int lane = tid & 31;
   for (int size = 2; size <= n; size <<= 1) {
     for (int stride = size >> 1; stride > 0; stride >>= 1) {
-      for (int i = tid; i < (n >> 1); i += NT) {
-        const int lo = 2 * i - (i & (stride - 1));
-        const int hi = lo + stride;
-        const uint64_t x = buf[lo], y = buf[hi];
-        const bool desc = (lo & size) == 0;
-        if (desc ? (x < y) : (x > y)) {
-          buf[lo] = y;
-          buf[hi] = x;
+      if (stride >= 32 * E) {
+        __syncthreads();
+#pragma unroll
+        for (int e = 0; e < E; ++e) buf[tid * E + e] = v[e];
+        __syncthreads();
+#pragma unroll
+        for (int e = 0; e < E; ++e) {
+          const int i = tid * E + e;
+          const uint64_t w = buf[i ^ stride];
+          const bool asc = (i & size) != 0, lower = (i & stride) == 0;
+          const bool keep_max = lower != asc;
+          v[e] = keep_max ? (v[e] > w ? v[e] : w) : (v[e] < w ? v[e] : w);
         }
+      } else if (stride >= E) {
+        const int ld = stride / E;
+#pragma unroll
+        for (int e = 0; e < E; ++e) {
+          const int i = tid * E + e;
+          const uint64_t w = __shfl_xor_sync(kFull, v[e], ld);
+          const bool asc = (i & size) != 0, lower = (i & stride) == 0;
+          const bool keep_max = lower != asc;
+          v[e] = keep_max ? (v[e] > w ? v[e] : w) : (v[e] < w ? v[e] : w);
+        }
+      } else {
+        // in-thread strides 1, 2, 4: compile-time indices keep v in registers
+        auto ce = [&](auto S_) {
+          constexpr int S = decltype(S_)::value;
+#pragma unroll
+          for (int e = 0; e < E; ++e) {
+            if constexpr (S < E) {
+              if (e & S) continue;
+              const int i = tid * E + e;
+              const uint64_t x = v[e], y = v[e + S];
+              const bool asc = (i & size) != 0;
+              const bool swap = asc ? (x > y) : (x < y);
+              v[e] = swap ? y : x;
+              v[e + S] = swap ? x : y;
+            }
+          }
+        };
+        if (stride == 1) ce(std::integral_constant<int, 1>{});
+        else if (stride == 2) ce(std::integral_constant<int, 2>{});
+        else ce(std::integral_constant<int, 4>{});
       }
-      sync();
     }
   }
+  (void)lane;
+}
+
+// Sorts buf[0..n) descending (n a power of two, n <= 8 * NT) with all NT threads.
+template <int NT>
+__device__ __forceinline__ void block_sort_desc(uint64_t* buf, int n, int tid) {
+  auto run = [&](auto E_) {
+    constexpr int E = decltype(E_)::value;
+    uint64_t v[E];
+    const bool active = tid * E < n;
+#pragma unroll
+    for (int e = 0; e < E; ++e) v[e] = active ? buf[tid * E + e] : 0ull;
+    bitonic_regs_desc<E, NT>(v, buf, n, tid);
+    __syncthreads();
+    if (active)
+#pragma unroll
+      for (int e = 0; e < E; ++e) buf[tid * E + e] = v[e];
+    __syncthreads();
+  };
+  if (n <= NT) run(std::integral_constant<int, 1>{});
+  else if (n <= 2 * NT) run(std::integral_constant<int, 2>{});
+  else if (n <= 4 * NT) run(std::integral_constant<int, 4>{});
+  else run(std::integral_constant<int, 8>{});
 }
 
 __device__ __forceinline__ void consumer_sync() { named_sync(1, kCT); }
@@ -707,7 +769,7 @@ __global__ void __launch_bounds__(kSelThreads) select_kernel(SelectArgs a) {
   __syncthreads();
   for (int e = count + tid; e < kpad; e += kSelThreads) sorted[e] = 0;
   __syncthreads();
-  bitonic_desc<kSelThreads>(sorted, kpad, tid, sync);
+  block_sort_desc<kSelThreads>(sorted, kpad, tid);
 
   const int u = a.units[i];
   const int64_t obase = ((int64_t)i * P + p) * k;
