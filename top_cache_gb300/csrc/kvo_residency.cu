@@ -167,7 +167,8 @@ __global__ void __launch_bounds__(kResThreads) residency_kernel(ResidencyArgs a)
     }
     const int per = (C + kResThreads - 1) / kResThreads;
     const int j0 = tid * per, j1 = min(C, j0 + per);
-    auto hit = [&](int s) { return ((bitmap[s >> 5] >> (s & 31)) & 1u) != 0; };
+    // slots outside [0, C) never come from a valid list; they count as touched
+    auto hit = [&](int s) { return (unsigned)s >= (unsigned)C || ((bitmap[s >> 5] >> (s & 31)) & 1u) != 0; };
     if (m > 0) {
       // victims: the first m slots of the LRU list that were not hit
       uint32_t c = 0;
@@ -203,7 +204,7 @@ __global__ void __launch_bounds__(kResThreads) residency_kernel(ResidencyArgs a)
       uint32_t q = block_excl_scan(c, wsum, &kept);
       for (int j = j0; j < j1; ++j) {
         const int s = cur[j];
-        if (!hit(s)) nxt[q++] = s;
+        if (!hit(s) && q < (uint32_t)C) nxt[q++] = s;
       }
       const int wper = (nwords + kResThreads - 1) / kResThreads;
       const int v0 = tid * wper, v1 = min(nwords, v0 + wper);
@@ -216,7 +217,7 @@ __global__ void __launch_bounds__(kResThreads) residency_kernel(ResidencyArgs a)
         while (bits) {
           const int b = __ffs(bits) - 1;
           bits &= bits - 1;
-          nxt[o++] = w * 32 + b;
+          if (o < (uint32_t)C) nxt[o++] = w * 32 + b;
         }
       }
       if (tid == 0) a.order_par[u] = par ^ 1;

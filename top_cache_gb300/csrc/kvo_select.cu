@@ -187,18 +187,22 @@ __device__ __forceinline__ void bitonic_regs_desc(uint64_t (&v)[E], uint64_t* bu
   for (int size = 2; size <= n; size <<= 1) {
     for (int stride = size >> 1; stride > 0; stride >>= 1) {
       if (stride >= 32 * E) {
+        // only threads that hold keys touch buf (n may be smaller than E * NT)
+        const bool active = tid * E < n;
         __syncthreads();
+        if (active)
 #pragma unroll
-        for (int e = 0; e < E; ++e) buf[tid * E + e] = v[e];
+          for (int e = 0; e < E; ++e) buf[tid * E + e] = v[e];
         __syncthreads();
+        if (active)
 #pragma unroll
-        for (int e = 0; e < E; ++e) {
-          const int i = tid * E + e;
-          const uint64_t w = buf[i ^ stride];
-          const bool asc = (i & size) != 0, lower = (i & stride) == 0;
-          const bool keep_max = lower != asc;
-          v[e] = keep_max ? (v[e] > w ? v[e] : w) : (v[e] < w ? v[e] : w);
-        }
+          for (int e = 0; e < E; ++e) {
+            const int i = tid * E + e;
+            const uint64_t w = buf[i ^ stride];
+            const bool asc = (i & size) != 0, lower = (i & stride) == 0;
+            const bool keep_max = lower != asc;
+            v[e] = keep_max ? (v[e] > w ? v[e] : w) : (v[e] < w ? v[e] : w);
+          }
       } else if (stride >= E) {
         const int ld = stride / E;
 #pragma unroll
