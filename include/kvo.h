@@ -245,6 +245,27 @@ int kvo_get_stats(kvo_handle* h, kvo_stats* out);
 int kvo_export_state(kvo_handle* h, int32_t unit, int32_t* cache_slots, int32_t* slot_token,
                      uint32_t* last_use, int64_t* length, uint32_t* stamp, void* hot_rows);
 
+/*
+ * kvo_select_noalloc: kvo_select for callers that cannot allocate memory.
+ * The pages have no counterpart of this call; it exists for callers such as
+ * an operator hosted by a framework that owns all device memory and forbids
+ * its extensions to call cudaMalloc, or a latency-critical loop that cannot
+ * afford an allocation.  Same arguments and results as kvo_select, without
+ * the workspace: the scratch is a fixed 16 MiB device array inside the
+ * library, held until exit by every GPU that loads the library (under lazy
+ * module loading, from the first call on that device), and an accepted call
+ * allocates nothing on the host or the device.  Limits: n_units <= 64
+ * and a scratch need (the kvo_select_workspace_size formula) of at most
+ * 16 MiB, else KVO_ERANGE with a message.  All calls share the array: the
+ * call clears what must start at zero, but calls that overlap on the GPU race
+ * (order them on one stream).  The first call on a device looks up the
+ * array's address for that device; make it before any stream capture.
+ */
+int kvo_select_noalloc(const void* keys, int64_t unit_stride, const int32_t* cache_slots,
+                       const int64_t* lengths, int32_t n_units, int32_t n_pos, int32_t k,
+                       const void* queries, int32_t* tokens, float* scores, int32_t* payload,
+                       void* stream);
+
 /* kvo_last_error: message of the last failing call on this thread ("" if none). */
 const char* kvo_last_error(void);
 

@@ -202,6 +202,10 @@ int grid_for(int64_t T, int G_max) {
 
 }  // namespace
 
+namespace kvo {
+void set_last_error(const char* msg) { g_err = msg; }
+}  // namespace kvo
+
 extern "C" {
 
 const char* kvo_last_error(void) { return g_err.c_str(); }

@@ -249,6 +249,9 @@ struct ResetArgs {
   int32_t* len;
 };
 
+// Sets the thread-local message returned by kvo_last_error().
+void set_last_error(const char* msg);
+
 // Host-side launchers (return cudaError_t of the launch).
 int score_cap_for(int P, int k);
 cudaError_t launch_plan(const SelectArgs& a, cudaStream_t s);

@@ -36,7 +36,8 @@ KVO_GATHER_BULK = 1
 
 EXPORTED = ("kvo_create", "kvo_destroy", "kvo_host_rows", "kvo_prefill", "kvo_append", "kvo_step",
             "kvo_select_workspace_size", "kvo_select", "kvo_reset", "kvo_profile_read",
-            "kvo_set_option", "kvo_get_stats", "kvo_export_state", "kvo_last_error")
+            "kvo_set_option", "kvo_get_stats", "kvo_export_state", "kvo_select_noalloc",
+            "kvo_last_error")
 
 
 class KvoConfig(ctypes.Structure):
@@ -94,6 +95,8 @@ def lib():
             L.kvo_select.restype = ctypes.c_int
             L.kvo_select.argtypes = [vp, i64, vp, vp, i32, i32, i32, vp, vp, vp, vp, vp,
                                      ctypes.c_size_t, vp]
+            L.kvo_select_noalloc.restype = ctypes.c_int
+            L.kvo_select_noalloc.argtypes = [vp, i64, vp, vp, i32, i32, i32, vp, vp, vp, vp, vp]
             L.kvo_reset.restype = ctypes.c_int
             L.kvo_reset.argtypes = [vp, vp, i32, i64, vp]
             L.kvo_profile_read.restype = ctypes.c_int
@@ -193,6 +196,16 @@ def kvo_select(keys, unit_stride, cache_slots, lengths, n_units, n_pos, k, queri
                                    n_units, n_pos, k, _ptr(queries), _ptr(tokens), _ptr(scores),
                                    _ptr(payload), _ptr(workspace), workspace_bytes,
                                    _stream(stream)))
+
+
+def kvo_select_noalloc(keys, unit_stride, cache_slots, lengths, n_units, n_pos, k, queries,
+                       tokens, scores, payload, stream=None):
+    """kvo_select without a workspace (fixed scratch inside the library; allocates nothing)."""
+    ln = np.ascontiguousarray(lengths, dtype=np.int64)
+    return _check(lib().kvo_select_noalloc(_ptr(keys), unit_stride, _ptr(cache_slots),
+                                           ln.ctypes.data, n_units, n_pos, k, _ptr(queries),
+                                           _ptr(tokens), _ptr(scores), _ptr(payload),
+                                           _stream(stream)))
 
 
 def kvo_reset(h, units, n_units, keep_tokens, stream=None):
