@@ -355,6 +355,8 @@ def run_kvo(args, log):
     if "append" in kernels:
         a = append_bytes / (prof["append"][0] / 1e3) / 1e9
         kernels["append"].update(achieved_gbs=round(a, 1))
+    for name in kernels:
+        kernels[name]["traffic"] = load_traffic(name, wl.name)
     dom = max(kernels, key=lambda n: kernels[n]["ms_total"])
     d = kernels[dom]
     roof = {"kernel": dom, "bound": d.get("bound", "latency"),
