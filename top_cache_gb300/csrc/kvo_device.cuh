@@ -1,0 +1,863 @@
+// Device building blocks shared by the step kernels (separate launches) and the
+// fused persistent step kernel: indexer scoring of a tile, candidate filter and
+// compaction, exact top-k select of one (unit, position), residency update of
+// one unit.  Every block-level routine takes its thread count NT and a barrier
+// functor, so it runs both as a whole CTA (__syncthreads) and as the consumer
+// warps of a warp-specialised CTA (named barrier).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include <type_traits>
+
+#include "kvo_internal.cuh"
+
+namespace kvo {
+namespace dev {
+
+constexpr int kTile = 128;                  // keys per ring stage
+constexpr int kTileBytes = kTile * kKeyBytes;
+constexpr int kStages = 3;
+constexpr int kCW = 16;                     // consumer warps
+constexpr int kCT = kCW * 32;               // consumer threads
+constexpr int kScoreThreads = kCT + 32;     // + one producer warp
+constexpr int kCheckTiles = 8;              // tiles between candidate-buffer checks
+constexpr int kSmemMax = 222 * 1024;        // leaves room for a co-resident copy CTA
+constexpr int kSelThreads = 512;
+constexpr int kSelSmemKeys = 8192;          // candidates held in shared memory by select
+constexpr int kMaxK = 4096;
+
+__device__ __forceinline__ void consumer_sync() { named_sync(1, kCT); }
+
+// ---------------------------------------------------------------------------
+// 16-lane tree reduction of chunk sums.  Lane j (of a half warp) holds chunk
+// j's partial sums for V (token, position) pairs.  Levels pair lanes j and
+// j^8, then j^4, j^2, j^1: exactly the tree c_j += c_{j+w}, w = 8, 4, 2, 1
+// (fp32 addition is commutative, so either lane of a pair may add).  While
+// more than one value is left per lane a level also transposes: each lane
+// keeps the lower half of its slots and receives the partner's upper half, so
+// V values cost V-1 shuffles and no selects.  That works because slot i of
+// lane l holds pair (i ^ X_l), X_l = tree_perm<V>(l): partners differ in
+// exactly the bit of X that the level splits on.
+// ---------------------------------------------------------------------------
+template <int CUR, int V>
+__device__ __forceinline__ void tree_level(float (&a)[V], int m) {
+  if constexpr (CUR > 1) {
+#pragma unroll
+    for (int i = 0; i < CUR / 2; ++i) a[i] = a[i] + __shfl_xor_sync(kFull, a[i + CUR / 2], m);
+  } else {
+    a[0] = a[0] + __shfl_xor_sync(kFull, a[0], m);
+  }
+}
+
+template <int V>
+__device__ __forceinline__ void tree16(float (&a)[V]) {
+  tree_level<V, V>(a, 8);
+  tree_level<(V >= 2 ? V / 2 : 1), V>(a, 4);
+  tree_level<(V >= 4 ? V / 4 : 1), V>(a, 2);
+  tree_level<(V >= 8 ? V / 8 : 1), V>(a, 1);
+}
+
+// X_l: the lane's slot permutation (slot i holds pair i ^ X_l), which is also
+// the pair held in slot 0 after tree16.
+template <int V>
+__device__ __forceinline__ int tree_perm(int lane) {
+  int x = 0, cur = V;
+#pragma unroll
+  for (int m = 8; m >= 1; m >>= 1) {
+    if (cur > 1) {
+      if (lane & m) x += cur / 2;
+      cur /= 2;
+    }
+  }
+  return x;
+}
+// After tree16 with V < 16 several lanes hold the same sum; one reports it.
+template <int V>
+__device__ __forceinline__ bool tree_owner(int lane) {
+  constexpr int dup = V >= 16 ? 0 : (16 / V - 1);
+  return (lane & dup) == 0;
+}
+
+// ---------------------------------------------------------------------------
+// Block-level helpers (first NT threads of the block, barrier `sync`)
+// ---------------------------------------------------------------------------
+// Warp 0: the histogram bin (counting from the top) holding the need-th
+// largest element.  rx[0] = bin, rx[1] = count above it, rx[2] = count in it.
+__device__ __forceinline__ void scan_bins_desc(const uint32_t* hist, uint32_t need, uint32_t* rx,
+                                               int lane) {
+  uint32_t v[8], sum = 0;
+#pragma unroll
+  for (int e = 0; e < 8; ++e) {
+    v[e] = hist[255 - 8 * lane - e];
+    sum += v[e];
+  }
+  uint32_t incl = sum;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const uint32_t y = __shfl_up_sync(kFull, incl, o);
+    if (lane >= o) incl += y;
+  }
+  uint32_t above = incl - sum;
+#pragma unroll
+  for (int e = 0; e < 8; ++e) {
+    if (above < need && need <= above + v[e]) {
+      rx[0] = 255 - 8 * lane - e;
+      rx[1] = above;
+      rx[2] = v[e];
+    }
+    above += v[e];
+  }
+}
+
+// Exact radix select over unique 64-bit keys: returns the smallest value
+// 'thr' such that exactly 'need' keys are >= thr.  for_each(f) must call f on
+// every key once (strided over the NT participating threads); sync() is the
+// barrier of those threads.  Requires need <= number of keys.  Uses rx[0..7]
+// (rx 8-byte aligned) and hist[256].
+template <int NT, class ForEach, class Sync>
+__device__ __forceinline__ uint64_t radix_threshold_desc(ForEach for_each, uint32_t need,
+                                                         uint32_t* hist, uint32_t* rx, int tid,
+                                                         Sync sync) {
+  // the bytes every key shares need no histogram pass
+  unsigned long long* mm = reinterpret_cast<unsigned long long*>(rx + 4);  // rx[4..7]: min, max
+  if (tid == 0) {
+    mm[0] = ~0ull;
+    mm[1] = 0ull;
+  }
+  sync();
+  unsigned long long lo = ~0ull, hi = 0ull;
+  for_each([&](uint64_t key) {
+    lo = key < lo ? key : lo;
+    hi = key > hi ? key : hi;
+  });
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    const unsigned long long l2 = __shfl_xor_sync(kFull, lo, o), h2 = __shfl_xor_sync(kFull, hi, o);
+    lo = l2 < lo ? l2 : lo;
+    hi = h2 > hi ? h2 : hi;
+  }
+  if ((tid & 31) == 0) {
+    atomicMin(&mm[0], lo);
+    atomicMax(&mm[1], hi);
+  }
+  sync();
+  const unsigned long long kmin = mm[0], kmax = mm[1];
+  sync();
+  const int common = kmin == kmax ? 64 : __clzll((long long)(kmin ^ kmax));
+  const int top = 56 - 8 * (common / 8);  // first byte that differs
+  if (top < 0) return kmin;               // all keys equal (cannot happen: keys are unique)
+  const uint64_t cmask = top >= 56 ? 0ull : ~((1ull << (top + 8)) - 1);
+  uint64_t prefix = kmin & cmask, mask = cmask;
+  for (int shift = top; shift >= 0; shift -= 8) {
+    for (int b = tid; b < 256; b += NT) hist[b] = 0;
+    sync();
+    for_each([&](uint64_t key) {
+      if ((key & mask) == prefix) atomicAdd(&hist[(uint32_t)(key >> shift) & 255u], 1u);
+    });
+    sync();
+    if (tid < 32) scan_bins_desc(hist, need, rx, tid);
+    sync();
+    const uint32_t bin = rx[0], above = rx[1], inbin = rx[2];
+    need -= above;
+    prefix |= (uint64_t)bin << shift;
+    mask |= 0xffull << shift;
+    if (inbin == need) break;
+  }
+  return prefix;
+}
+
+// Bitonic sort, descending, of n = E * NT keys (n a power of two) held in
+// registers, E consecutive keys per thread; buf (n keys of shared memory) is
+// only the exchange area of strides that cross warps.  Strides below E stay
+// in a thread, strides below 32 E use warp shuffles.
+template <int E, int NT, class Sync>
+__device__ __forceinline__ void bitonic_regs_desc(uint64_t (&v)[E], uint64_t* buf, int n, int tid,
+                                                  Sync sync) {
+  for (int size = 2; size <= n; size <<= 1) {
+    for (int stride = size >> 1; stride > 0; stride >>= 1) {
+      if (stride >= 32 * E) {
+        // only threads that hold keys touch buf (n may be smaller than E * NT)
+        const bool active = tid * E < n;
+        sync();
+        if (active)
+#pragma unroll
+          for (int e = 0; e < E; ++e) buf[tid * E + e] = v[e];
+        sync();
+        if (active)
+#pragma unroll
+          for (int e = 0; e < E; ++e) {
+            const int i = tid * E + e;
+            const uint64_t w = buf[i ^ stride];
+            const bool asc = (i & size) != 0, lower = (i & stride) == 0;
+            const bool keep_max = lower != asc;
+            v[e] = keep_max ? (v[e] > w ? v[e] : w) : (v[e] < w ? v[e] : w);
+          }
+      } else if (stride >= E) {
+        const int ld = stride / E;
+#pragma unroll
+        for (int e = 0; e < E; ++e) {
+          const int i = tid * E + e;
+          const uint64_t w = __shfl_xor_sync(kFull, v[e], ld);
+          const bool asc = (i & size) != 0, lower = (i & stride) == 0;
+          const bool keep_max = lower != asc;
+          v[e] = keep_max ? (v[e] > w ? v[e] : w) : (v[e] < w ? v[e] : w);
+        }
+      } else {
+        // in-thread strides 1, 2, 4: compile-time indices keep v in registers
+        auto ce = [&](auto S_) {
+          constexpr int S = decltype(S_)::value;
+#pragma unroll
+          for (int e = 0; e < E; ++e) {
+            if constexpr (S < E) {
+              if (e & S) continue;
+              const int i = tid * E + e;
+              const uint64_t x = v[e], y = v[e + S];
+              const bool asc = (i & size) != 0;
+              const bool swap = asc ? (x > y) : (x < y);
+              v[e] = swap ? y : x;
+              v[e + S] = swap ? x : y;
+            }
+          }
+        };
+        if (stride == 1) ce(std::integral_constant<int, 1>{});
+        else if (stride == 2) ce(std::integral_constant<int, 2>{});
+        else ce(std::integral_constant<int, 4>{});
+      }
+    }
+  }
+}
+
+// Sorts buf[0..n) descending (n a power of two, n <= 8 * NT) with NT threads.
+template <int NT, class Sync>
+__device__ __forceinline__ void block_sort_desc(uint64_t* buf, int n, int tid, Sync sync) {
+  auto run = [&](auto E_) {
+    constexpr int E = decltype(E_)::value;
+    uint64_t v[E];
+    const bool active = tid * E < n;
+#pragma unroll
+    for (int e = 0; e < E; ++e) v[e] = active ? buf[tid * E + e] : 0ull;
+    bitonic_regs_desc<E, NT>(v, buf, n, tid, sync);
+    sync();
+    if (active)
+#pragma unroll
+      for (int e = 0; e < E; ++e) buf[tid * E + e] = v[e];
+    sync();
+  };
+  if (n <= NT) run(std::integral_constant<int, 1>{});
+  else if (n <= 2 * NT) run(std::integral_constant<int, 2>{});
+  else if (n <= 4 * NT) run(std::integral_constant<int, 4>{});
+  else run(std::integral_constant<int, 8>{});
+}
+
+template <int NT, class Sync>
+__device__ __forceinline__ uint32_t block_sum(uint32_t v, uint32_t* wsum, int tid, Sync sync) {
+  const int lane = tid & 31, w = tid >> 5;
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(kFull, v, o);
+  if (lane == 0) wsum[w] = v;
+  sync();
+  uint32_t t = 0;
+#pragma unroll 4
+  for (int x = 0; x < NT / 32; ++x) t += wsum[x];
+  sync();
+  return t;
+}
+
+// Exclusive scan of v over the NT threads; *total gets the sum.
+template <int NT, class Sync>
+__device__ __forceinline__ uint32_t block_excl_scan(uint32_t v, uint32_t* wsum, uint32_t* total, int tid,
+                                                    Sync sync) {
+  constexpr int NW = NT / 32;
+  const int lane = tid & 31, w = tid >> 5;
+  uint32_t incl = v;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const uint32_t y = __shfl_up_sync(kFull, incl, o);
+    if (lane >= o) incl += y;
+  }
+  if (lane == 31) wsum[w] = incl;
+  sync();
+  if (w == 0) {
+    uint32_t s = lane < NW ? wsum[lane] : 0;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const uint32_t y = __shfl_up_sync(kFull, s, o);
+      if (lane >= o) s += y;
+    }
+    if (lane < NW) wsum[lane] = s;
+  }
+  sync();
+  const uint32_t excl = (w ? wsum[w - 1] : 0) + incl - v;
+  *total = wsum[NW - 1];
+  sync();
+  return excl;
+}
+
+// ---------------------------------------------------------------------------
+// Candidate buffers of the scoring consumers
+// ---------------------------------------------------------------------------
+// Shrink one candidate buffer to at most k keys, all >= floor, that include
+// every key of the buffer which can still be among the unit's k best:
+// floor = max(local threshold, the unit's shared threshold gth), then, if
+// more than k keys reach it, the k-th largest of them.  A threshold found by
+// the radix select is a lower bound of the unit's k-th best (k keys of this
+// piece reach it) and is published to gth.  All consumer threads call it.
+// rx needs 10 words (8-byte aligned).
+__device__ __forceinline__ void compact_candidates(uint64_t* cand, uint32_t* cnt, uint64_t* thr,
+                                                   uint64_t* gth, uint64_t* fl, uint64_t* scratch,
+                                                   uint32_t* hist, uint32_t* rx, int k, int ctid) {
+  const int lane = ctid & 31;
+  if (ctid == 0) {
+    uint64_t f = *thr;
+    const uint64_t g = __ldcg(reinterpret_cast<const unsigned long long*>(gth));
+    *fl = g > f ? g : f;
+    rx[3] = 0;
+    rx[8] = 0;
+    rx[9] = (*cnt <= (uint32_t)k && *fl == *thr) ? 1u : 0u;  // nothing to do
+  }
+  consumer_sync();
+  if (rx[9]) {
+    consumer_sync();
+    return;
+  }
+  const uint64_t floor = *fl;
+  const uint32_t n = *cnt;
+  uint32_t c = 0;
+  for (uint32_t i = ctid; i < n; i += kCT) c += cand[i] >= floor ? 1u : 0u;
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) c += __shfl_xor_sync(kFull, c, o);
+  if (lane == 0 && c) atomicAdd(&rx[8], c);
+  consumer_sync();
+  const uint32_t nge = rx[8];
+  uint64_t t = floor;
+  if (nge > (uint32_t)k) {
+    auto for_each = [&](auto f) {
+      for (uint32_t i = ctid; i < n; i += kCT) {
+        const uint64_t key = cand[i];
+        if (key >= floor) f(key);
+      }
+    };
+    t = radix_threshold_desc<kCT>(for_each, (uint32_t)k, hist, rx, ctid, consumer_sync);
+  }
+  for (uint32_t i0 = 0; i0 < n; i0 += kCT) {
+    const uint32_t i = i0 + ctid;
+    const uint64_t key = i < n ? cand[i] : 0;
+    const bool keep = i < n && key >= t;
+    const uint32_t m = __ballot_sync(kFull, keep);
+    if (m) {
+      uint32_t base = 0;
+      if (lane == 0) base = atomicAdd(&rx[3], __popc(m));
+      base = __shfl_sync(kFull, base, 0);
+      const uint32_t dst = base + __popc(m & lanemask_lt());
+      if (keep && dst < (uint32_t)k) scratch[dst] = key;
+    }
+  }
+  consumer_sync();
+  const uint32_t kept = rx[3] < (uint32_t)k ? rx[3] : (uint32_t)k;
+  for (uint32_t i = ctid; i < kept; i += kCT) cand[i] = scratch[i];
+  if (ctid == 0) {
+    *cnt = kept;
+    *thr = t;
+    if (nge > (uint32_t)k) atomicMax(reinterpret_cast<unsigned long long*>(gth), (unsigned long long)t);
+  }
+  consumer_sync();
+}
+
+// Shared-memory layout of a scoring CTA.
+struct ScoreSmem {
+  uint8_t* ring;
+  uint64_t* full;
+  uint64_t* empty;
+  uint32_t* cnt;      // [8]
+  uint64_t* thr;      // [8]
+  uint32_t* hist;     // [256]
+  uint32_t* rx;       // [10]
+  uint64_t* fl;       // [1]
+  uint64_t* cand;     // [P][cap]
+  uint64_t* scratch;  // [k]
+  __device__ void carve(uint8_t* smem, int P, int cap) {
+    ring = smem;
+    full = reinterpret_cast<uint64_t*>(smem + kStages * kTileBytes);
+    empty = full + kStages;
+    cnt = reinterpret_cast<uint32_t*>(empty + kStages);
+    thr = reinterpret_cast<uint64_t*>(cnt + 8);
+    hist = reinterpret_cast<uint32_t*>(thr + 8);
+    rx = hist + 256;
+    fl = reinterpret_cast<uint64_t*>(rx + 10);
+    cand = fl + 1;
+    scratch = cand + (size_t)P * cap;
+  }
+};
+constexpr int kSmemFixed = kStages * kTileBytes + 2 * kStages * 8 + 8 * 4 + 8 * 8 + 256 * 4 + 10 * 4 + 8;
+
+// ---------------------------------------------------------------------------
+// Per-lane scoring machinery of one consumer warp (16 warps x 8 keys = one tile)
+// ---------------------------------------------------------------------------
+template <int PP>
+struct Scorer {
+  static constexpr int V = 4 * PP;                 // (token, position) pairs per lane
+  static constexpr int VL = V >= 16 ? V / 16 : 1;  // values left per lane after the tree
+  static constexpr int LPP = PP == 1 ? 0 : PP == 2 ? 1 : PP == 4 ? 2 : 3;
+  static constexpr int PH = PP >= 2 ? PP / 2 : 1;  // position pairs (packed fp32x2 FMA)
+
+  int lane, j, X, px;
+  bool owner;
+  int rowoff[4];
+  int rrow[VL], rpos[VL];
+  uint32_t lead[VL], same[VL];
+  float qf[PP][8];
+  float2 qp[PH][8];
+
+  // Slot (tau, p) of this lane scores token row tau ^ tx against position
+  // p ^ px.  Result r is (row rrow[r], position rpos[r]); for insertion, lane
+  // q < P leads position q: lead[r] = lanes reporting position q, same[r] =
+  // lanes reporting this lane's position.
+  __device__ __forceinline__ void init(int warp, int lane_) {
+    lane = lane_;
+    const int h = lane >> 4;
+    j = lane & 15;
+    X = tree_perm<V>(lane);
+    const int tx = X >> LPP;
+    px = X & (PP - 1);
+    owner = tree_owner<V>(lane);
+#pragma unroll
+    for (int tau = 0; tau < 4; ++tau) rowoff[tau] = (warp * 8 + h * 4 + (tau ^ tx)) * kKeyBytes + j * 16;
+#pragma unroll
+    for (int r = 0; r < VL; ++r) {
+      const int cmb = r ^ X;
+      rrow[r] = warp * 8 + h * 4 + (cmb >> LPP);
+      rpos[r] = cmb & (PP - 1);
+      lead[r] = 0;
+      same[r] = 0;
+      for (int q = 0; q < PP; ++q) {
+        const uint32_t m = __ballot_sync(kFull, owner && rpos[r] == q);
+        if (lane == q) lead[r] = m;
+        if (rpos[r] == q) same[r] = m;
+      }
+    }
+  }
+
+  // This lane's chunk of unit i's queries, in slot order (fp32, exact).
+  __device__ __forceinline__ void load_queries(const uint16_t* queries, int64_t i, int P) {
+#pragma unroll
+    for (int p = 0; p < PP; ++p) {
+      const int pq = p ^ px;
+      if (pq < P) {
+        const uint4 v = *reinterpret_cast<const uint4*>(queries + (i * P + pq) * kDim + j * 8);
+        qf[p][0] = bf_lo(v.x); qf[p][1] = bf_hi(v.x);
+        qf[p][2] = bf_lo(v.y); qf[p][3] = bf_hi(v.y);
+        qf[p][4] = bf_lo(v.z); qf[p][5] = bf_hi(v.z);
+        qf[p][6] = bf_lo(v.w); qf[p][7] = bf_hi(v.w);
+      } else {
+#pragma unroll
+        for (int e = 0; e < 8; ++e) qf[p][e] = 0.f;
+      }
+    }
+#pragma unroll
+    for (int m = 0; m < PH; ++m)
+#pragma unroll
+      for (int e = 0; e < 8; ++e) qp[m][e] = make_float2(qf[2 * m][e], PP >= 2 ? qf[(2 * m + 1) % PP][e] : 0.f);
+  }
+
+  // Scores the tile's keys (row stride 256 B at `tile`, shared or global
+  // memory); release() is called once the tile's memory is no longer read.
+  template <class Release>
+  __device__ __forceinline__ void score(const uint8_t* tile, float (&acc)[V], Release release) {
+#pragma unroll
+    for (int tau = 0; tau < 4; ++tau) {
+      const uint4 kv = *reinterpret_cast<const uint4*>(tile + rowoff[tau]);
+      const float kf[8] = {bf_lo(kv.x), bf_hi(kv.x), bf_lo(kv.y), bf_hi(kv.y),
+                           bf_lo(kv.z), bf_hi(kv.z), bf_lo(kv.w), bf_hi(kv.w)};
+      if constexpr (PP >= 2) {
+        // positions 2m and 2m+1 at once; each lane of the pair is the
+        // position's own FMA chain in element order
+        float2 s2[PH];
+#pragma unroll
+        for (int m = 0; m < PH; ++m) s2[m] = make_float2(0.f, 0.f);
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+          const float2 kk = make_float2(kf[e], kf[e]);
+#pragma unroll
+          for (int m = 0; m < PH; ++m) s2[m] = __ffma2_rn(qp[m][e], kk, s2[m]);
+        }
+#pragma unroll
+        for (int m = 0; m < PH; ++m) {
+          acc[tau * PP + 2 * m] = s2[m].x;
+          acc[tau * PP + 2 * m + 1] = s2[m].y;
+        }
+      } else {
+        float s = 0.f;
+#pragma unroll
+        for (int e = 0; e < 8; ++e) s = __fmaf_rn(qf[0][e], kf[e], s);
+        acc[tau] = s;
+      }
+    }
+    release();
+    tree16<V>(acc);
+  }
+
+  // Inserts the tile's results that reach their position's threshold.
+  // t: token of row 0; nt: rows in the tile; len: unit length.
+  __device__ __forceinline__ void filter(const float (&acc)[V], int64_t t, int nt, int64_t len, int P,
+                                         const uint64_t* thr, uint32_t* cnt, uint64_t* cand, int cap) {
+    // full tiles whose tokens every position sees need no per-result tests
+    const bool interior = nt == kTile && t + kTile <= len - (P - 1);
+#pragma unroll
+    for (int r = 0; r < VL; ++r) {
+      const int p = rpos[r];
+      const int64_t tok = t + rrow[r];
+      float s = acc[r];
+      if (s == 0.f) s = 0.f;  // +0 for a zero score
+      const uint64_t key = sel_key(s, (uint32_t)tok);
+      bool ok = owner && p < P;
+      if (!interior) ok = ok && rrow[r] < nt && tok < len - (P - 1 - p);
+      const bool pass = ok && key >= thr[p];
+      const uint32_t mall = __ballot_sync(kFull, pass);
+      if (mall) {
+        uint32_t base = 0;
+        if (lane < P) {
+          const uint32_t n_here = __popc(mall & lead[r]);
+          if (n_here) base = atomicAdd(&cnt[lane], n_here);
+        }
+        base = __shfl_sync(kFull, base, p);
+        if (pass) {
+          const uint32_t dst = base + __popc(mall & same[r] & lanemask_lt());
+          if (dst < (uint32_t)cap) cand[(size_t)p * cap + dst] = key;
+        }
+      }
+    }
+  }
+};
+
+// Start of a piece: counters cleared, thresholds set (consumer threads).
+__device__ __forceinline__ void piece_begin(const ScoreSmem& sm, int P, const uint64_t* start_thr, int ctid) {
+  if (ctid < P) {
+    sm.cnt[ctid] = 0;
+    sm.thr[ctid] = start_thr ? start_thr[ctid] : 0ull;
+  }
+  consumer_sync();
+}
+
+// Every kCheckTiles tiles: adopt the unit's shared thresholds and compact the
+// buffers that could overflow within the next tiles.
+__device__ __forceinline__ void piece_check(const ScoreSmem& sm, int P, int k, int cap, uint64_t* gth, int ctid) {
+  consumer_sync();
+  const uint32_t trigger = (uint32_t)(cap - kCheckTiles * kTile);
+  bool need = false;
+  for (int p = 0; p < P; ++p) need |= sm.cnt[p] > trigger;
+  if (ctid < P) {
+    const uint64_t g = __ldcg(reinterpret_cast<const unsigned long long*>(gth + ctid));
+    if (g > sm.thr[ctid]) sm.thr[ctid] = g;
+  }
+  if (need) {
+    for (int p = 0; p < P; ++p)
+      if (sm.cnt[p] > trigger)
+        compact_candidates(sm.cand + (size_t)p * cap, &sm.cnt[p], &sm.thr[p], gth + p, sm.fl, sm.scratch, sm.hist,
+                           sm.rx, k, ctid);
+  }
+}
+
+// End of a piece: at most k candidates per position, all above the shared
+// threshold, written to segment `seg`.
+__device__ __forceinline__ void piece_end(const ScoreSmem& sm, int P, int k, int cap, uint64_t* gth, int64_t seg,
+                                          uint64_t* seg_keys, int32_t* seg_cnt, int ctid) {
+  consumer_sync();
+  for (int p = 0; p < P; ++p)
+    compact_candidates(sm.cand + (size_t)p * cap, &sm.cnt[p], &sm.thr[p], gth + p, sm.fl, sm.scratch, sm.hist, sm.rx,
+                       k, ctid);
+  for (int p = 0; p < P; ++p) {
+    const uint32_t np = sm.cnt[p];
+    uint64_t* dst = seg_keys + (seg * P + p) * (int64_t)k;
+    for (uint32_t e = ctid; e < np; e += kCT) dst[e] = sm.cand[(size_t)p * cap + e];
+    if (ctid == 0) seg_cnt[seg * P + p] = (int32_t)np;
+  }
+  consumer_sync();
+}
+
+// ---------------------------------------------------------------------------
+// Exact top-k of one (unit i, position p) over segments [seg0, seg0 + nseg)
+// (NT = kSelThreads threads).  Returns false when the speculative threshold
+// of (i, p) was too high (then nothing is written).
+// keys: kSelSmemKeys u64, sorted: kpad u64, hist[256], rx[10] (8-aligned).
+// ---------------------------------------------------------------------------
+template <int NT, class Sync>
+__device__ __forceinline__ bool select_body(const SelectArgs& a, int i, int p, int64_t seg0, int nseg,
+                                            bool verify, uint64_t* keys, uint64_t* sorted, uint32_t* hist,
+                                            uint32_t* rx, int tid, Sync sync) {
+  const int P = a.P, k = a.k;
+  const int64_t s0 = a.off[i], s1 = a.off[i + 1];
+  uint32_t n = 0;
+  for (int c = 0; c < nseg; ++c) n += (uint32_t)a.seg_cnt[(seg0 + c) * P + p];
+  // A speculative threshold is exact when at least min(k, visible) keys
+  // reached it: then every key of the top k did.
+  if (verify && a.tspec && a.tspec[(int64_t)i * P + p] != 0) {
+    const int64_t vis = (s1 - s0) - (P - 1 - p);
+    const uint32_t need = (uint32_t)(vis < k ? (vis > 0 ? vis : 0) : k);
+    if (n < need) return false;
+  }
+  const bool in_smem = n <= (uint32_t)kSelSmemKeys;
+  if (in_smem) {
+    uint32_t base = 0;
+    for (int c = 0; c < nseg; ++c) {
+      const int64_t seg = seg0 + c;
+      const uint32_t m = (uint32_t)a.seg_cnt[seg * P + p];
+      const uint64_t* src = a.seg_keys + (seg * P + p) * (int64_t)k;
+      for (uint32_t e = tid; e < m; e += NT) keys[base + e] = src[e];
+      base += m;
+    }
+    sync();
+  }
+  auto for_each = [&](auto f) {
+    if (in_smem) {
+      for (uint32_t e = tid; e < n; e += NT) f(keys[e]);
+    } else {
+      for (int c = 0; c < nseg; ++c) {
+        const int64_t seg = seg0 + c;
+        const uint32_t m = (uint32_t)a.seg_cnt[seg * P + p];
+        const uint64_t* src = a.seg_keys + (seg * P + p) * (int64_t)k;
+        for (uint32_t e = tid; e < m; e += NT) f(src[e]);
+      }
+    }
+  };
+  uint64_t thr = 0;
+  if (n > (uint32_t)k) thr = radix_threshold_desc<NT>(for_each, (uint32_t)k, hist, rx, tid, sync);
+  const uint32_t count = n < (uint32_t)k ? n : (uint32_t)k;
+  int kpad = 1;
+  while (kpad < k) kpad <<= 1;
+  if (tid == 0) rx[9] = 0;
+  sync();
+  const int lane = tid & 31;
+  // keys >= thr go to the sort buffer (uniform trip counts: full-warp ballots)
+  auto keep_from = [&](const uint64_t* src, uint32_t m) {
+    for (uint32_t b = 0; b < m; b += NT) {
+      const uint32_t e = b + tid;
+      const uint64_t key = e < m ? src[e] : 0;
+      const bool keep = e < m && key >= thr;
+      const uint32_t msk = __ballot_sync(kFull, keep);
+      if (msk) {
+        uint32_t base = 0;
+        if (lane == 0) base = atomicAdd(&rx[9], __popc(msk));
+        base = __shfl_sync(kFull, base, 0);
+        const uint32_t dst = base + __popc(msk & lanemask_lt());
+        if (keep && dst < (uint32_t)kpad) sorted[dst] = key;
+      }
+    }
+  };
+  if (in_smem) {
+    keep_from(keys, n);
+  } else {
+    for (int c = 0; c < nseg; ++c) {
+      const int64_t seg = seg0 + c;
+      keep_from(a.seg_keys + (seg * P + p) * (int64_t)k, (uint32_t)a.seg_cnt[seg * P + p]);
+    }
+  }
+  sync();
+  for (int e = count + tid; e < kpad; e += NT) sorted[e] = 0;
+  sync();
+  block_sort_desc<NT>(sorted, kpad, tid, sync);
+
+  const int u = a.units[i];
+  const int64_t obase = ((int64_t)i * P + p) * k;
+  for (int r = tid; r < k; r += NT) {
+    int32_t tok = -1, pay = KVO_PAD_PAYLOAD;
+    float sc = __uint_as_float(0xff800000u);
+    if (r < (int)count) {
+      const uint64_t key = sorted[r];
+      tok = (int32_t)key_token(key);
+      sc = key_score(key);
+      const int32_t cs = a.cache_slots ? a.cache_slots[(int64_t)u * a.stride + tok] : -1;
+      pay = cs >= 0 ? cs : -(tok + 1);
+    }
+    a.out_tok[obase + r] = tok;
+    if (a.out_score) a.out_score[obase + r] = sc;
+    a.out_pay[obase + r] = pay;
+    if (a.out_pay_user && a.out_pay_user != a.out_pay) a.out_pay_user[obase + r] = pay;
+  }
+  if (a.spec && tid == 0) {
+    a.spec[(int64_t)u * P + p] = count >= (uint32_t)k ? sorted[k - 1] : 0ull;
+    if (a.qn_prev && a.qn_cur) a.qn_prev[(int64_t)u * P + p] = a.qn_cur[(int64_t)i * P + p];
+  }
+  sync();
+  return true;
+}
+
+// ---------------------------------------------------------------------------
+// Residency update of one unit (listed index i) with NT threads.
+//
+// No sorting: the distinct misses come out in token order from a token
+// bitmap (each thread owns a contiguous run of words; one block scan), and
+// the LRU order is an explicit list of the unit's slots kept in (last_use,
+// slot) order: victims are the first m entries not hit this step, and the
+// step's touched slots (hits and filled misses, all with the new stamp) move
+// to the end in slot order.  Every slot starts free with last_use 0, so the
+// initial list 0..C-1 is in that order, and the update preserves it.
+// Shared memory: bitmap [(C+31)/32] u32, M [P*k] i32, V [P*k] i32, wsum[32].
+// Returns the miss count (0 unless the status is OK).
+// ---------------------------------------------------------------------------
+template <int NT, class Sync>
+__device__ __forceinline__ uint32_t residency_body(const ResidencyArgs& a, int i, uint32_t* bitmap, int32_t* M,
+                                                   int32_t* V, uint32_t* wsum, int tid, Sync sync,
+                                                   int32_t* status_out) {
+  const int C = a.C, PK = a.P * a.k;
+  const int nwords = (C + 31) >> 5;
+  const int u = a.units[i];
+  const int32_t* tok = a.tok + (int64_t)i * PK;
+  const int32_t* pay = a.pay + (int64_t)i * PK;
+  int32_t* out_slot = a.out_slot + (int64_t)i * PK;
+  int32_t* cs = a.cache_slots + (int64_t)u * a.stride;
+  int32_t* st = a.slot_token + (int64_t)u * C;
+  uint32_t* lu = a.last_use + (int64_t)u * C;
+  uint32_t* tbm = a.tok_bits + (int64_t)u * a.tok_words;
+  const int par = a.order_par[u];
+  const int32_t* cur = a.order + ((int64_t)par * a.U + u) * C;
+  int32_t* nxt = a.order + ((int64_t)(par ^ 1) * a.U + u) * C;
+
+  int32_t status = KVO_OK;
+  uint32_t m = 0, hits = 0;
+  if (*((volatile uint32_t*)a.err) != 0) status = KVO_ETIMEOUT;
+
+  if (status == KVO_OK) {
+    for (int w = tid; w < nwords; w += NT) bitmap[w] = 0;
+    sync();
+    // payload says hit (slot) or miss (token): mark hit slots and miss tokens
+    for (int e = tid; e < PK; e += NT) {
+      const int32_t t = tok[e];
+      if (t < 0) continue;
+      const int32_t p = pay[e];
+      if (p >= 0) {
+        if (p < C) atomicOr(&bitmap[p >> 5], 1u << (p & 31));
+      } else {
+        atomicOr(&tbm[t >> 5], 1u << (t & 31));
+      }
+    }
+    __threadfence_block();
+    sync();
+    // distinct misses in token order; the bitmap words are cleared behind
+    const int tw = (int)((a.len[u] + 31) >> 5);
+    const int per = (tw + NT - 1) / NT;
+    const int w0 = tid * per, w1 = min(tw, w0 + per);
+    uint32_t c = 0;
+    for (int w = w0; w < w1; ++w) c += __popc(__ldcg(&tbm[w]));
+    uint32_t total;
+    uint32_t pos = block_excl_scan<NT>(c, wsum, &total, tid, sync);
+    m = total;
+    for (int w = w0; w < w1; ++w) {
+      uint32_t bits = __ldcg(&tbm[w]);
+      if (!bits) continue;
+      tbm[w] = 0;
+      while (bits) {
+        const int b = __ffs(bits) - 1;
+        bits &= bits - 1;
+        if (pos < (uint32_t)PK) M[pos] = w * 32 + b;
+        ++pos;
+      }
+    }
+    uint32_t hc = 0;
+    for (int w = tid; w < nwords; w += NT) hc += __popc(bitmap[w]);
+    hits = block_sum<NT>(hc, wsum, tid, sync);
+    if (hits + m > (uint32_t)C) status = KVO_ECAPACITY;
+  }
+
+  if (status == KVO_OK) {
+    const uint32_t stamp = a.stamp[u] + 1;
+    sync();
+    if (tid == 0) a.stamp[u] = stamp;
+    for (int w = tid; w < nwords; w += NT) {
+      uint32_t bits = bitmap[w];
+      while (bits) {
+        const int b = __ffs(bits) - 1;
+        bits &= bits - 1;
+        lu[w * 32 + b] = stamp;
+      }
+    }
+    const int per = (C + NT - 1) / NT;
+    const int j0 = tid * per, j1 = min(C, j0 + per);
+    // slots outside [0, C) never come from a valid list; they count as touched
+    auto hit = [&](int s) { return (unsigned)s >= (unsigned)C || ((bitmap[s >> 5] >> (s & 31)) & 1u) != 0; };
+    if (m > 0) {
+      // victims: the first m slots of the LRU list that were not hit
+      uint32_t c = 0;
+      for (int jj = j0; jj < j1; ++jj) c += hit(cur[jj]) ? 0u : 1u;
+      uint32_t total;
+      uint32_t rank = block_excl_scan<NT>(c, wsum, &total, tid, sync);
+      for (int jj = j0; jj < j1 && rank < m; ++jj) {
+        const int s = cur[jj];
+        if (!hit(s)) V[rank++] = s;
+      }
+      sync();
+      // i-th miss (token order) takes the i-th victim
+      for (uint32_t r = tid; r < m; r += NT) {
+        const int s = V[r];
+        const int32_t t = M[r];
+        const int32_t old = st[s];
+        if (old >= 0) cs[old] = -1;
+        st[s] = t;
+        cs[t] = s;
+        lu[s] = stamp;
+        a.miss_tok[(int64_t)i * PK + r] = t;
+        a.miss_slot[(int64_t)i * PK + r] = s;
+      }
+      sync();
+      for (uint32_t r = tid; r < m; r += NT) atomicOr(&bitmap[V[r] >> 5], 1u << (V[r] & 31));
+    }
+    sync();
+    if (hits + m > 0) {
+      // new list: untouched slots in their order, then the touched ones in slot order
+      uint32_t c = 0;
+      for (int jj = j0; jj < j1; ++jj) c += hit(cur[jj]) ? 0u : 1u;
+      uint32_t kept;
+      uint32_t q = block_excl_scan<NT>(c, wsum, &kept, tid, sync);
+      for (int jj = j0; jj < j1; ++jj) {
+        const int s = cur[jj];
+        if (!hit(s) && q < (uint32_t)C) nxt[q++] = s;
+      }
+      const int wper = (nwords + NT - 1) / NT;
+      const int v0 = tid * wper, v1 = min(nwords, v0 + wper);
+      uint32_t tc = 0;
+      for (int w = v0; w < v1; ++w) tc += __popc(bitmap[w]);
+      uint32_t tt;
+      uint32_t o = kept + block_excl_scan<NT>(tc, wsum, &tt, tid, sync);
+      for (int w = v0; w < v1; ++w) {
+        uint32_t bits = bitmap[w];
+        while (bits) {
+          const int b = __ffs(bits) - 1;
+          bits &= bits - 1;
+          if (o < (uint32_t)C) nxt[o++] = w * 32 + b;
+        }
+      }
+      if (tid == 0) a.order_par[u] = par ^ 1;
+    }
+    __threadfence_block();
+    sync();
+    // remap logical top-k positions to physical slots
+    for (int e = tid; e < PK; e += NT) {
+      const int32_t t = tok[e];
+      out_slot[e] = t >= 0 ? cs[t] : -1;
+    }
+  } else {
+    m = 0;
+    for (int e = tid; e < PK; e += NT) out_slot[e] = -1;
+  }
+
+  if (tid == 0) {
+    a.status[i] = status;
+    a.miss_cnt[i] = (int32_t)m;
+    if (a.stats) {
+      if (status == KVO_OK) {
+        atomicAdd(&a.stats->unit_steps, 1ull);
+        atomicAdd(&a.stats->hits, (unsigned long long)hits);
+        atomicAdd(&a.stats->misses, (unsigned long long)m);
+      } else if (status == KVO_ECAPACITY) {
+        atomicAdd(&a.stats->capacity_errors, 1ull);
+      }
+    }
+  }
+  if (status_out) *status_out = status;
+  sync();
+  return m;
+}
+
+}  // namespace dev
+}  // namespace kvo

@@ -20,6 +20,7 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include "kvo_device.cuh"
 #include "kvo_internal.cuh"
 
 namespace kvo {
@@ -30,45 +31,6 @@ constexpr int kResThreads = 1024;
 constexpr int kGatherThreads = 256;
 constexpr int kGatherRows = 32;     // rows per batch (LDG gather)
 constexpr int kBulkDepth = 4;       // rows in flight per warp (bulk gather)
-
-__device__ __forceinline__ uint32_t block_sum_u32(uint32_t v, uint32_t* wsum) {
-  const int lane = threadIdx.x & 31, w = threadIdx.x >> 5, nw = blockDim.x >> 5;
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(kFull, v, o);
-  if (lane == 0) wsum[w] = v;
-  __syncthreads();
-  uint32_t t = 0;
-  for (int x = 0; x < nw; ++x) t += wsum[x];
-  __syncthreads();
-  return t;
-}
-
-// Exclusive block scan of v; *total gets the block sum.
-__device__ __forceinline__ uint32_t block_excl_scan(uint32_t v, uint32_t* wsum, uint32_t* total) {
-  const int lane = threadIdx.x & 31, w = threadIdx.x >> 5, nw = blockDim.x >> 5;
-  uint32_t incl = v;
-#pragma unroll
-  for (int o = 1; o < 32; o <<= 1) {
-    const uint32_t y = __shfl_up_sync(kFull, incl, o);
-    if (lane >= o) incl += y;
-  }
-  if (lane == 31) wsum[w] = incl;
-  __syncthreads();
-  if (w == 0) {
-    uint32_t s = lane < nw ? wsum[lane] : 0;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      const uint32_t y = __shfl_up_sync(kFull, s, o);
-      if (lane >= o) s += y;
-    }
-    if (lane < nw) wsum[lane] = s;
-  }
-  __syncthreads();
-  const uint32_t excl = (w ? wsum[w - 1] : 0) + incl - v;
-  *total = wsum[nw - 1];
-  __syncthreads();
-  return excl;
-}
 
 }  // namespace
 
@@ -85,167 +47,16 @@ __device__ __forceinline__ uint32_t block_excl_scan(uint32_t v, uint32_t* wsum, 
 // ---------------------------------------------------------------------------
 __global__ void __launch_bounds__(kResThreads) residency_kernel(ResidencyArgs a) {
   extern __shared__ __align__(128) uint8_t smem[];
-  const int C = a.C, PK = a.P * a.k;
-  const int nwords = (C + 31) >> 5;
-  const int nwords_pad = (nwords + 3) & ~3;
+  const int PK = a.P * a.k;
+  const int nwords_pad = (((a.C + 31) >> 5) + 3) & ~3;
   uint32_t* bitmap = reinterpret_cast<uint32_t*>(smem);        // [nwords_pad] hit, then touched slots
   int32_t* M = reinterpret_cast<int32_t*>(bitmap + nwords_pad);  // [PK] distinct misses, ascending
   int32_t* V = M + PK;                                          // [PK] victims in LRU order
   __shared__ uint32_t wsum[32];
   __shared__ uint32_t sc[8];
-
   const int tid = threadIdx.x;
-  const int i = blockIdx.x;
-  const int u = a.units[i];
-  const int32_t* tok = a.tok + (int64_t)i * PK;
-  const int32_t* pay = a.pay + (int64_t)i * PK;
-  int32_t* out_slot = a.out_slot + (int64_t)i * PK;
-  int32_t* cs = a.cache_slots + (int64_t)u * a.stride;
-  int32_t* st = a.slot_token + (int64_t)u * C;
-  uint32_t* lu = a.last_use + (int64_t)u * C;
-  uint32_t* tbm = a.tok_bits + (int64_t)u * a.tok_words;
-  const int par = a.order_par[u];
-  const int32_t* cur = a.order + ((int64_t)par * a.U + u) * C;
-  int32_t* nxt = a.order + ((int64_t)(par ^ 1) * a.U + u) * C;
-
-  int32_t status = KVO_OK;
-  uint32_t m = 0, hits = 0;
-  if (*((volatile uint32_t*)a.err) != 0) status = KVO_ETIMEOUT;
-
-  if (status == KVO_OK) {
-    for (int w = tid; w < nwords; w += kResThreads) bitmap[w] = 0;
-    __syncthreads();
-    // payload says hit (slot) or miss (token): mark hit slots and miss tokens
-    for (int e = tid; e < PK; e += kResThreads) {
-      const int32_t t = tok[e];
-      if (t < 0) continue;
-      const int32_t p = pay[e];
-      if (p >= 0) {
-        if (p < C) atomicOr(&bitmap[p >> 5], 1u << (p & 31));
-      } else {
-        atomicOr(&tbm[t >> 5], 1u << (t & 31));
-      }
-    }
-    __syncthreads();
-    // distinct misses in token order; the bitmap words are cleared behind
-    const int tw = (int)((a.len[u] + 31) >> 5);
-    const int per = (tw + kResThreads - 1) / kResThreads;
-    const int w0 = tid * per, w1 = min(tw, w0 + per);
-    uint32_t c = 0;
-    for (int w = w0; w < w1; ++w) c += __popc(__ldcg(&tbm[w]));
-    uint32_t total;
-    uint32_t pos = block_excl_scan(c, wsum, &total);
-    m = total;
-    for (int w = w0; w < w1; ++w) {
-      uint32_t bits = __ldcg(&tbm[w]);
-      if (!bits) continue;
-      tbm[w] = 0;
-      while (bits) {
-        const int b = __ffs(bits) - 1;
-        bits &= bits - 1;
-        if (pos < (uint32_t)PK) M[pos] = w * 32 + b;
-        ++pos;
-      }
-    }
-    uint32_t hc = 0;
-    for (int w = tid; w < nwords; w += kResThreads) hc += __popc(bitmap[w]);
-    hits = block_sum_u32(hc, wsum);
-    if (hits + m > (uint32_t)C) status = KVO_ECAPACITY;
-  }
-
-  if (status == KVO_OK) {
-    const uint32_t stamp = a.stamp[u] + 1;
-    __syncthreads();
-    if (tid == 0) a.stamp[u] = stamp;
-    for (int w = tid; w < nwords; w += kResThreads) {
-      uint32_t bits = bitmap[w];
-      while (bits) {
-        const int b = __ffs(bits) - 1;
-        bits &= bits - 1;
-        lu[w * 32 + b] = stamp;
-      }
-    }
-    const int per = (C + kResThreads - 1) / kResThreads;
-    const int j0 = tid * per, j1 = min(C, j0 + per);
-    // slots outside [0, C) never come from a valid list; they count as touched
-    auto hit = [&](int s) { return (unsigned)s >= (unsigned)C || ((bitmap[s >> 5] >> (s & 31)) & 1u) != 0; };
-    if (m > 0) {
-      // victims: the first m slots of the LRU list that were not hit
-      uint32_t c = 0;
-      for (int j = j0; j < j1; ++j) c += hit(cur[j]) ? 0u : 1u;
-      uint32_t total;
-      uint32_t rank = block_excl_scan(c, wsum, &total);
-      for (int j = j0; j < j1 && rank < m; ++j) {
-        const int s = cur[j];
-        if (!hit(s)) V[rank++] = s;
-      }
-      __syncthreads();
-      // i-th miss (token order) takes the i-th victim
-      for (uint32_t r = tid; r < m; r += kResThreads) {
-        const int s = V[r];
-        const int32_t t = M[r];
-        const int32_t old = st[s];
-        if (old >= 0) cs[old] = -1;
-        st[s] = t;
-        cs[t] = s;
-        lu[s] = stamp;
-        a.miss_tok[(int64_t)i * PK + r] = t;
-        a.miss_slot[(int64_t)i * PK + r] = s;
-      }
-      __syncthreads();
-      for (uint32_t r = tid; r < m; r += kResThreads) atomicOr(&bitmap[V[r] >> 5], 1u << (V[r] & 31));
-    }
-    __syncthreads();
-    if (hits + m > 0) {
-      // new list: untouched slots in their order, then the touched ones in slot order
-      uint32_t c = 0;
-      for (int j = j0; j < j1; ++j) c += hit(cur[j]) ? 0u : 1u;
-      uint32_t kept;
-      uint32_t q = block_excl_scan(c, wsum, &kept);
-      for (int j = j0; j < j1; ++j) {
-        const int s = cur[j];
-        if (!hit(s) && q < (uint32_t)C) nxt[q++] = s;
-      }
-      const int wper = (nwords + kResThreads - 1) / kResThreads;
-      const int v0 = tid * wper, v1 = min(nwords, v0 + wper);
-      uint32_t tc = 0;
-      for (int w = v0; w < v1; ++w) tc += __popc(bitmap[w]);
-      uint32_t tt;
-      uint32_t o = kept + block_excl_scan(tc, wsum, &tt);
-      for (int w = v0; w < v1; ++w) {
-        uint32_t bits = bitmap[w];
-        while (bits) {
-          const int b = __ffs(bits) - 1;
-          bits &= bits - 1;
-          if (o < (uint32_t)C) nxt[o++] = w * 32 + b;
-        }
-      }
-      if (tid == 0) a.order_par[u] = par ^ 1;
-    }
-    __syncthreads();
-    // remap logical top-k positions to physical slots
-    for (int e = tid; e < PK; e += kResThreads) {
-      const int32_t t = tok[e];
-      out_slot[e] = t >= 0 ? cs[t] : -1;
-    }
-  } else {
-    m = 0;
-    for (int e = tid; e < PK; e += kResThreads) out_slot[e] = -1;
-  }
-
-  if (tid == 0) {
-    a.status[i] = status;
-    a.miss_cnt[i] = (int32_t)m;
-    if (a.stats) {
-      if (status == KVO_OK) {
-        atomicAdd(&a.stats->unit_steps, 1ull);
-        atomicAdd(&a.stats->hits, (unsigned long long)hits);
-        atomicAdd(&a.stats->misses, (unsigned long long)m);
-      } else if (status == KVO_ECAPACITY) {
-        atomicAdd(&a.stats->capacity_errors, 1ull);
-      }
-    }
-  }
+  auto sync = [] { __syncthreads(); };
+  dev::residency_body<kResThreads>(a, blockIdx.x, bitmap, M, V, wsum, tid, sync, nullptr);
 
   // the last CTA writes the prefix sums of the miss counts
   __threadfence();
@@ -259,7 +70,7 @@ __global__ void __launch_bounds__(kResThreads) residency_kernel(ResidencyArgs a)
       const int e = base + tid;
       const uint32_t v = e < a.n ? (uint32_t)__ldcg(&a.miss_cnt[e]) : 0u;
       uint32_t total;
-      const uint32_t pos = block_excl_scan(v, wsum, &total);
+      const uint32_t pos = dev::block_excl_scan<kResThreads>(v, wsum, &total, tid, sync);
       if (e < a.n) a.miss_off[e] = carry + pos;
       carry += total;
     }
