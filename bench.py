@@ -287,6 +287,12 @@ def run_kvo(args, log):
     kv.set_option(K.KVO_OPT_GATHER_MODE, K.KVO_GATHER_BULK if args.gather == "bulk" else K.KVO_GATHER_LDG)
     kv.set_option(K.KVO_OPT_GROUPS, args.groups)
     kv.set_option(K.KVO_OPT_SCORE_CTAS, args.score_ctas)
+    kv.set_option(K.KVO_OPT_FUSED, 1 if args.path == "fused" else 0)
+    if args.path == "fused":
+        if args.gather_ctas is not None:
+            kv.set_option(K.KVO_OPT_GATHER_CTAS, args.gather_ctas)
+        if args.piece_tokens is not None:
+            kv.set_option(K.KVO_OPT_PIECE_TOKENS, args.piece_tokens)
     seq = Sequence(kv, inp, wl)
     stream = torch.cuda.current_stream(device)
 
@@ -352,6 +358,24 @@ def run_kvo(args, log):
                                  achieved_gbs=round(a, 1), peak_gbs=round(link["h2d"], 1),
                                  frac=round(a / link["h2d"], 4),
                                  peak_source="measured pinned host->device copy, this run")
+    if "fused" in kernels:
+        # one launch moves both the keys (HBM) and the miss rows (host link):
+        # its bound is whichever takes longer at its peak
+        t = prof["fused"][0] / 1e3
+        hbm_b = score_bytes + bytes_h2d
+        t_hbm, t_link = hbm_b / (hbm_peak * 1e9), bytes_h2d / (link["h2d"] * 1e9)
+        hbm_gbs, link_gbs = hbm_b / t / 1e9, bytes_h2d / t / 1e9
+        if t_link >= t_hbm:
+            kernels["fused"].update(bound="host-link", achieved_gbs=round(link_gbs, 1),
+                                    peak_gbs=round(link["h2d"], 1), frac=round(t_link / t, 4),
+                                    peak_source="measured pinned host->device copy, this run")
+        else:
+            kernels["fused"].update(bound="hbm", achieved_gbs=round(hbm_gbs, 1), peak_gbs=hbm_peak,
+                                    frac=round(t_hbm / t, 4), peak_source=hbm_src)
+        kernels["fused"].update(bytes_per_launch=hbm_b / prof["fused"][1], hbm_gbs=round(hbm_gbs, 1),
+                                host_link_gbs=round(link_gbs, 1),
+                                hbm_frac=round(hbm_gbs / hbm_peak, 4),
+                                host_link_frac=round(link_gbs / link["h2d"], 4))
     if "append" in kernels:
         a = append_bytes / (prof["append"][0] / 1e3) / 1e9
         kernels["append"].update(achieved_gbs=round(a, 1))
@@ -392,14 +416,17 @@ def run_kvo(args, log):
         "config": {"workload": wl.name, "n_requests": wl.n_requests, "n_layers": wl.n_layers,
                    "context": wl.context, "n_pos": P, "n_new": wl.n_new, "topk": k,
                    "hot_capacity": wl.hot_capacity, "drift": wl.drift,
-                   "steps_per_sequence": wl.steps, "gather": args.gather, "groups": args.groups,
+                   "steps_per_sequence": wl.steps, "path": args.path,
+                   "gather": "bulk" if args.path == "fused" else args.gather, "groups": args.groups,
                    "parallelism": "replicas%d" % world,
                    "l2": "inputs larger than L2: %.2f GB of indexer keys read per step"
                          % (score_bytes / n_steps / 1e9)},
         "roofline": roof,
-        "miss_fill": {"gbs": kernels.get("gather", {}).get("achieved_gbs"),
+        "miss_fill": {"gbs": kernels.get("gather", kernels.get("fused", {})).get(
+                          "achieved_gbs" if "gather" in kernels else "host_link_gbs"),
                       "peak_gbs": round(link["h2d"], 1), "rows_per_step": rows_h2d / n_steps,
-                      "frac": kernels.get("gather", {}).get("frac")},
+                      "frac": kernels.get("gather", kernels.get("fused", {})).get(
+                          "frac" if "gather" in kernels else "host_link_frac")},
         "step_roofline": {"hbm_bytes": round(hbm_step), "host_link_bytes": round(host_step),
                           "t_roofline_ms": round(t_roof, 4), "t_measured_ms": round(t_meas, 4),
                           "frac": round(t_roof / t_meas, 4)},
@@ -586,6 +613,10 @@ def main(argv=None):
     ap.add_argument("--groups", type=int, default=1,
                     help="unit groups per step; miss-row copies overlap the next group's scoring")
     ap.add_argument("--score-ctas", type=int, default=0, help="cap on scoring CTAs (0 = one per SM)")
+    ap.add_argument("--path", choices=("fused", "staged"), default="staged",
+                    help="fused: one cooperative launch per step; staged: one launch per stage")
+    ap.add_argument("--gather-ctas", type=int, default=None, help="fused step: CTAs that only fill rows")
+    ap.add_argument("--piece-tokens", type=int, default=None, help="fused step: tokens per piece")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-units", type=int, default=32)

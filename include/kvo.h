@@ -111,6 +111,16 @@ typedef struct kvo_stats {
                                    with threshold (previous step's k-th score) x (query norm
                                    ratio) x v/1000, and a unit whose candidates fall short is
                                    rescored exactly in the same call (default 900) */
+#define KVO_OPT_FUSED 7         /* 1: kvo_step is one cooperative launch that overlaps the scoring of
+                                   some units with the select, residency and miss-row fill of
+                                   others; 0: one launch per stage (default).  KVO_EINVAL for 1
+                                   when the configuration does not fit its shared-memory layout.
+                                   The fused step moves miss rows with bulk async copies and
+                                   ignores KVO_OPT_GATHER_MODE, GROUPS and SCORE_CTAS. */
+#define KVO_OPT_GATHER_CTAS 8   /* fused step: CTAs that only fill miss rows, 0 .. SMs-1 (default 16);
+                                   the others score and join the fill when no piece is left */
+#define KVO_OPT_PIECE_TOKENS 9  /* fused step: tokens per scoring piece, a multiple of 128 in
+                                   [128, 2^20] (default 4096); resizes scratch, synchronous */
 #define KVO_GATHER_LDG 0  /* miss rows read by 16-byte loads from the mapped host pool */
 #define KVO_GATHER_BULK 1 /* miss rows moved by bulk async copies through shared memory */
 
@@ -227,7 +237,8 @@ int kvo_reset(kvo_handle* h, const int32_t* units, int32_t n_units, int64_t keep
 #define KVO_PROF_RESET 6
 #define KVO_PROF_RESCORE 7   /* rescoring pass of units whose speculative threshold was too high */
 #define KVO_PROF_RESELECT 8
-#define KVO_PROF_KINDS 9
+#define KVO_PROF_FUSED 9     /* the fused step launch (KVO_OPT_FUSED) */
+#define KVO_PROF_KINDS 10
 int kvo_profile_read(kvo_handle* h, double* ms, uint64_t* launches, int32_t n_kinds);
 
 /* kvo_set_option: KVO_OPT_* above.  KVO_EINVAL on unknown key or value. */

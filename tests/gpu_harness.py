@@ -26,6 +26,10 @@ def _fill_host_rows(kv, wl, units_rl, unit_ids, t0, n_tok):
                           wl.row_elems)
 
 
+# Options every Runner applies first (the parity tests select the step path here).
+PATH_OPTIONS = {}
+
+
 class Runner:
     """One workload run: GPU handle + oracle replicas of the checked units."""
 
@@ -42,7 +46,7 @@ class Runner:
         self.kv = K.Kvo(wl.n_requests, wl.n_layers, self.tmax, wl.topk, wl.hot_capacity,
                         wl.n_pos, wl.row_elems)
         self.kv.set_option(K.KVO_OPT_GATHER_MODE, gather_mode)
-        for key, value in (options or {}).items():
+        for key, value in {**PATH_OPTIONS, **(options or {})}.items():
             self.kv.set_option(key, value)
         self.keys_fn = keys_fn
         # prefill: rows into the pinned pool, keys into the indexer cache

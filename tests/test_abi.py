@@ -73,3 +73,17 @@ def test_null_handles(L):
     assert L.kvo_step(None, None, 1, None, None, None, None, None, None, None) == kvo.KVO_EINVAL
     assert L.kvo_append(None, None, 1, 1, None, None, None) == kvo.KVO_EINVAL
     assert L.kvo_set_option(None, 1, 0) == kvo.KVO_EINVAL
+
+
+def test_header_constants_match_binding():
+    from top_cache_gb300 import kvo
+    src = open(HEADER).read()
+    defs = dict((m.group(1), int(m.group(2)))
+                for m in re.finditer(r"^#define\s+(KVO_\w+)\s+(-?\d+)", src, flags=re.M))
+    for name, value in defs.items():
+        if name.startswith("KVO_PROF_") and name != "KVO_PROF_KINDS":
+            assert kvo.PROF_KINDS[value] == name[len("KVO_PROF_"):].lower(), name
+        elif name == "KVO_PROF_KINDS":
+            assert len(kvo.PROF_KINDS) == value
+        else:
+            assert getattr(kvo, name) == value, name

@@ -4,7 +4,9 @@ Reduced sizes check every unit at every step (tokens, payloads, slots, status
 bit-exact; scores within 1e-5 relative and, by construction, bit-identical;
 exported residency state and hot rows bit-exact).  The full-size workloads
 run in the launch configuration the benchmark times and check sampled units,
-which the oracle replays one by one.
+which the oracle replays one by one.  Every workload test runs twice: through
+the fused step (one cooperative launch) and through the staged step (one
+launch per stage, the default).
 """
 import numpy as np
 import pytest
@@ -12,6 +14,7 @@ import torch
 
 import oracle
 import workload as W
+from tests import gpu_harness
 from tests.gpu_harness import Runner
 from tests.helpers import int_bf16
 from top_cache_gb300 import kvo as K
@@ -24,6 +27,23 @@ def _built():
     from top_cache_gb300 import build
     build.build()
     yield
+
+
+@pytest.fixture(params=["fused", "staged"], autouse=True)
+def path(request):
+    gpu_harness.PATH_OPTIONS = {K.KVO_OPT_FUSED: 1 if request.param == "fused" else 0}
+    yield request.param
+    gpu_harness.PATH_OPTIONS = {}
+
+
+def _staged_only(path):
+    if path != "staged":
+        pytest.skip("option of the staged step")
+
+
+def _once(path):
+    if path != "fused":
+        pytest.skip("does not depend on the step path")
 
 
 def _run(wl, steps=None, check_state=True, count_rows=True, **kw):
@@ -79,7 +99,8 @@ def test_sweep_reduced(drift):
     _run(wl)
 
 
-def test_bulk_gather_mode():
+def test_bulk_gather_mode(path):
+    _staged_only(path)
     wl = W.reduced(W.WORKLOADS["batch16x8_32k_mtp3"], n_requests=2, n_layers=2, context=3000,
                    topk=256, hot_capacity=600, steps=5)
     _run(wl, gather_mode=K.KVO_GATHER_BULK)
@@ -105,14 +126,16 @@ def test_speculation_without_margin_falls_back_exactly(drift):
 
 
 @pytest.mark.parametrize("groups", [2, 3, 5])
-def test_unit_groups_two_streams(groups):
+def test_unit_groups_two_streams(groups, path):
+    _staged_only(path)
     # the miss-row copy of each group overlaps the next group's scoring
     wl = W.reduced(W.WORKLOADS["batch16x8_32k_mtp3"], n_requests=3, n_layers=2, context=3001,
                    topk=256, hot_capacity=600, steps=5)
     _run(wl, options={K.KVO_OPT_GROUPS: groups})
 
 
-def test_few_score_ctas_long_pieces():
+def test_few_score_ctas_long_pieces(path):
+    _staged_only(path)
     # a cap on scoring CTAs makes each CTA stream long pieces (many compactions)
     wl = W.reduced(W.WORKLOADS["batch16x8_32k_mtp3"], n_requests=1, n_layers=3, context=40000,
                    topk=512, hot_capacity=1024, steps=3)
@@ -189,7 +212,8 @@ def test_empty_and_short_units():
     _run(wl)
 
 
-def test_append_past_max_tokens_rejected():
+def test_append_past_max_tokens_rejected(path):
+    _once(path)
     wl = W.Workload("range", 1, 1, 64, 1, 1, 8, 16, 2, 0.9, 82)
     r = Runner(wl)
     try:
@@ -203,7 +227,8 @@ def test_append_past_max_tokens_rejected():
         r.close()
 
 
-def test_bad_arguments():
+def test_bad_arguments(path):
+    _once(path)
     with pytest.raises(K.KvoError) as e:
         K.kvo_create(1, 1, 100, 64, 32, 1)  # capacity < k
     assert e.value.code == K.KVO_EINVAL
@@ -222,7 +247,8 @@ def test_bad_arguments():
         kv.close()
 
 
-def test_select_stateless():
+def test_select_stateless(path):
+    _once(path)
     n, P, k = 5, 3, 200
     lengths = [0, 150, 3000, 12345, 777]
     stride = 12352
@@ -259,6 +285,49 @@ def test_select_stateless():
         assert np.array_equal(pay[i], exp)
 
 
+# ---------------------------------------------------------------- fused step only
+@pytest.mark.parametrize("piece", [128, 384])
+def test_fused_small_pieces(piece, path):
+    # many pieces per unit: several CTAs share each unit, the piece ring of a
+    # CTA wraps many times, and finishers run while other units still score
+    _once(path)
+    wl = W.reduced(W.WORKLOADS["batch16x8_32k_mtp3"], n_requests=2, n_layers=3, context=6001,
+                   topk=256, hot_capacity=600, steps=5)
+    _run(wl, options={K.KVO_OPT_PIECE_TOKENS: piece})
+
+
+@pytest.mark.parametrize("gather_ctas", [0, 1, -2])
+def test_fused_gather_cta_split(gather_ctas, path):
+    # 0: only scorer CTAs fill rows, after their last piece; -2 (all SMs but
+    # two): two scorer CTAs do every piece while the rest wait for rows
+    _once(path)
+    if gather_ctas < 0:
+        gather_ctas += torch.cuda.get_device_properties(0).multi_processor_count
+    wl = W.reduced(W.WORKLOADS["sweep64x4_16k_mtp3"], n_requests=3, n_layers=2, context=5000,
+                   topk=128, hot_capacity=256, steps=4, drift=0.5)
+    _run(wl, options={K.KVO_OPT_GATHER_CTAS: gather_ctas, K.KVO_OPT_PIECE_TOKENS: 1024})
+
+
+def test_fused_options_validated(path):
+    _once(path)
+    kv = K.Kvo(1, 2, 1000, 16, 64, 2)
+    try:
+        for key, value in ((K.KVO_OPT_PIECE_TOKENS, 100), (K.KVO_OPT_PIECE_TOKENS, 0),
+                           (K.KVO_OPT_FUSED, 2), (K.KVO_OPT_GATHER_CTAS, -1),
+                           (K.KVO_OPT_GATHER_CTAS, 1 << 20)):
+            with pytest.raises(K.KvoError) as e:
+                kv.set_option(key, value)
+            assert e.value.code == K.KVO_EINVAL
+        kv.set_option(K.KVO_OPT_FUSED, 1)
+        kv.set_option(K.KVO_OPT_PROFILE, 1)
+        q = torch.zeros((2, 2, 128), dtype=torch.bfloat16, device="cuda")
+        kv.step(q)
+        prof = kv.profile_read()
+        assert prof["fused"][1] == 1 and prof["score"][1] == 0
+    finally:
+        kv.close()
+
+
 # ---------------------------------------------------------------- full sizes
 def _meminfo_gb():
     try:
@@ -276,7 +345,8 @@ def test_full_batch16x8_mtp3_sampled():
     _run(wl, check_units=[0, 61, 127], count_rows=False)
 
 
-def test_full_batch16x8_mtp3_grouped_sampled():
+def test_full_batch16x8_mtp3_grouped_sampled(path):
+    _staged_only(path)
     wl = W.WORKLOADS["batch16x8_32k_mtp3"]
     _run(wl, steps=20, check_units=[0, 40, 127], count_rows=False, options={K.KVO_OPT_GROUPS: 4})
 

@@ -63,6 +63,23 @@ struct kvo_handle {
   uint64_t host_steps = 0;
   int gather_mode = KVO_GATHER_LDG;
   uint64_t wait_ns = 2000000000ull;
+  // fused step (one cooperative launch per kvo_step)
+  bool fused_ok = false;        // the configuration fits the fused kernel's layout
+  int fused = 0;
+  int gather_ctas = 16;
+  int piece_tokens = 4096;
+  int64_t fseg_pieces = 0;      // pieces the segment buffers hold
+  int64_t* pbeg = nullptr;      // [U+1]
+  int32_t* pdone = nullptr;     // [U]
+  unsigned long long* ctr = nullptr;  // [4]
+  uint64_t* fseg_keys = nullptr;      // [pieces][P][k]
+  int32_t* fseg_cnt = nullptr;        // [pieces][P]
+  int32_t* chunk_unit = nullptr;
+  int32_t* chunk_start = nullptr;
+  int32_t* chunk_cnt = nullptr;
+  uint32_t* chunk_flag = nullptr;
+  int64_t chunk_cap = 0;
+  uint32_t epoch = 0;
   // unit groups: miss-row copies overlap the next group's scoring
   int groups = 1;
   int score_ctas = 0;
@@ -128,7 +145,8 @@ void free_all(kvo_handle* h) {
                  h->all_units, h->units_dev, h->off, h->gthr, h->spec, h->qn_prev, h->qn_cur,
                  h->tspec, h->fb, h->fb_any, h->tok_bits, h->order, h->order_par, h->seg_keys, h->seg_cnt, h->sel_pay,
                  h->miss_tok, h->miss_slot, h->miss_cnt, h->miss_off, h->done_ctr, h->err,
-                 h->stats};
+                 h->stats, h->pbeg, h->pdone, h->ctr, h->fseg_keys, h->fseg_cnt, h->chunk_unit,
+                 h->chunk_start, h->chunk_cnt, h->chunk_flag};
   for (void* p : dev)
     if (p) cudaFree(p);
   if (h->host_pool) cudaFreeHost(h->host_pool);
@@ -140,6 +158,50 @@ size_t residency_smem_bytes(int C, int P, int k) {
 }
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// Whether the fused step's shared-memory layout holds this configuration:
+// the finisher's select and residency reuse the candidate buffers.
+bool fused_fits(int P, int k, int cap, int C) {
+  const size_t region = (size_t)P * cap * 8 + (size_t)k * 8;
+  int kpad = 1;
+  while (kpad < k) kpad <<= 1;
+  return kvo::fused_smem_bytes(P, k, cap) <= 227 * 1024 && residency_smem_bytes(C, P, k) <= region &&
+         (size_t)kpad * 8 + 8 * 256 <= region;
+}
+
+int64_t pieces_of(int64_t len, int piece_tokens) {
+  return len > 0 ? (len + piece_tokens - 1) / piece_tokens : 1;
+}
+
+// (Re)allocates the per-piece candidate segments for the current piece size.
+cudaError_t alloc_fused_segments(kvo_handle* h) {
+  if (h->fseg_keys) cudaFree(h->fseg_keys);
+  if (h->fseg_cnt) cudaFree(h->fseg_cnt);
+  h->fseg_keys = nullptr;
+  h->fseg_cnt = nullptr;
+  h->fseg_pieces = (int64_t)h->U * pieces_of(h->cfg.max_tokens, h->piece_tokens);
+  cudaError_t e = dalloc(&h->fseg_keys, (size_t)h->fseg_pieces * h->P * h->k);
+  if (e == cudaSuccess) e = dalloc(&h->fseg_cnt, (size_t)h->fseg_pieces * h->P);
+  if (e != cudaSuccess) h->fseg_pieces = 0;
+  return e;
+}
+
+cudaError_t alloc_fused(kvo_handle* h) {
+  const size_t U = (size_t)h->U;
+  const int rows = kvo::fused_chunk_rows();
+  h->chunk_cap = (int64_t)U * ((h->P * h->k + rows - 1) / rows);
+  cudaError_t e = dalloc(&h->pbeg, U + 1);
+  if (e == cudaSuccess) e = dalloc(&h->pdone, U);
+  if (e == cudaSuccess) e = dalloc(&h->ctr, 4);
+  if (e == cudaSuccess) e = dalloc(&h->chunk_unit, (size_t)h->chunk_cap);
+  if (e == cudaSuccess) e = dalloc(&h->chunk_start, (size_t)h->chunk_cap);
+  if (e == cudaSuccess) e = dalloc(&h->chunk_cnt, (size_t)h->chunk_cap);
+  if (e == cudaSuccess) e = dalloc(&h->chunk_flag, (size_t)h->chunk_cap);
+  if (e == cudaSuccess) e = cudaMemset(h->chunk_flag, 0, (size_t)h->chunk_cap * 4);
+  if (e == cudaSuccess) e = cudaMemset(h->ctr, 0, 4 * 8);
+  if (e == cudaSuccess) e = alloc_fused_segments(h);
+  return e;
+}
 
 // Resolve the unit list of a call: NULL = all; else validate and upload.
 int resolve_units(kvo_handle* h, const int32_t* units, int32_t n_units, cudaStream_t s,
@@ -198,6 +260,116 @@ int grid_for(int64_t T, int G_max) {
   if (g < 1) g = 1;
   if (g > G_max) g = G_max;
   return (int)g;
+}
+
+// kvo_step as one fused launch (after the plan kernel).
+int fused_step(kvo_handle* h, const int32_t* du, const int32_t* units, int32_t n_units, const void* queries,
+               int32_t* topk_tokens, int32_t* topk_slots, float* topk_scores, int32_t* topk_payload,
+               int32_t* unit_status, cudaStream_t s) {
+  const int PK = h->P * h->k;
+  int64_t T = 0, NP = 0;
+  for (int32_t i = 0; i < n_units; ++i) {
+    const int64_t L = h->len_host[(size_t)(units ? units[i] : i)];
+    T += L;
+    NP += pieces_of(L, h->piece_tokens);
+  }
+  if (NP > h->fseg_pieces) return fail(KVO_EINVAL, "more pieces than the segment buffers hold");
+  kvo::FusedArgs f{};
+  kvo::SelectArgs& sa = f.s;
+  sa.keys = h->idx;
+  sa.stride = h->stride;
+  sa.units = du;
+  sa.len = h->len;
+  sa.queries = static_cast<const uint16_t*>(queries);
+  sa.cache_slots = h->cache_slots;
+  sa.n = n_units;
+  sa.P = h->P;
+  sa.k = h->k;
+  sa.cap = h->cap;
+  sa.T = T;
+  sa.G = 1;
+  sa.off = h->off;
+  sa.gthr = h->gthr;
+  sa.seg_keys = h->fseg_keys;
+  sa.seg_cnt = h->fseg_cnt;
+  sa.out_tok = topk_tokens;
+  sa.out_score = topk_scores;
+  sa.out_pay = h->sel_pay;
+  sa.out_pay_user = topk_payload;
+  sa.err = h->err;
+  sa.stats = h->stats;
+  sa.wait_ns = h->wait_ns;
+  sa.spec = h->spec;
+  sa.qn_prev = h->qn_prev;
+  sa.qn_cur = h->qn_cur;
+  sa.tspec = h->tspec;
+  sa.spec_scale = h->speculate > 0 ? (float)h->speculate / 1000.f : 0.f;
+  sa.fallback = 0;
+  sa.pbeg = h->pbeg;
+  sa.pdone = h->pdone;
+  sa.ctr = h->ctr;
+  sa.status_init = unit_status;
+  sa.piece_tokens = h->piece_tokens;
+  sa.n_pieces = NP;
+
+  kvo::ResidencyArgs& ra = f.r;
+  ra.units = du;
+  ra.n = n_units;
+  ra.P = h->P;
+  ra.k = h->k;
+  ra.C = h->C;
+  ra.stride = h->stride;
+  ra.tok = topk_tokens;
+  ra.pay = h->sel_pay;
+  ra.cache_slots = h->cache_slots;
+  ra.slot_token = h->slot_token;
+  ra.last_use = h->last_use;
+  ra.stamp = h->stamp;
+  ra.out_slot = topk_slots;
+  ra.status = unit_status;
+  ra.miss_tok = h->miss_tok;
+  ra.miss_slot = h->miss_slot;
+  ra.miss_cnt = h->miss_cnt;
+  ra.err = h->err;
+  ra.stats = h->stats;
+  ra.len = h->len;
+  ra.tok_bits = h->tok_bits;
+  ra.tok_words = h->tok_words;
+  ra.order = h->order;
+  ra.order_par = h->order_par;
+  ra.U = h->U;
+
+  kvo::GatherArgs& ga = f.g;
+  ga.units = du;
+  ga.n = n_units;
+  ga.row_elems = h->R;
+  ga.C = h->C;
+  ga.mode = KVO_GATHER_BULK;
+  ga.stride = h->stride;
+  ga.host_pool = h->host_pool_dev;
+  ga.hot = h->hot;
+  ga.miss_tok = h->miss_tok;
+  ga.miss_slot = h->miss_slot;
+  ga.pk = PK;
+  ga.stats = h->stats;
+  ga.err = h->err;
+  ga.wait_ns = h->wait_ns;
+
+  f.chunk_unit = h->chunk_unit;
+  f.chunk_start = h->chunk_start;
+  f.chunk_cnt = h->chunk_cnt;
+  f.chunk_flag = h->chunk_flag;
+  f.chunk_cap = h->chunk_cap;
+  if (++h->epoch == 0) ++h->epoch;  // 0 marks a never-written chunk
+  f.epoch = h->epoch;
+  f.n_gather = h->gather_ctas < h->n_sm ? h->gather_ctas : h->n_sm - 1;
+  f.smem_bytes = (int)kvo::fused_smem_bytes(h->P, h->k, h->cap);
+
+  cudaError_t e = timed(h, KVO_PROF_PLAN, s, [&] { return kvo::launch_plan(sa, s); });
+  if (e == cudaSuccess) e = timed(h, KVO_PROF_FUSED, s, [&] { return kvo::launch_fused(f, h->n_sm, s); });
+  if (e != cudaSuccess) return cuda_fail(e, "fused step launch");
+  ++h->host_steps;
+  return KVO_OK;
 }
 
 }  // namespace
@@ -296,6 +468,9 @@ int kvo_create(const kvo_config* cfg, kvo_handle** out) {
   for (int g = 0; g < 16 && e == cudaSuccess; ++g) e = cudaEventCreateWithFlags(&h->ev_group[g], cudaEventDisableTiming);
   if (e == cudaSuccess) e = dalloc(&h->err, 1);
   if (e == cudaSuccess) e = dalloc(&h->stats, 1);
+  h->fused_ok = fused_fits(h->P, h->k, h->cap, h->C);
+  if (e == cudaSuccess && h->fused_ok) e = alloc_fused(h);
+  if (h->gather_ctas > h->n_sm - 1) h->gather_ctas = h->n_sm - 1;
   if (e != cudaSuccess) {
     free_all(h);
     delete h;
@@ -414,6 +589,8 @@ int kvo_step(kvo_handle* h, const int32_t* units, int32_t n_units, const void* q
   const int32_t* du = nullptr;
   int rc = resolve_units(h, units, n_units, s, &du);
   if (rc != KVO_OK) return rc;
+  if (h->fused) return fused_step(h, du, units, n_units, queries, topk_tokens, topk_slots, topk_scores,
+                                  topk_payload, unit_status, s);
   const int PK = h->P * h->k;
   int NG = h->groups < n_units ? h->groups : n_units;
   if (NG < 1) NG = 1;
@@ -644,6 +821,26 @@ int kvo_set_option(kvo_handle* h, int32_t key, int64_t value) {
       if (value < 0 || value > 1000) return fail(KVO_EINVAL, "speculate must be in [0, 1000]");
       h->speculate = (int)value;
       return KVO_OK;
+    case KVO_OPT_FUSED:
+      if (value != 0 && value != 1) return fail(KVO_EINVAL, "fused is 0 or 1");
+      if (value == 1 && !h->fused_ok) return fail(KVO_EINVAL, "configuration does not fit the fused step");
+      h->fused = (int)value;
+      return KVO_OK;
+    case KVO_OPT_GATHER_CTAS:
+      if (value < 0 || value > h->n_sm - 1) return fail(KVO_EINVAL, "gather_ctas must be in [0, SMs-1]");
+      h->gather_ctas = (int)value;
+      return KVO_OK;
+    case KVO_OPT_PIECE_TOKENS: {
+      if (value < kvo::kDim || value > (1 << 20) || value % 128) return fail(KVO_EINVAL, "bad piece_tokens");
+      if (!h->fused_ok) return fail(KVO_EINVAL, "configuration does not fit the fused step");
+      DeviceGuard guard(h->device);
+      cudaError_t e = cudaDeviceSynchronize();
+      if (e != cudaSuccess) return cuda_fail(e, "piece_tokens");
+      h->piece_tokens = (int)value;
+      e = alloc_fused_segments(h);
+      if (e != cudaSuccess) return fail(KVO_ENOMEM, std::string("piece segments: ") + cudaGetErrorString(e));
+      return KVO_OK;
+    }
     case KVO_OPT_WAIT_LIMIT_NS:
       if (value < 1000) return fail(KVO_EINVAL, "wait limit below 1 us");
       h->wait_ns = (uint64_t)value;

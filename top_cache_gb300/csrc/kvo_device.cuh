@@ -402,7 +402,7 @@ struct Scorer {
   static constexpr int LPP = PP == 1 ? 0 : PP == 2 ? 1 : PP == 4 ? 2 : 3;
   static constexpr int PH = PP >= 2 ? PP / 2 : 1;  // position pairs (packed fp32x2 FMA)
 
-  int lane, j, X, px;
+  int lane, j, X, px, tx, rowbase;
   bool owner;
   int rowoff[4];
   int rrow[VL], rpos[VL];
@@ -419,11 +419,12 @@ struct Scorer {
     const int h = lane >> 4;
     j = lane & 15;
     X = tree_perm<V>(lane);
-    const int tx = X >> LPP;
+    tx = X >> LPP;
     px = X & (PP - 1);
     owner = tree_owner<V>(lane);
+    rowbase = warp * 8 + h * 4;
 #pragma unroll
-    for (int tau = 0; tau < 4; ++tau) rowoff[tau] = (warp * 8 + h * 4 + (tau ^ tx)) * kKeyBytes + j * 16;
+    for (int tau = 0; tau < 4; ++tau) rowoff[tau] = (rowbase + (tau ^ tx)) * kKeyBytes + j * 16;
 #pragma unroll
     for (int r = 0; r < VL; ++r) {
       const int cmb = r ^ X;
@@ -465,9 +466,23 @@ struct Scorer {
   // memory); release() is called once the tile's memory is no longer read.
   template <class Release>
   __device__ __forceinline__ void score(const uint8_t* tile, float (&acc)[V], Release release) {
+    score_rows(tile, acc, release, [&](int tau) { return rowoff[tau]; });
+  }
+
+  // Same for a tile in global memory with nt rows: rows past the end read the
+  // last row instead (their results are discarded by filter()).
+  __device__ __forceinline__ void score_global(const uint8_t* tile, int nt, float (&acc)[V]) {
+    score_rows(tile, acc, [] {}, [&](int tau) {
+      const int r = rowbase + (tau ^ tx);
+      return (r < nt ? r : nt - 1) * kKeyBytes + j * 16;
+    });
+  }
+
+  template <class Release, class Off>
+  __device__ __forceinline__ void score_rows(const uint8_t* tile, float (&acc)[V], Release release, Off off) {
 #pragma unroll
     for (int tau = 0; tau < 4; ++tau) {
-      const uint4 kv = *reinterpret_cast<const uint4*>(tile + rowoff[tau]);
+      const uint4 kv = *reinterpret_cast<const uint4*>(tile + off(tau));
       const float kf[8] = {bf_lo(kv.x), bf_hi(kv.x), bf_lo(kv.y), bf_hi(kv.y),
                            bf_lo(kv.z), bf_hi(kv.z), bf_lo(kv.w), bf_hi(kv.w)};
       if constexpr (PP >= 2) {
@@ -559,14 +574,15 @@ __device__ __forceinline__ void piece_check(const ScoreSmem& sm, int P, int k, i
   }
 }
 
-// End of a piece: at most k candidates per position, all above the shared
-// threshold, written to segment `seg`.
+// End of a piece: at most k candidates per position, written to segment `seg`.
 __device__ __forceinline__ void piece_end(const ScoreSmem& sm, int P, int k, int cap, uint64_t* gth, int64_t seg,
                                           uint64_t* seg_keys, int32_t* seg_cnt, int ctid) {
   consumer_sync();
+  // at most k per position; keys under the shared threshold may stay (select drops them)
   for (int p = 0; p < P; ++p)
-    compact_candidates(sm.cand + (size_t)p * cap, &sm.cnt[p], &sm.thr[p], gth + p, sm.fl, sm.scratch, sm.hist, sm.rx,
-                       k, ctid);
+    if (sm.cnt[p] > (uint32_t)k)
+      compact_candidates(sm.cand + (size_t)p * cap, &sm.cnt[p], &sm.thr[p], gth + p, sm.fl, sm.scratch, sm.hist,
+                         sm.rx, k, ctid);
   for (int p = 0; p < P; ++p) {
     const uint32_t np = sm.cnt[p];
     uint64_t* dst = seg_keys + (seg * P + p) * (int64_t)k;
@@ -578,18 +594,22 @@ __device__ __forceinline__ void piece_end(const ScoreSmem& sm, int P, int k, int
 
 // ---------------------------------------------------------------------------
 // Exact top-k of one (unit i, position p) over segments [seg0, seg0 + nseg)
-// (NT = kSelThreads threads).  Returns false when the speculative threshold
-// of (i, p) was too high (then nothing is written).
-// keys: kSelSmemKeys u64, sorted: kpad u64, hist[256], rx[10] (8-aligned).
+// with NT threads.  Returns false when the speculative threshold of (i, p)
+// was too high (then nothing is written).  Shared memory: keys (keycap u64;
+// more candidates than that are read from global memory instead), sorted
+// (kpad u64, kpad = k rounded up to a power of two), hist[256], rx[10]
+// (8-byte aligned).
 // ---------------------------------------------------------------------------
 template <int NT, class Sync>
 __device__ __forceinline__ bool select_body(const SelectArgs& a, int i, int p, int64_t seg0, int nseg,
-                                            bool verify, uint64_t* keys, uint64_t* sorted, uint32_t* hist,
-                                            uint32_t* rx, int tid, Sync sync) {
+                                            bool verify, uint64_t* keys, uint32_t keycap, uint64_t* sorted,
+                                            uint32_t* hist, uint32_t* rx, int tid, Sync sync) {
   const int P = a.P, k = a.k;
   const int64_t s0 = a.off[i], s1 = a.off[i + 1];
+  // segments may have been written by other CTAs of the same launch: read through L2
+  auto seg_count = [&](int64_t seg) { return (uint32_t)__ldcg(&a.seg_cnt[seg * P + p]); };
   uint32_t n = 0;
-  for (int c = 0; c < nseg; ++c) n += (uint32_t)a.seg_cnt[(seg0 + c) * P + p];
+  for (int c = 0; c < nseg; ++c) n += seg_count(seg0 + c);
   // A speculative threshold is exact when at least min(k, visible) keys
   // reached it: then every key of the top k did.
   if (verify && a.tspec && a.tspec[(int64_t)i * P + p] != 0) {
@@ -597,14 +617,14 @@ __device__ __forceinline__ bool select_body(const SelectArgs& a, int i, int p, i
     const uint32_t need = (uint32_t)(vis < k ? (vis > 0 ? vis : 0) : k);
     if (n < need) return false;
   }
-  const bool in_smem = n <= (uint32_t)kSelSmemKeys;
+  const bool in_smem = n <= keycap;
   if (in_smem) {
     uint32_t base = 0;
     for (int c = 0; c < nseg; ++c) {
       const int64_t seg = seg0 + c;
-      const uint32_t m = (uint32_t)a.seg_cnt[seg * P + p];
+      const uint32_t m = seg_count(seg);
       const uint64_t* src = a.seg_keys + (seg * P + p) * (int64_t)k;
-      for (uint32_t e = tid; e < m; e += NT) keys[base + e] = src[e];
+      for (uint32_t e = tid; e < m; e += NT) keys[base + e] = __ldcg(src + e);
       base += m;
     }
     sync();
@@ -615,9 +635,9 @@ __device__ __forceinline__ bool select_body(const SelectArgs& a, int i, int p, i
     } else {
       for (int c = 0; c < nseg; ++c) {
         const int64_t seg = seg0 + c;
-        const uint32_t m = (uint32_t)a.seg_cnt[seg * P + p];
+        const uint32_t m = seg_count(seg);
         const uint64_t* src = a.seg_keys + (seg * P + p) * (int64_t)k;
-        for (uint32_t e = tid; e < m; e += NT) f(src[e]);
+        for (uint32_t e = tid; e < m; e += NT) f(__ldcg(src + e));
       }
     }
   };
@@ -630,10 +650,11 @@ __device__ __forceinline__ bool select_body(const SelectArgs& a, int i, int p, i
   sync();
   const int lane = tid & 31;
   // keys >= thr go to the sort buffer (uniform trip counts: full-warp ballots)
-  auto keep_from = [&](const uint64_t* src, uint32_t m) {
+  // src is shared memory (from_global false) or a segment in global memory
+  auto keep_from = [&](const uint64_t* src, uint32_t m, bool from_global) {
     for (uint32_t b = 0; b < m; b += NT) {
       const uint32_t e = b + tid;
-      const uint64_t key = e < m ? src[e] : 0;
+      const uint64_t key = e < m ? (from_global ? __ldcg(src + e) : src[e]) : 0;
       const bool keep = e < m && key >= thr;
       const uint32_t msk = __ballot_sync(kFull, keep);
       if (msk) {
@@ -646,11 +667,11 @@ __device__ __forceinline__ bool select_body(const SelectArgs& a, int i, int p, i
     }
   };
   if (in_smem) {
-    keep_from(keys, n);
+    keep_from(keys, n, false);
   } else {
     for (int c = 0; c < nseg; ++c) {
       const int64_t seg = seg0 + c;
-      keep_from(a.seg_keys + (seg * P + p) * (int64_t)k, (uint32_t)a.seg_cnt[seg * P + p]);
+      keep_from(a.seg_keys + (seg * P + p) * (int64_t)k, seg_count(seg), true);
     }
   }
   sync();
@@ -714,9 +735,11 @@ __device__ __forceinline__ uint32_t residency_body(const ResidencyArgs& a, int i
   const int32_t* cur = a.order + ((int64_t)par * a.U + u) * C;
   int32_t* nxt = a.order + ((int64_t)(par ^ 1) * a.U + u) * C;
 
-  int32_t status = KVO_OK;
+  // the error word can change under a concurrent launch: one read, shared
+  if (tid == 0) wsum[0] = *((volatile uint32_t*)a.err);
+  sync();
+  int32_t status = wsum[0] != 0 ? KVO_ETIMEOUT : KVO_OK;
   uint32_t m = 0, hits = 0;
-  if (*((volatile uint32_t*)a.err) != 0) status = KVO_ETIMEOUT;
 
   if (status == KVO_OK) {
     for (int w = tid; w < nwords; w += NT) bitmap[w] = 0;

@@ -59,6 +59,9 @@ __device__ __forceinline__ uint64_t global_ns() {
 __device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
   asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count) : "memory");
 }
+__device__ __forceinline__ void mbar_inval(uint64_t* bar) {
+  asm volatile("mbarrier.inval.shared::cta.b64 [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
 __device__ __forceinline__ void fence_mbar_init() {
   asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
 }
@@ -178,6 +181,16 @@ struct SelectArgs {
   uint32_t* fb_any;
   float spec_scale;            // threshold = previous k-th score * norm ratio * spec_scale
   int32_t fallback;            // 1: rescoring pass over the flagged units, no speculation
+  // Fused step only (all nullable: off).  Unit i's tokens are cut into
+  // max(1, ceil(len / piece_tokens)) pieces numbered unit-major from pbeg[i];
+  // plan writes pbeg, zeroes pdone and the work counters, and marks every
+  // status KVO_ETIMEOUT until the unit's finisher overwrites it.
+  int64_t* pbeg;               // [n+1]
+  int32_t* pdone;              // [n] pieces of the unit completed
+  unsigned long long* ctr;     // [4] work counters of the fused step
+  int32_t* status_init;        // [n]
+  int32_t piece_tokens;        // multiple of the 128-token tile
+  int64_t n_pieces;            // pbeg[n], checked by plan
 };
 
 struct ResidencyArgs {
@@ -249,6 +262,22 @@ struct ResetArgs {
   int32_t* len;
 };
 
+// One fused launch of the decode step: scoring, select, residency and the
+// miss-row fill of every listed unit, overlapped across units.
+struct FusedArgs {
+  SelectArgs s;                // pbeg, pdone, ctr, status_init set
+  ResidencyArgs r;             // miss_off / done_ctr unused
+  GatherArgs g;                // miss_off unused
+  int32_t* chunk_unit;         // [chunk_cap] published gather work: listed unit index,
+  int32_t* chunk_start;        //   first row in the unit's miss list,
+  int32_t* chunk_cnt;          //   row count,
+  uint32_t* chunk_flag;        //   == epoch once the entry is valid
+  int64_t chunk_cap;
+  uint32_t epoch;              // differs between consecutive launches
+  int32_t n_gather;            // CTAs 0 .. n_gather-1 only fill miss rows
+  int32_t smem_bytes;          // dynamic shared memory of one CTA
+};
+
 // Sets the thread-local message returned by kvo_last_error().
 void set_last_error(const char* msg);
 
@@ -264,5 +293,8 @@ cudaError_t launch_reset(const ResetArgs& a, cudaStream_t s);
 cudaError_t launch_order_init(int32_t* order, int32_t* par, int U, int C, cudaStream_t s);
 cudaError_t launch_set_len(int32_t* len, int32_t unit, int32_t value, cudaStream_t s);
 cudaError_t launch_fill_i32(int32_t* p, int32_t v, size_t n, cudaStream_t s);
+size_t fused_smem_bytes(int P, int k, int cap);
+int fused_chunk_rows();
+cudaError_t launch_fused(const FusedArgs& a, int grid, cudaStream_t s);
 
 }  // namespace kvo

@@ -149,6 +149,52 @@ __global__ void __launch_bounds__(1024) plan_kernel(SelectArgs a) {
     a.off[a.n] = carry;
     if (carry != a.T) atomicOr(a.err, kErrPlan);
   }
+  if (a.pbeg) {
+    // pieces of the fused step: unit i owns max(1, ceil(len / piece_tokens)) of them
+    __syncthreads();
+    if (tid == 0) carry = 0;
+    __syncthreads();
+    for (int base = 0; base < a.n; base += 1024) {
+      const int i = base + tid;
+      int64_t v = 0;
+      if (i < a.n) {
+        const int64_t L = a.len[a.units[i]];
+        v = L > 0 ? (L + a.piece_tokens - 1) / a.piece_tokens : 1;
+      }
+      int64_t incl = v;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int64_t y = __shfl_up_sync(kFull, incl, o);
+        if (lane >= o) incl += y;
+      }
+      if (lane == 31) warp_sums[w] = incl;
+      __syncthreads();
+      if (w == 0) {
+        int64_t s = warp_sums[lane];
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+          const int64_t y = __shfl_up_sync(kFull, s, o);
+          if (lane >= o) s += y;
+        }
+        warp_sums[lane] = s;
+      }
+      __syncthreads();
+      const int64_t excl = carry + (w ? warp_sums[w - 1] : 0) + incl - v;
+      if (i < a.n) a.pbeg[i] = excl;
+      __syncthreads();
+      if (tid == 1023) carry = excl + v;
+      __syncthreads();
+    }
+    for (int i = tid; i < a.n; i += 1024) {
+      a.pdone[i] = 0;
+      a.status_init[i] = KVO_ETIMEOUT;
+    }
+    if (tid < 4) a.ctr[tid] = 0ull;
+    if (tid == 0) {
+      a.pbeg[a.n] = carry;
+      if (carry != a.n_pieces) atomicOr(a.err, kErrPlan);
+    }
+  }
 }
 
 // ---------------------------------------------------------------------------
@@ -259,8 +305,8 @@ __global__ void __launch_bounds__(kSelThreads) select_kernel(SelectArgs a) {
     c1 = cta_of(s1 - 1, a.T, a.G);
   }
   // A failed speculative threshold sends the unit to the rescoring pass.
-  if (!select_body<kSelThreads>(a, i, p, (int64_t)c0 + i, c1 - c0 + 1, !a.fallback, keys, sorted, hist, rx, tid,
-                                [] { __syncthreads(); })) {
+  if (!select_body<kSelThreads>(a, i, p, (int64_t)c0 + i, c1 - c0 + 1, !a.fallback, keys, kSelSmemKeys, sorted,
+                                hist, rx, tid, [] { __syncthreads(); })) {
     if (tid == 0) {
       a.fb[i] = 1;
       atomicExch(a.fb_any, 1u);

@@ -29,8 +29,11 @@ KVO_OPT_PROFILE = 3
 KVO_OPT_GROUPS = 4
 KVO_OPT_SCORE_CTAS = 5
 KVO_OPT_SPECULATE = 6
+KVO_OPT_FUSED = 7
+KVO_OPT_GATHER_CTAS = 8
+KVO_OPT_PIECE_TOKENS = 9
 PROF_KINDS = ("append", "plan", "score", "select", "residency", "gather", "reset", "rescore",
-              "reselect")
+              "reselect", "fused")
 KVO_GATHER_LDG = 0
 KVO_GATHER_BULK = 1
 
