@@ -169,17 +169,17 @@ bool fused_fits(int P, int k, int cap, int C) {
          (size_t)kpad * 8 + 8 * 256 <= region;
 }
 
-int64_t pieces_of(int64_t len, int piece_tokens) {
-  return len > 0 ? (len + piece_tokens - 1) / piece_tokens : 1;
-}
-
 // (Re)allocates the per-piece candidate segments for the current piece size.
 cudaError_t alloc_fused_segments(kvo_handle* h) {
   if (h->fseg_keys) cudaFree(h->fseg_keys);
   if (h->fseg_cnt) cudaFree(h->fseg_cnt);
   h->fseg_keys = nullptr;
   h->fseg_cnt = nullptr;
-  h->fseg_pieces = (int64_t)h->U * pieces_of(h->cfg.max_tokens, h->piece_tokens);
+  // every unit at the full piece size, plus the finer pieces of the first units
+  const int64_t small = kvo::kSmallPieceUnits < h->U ? kvo::kSmallPieceUnits : h->U;
+  const int64_t lmax = h->cfg.max_tokens, lsmall = lmax < kvo::kSmallPieceMaxLen ? lmax : kvo::kSmallPieceMaxLen;
+  h->fseg_pieces = (int64_t)h->U * kvo::pieces_of(h->U, lmax, h->piece_tokens) +
+                   small * kvo::pieces_of(0, lsmall, h->piece_tokens);
   cudaError_t e = dalloc(&h->fseg_keys, (size_t)h->fseg_pieces * h->P * h->k);
   if (e == cudaSuccess) e = dalloc(&h->fseg_cnt, (size_t)h->fseg_pieces * h->P);
   if (e != cudaSuccess) h->fseg_pieces = 0;
@@ -271,7 +271,7 @@ int fused_step(kvo_handle* h, const int32_t* du, const int32_t* units, int32_t n
   for (int32_t i = 0; i < n_units; ++i) {
     const int64_t L = h->len_host[(size_t)(units ? units[i] : i)];
     T += L;
-    NP += pieces_of(L, h->piece_tokens);
+    NP += kvo::pieces_of(i, L, h->piece_tokens);
   }
   if (NP > h->fseg_pieces) return fail(KVO_EINVAL, "more pieces than the segment buffers hold");
   kvo::FusedArgs f{};

@@ -25,7 +25,11 @@ constexpr int kScoreThreads = kCT + 32;     // + one producer warp
 constexpr int kCheckTiles = 8;              // tiles between candidate-buffer checks
 constexpr int kSmemMax = 222 * 1024;        // leaves room for a co-resident copy CTA
 constexpr int kSelThreads = 512;
-constexpr int kSelSmemKeys = 8192;          // candidates held in shared memory by select
+constexpr int kSelSmemKeys = 8192;          // candidates held in shared memory by select (fallback)
+constexpr int kSelBucketKeys = 4096;        // candidates the bucket sort of the select kernel holds
+constexpr int kSelLog2B = 12;               // its buckets
+constexpr int kSelMaxSegs = 512;            // segments whose offsets the select kernel holds
+constexpr int kSelSmemBytes = 2 * kSelBucketKeys * 8 + 2 * (1 << kSelLog2B) * 4 + 32;
 constexpr int kMaxK = 4096;
 
 __device__ __forceinline__ void consumer_sync() { named_sync(1, kCT); }
@@ -592,6 +596,99 @@ __device__ __forceinline__ void piece_end(const ScoreSmem& sm, int P, int k, int
   consumer_sync();
 }
 
+// Candidates of (unit i, position p) over segments [seg0, seg0 + nseg).
+// Segments may have been written by other CTAs of the same launch: read
+// through L2.
+__device__ __forceinline__ uint32_t candidate_count(const SelectArgs& a, int p, int64_t seg0, int nseg) {
+  uint32_t n = 0;
+  for (int c = 0; c < nseg; ++c) n += (uint32_t)__ldcg(&a.seg_cnt[(seg0 + c) * a.P + p]);
+  return n;
+}
+
+// Whether the speculative threshold of (unit i, position p) was too high.  It
+// is exact when at least min(k, visible) keys reached it: then every key of
+// the top k did.
+__device__ __forceinline__ bool spec_short(const SelectArgs& a, int i, int p, uint32_t n) {
+  if (!a.tspec || a.tspec[(int64_t)i * a.P + p] == 0) return false;
+  const int64_t vis = (a.off[i + 1] - a.off[i]) - (a.P - 1 - p);
+  const uint32_t need = (uint32_t)(vis < a.k ? (vis > 0 ? vis : 0) : a.k);
+  return n < need;
+}
+
+// For positions p0 .. p0+np-1 (warp w handles p0 + w; np <= NT / 32):
+// seg_off[w * (nseg + 1) + c] = candidates of (., p0 + w) in segments
+// seg0 .. seg0+c-1, c <= nseg; one load per lane per 32 segments.
+template <int NT, class Sync>
+__device__ __forceinline__ void segment_offsets(const SelectArgs& a, int p0, int np, int64_t seg0, int nseg,
+                                                uint32_t* seg_off, int tid, Sync sync) {
+  const int w = tid >> 5, lane = tid & 31;
+  if (w < np) {
+    const int p = p0 + w;
+    uint32_t* so = seg_off + w * (nseg + 1);
+    uint32_t carry = 0;
+    for (int b = 0; b < nseg; b += 32) {
+      const int c = b + lane;
+      const uint32_t v = c < nseg ? (uint32_t)__ldcg(&a.seg_cnt[(seg0 + c) * a.P + p]) : 0u;
+      uint32_t incl = v;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const uint32_t y = __shfl_up_sync(kFull, incl, o);
+        if (lane >= o) incl += y;
+      }
+      if (c < nseg) so[c] = carry + incl - v;
+      carry += __shfl_sync(kFull, incl, 31);
+    }
+    if (lane == 0) so[nseg] = carry;
+  }
+  sync();
+}
+
+// Writes ranks [0, k) of (unit i, position p) from W[0 .. count) (winners in
+// rank order, shared memory), padding after; four payload lookups in flight
+// per thread.
+template <int NT>
+__device__ __forceinline__ void write_ranks(const SelectArgs& a, int i, int p, const uint64_t* W, int count,
+                                            int tid) {
+  const int k = a.k;
+  const int64_t ob = ((int64_t)i * a.P + p) * k;
+  const int32_t* cs = a.cache_slots ? a.cache_slots + (int64_t)a.units[i] * a.stride : nullptr;
+  for (int r0 = tid; r0 < k; r0 += 4 * NT) {
+    uint64_t key[4];
+    int32_t slot[4];
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const int r = r0 + u * NT;
+      key[u] = r < count ? W[r] : 0ull;
+      slot[u] = (r < count && cs) ? cs[key_token(key[u])] : -1;
+    }
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const int r = r0 + u * NT;
+      if (r >= k) break;
+      int32_t tok = -1, pay = KVO_PAD_PAYLOAD;
+      float sc = __uint_as_float(0xff800000u);
+      if (r < count) {
+        tok = (int32_t)key_token(key[u]);
+        sc = key_score(key[u]);
+        pay = slot[u] >= 0 ? slot[u] : -(tok + 1);
+      }
+      a.out_tok[ob + r] = tok;
+      if (a.out_score) a.out_score[ob + r] = sc;
+      a.out_pay[ob + r] = pay;
+      if (a.out_pay_user && a.out_pay_user != a.out_pay) a.out_pay_user[ob + r] = pay;
+    }
+  }
+}
+
+// State the next step's speculative threshold starts from: the k-th best key
+// (0 when fewer than k tokens were visible) and this step's query norm.
+__device__ __forceinline__ void write_spec(const SelectArgs& a, int i, int p, uint64_t kth) {
+  if (!a.spec) return;
+  const int u = a.units[i];
+  a.spec[(int64_t)u * a.P + p] = kth;
+  if (a.qn_prev && a.qn_cur) a.qn_prev[(int64_t)u * a.P + p] = a.qn_cur[(int64_t)i * a.P + p];
+}
+
 // ---------------------------------------------------------------------------
 // Exact top-k of one (unit i, position p) over segments [seg0, seg0 + nseg)
 // with NT threads.  Returns false when the speculative threshold of (i, p)
@@ -679,27 +776,143 @@ __device__ __forceinline__ bool select_body(const SelectArgs& a, int i, int p, i
   sync();
   block_sort_desc<NT>(sorted, kpad, tid, sync);
 
-  const int u = a.units[i];
-  const int64_t obase = ((int64_t)i * P + p) * k;
-  for (int r = tid; r < k; r += NT) {
-    int32_t tok = -1, pay = KVO_PAD_PAYLOAD;
-    float sc = __uint_as_float(0xff800000u);
-    if (r < (int)count) {
-      const uint64_t key = sorted[r];
-      tok = (int32_t)key_token(key);
-      sc = key_score(key);
-      const int32_t cs = a.cache_slots ? a.cache_slots[(int64_t)u * a.stride + tok] : -1;
-      pay = cs >= 0 ? cs : -(tok + 1);
+  write_ranks<NT>(a, i, p, sorted, (int)count, tid);
+  if (tid == 0) write_spec(a, i, p, count >= (uint32_t)k ? sorted[k - 1] : 0ull);
+  sync();
+  return true;
+}
+
+constexpr uint32_t kMaxBucket = 256;
+
+// ---------------------------------------------------------------------------
+// Exact top-k of one (unit i, position p) by a bucket sort, for candidate
+// sets that fit shared memory: the key range [lo, hi] is cut into B buckets
+// of equal width (numbered from the top), a histogram and its
+// prefix give each bucket's first rank, the keys are scattered to their
+// buckets, and a key's rank is its bucket's first rank plus the number of
+// larger keys in the same bucket.  A few barriers instead of the radix passes
+// and the bitonic network.  seg_off: segment_offsets() of (., p) in shared
+// memory.  Returns false, having written nothing, when the candidates exceed
+// keycap or a bucket holds more than kMaxBucket keys (then the caller runs
+// select_body).  Shared memory: K, S (keycap u64 each), cnt, pos (B u32
+// each), red (4 u64, 8-byte aligned), wsum[32].
+// ---------------------------------------------------------------------------
+template <int NT, class Sync>
+__device__ __forceinline__ bool bucket_select(const SelectArgs& a, int i, int p, int64_t seg0, int nseg,
+                                              const uint32_t* seg_off, uint64_t* K, uint64_t* S, uint32_t keycap,
+                                              uint32_t* cnt, uint32_t* pos, int log2B, unsigned long long* red,
+                                              uint32_t* wsum, int tid, Sync sync) {
+  const int P = a.P, k = a.k;
+  const uint32_t n = seg_off[nseg];
+  if (n > keycap) return false;
+  if (n == 0) {
+    write_ranks<NT>(a, i, p, K, 0, tid);
+    if (tid == 0) write_spec(a, i, p, 0ull);
+    sync();
+    return true;
+  }
+  const int B = 1 << log2B;
+  if (tid == 0) {
+    red[0] = ~0ull;
+    red[1] = 0ull;
+    red[2] = 0ull;
+  }
+  for (int b = tid; b < B; b += NT) cnt[b] = 0;
+  // candidates of every piece into K (eight loads in flight per thread), with the key range
+  unsigned long long lo = ~0ull, hi = 0ull;
+  for (uint32_t e0 = tid; e0 < n; e0 += 8 * NT) {
+    uint64_t v[8];
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+      const uint32_t e = e0 + u * NT;
+      v[u] = 0;
+      if (e < n) {
+        int lo_c = 0, hi_c = nseg - 1;  // last segment with seg_off <= e
+        while (lo_c < hi_c) {
+          const int mid = (lo_c + hi_c + 1) >> 1;
+          if (seg_off[mid] <= e) lo_c = mid; else hi_c = mid - 1;
+        }
+        v[u] = __ldcg(a.seg_keys + ((seg0 + lo_c) * P + p) * (int64_t)k + (e - seg_off[lo_c]));
+      }
     }
-    a.out_tok[obase + r] = tok;
-    if (a.out_score) a.out_score[obase + r] = sc;
-    a.out_pay[obase + r] = pay;
-    if (a.out_pay_user && a.out_pay_user != a.out_pay) a.out_pay_user[obase + r] = pay;
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+      const uint32_t e = e0 + u * NT;
+      if (e < n) {
+        K[e] = v[u];
+        lo = v[u] < lo ? v[u] : lo;
+        hi = v[u] > hi ? v[u] : hi;
+      }
+    }
   }
-  if (a.spec && tid == 0) {
-    a.spec[(int64_t)u * P + p] = count >= (uint32_t)k ? sorted[k - 1] : 0ull;
-    if (a.qn_prev && a.qn_cur) a.qn_prev[(int64_t)u * P + p] = a.qn_cur[(int64_t)i * P + p];
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    const unsigned long long l2 = __shfl_xor_sync(kFull, lo, o), h2 = __shfl_xor_sync(kFull, hi, o);
+    lo = l2 < lo ? l2 : lo;
+    hi = h2 > hi ? h2 : hi;
   }
+  sync();  // red initialised before the atomics
+  if ((tid & 31) == 0) {
+    atomicMin(&red[0], lo);
+    atomicMax(&red[1], hi);
+  }
+  sync();
+  // bucket = floor((x - lo) * B / (range + 1)) up to rounding, through one
+  // precomputed multiplier (exact offsets when the range is below B)
+  const uint64_t kmin = red[0], range = red[1] - red[0];
+  const bool direct = range < (uint64_t)B;
+  const uint64_t mul = direct ? 0ull : (range == ~0ull ? (uint64_t)B : (~0ull / (range + 1)) * (uint64_t)B);
+  auto bucket = [&](uint64_t x) {
+    const uint64_t d = x - kmin;
+    return (uint32_t)(B - 1) - (uint32_t)(direct ? d : __umul64hi(d, mul));
+  };
+  for (uint32_t e = tid; e < n; e += NT) atomicAdd(&cnt[bucket(K[e])], 1u);
+  sync();
+  // first rank of every bucket (each thread owns B / NT consecutive buckets)
+  constexpr int kMaxPer = 8;
+  const int per = B / NT;  // B is a multiple of NT, at most kMaxPer * NT
+  uint32_t loc = 0, mx = 0;
+  for (int j = 0; j < per && j < kMaxPer; ++j) {
+    const uint32_t c = cnt[tid * per + j];
+    loc += c;
+    mx = c > mx ? c : mx;
+  }
+  uint32_t total;
+  uint32_t run = block_excl_scan<NT>(loc, wsum, &total, tid, sync);
+  for (int j = 0; j < per && j < kMaxPer; ++j) {
+    pos[tid * per + j] = run;
+    run += cnt[tid * per + j];
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    const uint32_t m2 = __shfl_xor_sync(kFull, mx, o);
+    mx = m2 > mx ? m2 : mx;
+  }
+  if ((tid & 31) == 0 && mx) atomicMax(&red[2], (unsigned long long)mx);
+  sync();
+  if (red[2] > kMaxBucket) {
+    sync();  // nothing written: the caller may reuse the buffers at once
+    return false;
+  }
+  // scatter (pos[b] ends as the end of bucket b)
+  for (uint32_t e = tid; e < n; e += NT) {
+    const uint64_t x = K[e];
+    S[atomicAdd(&pos[bucket(x)], 1u)] = x;
+  }
+  sync();
+  // rank within the bucket; the winners go to K in rank order
+  for (uint32_t j = tid; j < n; j += NT) {
+    const uint64_t x = S[j];
+    const uint32_t b = bucket(x);
+    const uint32_t end = pos[b], beg = end - cnt[b];
+    uint32_t r = beg;
+    for (uint32_t t = beg; t < end; ++t) r += S[t] > x ? 1u : 0u;
+    if (r < (uint32_t)k) K[r] = x;
+  }
+  sync();
+  const int count = n < (uint32_t)k ? (int)n : k;
+  write_ranks<NT>(a, i, p, K, count, tid);
+  if (tid == 0) write_spec(a, i, p, count == k ? K[k - 1] : 0ull);
   sync();
   return true;
 }
@@ -721,6 +934,7 @@ template <int NT, class Sync>
 __device__ __forceinline__ uint32_t residency_body(const ResidencyArgs& a, int i, uint32_t* bitmap, int32_t* M,
                                                    int32_t* V, uint32_t* wsum, int tid, Sync sync,
                                                    int32_t* status_out) {
+  constexpr int kB = 8;  // loads in flight per thread in the list passes
   const int C = a.C, PK = a.P * a.k;
   const int nwords = (C + 31) >> 5;
   const int u = a.units[i];
@@ -731,50 +945,68 @@ __device__ __forceinline__ uint32_t residency_body(const ResidencyArgs& a, int i
   int32_t* st = a.slot_token + (int64_t)u * C;
   uint32_t* lu = a.last_use + (int64_t)u * C;
   uint32_t* tbm = a.tok_bits + (int64_t)u * a.tok_words;
-  const int par = a.order_par[u];
-  const int32_t* cur = a.order + ((int64_t)par * a.U + u) * C;
-  int32_t* nxt = a.order + ((int64_t)(par ^ 1) * a.U + u) * C;
 
-  // the error word can change under a concurrent launch: one read, shared
-  if (tid == 0) wsum[0] = *((volatile uint32_t*)a.err);
+  // scalars in one round trip; the error word can change under a concurrent
+  // launch, so it is read once and shared
+  if (tid == 0) {
+    wsum[0] = *((volatile uint32_t*)a.err);
+    wsum[1] = a.stamp[u];
+    wsum[2] = (uint32_t)a.order_par[u];
+    wsum[3] = (uint32_t)a.len[u];
+  }
+  for (int w = tid; w < nwords; w += NT) bitmap[w] = 0;
   sync();
   int32_t status = wsum[0] != 0 ? KVO_ETIMEOUT : KVO_OK;
+  const uint32_t stamp = wsum[1] + 1;
+  const int par = (int)wsum[2];
+  const int tw = (int)((wsum[3] + 31) >> 5);
+  const int32_t* cur = a.order + ((int64_t)par * a.U + u) * C;
+  int32_t* nxt = a.order + ((int64_t)(par ^ 1) * a.U + u) * C;
+  sync();  // wsum is reused below
   uint32_t m = 0, hits = 0;
 
   if (status == KVO_OK) {
-    for (int w = tid; w < nwords; w += NT) bitmap[w] = 0;
-    sync();
     // payload says hit (slot) or miss (token): mark hit slots and miss tokens
-    for (int e = tid; e < PK; e += NT) {
-      const int32_t t = tok[e];
-      if (t < 0) continue;
-      const int32_t p = pay[e];
-      if (p >= 0) {
-        if (p < C) atomicOr(&bitmap[p >> 5], 1u << (p & 31));
-      } else {
-        atomicOr(&tbm[t >> 5], 1u << (t & 31));
+    for (int e0 = tid; e0 < PK; e0 += kB * NT) {
+      int32_t t[kB], pv[kB];
+#pragma unroll
+      for (int x = 0; x < kB; ++x) {
+        const int e = e0 + x * NT;
+        t[x] = e < PK ? tok[e] : -1;
+        pv[x] = e < PK ? pay[e] : -1;
+      }
+#pragma unroll
+      for (int x = 0; x < kB; ++x) {
+        if (t[x] < 0) continue;
+        if (pv[x] >= 0) {
+          if (pv[x] < C) atomicOr(&bitmap[pv[x] >> 5], 1u << (pv[x] & 31));
+        } else {
+          atomicOr(&tbm[t[x] >> 5], 1u << (t[x] & 31));
+        }
       }
     }
     __threadfence_block();
     sync();
     // distinct misses in token order; the bitmap words are cleared behind
-    const int tw = (int)((a.len[u] + 31) >> 5);
     const int per = (tw + NT - 1) / NT;
     const int w0 = tid * per, w1 = min(tw, w0 + per);
     uint32_t c = 0;
+#pragma unroll 8
     for (int w = w0; w < w1; ++w) c += __popc(__ldcg(&tbm[w]));
     uint32_t total;
     uint32_t pos = block_excl_scan<NT>(c, wsum, &total, tid, sync);
     m = total;
-    for (int w = w0; w < w1; ++w) {
-      uint32_t bits = __ldcg(&tbm[w]);
-      if (!bits) continue;
-      tbm[w] = 0;
-      while (bits) {
-        const int b = __ffs(bits) - 1;
-        bits &= bits - 1;
-        if (pos < (uint32_t)PK) M[pos] = w * 32 + b;
-        ++pos;
+    if (c) {
+      for (int w = w0; w < w1; ++w) {
+        uint32_t bits = __ldcg(&tbm[w]);
+        if (!bits) continue;
+        tbm[w] = 0;
+        while (bits) {
+          const int b = __ffs(bits) - 1;
+          bits &= bits - 1;
+          if (pos < (uint32_t)PK) M[pos] = w * 32 + b;
+          ++pos;
+        }
       }
     }
     uint32_t hc = 0;
@@ -784,8 +1016,6 @@ __device__ __forceinline__ uint32_t residency_body(const ResidencyArgs& a, int i
   }
 
   if (status == KVO_OK) {
-    const uint32_t stamp = a.stamp[u] + 1;
-    sync();
     if (tid == 0) a.stamp[u] = stamp;
     for (int w = tid; w < nwords; w += NT) {
       uint32_t bits = bitmap[w];
@@ -799,28 +1029,49 @@ __device__ __forceinline__ uint32_t residency_body(const ResidencyArgs& a, int i
     const int j0 = tid * per, j1 = min(C, j0 + per);
     // slots outside [0, C) never come from a valid list; they count as touched
     auto hit = [&](int s) { return (unsigned)s >= (unsigned)C || ((bitmap[s >> 5] >> (s & 31)) & 1u) != 0; };
+    // the thread's run of the LRU list, kB entries per batch of loads
+    auto count_untouched = [&]() {
+      uint32_t c = 0;
+      for (int j = j0; j < j1; j += kB) {
+        int32_t v[kB];
+#pragma unroll
+        for (int x = 0; x < kB; ++x) v[x] = j + x < j1 ? cur[j + x] : 0;
+#pragma unroll
+        for (int x = 0; x < kB; ++x)
+          if (j + x < j1) c += hit(v[x]) ? 0u : 1u;
+      }
+      return c;
+    };
     if (m > 0) {
       // victims: the first m slots of the LRU list that were not hit
-      uint32_t c = 0;
-      for (int jj = j0; jj < j1; ++jj) c += hit(cur[jj]) ? 0u : 1u;
       uint32_t total;
-      uint32_t rank = block_excl_scan<NT>(c, wsum, &total, tid, sync);
-      for (int jj = j0; jj < j1 && rank < m; ++jj) {
-        const int s = cur[jj];
+      uint32_t rank = block_excl_scan<NT>(count_untouched(), wsum, &total, tid, sync);
+      for (int j = j0; j < j1 && rank < m; ++j) {
+        const int s = cur[j];
         if (!hit(s)) V[rank++] = s;
       }
       sync();
       // i-th miss (token order) takes the i-th victim
-      for (uint32_t r = tid; r < m; r += NT) {
-        const int s = V[r];
-        const int32_t t = M[r];
-        const int32_t old = st[s];
-        if (old >= 0) cs[old] = -1;
-        st[s] = t;
-        cs[t] = s;
-        lu[s] = stamp;
-        a.miss_tok[(int64_t)i * PK + r] = t;
-        a.miss_slot[(int64_t)i * PK + r] = s;
+      for (uint32_t r0 = tid; r0 < m; r0 += 4 * NT) {
+        int32_t old[4];
+#pragma unroll
+        for (int x = 0; x < 4; ++x) {
+          const uint32_t r = r0 + x * NT;
+          old[x] = r < m ? st[V[r]] : -1;
+        }
+#pragma unroll
+        for (int x = 0; x < 4; ++x) {
+          const uint32_t r = r0 + x * NT;
+          if (r >= m) break;
+          const int s = V[r];
+          const int32_t t = M[r];
+          if (old[x] >= 0) cs[old[x]] = -1;
+          st[s] = t;
+          cs[t] = s;
+          lu[s] = stamp;
+          a.miss_tok[(int64_t)i * PK + r] = t;
+          a.miss_slot[(int64_t)i * PK + r] = s;
+        }
       }
       sync();
       for (uint32_t r = tid; r < m; r += NT) atomicOr(&bitmap[V[r] >> 5], 1u << (V[r] & 31));
@@ -828,12 +1079,10 @@ __device__ __forceinline__ uint32_t residency_body(const ResidencyArgs& a, int i
     sync();
     if (hits + m > 0) {
       // new list: untouched slots in their order, then the touched ones in slot order
-      uint32_t c = 0;
-      for (int jj = j0; jj < j1; ++jj) c += hit(cur[jj]) ? 0u : 1u;
       uint32_t kept;
-      uint32_t q = block_excl_scan<NT>(c, wsum, &kept, tid, sync);
-      for (int jj = j0; jj < j1; ++jj) {
-        const int s = cur[jj];
+      uint32_t q = block_excl_scan<NT>(count_untouched(), wsum, &kept, tid, sync);
+      for (int j = j0; j < j1; ++j) {
+        const int s = cur[j];
         if (!hit(s) && q < (uint32_t)C) nxt[q++] = s;
       }
       const int wper = (nwords + NT - 1) / NT;
@@ -854,10 +1103,37 @@ __device__ __forceinline__ uint32_t residency_body(const ResidencyArgs& a, int i
     }
     __threadfence_block();
     sync();
-    // remap logical top-k positions to physical slots
-    for (int e = tid; e < PK; e += NT) {
-      const int32_t t = tok[e];
-      out_slot[e] = t >= 0 ? cs[t] : -1;
+    // remap logical top-k positions to physical slots: a hit keeps its slot
+    // (victims are never hit), a miss takes the victim its rank among the
+    // distinct misses (M, ascending) points to
+    const int mm = (int)(m < (uint32_t)PK ? m : (uint32_t)PK);
+    for (int e0 = tid; e0 < PK; e0 += kB * NT) {
+      int32_t t[kB], pv[kB];
+#pragma unroll
+      for (int x = 0; x < kB; ++x) {
+        const int e = e0 + x * NT;
+        t[x] = e < PK ? tok[e] : -1;
+        pv[x] = e < PK ? pay[e] : -1;
+      }
+#pragma unroll
+      for (int x = 0; x < kB; ++x) {
+        const int e = e0 + x * NT;
+        if (e >= PK) break;
+        int32_t slot = -1;
+        if (t[x] >= 0) {
+          if (pv[x] >= 0) {
+            slot = pv[x];
+          } else {
+            int lo = 0, hi = mm;  // first M[j] >= t
+            while (lo < hi) {
+              const int mid = (lo + hi) >> 1;
+              if (M[mid] < t[x]) lo = mid + 1; else hi = mid;
+            }
+            slot = lo < mm && M[lo] == t[x] ? V[lo] : -1;
+          }
+        }
+        out_slot[e] = slot;
+      }
     }
   } else {
     m = 0;

@@ -8,11 +8,13 @@
 // its own scores are complete:
 //
 //  scorer CTAs   a producer warp claims pieces (up to piece_tokens tokens of
-//                one unit, numbered unit-major) from a global counter and
+//                one unit, a quarter of that for the first units; numbered
+//                unit-major) from a global counter and
 //                streams their keys through the bulk-copy ring; the 16
 //                consumer warps score and filter them exactly as the score
 //                kernel does and write each piece's candidates.  The CTA that
-//                completes a unit's last piece finishes the unit: exact top-k
+//                holds a unit's last-claimed piece finishes the unit (its
+//                producer claims nothing more meanwhile): exact top-k
 //                of every position (after checking the speculative threshold,
 //                rescanning the unit from global memory when it was too high),
 //                the residency update, then it publishes the unit's miss rows
@@ -39,7 +41,8 @@ namespace {
 constexpr int kFusedThreads = kScoreThreads;  // 16 consumer warps + 1 producer warp
 constexpr int kFusedWarps = kFusedThreads / 32;
 constexpr int kPieceRing = 16;                // claimed pieces passed to the consumers
-constexpr int kFusedExtra = kPieceRing * 8 + 64;
+constexpr int kFusedSegs = 1024;              // segment offsets the finisher holds (both groups)
+constexpr int kFusedExtra = kPieceRing * 8 + 64 + kFusedSegs * 4 + 256 * 4 + 12 * 4;
 constexpr int kChunkRows = 32;                // miss rows per gather work item
 constexpr int kGatherLag = 2;                 // hot-buffer stores left in flight per warp
 constexpr int kGatherMinSlots = 4;
@@ -85,6 +88,7 @@ struct RowPipe {
   uint32_t bytes, slot_bytes;
   uint32_t issued, stored;
   uint64_t wait_ns;
+  uint64_t pol;  // L2 policy of the rows (read and written once)
   bool timed_out;
 
   __device__ __forceinline__ bool retire(bool block) {
@@ -96,7 +100,7 @@ struct RowPipe {
     } else if (!mbar_try_wait(&bar[d], parity)) {
       return false;
     }
-    bulk_s2g(reinterpret_cast<void*>(dstq[d]), slots + (size_t)d * slot_bytes, bytes);
+    bulk_s2g_hint(reinterpret_cast<void*>(dstq[d]), slots + (size_t)d * slot_bytes, bytes, pol);
     bulk_commit();
     ++stored;
     return true;
@@ -107,7 +111,7 @@ struct RowPipe {
     const int d = (int)(issued % (uint32_t)D);
     dstq[d] = dst;
     mbar_arrive_expect_tx(&bar[d], bytes);
-    bulk_g2s(slots + (size_t)d * slot_bytes, reinterpret_cast<const void*>(src), bytes, &bar[d]);
+    bulk_g2s_hint(slots + (size_t)d * slot_bytes, reinterpret_cast<const void*>(src), bytes, &bar[d], pol);
     ++issued;
   }
   __device__ __forceinline__ void drain() {
@@ -154,6 +158,7 @@ __device__ __forceinline__ void gather_warp(const FusedArgs& f, uint8_t* slice, 
   pipe.D = D;
   pipe.issued = pipe.stored = 0;
   pipe.wait_ns = g.wait_ns;
+  pipe.pol = l2_evict_first();
   pipe.timed_out = false;
   if (lane == 0) {
     for (int d = 0; d < D; ++d) mbar_init(&pipe.bar[d], 1);
@@ -253,6 +258,11 @@ struct FusedSmem {
   volatile int64_t* s_piece;
   volatile int32_t* pcons;  // pieces the consumers have taken from the ring
   volatile int32_t* s_flag;
+  volatile int32_t* s_ready;  // pieces the consumers have completed, finishing included
+  uint32_t* s_tot;          // [8] candidates per position of the unit being finished
+  uint32_t* seg_off;        // [kFusedSegs]
+  uint32_t* hist1;          // [256] histogram / scan words of the second select group
+  uint32_t* rx1;            // [12] (8-byte aligned)
   __device__ void carve(uint8_t* smem, int P, int cap, int k) {
     sm.carve(smem, P, cap);
     region = reinterpret_cast<uint8_t*>(sm.cand);
@@ -261,6 +271,11 @@ struct FusedSmem {
     s_piece = reinterpret_cast<volatile int64_t*>(pring + kPieceRing);
     pcons = reinterpret_cast<volatile int32_t*>(s_piece + 1);
     s_flag = pcons + 1;
+    s_ready = s_flag + 1;
+    s_tot = reinterpret_cast<uint32_t*>(reinterpret_cast<uint8_t*>(pring + kPieceRing) + 32);
+    seg_off = reinterpret_cast<uint32_t*>(reinterpret_cast<uint8_t*>(pring + kPieceRing) + 64);
+    hist1 = seg_off + kFusedSegs;
+    rx1 = hist1 + 256;
   }
 };
 
@@ -269,7 +284,20 @@ struct FusedSmem {
 __device__ __forceinline__ void fused_producer(const FusedArgs& f, const FusedSmem& fs) {
   const SelectArgs& a = f.s;
   uint32_t seq = 0;
+  bool finishes = false;  // the last piece claimed is its unit's last: the consumers finish that unit
+  const uint64_t pol = l2_evict_first();  // keys are read once per step
   for (uint32_t q = 0;; ++q) {
+    // nothing is claimed behind a finisher (that piece would wait for it);
+    // the ring stays idle meanwhile and the finisher uses it
+    if (finishes) {
+      if (!spin_until([&] { return *fs.s_ready >= (int)q; }, a.wait_ns)) {
+        atomicOr(a.err, kErrTimeout);
+        return;
+      }
+      // the finisher wrote the ring with ordinary stores; bulk copies follow
+      __threadfence_block();
+      fence_proxy_async_smem();
+    }
     if (q >= (uint32_t)kPieceRing) {
       // the ring entry about to be replaced must have been taken
       const int need = (int)(q - kPieceRing + 1);
@@ -284,9 +312,11 @@ __device__ __forceinline__ void fused_producer(const FusedArgs& f, const FusedSm
         ((unsigned long long)q << 32) | (end ? kPieceEnd : (uint32_t)piece);
     if (end) return;
     const int i = find_segment(a.pbeg, a.n, (int64_t)piece);
+    finishes = (int64_t)piece == a.pbeg[i + 1] - 1;
     const int64_t len = a.off[i + 1] - a.off[i];
-    const int64_t t0 = ((int64_t)piece - a.pbeg[i]) * a.piece_tokens;
-    const int64_t t1 = min(t0 + (int64_t)a.piece_tokens, len);
+    const int64_t ps = piece_tokens_of(i, len, a.piece_tokens);
+    const int64_t t0 = ((int64_t)piece - a.pbeg[i]) * ps;
+    const int64_t t1 = min(t0 + ps, len);
     const uint16_t* kb = a.keys + (int64_t)a.units[i] * a.stride * kDim;
     for (int64_t t = t0; t < t1; t += kTile, ++seq) {
       const int stage = seq % kStages;
@@ -298,7 +328,7 @@ __device__ __forceinline__ void fused_producer(const FusedArgs& f, const FusedSm
       const int64_t nt = (t1 - t) < kTile ? (t1 - t) : kTile;
       const uint32_t bytes = (uint32_t)nt * kKeyBytes;
       mbar_arrive_expect_tx(&fs.sm.full[stage], bytes);
-      bulk_g2s(fs.sm.ring + stage * kTileBytes, kb + t * kDim, bytes, &fs.sm.full[stage]);
+      bulk_g2s_hint(fs.sm.ring + stage * kTileBytes, kb + t * kDim, bytes, &fs.sm.full[stage], pol);
     }
   }
 }
@@ -327,6 +357,38 @@ __device__ __forceinline__ void rescan_unit(const SelectArgs& a, const FusedSmem
   consumer_sync();
 }
 
+// Exact top-k of positions p0, p0 + step, ... of unit i by one group of NTG
+// consumer threads (barrier `sync`) in its own part of the finisher's
+// shared memory: bucket sort when the candidates fit and spread, radix
+// select and bitonic sort otherwise.
+template <int NTG, class Sync>
+__device__ __forceinline__ void select_positions(const SelectArgs& a, int i, int p0, int step, int64_t pb, int nseg,
+                                                 uint8_t* region, size_t bytes, uint32_t* seg_off, int seg_cap,
+                                                 uint32_t* hist, uint32_t* rx, int gtid, Sync sync) {
+  const int k = a.k;
+  int kpad = 1;
+  while (kpad < k) kpad <<= 1;
+  uint64_t* keys = reinterpret_cast<uint64_t*>(region);
+  const uint32_t words = (uint32_t)(bytes / 8);
+  int log2B = 12;
+  while ((1 << log2B) > 8 * NTG || (log2B > 9 && (8u << log2B) > bytes / 4)) --log2B;
+  const uint32_t bkeys = words > (1u << log2B) + 4 ? (words - (1u << log2B) - 4) / 2 : 0u;
+  uint32_t* cnt = reinterpret_cast<uint32_t*>(keys + 2 * bkeys);
+  uint32_t* pos = cnt + (1 << log2B);
+  unsigned long long* red = reinterpret_cast<unsigned long long*>(pos + (1 << log2B));
+  for (int p = p0; p < a.P; p += step) {
+    bool done = false;
+    if (nseg + 1 <= seg_cap) {
+      segment_offsets<NTG>(a, p, 1, pb, nseg, seg_off, gtid, sync);
+      done = bucket_select<NTG>(a, i, p, pb, nseg, seg_off, keys, keys + bkeys, bkeys, cnt, pos, log2B, red, hist,
+                                gtid, sync);
+    }
+    if (!done)
+      select_body<NTG>(a, i, p, pb, nseg, false, keys, words - (uint32_t)kpad, keys + (words - kpad), hist, rx, gtid,
+                       sync);
+  }
+}
+
 // Select, residency and publication of unit i (the consumer threads).
 template <int PP>
 __device__ __forceinline__ void finish_unit(const FusedArgs& f, const FusedSmem& fs, Scorer<PP>& sc, int i,
@@ -334,37 +396,50 @@ __device__ __forceinline__ void finish_unit(const FusedArgs& f, const FusedSmem&
   const SelectArgs& a = f.s;
   const int P = a.P, k = a.k;
   const int64_t pb = a.pbeg[i], pe = a.pbeg[i + 1];
-  auto sync = [] { consumer_sync(); };
-  // A speculative threshold is exact when at least min(k, visible) keys of
-  // every position reached it.
-  bool exact = true;
-  if (a.tspec) {
-    const int64_t L = a.off[i + 1] - a.off[i];
-    for (int p = 0; p < P; ++p) {
-      if (a.tspec[(int64_t)i * P + p] == 0) continue;
-      uint32_t n = 0;
-      for (int64_t s = pb; s < pe; ++s) n += (uint32_t)__ldcg(&a.seg_cnt[s * P + p]);
-      const int64_t vis = L - (P - 1 - p);
-      const uint32_t need = (uint32_t)(vis < k ? (vis > 0 ? vis : 0) : k);
-      exact = exact && n >= need;
+  const int nseg = (int)(pe - pb);
+  const int warp = ctid >> 5, lane = ctid & 31;
+  // candidates per position (warp p sums position p's segment counts)
+  auto totals = [&] {
+    if (warp < P) {
+      uint32_t t = 0;
+      for (int c = lane; c < nseg; c += 32) t += (uint32_t)__ldcg(&a.seg_cnt[(pb + c) * P + warp]);
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) t += __shfl_xor_sync(kFull, t, o);
+      if (lane == 0) fs.s_tot[warp] = t;
     }
-  }
+    consumer_sync();
+  };
+  totals();
+  bool exact = true;
+  for (int p = 0; p < P; ++p) exact = exact && !spec_short(a, i, p, fs.s_tot[p]);
   if (!exact) {
     rescan_unit<PP>(a, fs, sc, i, pb, pe, ctid);
     if (ctid == 0 && a.stats) atomicAdd(&a.stats->rescored, 1ull);
   }
+  // positions in two concurrent groups of 256 threads (their barriers and
+  // memory waits overlap), one in the idle key ring and one in the candidate
+  // buffers; or all 512 threads on one position at a time
   int kpad = 1;
   while (kpad < k) kpad <<= 1;
-  uint64_t* keys = reinterpret_cast<uint64_t*>(fs.region);
-  const uint32_t keycap = (uint32_t)(fs.region_bytes / 8) - (uint32_t)kpad;
-  for (int p = 0; p < P; ++p)
-    select_body<kCT>(a, i, p, pb, (int)(pe - pb), false, keys, keycap, keys + keycap, fs.sm.hist, fs.sm.rx, ctid,
-                     sync);
+  const size_t ring_bytes = (size_t)kStages * kTileBytes;
+  if (P >= 2 && kpad <= 8 * (kCT / 2)) {
+    const int g = ctid / (kCT / 2), gtid = ctid % (kCT / 2);
+    auto gsync = [g] { named_sync(2 + g, kCT / 2); };
+    select_positions<kCT / 2>(a, i, g, 2, pb, nseg, g ? fs.region : fs.sm.ring, g ? fs.region_bytes : ring_bytes,
+                              fs.seg_off + g * (kFusedSegs / 2), kFusedSegs / 2, g ? fs.hist1 : fs.sm.hist,
+                              g ? fs.rx1 : fs.sm.rx, gtid, gsync);
+  } else {
+    const bool in_ring = ring_bytes > fs.region_bytes;
+    select_positions<kCT>(a, i, 0, 1, pb, nseg, in_ring ? fs.sm.ring : fs.region,
+                          in_ring ? ring_bytes : fs.region_bytes, fs.seg_off, kFusedSegs, fs.sm.hist, fs.sm.rx, ctid,
+                          [] { consumer_sync(); });
+  }
+  consumer_sync();
   const int nwords_pad = (((f.r.C + 31) >> 5) + 3) & ~3;
   uint32_t* bitmap = reinterpret_cast<uint32_t*>(fs.region);
   int32_t* M = reinterpret_cast<int32_t*>(bitmap + nwords_pad);
   int32_t* V = M + P * k;
-  const uint32_t m = residency_body<kCT>(f.r, i, bitmap, M, V, fs.sm.hist, ctid, sync, nullptr);
+  const uint32_t m = residency_body<kCT>(f.r, i, bitmap, M, V, fs.sm.hist, ctid, [] { consumer_sync(); }, nullptr);
   __threadfence();
   consumer_sync();
   if (ctid < 32) publish_chunks(f, i, m, ctid);
@@ -400,8 +475,9 @@ __device__ __forceinline__ void fused_consumers(const FusedArgs& f, const FusedS
     if (piece < 0) break;
     const int i = find_segment(a.pbeg, a.n, piece);
     const int64_t len = a.off[i + 1] - a.off[i];
-    const int64_t t0 = (piece - a.pbeg[i]) * a.piece_tokens;
-    const int64_t t1 = min(t0 + (int64_t)a.piece_tokens, len);
+    const int64_t ps = piece_tokens_of(i, len, a.piece_tokens);
+    const int64_t t0 = (piece - a.pbeg[i]) * ps;
+    const int64_t t1 = min(t0 + ps, len);
     uint64_t* gth = a.gthr + (int64_t)i * P;
     sc.load_queries(a.queries, i, P);
     piece_begin(fs.sm, P, a.tspec ? a.tspec + (int64_t)i * P : nullptr, ctid);
@@ -423,17 +499,30 @@ __device__ __forceinline__ void fused_consumers(const FusedArgs& f, const FusedS
       if (t + kTile < t1 && (ti + 1) % kCheckTiles == 0) piece_check(fs.sm, P, k, cap, gth, ctid);
     }
     piece_end(fs.sm, P, k, cap, gth, piece, a.seg_keys, a.seg_cnt, ctid);
-    // the CTA completing the unit's last piece finishes the unit
+    // The CTA holding a unit's last-claimed piece finishes the unit, once the
+    // unit's other pieces (claimed earlier, by CTAs that claim nothing
+    // behind a finisher) are complete.
     __threadfence();
     consumer_sync();
+    const int np = (int)(a.pbeg[i + 1] - a.pbeg[i]);
+    const bool finisher = piece == a.pbeg[i + 1] - 1;
     if (ctid == 0) {
-      const int np = (int)(a.pbeg[i + 1] - a.pbeg[i]);
-      const int last = atomicAdd(&a.pdone[i], 1) == np - 1;
-      if (last) __threadfence();
-      *fs.s_flag = last;
+      atomicAdd(&a.pdone[i], 1);
+      if (finisher) {
+        if (!spin_until([&] { return ld_volatile_u32(&a.pdone[i]) >= (uint32_t)np; }, a.wait_ns))
+          atomicOr(a.err, kErrTimeout);
+        __threadfence();
+      }
     }
     consumer_sync();
-    if (*fs.s_flag) finish_unit<PP>(f, fs, sc, i, ctid);
+    if (finisher) {
+      finish_unit<PP>(f, fs, sc, i, ctid);
+      consumer_sync();
+    }
+    if (ctid == 0) {
+      __threadfence_block();
+      *fs.s_ready = (int32_t)(q + 1);
+    }
   }
 }
 
@@ -451,6 +540,7 @@ __global__ void __launch_bounds__(kFusedThreads, 1) fused_step_kernel(FusedArgs 
       }
       for (int q = 0; q < kPieceRing; ++q) fs.pring[q] = ~0ull;
       *fs.pcons = 0;
+      *fs.s_ready = 0;
       fence_mbar_init();
     }
     __syncthreads();

@@ -102,6 +102,28 @@ __device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t by
       "l"(src), "r"(bytes), "r"(smem_u32(bar))
       : "memory");
 }
+// L2 policy for data read or written once per step (the indexer key stream,
+// miss rows): evicted first, so that per-unit state stays in L2.
+__device__ __forceinline__ uint64_t l2_evict_first() {
+  uint64_t pol;
+  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
+  return pol;
+}
+// bulk_g2s with an L2 cache policy.
+__device__ __forceinline__ void bulk_g2s_hint(void* dst, const void* src, uint32_t bytes, uint64_t* bar,
+                                              uint64_t pol) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1], %2, [%3], "
+      "%4;" ::"r"(smem_u32(dst)),
+      "l"(src), "r"(bytes), "r"(smem_u32(bar)), "l"(pol)
+      : "memory");
+}
+// 1-D bulk copy shared -> global with an L2 cache policy.
+__device__ __forceinline__ void bulk_s2g_hint(void* dst, const void* src, uint32_t bytes, uint64_t pol) {
+  asm volatile("cp.async.bulk.global.shared::cta.bulk_group.L2::cache_hint [%0], [%1], %2, %3;" ::"l"(dst),
+               "r"(smem_u32(src)), "r"(bytes), "l"(pol)
+               : "memory");
+}
 // 1-D bulk copy shared -> global, tracked by the issuing thread's bulk group.
 __device__ __forceinline__ void bulk_s2g(void* dst, const void* src, uint32_t bytes) {
   asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(dst),
@@ -261,6 +283,20 @@ struct ResetArgs {
   uint32_t* stamp;
   int32_t* len;
 };
+
+// Tokens per scoring piece of listed unit i (length len) in the fused step.
+// The first units are cut four times finer (when they are not long), so that
+// they complete, and their miss rows can start moving, early in the step.
+constexpr int kSmallPieceUnits = 16;
+constexpr int64_t kSmallPieceMaxLen = 65536;
+__host__ __device__ inline int64_t piece_tokens_of(int i, int64_t len, int piece_tokens) {
+  if (i < kSmallPieceUnits && len <= kSmallPieceMaxLen && piece_tokens >= 512) return (piece_tokens / 4) & ~127;
+  return piece_tokens;
+}
+__host__ __device__ inline int64_t pieces_of(int i, int64_t len, int piece_tokens) {
+  const int64_t ps = piece_tokens_of(i, len, piece_tokens);
+  return len > 0 ? (len + ps - 1) / ps : 1;
+}
 
 // One fused launch of the decode step: scoring, select, residency and the
 // miss-row fill of every listed unit, overlapped across units.

@@ -14,10 +14,11 @@
 //                  can still be in the top-k in a shared-memory candidate
 //                  buffer filtered by a rising threshold.  At the end of each
 //                  unit piece it writes at most k candidates per position.
-//  select_kernel : one CTA per (unit, position): exact radix select of the k
-//                  best candidates over the unit's pieces, bitonic sort into
-//                  (score desc, token asc) order, payload packed from
-//                  cache_slots for the winners.
+//  select_kernel : one CTA per (unit, position): exact top-k of the unit's
+//                  candidates in (score desc, token asc) order by a bucket
+//                  sort, or by radix select and a bitonic sort when they
+//                  crowd one bucket; payload packed from cache_slots for the
+//                  winners.
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -150,17 +151,14 @@ __global__ void __launch_bounds__(1024) plan_kernel(SelectArgs a) {
     if (carry != a.T) atomicOr(a.err, kErrPlan);
   }
   if (a.pbeg) {
-    // pieces of the fused step: unit i owns max(1, ceil(len / piece_tokens)) of them
+    // pieces of the fused step: unit i owns pieces_of(i, len) of them
     __syncthreads();
     if (tid == 0) carry = 0;
     __syncthreads();
     for (int base = 0; base < a.n; base += 1024) {
       const int i = base + tid;
       int64_t v = 0;
-      if (i < a.n) {
-        const int64_t L = a.len[a.units[i]];
-        v = L > 0 ? (L + a.piece_tokens - 1) / a.piece_tokens : 1;
-      }
+      if (i < a.n) v = pieces_of(i, a.len[a.units[i]], a.piece_tokens);
       int64_t incl = v;
 #pragma unroll
       for (int o = 1; o < 32; o <<= 1) {
@@ -225,6 +223,7 @@ __global__ void __launch_bounds__(kScoreThreads, 1) score_kernel(SelectArgs a) {
   if (warp == kCW) {
     // ---------------- producer: stream every tile of every piece ----------
     if (lane == 0) {
+      const uint64_t pol = l2_evict_first();  // keys are read once per step
       PieceIter it;
       it.begin(a.off, a.n, g0, g1, only);
       Piece pc;
@@ -240,7 +239,7 @@ __global__ void __launch_bounds__(kScoreThreads, 1) score_kernel(SelectArgs a) {
           const int64_t nt = (pc.t1 - t) < kTile ? (pc.t1 - t) : kTile;
           const uint32_t bytes = (uint32_t)nt * kKeyBytes;
           mbar_arrive_expect_tx(&full[stage], bytes);
-          bulk_g2s(ring + stage * kTileBytes, kb + t * kDim, bytes, &full[stage]);
+          bulk_g2s_hint(ring + stage * kTileBytes, kb + t * kDim, bytes, &full[stage], pol);
         }
       }
     }
@@ -288,10 +287,15 @@ __global__ void __launch_bounds__(kScoreThreads, 1) score_kernel(SelectArgs a) {
 // ---------------------------------------------------------------------------
 __global__ void __launch_bounds__(kSelThreads) select_kernel(SelectArgs a) {
   extern __shared__ __align__(128) uint8_t smem[];
-  uint64_t* keys = reinterpret_cast<uint64_t*>(smem);          // [kSelSmemKeys]
-  uint64_t* sorted = keys + kSelSmemKeys;                       // [kpad]
+  // bucket sort: K, S [kSelBucketKeys], cnt, pos [1 << kSelLog2B], red;
+  // fallback: keys [kSelSmemKeys], sorted [kpad] over the same bytes
+  uint64_t* base = reinterpret_cast<uint64_t*>(smem);
+  uint32_t* cnt = reinterpret_cast<uint32_t*>(base + 2 * kSelBucketKeys);
+  uint32_t* pos = cnt + (1 << kSelLog2B);
+  unsigned long long* red = reinterpret_cast<unsigned long long*>(pos + (1 << kSelLog2B));
   __shared__ uint32_t hist[256];
   __shared__ __align__(8) uint32_t rx[10];
+  __shared__ uint32_t seg_off[kSelMaxSegs + 1];
 
   const int tid = threadIdx.x;
   const int P = a.P;
@@ -304,14 +308,24 @@ __global__ void __launch_bounds__(kSelThreads) select_kernel(SelectArgs a) {
     c0 = cta_of(s0, a.T, a.G);
     c1 = cta_of(s1 - 1, a.T, a.G);
   }
-  // A failed speculative threshold sends the unit to the rescoring pass.
-  if (!select_body<kSelThreads>(a, i, p, (int64_t)c0 + i, c1 - c0 + 1, !a.fallback, keys, kSelSmemKeys, sorted,
-                                hist, rx, tid, [] { __syncthreads(); })) {
+  const int64_t seg0 = (int64_t)c0 + i;
+  const int nseg = c1 - c0 + 1;
+  auto sync = [] { __syncthreads(); };
+  const bool few = nseg <= kSelMaxSegs;
+  if (few) segment_offsets<kSelThreads>(a, p, 1, seg0, nseg, seg_off, tid, sync);
+  const uint32_t n = few ? seg_off[nseg] : candidate_count(a, p, seg0, nseg);
+  // a speculative threshold that was too high sends the unit to the rescoring pass
+  if (!a.fallback && spec_short(a, i, p, n)) {
     if (tid == 0) {
       a.fb[i] = 1;
       atomicExch(a.fb_any, 1u);
     }
+    return;
   }
+  if (!few || !bucket_select<kSelThreads>(a, i, p, seg0, nseg, seg_off, base, base + kSelBucketKeys, kSelBucketKeys,
+                                          cnt, pos, kSelLog2B, red, hist, tid, sync))
+    select_body<kSelThreads>(a, i, p, seg0, nseg, false, base, kSelSmemKeys, base + kSelSmemKeys, hist, rx, tid,
+                             sync);
 }
 
 // ---------------------------------------------------------------------------
@@ -359,7 +373,8 @@ cudaError_t launch_select(const SelectArgs& a, cudaStream_t s) {
   if (a.k > kMaxK) return cudaErrorInvalidValue;
   int kpad = 1;
   while (kpad < a.k) kpad <<= 1;
-  const size_t smem = (size_t)kSelSmemKeys * 8 + (size_t)kpad * 8;
+  const size_t smem = kSelSmemBytes;
+  if ((size_t)kSelSmemKeys * 8 + (size_t)kpad * 8 > smem) return cudaErrorInvalidValue;
   cudaError_t e = cudaFuncSetAttribute(select_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
   select_kernel<<<a.n * a.P, kSelThreads, smem, s>>>(a);
