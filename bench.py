@@ -287,14 +287,16 @@ def run_kvo(args, log):
     kv.set_option(K.KVO_OPT_GATHER_MODE, K.KVO_GATHER_BULK if args.gather == "bulk" else K.KVO_GATHER_LDG)
     kv.set_option(K.KVO_OPT_GROUPS, args.groups)
     kv.set_option(K.KVO_OPT_SCORE_CTAS, args.score_ctas)
-    kv.set_option(K.KVO_OPT_FUSED, 1 if args.path == "fused" else 0)
-    if args.path == "fused":
+    if args.path != "auto":
+        kv.set_option(K.KVO_OPT_FUSED, 1 if args.path == "fused" else 0)
+    if args.path != "staged":
         if args.gather_ctas is not None:
             kv.set_option(K.KVO_OPT_GATHER_CTAS, args.gather_ctas)
         if args.piece_tokens is not None:
             kv.set_option(K.KVO_OPT_PIECE_TOKENS, args.piece_tokens)
     seq = Sequence(kv, inp, wl)
     stream = torch.cuda.current_stream(device)
+    path = "fused" if kv.get_option(K.KVO_OPT_FUSED) else "staged"
 
     # warm-up (the first step of the sequence is the cold, all-miss step)
     for _ in range(args.warmup):
@@ -416,8 +418,8 @@ def run_kvo(args, log):
         "config": {"workload": wl.name, "n_requests": wl.n_requests, "n_layers": wl.n_layers,
                    "context": wl.context, "n_pos": P, "n_new": wl.n_new, "topk": k,
                    "hot_capacity": wl.hot_capacity, "drift": wl.drift,
-                   "steps_per_sequence": wl.steps, "path": args.path,
-                   "gather": "bulk" if args.path == "fused" else args.gather, "groups": args.groups,
+                   "steps_per_sequence": wl.steps, "path": path,
+                   "gather": "bulk" if path == "fused" else args.gather, "groups": args.groups,
                    "parallelism": "replicas%d" % world,
                    "l2": "inputs larger than L2: %.2f GB of indexer keys read per step"
                          % (score_bytes / n_steps / 1e9)},
@@ -613,8 +615,9 @@ def main(argv=None):
     ap.add_argument("--groups", type=int, default=1,
                     help="unit groups per step; miss-row copies overlap the next group's scoring")
     ap.add_argument("--score-ctas", type=int, default=0, help="cap on scoring CTAs (0 = one per SM)")
-    ap.add_argument("--path", choices=("fused", "staged"), default="staged",
-                    help="fused: one cooperative launch per step; staged: one launch per stage")
+    ap.add_argument("--path", choices=("auto", "fused", "staged"), default="auto",
+                    help="fused: one cooperative launch per step; staged: one launch per stage; "
+                         "auto: the library's default for the configuration")
     ap.add_argument("--gather-ctas", type=int, default=None, help="fused step: CTAs that only fill rows")
     ap.add_argument("--piece-tokens", type=int, default=None, help="fused step: tokens per piece")
     ap.add_argument("--no-e2e", action="store_true")

@@ -113,10 +113,12 @@ typedef struct kvo_stats {
                                    rescored exactly in the same call (default 900) */
 #define KVO_OPT_FUSED 7         /* 1: kvo_step is one cooperative launch that overlaps the scoring of
                                    some units with the select, residency and miss-row fill of
-                                   others; 0: one launch per stage (default).  KVO_EINVAL for 1
-                                   when the configuration does not fit its shared-memory layout.
-                                   The fused step moves miss rows with bulk async copies and
-                                   ignores KVO_OPT_GATHER_MODE, GROUPS and SCORE_CTAS. */
+                                   others; 0: one launch per stage.  Default 1 when the
+                                   configuration fits the fused layout and hot_capacity <= 65536
+                                   (longer LRU lists favour the staged step), else 0.  KVO_EINVAL
+                                   for 1 when it does not fit.  The fused step moves miss rows
+                                   with bulk async copies and ignores KVO_OPT_GATHER_MODE, GROUPS
+                                   and SCORE_CTAS. */
 #define KVO_OPT_GATHER_CTAS 8   /* fused step: CTAs that only fill miss rows, 0 .. SMs-1 (default 16);
                                    the others score and join the fill when no piece is left */
 #define KVO_OPT_PIECE_TOKENS 9  /* fused step: tokens per scoring piece, a multiple of 128 in
@@ -243,6 +245,10 @@ int kvo_profile_read(kvo_handle* h, double* ms, uint64_t* launches, int32_t n_ki
 
 /* kvo_set_option: KVO_OPT_* above.  KVO_EINVAL on unknown key or value. */
 int kvo_set_option(kvo_handle* h, int32_t key, int64_t value);
+
+/* kvo_get_option: the current value of KVO_OPT_* key into *value (host
+ * memory).  KVO_EINVAL on unknown key or NULL arguments. */
+int kvo_get_option(kvo_handle* h, int32_t key, int64_t* value);
 
 /* kvo_get_stats: synchronises the device, then copies the counters. */
 int kvo_get_stats(kvo_handle* h, kvo_stats* out);

@@ -73,6 +73,7 @@ def test_null_handles(L):
     assert L.kvo_step(None, None, 1, None, None, None, None, None, None, None) == kvo.KVO_EINVAL
     assert L.kvo_append(None, None, 1, 1, None, None, None) == kvo.KVO_EINVAL
     assert L.kvo_set_option(None, 1, 0) == kvo.KVO_EINVAL
+    assert L.kvo_get_option(None, 1, None) == kvo.KVO_EINVAL
 
 
 def test_header_constants_match_binding():

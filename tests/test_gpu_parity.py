@@ -318,7 +318,9 @@ def test_fused_options_validated(path):
             with pytest.raises(K.KvoError) as e:
                 kv.set_option(key, value)
             assert e.value.code == K.KVO_EINVAL
-        kv.set_option(K.KVO_OPT_FUSED, 1)
+        assert kv.get_option(K.KVO_OPT_FUSED) == 1  # the default at this capacity
+        kv.set_option(K.KVO_OPT_GATHER_CTAS, 3)
+        assert kv.get_option(K.KVO_OPT_GATHER_CTAS) == 3
         kv.set_option(K.KVO_OPT_PROFILE, 1)
         q = torch.zeros((2, 2, 128), dtype=torch.bfloat16, device="cuda")
         kv.step(q)

@@ -159,6 +159,9 @@ size_t residency_smem_bytes(int C, int P, int k) {
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
+// Largest hot capacity for which kvo_step takes the fused path by default.
+constexpr int kFusedDefaultMaxCapacity = 65536;
+
 // Whether the fused step's shared-memory layout holds this configuration:
 // the finisher's select and residency reuse the candidate buffers.
 bool fused_fits(int P, int k, int cap, int C) {
@@ -470,6 +473,9 @@ int kvo_create(const kvo_config* cfg, kvo_handle** out) {
   if (e == cudaSuccess) e = dalloc(&h->stats, 1);
   h->fused_ok = fused_fits(h->P, h->k, h->cap, h->C);
   if (e == cudaSuccess && h->fused_ok) e = alloc_fused(h);
+  // by measurement: one fused launch wins unless the LRU lists are so long
+  // that the per-unit finishers (one SM each) dominate the step
+  h->fused = h->fused_ok && h->C <= kFusedDefaultMaxCapacity ? 1 : 0;
   if (h->gather_ctas > h->n_sm - 1) h->gather_ctas = h->n_sm - 1;
   if (e != cudaSuccess) {
     free_all(h);
@@ -847,6 +853,22 @@ int kvo_set_option(kvo_handle* h, int32_t key, int64_t value) {
       return KVO_OK;
     default:
       return fail(KVO_EINVAL, "unknown option");
+  }
+}
+
+int kvo_get_option(kvo_handle* h, int32_t key, int64_t* value) {
+  if (!h || !value) return fail(KVO_EINVAL, "NULL argument");
+  switch (key) {
+    case KVO_OPT_GATHER_MODE: *value = h->gather_mode; return KVO_OK;
+    case KVO_OPT_WAIT_LIMIT_NS: *value = (int64_t)h->wait_ns; return KVO_OK;
+    case KVO_OPT_PROFILE: *value = h->profile ? 1 : 0; return KVO_OK;
+    case KVO_OPT_GROUPS: *value = h->groups; return KVO_OK;
+    case KVO_OPT_SCORE_CTAS: *value = h->score_ctas; return KVO_OK;
+    case KVO_OPT_SPECULATE: *value = h->speculate; return KVO_OK;
+    case KVO_OPT_FUSED: *value = h->fused; return KVO_OK;
+    case KVO_OPT_GATHER_CTAS: *value = h->gather_ctas; return KVO_OK;
+    case KVO_OPT_PIECE_TOKENS: *value = h->piece_tokens; return KVO_OK;
+    default: return fail(KVO_EINVAL, "unknown option");
   }
 }
 

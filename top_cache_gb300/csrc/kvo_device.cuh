@@ -26,10 +26,9 @@ constexpr int kCheckTiles = 8;              // tiles between candidate-buffer ch
 constexpr int kSmemMax = 222 * 1024;        // leaves room for a co-resident copy CTA
 constexpr int kSelThreads = 512;
 constexpr int kSelSmemKeys = 8192;          // candidates held in shared memory by select (fallback)
-constexpr int kSelBucketKeys = 4096;        // candidates the bucket sort of the select kernel holds
-constexpr int kSelLog2B = 12;               // its buckets
+constexpr int kSelLog2B = 11;               // buckets of the select kernel's bucket sort
 constexpr int kSelMaxSegs = 512;            // segments whose offsets the select kernel holds
-constexpr int kSelSmemBytes = 2 * kSelBucketKeys * 8 + 2 * (1 << kSelLog2B) * 4 + 32;
+constexpr int kSelSmemBytes = 104 * 1024;   // two CTAs per SM
 constexpr int kMaxK = 4096;
 
 __device__ __forceinline__ void consumer_sync() { named_sync(1, kCT); }
@@ -787,61 +786,93 @@ constexpr uint32_t kMaxBucket = 256;
 // ---------------------------------------------------------------------------
 // Exact top-k of one (unit i, position p) by a bucket sort, for candidate
 // sets that fit shared memory: the key range [lo, hi] is cut into B buckets
-// of equal width (numbered from the top), a histogram and its
-// prefix give each bucket's first rank, the keys are scattered to their
-// buckets, and a key's rank is its bucket's first rank plus the number of
-// larger keys in the same bucket.  A few barriers instead of the radix passes
-// and the bitonic network.  seg_off: segment_offsets() of (., p) in shared
-// memory.  Returns false, having written nothing, when the candidates exceed
-// keycap or a bucket holds more than kMaxBucket keys (then the caller runs
-// select_body).  Shared memory: K, S (keycap u64 each), cnt, pos (B u32
-// each), red (4 u64, 8-byte aligned), wsum[32].
+// of equal width (numbered from the top), a histogram and its prefix give
+// each bucket's first rank, the keys are scattered to their buckets, and a
+// key's rank is its bucket's first rank plus the number of larger keys in the
+// same bucket.  A few barriers instead of the radix passes and the bitonic
+// network; each candidate's cache_slots entry is fetched with the candidates
+// (one more batch of loads) and the outputs are written straight from the
+// rank pass.  seg_off: segment_offsets() of (., p) in shared memory.  Returns
+// false, having written nothing, when the candidates exceed what `region`
+// holds or a bucket holds more than kMaxBucket keys (then the caller runs
+// select_body).  region: `bytes` of shared memory (16-byte aligned); wsum:
+// 32 words.
 // ---------------------------------------------------------------------------
 template <int NT, class Sync>
 __device__ __forceinline__ bool bucket_select(const SelectArgs& a, int i, int p, int64_t seg0, int nseg,
-                                              const uint32_t* seg_off, uint64_t* K, uint64_t* S, uint32_t keycap,
-                                              uint32_t* cnt, uint32_t* pos, int log2B, unsigned long long* red,
+                                              const uint32_t* seg_off, uint8_t* region, size_t bytes, int log2B,
                                               uint32_t* wsum, int tid, Sync sync) {
   const int P = a.P, k = a.k;
+  const int B = 1 << log2B;
+  uint32_t* cnt = reinterpret_cast<uint32_t*>(region);        // [B]
+  uint32_t* pos = cnt + B;                                    // [B]
+  unsigned long long* red = reinterpret_cast<unsigned long long*>(pos + B);  // [4]
+  const size_t fixed = (size_t)8 * B + 32;
+  const uint32_t keycap = bytes > fixed ? (uint32_t)((bytes - fixed) / 24) : 0u;
+  uint64_t* K = reinterpret_cast<uint64_t*>(red + 4);         // [keycap] candidates
+  uint64_t* S = K + keycap;                                   // [keycap] candidates by bucket
+  int32_t* KC = reinterpret_cast<int32_t*>(S + keycap);       // [keycap] cache_slots of K
+  int32_t* SC = KC + keycap;                                  // [keycap] cache_slots of S
   const uint32_t n = seg_off[nseg];
   if (n > keycap) return false;
+  const int u = a.units[i];
+  const int32_t* cs = a.cache_slots ? a.cache_slots + (int64_t)u * a.stride : nullptr;
+  const int64_t ob = ((int64_t)i * P + p) * k;
+  auto emit = [&](int r, uint64_t key, int32_t slot) {
+    const int32_t tok = (int32_t)key_token(key);
+    a.out_tok[ob + r] = tok;
+    if (a.out_score) a.out_score[ob + r] = key_score(key);
+    const int32_t pay = slot >= 0 ? slot : -(tok + 1);
+    a.out_pay[ob + r] = pay;
+    if (a.out_pay_user && a.out_pay_user != a.out_pay) a.out_pay_user[ob + r] = pay;
+  };
+  auto pad = [&](int r) {
+    a.out_tok[ob + r] = -1;
+    if (a.out_score) a.out_score[ob + r] = __uint_as_float(0xff800000u);
+    a.out_pay[ob + r] = KVO_PAD_PAYLOAD;
+    if (a.out_pay_user && a.out_pay_user != a.out_pay) a.out_pay_user[ob + r] = KVO_PAD_PAYLOAD;
+  };
   if (n == 0) {
-    write_ranks<NT>(a, i, p, K, 0, tid);
+    for (int r = tid; r < k; r += NT) pad(r);
     if (tid == 0) write_spec(a, i, p, 0ull);
     sync();
     return true;
   }
-  const int B = 1 << log2B;
   if (tid == 0) {
     red[0] = ~0ull;
     red[1] = 0ull;
     red[2] = 0ull;
   }
   for (int b = tid; b < B; b += NT) cnt[b] = 0;
-  // candidates of every piece into K (eight loads in flight per thread), with the key range
+  // candidates of every piece into K with their cache_slots entries (eight
+  // of each in flight per thread), and the key range
   unsigned long long lo = ~0ull, hi = 0ull;
   for (uint32_t e0 = tid; e0 < n; e0 += 8 * NT) {
     uint64_t v[8];
+    int32_t c[8];
 #pragma unroll
-    for (int u = 0; u < 8; ++u) {
-      const uint32_t e = e0 + u * NT;
-      v[u] = 0;
+    for (int x = 0; x < 8; ++x) {
+      const uint32_t e = e0 + x * NT;
+      v[x] = 0;
       if (e < n) {
         int lo_c = 0, hi_c = nseg - 1;  // last segment with seg_off <= e
         while (lo_c < hi_c) {
           const int mid = (lo_c + hi_c + 1) >> 1;
           if (seg_off[mid] <= e) lo_c = mid; else hi_c = mid - 1;
         }
-        v[u] = __ldcg(a.seg_keys + ((seg0 + lo_c) * P + p) * (int64_t)k + (e - seg_off[lo_c]));
+        v[x] = __ldcg(a.seg_keys + ((seg0 + lo_c) * P + p) * (int64_t)k + (e - seg_off[lo_c]));
       }
     }
 #pragma unroll
-    for (int u = 0; u < 8; ++u) {
-      const uint32_t e = e0 + u * NT;
+    for (int x = 0; x < 8; ++x) c[x] = (e0 + x * NT < n && cs) ? cs[key_token(v[x])] : -1;
+#pragma unroll
+    for (int x = 0; x < 8; ++x) {
+      const uint32_t e = e0 + x * NT;
       if (e < n) {
-        K[e] = v[u];
-        lo = v[u] < lo ? v[u] : lo;
-        hi = v[u] > hi ? v[u] : hi;
+        K[e] = v[x];
+        KC[e] = c[x];
+        lo = v[x] < lo ? v[x] : lo;
+        hi = v[x] > hi ? v[x] : hi;
       }
     }
   }
@@ -897,22 +928,25 @@ __device__ __forceinline__ bool bucket_select(const SelectArgs& a, int i, int p,
   // scatter (pos[b] ends as the end of bucket b)
   for (uint32_t e = tid; e < n; e += NT) {
     const uint64_t x = K[e];
-    S[atomicAdd(&pos[bucket(x)], 1u)] = x;
+    const uint32_t j = atomicAdd(&pos[bucket(x)], 1u);
+    S[j] = x;
+    SC[j] = KC[e];
   }
   sync();
-  // rank within the bucket; the winners go to K in rank order
+  // rank within the bucket; winners written at their rank
   for (uint32_t j = tid; j < n; j += NT) {
     const uint64_t x = S[j];
     const uint32_t b = bucket(x);
     const uint32_t end = pos[b], beg = end - cnt[b];
     uint32_t r = beg;
     for (uint32_t t = beg; t < end; ++t) r += S[t] > x ? 1u : 0u;
-    if (r < (uint32_t)k) K[r] = x;
+    if (r < (uint32_t)k) {
+      emit((int)r, x, SC[j]);
+      if (r == (uint32_t)k - 1) write_spec(a, i, p, x);
+    }
   }
-  sync();
-  const int count = n < (uint32_t)k ? (int)n : k;
-  write_ranks<NT>(a, i, p, K, count, tid);
-  if (tid == 0) write_spec(a, i, p, count == k ? K[k - 1] : 0ull);
+  for (int r = (int)n + tid; r < k; r += NT) pad(r);
+  if (tid == 0 && n < (uint32_t)k) write_spec(a, i, p, 0ull);
   sync();
   return true;
 }
@@ -934,7 +968,8 @@ template <int NT, class Sync>
 __device__ __forceinline__ uint32_t residency_body(const ResidencyArgs& a, int i, uint32_t* bitmap, int32_t* M,
                                                    int32_t* V, uint32_t* wsum, int tid, Sync sync,
                                                    int32_t* status_out) {
-  constexpr int kB = 8;  // loads in flight per thread in the list passes
+  constexpr int kB = 8;    // loads in flight per thread in the list passes
+  constexpr int kTB = 16;  // and in the top-k passes
   const int C = a.C, PK = a.P * a.k;
   const int nwords = (C + 31) >> 5;
   const int u = a.units[i];
@@ -967,16 +1002,16 @@ __device__ __forceinline__ uint32_t residency_body(const ResidencyArgs& a, int i
 
   if (status == KVO_OK) {
     // payload says hit (slot) or miss (token): mark hit slots and miss tokens
-    for (int e0 = tid; e0 < PK; e0 += kB * NT) {
-      int32_t t[kB], pv[kB];
+    for (int e0 = tid; e0 < PK; e0 += kTB * NT) {
+      int32_t t[kTB], pv[kTB];
 #pragma unroll
-      for (int x = 0; x < kB; ++x) {
+      for (int x = 0; x < kTB; ++x) {
         const int e = e0 + x * NT;
         t[x] = e < PK ? tok[e] : -1;
         pv[x] = e < PK ? pay[e] : -1;
       }
 #pragma unroll
-      for (int x = 0; x < kB; ++x) {
+      for (int x = 0; x < kTB; ++x) {
         if (t[x] < 0) continue;
         if (pv[x] >= 0) {
           if (pv[x] < C) atomicOr(&bitmap[pv[x] >> 5], 1u << (pv[x] & 31));
@@ -990,16 +1025,22 @@ __device__ __forceinline__ uint32_t residency_body(const ResidencyArgs& a, int i
     // distinct misses in token order; the bitmap words are cleared behind
     const int per = (tw + NT - 1) / NT;
     const int w0 = tid * per, w1 = min(tw, w0 + per);
+    constexpr int kWC = 4;  // words kept in registers between the two passes
+    uint32_t wc[kWC];
     uint32_t c = 0;
+#pragma unroll
+    for (int x = 0; x < kWC; ++x) {
+      wc[x] = w0 + x < w1 ? __ldcg(&tbm[w0 + x]) : 0u;
+      c += __popc(wc[x]);
+    }
 #pragma unroll 8
-    for (int w = w0; w < w1; ++w) c += __popc(__ldcg(&tbm[w]));
+    for (int w = w0 + kWC; w < w1; ++w) c += __popc(__ldcg(&tbm[w]));
     uint32_t total;
     uint32_t pos = block_excl_scan<NT>(c, wsum, &total, tid, sync);
     m = total;
     if (c) {
-      for (int w = w0; w < w1; ++w) {
-        uint32_t bits = __ldcg(&tbm[w]);
-        if (!bits) continue;
+      auto emit_word = [&](int w, uint32_t bits) {
+        if (!bits) return;
         tbm[w] = 0;
         while (bits) {
           const int b = __ffs(bits) - 1;
@@ -1007,7 +1048,10 @@ __device__ __forceinline__ uint32_t residency_body(const ResidencyArgs& a, int i
           if (pos < (uint32_t)PK) M[pos] = w * 32 + b;
           ++pos;
         }
-      }
+      };
+#pragma unroll
+      for (int x = 0; x < kWC; ++x) emit_word(w0 + x, wc[x]);
+      for (int w = w0 + kWC; w < w1; ++w) emit_word(w, __ldcg(&tbm[w]));
     }
     uint32_t hc = 0;
     for (int w = tid; w < nwords; w += NT) hc += __popc(bitmap[w]);
@@ -1029,10 +1073,17 @@ __device__ __forceinline__ uint32_t residency_body(const ResidencyArgs& a, int i
     const int j0 = tid * per, j1 = min(C, j0 + per);
     // slots outside [0, C) never come from a valid list; they count as touched
     auto hit = [&](int s) { return (unsigned)s >= (unsigned)C || ((bitmap[s >> 5] >> (s & 31)) & 1u) != 0; };
-    // the thread's run of the LRU list, kB entries per batch of loads
+    // the thread's run of the LRU list: its first kB entries stay in
+    // registers, the rest is read in batches of kB loads
+    int32_t cv[kB];
+#pragma unroll
+    for (int x = 0; x < kB; ++x) cv[x] = j0 + x < j1 ? cur[j0 + x] : 0;
     auto count_untouched = [&]() {
       uint32_t c = 0;
-      for (int j = j0; j < j1; j += kB) {
+#pragma unroll
+      for (int x = 0; x < kB; ++x)
+        if (j0 + x < j1) c += hit(cv[x]) ? 0u : 1u;
+      for (int j = j0 + kB; j < j1; j += kB) {
         int32_t v[kB];
 #pragma unroll
         for (int x = 0; x < kB; ++x) v[x] = j + x < j1 ? cur[j + x] : 0;
@@ -1046,7 +1097,10 @@ __device__ __forceinline__ uint32_t residency_body(const ResidencyArgs& a, int i
       // victims: the first m slots of the LRU list that were not hit
       uint32_t total;
       uint32_t rank = block_excl_scan<NT>(count_untouched(), wsum, &total, tid, sync);
-      for (int j = j0; j < j1 && rank < m; ++j) {
+#pragma unroll
+      for (int x = 0; x < kB; ++x)
+        if (j0 + x < j1 && rank < m && !hit(cv[x])) V[rank++] = cv[x];
+      for (int j = j0 + kB; j < j1 && rank < m; ++j) {
         const int s = cur[j];
         if (!hit(s)) V[rank++] = s;
       }
@@ -1081,7 +1135,10 @@ __device__ __forceinline__ uint32_t residency_body(const ResidencyArgs& a, int i
       // new list: untouched slots in their order, then the touched ones in slot order
       uint32_t kept;
       uint32_t q = block_excl_scan<NT>(count_untouched(), wsum, &kept, tid, sync);
-      for (int j = j0; j < j1; ++j) {
+#pragma unroll
+      for (int x = 0; x < kB; ++x)
+        if (j0 + x < j1 && !hit(cv[x]) && q < (uint32_t)C) nxt[q++] = cv[x];
+      for (int j = j0 + kB; j < j1; ++j) {
         const int s = cur[j];
         if (!hit(s) && q < (uint32_t)C) nxt[q++] = s;
       }
@@ -1107,16 +1164,16 @@ __device__ __forceinline__ uint32_t residency_body(const ResidencyArgs& a, int i
     // (victims are never hit), a miss takes the victim its rank among the
     // distinct misses (M, ascending) points to
     const int mm = (int)(m < (uint32_t)PK ? m : (uint32_t)PK);
-    for (int e0 = tid; e0 < PK; e0 += kB * NT) {
-      int32_t t[kB], pv[kB];
+    for (int e0 = tid; e0 < PK; e0 += kTB * NT) {
+      int32_t t[kTB], pv[kTB];
 #pragma unroll
-      for (int x = 0; x < kB; ++x) {
+      for (int x = 0; x < kTB; ++x) {
         const int e = e0 + x * NT;
         t[x] = e < PK ? tok[e] : -1;
         pv[x] = e < PK ? pay[e] : -1;
       }
 #pragma unroll
-      for (int x = 0; x < kB; ++x) {
+      for (int x = 0; x < kTB; ++x) {
         const int e = e0 + x * NT;
         if (e >= PK) break;
         int32_t slot = -1;

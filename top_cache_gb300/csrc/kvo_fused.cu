@@ -372,16 +372,11 @@ __device__ __forceinline__ void select_positions(const SelectArgs& a, int i, int
   const uint32_t words = (uint32_t)(bytes / 8);
   int log2B = 12;
   while ((1 << log2B) > 8 * NTG || (log2B > 9 && (8u << log2B) > bytes / 4)) --log2B;
-  const uint32_t bkeys = words > (1u << log2B) + 4 ? (words - (1u << log2B) - 4) / 2 : 0u;
-  uint32_t* cnt = reinterpret_cast<uint32_t*>(keys + 2 * bkeys);
-  uint32_t* pos = cnt + (1 << log2B);
-  unsigned long long* red = reinterpret_cast<unsigned long long*>(pos + (1 << log2B));
   for (int p = p0; p < a.P; p += step) {
     bool done = false;
     if (nseg + 1 <= seg_cap) {
       segment_offsets<NTG>(a, p, 1, pb, nseg, seg_off, gtid, sync);
-      done = bucket_select<NTG>(a, i, p, pb, nseg, seg_off, keys, keys + bkeys, bkeys, cnt, pos, log2B, red, hist,
-                                gtid, sync);
+      done = bucket_select<NTG>(a, i, p, pb, nseg, seg_off, region, bytes, log2B, hist, gtid, sync);
     }
     if (!done)
       select_body<NTG>(a, i, p, pb, nseg, false, keys, words - (uint32_t)kpad, keys + (words - kpad), hist, rx, gtid,

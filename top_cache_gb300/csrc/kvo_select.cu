@@ -287,12 +287,9 @@ __global__ void __launch_bounds__(kScoreThreads, 1) score_kernel(SelectArgs a) {
 // ---------------------------------------------------------------------------
 __global__ void __launch_bounds__(kSelThreads) select_kernel(SelectArgs a) {
   extern __shared__ __align__(128) uint8_t smem[];
-  // bucket sort: K, S [kSelBucketKeys], cnt, pos [1 << kSelLog2B], red;
-  // fallback: keys [kSelSmemKeys], sorted [kpad] over the same bytes
+  // bucket sort over all kSelSmemBytes, or the fallback's keys [kSelSmemKeys]
+  // and sorted [kpad] over the same bytes
   uint64_t* base = reinterpret_cast<uint64_t*>(smem);
-  uint32_t* cnt = reinterpret_cast<uint32_t*>(base + 2 * kSelBucketKeys);
-  uint32_t* pos = cnt + (1 << kSelLog2B);
-  unsigned long long* red = reinterpret_cast<unsigned long long*>(pos + (1 << kSelLog2B));
   __shared__ uint32_t hist[256];
   __shared__ __align__(8) uint32_t rx[10];
   __shared__ uint32_t seg_off[kSelMaxSegs + 1];
@@ -322,8 +319,8 @@ __global__ void __launch_bounds__(kSelThreads) select_kernel(SelectArgs a) {
     }
     return;
   }
-  if (!few || !bucket_select<kSelThreads>(a, i, p, seg0, nseg, seg_off, base, base + kSelBucketKeys, kSelBucketKeys,
-                                          cnt, pos, kSelLog2B, red, hist, tid, sync))
+  if (!few || !bucket_select<kSelThreads>(a, i, p, seg0, nseg, seg_off, smem, kSelSmemBytes, kSelLog2B, hist, tid,
+                                          sync))
     select_body<kSelThreads>(a, i, p, seg0, nseg, false, base, kSelSmemKeys, base + kSelSmemKeys, hist, rx, tid,
                              sync);
 }

@@ -39,7 +39,7 @@ KVO_GATHER_BULK = 1
 
 EXPORTED = ("kvo_create", "kvo_destroy", "kvo_host_rows", "kvo_prefill", "kvo_append", "kvo_step",
             "kvo_select_workspace_size", "kvo_select", "kvo_reset", "kvo_profile_read",
-            "kvo_set_option", "kvo_get_stats", "kvo_export_state", "kvo_select_noalloc",
+            "kvo_set_option", "kvo_get_option", "kvo_get_stats", "kvo_export_state", "kvo_select_noalloc",
             "kvo_last_error")
 
 
@@ -106,6 +106,8 @@ def lib():
             L.kvo_profile_read.argtypes = [vp, vp, vp, i32]
             L.kvo_set_option.restype = ctypes.c_int
             L.kvo_set_option.argtypes = [vp, i32, i64]
+            L.kvo_get_option.restype = ctypes.c_int
+            L.kvo_get_option.argtypes = [vp, i32, ctypes.POINTER(ctypes.c_int64)]
             L.kvo_get_stats.restype = ctypes.c_int
             L.kvo_get_stats.argtypes = [vp, ctypes.POINTER(KvoStats)]
             L.kvo_export_state.restype = ctypes.c_int
@@ -229,6 +231,12 @@ def kvo_set_option(h, key, value):
     return _check(lib().kvo_set_option(h, key, value))
 
 
+def kvo_get_option(h, key):
+    v = ctypes.c_int64(0)
+    _check(lib().kvo_get_option(h, key, ctypes.byref(v)))
+    return v.value
+
+
 def kvo_get_stats(h):
     s = KvoStats()
     _check(lib().kvo_get_stats(h, ctypes.byref(s)))
@@ -309,6 +317,9 @@ class Kvo:
 
     def set_option(self, key, value):
         return kvo_set_option(self.h, key, value)
+
+    def get_option(self, key):
+        return kvo_get_option(self.h, key)
 
     def stats(self):
         return kvo_get_stats(self.h)
