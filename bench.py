@@ -287,6 +287,8 @@ def run_kvo(args, log):
     kv.set_option(K.KVO_OPT_GATHER_MODE, K.KVO_GATHER_BULK if args.gather == "bulk" else K.KVO_GATHER_LDG)
     kv.set_option(K.KVO_OPT_GROUPS, args.groups)
     kv.set_option(K.KVO_OPT_SCORE_CTAS, args.score_ctas)
+    if args.speculate is not None:
+        kv.set_option(K.KVO_OPT_SPECULATE, args.speculate)
     if args.path != "auto":
         kv.set_option(K.KVO_OPT_FUSED, 1 if args.path == "fused" else 0)
     if args.path != "staged":
@@ -619,6 +621,8 @@ def main(argv=None):
                     help="fused: one cooperative launch per step; staged: one launch per stage; "
                          "auto: the library's default for the configuration")
     ap.add_argument("--gather-ctas", type=int, default=None, help="fused step: CTAs that only fill rows")
+    ap.add_argument("--speculate", type=int, default=None,
+                    help="speculative threshold margin in permille (library default 900)")
     ap.add_argument("--piece-tokens", type=int, default=None, help="fused step: tokens per piece")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")

@@ -182,7 +182,7 @@ cudaError_t alloc_fused_segments(kvo_handle* h) {
   const int64_t small = kvo::kSmallPieceUnits < h->U ? kvo::kSmallPieceUnits : h->U;
   const int64_t lmax = h->cfg.max_tokens, lsmall = lmax < kvo::kSmallPieceMaxLen ? lmax : kvo::kSmallPieceMaxLen;
   h->fseg_pieces = (int64_t)h->U * kvo::pieces_of(h->U, lmax, h->piece_tokens) +
-                   small * kvo::pieces_of(0, lsmall, h->piece_tokens);
+                   small * kvo::pieces_of(0, lsmall, h->piece_tokens);  // unit 0 has the finest pieces
   cudaError_t e = dalloc(&h->fseg_keys, (size_t)h->fseg_pieces * h->P * h->k);
   if (e == cudaSuccess) e = dalloc(&h->fseg_cnt, (size_t)h->fseg_pieces * h->P);
   if (e != cudaSuccess) h->fseg_pieces = 0;

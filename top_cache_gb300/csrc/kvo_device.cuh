@@ -962,12 +962,15 @@ __device__ __forceinline__ bool bucket_select(const SelectArgs& a, int i, int p,
 // to the end in slot order.  Every slot starts free with last_use 0, so the
 // initial list 0..C-1 is in that order, and the update preserves it.
 // Shared memory: bitmap [(C+31)/32] u32, M [P*k] i32, V [P*k] i32, wsum[32].
-// Returns the miss count (0 unless the status is OK).
+// ready(m) is called once by all NT threads as soon as the m miss rows and
+// their slots (miss_tok, miss_slot) are written: before the LRU list and the
+// remap when m > 0, at the end otherwise.  Returns the miss count (0 unless
+// the status is OK).
 // ---------------------------------------------------------------------------
-template <int NT, class Sync>
+template <int NT, class Sync, class Ready>
 __device__ __forceinline__ uint32_t residency_body(const ResidencyArgs& a, int i, uint32_t* bitmap, int32_t* M,
                                                    int32_t* V, uint32_t* wsum, int tid, Sync sync,
-                                                   int32_t* status_out) {
+                                                   int32_t* status_out, Ready ready) {
   constexpr int kB = 8;    // loads in flight per thread in the list passes
   constexpr int kTB = 16;  // and in the top-k passes
   const int C = a.C, PK = a.P * a.k;
@@ -1128,6 +1131,7 @@ __device__ __forceinline__ uint32_t residency_body(const ResidencyArgs& a, int i
         }
       }
       sync();
+      ready(m);  // the miss rows and their slots are final
       for (uint32_t r = tid; r < m; r += NT) atomicOr(&bitmap[V[r] >> 5], 1u << (V[r] & 31));
     }
     sync();
@@ -1212,6 +1216,7 @@ __device__ __forceinline__ uint32_t residency_body(const ResidencyArgs& a, int i
   }
   if (status_out) *status_out = status;
   sync();
+  if (m == 0) ready(0u);
   return m;
 }
 

@@ -434,10 +434,12 @@ __device__ __forceinline__ void finish_unit(const FusedArgs& f, const FusedSmem&
   uint32_t* bitmap = reinterpret_cast<uint32_t*>(fs.region);
   int32_t* M = reinterpret_cast<int32_t*>(bitmap + nwords_pad);
   int32_t* V = M + P * k;
-  const uint32_t m = residency_body<kCT>(f.r, i, bitmap, M, V, fs.sm.hist, ctid, [] { consumer_sync(); }, nullptr);
-  __threadfence();
-  consumer_sync();
-  if (ctid < 32) publish_chunks(f, i, m, ctid);
+  // the unit's miss rows are published as soon as their slots are assigned
+  residency_body<kCT>(f.r, i, bitmap, M, V, fs.sm.hist, ctid, [] { consumer_sync(); }, nullptr, [&](uint32_t m) {
+    __threadfence();
+    consumer_sync();
+    if (ctid < 32) publish_chunks(f, i, m, ctid);
+  });
 }
 
 template <int PP>

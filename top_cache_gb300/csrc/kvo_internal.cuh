@@ -285,12 +285,19 @@ struct ResetArgs {
 };
 
 // Tokens per scoring piece of listed unit i (length len) in the fused step.
-// The first units are cut four times finer (when they are not long), so that
-// they complete, and their miss rows can start moving, early in the step.
+// The first units are cut finer (when they are not long): the first
+// kTinyPieceUnits eight times, the next ones up to kSmallPieceUnits four
+// times, so that they complete, and their miss rows start moving, early in
+// the step.
+constexpr int kTinyPieceUnits = 4;
 constexpr int kSmallPieceUnits = 16;
 constexpr int64_t kSmallPieceMaxLen = 65536;
 __host__ __device__ inline int64_t piece_tokens_of(int i, int64_t len, int piece_tokens) {
-  if (i < kSmallPieceUnits && len <= kSmallPieceMaxLen && piece_tokens >= 512) return (piece_tokens / 4) & ~127;
+  if (i < kSmallPieceUnits && len <= kSmallPieceMaxLen) {
+    const int div = i < kTinyPieceUnits ? 8 : 4;
+    const int64_t ps = (piece_tokens / div) & ~127;
+    if (ps >= 128) return ps;
+  }
   return piece_tokens;
 }
 __host__ __device__ inline int64_t pieces_of(int i, int64_t len, int piece_tokens) {

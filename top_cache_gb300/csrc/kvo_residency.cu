@@ -56,7 +56,7 @@ __global__ void __launch_bounds__(kResThreads) residency_kernel(ResidencyArgs a)
   __shared__ uint32_t sc[8];
   const int tid = threadIdx.x;
   auto sync = [] { __syncthreads(); };
-  dev::residency_body<kResThreads>(a, blockIdx.x, bitmap, M, V, wsum, tid, sync, nullptr);
+  dev::residency_body<kResThreads>(a, blockIdx.x, bitmap, M, V, wsum, tid, sync, nullptr, [](uint32_t) {});
 
   // the last CTA writes the prefix sums of the miss counts
   __threadfence();
