@@ -298,7 +298,6 @@ def run_kvo(args, log):
             kv.set_option(K.KVO_OPT_PIECE_TOKENS, args.piece_tokens)
     seq = Sequence(kv, inp, wl)
     stream = torch.cuda.current_stream(device)
-    path = "fused" if kv.get_option(K.KVO_OPT_FUSED) else "staged"
 
     # warm-up (the first step of the sequence is the cold, all-miss step)
     for _ in range(args.warmup):
@@ -336,6 +335,8 @@ def run_kvo(args, log):
     sampler.stop()
     clocks = sampler.summary(t_wall0, t_wall1)
 
+    fused_frac = (st1["fused_steps"] - st0["fused_steps"]) / args.steps
+    path = "fused" if fused_frac == 1 else "staged" if fused_frac == 0 else "mixed (%.0f%% fused)" % (100 * fused_frac)
     max_ms = reduce_max(total_ms, world, device)
     value = whole_job_rate(U, args.steps, max_ms, world)
 

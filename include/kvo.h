@@ -98,6 +98,7 @@ typedef struct kvo_stats {
   uint64_t bytes_d2h;
   uint64_t timeouts;        /* bounded device waits that expired */
   uint64_t rescored;        /* units rescored because a speculative threshold was too high */
+  uint64_t fused_steps;     /* kvo_step calls that ran as one fused launch (KVO_OPT_FUSED) */
 } kvo_stats;
 
 /* Options for kvo_set_option. */
@@ -113,13 +114,17 @@ typedef struct kvo_stats {
                                    rescored exactly in the same call (default 900) */
 #define KVO_OPT_FUSED 7         /* 1: kvo_step is one cooperative launch that overlaps the scoring of
                                    some units with the select, residency and miss-row fill of
-                                   others; 0: one launch per stage.  Default 1 when the
-                                   configuration fits the fused layout and hot_capacity <= 65536
-                                   (longer LRU lists favour the staged step), else 0.  KVO_EINVAL
-                                   for 1 when it does not fit.  The fused step moves miss rows
-                                   with bulk async copies and ignores KVO_OPT_GATHER_MODE, GROUPS
-                                   and SCORE_CTAS. */
-#define KVO_OPT_GATHER_CTAS 8   /* fused step: CTAs that only fill miss rows, 0 .. SMs-1 (default 16);
+                                   others; 0: one launch per stage; 2 (default): per call, the
+                                   fused launch when the configuration fits its layout,
+                                   hot_capacity <= 65536 and the miss rows of the previous step
+                                   amount to at least 1.5% of the indexer key bytes (the staged
+                                   step wins when few rows move or the LRU lists are long), else
+                                   the staged one.  Both give identical results.  When the
+                                   configuration does not fit the fused layout the default is 0
+                                   and setting 1 or 2 returns KVO_EINVAL.  The fused step moves
+                                   miss rows with bulk async copies and ignores
+                                   KVO_OPT_GATHER_MODE, GROUPS and SCORE_CTAS. */
+#define KVO_OPT_GATHER_CTAS 8   /* fused step: CTAs that only fill miss rows, 0 .. SMs-1 (default 8);
                                    the others score and join the fill when no piece is left */
 #define KVO_OPT_PIECE_TOKENS 9  /* fused step: tokens per scoring piece, a multiple of 128 in
                                    [128, 2^20] (default 4096); resizes scratch, synchronous */

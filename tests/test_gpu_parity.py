@@ -313,21 +313,39 @@ def test_fused_options_validated(path):
     kv = K.Kvo(1, 2, 1000, 16, 64, 2)
     try:
         for key, value in ((K.KVO_OPT_PIECE_TOKENS, 100), (K.KVO_OPT_PIECE_TOKENS, 0),
-                           (K.KVO_OPT_FUSED, 2), (K.KVO_OPT_GATHER_CTAS, -1),
+                           (K.KVO_OPT_FUSED, 3), (K.KVO_OPT_GATHER_CTAS, -1),
                            (K.KVO_OPT_GATHER_CTAS, 1 << 20)):
             with pytest.raises(K.KvoError) as e:
                 kv.set_option(key, value)
             assert e.value.code == K.KVO_EINVAL
-        assert kv.get_option(K.KVO_OPT_FUSED) == 1  # the default at this capacity
+        assert kv.get_option(K.KVO_OPT_FUSED) == 2  # the default: chosen per call
         kv.set_option(K.KVO_OPT_GATHER_CTAS, 3)
         assert kv.get_option(K.KVO_OPT_GATHER_CTAS) == 3
         kv.set_option(K.KVO_OPT_PROFILE, 1)
         q = torch.zeros((2, 2, 128), dtype=torch.bfloat16, device="cuda")
         kv.step(q)
         prof = kv.profile_read()
-        assert prof["fused"][1] == 1 and prof["score"][1] == 0
+        assert prof["fused"][1] == 1 and prof["score"][1] == 0  # no measurement yet: fused
+        assert kv.stats()["fused_steps"] == 1
     finally:
         kv.close()
+
+
+def test_paths_alternate_per_step(path):
+    # the two step paths share all persistent state (residency, LRU lists,
+    # speculative thresholds): switching between them every call stays exact
+    _once(path)
+    wl = W.reduced(W.WORKLOADS["batch16x8_32k_mtp3"], n_requests=2, n_layers=3, context=5001,
+                   topk=256, hot_capacity=600, steps=8)
+    r = Runner(wl)
+    try:
+        for s in range(r.steps):
+            r.kv.set_option(K.KVO_OPT_FUSED, s % 2)
+            r.append(wl.n_new)
+            r.compare(r.step(s))
+        assert r.kv.stats()["fused_steps"] == r.steps // 2
+    finally:
+        r.close()
 
 
 # ---------------------------------------------------------------- full sizes

@@ -65,8 +65,13 @@ struct kvo_handle {
   uint64_t wait_ns = 2000000000ull;
   // fused step (one cooperative launch per kvo_step)
   bool fused_ok = false;        // the configuration fits the fused kernel's layout
-  int fused = 0;
-  int gather_ctas = 16;
+  int fused = 2;                // KVO_OPT_FUSED mode: 0 staged, 1 fused, 2 per call
+  int gather_ctas = 8;
+  uint64_t fused_steps = 0;
+  unsigned long long* bytes_prev_host = nullptr;  // pinned, mapped: previous step's miss bytes
+  unsigned long long* bytes_prev_dev = nullptr;   // its device address
+  unsigned long long* bytes_seen = nullptr;       // device
+  uint64_t planned_steps = 0;
   int piece_tokens = 4096;
   int64_t fseg_pieces = 0;      // pieces the segment buffers hold
   int64_t* pbeg = nullptr;      // [U+1]
@@ -149,6 +154,8 @@ void free_all(kvo_handle* h) {
                  h->chunk_start, h->chunk_cnt, h->chunk_flag};
   for (void* p : dev)
     if (p) cudaFree(p);
+  if (h->bytes_seen) cudaFree(h->bytes_seen);
+  if (h->bytes_prev_host) cudaFreeHost(h->bytes_prev_host);
   if (h->host_pool) cudaFreeHost(h->host_pool);
 }
 
@@ -265,6 +272,22 @@ int grid_for(int64_t T, int G_max) {
   return (int)g;
 }
 
+// Step path of this call.  Mode 2 measures: the fused launch pays when miss
+// rows keep the host link busy for a good part of the step (it overlaps them
+// with scoring); with few rows, or long LRU lists that make its one-SM
+// finishers slow, the staged launches are faster.  The previous step's row
+// bytes come from plan through mapped host memory (one or two steps old).
+bool use_fused(kvo_handle* h, const int32_t* units, int32_t n_units) {
+  if (h->fused == 0 || !h->fused_ok) return false;
+  if (h->fused == 1) return true;
+  if (h->C > kFusedDefaultMaxCapacity) return false;
+  if (h->planned_steps < 2 || !h->bytes_prev_host) return true;
+  int64_t T = 0;
+  for (int32_t i = 0; i < n_units; ++i) T += h->len_host[(size_t)(units ? units[i] : i)];
+  const unsigned long long rows = *reinterpret_cast<volatile unsigned long long*>(h->bytes_prev_host);
+  return (double)rows >= 0.015 * (double)T * kvo::kKeyBytes;
+}
+
 // kvo_step as one fused launch (after the plan kernel).
 int fused_step(kvo_handle* h, const int32_t* du, const int32_t* units, int32_t n_units, const void* queries,
                int32_t* topk_tokens, int32_t* topk_slots, float* topk_scores, int32_t* topk_payload,
@@ -314,6 +337,8 @@ int fused_step(kvo_handle* h, const int32_t* du, const int32_t* units, int32_t n
   sa.status_init = unit_status;
   sa.piece_tokens = h->piece_tokens;
   sa.n_pieces = NP;
+  sa.bytes_prev = h->bytes_prev_dev;
+  sa.bytes_seen = h->bytes_seen;
 
   kvo::ResidencyArgs& ra = f.r;
   ra.units = du;
@@ -372,6 +397,8 @@ int fused_step(kvo_handle* h, const int32_t* du, const int32_t* units, int32_t n
   if (e == cudaSuccess) e = timed(h, KVO_PROF_FUSED, s, [&] { return kvo::launch_fused(f, h->n_sm, s); });
   if (e != cudaSuccess) return cuda_fail(e, "fused step launch");
   ++h->host_steps;
+  ++h->fused_steps;
+  ++h->planned_steps;
   return KVO_OK;
 }
 
@@ -473,9 +500,18 @@ int kvo_create(const kvo_config* cfg, kvo_handle** out) {
   if (e == cudaSuccess) e = dalloc(&h->stats, 1);
   h->fused_ok = fused_fits(h->P, h->k, h->cap, h->C);
   if (e == cudaSuccess && h->fused_ok) e = alloc_fused(h);
-  // by measurement: one fused launch wins unless the LRU lists are so long
-  // that the per-unit finishers (one SM each) dominate the step
-  h->fused = h->fused_ok && h->C <= kFusedDefaultMaxCapacity ? 1 : 0;
+  h->fused = h->fused_ok ? 2 : 0;
+  if (e == cudaSuccess) e = dalloc(&h->bytes_seen, 1);
+  if (e == cudaSuccess) e = cudaMemset(h->bytes_seen, 0, 8);
+  if (e == cudaSuccess) {
+    e = cudaHostAlloc(reinterpret_cast<void**>(&h->bytes_prev_host), 8, cudaHostAllocMapped);
+    if (e == cudaSuccess) {
+      *h->bytes_prev_host = 0;
+      e = cudaHostGetDevicePointer(reinterpret_cast<void**>(&h->bytes_prev_dev), h->bytes_prev_host, 0);
+    } else {
+      h->bytes_prev_host = nullptr;
+    }
+  }
   if (h->gather_ctas > h->n_sm - 1) h->gather_ctas = h->n_sm - 1;
   if (e != cudaSuccess) {
     free_all(h);
@@ -595,8 +631,9 @@ int kvo_step(kvo_handle* h, const int32_t* units, int32_t n_units, const void* q
   const int32_t* du = nullptr;
   int rc = resolve_units(h, units, n_units, s, &du);
   if (rc != KVO_OK) return rc;
-  if (h->fused) return fused_step(h, du, units, n_units, queries, topk_tokens, topk_slots, topk_scores,
-                                  topk_payload, unit_status, s);
+  if (use_fused(h, units, n_units))
+    return fused_step(h, du, units, n_units, queries, topk_tokens, topk_slots, topk_scores, topk_payload,
+                      unit_status, s);
   const int PK = h->P * h->k;
   int NG = h->groups < n_units ? h->groups : n_units;
   if (NG < 1) NG = 1;
@@ -647,6 +684,10 @@ int kvo_step(kvo_handle* h, const int32_t* units, int32_t n_units, const void* q
     sa.fb_any = h->fb_any;
     sa.spec_scale = spec_on ? (float)h->speculate / 1000.f : 0.f;
     sa.fallback = 0;
+    if (g == 0) {
+      sa.bytes_prev = h->bytes_prev_dev;
+      sa.bytes_seen = h->bytes_seen;
+    }
     e = timed(h, KVO_PROF_PLAN, s, [&] { return kvo::launch_plan(sa, s); });
     if (e == cudaSuccess) e = timed(h, KVO_PROF_SCORE, s, [&] { return kvo::launch_score(sa, s); });
     if (e == cudaSuccess) e = timed(h, KVO_PROF_SELECT, s, [&] { return kvo::launch_select(sa, s); });
@@ -719,6 +760,7 @@ int kvo_step(kvo_handle* h, const int32_t* units, int32_t n_units, const void* q
   }
   if (e != cudaSuccess) return cuda_fail(e, "step launch");
   ++h->host_steps;
+  ++h->planned_steps;
   return KVO_OK;
 }
 
@@ -828,8 +870,8 @@ int kvo_set_option(kvo_handle* h, int32_t key, int64_t value) {
       h->speculate = (int)value;
       return KVO_OK;
     case KVO_OPT_FUSED:
-      if (value != 0 && value != 1) return fail(KVO_EINVAL, "fused is 0 or 1");
-      if (value == 1 && !h->fused_ok) return fail(KVO_EINVAL, "configuration does not fit the fused step");
+      if (value < 0 || value > 2) return fail(KVO_EINVAL, "fused is 0, 1 or 2");
+      if (value != 0 && !h->fused_ok) return fail(KVO_EINVAL, "configuration does not fit the fused step");
       h->fused = (int)value;
       return KVO_OK;
     case KVO_OPT_GATHER_CTAS:
@@ -946,6 +988,7 @@ int kvo_get_stats(kvo_handle* h, kvo_stats* out) {
   out->bytes_d2h = d.bytes_d2h;
   out->timeouts = (err & kvo::kErrTimeout) ? 1 : 0;
   out->rescored = d.rescored;
+  out->fused_steps = h->fused_steps;
   return KVO_OK;
 }
 

@@ -213,6 +213,11 @@ struct SelectArgs {
   int32_t* status_init;        // [n]
   int32_t piece_tokens;        // multiple of the 128-token tile
   int64_t n_pieces;            // pbeg[n], checked by plan
+  // Miss-row bytes of the previous step for the host's choice of step path
+  // (nullable): plan writes stats->bytes_h2d - *bytes_seen to *bytes_prev
+  // (mapped host memory) and stores the total in *bytes_seen.
+  unsigned long long* bytes_prev;
+  unsigned long long* bytes_seen;
 };
 
 struct ResidencyArgs {

@@ -149,6 +149,11 @@ __global__ void __launch_bounds__(1024) plan_kernel(SelectArgs a) {
   if (tid == 0) {
     a.off[a.n] = carry;
     if (carry != a.T) atomicOr(a.err, kErrPlan);
+    if (a.bytes_prev && a.stats) {
+      const unsigned long long total = a.stats->bytes_h2d;
+      *reinterpret_cast<volatile unsigned long long*>(a.bytes_prev) = total - *a.bytes_seen;
+      *a.bytes_seen = total;
+    }
   }
   if (a.pbeg) {
     // pieces of the fused step: unit i owns pieces_of(i, len) of them

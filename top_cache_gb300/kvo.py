@@ -54,7 +54,7 @@ class KvoConfig(ctypes.Structure):
 class KvoStats(ctypes.Structure):
     _fields_ = [(n, ctypes.c_uint64) for n in
                 ("steps", "unit_steps", "capacity_errors", "hits", "misses", "rows_h2d",
-                 "bytes_h2d", "rows_d2h", "bytes_d2h", "timeouts", "rescored")]
+                 "bytes_h2d", "rows_d2h", "bytes_d2h", "timeouts", "rescored", "fused_steps")]
 
 
 class KvoError(RuntimeError):
