@@ -352,14 +352,20 @@ def run_kvo(args, log):
             continue
         kernels[name] = {"launches": n, "ms_total": round(ms, 4), "ms_per_launch": round(ms / n, 5),
                          "share": round(ms / max(1e-9, sum(v[0] for v in prof.values())), 4)}
+    # per-launch bytes: each step's share (a step runs either the staged or the
+    # fused launches; with the per-call choice both can appear in one run)
+    score_step = score_bytes / args.steps
+    rows_step = bytes_h2d / args.steps
     if "score" in kernels:
-        a = score_bytes / (prof["score"][0] / 1e3) / 1e9
-        kernels["score"].update(bound="hbm", bytes_per_launch=score_bytes / prof["score"][1],
+        sb = score_step * prof["score"][1]
+        a = sb / (prof["score"][0] / 1e3) / 1e9
+        kernels["score"].update(bound="hbm", bytes_per_launch=score_step,
                                 achieved_gbs=round(a, 1), peak_gbs=hbm_peak,
                                 frac=round(a / hbm_peak, 4), peak_source=hbm_src)
     if "gather" in kernels and bytes_h2d:
-        a = bytes_h2d / (prof["gather"][0] / 1e3) / 1e9
-        kernels["gather"].update(bound="host-link", bytes_per_launch=bytes_h2d / prof["gather"][1],
+        gb = rows_step * prof["gather"][1]
+        a = gb / (prof["gather"][0] / 1e3) / 1e9
+        kernels["gather"].update(bound="host-link", bytes_per_launch=rows_step,
                                  achieved_gbs=round(a, 1), peak_gbs=round(link["h2d"], 1),
                                  frac=round(a / link["h2d"], 4),
                                  peak_source="measured pinned host->device copy, this run")
@@ -367,9 +373,11 @@ def run_kvo(args, log):
         # one launch moves both the keys (HBM) and the miss rows (host link):
         # its bound is whichever takes longer at its peak
         t = prof["fused"][0] / 1e3
-        hbm_b = score_bytes + bytes_h2d
-        t_hbm, t_link = hbm_b / (hbm_peak * 1e9), bytes_h2d / (link["h2d"] * 1e9)
-        hbm_gbs, link_gbs = hbm_b / t / 1e9, bytes_h2d / t / 1e9
+        nf = prof["fused"][1]
+        rows_b = rows_step * nf
+        hbm_b = (score_step + rows_step) * nf
+        t_hbm, t_link = hbm_b / (hbm_peak * 1e9), rows_b / (link["h2d"] * 1e9)
+        hbm_gbs, link_gbs = hbm_b / t / 1e9, rows_b / t / 1e9
         if t_link >= t_hbm:
             kernels["fused"].update(bound="host-link", achieved_gbs=round(link_gbs, 1),
                                     peak_gbs=round(link["h2d"], 1), frac=round(t_link / t, 4),
@@ -377,7 +385,7 @@ def run_kvo(args, log):
         else:
             kernels["fused"].update(bound="hbm", achieved_gbs=round(hbm_gbs, 1), peak_gbs=hbm_peak,
                                     frac=round(t_hbm / t, 4), peak_source=hbm_src)
-        kernels["fused"].update(bytes_per_launch=hbm_b / prof["fused"][1], hbm_gbs=round(hbm_gbs, 1),
+        kernels["fused"].update(bytes_per_launch=hbm_b / nf, hbm_gbs=round(hbm_gbs, 1),
                                 host_link_gbs=round(link_gbs, 1),
                                 hbm_frac=round(hbm_gbs / hbm_peak, 4),
                                 host_link_frac=round(link_gbs / link["h2d"], 4))
