@@ -77,6 +77,7 @@ struct kvo_handle {
   int64_t* pbeg = nullptr;      // [U+1]
   int32_t* pdone = nullptr;     // [U]
   unsigned long long* ctr = nullptr;  // [4]
+  uint32_t* plan_flag = nullptr;      // [1]
   uint64_t* fseg_keys = nullptr;      // [pieces][P][k]
   int32_t* fseg_cnt = nullptr;        // [pieces][P]
   int32_t* chunk_unit = nullptr;
@@ -150,7 +151,7 @@ void free_all(kvo_handle* h) {
                  h->all_units, h->units_dev, h->off, h->gthr, h->spec, h->qn_prev, h->qn_cur,
                  h->tspec, h->fb, h->fb_any, h->tok_bits, h->order, h->order_par, h->seg_keys, h->seg_cnt, h->sel_pay,
                  h->miss_tok, h->miss_slot, h->miss_cnt, h->miss_off, h->done_ctr, h->err,
-                 h->stats, h->pbeg, h->pdone, h->ctr, h->fseg_keys, h->fseg_cnt, h->chunk_unit,
+                 h->stats, h->pbeg, h->pdone, h->ctr, h->plan_flag, h->fseg_keys, h->fseg_cnt, h->chunk_unit,
                  h->chunk_start, h->chunk_cnt, h->chunk_flag};
   for (void* p : dev)
     if (p) cudaFree(p);
@@ -203,6 +204,8 @@ cudaError_t alloc_fused(kvo_handle* h) {
   cudaError_t e = dalloc(&h->pbeg, U + 1);
   if (e == cudaSuccess) e = dalloc(&h->pdone, U);
   if (e == cudaSuccess) e = dalloc(&h->ctr, 4);
+  if (e == cudaSuccess) e = dalloc(&h->plan_flag, 1);
+  if (e == cudaSuccess) e = cudaMemset(h->plan_flag, 0, 4);
   if (e == cudaSuccess) e = dalloc(&h->chunk_unit, (size_t)h->chunk_cap);
   if (e == cudaSuccess) e = dalloc(&h->chunk_start, (size_t)h->chunk_cap);
   if (e == cudaSuccess) e = dalloc(&h->chunk_cnt, (size_t)h->chunk_cap);
@@ -288,7 +291,7 @@ bool use_fused(kvo_handle* h, const int32_t* units, int32_t n_units) {
   return (double)rows >= 0.015 * (double)T * kvo::kKeyBytes;
 }
 
-// kvo_step as one fused launch (after the plan kernel).
+// kvo_step as one fused launch (its CTA 0 plans the step).
 int fused_step(kvo_handle* h, const int32_t* du, const int32_t* units, int32_t n_units, const void* queries,
                int32_t* topk_tokens, int32_t* topk_slots, float* topk_scores, int32_t* topk_payload,
                int32_t* unit_status, cudaStream_t s) {
@@ -392,9 +395,10 @@ int fused_step(kvo_handle* h, const int32_t* du, const int32_t* units, int32_t n
   f.epoch = h->epoch;
   f.n_gather = h->gather_ctas < h->n_sm ? h->gather_ctas : h->n_sm - 1;
   f.smem_bytes = (int)kvo::fused_smem_bytes(h->P, h->k, h->cap);
+  f.plan_flag = h->plan_flag;
 
-  cudaError_t e = timed(h, KVO_PROF_PLAN, s, [&] { return kvo::launch_plan(sa, s); });
-  if (e == cudaSuccess) e = timed(h, KVO_PROF_FUSED, s, [&] { return kvo::launch_fused(f, h->n_sm, s); });
+  // the plan runs inside the fused launch (its CTA 0)
+  cudaError_t e = timed(h, KVO_PROF_FUSED, s, [&] { return kvo::launch_fused(f, h->n_sm, s); });
   if (e != cudaSuccess) return cuda_fail(e, "fused step launch");
   ++h->host_steps;
   ++h->fused_steps;

@@ -952,6 +952,133 @@ __device__ __forceinline__ bool bucket_select(const SelectArgs& a, int i, int p,
 }
 
 // ---------------------------------------------------------------------------
+// plan (all NT threads of a CTA; warp_sums[32] and carry in shared memory):
+// off[i] = sum of len[units[j]] for j < i (checked against T); the unit's
+// shared thresholds zeroed; squared query norms and speculative start
+// thresholds; with pbeg set, the piece table, counters and statuses of the
+// fused step; the previous step's miss bytes to the host mirror.
+// ---------------------------------------------------------------------------
+template <int NT>
+__device__ __forceinline__ void plan_body(const SelectArgs& a, int tid, int64_t* warp_sums, int64_t* carry_p) {
+  int64_t& carry = *carry_p;
+  const int lane = tid & 31, w = tid >> 5;
+  if (tid == 0) carry = 0;
+  __syncthreads();
+  for (int base = 0; base < a.n; base += NT) {
+    const int i = base + tid;
+    const int64_t v = i < a.n ? (int64_t)a.len[a.units[i]] : 0;
+    int64_t incl = v;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int64_t y = __shfl_up_sync(kFull, incl, o);
+      if (lane >= o) incl += y;
+    }
+    if (lane == 31) warp_sums[w] = incl;
+    __syncthreads();
+    if (w == 0) {
+      int64_t s = warp_sums[lane];
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int64_t y = __shfl_up_sync(kFull, s, o);
+        if (lane >= o) s += y;
+      }
+      warp_sums[lane] = s;
+    }
+    __syncthreads();
+    const int64_t excl = carry + (w ? warp_sums[w - 1] : 0) + incl - v;
+    if (i < a.n) a.off[i] = excl;
+    __syncthreads();
+    if (tid == NT - 1) carry = excl + v;
+    __syncthreads();
+  }
+  for (int e = tid; e < a.n * a.P; e += NT) {
+    a.gthr[e] = 0;
+    if (!a.tspec) continue;
+    const int i = e / a.P, p = e - (e / a.P) * a.P;
+    const int u = a.units[i];
+    // squared query norm (fp32; only steers the speculative threshold)
+    const uint4* q = reinterpret_cast<const uint4*>(a.queries + (int64_t)e * kDim);
+    float s2 = 0.f;
+#pragma unroll 8
+    for (int c = 0; c < kDim / 8; ++c) {
+      const uint4 v = q[c];
+      const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+      for (int x = 0; x < 4; ++x) s2 += bf_lo(w[x]) * bf_lo(w[x]) + bf_hi(w[x]) * bf_hi(w[x]);
+    }
+    if (a.qn_cur) a.qn_cur[e] = s2;
+    uint64_t t = 0;
+    if (a.spec && a.qn_prev && a.spec_scale > 0.f) {
+      const uint64_t kth = a.spec[(int64_t)u * a.P + p];
+      const float sk = key_score(kth);
+      const float prev = a.qn_prev[(int64_t)u * a.P + p];
+      const int64_t vis = (int64_t)a.len[u] - (a.P - 1 - p);
+      if (kth != 0 && sk > 0.f && prev > 0.f && s2 > 0.f && vis > a.k) {
+        const float ts = sk * sqrtf(s2 / prev) * a.spec_scale;
+        if (ts > 0.f) t = (uint64_t)order_bits(ts) << 32;
+      }
+    }
+    a.tspec[e] = t;
+  }
+  if (a.fb) {
+    for (int i = tid; i < a.n; i += NT) a.fb[i] = 0;
+    if (tid == 0) *a.fb_any = 0;
+  }
+  if (tid == 0) {
+    a.off[a.n] = carry;
+    if (carry != a.T) atomicOr(a.err, kErrPlan);
+    if (a.bytes_prev && a.stats) {
+      const unsigned long long total = a.stats->bytes_h2d;
+      *reinterpret_cast<volatile unsigned long long*>(a.bytes_prev) = total - *a.bytes_seen;
+      *a.bytes_seen = total;
+    }
+  }
+  if (a.pbeg) {
+    // pieces of the fused step: unit i owns pieces_of(i, len) of them
+    __syncthreads();
+    if (tid == 0) carry = 0;
+    __syncthreads();
+    for (int base = 0; base < a.n; base += NT) {
+      const int i = base + tid;
+      int64_t v = 0;
+      if (i < a.n) v = pieces_of(i, a.len[a.units[i]], a.piece_tokens);
+      int64_t incl = v;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int64_t y = __shfl_up_sync(kFull, incl, o);
+        if (lane >= o) incl += y;
+      }
+      if (lane == 31) warp_sums[w] = incl;
+      __syncthreads();
+      if (w == 0) {
+        int64_t s = warp_sums[lane];
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+          const int64_t y = __shfl_up_sync(kFull, s, o);
+          if (lane >= o) s += y;
+        }
+        warp_sums[lane] = s;
+      }
+      __syncthreads();
+      const int64_t excl = carry + (w ? warp_sums[w - 1] : 0) + incl - v;
+      if (i < a.n) a.pbeg[i] = excl;
+      __syncthreads();
+      if (tid == NT - 1) carry = excl + v;
+      __syncthreads();
+    }
+    for (int i = tid; i < a.n; i += NT) {
+      a.pdone[i] = 0;
+      a.status_init[i] = KVO_ETIMEOUT;
+    }
+    if (tid < 4) a.ctr[tid] = 0ull;
+    if (tid == 0) {
+      a.pbeg[a.n] = carry;
+      if (carry != a.n_pieces) atomicOr(a.err, kErrPlan);
+    }
+  }
+}
+
+// ---------------------------------------------------------------------------
 // Residency update of one unit (listed index i) with NT threads.
 //
 // No sorting: the distinct misses come out in token order from a token

@@ -527,6 +527,20 @@ template <int PP>
 __global__ void __launch_bounds__(kFusedThreads, 1) fused_step_kernel(FusedArgs f) {
   extern __shared__ __align__(128) uint8_t smem[];
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  // CTA 0 plans the step (offsets, piece table, thresholds, counters); every
+  // CTA starts once the plan is published
+  if (blockIdx.x == 0) {
+    plan_body<kFusedThreads>(f.s, tid, reinterpret_cast<int64_t*>(smem), reinterpret_cast<int64_t*>(smem) + 32);
+    __threadfence();
+    __syncthreads();
+    if (tid == 0) *reinterpret_cast<volatile uint32_t*>(f.plan_flag) = f.epoch;
+  }
+  if (tid == 0) {
+    if (!spin_until([&] { return ld_volatile_u32(f.plan_flag) == f.epoch; }, f.s.wait_ns))
+      atomicOr(f.s.err, kErrTimeout);
+    __threadfence();
+  }
+  __syncthreads();
   if ((int)blockIdx.x >= f.n_gather) {
     FusedSmem fs;
     fs.carve(smem, f.s.P, f.s.cap, f.s.k);

@@ -324,6 +324,7 @@ struct FusedArgs {
   uint32_t epoch;              // differs between consecutive launches
   int32_t n_gather;            // CTAs 0 .. n_gather-1 only fill miss rows
   int32_t smem_bytes;          // dynamic shared memory of one CTA
+  uint32_t* plan_flag;         // == epoch once CTA 0 has run the plan
 };
 
 // Sets the thread-local message returned by kvo_last_error().
