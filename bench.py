@@ -430,6 +430,7 @@ def run_kvo(args, log):
                    "context": wl.context, "n_pos": P, "n_new": wl.n_new, "topk": k,
                    "hot_capacity": wl.hot_capacity, "drift": wl.drift,
                    "steps_per_sequence": wl.steps, "path": path,
+                   "host_pool_page": kv.get_option(K.KVO_OPT_HOST_HUGE_PAGE) or "base",
                    "gather": "bulk" if path == "fused" else args.gather, "groups": args.groups,
                    "parallelism": "replicas%d" % world,
                    "l2": "inputs larger than L2: %.2f GB of indexer keys read per step"

@@ -128,6 +128,9 @@ typedef struct kvo_stats {
                                    the others score and join the fill when no piece is left */
 #define KVO_OPT_PIECE_TOKENS 9  /* fused step: tokens per scoring piece, a multiple of 128 in
                                    [128, 2^20] (default 4096); resizes scratch, synchronous */
+#define KVO_OPT_HOST_HUGE_PAGE 10 /* read only (kvo_get_option): page size of the pinned host pool
+                                     when it is backed by transparent huge pages (pools of at
+                                     least four huge pages), 0 when it comes from cudaHostAlloc */
 #define KVO_GATHER_LDG 0  /* miss rows read by 16-byte loads from the mapped host pool */
 #define KVO_GATHER_BULK 1 /* miss rows moved by bulk async copies through shared memory */
 

@@ -5,11 +5,14 @@
 // allocation [units][stride][row_elems] bf16 that kernels read and write in
 // place over the host link; the indexer cache [units][stride][128] bf16, the
 // hot buffers [units][C][row_elems] bf16 and the residency metadata live in
-// device memory.  A decode step is five launches on the caller's stream:
-// plan -> score -> select -> residency -> gather.
+// device memory.  A decode step is either one fused cooperative launch or
+// five launches on the caller's stream: plan -> score -> select -> residency
+// -> gather.
 #include <cuda_runtime.h>
 #include <stdint.h>
+#include <stdio.h>
 #include <string.h>
+#include <sys/mman.h>
 
 #include <string>
 #include <vector>
@@ -26,6 +29,8 @@ struct kvo_handle {
   int G_max = 0;
   uint16_t* host_pool = nullptr;      // host address
   uint16_t* host_pool_dev = nullptr;  // device-visible address of the same memory
+  size_t pool_map_bytes = 0;          // > 0: mmap'ed with transparent huge pages, registered
+  size_t pool_huge_page = 0;
   uint16_t* idx = nullptr;
   uint16_t* hot = nullptr;
   int32_t* cache_slots = nullptr;
@@ -157,7 +162,12 @@ void free_all(kvo_handle* h) {
     if (p) cudaFree(p);
   if (h->bytes_seen) cudaFree(h->bytes_seen);
   if (h->bytes_prev_host) cudaFreeHost(h->bytes_prev_host);
-  if (h->host_pool) cudaFreeHost(h->host_pool);
+  if (h->host_pool && h->pool_map_bytes) {
+    cudaHostUnregister(h->host_pool);
+    munmap(h->host_pool, h->pool_map_bytes);
+  } else if (h->host_pool) {
+    cudaFreeHost(h->host_pool);
+  }
 }
 
 size_t residency_smem_bytes(int C, int P, int k) {
@@ -166,6 +176,58 @@ size_t residency_smem_bytes(int C, int P, int k) {
 }
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// Size of the kernel's transparent huge pages (0 when not offered).
+size_t thp_size() {
+  FILE* f = fopen("/sys/kernel/mm/transparent_hugepage/hpage_pmd_size", "r");
+  if (!f) return 0;
+  unsigned long long v = 0;
+  if (fscanf(f, "%llu", &v) != 1) v = 0;
+  fclose(f);
+  FILE* e = fopen("/sys/kernel/mm/transparent_hugepage/enabled", "r");
+  if (!e) return 0;
+  char buf[128] = {};
+  const size_t n = fread(buf, 1, sizeof(buf) - 1, e);
+  fclose(e);
+  buf[n] = 0;
+  if (strstr(buf, "[never]")) return 0;
+  return (size_t)v;
+}
+
+// The pinned host pool.  Rows are read at random by the GPU over the host
+// link, and with base pages the address translation of a large pool becomes
+// the limit (measured: ~200 GB/s up to ~21 GB of pool, 37-52 GB/s at 43 GB
+// with 64 KB pages, 80 GB/s with 512 MB pages).  Pools of at least four huge
+// pages are therefore mapped with transparent huge pages (madvise) and
+// registered; otherwise, or when that fails, cudaHostAlloc.
+cudaError_t alloc_host_pool(kvo_handle* h, size_t bytes) {
+  const size_t huge = thp_size();
+  if (huge >= (2u << 20) && bytes >= 4 * huge) {
+    const size_t len = (bytes + huge - 1) / huge * huge;
+    void* raw = mmap(nullptr, len + huge, PROT_READ | PROT_WRITE, MAP_PRIVATE | MAP_ANONYMOUS | MAP_NORESERVE, -1, 0);
+    if (raw != MAP_FAILED) {
+      const uintptr_t r = reinterpret_cast<uintptr_t>(raw);
+      const uintptr_t a = (r + huge - 1) / huge * huge;
+      if (a > r) munmap(raw, a - r);
+      const size_t tail = (r + len + huge) - (a + len);
+      if (tail) munmap(reinterpret_cast<void*>(a + len), tail);
+      void* p = reinterpret_cast<void*>(a);
+      if (madvise(p, len, MADV_HUGEPAGE) == 0 &&
+          cudaHostRegister(p, len, cudaHostRegisterMapped | cudaHostRegisterPortable) == cudaSuccess) {
+        h->host_pool = static_cast<uint16_t*>(p);
+        h->pool_map_bytes = len;
+        h->pool_huge_page = huge;
+        return cudaSuccess;
+      }
+      cudaGetLastError();  // clear a failed registration
+      munmap(p, len);
+    }
+  }
+  cudaError_t e = cudaHostAlloc(reinterpret_cast<void**>(&h->host_pool), bytes,
+                                cudaHostAllocMapped | cudaHostAllocPortable);
+  if (e != cudaSuccess) h->host_pool = nullptr;
+  return e;
+}
 
 // Largest hot capacity for which kvo_step takes the fused path by default.
 constexpr int kFusedDefaultMaxCapacity = 65536;
@@ -458,10 +520,8 @@ int kvo_create(const kvo_config* cfg, kvo_handle** out) {
   h->len_host.assign((size_t)h->U, 0);
 
   const size_t U = (size_t)h->U, S = (size_t)h->stride, C = (size_t)h->C, PK = (size_t)h->P * h->k;
-  cudaError_t e = cudaHostAlloc(reinterpret_cast<void**>(&h->host_pool), U * S * h->R * 2,
-                                cudaHostAllocMapped | cudaHostAllocPortable);
+  cudaError_t e = alloc_host_pool(h, U * S * h->R * 2);
   if (e != cudaSuccess) {
-    h->host_pool = nullptr;
     delete h;
     return fail(KVO_ENOMEM, std::string("pinned host pool: ") + cudaGetErrorString(e));
   }
@@ -893,6 +953,8 @@ int kvo_set_option(kvo_handle* h, int32_t key, int64_t value) {
       if (e != cudaSuccess) return fail(KVO_ENOMEM, std::string("piece segments: ") + cudaGetErrorString(e));
       return KVO_OK;
     }
+    case KVO_OPT_HOST_HUGE_PAGE:
+      return fail(KVO_EINVAL, "read-only option");
     case KVO_OPT_WAIT_LIMIT_NS:
       if (value < 1000) return fail(KVO_EINVAL, "wait limit below 1 us");
       h->wait_ns = (uint64_t)value;
@@ -914,6 +976,7 @@ int kvo_get_option(kvo_handle* h, int32_t key, int64_t* value) {
     case KVO_OPT_FUSED: *value = h->fused; return KVO_OK;
     case KVO_OPT_GATHER_CTAS: *value = h->gather_ctas; return KVO_OK;
     case KVO_OPT_PIECE_TOKENS: *value = h->piece_tokens; return KVO_OK;
+    case KVO_OPT_HOST_HUGE_PAGE: *value = (int64_t)h->pool_huge_page; return KVO_OK;
     default: return fail(KVO_EINVAL, "unknown option");
   }
 }

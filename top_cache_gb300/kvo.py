@@ -32,6 +32,7 @@ KVO_OPT_SPECULATE = 6
 KVO_OPT_FUSED = 7
 KVO_OPT_GATHER_CTAS = 8
 KVO_OPT_PIECE_TOKENS = 9
+KVO_OPT_HOST_HUGE_PAGE = 10
 PROF_KINDS = ("append", "plan", "score", "select", "residency", "gather", "reset", "rescore",
               "reselect", "fused")
 KVO_GATHER_LDG = 0
