@@ -1181,7 +1181,14 @@ __device__ __forceinline__ uint32_t residency_body(const ResidencyArgs& a, int i
       };
 #pragma unroll
       for (int x = 0; x < kWC; ++x) emit_word(w0 + x, wc[x]);
-      for (int w = w0 + kWC; w < w1; ++w) emit_word(w, __ldcg(&tbm[w]));
+      for (int w = w0 + kWC; w < w1; w += kB) {
+        uint32_t wv[kB];
+#pragma unroll
+        for (int x = 0; x < kB; ++x) wv[x] = w + x < w1 ? __ldcg(&tbm[w + x]) : 0u;
+#pragma unroll
+        for (int x = 0; x < kB; ++x)
+          if (w + x < w1) emit_word(w + x, wv[x]);
+      }
     }
     uint32_t hc = 0;
     for (int w = tid; w < nwords; w += NT) hc += __popc(bitmap[w]);
@@ -1230,9 +1237,13 @@ __device__ __forceinline__ uint32_t residency_body(const ResidencyArgs& a, int i
 #pragma unroll
       for (int x = 0; x < kB; ++x)
         if (j0 + x < j1 && rank < m && !hit(cv[x])) V[rank++] = cv[x];
-      for (int j = j0 + kB; j < j1 && rank < m; ++j) {
-        const int s = cur[j];
-        if (!hit(s)) V[rank++] = s;
+      for (int j = j0 + kB; j < j1 && rank < m; j += kB) {
+        int32_t v[kB];
+#pragma unroll
+        for (int x = 0; x < kB; ++x) v[x] = j + x < j1 ? cur[j + x] : 0;
+#pragma unroll
+        for (int x = 0; x < kB; ++x)
+          if (j + x < j1 && rank < m && !hit(v[x])) V[rank++] = v[x];
       }
       sync();
       // i-th miss (token order) takes the i-th victim
@@ -1269,9 +1280,13 @@ __device__ __forceinline__ uint32_t residency_body(const ResidencyArgs& a, int i
 #pragma unroll
       for (int x = 0; x < kB; ++x)
         if (j0 + x < j1 && !hit(cv[x]) && q < (uint32_t)C) nxt[q++] = cv[x];
-      for (int j = j0 + kB; j < j1; ++j) {
-        const int s = cur[j];
-        if (!hit(s) && q < (uint32_t)C) nxt[q++] = s;
+      for (int j = j0 + kB; j < j1; j += kB) {
+        int32_t v[kB];
+#pragma unroll
+        for (int x = 0; x < kB; ++x) v[x] = j + x < j1 ? cur[j + x] : 0;
+#pragma unroll
+        for (int x = 0; x < kB; ++x)
+          if (j + x < j1 && !hit(v[x]) && q < (uint32_t)C) nxt[q++] = v[x];
       }
       const int wper = (nwords + NT - 1) / NT;
       const int v0 = tid * wper, v1 = min(nwords, v0 + wper);
