@@ -38,6 +38,23 @@
  *  R7 capacity: |W| > capacity -> unit status ORACLE_ECAPACITY, nothing
  *               changes, slots -1.
  *  R8 append  : new rows go to the host rows only; their cache_slots are -1.
+ *  R9 int8 indexer ("FlashOffloading ... What does it mean?", the LIM C8
+ *               paragraph: Hadamard rotation and int8 quantization of the
+ *               indexer query and key, fp16 dequantization scales that follow
+ *               the indexer layout):
+ *               rotation y = H x with the 128-point Walsh-Hadamard matrix
+ *               (entries +-1, unnormalised), computed in fp32 by the fast
+ *               transform: stages h = 1, 2, ..., 64, each pair (i, i + h)
+ *               with i & h == 0 becomes (a + b, a - b);
+ *               scale s = fp16(max|y| / 127) (fp32 division, then
+ *               round-to-nearest-even to fp16), one per vector (per key, per
+ *               query position); codes c = clamp(rint(y / s), -127, 127) with
+ *               s read back as fp32 (all 0 when s = 0);
+ *               score = (((float)(sum c_q c_k) * s_q) * s_k) / 128, in that
+ *               order (the integer sum is exact; / 128 undoes the unnormalised
+ *               rotation, H H = 128 I, so the score estimates q . k); a zero
+ *               score is +0.  Keys are quantized when they are appended,
+ *               queries at each step; the bf16 keys are kept only for tests.
  */
 #include <math.h>
 #include <stdint.h>
@@ -58,6 +75,9 @@
 typedef struct oracle_unit {
   int64_t tmax;
   int32_t row_elems, topk, capacity, n_pos, keep_rows;
+  int32_t idx_int8;      /* R9: 1 = scores from the int8 indexer */
+  int8_t* kcode;         /* [tmax][128] int8 key codes (R9), or NULL */
+  uint16_t* kscale;      /* [tmax] fp16 key scales (R9), or NULL */
   int64_t len;
   uint32_t stamp;
   uint16_t* keys;        /* [tmax][128] indexer keys (device copy in the real system) */
@@ -86,6 +106,108 @@ float oracle_score(const uint16_t* q, const uint16_t* k) {
   for (int w = 8; w >= 1; w >>= 1)
     for (int j = 0; j < w; ++j) c[j] = c[j] + c[j + w];
   float s = c[0];
+  if (s == 0.0f) s = 0.0f;
+  return s;
+}
+
+/* ---- R9: int8 indexer ------------------------------------------------ */
+
+/* fp32 -> fp16 bits, round to nearest even (IEEE 754 binary16). */
+uint16_t oracle_f32_to_f16(float f) {
+  uint32_t x;
+  memcpy(&x, &f, 4);
+  const uint32_t sign = (x >> 16) & 0x8000u;
+  const int32_t exp = (int32_t)((x >> 23) & 0xffu);
+  uint32_t man = x & 0x7fffffu;
+  if (exp == 0xff) return (uint16_t)(sign | 0x7c00u | (man ? 0x200u : 0u));
+  const int32_t e = exp - 127 + 15;
+  if (e >= 31) return (uint16_t)(sign | 0x7c00u);
+  if (e <= 0) {
+    /* half subnormal: units of 2^-24; value = (1.man) 2^(exp-127) */
+    if (exp == 0) return (uint16_t)sign; /* fp32 subnormals are far below 2^-25 */
+    const uint32_t full = man | 0x800000u;
+    const int32_t shift = 14 - e;
+    if (shift > 24) return (uint16_t)sign;
+    uint32_t hm = full >> shift;
+    const uint32_t rem = full & ((1u << shift) - 1u), half = 1u << (shift - 1);
+    if (rem > half || (rem == half && (hm & 1u))) ++hm;
+    return (uint16_t)(sign | hm); /* hm == 0x400 is the smallest normal */
+  }
+  uint32_t hm = man >> 13;
+  const uint32_t rem = man & 0x1fffu;
+  int32_t he = e;
+  if (rem > 0x1000u || (rem == 0x1000u && (hm & 1u))) ++hm;
+  if (hm == 0x400u) {
+    hm = 0;
+    if (++he >= 31) return (uint16_t)(sign | 0x7c00u);
+  }
+  return (uint16_t)(sign | ((uint32_t)he << 10) | hm);
+}
+
+/* fp16 bits -> fp32 (exact). */
+float oracle_f16_to_f32(uint16_t h) {
+  const uint32_t sign = (uint32_t)(h & 0x8000u) << 16;
+  const uint32_t e = (h >> 10) & 0x1fu, m = h & 0x3ffu;
+  uint32_t x;
+  if (e == 0) {
+    float v = (float)m * 5.9604644775390625e-8f; /* m * 2^-24, exact */
+    memcpy(&x, &v, 4);
+    x |= sign;
+  } else if (e == 31) {
+    x = sign | 0x7f800000u | (m << 13);
+  } else {
+    x = sign | ((e - 15 + 127) << 23) | (m << 13);
+  }
+  float f;
+  memcpy(&f, &x, 4);
+  return f;
+}
+
+/* R9 rotation: unnormalised fast Walsh-Hadamard transform, fixed stage order. */
+void oracle_fwht128(const float* in, float* out) {
+  float y[ORACLE_DIM];
+  memcpy(y, in, sizeof(y));
+  for (int h = 1; h < ORACLE_DIM; h <<= 1)
+    for (int i = 0; i < ORACLE_DIM; ++i)
+      if ((i & h) == 0) {
+        const float a = y[i], b = y[i + h];
+        y[i] = a + b;
+        y[i + h] = a - b;
+      }
+  memcpy(out, y, sizeof(y));
+}
+
+/* R9 quantization of an already rotated vector: fp16 scale, int8 codes. */
+void oracle_quant_rotated(const float* y, int8_t* code, uint16_t* scale) {
+  float m = 0.0f;
+  for (int d = 0; d < ORACLE_DIM; ++d) {
+    const float a = fabsf(y[d]);
+    if (a > m) m = a;
+  }
+  const uint16_t s16 = oracle_f32_to_f16(m / 127.0f);
+  const float s = oracle_f16_to_f32(s16);
+  for (int d = 0; d < ORACLE_DIM; ++d) {
+    float c = s > 0.0f ? rintf(y[d] / s) : 0.0f;
+    if (c > 127.0f) c = 127.0f;
+    if (c < -127.0f) c = -127.0f;
+    code[d] = (int8_t)c;
+  }
+  *scale = s16;
+}
+
+/* R9: rotate and quantize one bf16 vector of 128. */
+void oracle_quant128(const uint16_t* x, int8_t* code, uint16_t* scale) {
+  float v[ORACLE_DIM], y[ORACLE_DIM];
+  for (int d = 0; d < ORACLE_DIM; ++d) v[d] = bf16_value(x[d]);
+  oracle_fwht128(v, y);
+  oracle_quant_rotated(y, code, scale);
+}
+
+/* R9 score of int8 codes with their fp16 scales. */
+float oracle_score_i8(const int8_t* q, uint16_t sq, const int8_t* k, uint16_t sk) {
+  int32_t dot = 0;
+  for (int d = 0; d < ORACLE_DIM; ++d) dot += (int32_t)q[d] * (int32_t)k[d];
+  float s = (((float)dot * oracle_f16_to_f32(sq)) * oracle_f16_to_f32(sk)) / 128.0f;
   if (s == 0.0f) s = 0.0f;
   return s;
 }
@@ -122,10 +244,29 @@ oracle_unit* oracle_unit_new(int64_t tmax, int32_t dim, int32_t row_elems, int32
   return u;
 }
 
+void oracle_unit_free(oracle_unit* u);
+
+/* As oracle_unit_new; idx_int8 = 1 selects the int8 indexer (R9). */
+oracle_unit* oracle_unit_new2(int64_t tmax, int32_t dim, int32_t row_elems, int32_t topk,
+                              int32_t capacity, int32_t n_pos, int32_t keep_rows, int32_t idx_int8) {
+  oracle_unit* u = oracle_unit_new(tmax, dim, row_elems, topk, capacity, n_pos, keep_rows);
+  if (!u || !idx_int8) return u;
+  u->idx_int8 = 1;
+  u->kcode = (int8_t*)malloc((size_t)(tmax > 0 ? tmax : 1) * ORACLE_DIM);
+  u->kscale = (uint16_t*)malloc((size_t)(tmax > 0 ? tmax : 1) * 2);
+  if (!u->kcode || !u->kscale) {
+    free(u->kcode); free(u->kscale);
+    u->kcode = NULL; u->kscale = NULL;
+    oracle_unit_free(u);
+    return NULL;
+  }
+  return u;
+}
+
 void oracle_unit_free(oracle_unit* u) {
   if (!u) return;
   free(u->keys); free(u->cache_slots); free(u->slot_token); free(u->last_use);
-  free(u->rows); free(u->hot); free(u);
+  free(u->rows); free(u->hot); free(u->kcode); free(u->kscale); free(u);
 }
 
 /* R8 / [LS] Decode step 1-2: new rows land at their logical slots len..len+n-1. */
@@ -133,6 +274,10 @@ int32_t oracle_append(oracle_unit* u, int32_t n_tok, const uint16_t* rows, const
   if (n_tok < 0) return ORACLE_EINVAL;
   if (u->len + n_tok > u->tmax) return ORACLE_ERANGE;
   memcpy(u->keys + (size_t)u->len * ORACLE_DIM, keys, (size_t)n_tok * ORACLE_DIM * 2);
+  if (u->idx_int8) /* R9: keys are quantized once, when they arrive */
+    for (int32_t j = 0; j < n_tok; ++j)
+      oracle_quant128(keys + (size_t)j * ORACLE_DIM, u->kcode + (size_t)(u->len + j) * ORACLE_DIM,
+                      u->kscale + u->len + j);
   if (u->keep_rows && rows)
     memcpy(u->rows + (size_t)u->len * u->row_elems, rows, (size_t)n_tok * u->row_elems * 2);
   for (int32_t j = 0; j < n_tok; ++j) u->cache_slots[u->len + j] = -1;
@@ -166,9 +311,20 @@ static int cmp_lru(const void* a, const void* b) {
   return (x->slot > y->slot) - (x->slot < y->slot);
 }
 
+/* Score of token t for query q under the unit's indexer (R1 or R9). */
+static float unit_score(const oracle_unit* u, const uint16_t* q, const int8_t* qcode, uint16_t qscale,
+                        int64_t t) {
+  if (u->idx_int8)
+    return oracle_score_i8(qcode, qscale, u->kcode + (size_t)t * ORACLE_DIM, u->kscale[t]);
+  return oracle_score(q, u->keys + (size_t)t * ORACLE_DIM);
+}
+
 /* Scores of every visible token for one query (used by tests). */
 void oracle_scores(const oracle_unit* u, const uint16_t* q, int64_t n, float* out) {
-  for (int64_t t = 0; t < n && t < u->len; ++t) out[t] = oracle_score(q, u->keys + (size_t)t * ORACLE_DIM);
+  int8_t qc[ORACLE_DIM];
+  uint16_t qs = 0;
+  if (u->idx_int8) oracle_quant128(q, qc, &qs);
+  for (int64_t t = 0; t < n && t < u->len; ++t) out[t] = unit_score(u, q, qc, qs, t);
 }
 
 /*
@@ -197,8 +353,11 @@ int32_t oracle_step(oracle_unit* u, const uint16_t* queries, int32_t* tok, float
     int64_t vis = u->len - (P - 1 - p); /* R3 */
     if (vis < 0) vis = 0;
     const uint16_t* q = queries + (size_t)p * ORACLE_DIM;
+    int8_t qc[ORACLE_DIM];
+    uint16_t qs = 0;
+    if (u->idx_int8) oracle_quant128(q, qc, &qs); /* R9: the query, each step */
     for (int64_t t = 0; t < vis; ++t) {
-      buf[t].score = oracle_score(q, u->keys + (size_t)t * ORACLE_DIM);
+      buf[t].score = unit_score(u, q, qc, qs, t);
       buf[t].token = (int32_t)t;
     }
     qsort(buf, (size_t)vis, sizeof(scored_t), cmp_scored);
@@ -314,3 +473,5 @@ uint32_t* oracle_last_use(oracle_unit* u) { return u->last_use; }
 uint16_t* oracle_hot(oracle_unit* u) { return u->hot; }
 uint16_t* oracle_rows(oracle_unit* u) { return u->rows; }
 uint16_t* oracle_keys(oracle_unit* u) { return u->keys; }
+int8_t* oracle_kcode(oracle_unit* u) { return u->kcode; }
+uint16_t* oracle_kscale(oracle_unit* u) { return u->kscale; }

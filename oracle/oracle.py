@@ -46,6 +46,21 @@ def lib():
             vp, i32, i64 = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64
             L.oracle_unit_new.restype = vp
             L.oracle_unit_new.argtypes = [i64, i32, i32, i32, i32, i32, i32]
+            L.oracle_unit_new2.restype = vp
+            L.oracle_unit_new2.argtypes = [i64, i32, i32, i32, i32, i32, i32, i32]
+            u16, f32 = ctypes.c_uint16, ctypes.c_float
+            L.oracle_f32_to_f16.restype = u16
+            L.oracle_f32_to_f16.argtypes = [f32]
+            L.oracle_f16_to_f32.restype = f32
+            L.oracle_f16_to_f32.argtypes = [u16]
+            L.oracle_fwht128.restype = None
+            L.oracle_fwht128.argtypes = [vp, vp]
+            L.oracle_quant_rotated.restype = None
+            L.oracle_quant_rotated.argtypes = [vp, vp, vp]
+            L.oracle_quant128.restype = None
+            L.oracle_quant128.argtypes = [vp, vp, vp]
+            L.oracle_score_i8.restype = f32
+            L.oracle_score_i8.argtypes = [vp, u16, vp, u16]
             L.oracle_unit_free.restype = None
             L.oracle_unit_free.argtypes = [vp]
             L.oracle_append.restype = i32
@@ -65,7 +80,8 @@ def lib():
             L.oracle_stamp.restype = ctypes.c_uint32
             L.oracle_stamp.argtypes = [vp]
             for name in ("oracle_cache_slots", "oracle_slot_token", "oracle_last_use",
-                         "oracle_hot", "oracle_rows", "oracle_keys"):
+                         "oracle_hot", "oracle_rows", "oracle_keys", "oracle_kcode",
+                         "oracle_kscale"):
                 getattr(L, name).restype = vp
                 getattr(L, name).argtypes = [vp]
             _lib = L
@@ -80,6 +96,48 @@ def score(q, k):
     return np.float32(lib().oracle_score(q.ctypes.data, k.ctypes.data))
 
 
+# ---- int8 indexer (reading R9 of kvo_oracle.c) ------------------------------
+def f32_to_f16(x):
+    """fp16 bits (uint16) of an fp32 value, round to nearest even."""
+    return int(lib().oracle_f32_to_f16(float(np.float32(x))))
+
+
+def f16_to_f32(h):
+    return np.float32(lib().oracle_f16_to_f32(int(h)))
+
+
+def fwht128(x):
+    """Unnormalised 128-point Walsh-Hadamard transform in fp32 (fixed stage order)."""
+    x = np.ascontiguousarray(x, dtype=np.float32).reshape(DIM)
+    out = np.empty(DIM, np.float32)
+    lib().oracle_fwht128(x.ctypes.data, out.ctypes.data)
+    return out
+
+
+def quant_rotated(y):
+    """int8 codes and fp16 scale bits of an already rotated fp32 vector."""
+    y = np.ascontiguousarray(y, dtype=np.float32).reshape(DIM)
+    code = np.empty(DIM, np.int8)
+    sc = np.zeros(1, np.uint16)
+    lib().oracle_quant_rotated(y.ctypes.data, code.ctypes.data, sc.ctypes.data)
+    return code, int(sc[0])
+
+
+def quant128(x):
+    """Rotate and quantize one bf16 vector (uint16[128]): (int8 codes, fp16 scale bits)."""
+    x = np.ascontiguousarray(x, dtype=np.uint16).reshape(DIM)
+    code = np.empty(DIM, np.int8)
+    sc = np.zeros(1, np.uint16)
+    lib().oracle_quant128(x.ctypes.data, code.ctypes.data, sc.ctypes.data)
+    return code, int(sc[0])
+
+
+def score_i8(qcode, qscale, kcode, kscale):
+    q = np.ascontiguousarray(qcode, dtype=np.int8)
+    k = np.ascontiguousarray(kcode, dtype=np.int8)
+    return np.float32(lib().oracle_score_i8(q.ctypes.data, int(qscale), k.ctypes.data, int(kscale)))
+
+
 class StepResult:
     __slots__ = ("tok", "score", "pay", "slot", "status", "miss_tok", "miss_slot", "n_miss")
 
@@ -90,12 +148,13 @@ class StepResult:
 class OracleUnit:
     """One (request, layer) unit: host rows, indexer keys, hot shelf, LRU table."""
 
-    def __init__(self, max_tokens, topk, capacity, n_pos, row_elems=576, keep_rows=True):
+    def __init__(self, max_tokens, topk, capacity, n_pos, row_elems=576, keep_rows=True,
+                 idx_int8=False):
         self.L = lib()
         self.max_tokens, self.topk, self.capacity, self.n_pos = max_tokens, topk, capacity, n_pos
-        self.row_elems, self.keep_rows = row_elems, keep_rows
-        self.h = self.L.oracle_unit_new(max_tokens, DIM, row_elems, topk, capacity, n_pos,
-                                        1 if keep_rows else 0)
+        self.row_elems, self.keep_rows, self.idx_int8 = row_elems, keep_rows, idx_int8
+        self.h = self.L.oracle_unit_new2(max_tokens, DIM, row_elems, topk, capacity, n_pos,
+                                         1 if keep_rows else 0, 1 if idx_int8 else 0)
         if not self.h:
             raise MemoryError("oracle_unit_new failed")
 
@@ -170,6 +229,13 @@ class OracleUnit:
         assert self.keep_rows
         return self._view("oracle_hot", self.capacity * self.row_elems, np.uint16).reshape(
             self.capacity, self.row_elems)
+
+    def key_codes(self):
+        """int8 codes and fp16 scale bits of the cached keys (int8 indexer)."""
+        assert self.idx_int8
+        n = self.length
+        return (self._view("oracle_kcode", n * DIM, np.int8).reshape(n, DIM),
+                self._view("oracle_kscale", n, np.uint16))
 
     def rows(self):
         assert self.keep_rows
