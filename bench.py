@@ -207,7 +207,7 @@ def make_workload(args):
     return wl
 
 
-def prepare(wl, rank, device, log):
+def prepare(wl, rank, device, log, idx="bf16"):
     """Handle with the prefilled context, plus per-sequence-step inputs on the device."""
     import numpy as np
     import torch
@@ -220,7 +220,7 @@ def prepare(wl, rank, device, log):
     tmax = wl.max_tokens(S)
     t0 = time.time()
     kv = K.Kvo(wl.n_requests, wl.n_layers, tmax, wl.topk, wl.hot_capacity, wl.n_pos, wl.row_elems,
-               device=device.index or 0)
+               device=device.index or 0, idx_dtype=K.KVO_IDX_INT8 if idx == "int8" else K.KVO_IDX_BF16)
     unit_stride = (kv.host_rows(1) - kv.host_rows(0)) // 2 if U > 1 else 0
     W.token_rows_into(kv.host_rows(0), unit_stride, wl.seed, W.KIND_ROWS, units, 0, wl.context,
                       wl.row_elems)
@@ -282,7 +282,7 @@ def run_kvo(args, log):
     wl = make_workload(args)
     hbm_peak, hbm_src = load_peaks()
     link = measure_host_link(torch, device)
-    kv, inp, units = prepare(wl, rank, device, log)
+    kv, inp, units = prepare(wl, rank, device, log, args.idx)
     U, P, k, R = len(units), wl.n_pos, wl.topk, wl.row_elems
     kv.set_option(K.KVO_OPT_GATHER_MODE, K.KVO_GATHER_BULK if args.gather == "bulk" else K.KVO_GATHER_LDG)
     kv.set_option(K.KVO_OPT_GROUPS, args.groups)
@@ -344,7 +344,8 @@ def run_kvo(args, log):
     rows_h2d = st1["rows_h2d"] - st0["rows_h2d"]
     bytes_h2d = st1["bytes_h2d"] - st0["bytes_h2d"]
     lens = [wl.context + (p + 1) * wl.n_new for p in positions]  # tokens per unit after append
-    score_bytes = sum(256.0 * U * L for L in lens)
+    key_bytes = 130.0 if args.idx == "int8" else 256.0  # int8: code row + fp16 scale
+    score_bytes = sum(key_bytes * U * L for L in lens)
     append_bytes = args.steps * U * wl.n_new * (R * 2 + 256)
     kernels = {}
     for name, (ms, n) in prof.items():
@@ -429,7 +430,7 @@ def run_kvo(args, log):
         "config": {"workload": wl.name, "n_requests": wl.n_requests, "n_layers": wl.n_layers,
                    "context": wl.context, "n_pos": P, "n_new": wl.n_new, "topk": k,
                    "hot_capacity": wl.hot_capacity, "drift": wl.drift,
-                   "steps_per_sequence": wl.steps, "path": path,
+                   "steps_per_sequence": wl.steps, "path": path, "indexer": args.idx,
                    "host_pool_page": kv.get_option(K.KVO_OPT_HOST_HUGE_PAGE) or "base",
                    "gather": "bulk" if path == "fused" else args.gather, "groups": args.groups,
                    "parallelism": "replicas%d" % world,
@@ -658,6 +659,8 @@ def main(argv=None):
                     help="fused: one cooperative launch per step; staged: one launch per stage; "
                          "auto: the library's default for the configuration")
     ap.add_argument("--gather-ctas", type=int, default=None, help="fused step: CTAs that only fill rows")
+    ap.add_argument("--idx", choices=("bf16", "int8"), default="bf16",
+                    help="indexer cache format (int8: Hadamard-rotated int8 codes + fp16 scales)")
     ap.add_argument("--speculate", type=int, default=None,
                     help="speculative threshold margin in permille (library default 900)")
     ap.add_argument("--piece-tokens", type=int, default=None, help="fused step: tokens per piece")

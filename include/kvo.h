@@ -84,7 +84,18 @@ typedef struct kvo_config {
   int32_t hot_capacity; /* hot slots per unit, 1..2^24 */
   int32_t n_positions;  /* P query positions per step, 1..8 (4 = MTP3) */
   int32_t device;       /* CUDA device ordinal */
+  int32_t idx_dtype;    /* KVO_IDX_BF16 (0) or KVO_IDX_INT8 (1): indexer cache format */
 } kvo_config;
+
+/* Indexer cache formats ("FlashOffloading ... What does it mean?", LIM C8
+ * paragraph).  BF16: keys stored as given, canonical fp32 score.  INT8: each
+ * key (at prefill/append) and each query (at kvo_step) is rotated by the
+ * 128-point Walsh-Hadamard transform and quantized to int8 codes with one
+ * fp16 scale per vector; the score is the exact int32 dot product of the
+ * codes times both scales / 128 (half the key bytes of BF16).  Inputs are
+ * bf16 in both formats. */
+#define KVO_IDX_BF16 0
+#define KVO_IDX_INT8 1
 
 typedef struct kvo_stats {
   uint64_t steps;           /* kvo_step calls */

@@ -35,7 +35,7 @@ class Runner:
 
     def __init__(self, wl, check_units=None, distinct=False, rows_for=None, steps=None,
                  gather_mode=K.KVO_GATHER_LDG, keys_fn=None, queries=None, max_tokens=None,
-                 options=None):
+                 options=None, idx_int8=False, prefill_from_host=False):
         self.wl = wl
         self.steps = wl.steps if steps is None else steps
         self.units_rl = wl.units_rl()
@@ -44,7 +44,8 @@ class Runner:
         rows_for = self.check if rows_for is None else rows_for
         self.tmax = wl.max_tokens(self.steps) if max_tokens is None else max_tokens
         self.kv = K.Kvo(wl.n_requests, wl.n_layers, self.tmax, wl.topk, wl.hot_capacity,
-                        wl.n_pos, wl.row_elems)
+                        wl.n_pos, wl.row_elems,
+                        idx_dtype=K.KVO_IDX_INT8 if idx_int8 else K.KVO_IDX_BF16)
         self.kv.set_option(K.KVO_OPT_GATHER_MODE, gather_mode)
         for key, value in {**PATH_OPTIONS, **(options or {})}.items():
             self.kv.set_option(key, value)
@@ -53,14 +54,16 @@ class Runner:
         _fill_host_rows(self.kv, wl, self.units_rl, rows_for, 0, wl.context)
         self.length = wl.context
         self.oracles = {u: oracle.OracleUnit(self.tmax, wl.topk, wl.hot_capacity, wl.n_pos,
-                                             wl.row_elems, keep_rows=True) for u in self.check}
+                                             wl.row_elems, keep_rows=True, idx_int8=idx_int8)
+                        for u in self.check}
         chunk = 16
         for b in range(0, self.U, chunk):
             ids = list(range(b, min(self.U, b + chunk)))
             keys = self._keys([self.units_rl[u] for u in ids], 0, wl.context)
             kd = torch.from_numpy(keys).cuda()
             for j, u in enumerate(ids):
-                self.kv.prefill(u, wl.context, kd[j])
+                # host (pageable) or device keys: the library handles both
+                self.kv.prefill(u, wl.context, np.ascontiguousarray(keys[j]) if prefill_from_host else kd[j])
                 if u in self.oracles:
                     rows = W.token_rows(wl.seed, W.KIND_ROWS, [self.units_rl[u]], 0, wl.context,
                                         wl.row_elems)[0]

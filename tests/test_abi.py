@@ -51,14 +51,15 @@ def test_invalid_config_rejected_before_device(L):
         dict(max_tokens=0),
         dict(n_requests=0),
         dict(topk=4000, hot_capacity=8192, n_positions=8),  # candidate buffer too small
+        dict(idx_dtype=2),
     ]
     for over in bad:
         cfg = dict(n_requests=1, n_layers=1, max_tokens=100, idx_dim=128, row_elems=576,
-                   topk=16, hot_capacity=32, n_positions=1, device=0)
+                   topk=16, hot_capacity=32, n_positions=1, device=0, idx_dtype=0)
         cfg.update(over)
         c = kvo.KvoConfig(cfg["n_requests"], cfg["n_layers"], cfg["max_tokens"], cfg["idx_dim"],
                           cfg["row_elems"], cfg["topk"], cfg["hot_capacity"], cfg["n_positions"],
-                          cfg["device"])
+                          cfg["device"], cfg["idx_dtype"])
         h = ctypes.c_void_p()
         rc = L.kvo_create(ctypes.byref(c), ctypes.byref(h))
         assert rc == kvo.KVO_EINVAL, over

@@ -348,6 +348,28 @@ def test_paths_alternate_per_step(path):
         r.close()
 
 
+# ---------------------------------------------------------------- int8 indexer
+def test_int8_indexer_reduced(path):
+    wl = W.reduced(W.WORKLOADS["batch16x8_32k_mtp3"], n_requests=2, n_layers=2, context=4001,
+                   topk=256, hot_capacity=512, steps=6)
+    _run(wl, idx_int8=True)
+
+
+def test_int8_indexer_positions_and_host_prefill(path):
+    for P in (1, 3, 8):
+        wl = W.Workload("i8p%d" % P, 1, 2, 2300, P, P, 64, 64 * P, 4, 0.5, 85)
+        _run(wl, distinct=True, idx_int8=True, prefill_from_host=(P == 3))
+
+
+def test_int8_indexer_ties_short_units_and_rescans(path):
+    # integer keys make many equal int8 scores; context 0 starts below k and P
+    wl = W.Workload("i8short", 1, 2, 0, 3, 3, 16, 64, 8, 0.9, 86)
+    _run(wl, idx_int8=True)
+    wl = W.Workload("i8nomargin", 3, 2, 4000, 4, 4, 200, 900, 6, 0.0, 87)
+    st, _ = _run(wl, distinct=True, idx_int8=True, options={K.KVO_OPT_SPECULATE: 1000})
+    assert st["rescored"] > 0
+
+
 # ---------------------------------------------------------------- full sizes
 def _meminfo_gb():
     try:
@@ -369,6 +391,11 @@ def test_full_batch16x8_mtp3_grouped_sampled(path):
     _staged_only(path)
     wl = W.WORKLOADS["batch16x8_32k_mtp3"]
     _run(wl, steps=20, check_units=[0, 40, 127], count_rows=False, options={K.KVO_OPT_GROUPS: 4})
+
+
+def test_full_batch16x8_mtp3_int8_sampled():
+    wl = W.WORKLOADS["batch16x8_32k_mtp3"]
+    _run(wl, steps=20, check_units=[0, 77, 127], count_rows=False, idx_int8=True)
 
 
 def test_full_long_1m_mtp3_sampled():

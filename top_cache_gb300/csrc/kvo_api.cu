@@ -31,7 +31,13 @@ struct kvo_handle {
   uint16_t* host_pool_dev = nullptr;  // device-visible address of the same memory
   size_t pool_map_bytes = 0;          // > 0: mmap'ed with transparent huge pages, registered
   size_t pool_huge_page = 0;
-  uint16_t* idx = nullptr;
+  uint16_t* idx = nullptr;           // bf16 indexer [U][stride][128]
+  int8_t* idx8 = nullptr;            // int8 indexer codes [U][stride][128]
+  uint16_t* idxs = nullptr;          // their fp16 scales [U][stride]
+  int8_t* q8 = nullptr;              // per-step query codes [U][P][128]
+  uint16_t* qscale = nullptr;        // their fp16 scales [U][P]
+  uint32_t* qdone = nullptr;         // fused launch: CTAs done quantizing queries
+  bool int8 = false;
   uint16_t* hot = nullptr;
   int32_t* cache_slots = nullptr;
   int32_t* slot_token = nullptr;
@@ -152,7 +158,7 @@ void free_all(kvo_handle* h) {
   if (h->ev_join) cudaEventDestroy(h->ev_join);
   for (auto& ev : h->ev_group)
     if (ev) cudaEventDestroy(ev);
-  void* dev[] = {h->idx, h->hot, h->cache_slots, h->slot_token, h->last_use, h->stamp, h->len,
+  void* dev[] = {h->idx, h->idx8, h->idxs, h->q8, h->qscale, h->qdone, h->hot, h->cache_slots, h->slot_token, h->last_use, h->stamp, h->len,
                  h->all_units, h->units_dev, h->off, h->gthr, h->spec, h->qn_prev, h->qn_cur,
                  h->tspec, h->fb, h->fb_any, h->tok_bits, h->order, h->order_par, h->seg_keys, h->seg_cnt, h->sel_pay,
                  h->miss_tok, h->miss_slot, h->miss_cnt, h->miss_off, h->done_ctr, h->err,
@@ -234,11 +240,11 @@ constexpr int kFusedDefaultMaxCapacity = 65536;
 
 // Whether the fused step's shared-memory layout holds this configuration:
 // the finisher's select and residency reuse the candidate buffers.
-bool fused_fits(int P, int k, int cap, int C) {
+bool fused_fits(int P, int k, int cap, int C, bool int8) {
   const size_t region = (size_t)P * cap * 8 + (size_t)k * 8;
   int kpad = 1;
   while (kpad < k) kpad <<= 1;
-  return kvo::fused_smem_bytes(P, k, cap) <= 227 * 1024 && residency_smem_bytes(C, P, k) <= region &&
+  return kvo::fused_smem_bytes(P, k, cap, int8) <= 227 * 1024 && residency_smem_bytes(C, P, k) <= region &&
          (size_t)kpad * 8 + 8 * 256 <= region;
 }
 
@@ -368,6 +374,10 @@ int fused_step(kvo_handle* h, const int32_t* du, const int32_t* units, int32_t n
   kvo::FusedArgs f{};
   kvo::SelectArgs& sa = f.s;
   sa.keys = h->idx;
+  sa.keys8 = h->idx8;
+  sa.kscale = h->idxs;
+  sa.q8 = h->q8;
+  sa.qscale = h->qscale;
   sa.stride = h->stride;
   sa.units = du;
   sa.len = h->len;
@@ -456,8 +466,9 @@ int fused_step(kvo_handle* h, const int32_t* du, const int32_t* units, int32_t n
   if (++h->epoch == 0) ++h->epoch;  // 0 marks a never-written chunk
   f.epoch = h->epoch;
   f.n_gather = h->gather_ctas < h->n_sm ? h->gather_ctas : h->n_sm - 1;
-  f.smem_bytes = (int)kvo::fused_smem_bytes(h->P, h->k, h->cap);
+  f.smem_bytes = (int)kvo::fused_smem_bytes(h->P, h->k, h->cap, h->int8);
   f.plan_flag = h->plan_flag;
+  f.qdone = h->qdone;
 
   // the plan runs inside the fused launch (its CTA 0)
   cudaError_t e = timed(h, KVO_PROF_FUSED, s, [&] { return kvo::launch_fused(f, h->n_sm, s); });
@@ -487,13 +498,14 @@ int kvo_create(const kvo_config* cfg, kvo_handle** out) {
     return fail(KVO_EINVAL, "n_requests * n_layers must be in [1, 2^20]");
   if (c.max_tokens < 1 || c.max_tokens >= (int64_t)1 << 31) return fail(KVO_EINVAL, "max_tokens out of range");
   if (c.idx_dim != kvo::kDim) return fail(KVO_EINVAL, "idx_dim must be 128");
+  if (c.idx_dtype != KVO_IDX_BF16 && c.idx_dtype != KVO_IDX_INT8) return fail(KVO_EINVAL, "bad idx_dtype");
   if (c.row_elems < 8 || c.row_elems > 4096 || c.row_elems % 8)
     return fail(KVO_EINVAL, "row_elems must be a multiple of 8 in [8, 4096]");
   if (c.topk < 1 || c.topk > 4096) return fail(KVO_EINVAL, "topk must be in [1, 4096]");
   if (c.hot_capacity < c.topk || c.hot_capacity > (1 << 24))
     return fail(KVO_EINVAL, "hot_capacity must be in [topk, 2^24]");
   if (c.n_positions < 1 || c.n_positions > 8) return fail(KVO_EINVAL, "n_positions must be in [1, 8]");
-  const int cap = kvo::score_cap_for(c.n_positions, c.topk);
+  const int cap = kvo::score_cap_for(c.n_positions, c.topk, c.idx_dtype == KVO_IDX_INT8);
   if (cap == 0) return fail(KVO_EINVAL, "topk too large for n_positions (shared-memory candidate buffer)");
   if (residency_smem_bytes(c.hot_capacity, c.n_positions, c.topk) > 224 * 1024)
     return fail(KVO_EINVAL, "hot_capacity / n_positions * topk too large for the residency kernel");
@@ -527,7 +539,17 @@ int kvo_create(const kvo_config* cfg, kvo_handle** out) {
   }
   e = cudaHostGetDevicePointer(reinterpret_cast<void**>(&h->host_pool_dev), h->host_pool, 0);
   const size_t segs = (size_t)h->G_max + U;
-  if (e == cudaSuccess) e = dalloc(&h->idx, U * S * kvo::kDim);
+  h->int8 = c.idx_dtype == KVO_IDX_INT8;
+  if (h->int8) {
+    if (e == cudaSuccess) e = dalloc(&h->idx8, U * S * kvo::kDim);
+    if (e == cudaSuccess) e = dalloc(&h->idxs, U * S);
+    if (e == cudaSuccess) e = dalloc(&h->q8, U * h->P * kvo::kDim);
+    if (e == cudaSuccess) e = dalloc(&h->qscale, U * h->P);
+    if (e == cudaSuccess) e = dalloc(&h->qdone, 1);
+    if (e == cudaSuccess) e = cudaMemset(h->qdone, 0, 4);
+  } else if (e == cudaSuccess) {
+    e = dalloc(&h->idx, U * S * kvo::kDim);
+  }
   if (e == cudaSuccess) e = dalloc(&h->hot, U * C * h->R);
   if (e == cudaSuccess) e = dalloc(&h->cache_slots, U * S);
   if (e == cudaSuccess) e = dalloc(&h->slot_token, U * C);
@@ -562,7 +584,7 @@ int kvo_create(const kvo_config* cfg, kvo_handle** out) {
   for (int g = 0; g < 16 && e == cudaSuccess; ++g) e = cudaEventCreateWithFlags(&h->ev_group[g], cudaEventDisableTiming);
   if (e == cudaSuccess) e = dalloc(&h->err, 1);
   if (e == cudaSuccess) e = dalloc(&h->stats, 1);
-  h->fused_ok = fused_fits(h->P, h->k, h->cap, h->C);
+  h->fused_ok = fused_fits(h->P, h->k, h->cap, h->C, h->int8);
   if (e == cudaSuccess && h->fused_ok) e = alloc_fused(h);
   h->fused = h->fused_ok ? 2 : 0;
   if (e == cudaSuccess) e = dalloc(&h->bytes_seen, 1);
@@ -638,9 +660,31 @@ int kvo_prefill(kvo_handle* h, int32_t unit, int64_t n_tokens, const void* idx_k
   DeviceGuard guard(h->device);
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   cudaError_t e = cudaSuccess;
-  if (n_tokens > 0)
-    e = cudaMemcpyAsync(h->idx + (size_t)unit * h->stride * kvo::kDim, idx_keys,
-                        (size_t)n_tokens * kvo::kKeyBytes, cudaMemcpyDefault, s);
+  const size_t row0 = (size_t)unit * h->stride;
+  if (n_tokens > 0 && !h->int8) {
+    e = cudaMemcpyAsync(h->idx + row0 * kvo::kDim, idx_keys, (size_t)n_tokens * kvo::kKeyBytes, cudaMemcpyDefault,
+                        s);
+  } else if (n_tokens > 0) {
+    // int8 indexer: the bf16 keys are rotated and quantized on the device
+    // (staged through a stream-ordered buffer when they are host memory)
+    cudaPointerAttributes at{};
+    const bool on_dev = cudaPointerGetAttributes(&at, idx_keys) == cudaSuccess &&
+                        (at.type == cudaMemoryTypeDevice || at.type == cudaMemoryTypeManaged);
+    cudaGetLastError();
+    const uint16_t* src = static_cast<const uint16_t*>(idx_keys);
+    void* staging = nullptr;
+    if (!on_dev) {
+      e = cudaMallocAsync(&staging, (size_t)n_tokens * kvo::kKeyBytes, s);
+      if (e == cudaSuccess)
+        e = cudaMemcpyAsync(staging, idx_keys, (size_t)n_tokens * kvo::kKeyBytes, cudaMemcpyDefault, s);
+      src = static_cast<const uint16_t*>(staging);
+    }
+    if (e == cudaSuccess) e = kvo::launch_quant_keys(src, n_tokens, h->idx8 + row0 * kvo::kDim, h->idxs + row0, s);
+    if (staging) {
+      const cudaError_t f = cudaFreeAsync(staging, s);
+      if (e == cudaSuccess) e = f;
+    }
+  }
   if (e == cudaSuccess) e = kvo::launch_set_len(h->len, unit, (int32_t)n_tokens, s);
   if (e != cudaSuccess) return cuda_fail(e, "prefill");
   h->len_host[(size_t)unit] = n_tokens;
@@ -676,6 +720,8 @@ int kvo_append(kvo_handle* h, const int32_t* units, int32_t n_units, int32_t n_t
   a.keys = static_cast<const uint16_t*>(idx_keys);
   a.host_pool = h->host_pool_dev;
   a.idx = h->idx;
+  a.idx8 = h->idx8;
+  a.idxs = h->idxs;
   a.len = h->len;
   a.stats = h->stats;
   cudaError_t e = timed(h, KVO_PROF_APPEND, s, [&] { return kvo::launch_append(a, s); });
@@ -717,6 +763,10 @@ int kvo_step(kvo_handle* h, const int32_t* units, int32_t n_units, const void* q
 
     kvo::SelectArgs sa{};
     sa.keys = h->idx;
+    sa.keys8 = h->idx8;
+    sa.kscale = h->idxs;
+    sa.q8 = h->q8 ? h->q8 + (size_t)b * h->P * kvo::kDim : nullptr;
+    sa.qscale = h->qscale ? h->qscale + (size_t)b * h->P : nullptr;
     sa.stride = h->stride;
     sa.units = du + b;
     sa.len = h->len;
@@ -752,7 +802,11 @@ int kvo_step(kvo_handle* h, const int32_t* units, int32_t n_units, const void* q
       sa.bytes_prev = h->bytes_prev_dev;
       sa.bytes_seen = h->bytes_seen;
     }
-    e = timed(h, KVO_PROF_PLAN, s, [&] { return kvo::launch_plan(sa, s); });
+    if (sa.q8)  // int8 indexer: this group's queries, one warp each
+      e = timed(h, KVO_PROF_PLAN, s, [&] {
+        return kvo::launch_quant_keys(sa.queries, (int64_t)ng * h->P, sa.q8, sa.qscale, s);
+      });
+    if (e == cudaSuccess) e = timed(h, KVO_PROF_PLAN, s, [&] { return kvo::launch_plan(sa, s); });
     if (e == cudaSuccess) e = timed(h, KVO_PROF_SCORE, s, [&] { return kvo::launch_score(sa, s); });
     if (e == cudaSuccess) e = timed(h, KVO_PROF_SELECT, s, [&] { return kvo::launch_select(sa, s); });
     if (spec_on) {
@@ -847,7 +901,7 @@ int kvo_select(const void* keys, int64_t unit_stride, const int32_t* cache_slots
   if (unit_stride < 1 || unit_stride >= (int64_t)1 << 31) return fail(KVO_EINVAL, "unit_stride out of range");
   if (!aligned16(keys) || !aligned16(queries)) return fail(KVO_EINVAL, "keys/queries not 16-byte aligned");
   if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return fail(KVO_EINVAL, "workspace not 256-byte aligned");
-  const int cap = kvo::score_cap_for(n_pos, k);
+  const int cap = kvo::score_cap_for(n_pos, k, false);
   if (cap == 0) return fail(KVO_EINVAL, "k too large for n_pos");
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return fail(KVO_ECUDA, "no current device");

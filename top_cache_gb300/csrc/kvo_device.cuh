@@ -9,6 +9,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <cuda_fp16.h>
+
 #include <type_traits>
 
 #include "kvo_internal.cuh"
@@ -33,6 +35,77 @@ constexpr int kMaxK = 4096;
 
 __device__ __forceinline__ void consumer_sync() { named_sync(1, kCT); }
 
+// Indexer key formats.  A ring stage holds one tile of kTile keys; int8
+// stages hold the keys' 128-byte code rows followed by their fp16 scales.
+struct KeysBf16 {
+  static constexpr bool kInt8 = false;
+  static constexpr int kRowBytes = kKeyBytes;
+  static constexpr int kStages = 3;
+  static constexpr int kStageBytes = kTile * kKeyBytes;  // 32 KB
+};
+struct KeysInt8 {
+  static constexpr bool kInt8 = true;
+  static constexpr int kRowBytes = kDim;
+  static constexpr int kStages = 6;
+  static constexpr int kScaleOff = kTile * kDim;         // codes, then scales
+  // the scales are copied from the 8-token boundary at or below the tile's
+  // first token (16-byte aligned source): up to 7 + kTile of them
+  static constexpr int kScaleBytes = ((kTile + 7) * 2 + 15) & ~15;
+  static constexpr int kStageBytes = kScaleOff + kScaleBytes;
+};
+// Shared memory of a scoring CTA besides the candidate buffers.
+template <class KF>
+constexpr int smem_fixed() {
+  return KF::kStages * KF::kStageBytes + 2 * KF::kStages * 8 + 8 * 4 + 8 * 8 + 256 * 4 + 10 * 4 + 8;
+}
+
+// Rotation and int8 quantization of one 128-element bf16 vector by a warp
+// (reading R9 of the oracle; "FlashOffloading ... What does it mean?", the
+// LIM C8 paragraph): y = H x by the unnormalised fast Walsh-Hadamard
+// transform in fp32, stages h = 1 .. 64, pair (i, i + h) -> (a + b, a - b);
+// scale = fp16(max|y| / 127) (round to nearest even); codes =
+// clamp(rint(y / scale), -127, 127).  Lane l holds elements 4l .. 4l+3.
+// Returns the scale as fp32; lane 0 writes its fp16 bits to *scale.
+__device__ __forceinline__ float warp_quant128(const uint16_t* x, int8_t* code, uint16_t* scale, int lane) {
+  // scale: nullable
+  const uint2 raw = *reinterpret_cast<const uint2*>(x + 4 * lane);
+  float v[4] = {bf_lo(raw.x), bf_hi(raw.x), bf_lo(raw.y), bf_hi(raw.y)};
+  // h = 1, 2 inside the lane
+  float a = v[0], b = v[1];
+  v[0] = a + b; v[1] = a - b;
+  a = v[2]; b = v[3];
+  v[2] = a + b; v[3] = a - b;
+  a = v[0]; b = v[2];
+  v[0] = a + b; v[2] = a - b;
+  a = v[1]; b = v[3];
+  v[1] = a + b; v[3] = a - b;
+  // h = 4 .. 64 across lanes (partner lane l ^ (h / 4))
+#pragma unroll
+  for (int m = 1; m < 32; m <<= 1) {
+    const bool upper = (lane & m) != 0;
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const float o = __shfl_xor_sync(kFull, v[e], m);
+      v[e] = upper ? o - v[e] : v[e] + o;  // lower: a + b; upper: a - b
+    }
+  }
+  float mx = fmaxf(fmaxf(fabsf(v[0]), fabsf(v[1])), fmaxf(fabsf(v[2]), fabsf(v[3])));
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(kFull, mx, o));
+  const __half h = __float2half_rn(__fdiv_rn(mx, 127.0f));
+  const float sc = __half2float(h);
+  uint32_t packed = 0;
+#pragma unroll
+  for (int e = 0; e < 4; ++e) {
+    float c = sc > 0.f ? rintf(__fdiv_rn(v[e], sc)) : 0.f;
+    c = fminf(fmaxf(c, -127.f), 127.f);
+    packed |= (uint32_t)(uint8_t)(int8_t)c << (8 * e);
+  }
+  *reinterpret_cast<uint32_t*>(code + 4 * lane) = packed;
+  if (lane == 0 && scale) *scale = __half_as_ushort(h);
+  return sc;
+}
+
 // ---------------------------------------------------------------------------
 // 16-lane tree reduction of chunk sums.  Lane j (of a half warp) holds chunk
 // j's partial sums for V (token, position) pairs.  Levels pair lanes j and
@@ -44,8 +117,8 @@ __device__ __forceinline__ void consumer_sync() { named_sync(1, kCT); }
 // lane l holds pair (i ^ X_l), X_l = tree_perm<V>(l): partners differ in
 // exactly the bit of X that the level splits on.
 // ---------------------------------------------------------------------------
-template <int CUR, int V>
-__device__ __forceinline__ void tree_level(float (&a)[V], int m) {
+template <int CUR, int V, class T>
+__device__ __forceinline__ void tree_level(T (&a)[V], int m) {
   if constexpr (CUR > 1) {
 #pragma unroll
     for (int i = 0; i < CUR / 2; ++i) a[i] = a[i] + __shfl_xor_sync(kFull, a[i + CUR / 2], m);
@@ -54,8 +127,8 @@ __device__ __forceinline__ void tree_level(float (&a)[V], int m) {
   }
 }
 
-template <int V>
-__device__ __forceinline__ void tree16(float (&a)[V]) {
+template <int V, class T>
+__device__ __forceinline__ void tree16(T (&a)[V]) {
   tree_level<V, V>(a, 8);
   tree_level<(V >= 2 ? V / 2 : 1), V>(a, 4);
   tree_level<(V >= 4 ? V / 4 : 1), V>(a, 2);
@@ -370,6 +443,7 @@ __device__ __forceinline__ void compact_candidates(uint64_t* cand, uint32_t* cnt
 
 // Shared-memory layout of a scoring CTA.
 struct ScoreSmem {
+  int stages, stage_bytes;
   uint8_t* ring;
   uint64_t* full;
   uint64_t* empty;
@@ -380,11 +454,14 @@ struct ScoreSmem {
   uint64_t* fl;       // [1]
   uint64_t* cand;     // [P][cap]
   uint64_t* scratch;  // [k]
+  template <class KF>
   __device__ void carve(uint8_t* smem, int P, int cap) {
+    stages = KF::kStages;
+    stage_bytes = KF::kStageBytes;
     ring = smem;
-    full = reinterpret_cast<uint64_t*>(smem + kStages * kTileBytes);
-    empty = full + kStages;
-    cnt = reinterpret_cast<uint32_t*>(empty + kStages);
+    full = reinterpret_cast<uint64_t*>(smem + KF::kStages * KF::kStageBytes);
+    empty = full + KF::kStages;
+    cnt = reinterpret_cast<uint32_t*>(empty + KF::kStages);
     thr = reinterpret_cast<uint64_t*>(cnt + 8);
     hist = reinterpret_cast<uint32_t*>(thr + 8);
     rx = hist + 256;
@@ -393,31 +470,29 @@ struct ScoreSmem {
     scratch = cand + (size_t)P * cap;
   }
 };
-constexpr int kSmemFixed = kStages * kTileBytes + 2 * kStages * 8 + 8 * 4 + 8 * 8 + 256 * 4 + 10 * 4 + 8;
 
 // ---------------------------------------------------------------------------
 // Per-lane scoring machinery of one consumer warp (16 warps x 8 keys = one tile)
 // ---------------------------------------------------------------------------
+// Lane layout of a consumer warp: a half-warp scores 4 keys, lane j holds
+// elements 8j .. 8j+7 of every query; after the 16-lane tree each lane keeps
+// VL (token, position) results.  Shared by both key formats.
 template <int PP>
-struct Scorer {
+struct ScorerLanes {
   static constexpr int V = 4 * PP;                 // (token, position) pairs per lane
   static constexpr int VL = V >= 16 ? V / 16 : 1;  // values left per lane after the tree
   static constexpr int LPP = PP == 1 ? 0 : PP == 2 ? 1 : PP == 4 ? 2 : 3;
-  static constexpr int PH = PP >= 2 ? PP / 2 : 1;  // position pairs (packed fp32x2 FMA)
 
   int lane, j, X, px, tx, rowbase;
   bool owner;
-  int rowoff[4];
   int rrow[VL], rpos[VL];
   uint32_t lead[VL], same[VL];
-  float qf[PP][8];
-  float2 qp[PH][8];
 
   // Slot (tau, p) of this lane scores token row tau ^ tx against position
   // p ^ px.  Result r is (row rrow[r], position rpos[r]); for insertion, lane
   // q < P leads position q: lead[r] = lanes reporting position q, same[r] =
   // lanes reporting this lane's position.
-  __device__ __forceinline__ void init(int warp, int lane_) {
+  __device__ __forceinline__ void init_lanes(int warp, int lane_) {
     lane = lane_;
     const int h = lane >> 4;
     j = lane & 15;
@@ -426,8 +501,6 @@ struct Scorer {
     px = X & (PP - 1);
     owner = tree_owner<V>(lane);
     rowbase = warp * 8 + h * 4;
-#pragma unroll
-    for (int tau = 0; tau < 4; ++tau) rowoff[tau] = (rowbase + (tau ^ tx)) * kKeyBytes + j * 16;
 #pragma unroll
     for (int r = 0; r < VL; ++r) {
       const int cmb = r ^ X;
@@ -443,13 +516,62 @@ struct Scorer {
     }
   }
 
+  // Inserts the tile's results that reach their position's threshold.
+  // t: token of row 0; nt: rows in the tile; len: unit length.
+  __device__ __forceinline__ void filter(const float (&acc)[V], int64_t t, int nt, int64_t len, int P,
+                                         const uint64_t* thr, uint32_t* cnt, uint64_t* cand, int cap) {
+    // full tiles whose tokens every position sees need no per-result tests
+    const bool interior = nt == kTile && t + kTile <= len - (P - 1);
+#pragma unroll
+    for (int r = 0; r < VL; ++r) {
+      const int p = rpos[r];
+      const int64_t tok = t + rrow[r];
+      float s = acc[r];
+      if (s == 0.f) s = 0.f;  // +0 for a zero score
+      const uint64_t key = sel_key(s, (uint32_t)tok);
+      bool ok = owner && p < P;
+      if (!interior) ok = ok && rrow[r] < nt && tok < len - (P - 1 - p);
+      const bool pass = ok && key >= thr[p];
+      const uint32_t mall = __ballot_sync(kFull, pass);
+      if (mall) {
+        uint32_t base = 0;
+        if (lane < P) {
+          const uint32_t n_here = __popc(mall & lead[r]);
+          if (n_here) base = atomicAdd(&cnt[lane], n_here);
+        }
+        base = __shfl_sync(kFull, base, p);
+        if (pass) {
+          const uint32_t dst = base + __popc(mall & same[r] & lanemask_lt());
+          if (dst < (uint32_t)cap) cand[(size_t)p * cap + dst] = key;
+        }
+      }
+    }
+  }
+};
+
+// bf16 keys: the canonical fp32 score (reading R1).
+template <int PP>
+struct Scorer : ScorerLanes<PP> {
+  using B = ScorerLanes<PP>;
+  using B::V; using B::VL; using B::j; using B::px; using B::tx; using B::rowbase;
+  static constexpr int PH = PP >= 2 ? PP / 2 : 1;  // position pairs (packed fp32x2 FMA)
+  int rowoff[4];
+  float qf[PP][8];
+  float2 qp[PH][8];
+
+  __device__ __forceinline__ void init(int warp, int lane_) {
+    B::init_lanes(warp, lane_);
+#pragma unroll
+    for (int tau = 0; tau < 4; ++tau) rowoff[tau] = (rowbase + (tau ^ tx)) * kKeyBytes + j * 16;
+  }
+
   // This lane's chunk of unit i's queries, in slot order (fp32, exact).
-  __device__ __forceinline__ void load_queries(const uint16_t* queries, int64_t i, int P) {
+  __device__ __forceinline__ void load_queries(const SelectArgs& a, int64_t i, int P) {
 #pragma unroll
     for (int p = 0; p < PP; ++p) {
       const int pq = p ^ px;
       if (pq < P) {
-        const uint4 v = *reinterpret_cast<const uint4*>(queries + (i * P + pq) * kDim + j * 8);
+        const uint4 v = *reinterpret_cast<const uint4*>(a.queries + (i * P + pq) * kDim + j * 8);
         qf[p][0] = bf_lo(v.x); qf[p][1] = bf_hi(v.x);
         qf[p][2] = bf_lo(v.y); qf[p][3] = bf_hi(v.y);
         qf[p][4] = bf_lo(v.z); qf[p][5] = bf_hi(v.z);
@@ -465,16 +587,17 @@ struct Scorer {
       for (int e = 0; e < 8; ++e) qp[m][e] = make_float2(qf[2 * m][e], PP >= 2 ? qf[(2 * m + 1) % PP][e] : 0.f);
   }
 
-  // Scores the tile's keys (row stride 256 B at `tile`, shared or global
-  // memory); release() is called once the tile's memory is no longer read.
+  // Scores a ring stage holding the tile that starts at token t; release() is
+  // called once the stage is no longer read.
   template <class Release>
-  __device__ __forceinline__ void score(const uint8_t* tile, float (&acc)[V], Release release) {
-    score_rows(tile, acc, release, [&](int tau) { return rowoff[tau]; });
+  __device__ __forceinline__ void score(const uint8_t* stage, int64_t t, float (&acc)[V], Release release) {
+    score_rows(stage, acc, release, [&](int tau) { return rowoff[tau]; });
   }
 
-  // Same for a tile in global memory with nt rows: rows past the end read the
-  // last row instead (their results are discarded by filter()).
-  __device__ __forceinline__ void score_global(const uint8_t* tile, int nt, float (&acc)[V]) {
+  // Same for nt keys of unit u from token t in global memory: rows past the
+  // end read the last row instead (their results are discarded by filter()).
+  __device__ __forceinline__ void score_global(const SelectArgs& a, int u, int64_t t, int nt, float (&acc)[V]) {
+    const uint8_t* tile = reinterpret_cast<const uint8_t*>(a.keys + ((int64_t)u * a.stride + t) * kDim);
     score_rows(tile, acc, [] {}, [&](int tau) {
       const int r = rowbase + (tau ^ tx);
       return (r < nt ? r : nt - 1) * kKeyBytes + j * 16;
@@ -515,40 +638,100 @@ struct Scorer {
     release();
     tree16<V>(acc);
   }
+};
 
-  // Inserts the tile's results that reach their position's threshold.
-  // t: token of row 0; nt: rows in the tile; len: unit length.
-  __device__ __forceinline__ void filter(const float (&acc)[V], int64_t t, int nt, int64_t len, int P,
-                                         const uint64_t* thr, uint32_t* cnt, uint64_t* cand, int cap) {
-    // full tiles whose tokens every position sees need no per-result tests
-    const bool interior = nt == kTile && t + kTile <= len - (P - 1);
+// int8 keys (reading R9): exact int32 dot products of the codes (4-byte dot
+// instructions, tree of integer sums), then (((float)dot * s_q) * s_k) / 128.
+template <int PP>
+struct ScorerI8 : ScorerLanes<PP> {
+  using B = ScorerLanes<PP>;
+  using B::V; using B::VL; using B::j; using B::px; using B::tx; using B::rowbase; using B::rrow; using B::rpos;
+  int qi[PP][2];    // this lane's 8 query codes per slot position
+  float qs[VL];     // query scale of each result's position (fp16, read as fp32)
+
+  __device__ __forceinline__ void init(int warp, int lane_) { B::init_lanes(warp, lane_); }
+
+  __device__ __forceinline__ void load_queries(const SelectArgs& a, int64_t i, int P) {
 #pragma unroll
-    for (int r = 0; r < VL; ++r) {
-      const int p = rpos[r];
-      const int64_t tok = t + rrow[r];
-      float s = acc[r];
-      if (s == 0.f) s = 0.f;  // +0 for a zero score
-      const uint64_t key = sel_key(s, (uint32_t)tok);
-      bool ok = owner && p < P;
-      if (!interior) ok = ok && rrow[r] < nt && tok < len - (P - 1 - p);
-      const bool pass = ok && key >= thr[p];
-      const uint32_t mall = __ballot_sync(kFull, pass);
-      if (mall) {
-        uint32_t base = 0;
-        if (lane < P) {
-          const uint32_t n_here = __popc(mall & lead[r]);
-          if (n_here) base = atomicAdd(&cnt[lane], n_here);
-        }
-        base = __shfl_sync(kFull, base, p);
-        if (pass) {
-          const uint32_t dst = base + __popc(mall & same[r] & lanemask_lt());
-          if (dst < (uint32_t)cap) cand[(size_t)p * cap + dst] = key;
-        }
+    for (int p = 0; p < PP; ++p) {
+      const int pq = p ^ px;
+      if (pq < P) {
+        const uint2 v = *reinterpret_cast<const uint2*>(a.q8 + (i * P + pq) * kDim + j * 8);
+        qi[p][0] = (int)v.x;
+        qi[p][1] = (int)v.y;
+      } else {
+        qi[p][0] = qi[p][1] = 0;
       }
     }
+#pragma unroll
+    for (int r = 0; r < VL; ++r)
+      qs[r] = rpos[r] < P ? __half2float(__ushort_as_half(a.qscale[i * P + rpos[r]])) : 0.f;
+  }
+
+  template <class Release>
+  __device__ __forceinline__ void score(const uint8_t* stage, int64_t t, float (&acc)[V], Release release) {
+    const uint16_t* scales = reinterpret_cast<const uint16_t*>(stage + KeysInt8::kScaleOff) + (t & 7);
+    score_rows(stage, scales, acc, release, [](int r) { return r; });
+  }
+
+  // nt keys of unit u from token t in global memory; rows past the end read
+  // the last row (their results are discarded by filter()).
+  __device__ __forceinline__ void score_global(const SelectArgs& a, int u, int64_t t, int nt, float (&acc)[V]) {
+    const int64_t base = (int64_t)u * a.stride + t;
+    score_rows(reinterpret_cast<const uint8_t*>(a.keys8 + base * kDim), a.kscale + base, acc, [] {},
+               [nt](int r) { return r < nt ? r : nt - 1; });
+  }
+
+  template <class Release, class Clamp>
+  __device__ __forceinline__ void score_rows(const uint8_t* codes, const uint16_t* scales, float (&acc)[V],
+                                             Release release, Clamp clamp) {
+    int32_t ai[V];
+#pragma unroll
+    for (int tau = 0; tau < 4; ++tau) {
+      const uint2 kv = *reinterpret_cast<const uint2*>(codes + clamp(rowbase + (tau ^ tx)) * kDim + j * 8);
+#pragma unroll
+      for (int p = 0; p < PP; ++p) ai[tau * PP + p] = __dp4a((int)kv.x, qi[p][0], __dp4a((int)kv.y, qi[p][1], 0));
+    }
+    // the results' key scales, before the stage may be refilled
+    float ks[VL];
+#pragma unroll
+    for (int r = 0; r < VL; ++r) ks[r] = __half2float(__ushort_as_half(scales[clamp(rrow[r])]));
+    release();
+    tree16<V>(ai);
+#pragma unroll
+    for (int r = 0; r < VL; ++r) acc[r] = ((((float)ai[r]) * qs[r]) * ks[r]) * 0.0078125f;
   }
 };
 
+// Producer side: streams keys [t, t + nt) of unit u into a ring stage and
+// arms its barrier with the byte count (int8: the code rows, then the scales
+// from token t - t % 8, rounded up to 16 bytes; the scale array of a unit is
+// padded to a multiple of 8 tokens, so the copy stays inside it).
+template <class KF>
+__device__ __forceinline__ void issue_tile(const SelectArgs& a, uint8_t* stage, uint64_t* full, int u, int64_t t,
+                                           int nt, uint64_t pol) {
+  const int64_t row = (int64_t)u * a.stride + t;
+  if constexpr (KF::kInt8) {
+    const int d = (int)(t & 7);  // the scales start at token t - d (16-byte aligned)
+    const uint32_t cb = (uint32_t)nt * kDim, sb = ((uint32_t)(nt + d) * 2u + 15u) & ~15u;
+    mbar_arrive_expect_tx(full, cb + sb);
+    bulk_g2s_hint(stage, a.keys8 + row * kDim, cb, full, pol);
+    bulk_g2s_hint(stage + KeysInt8::kScaleOff, a.kscale + (row - d), sb, full, pol);
+  } else {
+    const uint32_t bytes = (uint32_t)nt * kKeyBytes;
+    mbar_arrive_expect_tx(full, bytes);
+    bulk_g2s_hint(stage, a.keys + row * kDim, bytes, full, pol);
+  }
+}
+
+template <int PP, class KF>
+struct ScorerFor {
+  using type = Scorer<PP>;
+};
+template <int PP>
+struct ScorerFor<PP, KeysInt8> {
+  using type = ScorerI8<PP>;
+};
 // Start of a piece: counters cleared, thresholds set (consumer threads).
 __device__ __forceinline__ void piece_begin(const ScoreSmem& sm, int P, const uint64_t* start_thr, int ctid) {
   if (ctid < P) {

@@ -171,7 +171,11 @@ __device__ __forceinline__ int64_t cta_start(int c, int64_t T, int G) {
 // Launch-side structures
 // ---------------------------------------------------------------------------
 struct SelectArgs {
-  const uint16_t* keys;        // bf16 [.][stride][128], unit id major
+  const uint16_t* keys;        // bf16 [.][stride][128], unit id major (bf16 indexer)
+  const int8_t* keys8;         // int8 [.][stride][128] codes (int8 indexer), else nullptr
+  const uint16_t* kscale;      // fp16 [.][stride] key scales (int8 indexer)
+  int8_t* q8;                  // [n][P][128] query codes of this step (int8 indexer)
+  uint16_t* qscale;            // [n][P] their fp16 scales
   int64_t stride;              // token stride between units
   const int32_t* units;        // [n] unit ids (device)
   const int32_t* len;          // device lengths indexed by unit id
@@ -269,7 +273,9 @@ struct AppendArgs {
   const uint16_t* rows;        // [n][n_tok][row_elems]
   const uint16_t* keys;        // [n][n_tok][128]
   uint16_t* host_pool;         // device-visible address
-  uint16_t* idx;               // [U][stride][128]
+  uint16_t* idx;               // [U][stride][128] bf16 indexer, or nullptr
+  int8_t* idx8;                // [U][stride][128] int8 codes, or nullptr
+  uint16_t* idxs;              // [U][stride] fp16 scales of idx8
   int32_t* len;                // [U]
   DevStats* stats;
 };
@@ -325,13 +331,14 @@ struct FusedArgs {
   int32_t n_gather;            // CTAs 0 .. n_gather-1 only fill miss rows
   int32_t smem_bytes;          // dynamic shared memory of one CTA
   uint32_t* plan_flag;         // == epoch once CTA 0 has run the plan
+  uint32_t* qdone;             // CTAs done quantizing queries (int8 indexer); zero between launches
 };
 
 // Sets the thread-local message returned by kvo_last_error().
 void set_last_error(const char* msg);
 
 // Host-side launchers (return cudaError_t of the launch).
-int score_cap_for(int P, int k);
+int score_cap_for(int P, int k, bool int8);
 cudaError_t launch_plan(const SelectArgs& a, cudaStream_t s);
 cudaError_t launch_score(const SelectArgs& a, cudaStream_t s);
 cudaError_t launch_select(const SelectArgs& a, cudaStream_t s);
@@ -342,7 +349,8 @@ cudaError_t launch_reset(const ResetArgs& a, cudaStream_t s);
 cudaError_t launch_order_init(int32_t* order, int32_t* par, int U, int C, cudaStream_t s);
 cudaError_t launch_set_len(int32_t* len, int32_t unit, int32_t value, cudaStream_t s);
 cudaError_t launch_fill_i32(int32_t* p, int32_t v, size_t n, cudaStream_t s);
-size_t fused_smem_bytes(int P, int k, int cap);
+size_t fused_smem_bytes(int P, int k, int cap, bool int8);
+cudaError_t launch_quant_keys(const uint16_t* src, int64_t n, int8_t* codes, uint16_t* scales, cudaStream_t s);
 int fused_chunk_rows();
 cudaError_t launch_fused(const FusedArgs& a, int grid, cudaStream_t s);
 

@@ -78,7 +78,7 @@ int kvo_select_noalloc(const void* keys, int64_t unit_stride, const int32_t* cac
     return noalloc_fail(KVO_EINVAL, "unit_stride out of range");
   if ((reinterpret_cast<uintptr_t>(keys) & 15u) || (reinterpret_cast<uintptr_t>(queries) & 15u))
     return noalloc_fail(KVO_EINVAL, "keys/queries not 16-byte aligned");
-  const int cap = kvo::score_cap_for(n_pos, k);
+  const int cap = kvo::score_cap_for(n_pos, k, false);
   if (cap == 0) return noalloc_fail(KVO_EINVAL, "k too large for n_pos");
   int dev = 0, n_sm = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kNoallocMaxDevices)

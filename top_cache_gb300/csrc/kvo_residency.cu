@@ -219,11 +219,20 @@ __global__ void __launch_bounds__(256) append_kernel(AppendArgs a) {
     *reinterpret_cast<uint4*>(a.host_pool + ((int64_t)u * a.stride + base + tj) * a.row_elems + c * 8) =
         src[q];
   }
-  const int64_t nkey_chunks = (int64_t)a.n_tok * (kDim / 8);
-  const uint4* ksrc = reinterpret_cast<const uint4*>(a.keys + (int64_t)i * a.n_tok * kDim);
-  for (int64_t q = tid; q < nkey_chunks; q += blockDim.x) {
-    const int64_t tj = q / (kDim / 8), c = q - tj * (kDim / 8);
-    *reinterpret_cast<uint4*>(a.idx + ((int64_t)u * a.stride + base + tj) * kDim + c * 8) = ksrc[q];
+  if (a.idx8) {
+    // int8 indexer: each new key rotated and quantized by one warp
+    const int w = tid >> 5, nw = blockDim.x >> 5;
+    for (int tj = w; tj < a.n_tok; tj += nw) {
+      const int64_t dst = (int64_t)u * a.stride + base + tj;
+      dev::warp_quant128(a.keys + ((int64_t)i * a.n_tok + tj) * kDim, a.idx8 + dst * kDim, a.idxs + dst, tid & 31);
+    }
+  } else {
+    const int64_t nkey_chunks = (int64_t)a.n_tok * (kDim / 8);
+    const uint4* ksrc = reinterpret_cast<const uint4*>(a.keys + (int64_t)i * a.n_tok * kDim);
+    for (int64_t q = tid; q < nkey_chunks; q += blockDim.x) {
+      const int64_t tj = q / (kDim / 8), c = q - tj * (kDim / 8);
+      *reinterpret_cast<uint4*>(a.idx + ((int64_t)u * a.stride + base + tj) * kDim + c * 8) = ksrc[q];
+    }
   }
   __syncthreads();
   if (tid == 0) {

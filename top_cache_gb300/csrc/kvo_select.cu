@@ -89,12 +89,11 @@ __global__ void __launch_bounds__(1024) plan_kernel(SelectArgs a) {
 // ---------------------------------------------------------------------------
 // score: one persistent CTA per flat piece of the token range.
 // ---------------------------------------------------------------------------
-template <int PP>
+template <int PP, class KF>
 __global__ void __launch_bounds__(kScoreThreads, 1) score_kernel(SelectArgs a) {
   extern __shared__ __align__(128) uint8_t smem[];
-  uint8_t* ring = smem;
-  uint64_t* full = reinterpret_cast<uint64_t*>(smem + kStages * kTileBytes);
-  uint64_t* empty = full + kStages;
+  ScoreSmem sm;
+  sm.carve<KF>(smem, a.P, a.cap);
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int c = blockIdx.x;
@@ -102,9 +101,9 @@ __global__ void __launch_bounds__(kScoreThreads, 1) score_kernel(SelectArgs a) {
   const int64_t g0 = cta_start(c, a.T, a.G), g1 = cta_start(c + 1, a.T, a.G);
   const int32_t* only = a.fallback ? a.fb : nullptr;  // rescoring pass: flagged units only
   if (tid == 0) {
-    for (int s = 0; s < kStages; ++s) {
-      mbar_init(&full[s], 1);
-      mbar_init(&empty[s], kCW);
+    for (int s = 0; s < KF::kStages; ++s) {
+      mbar_init(&sm.full[s], 1);
+      mbar_init(&sm.empty[s], kCW);
     }
     fence_mbar_init();
   }
@@ -121,16 +120,13 @@ __global__ void __launch_bounds__(kScoreThreads, 1) score_kernel(SelectArgs a) {
       uint32_t seq = 0;
       while (it.next(pc)) {
         const int u = a.units[pc.i];
-        const uint16_t* kb = a.keys + ((int64_t)u * a.stride) * kDim;
         for (int64_t t = pc.t0; t < pc.t1; t += kTile, ++seq) {
-          const int stage = seq % kStages;
-          const uint32_t round = seq / kStages;
-          if (round > 0 && !mbar_wait(&empty[stage], (round - 1) & 1u, a.wait_ns))
+          const int stage = seq % KF::kStages;
+          const uint32_t round = seq / KF::kStages;
+          if (round > 0 && !mbar_wait(&sm.empty[stage], (round - 1) & 1u, a.wait_ns))
             atomicOr(a.err, kErrTimeout);
-          const int64_t nt = (pc.t1 - t) < kTile ? (pc.t1 - t) : kTile;
-          const uint32_t bytes = (uint32_t)nt * kKeyBytes;
-          mbar_arrive_expect_tx(&full[stage], bytes);
-          bulk_g2s_hint(ring + stage * kTileBytes, kb + t * kDim, bytes, &full[stage], pol);
+          const int nt = (int)((pc.t1 - t) < kTile ? (pc.t1 - t) : kTile);
+          issue_tile<KF>(a, sm.ring + stage * KF::kStageBytes, &sm.full[stage], u, t, nt, pol);
         }
       }
     }
@@ -140,11 +136,9 @@ __global__ void __launch_bounds__(kScoreThreads, 1) score_kernel(SelectArgs a) {
   // ---------------- consumers ----------------------------------------------
   const int ctid = tid;  // consumers are threads 0..kCT-1
   const int P = a.P, k = a.k, cap = a.cap;
-  ScoreSmem sm;
-  sm.carve(smem, P, cap);
-  Scorer<PP> sc;
+  typename ScorerFor<PP, KF>::type sc;
   sc.init(warp, lane);
-  constexpr int V = Scorer<PP>::V;
+  constexpr int V = ScorerLanes<PP>::V;
 
   PieceIter it;
   it.begin(a.off, a.n, g0, g1, only);
@@ -153,24 +147,33 @@ __global__ void __launch_bounds__(kScoreThreads, 1) score_kernel(SelectArgs a) {
   while (it.next(pc)) {
     const int i = pc.i;
     uint64_t* gth = a.gthr + (int64_t)i * P;
-    sc.load_queries(a.queries, i, P);
+    sc.load_queries(a, i, P);
     piece_begin(sm, P, (!a.fallback && a.tspec) ? a.tspec + (int64_t)i * P : nullptr, ctid);
     int ti = 0;
     for (int64_t t = pc.t0; t < pc.t1; t += kTile, ++seq, ++ti) {
-      const int stage = seq % kStages;
-      const uint32_t round = seq / kStages;
-      if (!mbar_wait(&full[stage], round & 1u, a.wait_ns) && lane == 0) atomicOr(a.err, kErrTimeout);
+      const int stage = seq % KF::kStages;
+      const uint32_t round = seq / KF::kStages;
+      if (!mbar_wait(&sm.full[stage], round & 1u, a.wait_ns) && lane == 0) atomicOr(a.err, kErrTimeout);
       const int nt = (int)((pc.t1 - t) < kTile ? (pc.t1 - t) : kTile);
       float acc[V];
-      sc.score(ring + stage * kTileBytes, acc, [&] {
+      sc.score(sm.ring + stage * KF::kStageBytes, t, acc, [&] {
         __syncwarp();
-        if (lane == 0) mbar_arrive(&empty[stage]);
+        if (lane == 0) mbar_arrive(&sm.empty[stage]);
       });
       sc.filter(acc, t, nt, pc.len, P, sm.thr, sm.cnt, sm.cand, cap);
       if (t + kTile < pc.t1 && (ti + 1) % kCheckTiles == 0) piece_check(sm, P, k, cap, gth, ctid);
     }
     piece_end(sm, P, k, cap, gth, (int64_t)c + i, a.seg_keys, a.seg_cnt, ctid);
   }
+}
+
+// int8 indexer: rotation and quantization of n keys (one warp per key).
+__global__ void __launch_bounds__(256) quant_keys_kernel(const uint16_t* src, int64_t n, int8_t* codes,
+                                                         uint16_t* scales) {
+  const int lane = threadIdx.x & 31;
+  const int64_t w0 = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  const int64_t nw = ((int64_t)gridDim.x * blockDim.x) >> 5;
+  for (int64_t r = w0; r < n; r += nw) warp_quant128(src + r * kDim, codes + r * kDim, scales + r, lane);
 }
 
 // ---------------------------------------------------------------------------
@@ -219,8 +222,9 @@ __global__ void __launch_bounds__(kSelThreads) select_kernel(SelectArgs a) {
 // ---------------------------------------------------------------------------
 // host launchers
 // ---------------------------------------------------------------------------
-int score_cap_for(int P, int k) {
-  const long avail = (long)kSmemMax - kSmemFixed - (long)k * 8 - 256;
+int score_cap_for(int P, int k, bool int8) {
+  const long fixed = int8 ? smem_fixed<KeysInt8>() : smem_fixed<KeysBf16>();
+  const long avail = (long)kSmemMax - fixed - (long)k * 8 - 256;
   if (avail <= 0) return 0;
   long cap = avail / ((long)P * 8);
   long target = 3L * k;
@@ -231,8 +235,17 @@ int score_cap_for(int P, int k) {
   return (int)cap;
 }
 
+template <class KF>
 static size_t score_smem(const SelectArgs& a) {
-  return (size_t)kSmemFixed + (size_t)a.P * a.cap * 8 + (size_t)a.k * 8;
+  return (size_t)smem_fixed<KF>() + (size_t)a.P * a.cap * 8 + (size_t)a.k * 8;
+}
+
+cudaError_t launch_quant_keys(const uint16_t* src, int64_t n, int8_t* codes, uint16_t* scales, cudaStream_t s) {
+  if (n <= 0) return cudaSuccess;
+  int64_t blocks = (n + 7) / 8;
+  if (blocks > 4096) blocks = 4096;
+  quant_keys_kernel<<<(int)blocks, 256, 0, s>>>(src, n, codes, scales);
+  return cudaGetLastError();
 }
 
 cudaError_t launch_plan(const SelectArgs& a, cudaStream_t s) {
@@ -240,21 +253,26 @@ cudaError_t launch_plan(const SelectArgs& a, cudaStream_t s) {
   return cudaGetLastError();
 }
 
-template <int PP>
+template <int PP, class KF>
 static cudaError_t launch_score_pp(const SelectArgs& a, cudaStream_t s) {
-  const size_t smem = score_smem(a);
-  cudaError_t e = cudaFuncSetAttribute(score_kernel<PP>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+  const size_t smem = score_smem<KF>(a);
+  cudaError_t e = cudaFuncSetAttribute(score_kernel<PP, KF>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        (int)smem);
   if (e != cudaSuccess) return e;
-  score_kernel<PP><<<a.G, kScoreThreads, smem, s>>>(a);
+  score_kernel<PP, KF><<<a.G, kScoreThreads, smem, s>>>(a);
   return cudaGetLastError();
 }
 
+template <class KF>
+static cudaError_t launch_score_kf(const SelectArgs& a, cudaStream_t s) {
+  if (a.P <= 1) return launch_score_pp<1, KF>(a, s);
+  if (a.P <= 2) return launch_score_pp<2, KF>(a, s);
+  if (a.P <= 4) return launch_score_pp<4, KF>(a, s);
+  return launch_score_pp<8, KF>(a, s);
+}
+
 cudaError_t launch_score(const SelectArgs& a, cudaStream_t s) {
-  if (a.P <= 1) return launch_score_pp<1>(a, s);
-  if (a.P <= 2) return launch_score_pp<2>(a, s);
-  if (a.P <= 4) return launch_score_pp<4>(a, s);
-  return launch_score_pp<8>(a, s);
+  return a.keys8 ? launch_score_kf<KeysInt8>(a, s) : launch_score_kf<KeysBf16>(a, s);
 }
 
 cudaError_t launch_select(const SelectArgs& a, cudaStream_t s) {

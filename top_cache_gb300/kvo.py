@@ -35,6 +35,8 @@ KVO_OPT_PIECE_TOKENS = 9
 KVO_OPT_HOST_HUGE_PAGE = 10
 PROF_KINDS = ("append", "plan", "score", "select", "residency", "gather", "reset", "rescore",
               "reselect", "fused")
+KVO_IDX_BF16 = 0
+KVO_IDX_INT8 = 1
 KVO_GATHER_LDG = 0
 KVO_GATHER_BULK = 1
 
@@ -49,7 +51,7 @@ class KvoConfig(ctypes.Structure):
                 ("max_tokens", ctypes.c_int64), ("idx_dim", ctypes.c_int32),
                 ("row_elems", ctypes.c_int32), ("topk", ctypes.c_int32),
                 ("hot_capacity", ctypes.c_int32), ("n_positions", ctypes.c_int32),
-                ("device", ctypes.c_int32)]
+                ("device", ctypes.c_int32), ("idx_dtype", ctypes.c_int32)]
 
 
 class KvoStats(ctypes.Structure):
@@ -153,9 +155,9 @@ def _units(units):
 
 
 def kvo_create(n_requests, n_layers, max_tokens, topk, hot_capacity, n_positions=1,
-               row_elems=576, idx_dim=128, device=0):
+               row_elems=576, idx_dim=128, device=0, idx_dtype=KVO_IDX_BF16):
     cfg = KvoConfig(n_requests, n_layers, max_tokens, idx_dim, row_elems, topk, hot_capacity,
-                    n_positions, device)
+                    n_positions, device, idx_dtype)
     h = ctypes.c_void_p()
     _check(lib().kvo_create(ctypes.byref(cfg), ctypes.byref(h)))
     return h.value
@@ -262,14 +264,15 @@ class Kvo:
     """A handle plus output buffers for all units (plumbing around the C ABI)."""
 
     def __init__(self, n_requests, n_layers, max_tokens, topk, hot_capacity, n_positions=1,
-                 row_elems=576, device=0):
+                 row_elems=576, device=0, idx_dtype=KVO_IDX_BF16):
         import torch
         self.n_requests, self.n_layers = n_requests, n_layers
         self.U = n_requests * n_layers
         self.max_tokens, self.topk, self.C = max_tokens, topk, hot_capacity
         self.P, self.R, self.device = n_positions, row_elems, device
+        self.idx_dtype = idx_dtype
         self.h = kvo_create(n_requests, n_layers, max_tokens, topk, hot_capacity, n_positions,
-                            row_elems, 128, device)
+                            row_elems, 128, device, idx_dtype)
         dev = torch.device("cuda", device)
         shape = (self.U, self.P, self.topk)
         self.tokens = torch.empty(shape, dtype=torch.int32, device=dev)
