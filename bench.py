@@ -448,7 +448,13 @@ def run_kvo(args, log):
         "steps_ms": {"median": round(statistics.median(step_ms), 4),
                      "p90": round(sorted(step_ms)[int(0.9 * (len(step_ms) - 1))], 4),
                      "warm_median": round(statistics.median(warm), 4) if warm else None,
-                     "cold_median": round(statistics.median(cold), 4) if cold else None},
+                     "cold_median": round(statistics.median(cold), 4) if cold else None,
+                     "p99": round(sorted(step_ms)[int(0.99 * (len(step_ms) - 1))], 4),
+                     "max": round(max(step_ms), 4),
+                     # the slowest steps as (position in the sequence, ms): tells a slow
+                     # cold start from stalls that hit arbitrary steps
+                     "slowest": [(positions[i], round(step_ms[i], 3)) for i in
+                                 sorted(range(len(step_ms)), key=lambda i: -step_ms[i])[:8]]},
         "kernels": kernels,
         "host_link_gbs": {k_: round(v, 1) for k_, v in link.items()},
         "hits_per_step": (st1["hits"] - st0["hits"]) / n_steps,

@@ -38,7 +38,10 @@
  *  R7 capacity: |W| > capacity -> unit status ORACLE_ECAPACITY, nothing
  *               changes, slots -1.
  *  R8 append  : new rows go to the host rows only; their cache_slots are -1.
- *  R9 int8 indexer ("FlashOffloading ... What does it mean?", the LIM C8
+ *  R9-R11     : an empty shelf at the start, the benchmark workloads' shared
+ *               queries across MTP positions and one contiguous 576-element
+ *               row per token need no arithmetic of their own here.
+ *  R12 int8 indexer ("FlashOffloading ... What does it mean?", the LIM C8
  *               paragraph: Hadamard rotation and int8 quantization of the
  *               indexer query and key, fp16 dequantization scales that follow
  *               the indexer layout):
@@ -75,9 +78,9 @@
 typedef struct oracle_unit {
   int64_t tmax;
   int32_t row_elems, topk, capacity, n_pos, keep_rows;
-  int32_t idx_int8;      /* R9: 1 = scores from the int8 indexer */
-  int8_t* kcode;         /* [tmax][128] int8 key codes (R9), or NULL */
-  uint16_t* kscale;      /* [tmax] fp16 key scales (R9), or NULL */
+  int32_t idx_int8;      /* R12: 1 = scores from the int8 indexer */
+  int8_t* kcode;         /* [tmax][128] int8 key codes (R12), or NULL */
+  uint16_t* kscale;      /* [tmax] fp16 key scales (R12), or NULL */
   int64_t len;
   uint32_t stamp;
   uint16_t* keys;        /* [tmax][128] indexer keys (device copy in the real system) */
@@ -110,7 +113,7 @@ float oracle_score(const uint16_t* q, const uint16_t* k) {
   return s;
 }
 
-/* ---- R9: int8 indexer ------------------------------------------------ */
+/* ---- R12: int8 indexer ------------------------------------------------ */
 
 /* fp32 -> fp16 bits, round to nearest even (IEEE 754 binary16). */
 uint16_t oracle_f32_to_f16(float f) {
@@ -163,7 +166,7 @@ float oracle_f16_to_f32(uint16_t h) {
   return f;
 }
 
-/* R9 rotation: unnormalised fast Walsh-Hadamard transform, fixed stage order. */
+/* R12 rotation: unnormalised fast Walsh-Hadamard transform, fixed stage order. */
 void oracle_fwht128(const float* in, float* out) {
   float y[ORACLE_DIM];
   memcpy(y, in, sizeof(y));
@@ -177,7 +180,7 @@ void oracle_fwht128(const float* in, float* out) {
   memcpy(out, y, sizeof(y));
 }
 
-/* R9 quantization of an already rotated vector: fp16 scale, int8 codes. */
+/* R12 quantization of an already rotated vector: fp16 scale, int8 codes. */
 void oracle_quant_rotated(const float* y, int8_t* code, uint16_t* scale) {
   float m = 0.0f;
   for (int d = 0; d < ORACLE_DIM; ++d) {
@@ -195,7 +198,7 @@ void oracle_quant_rotated(const float* y, int8_t* code, uint16_t* scale) {
   *scale = s16;
 }
 
-/* R9: rotate and quantize one bf16 vector of 128. */
+/* R12: rotate and quantize one bf16 vector of 128. */
 void oracle_quant128(const uint16_t* x, int8_t* code, uint16_t* scale) {
   float v[ORACLE_DIM], y[ORACLE_DIM];
   for (int d = 0; d < ORACLE_DIM; ++d) v[d] = bf16_value(x[d]);
@@ -203,7 +206,7 @@ void oracle_quant128(const uint16_t* x, int8_t* code, uint16_t* scale) {
   oracle_quant_rotated(y, code, scale);
 }
 
-/* R9 score of int8 codes with their fp16 scales. */
+/* R12 score of int8 codes with their fp16 scales. */
 float oracle_score_i8(const int8_t* q, uint16_t sq, const int8_t* k, uint16_t sk) {
   int32_t dot = 0;
   for (int d = 0; d < ORACLE_DIM; ++d) dot += (int32_t)q[d] * (int32_t)k[d];
@@ -246,7 +249,7 @@ oracle_unit* oracle_unit_new(int64_t tmax, int32_t dim, int32_t row_elems, int32
 
 void oracle_unit_free(oracle_unit* u);
 
-/* As oracle_unit_new; idx_int8 = 1 selects the int8 indexer (R9). */
+/* As oracle_unit_new; idx_int8 = 1 selects the int8 indexer (R12). */
 oracle_unit* oracle_unit_new2(int64_t tmax, int32_t dim, int32_t row_elems, int32_t topk,
                               int32_t capacity, int32_t n_pos, int32_t keep_rows, int32_t idx_int8) {
   oracle_unit* u = oracle_unit_new(tmax, dim, row_elems, topk, capacity, n_pos, keep_rows);
@@ -274,7 +277,7 @@ int32_t oracle_append(oracle_unit* u, int32_t n_tok, const uint16_t* rows, const
   if (n_tok < 0) return ORACLE_EINVAL;
   if (u->len + n_tok > u->tmax) return ORACLE_ERANGE;
   memcpy(u->keys + (size_t)u->len * ORACLE_DIM, keys, (size_t)n_tok * ORACLE_DIM * 2);
-  if (u->idx_int8) /* R9: keys are quantized once, when they arrive */
+  if (u->idx_int8) /* R12: keys are quantized once, when they arrive */
     for (int32_t j = 0; j < n_tok; ++j)
       oracle_quant128(keys + (size_t)j * ORACLE_DIM, u->kcode + (size_t)(u->len + j) * ORACLE_DIM,
                       u->kscale + u->len + j);
@@ -311,7 +314,7 @@ static int cmp_lru(const void* a, const void* b) {
   return (x->slot > y->slot) - (x->slot < y->slot);
 }
 
-/* Score of token t for query q under the unit's indexer (R1 or R9). */
+/* Score of token t for query q under the unit's indexer (R1 or R12). */
 static float unit_score(const oracle_unit* u, const uint16_t* q, const int8_t* qcode, uint16_t qscale,
                         int64_t t) {
   if (u->idx_int8)
@@ -355,7 +358,7 @@ int32_t oracle_step(oracle_unit* u, const uint16_t* queries, int32_t* tok, float
     const uint16_t* q = queries + (size_t)p * ORACLE_DIM;
     int8_t qc[ORACLE_DIM];
     uint16_t qs = 0;
-    if (u->idx_int8) oracle_quant128(q, qc, &qs); /* R9: the query, each step */
+    if (u->idx_int8) oracle_quant128(q, qc, &qs); /* R12: the query, each step */
     for (int64_t t = 0; t < vis; ++t) {
       buf[t].score = unit_score(u, q, qc, qs, t);
       buf[t].token = (int32_t)t;

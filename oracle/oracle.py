@@ -96,7 +96,7 @@ def score(q, k):
     return np.float32(lib().oracle_score(q.ctypes.data, k.ctypes.data))
 
 
-# ---- int8 indexer (reading R9 of kvo_oracle.c) ------------------------------
+# ---- int8 indexer (reading R12 of kvo_oracle.c) ------------------------------
 def f32_to_f16(x):
     """fp16 bits (uint16) of an fp32 value, round to nearest even."""
     return int(lib().oracle_f32_to_f16(float(np.float32(x))))

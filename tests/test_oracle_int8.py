@@ -1,4 +1,4 @@
-"""Pins of the oracle's int8 indexer (reading R9: Hadamard rotation, fp16 scale, int8 codes).
+"""Pins of the oracle's int8 indexer (reading R12: Hadamard rotation, fp16 scale, int8 codes).
 
 Each check compares the oracle with something other than itself: numpy's fp16
 conversion, the closed form of the Walsh-Hadamard matrix, hand-derived cases

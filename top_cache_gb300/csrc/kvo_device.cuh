@@ -60,7 +60,7 @@ constexpr int smem_fixed() {
 }
 
 // Rotation and int8 quantization of one 128-element bf16 vector by a warp
-// (reading R9 of the oracle; "FlashOffloading ... What does it mean?", the
+// (reading R12 of the oracle; "FlashOffloading ... What does it mean?", the
 // LIM C8 paragraph): y = H x by the unnormalised fast Walsh-Hadamard
 // transform in fp32, stages h = 1 .. 64, pair (i, i + h) -> (a + b, a - b);
 // scale = fp16(max|y| / 127) (round to nearest even); codes =
@@ -640,7 +640,7 @@ struct Scorer : ScorerLanes<PP> {
   }
 };
 
-// int8 keys (reading R9): exact int32 dot products of the codes (4-byte dot
+// int8 keys (reading R12): exact int32 dot products of the codes (4-byte dot
 // instructions, tree of integer sums), then (((float)dot * s_q) * s_k) / 128.
 template <int PP>
 struct ScorerI8 : ScorerLanes<PP> {
@@ -1283,6 +1283,8 @@ __device__ __forceinline__ uint32_t residency_body(const ResidencyArgs& a, int i
                                                    int32_t* status_out, Ready ready) {
   constexpr int kB = 8;    // loads in flight per thread in the list passes
   constexpr int kTB = 16;  // and in the top-k passes
+  constexpr int NW = NT / 32;
+  const int lane = tid & 31, wid = tid >> 5;
   const int C = a.C, PK = a.P * a.k;
   const int nwords = (C + 31) >> 5;
   const int u = a.units[i];
@@ -1335,42 +1337,49 @@ __device__ __forceinline__ uint32_t residency_body(const ResidencyArgs& a, int i
     }
     __threadfence_block();
     sync();
-    // distinct misses in token order; the bitmap words are cleared behind
-    const int per = (tw + NT - 1) / NT;
-    const int w0 = tid * per, w1 = min(tw, w0 + per);
-    constexpr int kWC = 4;  // words kept in registers between the two passes
-    uint32_t wc[kWC];
+    // distinct misses in token order; the bitmap words are cleared behind.
+    // Warp w owns words [tb, te); a slice is 32 consecutive words, one per
+    // lane, so every load is one coalesced line and emission follows token order.
+    const int tpw = (tw + NW - 1) / NW;
+    const int tb = min(tw, wid * tpw), te = min(tw, tb + tpw);
     uint32_t c = 0;
+    for (int w = tb; w < te; w += 32 * kB) {
+      uint32_t wv[kB];
 #pragma unroll
-    for (int x = 0; x < kWC; ++x) {
-      wc[x] = w0 + x < w1 ? __ldcg(&tbm[w0 + x]) : 0u;
-      c += __popc(wc[x]);
+      for (int x = 0; x < kB; ++x) wv[x] = w + x * 32 + lane < te ? __ldcg(&tbm[w + x * 32 + lane]) : 0u;
+#pragma unroll
+      for (int x = 0; x < kB; ++x) c += __popc(wv[x]);
     }
-#pragma unroll 8
-    for (int w = w0 + kWC; w < w1; ++w) c += __popc(__ldcg(&tbm[w]));
     uint32_t total;
-    uint32_t pos = block_excl_scan<NT>(c, wsum, &total, tid, sync);
+    // the exclusive prefix of lane 0 is everything the lower warps hold
+    uint32_t pos = __shfl_sync(kFull, block_excl_scan<NT>(c, wsum, &total, tid, sync), 0);
     m = total;
-    if (c) {
-      auto emit_word = [&](int w, uint32_t bits) {
-        if (!bits) return;
-        tbm[w] = 0;
-        while (bits) {
-          const int b = __ffs(bits) - 1;
-          bits &= bits - 1;
-          if (pos < (uint32_t)PK) M[pos] = w * 32 + b;
-          ++pos;
-        }
-      };
-#pragma unroll
-      for (int x = 0; x < kWC; ++x) emit_word(w0 + x, wc[x]);
-      for (int w = w0 + kWC; w < w1; w += kB) {
+    if (__any_sync(kFull, c != 0)) {
+      for (int w = tb; w < te; w += 32 * kB) {
         uint32_t wv[kB];
 #pragma unroll
-        for (int x = 0; x < kB; ++x) wv[x] = w + x < w1 ? __ldcg(&tbm[w + x]) : 0u;
+        for (int x = 0; x < kB; ++x) wv[x] = w + x * 32 + lane < te ? __ldcg(&tbm[w + x * 32 + lane]) : 0u;
 #pragma unroll
-        for (int x = 0; x < kB; ++x)
-          if (w + x < w1) emit_word(w + x, wv[x]);
+        for (int x = 0; x < kB; ++x) {
+          uint32_t bits = wv[x];
+          if (__ballot_sync(kFull, bits != 0) == 0) continue;
+          const uint32_t cnt = __popc(bits);
+          uint32_t incl = cnt;
+#pragma unroll
+          for (int o = 1; o < 32; o <<= 1) {
+            const uint32_t y = __shfl_up_sync(kFull, incl, o);
+            if (lane >= o) incl += y;
+          }
+          uint32_t p = pos + incl - cnt;
+          if (bits) tbm[w + x * 32 + lane] = 0;
+          while (bits) {
+            const int b = __ffs(bits) - 1;
+            bits &= bits - 1;
+            if (p < (uint32_t)PK) M[p] = (w + x * 32 + lane) * 32 + b;
+            ++p;
+          }
+          pos += __shfl_sync(kFull, incl, 31);
+        }
       }
     }
     uint32_t hc = 0;
@@ -1389,45 +1398,46 @@ __device__ __forceinline__ uint32_t residency_body(const ResidencyArgs& a, int i
         lu[w * 32 + b] = stamp;
       }
     }
-    const int per = (C + NT - 1) / NT;
-    const int j0 = tid * per, j1 = min(C, j0 + per);
+    // warp w owns list entries [lb, le); a slice is 32 consecutive entries,
+    // one per lane (coalesced loads), ranked in list order by ballots
+    const int lpw = (C + NW - 1) / NW;
+    const int lb = min(C, wid * lpw), le = min(C, lb + lpw);
     // slots outside [0, C) never come from a valid list; they count as touched
     auto hit = [&](int s) { return (unsigned)s >= (unsigned)C || ((bitmap[s >> 5] >> (s & 31)) & 1u) != 0; };
-    // the thread's run of the LRU list: its first kB entries stay in
-    // registers, the rest is read in batches of kB loads
-    int32_t cv[kB];
-#pragma unroll
-    for (int x = 0; x < kB; ++x) cv[x] = j0 + x < j1 ? cur[j0 + x] : 0;
     auto count_untouched = [&]() {
       uint32_t c = 0;
-#pragma unroll
-      for (int x = 0; x < kB; ++x)
-        if (j0 + x < j1) c += hit(cv[x]) ? 0u : 1u;
-      for (int j = j0 + kB; j < j1; j += kB) {
+      for (int j = lb; j < le; j += 32 * kB) {
         int32_t v[kB];
 #pragma unroll
-        for (int x = 0; x < kB; ++x) v[x] = j + x < j1 ? cur[j + x] : 0;
+        for (int x = 0; x < kB; ++x) v[x] = j + x * 32 + lane < le ? cur[j + x * 32 + lane] : 0;
 #pragma unroll
-        for (int x = 0; x < kB; ++x)
-          if (j + x < j1) c += hit(v[x]) ? 0u : 1u;
+        for (int x = 0; x < kB; ++x) c += (j + x * 32 + lane < le && !hit(v[x])) ? 1u : 0u;
       }
       return c;
+    };
+    // the untouched entries of this warp's range, in list order, go to
+    // out[q0 + rank] while q0 + rank < lim; returns nothing
+    auto emit_untouched = [&](uint32_t q0, uint32_t lim, int32_t* out) {
+      const uint32_t lt = (1u << lane) - 1u;
+      for (int j = lb; j < le && q0 < lim; j += 32 * kB) {
+        int32_t v[kB];
+#pragma unroll
+        for (int x = 0; x < kB; ++x) v[x] = j + x * 32 + lane < le ? cur[j + x * 32 + lane] : 0;
+#pragma unroll
+        for (int x = 0; x < kB; ++x) {
+          const bool un = j + x * 32 + lane < le && !hit(v[x]);
+          const uint32_t bal = __ballot_sync(kFull, un);
+          const uint32_t r = q0 + __popc(bal & lt);
+          if (un && r < lim) out[r] = v[x];
+          q0 += __popc(bal);
+        }
+      }
     };
     if (m > 0) {
       // victims: the first m slots of the LRU list that were not hit
       uint32_t total;
-      uint32_t rank = block_excl_scan<NT>(count_untouched(), wsum, &total, tid, sync);
-#pragma unroll
-      for (int x = 0; x < kB; ++x)
-        if (j0 + x < j1 && rank < m && !hit(cv[x])) V[rank++] = cv[x];
-      for (int j = j0 + kB; j < j1 && rank < m; j += kB) {
-        int32_t v[kB];
-#pragma unroll
-        for (int x = 0; x < kB; ++x) v[x] = j + x < j1 ? cur[j + x] : 0;
-#pragma unroll
-        for (int x = 0; x < kB; ++x)
-          if (j + x < j1 && rank < m && !hit(v[x])) V[rank++] = v[x];
-      }
+      const uint32_t rank = __shfl_sync(kFull, block_excl_scan<NT>(count_untouched(), wsum, &total, tid, sync), 0);
+      emit_untouched(rank, m, V);
       sync();
       // i-th miss (token order) takes the i-th victim
       for (uint32_t r0 = tid; r0 < m; r0 += 4 * NT) {
@@ -1459,18 +1469,8 @@ __device__ __forceinline__ uint32_t residency_body(const ResidencyArgs& a, int i
     if (hits + m > 0) {
       // new list: untouched slots in their order, then the touched ones in slot order
       uint32_t kept;
-      uint32_t q = block_excl_scan<NT>(count_untouched(), wsum, &kept, tid, sync);
-#pragma unroll
-      for (int x = 0; x < kB; ++x)
-        if (j0 + x < j1 && !hit(cv[x]) && q < (uint32_t)C) nxt[q++] = cv[x];
-      for (int j = j0 + kB; j < j1; j += kB) {
-        int32_t v[kB];
-#pragma unroll
-        for (int x = 0; x < kB; ++x) v[x] = j + x < j1 ? cur[j + x] : 0;
-#pragma unroll
-        for (int x = 0; x < kB; ++x)
-          if (j + x < j1 && !hit(v[x]) && q < (uint32_t)C) nxt[q++] = v[x];
-      }
+      const uint32_t q = __shfl_sync(kFull, block_excl_scan<NT>(count_untouched(), wsum, &kept, tid, sync), 0);
+      emit_untouched(q, (uint32_t)C, nxt);
       const int wper = (nwords + NT - 1) / NT;
       const int v0 = tid * wper, v1 = min(nwords, v0 + wper);
       uint32_t tc = 0;

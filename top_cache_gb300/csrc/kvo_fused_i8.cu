@@ -1,4 +1,4 @@
-// The fused decode step for int8 indexer keys (reading R9 of the oracle;
+// The fused decode step for int8 indexer keys (reading R12 of the oracle;
 // "FlashOffloading ... What does it mean?", the LIM C8 paragraph): the same
 // kernel as kvo_fused.cu, scoring int8 code rows with their fp16 scales.
 #include "kvo_fused.cuh"
