@@ -1281,8 +1281,9 @@ template <int NT, class Sync, class Ready>
 __device__ __forceinline__ uint32_t residency_body(const ResidencyArgs& a, int i, uint32_t* bitmap, int32_t* M,
                                                    int32_t* V, uint32_t* wsum, int tid, Sync sync,
                                                    int32_t* status_out, Ready ready) {
-  constexpr int kB = 8;    // loads in flight per thread in the list passes
+  constexpr int kB = 8;    // loads in flight per thread in the token-bitmap passes
   constexpr int kTB = 16;  // and in the top-k passes
+  constexpr int kLB = 16;  // and in the LRU-list passes (one line per lane per load)
   constexpr int NW = NT / 32;
   const int lane = tid & 31, wid = tid >> 5;
   const int C = a.C, PK = a.P * a.k;
@@ -1406,39 +1407,45 @@ __device__ __forceinline__ uint32_t residency_body(const ResidencyArgs& a, int i
     auto hit = [&](int s) { return (unsigned)s >= (unsigned)C || ((bitmap[s >> 5] >> (s & 31)) & 1u) != 0; };
     auto count_untouched = [&]() {
       uint32_t c = 0;
-      for (int j = lb; j < le; j += 32 * kB) {
-        int32_t v[kB];
+      for (int j = lb; j < le; j += 32 * kLB) {
+        int32_t v[kLB];
 #pragma unroll
-        for (int x = 0; x < kB; ++x) v[x] = j + x * 32 + lane < le ? cur[j + x * 32 + lane] : 0;
+        for (int x = 0; x < kLB; ++x) v[x] = j + x * 32 + lane < le ? cur[j + x * 32 + lane] : 0;
 #pragma unroll
-        for (int x = 0; x < kB; ++x) c += (j + x * 32 + lane < le && !hit(v[x])) ? 1u : 0u;
+        for (int x = 0; x < kLB; ++x) c += (j + x * 32 + lane < le && !hit(v[x])) ? 1u : 0u;
       }
       return c;
     };
-    // the untouched entries of this warp's range, in list order, go to
-    // out[q0 + rank] while q0 + rank < lim; returns nothing
-    auto emit_untouched = [&](uint32_t q0, uint32_t lim, int32_t* out) {
+    // One pass over this warp's range in list order: the untouched entry of
+    // rank r is the r-th victim while r < m and otherwise keeps its order at
+    // position r - m of the new list (victims are the first m untouched
+    // entries, so this is the old list without the touched slots and victims).
+    auto split_untouched = [&](uint32_t q0) {
       const uint32_t lt = (1u << lane) - 1u;
-      for (int j = lb; j < le && q0 < lim; j += 32 * kB) {
-        int32_t v[kB];
+      for (int j = lb; j < le; j += 32 * kLB) {
+        int32_t v[kLB];
 #pragma unroll
-        for (int x = 0; x < kB; ++x) v[x] = j + x * 32 + lane < le ? cur[j + x * 32 + lane] : 0;
+        for (int x = 0; x < kLB; ++x) v[x] = j + x * 32 + lane < le ? cur[j + x * 32 + lane] : 0;
 #pragma unroll
-        for (int x = 0; x < kB; ++x) {
+        for (int x = 0; x < kLB; ++x) {
           const bool un = j + x * 32 + lane < le && !hit(v[x]);
           const uint32_t bal = __ballot_sync(kFull, un);
           const uint32_t r = q0 + __popc(bal & lt);
-          if (un && r < lim) out[r] = v[x];
+          if (un) {
+            if (r < m) V[r] = v[x];
+            else if (r - m < (uint32_t)C) nxt[r - m] = v[x];
+          }
           q0 += __popc(bal);
         }
       }
     };
-    if (m > 0) {
-      // victims: the first m slots of the LRU list that were not hit
-      uint32_t total;
-      const uint32_t rank = __shfl_sync(kFull, block_excl_scan<NT>(count_untouched(), wsum, &total, tid, sync), 0);
-      emit_untouched(rank, m, V);
+    uint32_t untouched = 0;
+    if (hits + m > 0) {
+      const uint32_t q0 = __shfl_sync(kFull, block_excl_scan<NT>(count_untouched(), wsum, &untouched, tid, sync), 0);
+      split_untouched(q0);
       sync();
+    }
+    if (m > 0) {
       // i-th miss (token order) takes the i-th victim
       for (uint32_t r0 = tid; r0 < m; r0 += 4 * NT) {
         int32_t old[4];
@@ -1467,10 +1474,8 @@ __device__ __forceinline__ uint32_t residency_body(const ResidencyArgs& a, int i
     }
     sync();
     if (hits + m > 0) {
-      // new list: untouched slots in their order, then the touched ones in slot order
-      uint32_t kept;
-      const uint32_t q = __shfl_sync(kFull, block_excl_scan<NT>(count_untouched(), wsum, &kept, tid, sync), 0);
-      emit_untouched(q, (uint32_t)C, nxt);
+      // the touched slots (hits and victims) follow in slot order
+      const uint32_t kept = untouched - m;
       const int wper = (nwords + NT - 1) / NT;
       const int v0 = tid * wper, v1 = min(nwords, v0 + wper);
       uint32_t tc = 0;
