@@ -58,6 +58,20 @@
  *               rotation, H H = 128 I, so the score estimates q . k); a zero
  *               score is +0.  Keys are quantized when they are appended,
  *               queries at each step; the bf16 keys are kept only for tests.
+ *  R13 sparse attention ([LS] Decode step 7, "sparse attention consumes the
+ *               resident K/V"; the pages name an SFA/MLA model but give no
+ *               formula, so the absorbed multi-head latent attention of the
+ *               DeepSeek family is taken): per unit, position p and head h,
+ *               over the tokens t of that position's top-k list (pads
+ *               skipped), with the 576-element row r_t = [latent (512) |
+ *               rope key (64)] of the main-KV history and the query
+ *               q_h (576, same split):
+ *                 s_t = scale * sum_{d<576} q_h[d] r_t[d],
+ *                 w_t = exp(s_t - max s) / sum_t' exp(s_t' - max s),
+ *                 out_h[d] = sum_t w_t r_t[d] for d < 512 (the latent part
+ *                 is the value), lse_h = max s + log(sum exp(s - max s)),
+ *               all in fp64; a list with no token gives out 0, lse -inf.
+ *               scale is the caller's softmax scale.
  */
 #include <math.h>
 #include <stdint.h>
@@ -457,6 +471,56 @@ int32_t oracle_step_many(oracle_unit** units, int32_t n, const uint16_t* queries
     }
   }
   return rc;
+}
+
+/*
+ * R13: sparse attention of one position over rows of the main-KV history.
+ * rows: [tmax][row_elems] bf16 (row_elems >= 576); tok: [k] tokens of the
+ * position's top-k list (< 0: pad, skipped); q: [n_heads][576] bf16.
+ * out: [n_heads][512] fp64; lse: [n_heads] fp64.  Plain two-pass softmax.
+ */
+void oracle_attend_rows(const uint16_t* rows, int32_t row_elems, int64_t n_rows, const int32_t* tok,
+                        int32_t k, const uint16_t* q, int32_t n_heads, double scale, double* out,
+                        double* lse) {
+  double* s = (double*)malloc((size_t)(k > 0 ? k : 1) * sizeof(double));
+  for (int32_t h = 0; h < n_heads; ++h) {
+    const uint16_t* qh = q + (size_t)h * 576;
+    double mx = -INFINITY;
+    for (int32_t i = 0; i < k; ++i) {
+      s[i] = -INFINITY;
+      if (tok[i] < 0 || tok[i] >= n_rows) continue;
+      const uint16_t* r = rows + (size_t)tok[i] * row_elems;
+      double dot = 0.0;
+      for (int d = 0; d < 576; ++d) dot += (double)bf16_value(qh[d]) * (double)bf16_value(r[d]);
+      s[i] = scale * dot;
+      if (s[i] > mx) mx = s[i];
+    }
+    double* o = out + (size_t)h * 512;
+    for (int d = 0; d < 512; ++d) o[d] = 0.0;
+    if (mx == -INFINITY) {
+      lse[h] = -INFINITY;
+      continue;
+    }
+    double sum = 0.0;
+    for (int32_t i = 0; i < k; ++i)
+      if (s[i] != -INFINITY) sum += exp(s[i] - mx);
+    for (int32_t i = 0; i < k; ++i) {
+      if (s[i] == -INFINITY) continue;
+      const double w = exp(s[i] - mx) / sum;
+      const uint16_t* r = rows + (size_t)tok[i] * row_elems;
+      for (int d = 0; d < 512; ++d) o[d] += w * (double)bf16_value(r[d]);
+    }
+    lse[h] = mx + log(sum);
+  }
+  free(s);
+}
+
+/* R13 over the unit's own history (kept when the unit was made with rows). */
+int32_t oracle_attend(const oracle_unit* u, const int32_t* tok, int32_t k, const uint16_t* q,
+                      int32_t n_heads, double scale, double* out, double* lse) {
+  if (!u->rows || u->row_elems < 576) return ORACLE_EINVAL;
+  oracle_attend_rows(u->rows, u->row_elems, u->len, tok, k, q, n_heads, scale, out, lse);
+  return ORACLE_OK;
 }
 
 int32_t oracle_threads(void) {

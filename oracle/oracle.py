@@ -75,6 +75,11 @@ def lib():
             L.oracle_scores.argtypes = [vp, vp, i64, vp]
             L.oracle_threads.restype = i32
             L.oracle_threads.argtypes = []
+            f64 = ctypes.c_double
+            L.oracle_attend_rows.restype = None
+            L.oracle_attend_rows.argtypes = [vp, i32, i64, vp, i32, vp, i32, f64, vp, vp]
+            L.oracle_attend.restype = i32
+            L.oracle_attend.argtypes = [vp, vp, i32, vp, i32, f64, vp, vp]
             L.oracle_len.restype = i64
             L.oracle_len.argtypes = [vp]
             L.oracle_stamp.restype = ctypes.c_uint32
@@ -242,6 +247,19 @@ class OracleUnit:
         return self._view("oracle_rows", self.max_tokens * self.row_elems, np.uint16).reshape(
             self.max_tokens, self.row_elems)
 
+    def attend(self, tokens, queries, scale):
+        """R13 attention of one position: tokens [k] int32 (< 0 = pad), queries [H][576]
+        bf16 bits.  Returns (out [H][512] float64, lse [H] float64)."""
+        tokens = np.ascontiguousarray(tokens, dtype=np.int32)
+        queries = np.ascontiguousarray(queries, dtype=np.uint16)
+        H = queries.shape[0]
+        out = np.zeros((H, 512), dtype=np.float64)
+        lse = np.zeros(H, dtype=np.float64)
+        rc = lib().oracle_attend(self.h, tokens.ctypes.data, len(tokens), queries.ctypes.data, H,
+                                 float(scale), out.ctypes.data, lse.ctypes.data)
+        assert rc == OK, rc
+        return out, lse
+
 
 def step_many(units, queries):
     """One step of many units in parallel (OpenMP).  queries: [n][P][128] uint16."""
@@ -264,6 +282,21 @@ def step_many(units, queries):
     if rc != OK:
         raise RuntimeError("oracle_step_many failed: %d" % rc)
     return tok, sc, pay, sl, st, nm
+
+
+def attend_rows(rows, tokens, queries, scale):
+    """R13 attention over explicit rows: rows [n][>=576] bf16 bits, tokens [k] int32
+    (< 0 = pad), queries [H][576] bf16 bits.  Returns (out [H][512], lse [H]) in float64."""
+    rows = np.ascontiguousarray(rows, dtype=np.uint16)
+    tokens = np.ascontiguousarray(tokens, dtype=np.int32)
+    queries = np.ascontiguousarray(queries, dtype=np.uint16)
+    H = queries.shape[0]
+    out = np.zeros((H, 512), dtype=np.float64)
+    lse = np.zeros(H, dtype=np.float64)
+    lib().oracle_attend_rows(rows.ctypes.data, rows.shape[1], rows.shape[0], tokens.ctypes.data,
+                             len(tokens), queries.ctypes.data, H, float(scale), out.ctypes.data,
+                             lse.ctypes.data)
+    return out, lse
 
 
 def threads():
