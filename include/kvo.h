@@ -259,7 +259,8 @@ int kvo_reset(kvo_handle* h, const int32_t* units, int32_t n_units, int64_t keep
 #define KVO_PROF_RESCORE 7   /* rescoring pass of units whose speculative threshold was too high */
 #define KVO_PROF_RESELECT 8
 #define KVO_PROF_FUSED 9     /* the fused step launch (KVO_OPT_FUSED) */
-#define KVO_PROF_KINDS 10
+#define KVO_PROF_ATTEND 10   /* kvo_attend */
+#define KVO_PROF_KINDS 11
 int kvo_profile_read(kvo_handle* h, double* ms, uint64_t* launches, int32_t n_kinds);
 
 /* kvo_set_option: KVO_OPT_* above.  KVO_EINVAL on unknown key or value. */
@@ -301,6 +302,37 @@ int kvo_select_noalloc(const void* keys, int64_t unit_stride, const int32_t* cac
                        const int64_t* lengths, int32_t n_units, int32_t n_pos, int32_t k,
                        const void* queries, int32_t* tokens, float* scores, int32_t* payload,
                        void* stream);
+
+/*
+ * kvo_attend ([LS] Decode step 7: sparse attention consumes the resident
+ * K/V; the pages name an SFA/MLA model without its formula, so this is the
+ * absorbed latent attention of the DeepSeek family, reading R13 of the
+ * oracle): for each listed unit u, position p and head h, over the hot rows
+ * named by that position's top-k slots (slot < 0 or >= hot_capacity: pad,
+ * skipped), with a row = [latent 512 | rope key 64] and the query of the same
+ * split,
+ *   s_i = scale * q[u][p][h] . row_i,
+ *   out[u][p][h][d] = sum_i softmax(s)_i * row_i[d]  (d < 512),
+ *   lse[u][p][h] = log sum_i exp(s_i)  (-inf when the list has no row).
+ * Run it after kvo_step on the same stream with that step's topk_slots: the
+ * hot rows it reads are the ones the step made resident.
+ *   units      : host array [n_units] (as kvo_step), or NULL = all units.
+ *   queries    : device bf16 [n_units][P][n_heads][576], 16-byte aligned.
+ *   n_heads    : a multiple of 128 (one CTA pair per 128 heads).
+ *   scale      : softmax scale (e.g. 1/sqrt(192)), finite.
+ *   topk_slots : device int32 [n_units][P][k], as written by kvo_step.
+ *   out        : device bf16 [n_units][P][n_heads][512] (written), 16-byte aligned.
+ *   lse        : device float [n_units][P][n_heads] (written), nullable.
+ * Precision: scores accumulate in fp32 on the tensor cores; softmax weights
+ * are rounded to bf16 before the value product and normalised by the sum of
+ * the rounded weights; out is rounded to bf16.  Requires row_elems == 576.
+ * Errors (nothing launched): KVO_EINVAL (NULL or misaligned pointer, n_heads,
+ * scale, row size), KVO_ERANGE (unit id).  A bounded device wait that expires
+ * sets the error word read by kvo_get_stats (the output is then unspecified).
+ */
+int kvo_attend(kvo_handle* h, const int32_t* units, int32_t n_units, const void* queries,
+               int32_t n_heads, float scale, const int32_t* topk_slots, void* out, float* lse,
+               void* stream);
 
 /* kvo_last_error: message of the last failing call on this thread ("" if none). */
 const char* kvo_last_error(void);

@@ -1070,6 +1070,40 @@ int kvo_reset(kvo_handle* h, const int32_t* units, int32_t n_units, int64_t keep
   return KVO_OK;
 }
 
+int kvo_attend(kvo_handle* h, const int32_t* units, int32_t n_units, const void* queries, int32_t n_heads,
+               float scale, const int32_t* topk_slots, void* out, float* lse, void* stream) {
+  if (!h) return fail(KVO_EINVAL, "handle is NULL");
+  if (!queries || !topk_slots || !out) return fail(KVO_EINVAL, "NULL argument");
+  if (!aligned16(queries) || !aligned16(out)) return fail(KVO_EINVAL, "queries or out not 16-byte aligned");
+  if (h->R != 576) return fail(KVO_EINVAL, "attention needs 576-element rows");
+  if (n_heads < 128 || n_heads % 128 != 0 || n_heads > 8192)
+    return fail(KVO_EINVAL, "n_heads must be a positive multiple of 128 (at most 8192)");
+  if (!(scale == scale) || scale > 3.0e38f || scale < -3.0e38f) return fail(KVO_EINVAL, "scale is not finite");
+  DeviceGuard guard(h->device);
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const int32_t* du = nullptr;
+  int rc = resolve_units(h, units, n_units, s, &du);
+  if (rc != KVO_OK) return rc;
+  kvo::AttendArgs a{};
+  a.units = du;
+  a.slots = topk_slots;
+  a.q = static_cast<const uint16_t*>(queries);
+  a.hot = h->hot;
+  a.out = static_cast<uint16_t*>(out);
+  a.lse = lse;
+  a.n = n_units;
+  a.P = h->P;
+  a.k = h->k;
+  a.H = n_heads;
+  a.C = h->C;
+  a.scale_log2 = scale * 1.4426950408889634f;
+  a.err = h->err;
+  a.wait_ns = h->wait_ns;
+  cudaError_t e = timed(h, KVO_PROF_ATTEND, s, [&] { return kvo::launch_attend(a, s); });
+  if (e != cudaSuccess) return cuda_fail(e, "attention launch");
+  return KVO_OK;
+}
+
 int kvo_profile_read(kvo_handle* h, double* ms, uint64_t* launches, int32_t n_kinds) {
   if (!h || !ms || !launches || n_kinds < 0) return fail(KVO_EINVAL, "NULL argument");
   DeviceGuard guard(h->device);

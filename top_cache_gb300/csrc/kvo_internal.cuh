@@ -266,6 +266,20 @@ struct GatherArgs {
   uint64_t wait_ns;
 };
 
+// Sparse attention over the hot buffer (kvo_attend.cu).
+struct AttendArgs {
+  const int32_t* units;   // [n] unit ids
+  const int32_t* slots;   // [n][P][k] hot slots of each position's top-k list (< 0: pad)
+  const uint16_t* q;      // [n][P][H][576] bf16 queries
+  const uint16_t* hot;    // [U][C][576] bf16 hot rows
+  uint16_t* out;          // [n][P][H][512] bf16
+  float* lse;             // [n][P][H] or null
+  int n, P, k, H, C;
+  float scale_log2;       // softmax scale * log2(e)
+  uint32_t* err;
+  uint64_t wait_ns;
+};
+
 struct AppendArgs {
   const int32_t* units;
   int32_t n, n_tok, row_elems;
@@ -345,6 +359,8 @@ cudaError_t launch_select(const SelectArgs& a, cudaStream_t s);
 cudaError_t launch_residency(const ResidencyArgs& a, cudaStream_t s);
 cudaError_t launch_gather(const GatherArgs& a, int n_sm, cudaStream_t s);
 cudaError_t launch_append(const AppendArgs& a, cudaStream_t s);
+cudaError_t launch_attend(const AttendArgs& a, cudaStream_t s);
+size_t attend_smem_bytes();
 cudaError_t launch_reset(const ResetArgs& a, cudaStream_t s);
 cudaError_t launch_order_init(int32_t* order, int32_t* par, int U, int C, cudaStream_t s);
 cudaError_t launch_set_len(int32_t* len, int32_t unit, int32_t value, cudaStream_t s);

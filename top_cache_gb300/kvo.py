@@ -34,7 +34,7 @@ KVO_OPT_GATHER_CTAS = 8
 KVO_OPT_PIECE_TOKENS = 9
 KVO_OPT_HOST_HUGE_PAGE = 10
 PROF_KINDS = ("append", "plan", "score", "select", "residency", "gather", "reset", "rescore",
-              "reselect", "fused")
+              "reselect", "fused", "attend")
 KVO_IDX_BF16 = 0
 KVO_IDX_INT8 = 1
 KVO_GATHER_LDG = 0
@@ -43,7 +43,7 @@ KVO_GATHER_BULK = 1
 EXPORTED = ("kvo_create", "kvo_destroy", "kvo_host_rows", "kvo_prefill", "kvo_append", "kvo_step",
             "kvo_select_workspace_size", "kvo_select", "kvo_reset", "kvo_profile_read",
             "kvo_set_option", "kvo_get_option", "kvo_get_stats", "kvo_export_state", "kvo_select_noalloc",
-            "kvo_last_error")
+            "kvo_attend", "kvo_last_error")
 
 
 class KvoConfig(ctypes.Structure):
@@ -103,6 +103,8 @@ def lib():
                                      ctypes.c_size_t, vp]
             L.kvo_select_noalloc.restype = ctypes.c_int
             L.kvo_select_noalloc.argtypes = [vp, i64, vp, vp, i32, i32, i32, vp, vp, vp, vp, vp]
+            L.kvo_attend.restype = ctypes.c_int
+            L.kvo_attend.argtypes = [vp, vp, i32, vp, i32, ctypes.c_float, vp, vp, vp, vp]
             L.kvo_reset.restype = ctypes.c_int
             L.kvo_reset.argtypes = [vp, vp, i32, i64, vp]
             L.kvo_profile_read.restype = ctypes.c_int
@@ -191,6 +193,12 @@ def kvo_step(h, units, n_units, queries, topk_tokens, topk_slots, topk_scores, t
     return _check(lib().kvo_step(h, up, n_units, _ptr(queries), _ptr(topk_tokens),
                                  _ptr(topk_slots), _ptr(topk_scores), _ptr(topk_payload),
                                  _ptr(unit_status), _stream(stream)))
+
+
+def kvo_attend(h, units, n_units, queries, n_heads, scale, topk_slots, out, lse=None, stream=None):
+    arr, up = _units(units)
+    return _check(lib().kvo_attend(h, up, n_units, _ptr(queries), n_heads, float(scale),
+                                   _ptr(topk_slots), _ptr(out), _ptr(lse), _stream(stream)))
 
 
 def kvo_select_workspace_size(n_units, n_pos, k, device=0):
@@ -311,6 +319,15 @@ class Kvo:
         tok, sl, sc, pay, st = out
         kvo_step(self.h, units, n, queries, tok, sl, sc, pay, st, stream)
         return out
+
+    def attend(self, queries, scale, out, lse=None, slots=None, units=None, stream=None):
+        """Sparse attention of the last step's lists: queries [n][P][H][576] bf16 device,
+        out [n][P][H][512] bf16 device, lse [n][P][H] float32 device or None."""
+        n = self.U if units is None else len(units)
+        if slots is None:
+            slots = self.slots[:n]
+        H = int(queries.shape[-2])
+        return kvo_attend(self.h, units, n, queries, H, scale, slots, out, lse, stream)
 
     def reset(self, keep_tokens, units=None, stream=None):
         n_units = self.U if units is None else len(units)

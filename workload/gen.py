@@ -10,6 +10,7 @@ KIND_KEYS = 1
 KIND_ROWS = 2
 KIND_QINIT = 3
 KIND_QNOISE = 4
+KIND_ATTN_Q = 5  # attention queries (one 576-element row per position and head)
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 _SRC = os.path.join(_HERE, "gen.c")
@@ -111,6 +112,13 @@ def unit_queries(seed, units_rl, a, n_steps, n_pos, distinct=False, dim=128):
             w = query_walk(seed, r, l, 0, a, n_steps, dim)
             out[:, i, :, :] = w[:, None, :]
     return out
+
+
+def attention_queries(seed, units_rl, step, n_pos, n_heads, width=576):
+    """bf16 (uint16) [n_units][n_pos][n_heads][width] attention queries of one decode step,
+    N(0,1): rows step*n_pos*n_heads .. of the KIND_ATTN_Q stream of each unit."""
+    q = token_rows(seed, KIND_ATTN_Q, units_rl, step * n_pos * n_heads, n_pos * n_heads, width)
+    return q.reshape(len(units_rl), n_pos, n_heads, width)
 
 
 def bf16_to_f32(a):
