@@ -87,6 +87,18 @@ def load_peaks():
         return FALLBACK_HBM_GBS, "fallback"
 
 
+FALLBACK_BF16_TFLOPS = 1900.0
+
+
+def load_bf16_peak():
+    """Dense bf16 tensor peak (TFLOP/s) for a kernel timed on its own: the burst figure."""
+    try:
+        with open(PEAKS_FILE) as f:
+            return float(json.load(f)["bf16_tflops"]), "measured"
+    except Exception:
+        return FALLBACK_BF16_TFLOPS, "fallback"
+
+
 def kernel_source_hash():
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "top_cache_gb300", "csrc")
@@ -269,6 +281,61 @@ class Sequence:
         return p
 
 
+# --------------------------------------------------------------------------- attention
+def run_attention(args, kv, wl, units, device, torch):
+    """Time kvo_attend (decode step 7) on the slots of the last step, on its own.
+
+    Algorithmic work per (unit, position): 2 * H * n * (576 + 512) FLOPs for n listed rows
+    (scores over the full row, values over the latent part).  The kernel computes the
+    scores once per half of the value columns, so it executes 2 * H * n * (2 * 576 + 512)."""
+    import numpy as np
+    import workload as W
+    H = args.attend_heads
+    P, k = wl.n_pos, wl.topk
+    U = len(units)
+    q = W.attention_queries(wl.seed, units, 0, P, H)
+    qd = torch.from_numpy(q.view(np.int16)).to(device)
+    del q
+    out = torch.empty((U, P, H, 512), dtype=torch.bfloat16, device=device)
+    lse = torch.empty((U, P, H), dtype=torch.float32, device=device)
+    slots = kv.slots[:U]
+    n_rows = int(((slots >= 0) & (slots < wl.hot_capacity)).sum().item())
+    scale = 1.0 / (192.0 ** 0.5)
+    stream = torch.cuda.current_stream(device)
+    for _ in range(3):
+        kv.attend(qd, scale, out, lse)
+    torch.cuda.synchronize(device)
+    n_launch = args.attend_launches
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(2 * n_launch)]
+    for i in range(n_launch):
+        ev[2 * i].record(stream)
+        kv.attend(qd, scale, out, lse)
+        ev[2 * i + 1].record(stream)
+    torch.cuda.synchronize(device)
+    st = kv.stats()
+    ms = [ev[2 * i].elapsed_time(ev[2 * i + 1]) for i in range(n_launch)]
+    t = statistics.mean(ms)
+    flops = 2.0 * H * n_rows * (576 + 512)
+    flops_exec = 2.0 * H * n_rows * (2 * 576 + 512)
+    peak, src = load_bf16_peak()
+    achieved = flops / (t * 1e-3) / 1e12
+    ctas = U * P * (H // 128) * 2
+    rows_bytes = ctas * k * 1152 + U * P * H * 576 * 2
+    return {
+        "kernel": "attend_kernel", "heads": H, "scale": round(scale, 6), "launches": n_launch,
+        "ms_per_launch": round(t, 4), "ms_min": round(min(ms), 4),
+        "selections_per_s": round(U / (t * 1e-3), 1),
+        "roofline": {"bound": "tensor", "achieved": round(achieved, 1), "peak": peak,
+                     "unit": "TFLOP/s", "frac": round(achieved / peak, 4),
+                     "peak_source": "%s bf16 dense (burst)" % src, "traffic": None},
+        "flops_per_launch": flops, "executed_tflops": round(flops_exec / (t * 1e-3) / 1e12, 1),
+        "rows_listed": n_rows, "l2_to_sm_bytes_per_launch": rows_bytes,
+        "l2": "inputs larger than L2: %.2f GB of listed hot rows and queries per launch"
+              % (rows_bytes / 1e9),
+        "timeouts": st["timeouts"],
+    }
+
+
 # --------------------------------------------------------------------------- GPU arm
 def run_kvo(args, log):
     import numpy as np
@@ -412,6 +479,11 @@ def run_kvo(args, log):
     cold = [m for m, p in zip(step_ms, positions) if p == 0]
     warm = [m for m, p in zip(step_ms, positions) if p != 0]
 
+    # ---------------- sparse attention over the hot buffer (decode step 7), timed on its own
+    attention = None
+    if args.attend_heads > 0 and wl.row_elems == 576:
+        attention = run_attention(args, kv, wl, units, device, torch)
+
     # ---------------- end to end through the public API with host buffers
     e2e = None
     if not args.no_e2e:
@@ -462,6 +534,7 @@ def run_kvo(args, log):
         "rescored_units_per_step": (st1["rescored"] - st0["rescored"]) / n_steps,
         "clocks": clocks,
         "e2e": e2e,
+        "attention": attention,
         "gpu_launches": launches,
         "cpu_baseline": cpu,
     }
@@ -670,6 +743,9 @@ def main(argv=None):
     ap.add_argument("--speculate", type=int, default=None,
                     help="speculative threshold margin in permille (library default 900)")
     ap.add_argument("--piece-tokens", type=int, default=None, help="fused step: tokens per piece")
+    ap.add_argument("--attend-heads", type=int, default=128,
+                    help="heads of the timed sparse attention (multiple of 128; 0 = skip it)")
+    ap.add_argument("--attend-launches", type=int, default=20)
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-units", type=int, default=32)

@@ -37,7 +37,8 @@ namespace {
 constexpr int kRow = 576;                 // elements per hot row
 constexpr int kVal = 512;                 // value (latent) elements
 constexpr int kM = 128;                   // heads per CTA: M of both MMAs
-constexpr int kBlk = 32;                  // rows per block: N of S, K of P V
+constexpr int kBlk = 16;                  // rows per block: N of S, K of P V
+constexpr int kStages = 4;                // row blocks in flight
 constexpr int kSlabs = kRow / 64;         // 128-byte slabs of a row
 constexpr int kHalfCols = kVal / 2;       // value columns per CTA: N of P V
 constexpr int kAttThreads = 256;
@@ -47,14 +48,16 @@ constexpr uint32_t kKSlab = kBlk * 128;   // one slab of a row block
 constexpr uint32_t kKStage = kSlabs * kKSlab;
 constexpr uint32_t kQOff = 0;
 constexpr uint32_t kKOff = kSlabs * kQSlab;
-constexpr uint32_t kBarOff = kKOff + 2 * kKStage;
-constexpr uint32_t kAttSmem = kBarOff + 128 + 1024;  // barriers, flags, 1 KB alignment slack
+constexpr uint32_t kBarOff = kKOff + kStages * kKStage;
+constexpr uint32_t kAttSmem = kBarOff + 256 + 1024;  // barriers, flags, 1 KB alignment slack
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kColO = 0;    // O: 256 fp32 columns
-constexpr uint32_t kColS = 256;  // S[2]: 32 fp32 columns each
-constexpr uint32_t kColP = 320;  // P[2]: 16 columns of bf16 pairs each
+constexpr uint32_t kColS = 256;  // S[2]: kBlk fp32 columns each
+constexpr uint32_t kColP = 256 + 2 * kBlk;  // P[2]: kBlk / 2 columns of bf16 pairs each
 constexpr float kRescaleLog2 = 8.f;
 static_assert(kAttSmem <= 232448, "shared memory of one CTA");
+static_assert(kBlk == 16, "the softmax moves one 16-column S tile and one 8-column P tile per block");
+static_assert(kStages - 2 <= 2, "cp_async_wait_n covers up to kStages - 2 younger groups");
 
 // Shared-memory matrix descriptor, 128-byte swizzle (start, leading and stride
 // byte offsets in 16-byte units; descriptor version 1).
@@ -108,6 +111,24 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32]) {
 #pragma unroll
   for (int c = 0; c < 32; ++c) v[c] = __uint_as_float(r[c]);
 }
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, float (&v)[16]) {
+  uint32_t r[16];
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, "
+      "%12, %13, %14, %15}, [%16];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
+        "=r"(r[14]), "=r"(r[15])
+      : "r"(taddr)
+      : "memory");
+#pragma unroll
+  for (int c = 0; c < 16; ++c) v[c] = __uint_as_float(r[c]);
+}
+__device__ __forceinline__ void tmem_st8(uint32_t taddr, const uint32_t (&r)[8]) {
+  asm volatile("tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"r"(taddr),
+               "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7])
+               : "memory");
+}
 __device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32]) {
   asm volatile(
       "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, "
@@ -137,6 +158,12 @@ template <int N>
 __device__ __forceinline__ void cp_async_wait() {
   asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
 }
+// wait until at most n committed groups are pending (n clamped to 0..2)
+__device__ __forceinline__ void cp_async_wait_n(int n) {
+  if (n <= 0) cp_async_wait<0>();
+  else if (n == 1) cp_async_wait<1>();
+  else cp_async_wait<2>();
+}
 // 16-byte chunk c (0..7) of row r in a 128-byte-swizzled slab (1 KB aligned).
 __device__ __forceinline__ uint32_t swz(uint32_t slab, int r, int c) {
   return slab + (uint32_t)r * 128u + ((uint32_t)(c ^ (r & 7)) << 4);
@@ -149,16 +176,16 @@ __global__ void __launch_bounds__(kAttThreads, 1) attend_kernel(AttendArgs a) {
   uint8_t* smem = smem_raw + pad;
   const uint32_t sb = raw + pad;
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kBarOff);
-  uint64_t* q_full = bars;        // producers: query tile in place
-  uint64_t* k_full = bars + 1;    // [2] producers: row block in place
-  uint64_t* k_empty = bars + 3;   // [2] MMA: block's P V done, stage free
-  uint64_t* s_full = bars + 5;    // [2] MMA: S of a block ready
-  uint64_t* s_empty = bars + 7;   // [2] softmax: S read
-  uint64_t* p_full = bars + 9;    // [2] softmax: P of a block in TMEM
-  uint64_t* pv_done = bars + 11;  // MMA: one more P V done
-  uint64_t* o_final = bars + 12;  // MMA: the last P V done
-  uint64_t* fin = bars + 13;      // MMA: everything issued is done
-  volatile uint32_t* tmem_slot = reinterpret_cast<volatile uint32_t*>(smem + kBarOff + 112);
+  uint64_t* q_full = bars;                       // producers: query tile in place
+  uint64_t* k_full = bars + 1;                   // [kStages] producers: row block in place
+  uint64_t* k_empty = k_full + kStages;          // [kStages] MMA: block's P V done, stage free
+  uint64_t* s_full = k_empty + kStages;          // [2] MMA: S of a block ready
+  uint64_t* s_empty = s_full + 2;                // [2] softmax: S read
+  uint64_t* p_full = s_empty + 2;                // [2] softmax: P of a block in TMEM
+  uint64_t* pv_done = p_full + 2;                // MMA: one more P V done
+  uint64_t* o_final = pv_done + 1;               // MMA: the last P V done
+  uint64_t* fin = o_final + 1;                   // MMA: everything issued is done
+  volatile uint32_t* tmem_slot = reinterpret_cast<volatile uint32_t*>(fin + 1);
   volatile uint32_t* abort_flag = tmem_slot + 1;
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -181,9 +208,11 @@ __global__ void __launch_bounds__(kAttThreads, 1) attend_kernel(AttendArgs a) {
 
   if (tid == 0) {
     mbar_init(q_full, kProducers);
-    for (int s = 0; s < 2; ++s) {
+    for (int s = 0; s < kStages; ++s) {
       mbar_init(&k_full[s], kProducers);
       mbar_init(&k_empty[s], 1);
+    }
+    for (int s = 0; s < 2; ++s) {
       mbar_init(&s_full[s], 1);
       mbar_init(&s_empty[s], 128);
       mbar_init(&p_full[s], 128);
@@ -207,7 +236,7 @@ __global__ void __launch_bounds__(kAttThreads, 1) attend_kernel(AttendArgs a) {
   const uint32_t tmem = *tmem_slot;
 
   if (warp < 2) {
-    // ---- copies: query tile, then row blocks (16 rows per warp) ----
+    // ---- copies: query tile, then row blocks (kBlk / 2 rows per warp) ----
     const uint8_t* qsrc = reinterpret_cast<const uint8_t*>(a.q) + qrow0 * (kRow * 2);
     for (int idx = tid; idx < kM * 72; idx += kProducers) {
       const int r = idx / 72, g = idx - r * 72;
@@ -215,37 +244,46 @@ __global__ void __launch_bounds__(kAttThreads, 1) attend_kernel(AttendArgs a) {
     }
     cp_async_commit();
     const uint8_t* ubase = reinterpret_cast<const uint8_t*>(a.hot) + (size_t)u * a.C * (kRow * 2);
-    auto gather = [&](int j) {
-      const uint32_t st = sb + kKOff + (uint32_t)(j & 1) * kKStage;
-      const int r0 = warp * 16;
-      const int r = j * kBlk + r0 + (lane & 15);
-      int32_t slot = r < a.k ? __ldg(a.slots + list + r) : -1;
+    // slot of row (lane & 15) of this warp's 16 rows of block j; loaded one
+    // block ahead so that its latency overlaps the wait for the previous block
+    auto load_slot = [&](int j) -> int32_t {
+      const int r = j * kBlk + warp * (kBlk / 2) + (lane % (kBlk / 2));
+      return j < nb && r < a.k ? __ldg(a.slots + list + r) : -1;
+    };
+    auto gather = [&](int j, int32_t slot) {
+      const uint32_t st = sb + kKOff + (uint32_t)(j % kStages) * kKStage;
+      const int r0 = warp * (kBlk / 2);
       if (slot < 0 || slot >= a.C) slot = 0;  // a pad reads a valid row; the softmax drops it
 #pragma unroll 4
-      for (int x = 0; x < 16; ++x) {
+      for (int x = 0; x < kBlk / 2; ++x) {
         const uint8_t* src = ubase + (size_t)__shfl_sync(kFull, slot, x) * (kRow * 2);
         const int row = r0 + x;
         for (int g = lane; g < 72; g += 32) cp_async16(swz(st + (uint32_t)(g >> 3) * kKSlab, row, g & 7), src + g * 16);
       }
       cp_async_commit();
     };
-    gather(0);
+    gather(0, load_slot(0));
+    int32_t slot_next = load_slot(1);
     // Block j is announced as soon as its copies have landed; only then does
-    // the warp wait for the other stage (P V of block j-1, which the MMA
-    // issues after it has seen block j) and start copying block j+1.
+    // the warp wait for the stage of block j+1 (freed by the P V of block
+    // j+1-kStages, which the MMA issues after it has seen block j+2-kStages)
+    // and start copying block j+1.
     for (int j = 0; j < nb; ++j) {
       cp_async_wait<0>();
       fence_proxy_async_smem();  // the tensor cores read what cp.async wrote
       if (j == 0) mbar_arrive(q_full);
-      mbar_arrive(&k_full[j & 1]);
+      mbar_arrive(&k_full[j % kStages]);
       if (j + 1 >= nb) break;
       if (__any_sync(kFull, *abort_flag != 0u)) break;  // warp-uniform: shuffles follow
-      const bool ok = __all_sync(kFull, j + 1 < 2 || mbar_wait(&k_empty[(j + 1) & 1], ((j - 1) >> 1) & 1, a.wait_ns));
+      // stage of block j+1 last held block j+1-kStages
+      const int jn = j + 1;
+      const bool ok = __all_sync(kFull, jn < kStages || mbar_wait(&k_empty[jn % kStages], ((jn / kStages) - 1) & 1, a.wait_ns));
       if (!ok) {
         fail();
         break;
       }
-      gather(j + 1);
+      gather(j + 1, slot_next);
+      slot_next = load_slot(j + 2);
     }
     cp_async_wait<0>();
   } else if (warp == 2) {
@@ -254,18 +292,19 @@ __global__ void __launch_bounds__(kAttThreads, 1) attend_kernel(AttendArgs a) {
       constexpr uint32_t kIdQK = idesc_bf16(kM, kBlk, false);
       constexpr uint32_t kIdPV = idesc_bf16(kM, kHalfCols, true);
       bool ok = mbar_wait(q_full, 0, a.wait_ns);
+      const uint64_t qdesc = sdesc(sb + kQOff, 16, 1024);
       auto issue_pv = [&](int jj) -> bool {
         const int sp = jj & 1;
         if (!mbar_wait(&p_full[sp], (jj >> 1) & 1, a.wait_ns)) return false;
         tc_after();
         // V = this CTA's 4 value slabs of the block: MN-major, 64 columns per
         // slab (leading offset = slab stride), 8-row groups 1 KB apart
-        const uint32_t vb = sb + kKOff + (uint32_t)sp * kKStage + (uint32_t)half * 4u * kKSlab;
+        const uint32_t vb = sb + kKOff + (uint32_t)(jj % kStages) * kKStage + (uint32_t)half * 4u * kKSlab;
 #pragma unroll
         for (int kk = 0; kk < kBlk / 16; ++kk)
-          mma_ts(tmem + kColO, tmem + kColP + (uint32_t)sp * 16u + (uint32_t)kk * 8u,
+          mma_ts(tmem + kColO, tmem + kColP + (uint32_t)sp * (kBlk / 2) + (uint32_t)kk * 8u,
                  sdesc(vb + (uint32_t)kk * 16u * 128u, kKSlab, 1024), kIdPV, (jj > 0 || kk > 0) ? 1u : 0u);
-        mma_commit(&k_empty[sp]);
+        mma_commit(&k_empty[jj % kStages]);
         mma_commit(pv_done);
         return true;
       };
@@ -275,18 +314,23 @@ __global__ void __launch_bounds__(kAttThreads, 1) attend_kernel(AttendArgs a) {
           break;
         }
         const int st = j & 1;
-        if (!mbar_wait(&k_full[st], (j >> 1) & 1, a.wait_ns) ||
+        if (!mbar_wait(&k_full[j % kStages], (j / kStages) & 1, a.wait_ns) ||
             (j >= 2 && !mbar_wait(&s_empty[st], ((j - 2) >> 1) & 1, a.wait_ns))) {
           ok = false;
           break;
         }
         tc_after();
-        const uint32_t kb = sb + kKOff + (uint32_t)st * kKStage;
-#pragma unroll 4
-        for (int kk = 0; kk < kRow / 16; ++kk) {
-          const uint32_t o = (uint32_t)(kk >> 2), c = (uint32_t)(kk & 3) * 32u;
-          mma_ss(tmem + kColS + (uint32_t)st * kBlk, sdesc(sb + kQOff + o * kQSlab + c, 16, 1024),
-                 sdesc(kb + o * kKSlab + c, 16, 1024), kIdQK, kk > 0 ? 1u : 0u);
+        // base descriptors once per block; the 36 K-steps add compile-time
+        // offsets to the start-address field (shared addresses stay below
+        // 2^18, so the 14-bit field never carries)
+        const uint64_t kdesc = sdesc(sb + kKOff + (uint32_t)(j % kStages) * kKStage, 16, 1024);
+        const uint32_t dS = tmem + kColS + (uint32_t)st * kBlk;
+        mma_ss(dS, qdesc, kdesc, kIdQK, 0u);
+#pragma unroll
+        for (int kk = 1; kk < kRow / 16; ++kk) {
+          const uint32_t c = (uint32_t)(kk & 3) * 32u;
+          mma_ss(dS, qdesc + (((uint32_t)(kk >> 2) * kQSlab + c) >> 4),
+                 kdesc + (((uint32_t)(kk >> 2) * kKSlab + c) >> 4), kIdQK, 1u);
         }
         mma_commit(&s_full[st]);
         if (j >= 1 && !issue_pv(j - 1)) {
@@ -308,6 +352,8 @@ __global__ void __launch_bounds__(kAttThreads, 1) attend_kernel(AttendArgs a) {
     const float sl2 = a.scale_log2;
     float m_run = -INFINITY, l_run = 0.f;
     bool ok = true;
+    // slot of row `lane` of the next block, loaded a block ahead (validity mask)
+    int32_t sl_next = lane < kBlk && lane < a.k ? __ldg(a.slots + list + lane) : -1;
     for (int j = 0; j < nb; ++j) {
       if (__any_sync(kFull, *abort_flag != 0u)) {  // warp-uniform: TMEM access is warp-wide
         ok = false;
@@ -317,17 +363,17 @@ __global__ void __launch_bounds__(kAttThreads, 1) attend_kernel(AttendArgs a) {
       ok = __all_sync(kFull, mbar_wait(&s_full[st], (j >> 1) & 1, a.wait_ns));
       if (!ok) break;
       tc_after();
-      float v[32];
-      tmem_ld32(tmem + lane_addr + kColS + (uint32_t)st * kBlk, v);
+      float v[kBlk];
+      tmem_ld16(tmem + lane_addr + kColS + (uint32_t)st * kBlk, v);
       tmem_wait_ld();
       tc_before();
       mbar_arrive(&s_empty[st]);
-      const int r = j * kBlk + lane;
-      const int32_t sl = r < a.k ? __ldg(a.slots + list + r) : -1;
+      const int32_t sl = sl_next;
+      sl_next = lane < kBlk && (j + 1) * kBlk + lane < a.k ? __ldg(a.slots + list + (j + 1) * kBlk + lane) : -1;
       const uint32_t vm = __ballot_sync(kFull, sl >= 0 && sl < a.C);
       float mx = -INFINITY;
 #pragma unroll
-      for (int c = 0; c < 32; ++c) {
+      for (int c = 0; c < kBlk; ++c) {
         v[c] = ((vm >> c) & 1u) ? v[c] * sl2 : -INFINITY;
         mx = fmaxf(mx, v[c]);
       }
@@ -355,16 +401,16 @@ __global__ void __launch_bounds__(kAttThreads, 1) attend_kernel(AttendArgs a) {
         m_run = m_new;
       }
       const float mu = m_run == -INFINITY ? 0.f : m_run;
-      uint32_t pk[16];
+      uint32_t pk[kBlk / 2];
       float ls = 0.f;
 #pragma unroll
-      for (int c = 0; c < 16; ++c) {
+      for (int c = 0; c < kBlk / 2; ++c) {
         const __nv_bfloat162 b2 = __floats2bfloat162_rn(exp2f(v[2 * c] - mu), exp2f(v[2 * c + 1] - mu));
         ls += __low2float(b2) + __high2float(b2);
         pk[c] = *reinterpret_cast<const uint32_t*>(&b2);
       }
       l_run += ls;
-      tmem_st16(tmem + lane_addr + kColP + (uint32_t)st * 16u, pk);
+      tmem_st8(tmem + lane_addr + kColP + (uint32_t)st * (kBlk / 2), pk);
       tmem_wait_st();
       tc_before();
       mbar_arrive(&p_full[st]);
