@@ -214,6 +214,8 @@ def make_workload(args):
         kw["n_layers"] = args.layers
     if args.context:
         kw["context"] = args.context
+    if args.drift is not None:
+        kw["drift"] = args.drift
     if kw:
         wl = W.reduced(wl, **kw)
     return wl
@@ -730,6 +732,8 @@ def main(argv=None):
     ap.add_argument("--requests", type=int, default=0)
     ap.add_argument("--layers", type=int, default=0)
     ap.add_argument("--context", type=int, default=0)
+    ap.add_argument("--drift", type=float, default=None,
+                    help="query drift a of the workload (the sweep workload's points: 0, .5, .9, .99, 1)")
     ap.add_argument("--gather", choices=("ldg", "bulk"), default="ldg")
     ap.add_argument("--groups", type=int, default=1,
                     help="unit groups per step; miss-row copies overlap the next group's scoring")
