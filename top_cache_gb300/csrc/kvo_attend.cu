@@ -11,20 +11,27 @@
 //   lse_h = log sum_i exp(s_i).
 //
 // One CTA per (unit, position, group of 128 heads, half of the 512 value
-// columns); 256 threads:
-//   warps 0-1  copy the query tile once, then 32-row blocks of the hot rows
-//              named by the list, with 16-byte cp.async into the 128-byte
-//              swizzled layout the MMA reads (two stages);
+// columns); 256 threads.  The list is cut into blocks of 128 rows, so that
+// every S MMA has N = 128 (issuing a tcgen05.mma costs tens of cycles; a
+// smaller N leaves the tensor pipe idle).  The query tile (128 x 576 bf16,
+// 147 KB) stays in shared memory; a block's rows stream through a ring of
+// five 16 KB entries, one 64-column slab of the block each, this CTA's four
+// value slabs last:
+//   warps 0-1  copy the query tile, then every slab of every block with
+//              16-byte cp.async into the 128-byte-swizzled K-major layout the
+//              MMA reads;
 //   warp 2     holds 512 TMEM columns; lane 0 issues every tcgen05.mma:
-//              S = Q K^T (M 128, N 32, K 576, both operands K-major in shared
-//              memory) into one of two S buffers, then O += P V (M 128, N 256,
-//              K 32) with P read from TMEM and V (the same rows) MN-major;
+//              S = Q K^T (M 128, N 128, K 64 per slab) into one of two S
+//              buffers; once P is ready, O[:, 64v..] += P V_v (M 128, N 64,
+//              K 128) for each value slab v, P read from TMEM;
 //   warps 4-7  online softmax, one head (TMEM lane) per thread: S from TMEM,
 //              exp2 against a running maximum that moves only when it grows by
-//              more than 2^8 (O is then rescaled in TMEM), P rounded to bf16
-//              and written back to TMEM, l summed from the rounded weights so
-//              that out is their exact weighted mean; at the end O / l in bf16
-//              and lse.
+//              more than 2^8 (O is then rescaled in TMEM), P rounded to bf16 and
+//              written back over the S buffer it came from, l summed from the
+//              rounded weights so that out is their exact weighted mean; at the
+//              end O / l in bf16 and lse.
+// A ring entry is freed by the MMAs that read it last: the S MMAs for the five
+// slabs only the scores use, the P V MMAs for the value slabs.
 // Every mbarrier wait is bounded: on expiry the CTA sets kErrTimeout in the
 // error word, stops, waits for its own copies and MMAs and frees its TMEM.
 #include <cuda_bf16.h>
@@ -36,28 +43,26 @@ namespace {
 
 constexpr int kRow = 576;                 // elements per hot row
 constexpr int kVal = 512;                 // value (latent) elements
-constexpr int kM = 128;                   // heads per CTA: M of both MMAs
-constexpr int kBlk = 16;                  // rows per block: N of S, K of P V
-constexpr int kStages = 4;                // row blocks in flight
+constexpr int kM = 128;                   // heads per CTA: M of the MMAs
+constexpr int kBlk = 128;                 // rows per block: N of S, K of P V
 constexpr int kSlabs = kRow / 64;         // 128-byte slabs of a row
-constexpr int kHalfCols = kVal / 2;       // value columns per CTA: N of P V
+constexpr int kVSlabs = 4;                // value slabs of this CTA's half
+constexpr int kRing = 5;                  // ring entries (one slab of a block each)
+constexpr int kHalfCols = kVal / 2;       // value columns per CTA
 constexpr int kAttThreads = 256;
 constexpr int kProducers = 64;            // warps 0-1
 constexpr uint32_t kQSlab = kM * 128;     // one slab of the query tile
-constexpr uint32_t kKSlab = kBlk * 128;   // one slab of a row block
-constexpr uint32_t kKStage = kSlabs * kKSlab;
+constexpr uint32_t kEntry = kBlk * 128;   // one slab of a row block
 constexpr uint32_t kQOff = 0;
-constexpr uint32_t kKOff = kSlabs * kQSlab;
-constexpr uint32_t kBarOff = kKOff + kStages * kKStage;
+constexpr uint32_t kROff = kSlabs * kQSlab;
+constexpr uint32_t kBarOff = kROff + kRing * kEntry;
 constexpr uint32_t kAttSmem = kBarOff + 256 + 1024;  // barriers, flags, 1 KB alignment slack
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kColO = 0;    // O: 256 fp32 columns
-constexpr uint32_t kColS = 256;  // S[2]: kBlk fp32 columns each
-constexpr uint32_t kColP = 256 + 2 * kBlk;  // P[2]: kBlk / 2 columns of bf16 pairs each
+constexpr uint32_t kColS = 256;  // S[2]: 128 fp32 columns each; P (bf16 pairs) over its first 64
 constexpr float kRescaleLog2 = 8.f;
 static_assert(kAttSmem <= 232448, "shared memory of one CTA");
-static_assert(kBlk == 16, "the softmax moves one 16-column S tile and one 8-column P tile per block");
-static_assert(kStages - 2 <= 2, "cp_async_wait_n covers up to kStages - 2 younger groups");
+static_assert(kRing > kVSlabs, "the ring must hold a block's value slabs and one more entry");
 
 // Shared-memory matrix descriptor, 128-byte swizzle (start, leading and stride
 // byte offsets in 16-byte units; descriptor version 1).
@@ -111,24 +116,6 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32]) {
 #pragma unroll
   for (int c = 0; c < 32; ++c) v[c] = __uint_as_float(r[c]);
 }
-__device__ __forceinline__ void tmem_ld16(uint32_t taddr, float (&v)[16]) {
-  uint32_t r[16];
-  asm volatile(
-      "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, "
-      "%12, %13, %14, %15}, [%16];"
-      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
-        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
-        "=r"(r[14]), "=r"(r[15])
-      : "r"(taddr)
-      : "memory");
-#pragma unroll
-  for (int c = 0; c < 16; ++c) v[c] = __uint_as_float(r[c]);
-}
-__device__ __forceinline__ void tmem_st8(uint32_t taddr, const uint32_t (&r)[8]) {
-  asm volatile("tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"r"(taddr),
-               "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7])
-               : "memory");
-}
 __device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32]) {
   asm volatile(
       "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, "
@@ -158,15 +145,39 @@ template <int N>
 __device__ __forceinline__ void cp_async_wait() {
   asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
 }
-// wait until at most n committed groups are pending (n clamped to 0..2)
+// wait until at most n committed groups are pending (n clamped to 0..5)
 __device__ __forceinline__ void cp_async_wait_n(int n) {
-  if (n <= 0) cp_async_wait<0>();
-  else if (n == 1) cp_async_wait<1>();
-  else cp_async_wait<2>();
+  switch (n <= 0 ? 0 : n >= 5 ? 5 : n) {
+    case 0: cp_async_wait<0>(); break;
+    case 1: cp_async_wait<1>(); break;
+    case 2: cp_async_wait<2>(); break;
+    case 3: cp_async_wait<3>(); break;
+    case 4: cp_async_wait<4>(); break;
+    default: cp_async_wait<5>(); break;
+  }
+}
+// non-blocking test of a phase parity
+__device__ __forceinline__ bool mbar_test(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
 }
 // 16-byte chunk c (0..7) of row r in a 128-byte-swizzled slab (1 KB aligned).
 __device__ __forceinline__ uint32_t swz(uint32_t slab, int r, int c) {
   return slab + (uint32_t)r * 128u + ((uint32_t)(c ^ (r & 7)) << 4);
+}
+
+// Slab of the row that entry t (0..8) of a block carries: first the five the
+// scores alone use (the other half's value slabs, the rope key), then this
+// CTA's value slabs in column order.
+__device__ __forceinline__ int slab_of(int t, int half) {
+  return t < 4 ? 4 * (1 - half) + t : t == 4 ? 8 : 4 * half + (t - 5);
 }
 
 __global__ void __launch_bounds__(kAttThreads, 1) attend_kernel(AttendArgs a) {
@@ -176,15 +187,14 @@ __global__ void __launch_bounds__(kAttThreads, 1) attend_kernel(AttendArgs a) {
   uint8_t* smem = smem_raw + pad;
   const uint32_t sb = raw + pad;
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kBarOff);
-  uint64_t* q_full = bars;                       // producers: query tile in place
-  uint64_t* k_full = bars + 1;                   // [kStages] producers: row block in place
-  uint64_t* k_empty = k_full + kStages;          // [kStages] MMA: block's P V done, stage free
-  uint64_t* s_full = k_empty + kStages;          // [2] MMA: S of a block ready
-  uint64_t* s_empty = s_full + 2;                // [2] softmax: S read
-  uint64_t* p_full = s_empty + 2;                // [2] softmax: P of a block in TMEM
-  uint64_t* pv_done = p_full + 2;                // MMA: one more P V done
-  uint64_t* o_final = pv_done + 1;               // MMA: the last P V done
-  uint64_t* fin = o_final + 1;                   // MMA: everything issued is done
+  uint64_t* q_full = bars;            // copies: query tile in place
+  uint64_t* e_full = bars + 1;        // [kRing] copies: entry in place
+  uint64_t* e_free = e_full + kRing;  // [kRing] MMA: the entry's last reader done
+  uint64_t* s_full = e_free + kRing;  // [2] MMA: S of a block ready
+  uint64_t* p_full = s_full + 2;      // [2] softmax: P of a block in TMEM
+  uint64_t* pv_done = p_full + 2;     // MMA: one more block's P V done
+  uint64_t* o_final = pv_done + 1;    // MMA: the last P V done
+  uint64_t* fin = o_final + 1;        // MMA: everything issued is done
   volatile uint32_t* tmem_slot = reinterpret_cast<volatile uint32_t*>(fin + 1);
   volatile uint32_t* abort_flag = tmem_slot + 1;
 
@@ -201,6 +211,7 @@ __global__ void __launch_bounds__(kAttThreads, 1) attend_kernel(AttendArgs a) {
   const int64_t list = ((int64_t)i * a.P + p) * a.k;
   const int64_t qrow0 = ((int64_t)i * a.P + p) * a.H + (int64_t)hg * kM;
   const int nb = (a.k + kBlk - 1) / kBlk;
+  const int ne = nb * kSlabs;  // ring entries over the whole list
   auto fail = [&]() {
     atomicOr(a.err, kErrTimeout);
     *abort_flag = 1u;
@@ -208,13 +219,12 @@ __global__ void __launch_bounds__(kAttThreads, 1) attend_kernel(AttendArgs a) {
 
   if (tid == 0) {
     mbar_init(q_full, kProducers);
-    for (int s = 0; s < kStages; ++s) {
-      mbar_init(&k_full[s], kProducers);
-      mbar_init(&k_empty[s], 1);
+    for (int s = 0; s < kRing; ++s) {
+      mbar_init(&e_full[s], kProducers);
+      mbar_init(&e_free[s], 1);
     }
     for (int s = 0; s < 2; ++s) {
       mbar_init(&s_full[s], 1);
-      mbar_init(&s_empty[s], 128);
       mbar_init(&p_full[s], 128);
     }
     mbar_init(pv_done, 1);
@@ -236,7 +246,7 @@ __global__ void __launch_bounds__(kAttThreads, 1) attend_kernel(AttendArgs a) {
   const uint32_t tmem = *tmem_slot;
 
   if (warp < 2) {
-    // ---- copies: query tile, then row blocks (kBlk / 2 rows per warp) ----
+    // ---- copies: the query tile, then every slab of every block ----
     const uint8_t* qsrc = reinterpret_cast<const uint8_t*>(a.q) + qrow0 * (kRow * 2);
     for (int idx = tid; idx < kM * 72; idx += kProducers) {
       const int r = idx / 72, g = idx - r * 72;
@@ -244,101 +254,123 @@ __global__ void __launch_bounds__(kAttThreads, 1) attend_kernel(AttendArgs a) {
     }
     cp_async_commit();
     const uint8_t* ubase = reinterpret_cast<const uint8_t*>(a.hot) + (size_t)u * a.C * (kRow * 2);
-    // slot of row (lane & 15) of this warp's 16 rows of block j; loaded one
-    // block ahead so that its latency overlaps the wait for the previous block
-    auto load_slot = [&](int j) -> int32_t {
-      const int r = j * kBlk + warp * (kBlk / 2) + (lane % (kBlk / 2));
-      return j < nb && r < a.k ? __ldg(a.slots + list + r) : -1;
-    };
-    auto gather = [&](int j, int32_t slot) {
-      const uint32_t st = sb + kKOff + (uint32_t)(j % kStages) * kKStage;
-      const int r0 = warp * (kBlk / 2);
-      if (slot < 0 || slot >= a.C) slot = 0;  // a pad reads a valid row; the softmax drops it
-#pragma unroll 4
-      for (int x = 0; x < kBlk / 2; ++x) {
-        const uint8_t* src = ubase + (size_t)__shfl_sync(kFull, slot, x) * (kRow * 2);
-        const int row = r0 + x;
-        for (int g = lane; g < 72; g += 32) cp_async16(swz(st + (uint32_t)(g >> 3) * kKSlab, row, g & 7), src + g * 16);
+    // this thread copies chunk csub of rows rsub + 8m (m < 16) of every entry
+    const int rsub = tid >> 3, csub = tid & 7;
+    int32_t rs[kBlk / 8];
+    int rs_block = -1;
+    auto issue = [&](int e) {
+      const int j = e / kSlabs, t = e - j * kSlabs;
+      if (j != rs_block) {
+#pragma unroll
+        for (int m = 0; m < kBlk / 8; ++m) {
+          const int r = j * kBlk + rsub + 8 * m;
+          int32_t sl = r < a.k ? __ldg(a.slots + list + r) : -1;
+          rs[m] = sl < 0 || sl >= a.C ? 0 : sl;  // a pad reads a valid row; the softmax drops it
+        }
+        rs_block = j;
       }
+      const uint32_t dst = sb + kROff + (uint32_t)(e % kRing) * kEntry;
+      const int s = slab_of(t, half);
+#pragma unroll
+      for (int m = 0; m < kBlk / 8; ++m)
+        cp_async16(swz(dst, rsub + 8 * m, csub), ubase + (size_t)rs[m] * (kRow * 2) + s * 128 + csub * 16);
       cp_async_commit();
     };
-    gather(0, load_slot(0));
-    int32_t slot_next = load_slot(1);
-    // Block j is announced as soon as its copies have landed; only then does
-    // the warp wait for the stage of block j+1 (freed by the P V of block
-    // j+1-kStages, which the MMA issues after it has seen block j+2-kStages)
-    // and start copying block j+1.
-    for (int j = 0; j < nb; ++j) {
-      cp_async_wait<0>();
-      fence_proxy_async_smem();  // the tensor cores read what cp.async wrote
-      if (j == 0) mbar_arrive(q_full);
-      mbar_arrive(&k_full[j % kStages]);
-      if (j + 1 >= nb) break;
+    // Entries go out as soon as their ring slot is free; an entry is announced
+    // once its copies (and all older ones) have landed.  The warp blocks on a
+    // slot only when everything it issued has been announced, so it never
+    // holds back an entry the MMA needs in order to free that slot.
+    int issued = 0, arrived = 0;
+    while (arrived < ne) {
       if (__any_sync(kFull, *abort_flag != 0u)) break;  // warp-uniform: shuffles follow
-      // stage of block j+1 last held block j+1-kStages
-      const int jn = j + 1;
-      const bool ok = __all_sync(kFull, jn < kStages || mbar_wait(&k_empty[jn % kStages], ((jn / kStages) - 1) & 1, a.wait_ns));
-      if (!ok) {
-        fail();
-        break;
+      while (issued < ne && issued - arrived < kRing &&
+             (issued < kRing ||
+              __all_sync(kFull, mbar_test(&e_free[issued % kRing], ((issued / kRing) - 1) & 1)))) {
+        issue(issued);
+        ++issued;
       }
-      gather(j + 1, slot_next);
-      slot_next = load_slot(j + 2);
+      if (arrived < issued) {
+        cp_async_wait_n(issued - 1 - arrived);
+        fence_proxy_async_smem();  // the tensor cores read what cp.async wrote
+        if (arrived == 0) mbar_arrive(q_full);
+        mbar_arrive(&e_full[arrived % kRing]);
+        ++arrived;
+      } else {
+        const bool ok =
+            __all_sync(kFull, mbar_wait(&e_free[issued % kRing], ((issued / kRing) - 1) & 1, a.wait_ns));
+        if (!ok) {
+          fail();
+          break;
+        }
+      }
     }
     cp_async_wait<0>();
   } else if (warp == 2) {
     // ---- MMA issue (one thread) ----
     if (lane == 0) {
       constexpr uint32_t kIdQK = idesc_bf16(kM, kBlk, false);
-      constexpr uint32_t kIdPV = idesc_bf16(kM, kHalfCols, true);
+      constexpr uint32_t kIdPV = idesc_bf16(kM, 64, true);
       bool ok = mbar_wait(q_full, 0, a.wait_ns);
       const uint64_t qdesc = sdesc(sb + kQOff, 16, 1024);
+      int pv_next = 0;  // first block whose P V is not issued yet
+      // O[:, 64v..64v+63] += P V_v for the value slabs v of block jj; each
+      // slab's entry is freed once its MMAs are done
       auto issue_pv = [&](int jj) -> bool {
-        const int sp = jj & 1;
-        if (!mbar_wait(&p_full[sp], (jj >> 1) & 1, a.wait_ns)) return false;
+        if (!mbar_wait(&p_full[jj & 1], (jj >> 1) & 1, a.wait_ns)) return false;
         tc_after();
-        // V = this CTA's 4 value slabs of the block: MN-major, 64 columns per
-        // slab (leading offset = slab stride), 8-row groups 1 KB apart
-        const uint32_t vb = sb + kKOff + (uint32_t)(jj % kStages) * kKStage + (uint32_t)half * 4u * kKSlab;
+        const uint32_t pa = tmem + kColS + (uint32_t)(jj & 1) * kBlk;  // P: first 64 columns of S
+#pragma unroll 1
+        for (int v = 0; v < kVSlabs; ++v) {
+          const int e = jj * kSlabs + (kSlabs - kVSlabs) + v;
+          // MN-major: 64 value columns per row of 128 bytes, 8-row groups 1 KB apart
+          const uint64_t vdesc = sdesc(sb + kROff + (uint32_t)(e % kRing) * kEntry, kEntry, 1024);
 #pragma unroll
-        for (int kk = 0; kk < kBlk / 16; ++kk)
-          mma_ts(tmem + kColO, tmem + kColP + (uint32_t)sp * (kBlk / 2) + (uint32_t)kk * 8u,
-                 sdesc(vb + (uint32_t)kk * 16u * 128u, kKSlab, 1024), kIdPV, (jj > 0 || kk > 0) ? 1u : 0u);
-        mma_commit(&k_empty[jj % kStages]);
+          for (int kk = 0; kk < kBlk / 16; ++kk)
+            mma_ts(tmem + kColO + 64u * (uint32_t)v, pa + 8u * (uint32_t)kk, vdesc + ((uint32_t)kk * 16u * 128u >> 4),
+                   kIdPV, (jj > 0 || kk > 0) ? 1u : 0u);
+          mma_commit(&e_free[e % kRing]);
+        }
         mma_commit(pv_done);
         return true;
       };
+      auto flush_pv = [&](int upto) -> bool {  // P V of blocks pv_next..upto, in order
+        for (; pv_next <= upto; ++pv_next)
+          if (!issue_pv(pv_next)) return false;
+        return true;
+      };
       for (int j = 0; ok && j < nb; ++j) {
-        if (*abort_flag) {
+        // S[j & 1] holds P of block j-2 until its P V is issued
+        if (j >= 2 && !flush_pv(j - 2)) {
           ok = false;
           break;
         }
-        const int st = j & 1;
-        if (!mbar_wait(&k_full[j % kStages], (j / kStages) & 1, a.wait_ns) ||
-            (j >= 2 && !mbar_wait(&s_empty[st], ((j - 2) >> 1) & 1, a.wait_ns))) {
-          ok = false;
-          break;
-        }
-        tc_after();
-        // base descriptors once per block; the 36 K-steps add compile-time
-        // offsets to the start-address field (shared addresses stay below
-        // 2^18, so the 14-bit field never carries)
-        const uint64_t kdesc = sdesc(sb + kKOff + (uint32_t)(j % kStages) * kKStage, 16, 1024);
-        const uint32_t dS = tmem + kColS + (uint32_t)st * kBlk;
-        mma_ss(dS, qdesc, kdesc, kIdQK, 0u);
+        const uint32_t dS = tmem + kColS + (uint32_t)(j & 1) * kBlk;
+        for (int t = 0; t < kSlabs; ++t) {
+          const int e = j * kSlabs + t;
+          // the slot last held entry e - kRing: a value slab is freed by its P V
+          if (e >= kRing) {
+            const int pj = (e - kRing) / kSlabs, pt = (e - kRing) - pj * kSlabs;
+            if (pt >= kSlabs - kVSlabs && !flush_pv(pj)) {
+              ok = false;
+              break;
+            }
+          }
+          if (*abort_flag || !mbar_wait(&e_full[e % kRing], (e / kRing) & 1, a.wait_ns)) {
+            ok = false;
+            break;
+          }
+          tc_after();
+          const uint64_t kdesc = sdesc(sb + kROff + (uint32_t)(e % kRing) * kEntry, 16, 1024);
+          const uint64_t qd = qdesc + (((uint32_t)slab_of(t, half) * kQSlab) >> 4);
 #pragma unroll
-        for (int kk = 1; kk < kRow / 16; ++kk) {
-          const uint32_t c = (uint32_t)(kk & 3) * 32u;
-          mma_ss(dS, qdesc + (((uint32_t)(kk >> 2) * kQSlab + c) >> 4),
-                 kdesc + (((uint32_t)(kk >> 2) * kKSlab + c) >> 4), kIdQK, 1u);
+          for (int kk = 0; kk < 4; ++kk)
+            mma_ss(dS, qd + (uint32_t)(kk * 2), kdesc + (uint32_t)(kk * 2), kIdQK, (t > 0 || kk > 0) ? 1u : 0u);
+          if (t < kSlabs - kVSlabs) mma_commit(&e_free[e % kRing]);  // only the scores read this slab
         }
-        mma_commit(&s_full[st]);
-        if (j >= 1 && !issue_pv(j - 1)) {
-          ok = false;
-          break;
-        }
+        if (!ok) break;
+        mma_commit(&s_full[j & 1]);
       }
-      if (ok && nb > 0 && !issue_pv(nb - 1)) ok = false;
+      if (ok && !flush_pv(nb - 1)) ok = false;
       if (ok) mma_commit(o_final);
       if (!ok) fail();
       mma_commit(fin);  // everything issued above is complete before TMEM is freed
@@ -352,30 +384,49 @@ __global__ void __launch_bounds__(kAttThreads, 1) attend_kernel(AttendArgs a) {
     const float sl2 = a.scale_log2;
     float m_run = -INFINITY, l_run = 0.f;
     bool ok = true;
-    // slot of row `lane` of the next block, loaded a block ahead (validity mask)
-    int32_t sl_next = lane < kBlk && lane < a.k ? __ldg(a.slots + list + lane) : -1;
+    // slots of rows 32c + lane of the next block (validity masks), a block ahead
+    int32_t sn[kBlk / 32];
+    auto load_valid = [&](int j) {
+#pragma unroll
+      for (int c = 0; c < kBlk / 32; ++c) {
+        const int r = j * kBlk + 32 * c + lane;
+        sn[c] = j < nb && r < a.k ? __ldg(a.slots + list + r) : -1;
+      }
+    };
+    load_valid(0);
     for (int j = 0; j < nb; ++j) {
       if (__any_sync(kFull, *abort_flag != 0u)) {  // warp-uniform: TMEM access is warp-wide
         ok = false;
         break;
       }
-      const int st = j & 1;
-      ok = __all_sync(kFull, mbar_wait(&s_full[st], (j >> 1) & 1, a.wait_ns));
+      ok = __all_sync(kFull, mbar_wait(&s_full[j & 1], (j >> 1) & 1, a.wait_ns));
       if (!ok) break;
       tc_after();
-      float v[kBlk];
-      tmem_ld16(tmem + lane_addr + kColS + (uint32_t)st * kBlk, v);
-      tmem_wait_ld();
-      tc_before();
-      mbar_arrive(&s_empty[st]);
-      const int32_t sl = sl_next;
-      sl_next = lane < kBlk && (j + 1) * kBlk + lane < a.k ? __ldg(a.slots + list + (j + 1) * kBlk + lane) : -1;
-      const uint32_t vm = __ballot_sync(kFull, sl >= 0 && sl < a.C);
-      float mx = -INFINITY;
+      uint32_t vm[kBlk / 32];
 #pragma unroll
-      for (int c = 0; c < kBlk; ++c) {
-        v[c] = ((vm >> c) & 1u) ? v[c] * sl2 : -INFINITY;
-        mx = fmaxf(mx, v[c]);
+      for (int c = 0; c < kBlk / 32; ++c) vm[c] = __ballot_sync(kFull, sn[c] >= 0 && sn[c] < a.C);
+      load_valid(j + 1);
+      const uint32_t sS = tmem + lane_addr + kColS + (uint32_t)(j & 1) * kBlk;
+      // One read of S: the weights against the running maximum go to registers,
+      // and only if some score passes it by more than 2^8 (always on the first
+      // block with a listed row) does the warp rescale and compute them again.
+      uint32_t pk[kBlk / 2];
+      float mx = -INFINITY, ls = 0.f;
+      const float mu0 = m_run == -INFINITY ? 0.f : m_run;
+#pragma unroll
+      for (int c = 0; c < kBlk / 32; ++c) {
+        float v[32];
+        tmem_ld32(sS + 32u * (uint32_t)c, v);
+        tmem_wait_ld();
+#pragma unroll
+        for (int e = 0; e < 16; ++e) {
+          const bool ok0 = (vm[c] >> (2 * e)) & 1u, ok1 = (vm[c] >> (2 * e + 1)) & 1u;
+          const float t0 = ok0 ? v[2 * e] * sl2 : -INFINITY, t1 = ok1 ? v[2 * e + 1] * sl2 : -INFINITY;
+          mx = fmaxf(mx, fmaxf(t0, t1));
+          const __nv_bfloat162 b2 = __floats2bfloat162_rn(ok0 ? exp2f(t0 - mu0) : 0.f, ok1 ? exp2f(t1 - mu0) : 0.f);
+          ls += __low2float(b2) + __high2float(b2);
+          pk[16 * c + e] = *reinterpret_cast<const uint32_t*>(&b2);
+        }
       }
       if (__any_sync(kFull, mx > m_run + kRescaleLog2)) {
         // the warp moves its maxima together (TMEM access is warp-wide)
@@ -399,21 +450,36 @@ __global__ void __launch_bounds__(kAttThreads, 1) attend_kernel(AttendArgs a) {
           tmem_wait_st();
         }
         m_run = m_new;
-      }
-      const float mu = m_run == -INFINITY ? 0.f : m_run;
-      uint32_t pk[kBlk / 2];
-      float ls = 0.f;
+        const float mu = m_run == -INFINITY ? 0.f : m_run;
+        ls = 0.f;
 #pragma unroll
-      for (int c = 0; c < kBlk / 2; ++c) {
-        const __nv_bfloat162 b2 = __floats2bfloat162_rn(exp2f(v[2 * c] - mu), exp2f(v[2 * c + 1] - mu));
-        ls += __low2float(b2) + __high2float(b2);
-        pk[c] = *reinterpret_cast<const uint32_t*>(&b2);
+        for (int c = 0; c < kBlk / 32; ++c) {
+          float v[32];
+          tmem_ld32(sS + 32u * (uint32_t)c, v);
+          tmem_wait_ld();
+#pragma unroll
+          for (int e = 0; e < 16; ++e) {
+            const float x0 = ((vm[c] >> (2 * e)) & 1u) ? exp2f(v[2 * e] * sl2 - mu) : 0.f;
+            const float x1 = ((vm[c] >> (2 * e + 1)) & 1u) ? exp2f(v[2 * e + 1] * sl2 - mu) : 0.f;
+            const __nv_bfloat162 b2 = __floats2bfloat162_rn(x0, x1);
+            ls += __low2float(b2) + __high2float(b2);
+            pk[16 * c + e] = *reinterpret_cast<const uint32_t*>(&b2);
+          }
+        }
       }
-      l_run += ls;
-      tmem_st8(tmem + lane_addr + kColP + (uint32_t)st * (kBlk / 2), pk);
+      // P (bf16 pairs) over the first 64 columns of this S buffer, all of which
+      // this thread has read
+#pragma unroll
+      for (int c = 0; c < kBlk / 32; ++c) {
+        uint32_t w[16];
+#pragma unroll
+        for (int e = 0; e < 16; ++e) w[e] = pk[16 * c + e];
+        tmem_st16(sS + 16u * (uint32_t)c, w);
+      }
       tmem_wait_st();
+      l_run += ls;
       tc_before();
-      mbar_arrive(&p_full[st]);
+      mbar_arrive(&p_full[j & 1]);
     }
     if (ok) ok = __all_sync(kFull, mbar_wait(o_final, 0, a.wait_ns));
     if (ok) {
