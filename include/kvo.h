@@ -334,6 +334,76 @@ int kvo_attend(kvo_handle* h, const int32_t* units, int32_t n_units, const void*
                int32_t n_heads, float scale, const int32_t* topk_slots, void* out, float* lse,
                void* stream);
 
+/* ------------------------------------------------------------------------
+ * Layerwise prefill offload ([LS] section 3 "Layerwise Prefill Offload":
+ * "Buffer planning", "Execution pipeline", "Reuse invariant"; [FO] prefill
+ * paragraph: four trays, tray B0 bound to the first layer, onload_layer_map).
+ * The main KV of every layer lives in a pinned host pool; N layers share
+ * I + min(B, N - I) device buffers.  A prefill pass walks the layers in order:
+ * the layer's cached prefix is loaded into its buffer (unless the buffer
+ * still holds it), the caller's compute for the layer reads it and writes the
+ * chunk's new rows after it, and those rows are saved back to the host pool.
+ * Loads and saves run on the copy engines on two library streams; a buffer is
+ * reloaded only after the save of its previous layer has finished.
+ * ------------------------------------------------------------------------ */
+typedef struct kvo_lw kvo_lw; /* opaque, library-owned */
+typedef struct {
+  int32_t n_layers;      /* N cache-bearing layers, >= 1 */
+  int32_t n_independent; /* I: layers 0..I-1 keep a dedicated buffer (tray B0 = layer 0); 0..N */
+  int32_t n_shared;      /* B shared buffers, round robin over layers I..N-1; >= 1 if I < N */
+  int32_t lookahead;     /* onload_layer_map: a layer's load is issued when the compute of the
+                            layer `lookahead` before it starts (>= 1) */
+  int64_t max_tokens;    /* rows per layer in the host pool and in every buffer */
+  int32_t row_elems;     /* bf16 elements per row (576); row bytes a multiple of 16 */
+  int32_t device;
+} kvo_lw_config;
+
+/* kvo_lw_create: the plan (reading R14 of the oracle: independent layers take
+ * buffers 0..I-1, the k-th reusable layer buffer I + k mod min(B, N - I)), the
+ * device buffers [n_phys][max_tokens][row_elems] bf16 and the pinned host pool
+ * [N][max_tokens][row_elems] bf16 (zeroed).  Cached length starts at 0.
+ * Errors: KVO_EINVAL (config), KVO_ENOMEM, KVO_ECUDA. */
+int kvo_lw_create(const kvo_lw_config* cfg, kvo_lw** out);
+int kvo_lw_destroy(kvo_lw* lw);
+
+/* kvo_lw_plan: *n_phys = the number of device buffers; phys_of_layer [N]
+ * (nullable) = the buffer of each layer. */
+int kvo_lw_plan(kvo_lw* lw, int32_t* n_phys, int32_t* phys_of_layer);
+
+/* kvo_lw_host_rows: host address of layer `layer`'s rows [max_tokens][row_elems]
+ * in the pinned pool (NULL on a bad argument).  Write the cached prefix there
+ * before kvo_lw_set_length; the library reads and writes it during passes. */
+void* kvo_lw_host_rows(kvo_lw* lw, int32_t layer);
+
+/* kvo_lw_set_length: the cached prefix now has `tokens` rows in every layer
+ * (host pool rows 0..tokens-1); forgets what the buffers hold.  Synchronises
+ * the library streams.  Errors: KVO_EINVAL (inside a pass), KVO_ERANGE. */
+int kvo_lw_set_length(kvo_lw* lw, int64_t tokens);
+
+/* kvo_lw_begin: start a pass over `chunk_tokens` new tokens on the caller's
+ * stream (loads wait for the work already on it).  Errors: KVO_EINVAL (pass
+ * already open), KVO_ERANGE (length + chunk_tokens > max_tokens). */
+int kvo_lw_begin(kvo_lw* lw, int64_t chunk_tokens, void* stream);
+
+/* kvo_lw_layer: the next layer of the pass (layers in order 0..N-1).  Issues
+ * the loads up to `lookahead` layers ahead, makes `stream` wait until this
+ * layer's buffer holds its cached rows 0..L-1, and returns the buffer
+ * (device, [max_tokens][row_elems] bf16) in *buffer.  The caller's compute on
+ * `stream` reads rows 0..L-1 and writes the chunk's rows L..L+c-1.
+ * Errors: KVO_EINVAL (no open pass, layer out of order). */
+int kvo_lw_layer(kvo_lw* lw, int32_t layer, void** buffer, void* stream);
+
+/* kvo_lw_layer_done: the compute of `layer` has been enqueued on `stream`;
+ * its rows L..L+c-1 are saved to the host pool once it finishes. */
+int kvo_lw_layer_done(kvo_lw* lw, int32_t layer, void* stream);
+
+/* kvo_lw_end: after the last layer: `stream` waits for every save of the pass;
+ * the cached length grows by the chunk.  Errors: KVO_EINVAL (layers missing). */
+int kvo_lw_end(kvo_lw* lw, void* stream);
+
+/* kvo_lw_stats: bytes copied host -> device and device -> host so far. */
+int kvo_lw_stats(kvo_lw* lw, uint64_t* bytes_h2d, uint64_t* bytes_d2h);
+
 /* kvo_last_error: message of the last failing call on this thread ("" if none). */
 const char* kvo_last_error(void);
 

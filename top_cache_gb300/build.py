@@ -8,7 +8,8 @@ HERE = os.path.dirname(os.path.abspath(__file__))
 CSRC = os.path.join(HERE, "csrc")
 BUILD = os.path.join(HERE, "_build")
 SO = os.path.join(HERE, "libkvo.so")
-SOURCES = ["kvo_api.cu", "kvo_select.cu", "kvo_residency.cu", "kvo_noalloc.cu", "kvo_fused.cu", "kvo_fused_i8.cu", "kvo_attend.cu"]
+SOURCES = ["kvo_api.cu", "kvo_select.cu", "kvo_residency.cu", "kvo_noalloc.cu", "kvo_fused.cu", "kvo_fused_i8.cu", "kvo_attend.cu",
+           "kvo_layerwise.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "--expt-relaxed-constexpr"]
 

@@ -168,12 +168,7 @@ void free_all(kvo_handle* h) {
     if (p) cudaFree(p);
   if (h->bytes_seen) cudaFree(h->bytes_seen);
   if (h->bytes_prev_host) cudaFreeHost(h->bytes_prev_host);
-  if (h->host_pool && h->pool_map_bytes) {
-    cudaHostUnregister(h->host_pool);
-    munmap(h->host_pool, h->pool_map_bytes);
-  } else if (h->host_pool) {
-    cudaFreeHost(h->host_pool);
-  }
+  kvo::free_pinned(h->host_pool, h->pool_map_bytes);
 }
 
 size_t residency_smem_bytes(int C, int P, int k) {
@@ -207,31 +202,9 @@ size_t thp_size() {
 // pages are therefore mapped with transparent huge pages (madvise) and
 // registered; otherwise, or when that fails, cudaHostAlloc.
 cudaError_t alloc_host_pool(kvo_handle* h, size_t bytes) {
-  const size_t huge = thp_size();
-  if (huge >= (2u << 20) && bytes >= 4 * huge) {
-    const size_t len = (bytes + huge - 1) / huge * huge;
-    void* raw = mmap(nullptr, len + huge, PROT_READ | PROT_WRITE, MAP_PRIVATE | MAP_ANONYMOUS | MAP_NORESERVE, -1, 0);
-    if (raw != MAP_FAILED) {
-      const uintptr_t r = reinterpret_cast<uintptr_t>(raw);
-      const uintptr_t a = (r + huge - 1) / huge * huge;
-      if (a > r) munmap(raw, a - r);
-      const size_t tail = (r + len + huge) - (a + len);
-      if (tail) munmap(reinterpret_cast<void*>(a + len), tail);
-      void* p = reinterpret_cast<void*>(a);
-      if (madvise(p, len, MADV_HUGEPAGE) == 0 &&
-          cudaHostRegister(p, len, cudaHostRegisterMapped | cudaHostRegisterPortable) == cudaSuccess) {
-        h->host_pool = static_cast<uint16_t*>(p);
-        h->pool_map_bytes = len;
-        h->pool_huge_page = huge;
-        return cudaSuccess;
-      }
-      cudaGetLastError();  // clear a failed registration
-      munmap(p, len);
-    }
-  }
-  cudaError_t e = cudaHostAlloc(reinterpret_cast<void**>(&h->host_pool), bytes,
-                                cudaHostAllocMapped | cudaHostAllocPortable);
-  if (e != cudaSuccess) h->host_pool = nullptr;
+  void* p = nullptr;
+  cudaError_t e = kvo::alloc_pinned(bytes, &p, &h->pool_map_bytes, &h->pool_huge_page);
+  h->host_pool = static_cast<uint16_t*>(p);
   return e;
 }
 
@@ -483,6 +456,60 @@ int fused_step(kvo_handle* h, const int32_t* du, const int32_t* units, int32_t n
 
 namespace kvo {
 void set_last_error(const char* msg) { g_err = msg; }
+}  // namespace kvo
+
+namespace kvo {
+
+int set_error(int code, const char* msg) { return fail(code, msg); }
+int set_cuda_error(cudaError_t e, const char* what) { return cuda_fail(e, what); }
+
+// Pinned, device-mapped host memory.  Rows are read at random by the GPU over
+// the host link, and with base pages the address translation of a large pool
+// becomes the limit (measured: ~200 GB/s up to ~21 GB of pool, 37-52 GB/s at
+// 43 GB with 64 KB pages, 80 GB/s with 512 MB pages).  Allocations of at least
+// four huge pages are therefore mapped with transparent huge pages (madvise)
+// and registered (*map_bytes > 0); otherwise, or when that fails,
+// cudaHostAlloc (*map_bytes = 0).
+cudaError_t alloc_pinned(size_t bytes, void** out, size_t* map_bytes, size_t* huge_page) {
+  *out = nullptr;
+  *map_bytes = 0;
+  *huge_page = 0;
+  const size_t huge = thp_size();
+  if (huge >= (2u << 20) && bytes >= 4 * huge) {
+    const size_t len = (bytes + huge - 1) / huge * huge;
+    void* raw = mmap(nullptr, len + huge, PROT_READ | PROT_WRITE, MAP_PRIVATE | MAP_ANONYMOUS | MAP_NORESERVE, -1, 0);
+    if (raw != MAP_FAILED) {
+      const uintptr_t r = reinterpret_cast<uintptr_t>(raw);
+      const uintptr_t a = (r + huge - 1) / huge * huge;
+      if (a > r) munmap(raw, a - r);
+      const size_t tail = (r + len + huge) - (a + len);
+      if (tail) munmap(reinterpret_cast<void*>(a + len), tail);
+      void* p = reinterpret_cast<void*>(a);
+      if (madvise(p, len, MADV_HUGEPAGE) == 0 &&
+          cudaHostRegister(p, len, cudaHostRegisterMapped | cudaHostRegisterPortable) == cudaSuccess) {
+        *out = p;
+        *map_bytes = len;
+        *huge_page = huge;
+        return cudaSuccess;
+      }
+      cudaGetLastError();  // clear a failed registration
+      munmap(p, len);
+    }
+  }
+  cudaError_t e = cudaHostAlloc(out, bytes, cudaHostAllocMapped | cudaHostAllocPortable);
+  if (e != cudaSuccess) *out = nullptr;
+  return e;
+}
+
+void free_pinned(void* p, size_t map_bytes) {
+  if (p && map_bytes) {
+    cudaHostUnregister(p);
+    munmap(p, map_bytes);
+  } else if (p) {
+    cudaFreeHost(p);
+  }
+}
+
 }  // namespace kvo
 
 extern "C" {

@@ -360,6 +360,11 @@ cudaError_t launch_residency(const ResidencyArgs& a, cudaStream_t s);
 cudaError_t launch_gather(const GatherArgs& a, int n_sm, cudaStream_t s);
 cudaError_t launch_append(const AppendArgs& a, cudaStream_t s);
 cudaError_t launch_attend(const AttendArgs& a, cudaStream_t s);
+// host helpers shared by the entry points (kvo_api.cu)
+int set_error(int code, const char* msg);
+int set_cuda_error(cudaError_t e, const char* what);
+cudaError_t alloc_pinned(size_t bytes, void** out, size_t* map_bytes, size_t* huge_page);
+void free_pinned(void* p, size_t map_bytes);
 size_t attend_smem_bytes();
 cudaError_t launch_reset(const ResetArgs& a, cudaStream_t s);
 cudaError_t launch_order_init(int32_t* order, int32_t* par, int U, int C, cudaStream_t s);

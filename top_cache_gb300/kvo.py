@@ -43,7 +43,9 @@ KVO_GATHER_BULK = 1
 EXPORTED = ("kvo_create", "kvo_destroy", "kvo_host_rows", "kvo_prefill", "kvo_append", "kvo_step",
             "kvo_select_workspace_size", "kvo_select", "kvo_reset", "kvo_profile_read",
             "kvo_set_option", "kvo_get_option", "kvo_get_stats", "kvo_export_state", "kvo_select_noalloc",
-            "kvo_attend", "kvo_last_error")
+            "kvo_attend", "kvo_lw_create", "kvo_lw_destroy", "kvo_lw_plan", "kvo_lw_host_rows",
+            "kvo_lw_set_length", "kvo_lw_begin", "kvo_lw_layer", "kvo_lw_layer_done", "kvo_lw_end",
+            "kvo_lw_stats", "kvo_last_error")
 
 
 class KvoConfig(ctypes.Structure):
@@ -52,6 +54,13 @@ class KvoConfig(ctypes.Structure):
                 ("row_elems", ctypes.c_int32), ("topk", ctypes.c_int32),
                 ("hot_capacity", ctypes.c_int32), ("n_positions", ctypes.c_int32),
                 ("device", ctypes.c_int32), ("idx_dtype", ctypes.c_int32)]
+
+
+class KvoLwConfig(ctypes.Structure):
+    _fields_ = [("n_layers", ctypes.c_int32), ("n_independent", ctypes.c_int32),
+                ("n_shared", ctypes.c_int32), ("lookahead", ctypes.c_int32),
+                ("max_tokens", ctypes.c_int64), ("row_elems", ctypes.c_int32),
+                ("device", ctypes.c_int32)]
 
 
 class KvoStats(ctypes.Structure):
@@ -119,6 +128,26 @@ def lib():
             L.kvo_export_state.argtypes = [vp, i32, vp, vp, vp, vp, vp, vp]
             L.kvo_last_error.restype = ctypes.c_char_p
             L.kvo_last_error.argtypes = []
+            L.kvo_lw_create.restype = ctypes.c_int
+            L.kvo_lw_create.argtypes = [ctypes.POINTER(KvoLwConfig), ctypes.POINTER(vp)]
+            L.kvo_lw_destroy.restype = ctypes.c_int
+            L.kvo_lw_destroy.argtypes = [vp]
+            L.kvo_lw_plan.restype = ctypes.c_int
+            L.kvo_lw_plan.argtypes = [vp, ctypes.POINTER(ctypes.c_int32), vp]
+            L.kvo_lw_host_rows.restype = vp
+            L.kvo_lw_host_rows.argtypes = [vp, i32]
+            L.kvo_lw_set_length.restype = ctypes.c_int
+            L.kvo_lw_set_length.argtypes = [vp, i64]
+            L.kvo_lw_begin.restype = ctypes.c_int
+            L.kvo_lw_begin.argtypes = [vp, i64, vp]
+            L.kvo_lw_layer.restype = ctypes.c_int
+            L.kvo_lw_layer.argtypes = [vp, i32, ctypes.POINTER(vp), vp]
+            L.kvo_lw_layer_done.restype = ctypes.c_int
+            L.kvo_lw_layer_done.argtypes = [vp, i32, vp]
+            L.kvo_lw_end.restype = ctypes.c_int
+            L.kvo_lw_end.argtypes = [vp, vp]
+            L.kvo_lw_stats.restype = ctypes.c_int
+            L.kvo_lw_stats.argtypes = [vp, ctypes.POINTER(ctypes.c_uint64), ctypes.POINTER(ctypes.c_uint64)]
             _lib = L
     return _lib
 
@@ -347,3 +376,80 @@ class Kvo:
 
     def export_state(self, unit, with_rows=False):
         return kvo_export_state(self.h, unit, self.max_tokens, self.C, self.R, with_rows)
+
+
+class _DeviceRows:
+    """__cuda_array_interface__ view of device rows (no copy), for torch.as_tensor."""
+
+    def __init__(self, ptr, rows, row_elems):
+        self.__cuda_array_interface__ = {"shape": (rows, row_elems), "typestr": "<i2",
+                                         "data": (int(ptr), False), "version": 3, "strides": None}
+
+
+class Layerwise:
+    """Layerwise prefill offload (kvo_lw_*): host pool of every layer, device buffers by plan."""
+
+    def __init__(self, n_layers, max_tokens, n_independent=1, n_shared=3, lookahead=1,
+                 row_elems=576, device=0):
+        cfg = KvoLwConfig(n_layers, n_independent, n_shared, lookahead, max_tokens, row_elems, device)
+        h = ctypes.c_void_p()
+        _check(lib().kvo_lw_create(ctypes.byref(cfg), ctypes.byref(h)))
+        self.h = h.value
+        self.n_layers, self.max_tokens, self.row_elems, self.device = n_layers, max_tokens, row_elems, device
+        n = ctypes.c_int32()
+        phys = np.zeros(n_layers, dtype=np.int32)
+        _check(lib().kvo_lw_plan(self.h, ctypes.byref(n), phys.ctypes.data))
+        self.n_phys, self.phys = int(n.value), phys
+        self._views = {}
+
+    def close(self):
+        if getattr(self, "h", None):
+            lib().kvo_lw_destroy(self.h)
+            self.h = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+    def host_rows(self, layer):
+        """numpy view [max_tokens][row_elems] uint16 of the layer's pinned host rows."""
+        ptr = lib().kvo_lw_host_rows(self.h, layer)
+        if not ptr:
+            raise KvoError(KVO_EINVAL, lib().kvo_last_error().decode())
+        n = self.max_tokens * self.row_elems
+        return np.ctypeslib.as_array((ctypes.c_uint16 * n).from_address(ptr)).reshape(
+            self.max_tokens, self.row_elems)
+
+    def host_rows_ptr(self, layer):
+        return lib().kvo_lw_host_rows(self.h, layer)
+
+    def set_length(self, tokens):
+        _check(lib().kvo_lw_set_length(self.h, tokens))
+
+    def begin(self, chunk_tokens, stream=None):
+        _check(lib().kvo_lw_begin(self.h, chunk_tokens, _stream(stream)))
+
+    def layer(self, layer, stream=None):
+        """The layer's device buffer as an int16 torch tensor [max_tokens][row_elems] (bf16 bits);
+        `stream` waits until it holds the cached rows."""
+        import torch
+        p = ctypes.c_void_p()
+        _check(lib().kvo_lw_layer(self.h, layer, ctypes.byref(p), _stream(stream)))
+        ptr = int(p.value)
+        if ptr not in self._views:
+            self._views[ptr] = torch.as_tensor(_DeviceRows(ptr, self.max_tokens, self.row_elems),
+                                               device="cuda:%d" % self.device)
+        return self._views[ptr]
+
+    def layer_done(self, layer, stream=None):
+        _check(lib().kvo_lw_layer_done(self.h, layer, _stream(stream)))
+
+    def end(self, stream=None):
+        _check(lib().kvo_lw_end(self.h, _stream(stream)))
+
+    def stats(self):
+        a, b = ctypes.c_uint64(), ctypes.c_uint64()
+        _check(lib().kvo_lw_stats(self.h, ctypes.byref(a), ctypes.byref(b)))
+        return {"bytes_h2d": int(a.value), "bytes_d2h": int(b.value)}
