@@ -99,6 +99,35 @@ def load_bf16_peak():
         return FALLBACK_BF16_TFLOPS, "fallback"
 
 
+def huge_backed_fraction(addr):
+    """Fraction of the mapping that holds host address addr backed by transparent huge
+    pages (from /proc/self/smaps), or None when it cannot be read."""
+    try:
+        with open("/proc/self/smaps") as f:
+            lines = f.read().splitlines()
+    except OSError:
+        return None
+    for i, line in enumerate(lines):
+        head = line.split()
+        if not head or "-" not in head[0]:
+            continue
+        try:
+            lo, hi = (int(x, 16) for x in head[0].split("-"))
+        except ValueError:
+            continue
+        if lo <= addr < hi:
+            size = anon_huge = None
+            for l2 in lines[i + 1:i + 40]:
+                if l2.startswith("Size:"):
+                    size = int(l2.split()[1])
+                elif l2.startswith("AnonHugePages:"):
+                    anon_huge = int(l2.split()[1])
+                if size is not None and anon_huge is not None:
+                    return round(anon_huge / size, 4) if size else None
+            return None
+    return None
+
+
 def kernel_source_hash():
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "top_cache_gb300", "csrc")
@@ -338,6 +367,97 @@ def run_attention(args, kv, wl, units, device, torch):
     }
 
 
+# --------------------------------------------------------------------------- layerwise prefill
+def run_layerwise(args, link, device, torch, log):
+    """Time prefill passes of the layerwise offload (kvo_lw_*) on their own.
+
+    Per pass and layer: the cached prefix is loaded into the layer's buffer (unless it is
+    resident), a stand-in compute of a fixed window runs on the caller's stream (a timed
+    spin, so that it takes no memory bandwidth, then the copy of the chunk's rows into the
+    buffer), and the chunk's rows are saved to the host pool.  Roofline of a pass: the
+    slower of the compute windows and each link direction at its measured peak."""
+    import numpy as np
+    import workload as W
+    from top_cache_gb300 import kvo as K
+    N, L0, c, n_pass = args.lw_layers, args.lw_prefix, args.lw_chunk, args.lw_passes
+    row = 576
+    T = L0 + c * (n_pass + 1)
+    t0 = time.time()
+    lw = K.Layerwise(N, T, 1, 3, 1, row)
+    try:
+        for l in range(N):
+            W.token_rows_into(lw.host_rows_ptr(l), 0, 3001, W.KIND_ROWS, [(0, l)], 0, L0, row)
+        lw.set_length(L0)
+        chunk = torch.zeros((c, row), dtype=torch.int16, device=device)
+        # compute window per layer: the load time of the mid-run prefix at the measured peak
+        # (the pages' condition for a free transfer: window >= copy time)
+        L_mid = L0 + c * (n_pass // 2)
+        win_us = args.lw_window_us or (L_mid * row * 2 / (link["h2d"] * 1e9) * 1e6)
+        stream = torch.cuda.current_stream(device)
+        # calibrate the spin: cycles per microsecond at the current clock
+        c0, c1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        torch.cuda._sleep(1000000)
+        c0.record(stream)
+        torch.cuda._sleep(2000000)
+        c1.record(stream)
+        torch.cuda.synchronize(device)
+        cycles = int(win_us * 2000000 / (c0.elapsed_time(c1) * 1e3))
+        scratch = torch.empty_like(chunk)
+
+        def one_pass(L):
+            lw.begin(c)
+            for l in range(N):
+                buf = lw.layer(l)
+                torch.cuda._sleep(cycles)
+                buf[L:L + c].copy_(chunk)
+                lw.layer_done(l)
+            lw.end()
+
+        log("[bench] layerwise set-up %.1f s (host pool %.2f GB)" % (time.time() - t0, N * T * row * 2 / 1e9))
+        one_pass(L0)  # warm-up pass
+        torch.cuda.synchronize(device)
+        st0 = lw.stats()
+        ev = [torch.cuda.Event(enable_timing=True) for _ in range(n_pass + 1)]
+        ev[0].record(stream)
+        L = L0 + c
+        for i in range(n_pass):
+            one_pass(L)
+            L += c
+            ev[i + 1].record(stream)
+        torch.cuda.synchronize(device)
+        pass_ms = [ev[i].elapsed_time(ev[i + 1]) for i in range(n_pass)]
+        # the stand-in compute alone, same launches, no library calls
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for l in range(N):
+            torch.cuda._sleep(cycles)
+            scratch.copy_(chunk)
+        e1.record(stream)
+        torch.cuda.synchronize(device)
+        compute_ms = e0.elapsed_time(e1)
+        st1 = lw.stats()
+    finally:
+        lw.close()
+    h2d = (st1["bytes_h2d"] - st0["bytes_h2d"]) / n_pass
+    d2h = (st1["bytes_d2h"] - st0["bytes_d2h"]) / n_pass
+    t_pass = statistics.mean(pass_ms)
+    t_h2d = h2d / (link["h2d"] * 1e9) * 1e3
+    t_d2h = d2h / (link["d2h"] * 1e9) * 1e3
+    t_roof = max(compute_ms, t_h2d, t_d2h)
+    return {
+        "layers": N, "trays": 4, "prefix_tokens": L0, "chunk_tokens": c, "passes": n_pass,
+        "ms_per_pass": round(t_pass, 4), "compute_window_us_per_layer": round(win_us, 1),
+        "compute_ms_per_pass": round(compute_ms, 4),
+        "exposed_transfer_ms_per_pass": round(max(0.0, t_pass - compute_ms), 4),
+        "h2d_bytes_per_pass": int(h2d), "d2h_bytes_per_pass": int(d2h),
+        "h2d_gbs": round(h2d / (t_pass * 1e-3) / 1e9, 1), "d2h_gbs": round(d2h / (t_pass * 1e-3) / 1e9, 1),
+        "roofline": {"bound": "compute window" if compute_ms >= max(t_h2d, t_d2h) else "host link",
+                     "t_roofline_ms": round(t_roof, 4), "frac": round(t_roof / t_pass, 4),
+                     "peaks_gbs": {"h2d": round(link["h2d"], 1), "d2h": round(link["d2h"], 1)}},
+        "device_buffer_bytes": 4 * T * row * 2, "host_pool_bytes": N * T * row * 2,
+    }
+
+
 # --------------------------------------------------------------------------- GPU arm
 def run_kvo(args, log):
     import numpy as np
@@ -486,6 +606,11 @@ def run_kvo(args, log):
     if args.attend_heads > 0 and wl.row_elems == 576:
         attention = run_attention(args, kv, wl, units, device, torch)
 
+    # ---------------- layerwise prefill offload, timed on its own
+    layerwise = None
+    if args.lw_layers > 0 and world == 1:
+        layerwise = run_layerwise(args, link, device, torch, log)
+
     # ---------------- end to end through the public API with host buffers
     e2e = None
     if not args.no_e2e:
@@ -506,6 +631,7 @@ def run_kvo(args, log):
                    "hot_capacity": wl.hot_capacity, "drift": wl.drift,
                    "steps_per_sequence": wl.steps, "path": path, "indexer": args.idx,
                    "host_pool_page": kv.get_option(K.KVO_OPT_HOST_HUGE_PAGE) or "base",
+                   "host_pool_huge_backed": huge_backed_fraction(kv.host_rows(0)),
                    "gather": "bulk" if path == "fused" else args.gather, "groups": args.groups,
                    "parallelism": "replicas%d" % world,
                    "l2": "inputs larger than L2: %.2f GB of indexer keys read per step"
@@ -537,6 +663,7 @@ def run_kvo(args, log):
         "clocks": clocks,
         "e2e": e2e,
         "attention": attention,
+        "layerwise_prefill": layerwise,
         "gpu_launches": launches,
         "cpu_baseline": cpu,
     }
@@ -750,6 +877,13 @@ def main(argv=None):
     ap.add_argument("--attend-heads", type=int, default=128,
                     help="heads of the timed sparse attention (multiple of 128; 0 = skip it)")
     ap.add_argument("--attend-launches", type=int, default=20)
+    ap.add_argument("--lw-layers", type=int, default=78,
+                    help="layers of the timed layerwise prefill passes (0 = skip them)")
+    ap.add_argument("--lw-prefix", type=int, default=16384)
+    ap.add_argument("--lw-chunk", type=int, default=4096)
+    ap.add_argument("--lw-passes", type=int, default=3)
+    ap.add_argument("--lw-window-us", type=float, default=0.0,
+                    help="stand-in compute per layer (0 = the layer's load time at the measured peak)")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-units", type=int, default=32)
