@@ -85,6 +85,12 @@ typedef struct kvo_config {
   int32_t n_positions;  /* P query positions per step, 1..8 (4 = MTP3) */
   int32_t device;       /* CUDA device ordinal */
   int32_t idx_dtype;    /* KVO_IDX_BF16 (0) or KVO_IDX_INT8 (1): indexer cache format */
+  int32_t host_block_tokens; /* 0: each unit owns rows 0..max_tokens-1 of the host pool.  > 0
+                                (a multiple of 8): the pool is host_blocks blocks of this many
+                                rows, shared by all units through per-unit block tables
+                                (kvo_set_blocks; "SFA Remote D2H Connector Design",
+                                "Data Ownership": main-KV block IDs) */
+  int64_t host_blocks;       /* blocks of a paged pool (0: enough for every unit's max_tokens) */
 } kvo_config;
 
 /* Indexer cache formats ("FlashOffloading ... What does it mean?", LIM C8
@@ -110,6 +116,7 @@ typedef struct kvo_stats {
   uint64_t timeouts;        /* bounded device waits that expired */
   uint64_t rescored;        /* units rescored because a speculative threshold was too high */
   uint64_t fused_steps;     /* kvo_step calls that ran as one fused launch (KVO_OPT_FUSED) */
+  uint64_t block_errors;    /* paged pool: rows of unmapped blocks skipped by append or gather */
 } kvo_stats;
 
 /* Options for kvo_set_option. */
@@ -165,6 +172,27 @@ int kvo_destroy(kvo_handle* h);
  * set-up, outside the decode step).  NULL if unit is out of range.
  */
 void* kvo_host_rows(kvo_handle* h, int32_t unit);
+
+/*
+ * Paged host pool (config host_block_tokens > 0).  A unit's token t lives in
+ * row t mod B of physical block blocks[t / B] of its block table (B =
+ * host_block_tokens); the indexer cache and the hot buffers stay per unit on
+ * the device.  kvo_host_rows returns NULL for a paged pool.
+ * kvo_set_blocks: entries first_block .. first_block+n_blocks-1 of unit's
+ * table = blocks[0..n_blocks-1] (host array; -1 = unmapped), copied on
+ * `stream`: from pageable memory the call returns once the array has been
+ * staged (the caller may reuse it); from pinned memory it is asynchronous
+ * (keep the array unchanged until the stream has passed the copy).  Rows of
+ * unmapped blocks are never read or written: an append skips them and a
+ * gather leaves the hot row as it was, and kvo_stats.block_errors counts
+ * them.  Errors: KVO_EINVAL (not paged, a block id >= host_blocks),
+ * KVO_ERANGE (unit or block range).
+ * kvo_host_block: host address of physical block `block` ([B][row_elems]
+ * bf16), for filling the cached rows; NULL on a bad argument.
+ */
+int kvo_set_blocks(kvo_handle* h, int32_t unit, int32_t first_block, int32_t n_blocks,
+                   const int32_t* blocks, void* stream);
+void* kvo_host_block(kvo_handle* h, int64_t block);
 
 /*
  * kvo_prefill: set an empty unit's context to n_tokens tokens whose rows are

@@ -12,9 +12,23 @@ from tests.helpers import check_residency_invariants
 from top_cache_gb300 import kvo as K
 
 
-def _fill_host_rows(kv, wl, units_rl, unit_ids, t0, n_tok):
-    """Write generator rows for the given units straight into the pinned pool."""
+def _fill_host_rows(kv, wl, units_rl, unit_ids, t0, n_tok, tables=None):
+    """Write generator rows for the given units straight into the pinned pool (through the
+    units' block tables when the pool is paged)."""
     if not unit_ids:
+        return
+    if tables is not None:
+        B = kv.block_tokens
+        for u in unit_ids:
+            t = t0
+            while t < t0 + n_tok:
+                j = t // B
+                n = min((j + 1) * B, t0 + n_tok) - t
+                pb = int(tables[u][j])
+                if pb >= 0:
+                    W.token_rows_into(kv.host_block(pb) + (t - j * B) * wl.row_elems * 2, 0, wl.seed,
+                                      W.KIND_ROWS, [units_rl[u]], t, n, wl.row_elems)
+                t += n
         return
     if kv.U > 1:
         unit_stride = (kv.host_rows(1) - kv.host_rows(0)) // 2
@@ -35,7 +49,7 @@ class Runner:
 
     def __init__(self, wl, check_units=None, distinct=False, rows_for=None, steps=None,
                  gather_mode=K.KVO_GATHER_LDG, keys_fn=None, queries=None, max_tokens=None,
-                 options=None, idx_int8=False, prefill_from_host=False):
+                 options=None, idx_int8=False, prefill_from_host=False, paged=0, unmapped=None):
         self.wl = wl
         self.steps = wl.steps if steps is None else steps
         self.units_rl = wl.units_rl()
@@ -45,13 +59,25 @@ class Runner:
         self.tmax = wl.max_tokens(self.steps) if max_tokens is None else max_tokens
         self.kv = K.Kvo(wl.n_requests, wl.n_layers, self.tmax, wl.topk, wl.hot_capacity,
                         wl.n_pos, wl.row_elems,
-                        idx_dtype=K.KVO_IDX_INT8 if idx_int8 else K.KVO_IDX_BF16)
+                        idx_dtype=K.KVO_IDX_INT8 if idx_int8 else K.KVO_IDX_BF16,
+                        host_block_tokens=paged)
+        self.tables = None
+        if paged:
+            # every unit's blocks scattered through the pool (seeded permutation); the
+            # (unit, logical block) pairs in `unmapped` are left unmapped (-1)
+            mb = -(-self.tmax // paged)
+            perm = np.random.default_rng(wl.seed).permutation(self.U * mb).astype(np.int32)
+            self.tables = perm.reshape(self.U, mb).copy()
+            for (u, j) in (unmapped or ()):
+                self.tables[u][j] = -1
+            for u in range(self.U):
+                self.kv.set_blocks(u, self.tables[u])
         self.kv.set_option(K.KVO_OPT_GATHER_MODE, gather_mode)
         for key, value in {**PATH_OPTIONS, **(options or {})}.items():
             self.kv.set_option(key, value)
         self.keys_fn = keys_fn
         # prefill: rows into the pinned pool, keys into the indexer cache
-        _fill_host_rows(self.kv, wl, self.units_rl, rows_for, 0, wl.context)
+        _fill_host_rows(self.kv, wl, self.units_rl, rows_for, 0, wl.context, self.tables)
         self.length = wl.context
         self.oracles = {u: oracle.OracleUnit(self.tmax, wl.topk, wl.hot_capacity, wl.n_pos,
                                              wl.row_elems, keep_rows=True, idx_int8=idx_int8)

@@ -416,3 +416,56 @@ def test_full_batch32x16_sampled():
     if _meminfo_gb() < need * 1.3 + 16:
         pytest.skip("host memory below %.0f GB for the pinned pool" % (need * 1.3 + 16))
     _run(wl, steps=12, check_units=[5, 400], count_rows=False)
+
+
+# ---------------------------------------------------------------- paged host pool
+def test_paged_host_pool():
+    # the host pool in 64-row blocks scattered through it by per-unit block tables: every
+    # appended row and every miss row goes through the table
+    wl = W.Workload("paged", 2, 2, 3000, 4, 4, 256, 1100, 6, 0.5, 96)
+    _run(wl, paged=64)
+
+
+def test_paged_host_pool_bulk_gather(path):
+    _staged_only(path)
+    wl = W.Workload("pagedb", 2, 2, 1500, 2, 2, 128, 400, 4, 0.3, 97)
+    _run(wl, paged=32, gather_mode=K.KVO_GATHER_BULK)
+
+
+def test_paged_unmapped_block_is_counted_not_touched():
+    # unit 1's block for the appended tokens is unmapped: its rows are neither written nor
+    # read (a gather leaves the hot row as it was); unit 0 still matches the oracle
+    wl = W.Workload("pagedx", 1, 2, 256, 2, 2, 64, 256, 3, 0.5, 98)
+    B = 64
+    r = Runner(wl, paged=B, unmapped=[(1, wl.context // B)], check_units=[0])
+    try:
+        before = r.kv.stats()
+        for s in range(r.steps):
+            r.append(wl.n_new)
+            r.compare(r.step(s))
+        st = r.kv.stats()
+        assert st["block_errors"] - before["block_errors"] >= r.steps * wl.n_new
+        assert st["timeouts"] == 0
+    finally:
+        r.close()
+
+
+def test_paged_pool_arguments():
+    kv = K.Kvo(1, 2, 100, 8, 16, 1, 576, host_block_tokens=16)
+    try:
+        with pytest.raises(K.KvoError):
+            kv.set_blocks(0, [0] * 8)  # 7 entries per unit (ceil(100 / 16))
+        with pytest.raises(K.KvoError):
+            kv.set_blocks(0, [14])  # 2 units x 7 blocks = 14 blocks: ids 0..13
+        with pytest.raises(K.KvoError):
+            kv.set_blocks(2, [0])  # unit out of range
+        with pytest.raises(K.KvoError):
+            kv.host_block(14)
+        with pytest.raises(K.KvoError):
+            K.kvo_host_rows(kv.h, 0)  # paged: rows are reached by block
+        kv.set_blocks(1, [13, -1], first_block=5)
+        assert kv.host_block(13) > 0
+    finally:
+        kv.close()
+    with pytest.raises(K.KvoError):
+        K.Kvo(1, 1, 100, 8, 16, 1, 576, host_block_tokens=12)  # not a multiple of 8

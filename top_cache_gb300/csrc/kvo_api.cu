@@ -29,6 +29,10 @@ struct kvo_handle {
   int G_max = 0;
   uint16_t* host_pool = nullptr;      // host address
   uint16_t* host_pool_dev = nullptr;  // device-visible address of the same memory
+  int32_t block_tokens = 0;           // > 0: paged pool of n_blocks blocks of this many rows
+  int64_t n_blocks = 0;
+  int32_t max_blocks = 0;             // block-table entries per unit
+  int32_t* blocks = nullptr;          // [U][max_blocks] block tables (device), -1 = unmapped
   size_t pool_map_bytes = 0;          // > 0: mmap'ed with transparent huge pages, registered
   size_t pool_huge_page = 0;
   uint16_t* idx = nullptr;           // bf16 indexer [U][stride][128]
@@ -158,7 +162,7 @@ void free_all(kvo_handle* h) {
   if (h->ev_join) cudaEventDestroy(h->ev_join);
   for (auto& ev : h->ev_group)
     if (ev) cudaEventDestroy(ev);
-  void* dev[] = {h->idx, h->idx8, h->idxs, h->q8, h->qscale, h->qdone, h->hot, h->cache_slots, h->slot_token, h->last_use, h->stamp, h->len,
+  void* dev[] = {h->idx, h->idx8, h->idxs, h->q8, h->qscale, h->qdone, h->blocks, h->hot, h->cache_slots, h->slot_token, h->last_use, h->stamp, h->len,
                  h->all_units, h->units_dev, h->off, h->gthr, h->spec, h->qn_prev, h->qn_cur,
                  h->tspec, h->fb, h->fb_any, h->tok_bits, h->order, h->order_par, h->seg_keys, h->seg_cnt, h->sel_pay,
                  h->miss_tok, h->miss_slot, h->miss_cnt, h->miss_off, h->done_ctr, h->err,
@@ -255,6 +259,17 @@ cudaError_t alloc_fused(kvo_handle* h) {
   if (e == cudaSuccess) e = cudaMemset(h->ctr, 0, 4 * 8);
   if (e == cudaSuccess) e = alloc_fused_segments(h);
   return e;
+}
+
+// Token -> host-pool row translation of the handle (contiguous or paged).
+kvo::HostRows host_rows_of(const kvo_handle* h) {
+  kvo::HostRows r{};
+  r.blocks = h->blocks;
+  r.block_tokens = h->block_tokens;
+  r.max_blocks = h->max_blocks;
+  r.n_blocks = h->n_blocks;
+  r.stride = h->stride;
+  return r;
 }
 
 // Resolve the unit list of a call: NULL = all; else validate and upload.
@@ -422,6 +437,7 @@ int fused_step(kvo_handle* h, const int32_t* du, const int32_t* units, int32_t n
   ga.C = h->C;
   ga.mode = KVO_GATHER_BULK;
   ga.stride = h->stride;
+  ga.rows = host_rows_of(h);
   ga.host_pool = h->host_pool_dev;
   ga.hot = h->hot;
   ga.miss_tok = h->miss_tok;
@@ -532,6 +548,9 @@ int kvo_create(const kvo_config* cfg, kvo_handle** out) {
   if (c.hot_capacity < c.topk || c.hot_capacity > (1 << 24))
     return fail(KVO_EINVAL, "hot_capacity must be in [topk, 2^24]");
   if (c.n_positions < 1 || c.n_positions > 8) return fail(KVO_EINVAL, "n_positions must be in [1, 8]");
+  if (c.host_block_tokens < 0 || c.host_block_tokens % 8 || (c.host_block_tokens == 0 && c.host_blocks != 0) ||
+      c.host_blocks < 0)
+    return fail(KVO_EINVAL, "host_block_tokens must be 0 or a positive multiple of 8 (host_blocks only with it)");
   const int cap = kvo::score_cap_for(c.n_positions, c.topk, c.idx_dtype == KVO_IDX_INT8);
   if (cap == 0) return fail(KVO_EINVAL, "topk too large for n_positions (shared-memory candidate buffer)");
   if (residency_smem_bytes(c.hot_capacity, c.n_positions, c.topk) > 224 * 1024)
@@ -559,7 +578,14 @@ int kvo_create(const kvo_config* cfg, kvo_handle** out) {
   h->len_host.assign((size_t)h->U, 0);
 
   const size_t U = (size_t)h->U, S = (size_t)h->stride, C = (size_t)h->C, PK = (size_t)h->P * h->k;
-  cudaError_t e = alloc_host_pool(h, U * S * h->R * 2);
+  size_t pool_rows = U * S;
+  if (c.host_block_tokens > 0) {
+    h->block_tokens = c.host_block_tokens;
+    h->max_blocks = (int32_t)((c.max_tokens + c.host_block_tokens - 1) / c.host_block_tokens);
+    h->n_blocks = c.host_blocks > 0 ? c.host_blocks : (int64_t)U * h->max_blocks;
+    pool_rows = (size_t)h->n_blocks * (size_t)h->block_tokens;
+  }
+  cudaError_t e = alloc_host_pool(h, pool_rows * h->R * 2);
   if (e != cudaSuccess) {
     delete h;
     return fail(KVO_ENOMEM, std::string("pinned host pool: ") + cudaGetErrorString(e));
@@ -578,6 +604,10 @@ int kvo_create(const kvo_config* cfg, kvo_handle** out) {
     e = dalloc(&h->idx, U * S * kvo::kDim);
   }
   if (e == cudaSuccess) e = dalloc(&h->hot, U * C * h->R);
+  if (e == cudaSuccess && h->block_tokens > 0) {
+    e = dalloc(&h->blocks, U * (size_t)h->max_blocks);
+    if (e == cudaSuccess) e = cudaMemset(h->blocks, 0xff, U * (size_t)h->max_blocks * 4);  // all unmapped
+  }
   if (e == cudaSuccess) e = dalloc(&h->cache_slots, U * S);
   if (e == cudaSuccess) e = dalloc(&h->slot_token, U * C);
   if (e == cudaSuccess) e = dalloc(&h->last_use, U * C);
@@ -675,7 +705,39 @@ int kvo_destroy(kvo_handle* h) {
 
 void* kvo_host_rows(kvo_handle* h, int32_t unit) {
   if (!h || unit < 0 || unit >= h->U) return nullptr;
+  if (h->block_tokens > 0) {
+    fail(KVO_EINVAL, "paged pool: use kvo_host_block");
+    return nullptr;
+  }
   return h->host_pool + (size_t)unit * h->stride * h->R;
+}
+
+void* kvo_host_block(kvo_handle* h, int64_t block) {
+  if (!h || h->block_tokens <= 0 || block < 0 || block >= h->n_blocks) {
+    fail(KVO_EINVAL, "not a block of a paged pool");
+    return nullptr;
+  }
+  return h->host_pool + (size_t)block * h->block_tokens * h->R;
+}
+
+int kvo_set_blocks(kvo_handle* h, int32_t unit, int32_t first_block, int32_t n_blocks, const int32_t* blocks,
+                   void* stream) {
+  if (!h) return fail(KVO_EINVAL, "handle is NULL");
+  if (h->block_tokens <= 0) return fail(KVO_EINVAL, "the host pool is not paged");
+  if (unit < 0 || unit >= h->U) return fail(KVO_ERANGE, "unit out of range");
+  if (n_blocks < 0 || first_block < 0 || (int64_t)first_block + n_blocks > h->max_blocks)
+    return fail(KVO_ERANGE, "block range past the table");
+  if (n_blocks == 0) return KVO_OK;
+  if (!blocks) return fail(KVO_EINVAL, "blocks is NULL");
+  for (int32_t j = 0; j < n_blocks; ++j)
+    if (blocks[j] < -1 || (int64_t)blocks[j] >= h->n_blocks) return fail(KVO_EINVAL, "block id out of range");
+  DeviceGuard guard(h->device);
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  // pageable source: the copy is staged before the call returns, so the caller may reuse the array
+  cudaError_t e = cudaMemcpyAsync(h->blocks + (size_t)unit * h->max_blocks + first_block, blocks,
+                                  (size_t)n_blocks * 4, cudaMemcpyHostToDevice, s);
+  if (e != cudaSuccess) return cuda_fail(e, "block table upload");
+  return KVO_OK;
 }
 
 int kvo_prefill(kvo_handle* h, int32_t unit, int64_t n_tokens, const void* idx_keys, void* stream) {
@@ -745,6 +807,7 @@ int kvo_append(kvo_handle* h, const int32_t* units, int32_t n_units, int32_t n_t
   a.stride = h->stride;
   a.rows = static_cast<const uint16_t*>(main_rows);
   a.keys = static_cast<const uint16_t*>(idx_keys);
+  a.hrows = host_rows_of(h);
   a.host_pool = h->host_pool_dev;
   a.idx = h->idx;
   a.idx8 = h->idx8;
@@ -881,6 +944,7 @@ int kvo_step(kvo_handle* h, const int32_t* units, int32_t n_units, const void* q
     ga.C = h->C;
     ga.mode = h->gather_mode;
     ga.stride = h->stride;
+    ga.rows = host_rows_of(h);
     ga.host_pool = h->host_pool_dev;
     ga.hot = h->hot;
     ga.miss_tok = h->miss_tok + ob;
@@ -1171,6 +1235,7 @@ int kvo_get_stats(kvo_handle* h, kvo_stats* out) {
   out->timeouts = (err & kvo::kErrTimeout) ? 1 : 0;
   out->rescored = d.rescored;
   out->fused_steps = h->fused_steps;
+  out->block_errors = d.block_errors;
   return KVO_OK;
 }
 

@@ -168,7 +168,7 @@ __device__ __forceinline__ void gather_warp(const FusedArgs& f, uint8_t* slice, 
     fence_proxy_async_smem();
   }
   __syncwarp();
-  unsigned long long rows = 0;
+  unsigned long long rows = 0, bad_rows = 0;
   bool failed = false;
   for (;;) {
     unsigned long long c = 0;
@@ -186,20 +186,27 @@ __device__ __forceinline__ void gather_warp(const FusedArgs& f, uint8_t* slice, 
     const int i = __ldcg(&f.chunk_unit[c]);
     const int r0 = __ldcg(&f.chunk_start[c]);
     const int cnt = __ldcg(&f.chunk_cnt[c]);
+    bool bad = false;
     if (lane < cnt) {
       const int64_t e = (int64_t)i * g.pk + r0 + lane;
       const int32_t t = __ldcg(&g.miss_tok[e]);
       const int32_t s = __ldcg(&g.miss_slot[e]);
       const int64_t u = g.units[i];
-      const uint16_t* src = g.host_pool + (u * g.stride + t) * g.row_elems;
+      const int64_t hr = host_row(g.rows, u, t);
       uint16_t* dst = g.hot + (u * g.C + s) * g.row_elems;
+      // a row of an unmapped block (paged pool) is copied onto itself, which
+      // leaves the hot row as it was
+      const uint16_t* src = hr < 0 ? dst : g.host_pool + hr * g.row_elems;
+      bad = hr < 0;
       abuf[lane] = make_ulonglong2(reinterpret_cast<uint64_t>(src), reinterpret_cast<uint64_t>(dst));
     }
     __syncwarp();
     if (lane == 0)
       for (int r = 0; r < cnt; ++r) pipe.push(abuf[r].x, abuf[r].y);
     __syncwarp();
-    rows += (unsigned long long)cnt;
+    const unsigned long long nb = __popc(__ballot_sync(kFull, bad));
+    rows += (unsigned long long)cnt - nb;
+    bad_rows += nb;
   }
   if (lane == 0) {
     pipe.drain();
@@ -208,6 +215,7 @@ __device__ __forceinline__ void gather_warp(const FusedArgs& f, uint8_t* slice, 
       atomicAdd(&g.stats->rows_h2d, rows);
       atomicAdd(&g.stats->bytes_h2d, rows * row_bytes);
     }
+    if (bad_rows && g.stats) atomicAdd(&g.stats->block_errors, bad_rows);
   }
   __syncwarp();
 }

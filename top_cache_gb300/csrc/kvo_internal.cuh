@@ -19,8 +19,24 @@ constexpr uint32_t kErrPlan = 2u;
 // Device-side counters (mirrors kvo_stats).
 struct DevStats {
   unsigned long long steps, unit_steps, capacity_errors, hits, misses, rows_h2d, bytes_h2d,
-      rows_d2h, bytes_d2h, timeouts, rescored;
+      rows_d2h, bytes_d2h, timeouts, rescored, block_errors;
 };
+
+// Host-pool row of token t of unit u: contiguous per unit (blocks == nullptr),
+// or row t mod B of physical block blocks[u][t / B] of a paged pool.  Returns
+// -1 for a row of an unmapped block (or a block id out of range).
+struct HostRows {
+  const int32_t* blocks;  // [U][max_blocks] block tables, or nullptr
+  int32_t block_tokens, max_blocks;
+  int64_t n_blocks;
+  int64_t stride;         // rows per unit when contiguous
+};
+__device__ __forceinline__ int64_t host_row(const HostRows& h, int64_t u, int64_t t) {
+  if (!h.blocks) return u * h.stride + t;
+  const int32_t b = __ldg(h.blocks + u * h.max_blocks + t / h.block_tokens);
+  if (b < 0 || (int64_t)b >= h.n_blocks) return -1;
+  return (int64_t)b * h.block_tokens + t % h.block_tokens;
+}
 
 // ---------------------------------------------------------------------------
 // Ordering keys.  A selection key is larger for a better candidate: the fp32
@@ -255,6 +271,7 @@ struct GatherArgs {
   const int32_t* units;
   int32_t n, row_elems, C, mode;
   int64_t stride;              // host pool rows per unit
+  HostRows rows;               // token -> host-pool row
   const uint16_t* host_pool;   // device-visible address of the pinned pool
   uint16_t* hot;               // [U][C][row_elems]
   const int32_t* miss_tok;
@@ -286,6 +303,7 @@ struct AppendArgs {
   int64_t stride;
   const uint16_t* rows;        // [n][n_tok][row_elems]
   const uint16_t* keys;        // [n][n_tok][128]
+  HostRows hrows;              // token -> host-pool row
   uint16_t* host_pool;         // device-visible address
   uint16_t* idx;               // [U][stride][128] bf16 indexer, or nullptr
   int8_t* idx8;                // [U][stride][128] int8 codes, or nullptr

@@ -87,10 +87,12 @@ __global__ void __launch_bounds__(kResThreads) residency_kernel(ResidencyArgs a)
 __global__ void __launch_bounds__(kGatherThreads) gather_ldg_kernel(GatherArgs a) {
   __shared__ int64_t src_off[kGatherRows];
   __shared__ int64_t dst_off[kGatherRows];
+  __shared__ unsigned int bad;  // rows of unmapped blocks (paged pool), left as they were
   const int tid = threadIdx.x;
   const int64_t R = a.miss_off[a.n];
   const int cpr = a.row_elems / 8;  // 16-byte chunks per row
   int64_t moved = 0;
+  if (tid == 0) bad = 0;
   for (int64_t b0 = (int64_t)blockIdx.x * kGatherRows; b0 < R; b0 += (int64_t)gridDim.x * kGatherRows) {
     const int nrow = (int)((R - b0) < kGatherRows ? (R - b0) : kGatherRows);
     if (tid < nrow) {
@@ -100,8 +102,10 @@ __global__ void __launch_bounds__(kGatherThreads) gather_ldg_kernel(GatherArgs a
       const int u = a.units[i];
       const int32_t t = a.miss_tok[(int64_t)i * a.pk + loc];
       const int32_t s = a.miss_slot[(int64_t)i * a.pk + loc];
-      src_off[tid] = ((int64_t)u * a.stride + t) * a.row_elems;
+      const int64_t hr = host_row(a.rows, u, t);
+      src_off[tid] = hr < 0 ? -1 : hr * a.row_elems;
       dst_off[tid] = ((int64_t)u * a.C + s) * a.row_elems;
+      if (hr < 0) atomicAdd(&bad, 1u);
     }
     __syncthreads();
     const int total = nrow * cpr;
@@ -113,7 +117,7 @@ __global__ void __launch_bounds__(kGatherThreads) gather_ldg_kernel(GatherArgs a
         const int q = q0 + x * kGatherThreads;
         if (q < total) {
           const int row = q / cpr, c = q - row * cpr;
-          v[x] = *reinterpret_cast<const uint4*>(a.host_pool + src_off[row] + c * 8);
+          if (src_off[row] >= 0) v[x] = *reinterpret_cast<const uint4*>(a.host_pool + src_off[row] + c * 8);
         }
       }
 #pragma unroll
@@ -121,16 +125,21 @@ __global__ void __launch_bounds__(kGatherThreads) gather_ldg_kernel(GatherArgs a
         const int q = q0 + x * kGatherThreads;
         if (q < total) {
           const int row = q / cpr, c = q - row * cpr;
-          *reinterpret_cast<uint4*>(a.hot + dst_off[row] + c * 8) = v[x];
+          if (src_off[row] >= 0) *reinterpret_cast<uint4*>(a.hot + dst_off[row] + c * 8) = v[x];
         }
       }
     }
     moved += nrow;
     __syncthreads();
   }
-  if (tid == 0 && moved && a.stats) {
-    atomicAdd(&a.stats->rows_h2d, (unsigned long long)moved);
-    atomicAdd(&a.stats->bytes_h2d, (unsigned long long)moved * a.row_elems * 2ull);
+  __syncthreads();
+  if (tid == 0 && a.stats) {
+    moved -= bad;
+    if (moved) {
+      atomicAdd(&a.stats->rows_h2d, (unsigned long long)moved);
+      atomicAdd(&a.stats->bytes_h2d, (unsigned long long)moved * a.row_elems * 2ull);
+    }
+    if (bad) atomicAdd(&a.stats->block_errors, (unsigned long long)bad);
   }
 }
 
@@ -159,22 +168,28 @@ __global__ void __launch_bounds__(kGatherThreads) gather_bulk_kernel(GatherArgs 
   const int64_t nw = (int64_t)gridDim.x * kWarps;
   // rows handled by this warp: r = gw + q * nw, q = 0, 1, ...
   const int64_t nq = R > gw ? (R - gw + nw - 1) / nw : 0;
-  auto addr = [&](int64_t q, const uint16_t** src, uint16_t** dst) {
+  // a row of an unmapped block (paged pool) is copied onto itself from the hot
+  // buffer, which leaves it as it was; *bad reports it
+  auto addr = [&](int64_t q, const uint16_t** src, uint16_t** dst, bool* bad) {
     const int64_t r = gw + q * nw;
     const int i = find_segment(a.miss_off, a.n, r);
     const int64_t loc = r - a.miss_off[i];
     const int u = a.units[i];
     const int32_t t = a.miss_tok[(int64_t)i * a.pk + loc];
     const int32_t s = a.miss_slot[(int64_t)i * a.pk + loc];
-    *src = a.host_pool + ((int64_t)u * a.stride + t) * a.row_elems;
+    const int64_t hr = host_row(a.rows, u, t);
     *dst = a.hot + ((int64_t)u * a.C + s) * a.row_elems;
+    *src = hr < 0 ? *dst : a.host_pool + hr * a.row_elems;
+    *bad = hr < 0;
   };
   bool timed_out = false;
+  unsigned long long n_bad = 0;
   const int64_t pro = nq < kBulkDepth ? nq : kBulkDepth;
   for (int64_t q = 0; q < pro; ++q) {
     const uint16_t* src;
     uint16_t* dst;
-    addr(q, &src, &dst);
+    bool bad;
+    addr(q, &src, &dst, &bad);
     mbar_arrive_expect_tx(&mybar[q], row_bytes);
     bulk_g2s(mybuf + q * slot_bytes, src, row_bytes, &mybar[q]);
   }
@@ -184,12 +199,14 @@ __global__ void __launch_bounds__(kGatherThreads) gather_bulk_kernel(GatherArgs 
     if (!mbar_wait(&mybar[d], parity, a.wait_ns)) timed_out = true;
     const uint16_t* src;
     uint16_t* dst;
-    addr(q, &src, &dst);
+    bool bad;
+    addr(q, &src, &dst, &bad);
+    n_bad += bad ? 1u : 0u;
     bulk_s2g(dst, mybuf + d * slot_bytes, row_bytes);
     bulk_commit();
     if (q + kBulkDepth < nq) {
       bulk_wait_read_all();  // staging slot d is free again
-      addr(q + kBulkDepth, &src, &dst);
+      addr(q + kBulkDepth, &src, &dst, &bad);
       mbar_arrive_expect_tx(&mybar[d], row_bytes);
       bulk_g2s(mybuf + d * slot_bytes, src, row_bytes, &mybar[d]);
     }
@@ -197,8 +214,11 @@ __global__ void __launch_bounds__(kGatherThreads) gather_bulk_kernel(GatherArgs 
   bulk_wait_all();
   if (timed_out) atomicOr(a.err, kErrTimeout);
   if (nq && a.stats) {
-    atomicAdd(&a.stats->rows_h2d, (unsigned long long)nq);
-    atomicAdd(&a.stats->bytes_h2d, (unsigned long long)nq * row_bytes);
+    if ((unsigned long long)nq > n_bad) {
+      atomicAdd(&a.stats->rows_h2d, (unsigned long long)nq - n_bad);
+      atomicAdd(&a.stats->bytes_h2d, ((unsigned long long)nq - n_bad) * row_bytes);
+    }
+    if (n_bad) atomicAdd(&a.stats->block_errors, n_bad);
   }
 }
 
@@ -207,17 +227,24 @@ __global__ void __launch_bounds__(kGatherThreads) gather_bulk_kernel(GatherArgs 
 // ---------------------------------------------------------------------------
 __global__ void __launch_bounds__(256) append_kernel(AppendArgs a) {
   __shared__ int32_t base;
+  __shared__ unsigned int bad;  // rows of unmapped blocks (paged pool), not written
   const int i = blockIdx.x, tid = threadIdx.x;
   const int u = a.units[i];
-  if (tid == 0) base = a.len[u];
+  if (tid == 0) {
+    base = a.len[u];
+    bad = 0;
+  }
   __syncthreads();
   const int cpr = a.row_elems / 8;
   const int64_t nrow_chunks = (int64_t)a.n_tok * cpr;
   const uint4* src = reinterpret_cast<const uint4*>(a.rows + (int64_t)i * a.n_tok * a.row_elems);
   for (int64_t q = tid; q < nrow_chunks; q += blockDim.x) {
     const int64_t tj = q / cpr, c = q - tj * cpr;
-    *reinterpret_cast<uint4*>(a.host_pool + ((int64_t)u * a.stride + base + tj) * a.row_elems + c * 8) =
-        src[q];
+    const int64_t hr = host_row(a.hrows, u, base + tj);
+    if (hr >= 0)
+      *reinterpret_cast<uint4*>(a.host_pool + hr * a.row_elems + c * 8) = src[q];
+    else if (c == 0)
+      atomicAdd(&bad, 1u);
   }
   if (a.idx8) {
     // int8 indexer: each new key rotated and quantized by one warp
@@ -238,8 +265,10 @@ __global__ void __launch_bounds__(256) append_kernel(AppendArgs a) {
   if (tid == 0) {
     a.len[u] = base + a.n_tok;
     if (a.stats) {
-      atomicAdd(&a.stats->rows_d2h, (unsigned long long)a.n_tok);
-      atomicAdd(&a.stats->bytes_d2h, (unsigned long long)a.n_tok * a.row_elems * 2ull);
+      const unsigned long long ok = (unsigned long long)a.n_tok - bad;
+      if (bad) atomicAdd(&a.stats->block_errors, (unsigned long long)bad);
+      atomicAdd(&a.stats->rows_d2h, ok);
+      atomicAdd(&a.stats->bytes_d2h, ok * a.row_elems * 2ull);
     }
   }
 }

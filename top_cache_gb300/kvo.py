@@ -43,7 +43,7 @@ KVO_GATHER_BULK = 1
 EXPORTED = ("kvo_create", "kvo_destroy", "kvo_host_rows", "kvo_prefill", "kvo_append", "kvo_step",
             "kvo_select_workspace_size", "kvo_select", "kvo_reset", "kvo_profile_read",
             "kvo_set_option", "kvo_get_option", "kvo_get_stats", "kvo_export_state", "kvo_select_noalloc",
-            "kvo_attend", "kvo_lw_create", "kvo_lw_destroy", "kvo_lw_plan", "kvo_lw_host_rows",
+            "kvo_attend", "kvo_set_blocks", "kvo_host_block", "kvo_lw_create", "kvo_lw_destroy", "kvo_lw_plan", "kvo_lw_host_rows",
             "kvo_lw_set_length", "kvo_lw_begin", "kvo_lw_layer", "kvo_lw_layer_done", "kvo_lw_end",
             "kvo_lw_stats", "kvo_last_error")
 
@@ -53,7 +53,8 @@ class KvoConfig(ctypes.Structure):
                 ("max_tokens", ctypes.c_int64), ("idx_dim", ctypes.c_int32),
                 ("row_elems", ctypes.c_int32), ("topk", ctypes.c_int32),
                 ("hot_capacity", ctypes.c_int32), ("n_positions", ctypes.c_int32),
-                ("device", ctypes.c_int32), ("idx_dtype", ctypes.c_int32)]
+                ("device", ctypes.c_int32), ("idx_dtype", ctypes.c_int32),
+                ("host_block_tokens", ctypes.c_int32), ("host_blocks", ctypes.c_int64)]
 
 
 class KvoLwConfig(ctypes.Structure):
@@ -66,7 +67,8 @@ class KvoLwConfig(ctypes.Structure):
 class KvoStats(ctypes.Structure):
     _fields_ = [(n, ctypes.c_uint64) for n in
                 ("steps", "unit_steps", "capacity_errors", "hits", "misses", "rows_h2d",
-                 "bytes_h2d", "rows_d2h", "bytes_d2h", "timeouts", "rescored", "fused_steps")]
+                 "bytes_h2d", "rows_d2h", "bytes_d2h", "timeouts", "rescored", "fused_steps",
+                 "block_errors")]
 
 
 class KvoError(RuntimeError):
@@ -128,6 +130,10 @@ def lib():
             L.kvo_export_state.argtypes = [vp, i32, vp, vp, vp, vp, vp, vp]
             L.kvo_last_error.restype = ctypes.c_char_p
             L.kvo_last_error.argtypes = []
+            L.kvo_set_blocks.restype = ctypes.c_int
+            L.kvo_set_blocks.argtypes = [vp, i32, i32, i32, vp, vp]
+            L.kvo_host_block.restype = vp
+            L.kvo_host_block.argtypes = [vp, i64]
             L.kvo_lw_create.restype = ctypes.c_int
             L.kvo_lw_create.argtypes = [ctypes.POINTER(KvoLwConfig), ctypes.POINTER(vp)]
             L.kvo_lw_destroy.restype = ctypes.c_int
@@ -186,9 +192,10 @@ def _units(units):
 
 
 def kvo_create(n_requests, n_layers, max_tokens, topk, hot_capacity, n_positions=1,
-               row_elems=576, idx_dim=128, device=0, idx_dtype=KVO_IDX_BF16):
+               row_elems=576, idx_dim=128, device=0, idx_dtype=KVO_IDX_BF16, host_block_tokens=0,
+               host_blocks=0):
     cfg = KvoConfig(n_requests, n_layers, max_tokens, idx_dim, row_elems, topk, hot_capacity,
-                    n_positions, device, idx_dtype)
+                    n_positions, device, idx_dtype, host_block_tokens, host_blocks)
     h = ctypes.c_void_p()
     _check(lib().kvo_create(ctypes.byref(cfg), ctypes.byref(h)))
     return h.value
@@ -301,15 +308,16 @@ class Kvo:
     """A handle plus output buffers for all units (plumbing around the C ABI)."""
 
     def __init__(self, n_requests, n_layers, max_tokens, topk, hot_capacity, n_positions=1,
-                 row_elems=576, device=0, idx_dtype=KVO_IDX_BF16):
+                 row_elems=576, device=0, idx_dtype=KVO_IDX_BF16, host_block_tokens=0, host_blocks=0):
         import torch
         self.n_requests, self.n_layers = n_requests, n_layers
+        self.block_tokens = host_block_tokens
         self.U = n_requests * n_layers
         self.max_tokens, self.topk, self.C = max_tokens, topk, hot_capacity
         self.P, self.R, self.device = n_positions, row_elems, device
         self.idx_dtype = idx_dtype
         self.h = kvo_create(n_requests, n_layers, max_tokens, topk, hot_capacity, n_positions,
-                            row_elems, 128, device, idx_dtype)
+                            row_elems, 128, device, idx_dtype, host_block_tokens, host_blocks)
         dev = torch.device("cuda", device)
         shape = (self.U, self.P, self.topk)
         self.tokens = torch.empty(shape, dtype=torch.int32, device=dev)
@@ -331,6 +339,19 @@ class Kvo:
 
     def host_rows(self, unit):
         return kvo_host_rows(self.h, unit)
+
+    def host_block(self, block):
+        """Host address of physical block `block` of a paged pool ([B][row_elems] bf16)."""
+        p = lib().kvo_host_block(self.h, block)
+        if not p:
+            raise KvoError(KVO_EINVAL, lib().kvo_last_error().decode())
+        return p
+
+    def set_blocks(self, unit, blocks, first_block=0, stream=None):
+        """Entries first_block.. of unit's block table (-1 = unmapped)."""
+        arr = np.ascontiguousarray(blocks, dtype=np.int32)
+        return _check(lib().kvo_set_blocks(self.h, unit, first_block, len(arr), arr.ctypes.data,
+                                           _stream(stream)))
 
     def prefill(self, unit, n_tokens, idx_keys, stream=None):
         return kvo_prefill(self.h, unit, n_tokens, idx_keys, stream)
