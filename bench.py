@@ -250,7 +250,7 @@ def make_workload(args):
     return wl
 
 
-def prepare(wl, rank, device, log, idx="bf16"):
+def prepare(wl, rank, device, log, idx="bf16", block_tokens=0):
     """Handle with the prefilled context, plus per-sequence-step inputs on the device."""
     import numpy as np
     import torch
@@ -263,10 +263,22 @@ def prepare(wl, rank, device, log, idx="bf16"):
     tmax = wl.max_tokens(S)
     t0 = time.time()
     kv = K.Kvo(wl.n_requests, wl.n_layers, tmax, wl.topk, wl.hot_capacity, wl.n_pos, wl.row_elems,
-               device=device.index or 0, idx_dtype=K.KVO_IDX_INT8 if idx == "int8" else K.KVO_IDX_BF16)
-    unit_stride = (kv.host_rows(1) - kv.host_rows(0)) // 2 if U > 1 else 0
-    W.token_rows_into(kv.host_rows(0), unit_stride, wl.seed, W.KIND_ROWS, units, 0, wl.context,
-                      wl.row_elems)
+               device=device.index or 0, idx_dtype=K.KVO_IDX_INT8 if idx == "int8" else K.KVO_IDX_BF16,
+               host_block_tokens=block_tokens)
+    if block_tokens:
+        # paged pool: every unit's blocks scattered through the pool (seeded permutation)
+        mb = -(-tmax // block_tokens)
+        tables = np.random.default_rng(wl.seed).permutation(U * mb).astype(np.int32).reshape(U, mb)
+        for u in range(U):
+            kv.set_blocks(u, tables[u])
+            for j in range(-(-wl.context // block_tokens)):
+                t = j * block_tokens
+                W.token_rows_into(kv.host_block(int(tables[u][j])), 0, wl.seed, W.KIND_ROWS, [units[u]], t,
+                                  min(block_tokens, wl.context - t), wl.row_elems)
+    else:
+        unit_stride = (kv.host_rows(1) - kv.host_rows(0)) // 2 if U > 1 else 0
+        W.token_rows_into(kv.host_rows(0), unit_stride, wl.seed, W.KIND_ROWS, units, 0, wl.context,
+                          wl.row_elems)
     chunk = max(1, (256 << 20) // max(1, wl.context * 256))
     for b in range(0, U, chunk):
         ids = list(range(b, min(U, b + chunk)))
@@ -471,7 +483,7 @@ def run_kvo(args, log):
     wl = make_workload(args)
     hbm_peak, hbm_src = load_peaks()
     link = measure_host_link(torch, device)
-    kv, inp, units = prepare(wl, rank, device, log, args.idx)
+    kv, inp, units = prepare(wl, rank, device, log, args.idx, args.host_block_tokens)
     U, P, k, R = len(units), wl.n_pos, wl.topk, wl.row_elems
     kv.set_option(K.KVO_OPT_GATHER_MODE, K.KVO_GATHER_BULK if args.gather == "bulk" else K.KVO_GATHER_LDG)
     kv.set_option(K.KVO_OPT_GROUPS, args.groups)
@@ -631,7 +643,9 @@ def run_kvo(args, log):
                    "hot_capacity": wl.hot_capacity, "drift": wl.drift,
                    "steps_per_sequence": wl.steps, "path": path, "indexer": args.idx,
                    "host_pool_page": kv.get_option(K.KVO_OPT_HOST_HUGE_PAGE) or "base",
-                   "host_pool_huge_backed": huge_backed_fraction(kv.host_rows(0)),
+                   "host_pool_huge_backed": huge_backed_fraction(
+                       kv.host_block(0) if args.host_block_tokens else kv.host_rows(0)),
+                   "host_block_tokens": args.host_block_tokens or None,
                    "gather": "bulk" if path == "fused" else args.gather, "groups": args.groups,
                    "parallelism": "replicas%d" % world,
                    "l2": "inputs larger than L2: %.2f GB of indexer keys read per step"
@@ -884,6 +898,8 @@ def main(argv=None):
     ap.add_argument("--lw-passes", type=int, default=3)
     ap.add_argument("--lw-window-us", type=float, default=0.0,
                     help="stand-in compute per layer (0 = the layer's load time at the measured peak)")
+    ap.add_argument("--host-block-tokens", type=int, default=0,
+                    help="paged host pool: rows per block, blocks scattered by a seeded permutation (0 = per-unit rows)")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-units", type=int, default=32)
