@@ -432,6 +432,16 @@ int kvo_lw_end(kvo_lw* lw, void* stream);
 /* kvo_lw_stats: bytes copied host -> device and device -> host so far. */
 int kvo_lw_stats(kvo_lw* lw, uint64_t* bytes_h2d, uint64_t* bytes_d2h);
 
+/*
+ * kvo_wait_selftest: runs, on `device`, one thread through the two bounded
+ * waits every kernel of the library relies on (a spin on a global flag and an
+ * mbarrier phase wait), each on a condition nothing satisfies and limited to
+ * limit_ns (1 us .. 10 s).  Both must give up; the call returns KVO_ETIMEOUT
+ * when they did, with the time waited in *waited_ns (nullable), and leaves
+ * the device usable.  Synchronous.  Errors: KVO_EINVAL (limit), KVO_ECUDA.
+ */
+int kvo_wait_selftest(int32_t device, int64_t limit_ns, int64_t* waited_ns);
+
 /* kvo_last_error: message of the last failing call on this thread ("" if none). */
 const char* kvo_last_error(void);
 

@@ -1195,6 +1195,19 @@ int kvo_attend(kvo_handle* h, const int32_t* units, int32_t n_units, const void*
   return KVO_OK;
 }
 
+int kvo_wait_selftest(int32_t device, int64_t limit_ns, int64_t* waited_ns) {
+  if (limit_ns < 1000 || limit_ns > 10000000000ll) return fail(KVO_EINVAL, "limit_ns must be in [1 us, 10 s]");
+  int ndev = 0;
+  if (cudaGetDeviceCount(&ndev) != cudaSuccess || device < 0 || device >= ndev) return fail(KVO_ECUDA, "no such device");
+  DeviceGuard guard(device);
+  unsigned long long out[3] = {0, 0, 0};
+  cudaError_t e = kvo::run_wait_selftest((uint64_t)limit_ns, out);
+  if (e != cudaSuccess) return cuda_fail(e, "wait self-test");
+  if (waited_ns) *waited_ns = (int64_t)out[2];
+  if (out[0] == 1 && out[1] == 1) return fail(KVO_ETIMEOUT, "both bounded waits expired, as designed");
+  return fail(KVO_ECUDA, "a wait on a condition nothing satisfies reported success");
+}
+
 int kvo_profile_read(kvo_handle* h, double* ms, uint64_t* launches, int32_t n_kinds) {
   if (!h || !ms || !launches || n_kinds < 0) return fail(KVO_EINVAL, "NULL argument");
   DeviceGuard guard(h->device);

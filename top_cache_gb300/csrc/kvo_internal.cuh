@@ -378,6 +378,7 @@ cudaError_t launch_residency(const ResidencyArgs& a, cudaStream_t s);
 cudaError_t launch_gather(const GatherArgs& a, int n_sm, cudaStream_t s);
 cudaError_t launch_append(const AppendArgs& a, cudaStream_t s);
 cudaError_t launch_attend(const AttendArgs& a, cudaStream_t s);
+cudaError_t run_wait_selftest(uint64_t limit_ns, unsigned long long* host_out);  // out[3]
 // host helpers shared by the entry points (kvo_api.cu)
 int set_error(int code, const char* msg);
 int set_cuda_error(cudaError_t e, const char* what);

@@ -43,7 +43,7 @@ KVO_GATHER_BULK = 1
 EXPORTED = ("kvo_create", "kvo_destroy", "kvo_host_rows", "kvo_prefill", "kvo_append", "kvo_step",
             "kvo_select_workspace_size", "kvo_select", "kvo_reset", "kvo_profile_read",
             "kvo_set_option", "kvo_get_option", "kvo_get_stats", "kvo_export_state", "kvo_select_noalloc",
-            "kvo_attend", "kvo_set_blocks", "kvo_host_block", "kvo_lw_create", "kvo_lw_destroy", "kvo_lw_plan", "kvo_lw_host_rows",
+            "kvo_attend", "kvo_set_blocks", "kvo_host_block", "kvo_wait_selftest", "kvo_lw_create", "kvo_lw_destroy", "kvo_lw_plan", "kvo_lw_host_rows",
             "kvo_lw_set_length", "kvo_lw_begin", "kvo_lw_layer", "kvo_lw_layer_done", "kvo_lw_end",
             "kvo_lw_stats", "kvo_last_error")
 
@@ -130,6 +130,8 @@ def lib():
             L.kvo_export_state.argtypes = [vp, i32, vp, vp, vp, vp, vp, vp]
             L.kvo_last_error.restype = ctypes.c_char_p
             L.kvo_last_error.argtypes = []
+            L.kvo_wait_selftest.restype = ctypes.c_int
+            L.kvo_wait_selftest.argtypes = [i32, i64, ctypes.POINTER(ctypes.c_int64)]
             L.kvo_set_blocks.restype = ctypes.c_int
             L.kvo_set_blocks.argtypes = [vp, i32, i32, i32, vp, vp]
             L.kvo_host_block.restype = vp
@@ -474,3 +476,10 @@ class Layerwise:
         a, b = ctypes.c_uint64(), ctypes.c_uint64()
         _check(lib().kvo_lw_stats(self.h, ctypes.byref(a), ctypes.byref(b)))
         return {"bytes_h2d": int(a.value), "bytes_d2h": int(b.value)}
+
+
+def kvo_wait_selftest(device, limit_ns):
+    """(return code, ns waited) of the bounded-wait self-test (KVO_ETIMEOUT expected)."""
+    w = ctypes.c_int64()
+    rc = lib().kvo_wait_selftest(device, int(limit_ns), ctypes.byref(w))
+    return rc, int(w.value)
