@@ -425,7 +425,8 @@ def run_layerwise(args, link, device, torch, log):
                 lw.layer_done(l)
             lw.end()
 
-        log("[bench] layerwise set-up %.1f s (host pool %.2f GB)" % (time.time() - t0, N * T * row * 2 / 1e9))
+        huge_frac = huge_backed_fraction(lw.host_rows_ptr(0))
+        log("layerwise set-up %.1f s (host pool %.2f GB)" % (time.time() - t0, N * T * row * 2 / 1e9))
         one_pass(L0)  # warm-up pass
         torch.cuda.synchronize(device)
         st0 = lw.stats()
@@ -467,6 +468,7 @@ def run_layerwise(args, link, device, torch, log):
                      "t_roofline_ms": round(t_roof, 4), "frac": round(t_roof / t_pass, 4),
                      "peaks_gbs": {"h2d": round(link["h2d"], 1), "d2h": round(link["d2h"], 1)}},
         "device_buffer_bytes": 4 * T * row * 2, "host_pool_bytes": N * T * row * 2,
+        "host_pool_huge_backed": huge_frac,
     }
 
 
