@@ -135,13 +135,22 @@ __device__ __forceinline__ void tree16(T (&a)[V]) {
   tree_level<(V >= 8 ? V / 8 : 1), V>(a, 1);
 }
 
+// The same tree over groups of 8 lanes (levels j^4, j^2, j^1), for sums whose
+// order is free (exact integer sums of the int8 indexer).
+template <int V, class T>
+__device__ __forceinline__ void tree8(T (&a)[V]) {
+  tree_level<V, V>(a, 4);
+  tree_level<(V >= 2 ? V / 2 : 1), V>(a, 2);
+  tree_level<(V >= 4 ? V / 4 : 1), V>(a, 1);
+}
+
 // X_l: the lane's slot permutation (slot i holds pair i ^ X_l), which is also
 // the pair held in slot 0 after tree16.
-template <int V>
+template <int V, int G = 16>
 __device__ __forceinline__ int tree_perm(int lane) {
   int x = 0, cur = V;
 #pragma unroll
-  for (int m = 8; m >= 1; m >>= 1) {
+  for (int m = G / 2; m >= 1; m >>= 1) {
     if (cur > 1) {
       if (lane & m) x += cur / 2;
       cur /= 2;
@@ -149,10 +158,11 @@ __device__ __forceinline__ int tree_perm(int lane) {
   }
   return x;
 }
-// After tree16 with V < 16 several lanes hold the same sum; one reports it.
-template <int V>
+// After the tree over G lanes with V < G several lanes hold the same sum; one
+// reports it.
+template <int V, int G = 16>
 __device__ __forceinline__ bool tree_owner(int lane) {
-  constexpr int dup = V >= 16 ? 0 : (16 / V - 1);
+  constexpr int dup = V >= G ? 0 : (G / V - 1);
   return (lane & dup) == 0;
 }
 
@@ -474,13 +484,16 @@ struct ScoreSmem {
 // ---------------------------------------------------------------------------
 // Per-lane scoring machinery of one consumer warp (16 warps x 8 keys = one tile)
 // ---------------------------------------------------------------------------
-// Lane layout of a consumer warp: a half-warp scores 4 keys, lane j holds
-// elements 8j .. 8j+7 of every query; after the 16-lane tree each lane keeps
-// VL (token, position) results.  Shared by both key formats.
-template <int PP>
+// Lane layout of a consumer warp: groups of G lanes (G = 16: a half-warp
+// scores 4 keys, lane j holds elements 8j .. 8j+7 of every query; G = 8: a
+// quarter-warp scores 2 keys, lane j holds elements 16j .. 16j+15); after the
+// tree over the group each lane keeps VL (token, position) results.  A warp
+// scores 8 keys either way.
+template <int PP, int G = 16>
 struct ScorerLanes {
-  static constexpr int V = 4 * PP;                 // (token, position) pairs per lane
-  static constexpr int VL = V >= 16 ? V / 16 : 1;  // values left per lane after the tree
+  static constexpr int KPG = G / 4;                 // keys per group: 8 keys per warp / (32 / G) groups
+  static constexpr int V = KPG * PP;                // (token, position) pairs per lane
+  static constexpr int VL = V >= G ? V / G : 1;     // values left per lane after the tree
   static constexpr int LPP = PP == 1 ? 0 : PP == 2 ? 1 : PP == 4 ? 2 : 3;
 
   int lane, j, X, px, tx, rowbase;
@@ -494,17 +507,17 @@ struct ScorerLanes {
   // lanes reporting this lane's position.
   __device__ __forceinline__ void init_lanes(int warp, int lane_) {
     lane = lane_;
-    const int h = lane >> 4;
-    j = lane & 15;
-    X = tree_perm<V>(lane);
+    const int h = lane / G;
+    j = lane & (G - 1);
+    X = tree_perm<V, G>(lane);
     tx = X >> LPP;
     px = X & (PP - 1);
-    owner = tree_owner<V>(lane);
-    rowbase = warp * 8 + h * 4;
+    owner = tree_owner<V, G>(lane);
+    rowbase = warp * 8 + h * KPG;
 #pragma unroll
     for (int r = 0; r < VL; ++r) {
       const int cmb = r ^ X;
-      rrow[r] = warp * 8 + h * 4 + (cmb >> LPP);
+      rrow[r] = warp * 8 + h * KPG + (cmb >> LPP);
       rpos[r] = cmb & (PP - 1);
       lead[r] = 0;
       same[r] = 0;
@@ -643,10 +656,13 @@ struct Scorer : ScorerLanes<PP> {
 // int8 keys (reading R12): exact int32 dot products of the codes (4-byte dot
 // instructions, tree of integer sums), then (((float)dot * s_q) * s_k) / 128.
 template <int PP>
-struct ScorerI8 : ScorerLanes<PP> {
-  using B = ScorerLanes<PP>;
-  using B::V; using B::VL; using B::j; using B::px; using B::tx; using B::rowbase; using B::rrow; using B::rpos;
-  int qi[PP][2];    // this lane's 8 query codes per slot position
+struct ScorerI8 : ScorerLanes<PP, 8> {
+  // Groups of 8 lanes: the integer dot products are exact, so their order is
+  // free, and 8 lanes per key halve the tree's shuffles against 16.
+  using B = ScorerLanes<PP, 8>;
+  using B::V; using B::VL; using B::KPG; using B::j; using B::px; using B::tx; using B::rowbase; using B::rrow;
+  using B::rpos;
+  int qi[PP][4];    // this lane's 16 query codes per slot position
   float qs[VL];     // query scale of each result's position (fp16, read as fp32)
 
   __device__ __forceinline__ void init(int warp, int lane_) { B::init_lanes(warp, lane_); }
@@ -656,11 +672,13 @@ struct ScorerI8 : ScorerLanes<PP> {
     for (int p = 0; p < PP; ++p) {
       const int pq = p ^ px;
       if (pq < P) {
-        const uint2 v = *reinterpret_cast<const uint2*>(a.q8 + (i * P + pq) * kDim + j * 8);
+        const uint4 v = *reinterpret_cast<const uint4*>(a.q8 + (i * P + pq) * kDim + j * 16);
         qi[p][0] = (int)v.x;
         qi[p][1] = (int)v.y;
+        qi[p][2] = (int)v.z;
+        qi[p][3] = (int)v.w;
       } else {
-        qi[p][0] = qi[p][1] = 0;
+        qi[p][0] = qi[p][1] = qi[p][2] = qi[p][3] = 0;
       }
     }
 #pragma unroll
@@ -687,17 +705,19 @@ struct ScorerI8 : ScorerLanes<PP> {
                                              Release release, Clamp clamp) {
     int32_t ai[V];
 #pragma unroll
-    for (int tau = 0; tau < 4; ++tau) {
-      const uint2 kv = *reinterpret_cast<const uint2*>(codes + clamp(rowbase + (tau ^ tx)) * kDim + j * 8);
+    for (int tau = 0; tau < KPG; ++tau) {
+      const uint4 kv = *reinterpret_cast<const uint4*>(codes + clamp(rowbase + (tau ^ tx)) * kDim + j * 16);
 #pragma unroll
-      for (int p = 0; p < PP; ++p) ai[tau * PP + p] = __dp4a((int)kv.x, qi[p][0], __dp4a((int)kv.y, qi[p][1], 0));
+      for (int p = 0; p < PP; ++p)
+        ai[tau * PP + p] = __dp4a((int)kv.x, qi[p][0],
+                                  __dp4a((int)kv.y, qi[p][1], __dp4a((int)kv.z, qi[p][2], __dp4a((int)kv.w, qi[p][3], 0))));
     }
     // the results' key scales, before the stage may be refilled
     float ks[VL];
 #pragma unroll
     for (int r = 0; r < VL; ++r) ks[r] = __half2float(__ushort_as_half(scales[clamp(rrow[r])]));
     release();
-    tree16<V>(ai);
+    tree8<V>(ai);
 #pragma unroll
     for (int r = 0; r < VL; ++r) acc[r] = ((((float)ai[r]) * qs[r]) * ks[r]) * 0.0078125f;
   }

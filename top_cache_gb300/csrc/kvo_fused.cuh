@@ -357,7 +357,7 @@ __device__ __forceinline__ void rescan_unit(const SelectArgs& a, const FusedSmem
   int ti = 0;
   for (int64_t t = 0; t < L; t += kTile, ++ti) {
     const int nt = (int)((L - t) < kTile ? (L - t) : kTile);
-    float acc[ScorerLanes<PP>::V];
+    float acc[SC::V];
     sc.score_global(a, u, t, nt, acc);
     sc.filter(acc, t, nt, L, P, fs.sm.thr, fs.sm.cnt, fs.sm.cand, cap);
     if (t + kTile < L && (ti + 1) % kCheckTiles == 0) piece_check(fs.sm, P, k, cap, gth, ctid);
@@ -458,7 +458,7 @@ __device__ __forceinline__ void fused_consumers(const FusedArgs& f, const FusedS
   const int P = a.P, k = a.k, cap = a.cap;
   typename ScorerFor<PP, KF>::type sc;
   sc.init(warp, lane);
-  constexpr int V = ScorerLanes<PP>::V;
+  constexpr int V = ScorerFor<PP, KF>::type::V;
   uint32_t seq = 0;
   bool stalled = false;  // a wait of this thread expired: later tiles are not waited for
   for (uint32_t q = 0;; ++q) {

@@ -138,7 +138,7 @@ __global__ void __launch_bounds__(kScoreThreads, 1) score_kernel(SelectArgs a) {
   const int P = a.P, k = a.k, cap = a.cap;
   typename ScorerFor<PP, KF>::type sc;
   sc.init(warp, lane);
-  constexpr int V = ScorerLanes<PP>::V;
+  constexpr int V = ScorerFor<PP, KF>::type::V;
 
   PieceIter it;
   it.begin(a.off, a.n, g0, g1, only);
