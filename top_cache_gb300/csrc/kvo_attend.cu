@@ -11,25 +11,32 @@
 //   lse_h = log sum_i exp(s_i).
 //
 // One CTA per (unit, position, group of 128 heads, half of the 512 value
-// columns); 256 threads.  The list is cut into blocks of 128 rows, so that
-// every S MMA has N = 128 (issuing a tcgen05.mma costs tens of cycles; a
-// smaller N leaves the tensor pipe idle).  The query tile (128 x 576 bf16,
-// 147 KB) stays in shared memory; a block's rows stream through a ring of
-// five 16 KB entries, one 64-column slab of the block each, this CTA's four
-// value slabs last:
-//   warps 0-1  copy the query tile, then every slab of every block with
+// columns); 384 threads.  The list is cut into blocks of 128 rows.  Issuing a
+// tcgen05.mma from one thread costs about a hundred cycles whatever N is up to
+// 128, so every MMA is made as wide as the operands allow: S MMAs have N = 128
+// (a block), and one block's P V is eight MMAs of N = 256 (this CTA's value
+// columns).  The query tile (128 x 576 bf16) stays on chip: its first four
+// 64-column slabs in TMEM (the A operand of their S MMAs), the other five in
+// shared memory.  That leaves room for a ring of nine 16 KB entries, one per
+// slab of a block (entry t always holds slab t of the current block), this
+// CTA's four value slabs last and side by side, so that they form the N = 256
+// operand of P V, while the next block's other five slabs stream in:
+//   warps 0-1  copy query slabs 4-8, then every slab of every block with
 //              16-byte cp.async into the 128-byte-swizzled K-major layout the
 //              MMA reads;
 //   warp 2     holds 512 TMEM columns; lane 0 issues every tcgen05.mma:
-//              S = Q K^T (M 128, N 128, K 64 per slab) into one of two S
-//              buffers; once P is ready, O[:, 64v..] += P V_v (M 128, N 64,
-//              K 128) for each value slab v, P read from TMEM;
-//   warps 4-7  online softmax, one head (TMEM lane) per thread: S from TMEM,
-//              exp2 against a running maximum that moves only when it grows by
-//              more than 2^8 (O is then rescaled in TMEM), P rounded to bf16 and
-//              written back over the S buffer it came from, l summed from the
-//              rounded weights so that out is their exact weighted mean; at the
-//              end O / l in bf16 and lse.
+//              S = Q K^T (M 128, N 128, K 64 per slab) into the S buffer;
+//              once P is ready, O += P V (M 128, N 256, K 128), P read from
+//              TMEM, before the next block's S (S is single-buffered);
+//   warps 4-11 put query slabs 0-3 into TMEM, then run the online softmax: a
+//              head (TMEM lane) per thread pair, warp 4+q taking the first 64
+//              rows of a block and warp 8+q the other 64 for heads 32q..;
+//              each reads its scores once, the pair agrees on the block
+//              maximum through TMEM and a named barrier, the running maximum
+//              moves only when it grows by more than 2^8 (O is then rescaled
+//              in TMEM), P is rounded to bf16 and written back over the first
+//              64 columns of S, and l sums the rounded weights so that out is
+//              their exact weighted mean; at the end O / l in bf16 and lse.
 // A ring entry is freed by the MMAs that read it last: the S MMAs for the five
 // slabs only the scores use, the P V MMAs for the value slabs.
 // Every mbarrier wait is bounded: on expiry the CTA sets kErrTimeout in the
@@ -47,22 +54,26 @@ constexpr int kM = 128;                   // heads per CTA: M of the MMAs
 constexpr int kBlk = 128;                 // rows per block: N of S, K of P V
 constexpr int kSlabs = kRow / 64;         // 128-byte slabs of a row
 constexpr int kVSlabs = 4;                // value slabs of this CTA's half
-constexpr int kRing = 5;                  // ring entries (one slab of a block each)
+constexpr int kRing = kSlabs;             // ring entries: entry t holds slab t of a block
+constexpr int kQTmemSlabs = 4;            // query slabs 0..3 live in TMEM, 4..8 in shared memory
 constexpr int kHalfCols = kVal / 2;       // value columns per CTA
-constexpr int kAttThreads = 256;
+constexpr int kAttThreads = 384;
+constexpr int kSoftThreads = 256;        // warps 4-11
 constexpr int kProducers = 64;            // warps 0-1
 constexpr uint32_t kQSlab = kM * 128;     // one slab of the query tile
 constexpr uint32_t kEntry = kBlk * 128;   // one slab of a row block
-constexpr uint32_t kQOff = 0;
-constexpr uint32_t kROff = kSlabs * kQSlab;
+constexpr uint32_t kQOff = 0;             // query slabs kQTmemSlabs..8
+constexpr uint32_t kROff = (kSlabs - kQTmemSlabs) * kQSlab;
 constexpr uint32_t kBarOff = kROff + kRing * kEntry;
 constexpr uint32_t kAttSmem = kBarOff + 256 + 1024;  // barriers, flags, 1 KB alignment slack
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kColO = 0;    // O: 256 fp32 columns
-constexpr uint32_t kColS = 256;  // S[2]: 128 fp32 columns each; P (bf16 pairs) over its first 64
+constexpr uint32_t kColS = 256;  // S: 128 fp32 columns; P (bf16 pairs) over its first 64
+constexpr uint32_t kColQ = 384;  // query slabs 0..3: 128 columns of bf16 pairs (32 per slab)
 constexpr float kRescaleLog2 = 8.f;
 static_assert(kAttSmem <= 232448, "shared memory of one CTA");
-static_assert(kRing > kVSlabs, "the ring must hold a block's value slabs and one more entry");
+static_assert(kRing == kSlabs, "entry t of the ring holds slab t of the current block");
+static_assert(kColQ + kQTmemSlabs * 32 <= kTmemCols, "TMEM columns");
 
 // Shared-memory matrix descriptor, 128-byte swizzle (start, leading and stride
 // byte offsets in 16-byte units; descriptor version 1).
@@ -145,15 +156,18 @@ template <int N>
 __device__ __forceinline__ void cp_async_wait() {
   asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
 }
-// wait until at most n committed groups are pending (n clamped to 0..5)
+// wait until at most n committed groups are pending (n clamped to 0..8)
 __device__ __forceinline__ void cp_async_wait_n(int n) {
-  switch (n <= 0 ? 0 : n >= 5 ? 5 : n) {
+  switch (n <= 0 ? 0 : n >= 8 ? 8 : n) {
     case 0: cp_async_wait<0>(); break;
     case 1: cp_async_wait<1>(); break;
     case 2: cp_async_wait<2>(); break;
     case 3: cp_async_wait<3>(); break;
     case 4: cp_async_wait<4>(); break;
-    default: cp_async_wait<5>(); break;
+    case 5: cp_async_wait<5>(); break;
+    case 6: cp_async_wait<6>(); break;
+    case 7: cp_async_wait<7>(); break;
+    default: cp_async_wait<8>(); break;
   }
 }
 // non-blocking test of a phase parity
@@ -167,6 +181,17 @@ __device__ __forceinline__ bool mbar_test(uint64_t* bar, uint32_t parity) {
       : "r"(smem_u32(bar)), "r"(parity)
       : "memory");
   return ok != 0;
+}
+// Two consecutive 32-bit columns of this thread's TMEM lane.
+__device__ __forceinline__ void tmem_st2(uint32_t taddr, uint32_t x, uint32_t y) {
+  asm volatile("tcgen05.st.sync.aligned.32x32b.x2.b32 [%0], {%1, %2};" ::"r"(taddr), "r"(x), "r"(y) : "memory");
+}
+__device__ __forceinline__ void tmem_ld2(uint32_t taddr, uint32_t& x, uint32_t& y) {
+  asm volatile("tcgen05.ld.sync.aligned.32x32b.x2.b32 {%0, %1}, [%2];" : "=r"(x), "=r"(y) : "r"(taddr) : "memory");
+}
+// Barrier `id` (1..15) over `threads` threads (whole warps).
+__device__ __forceinline__ void named_bar_sync(int id, int threads) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(threads) : "memory");
 }
 // 16-byte chunk c (0..7) of row r in a 128-byte-swizzled slab (1 KB aligned).
 __device__ __forceinline__ uint32_t swz(uint32_t slab, int r, int c) {
@@ -187,12 +212,12 @@ __global__ void __launch_bounds__(kAttThreads, 1) attend_kernel(AttendArgs a) {
   uint8_t* smem = smem_raw + pad;
   const uint32_t sb = raw + pad;
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kBarOff);
-  uint64_t* q_full = bars;            // copies: query tile in place
+  uint64_t* q_full = bars;            // copies and softmax warps: query tile in place
   uint64_t* e_full = bars + 1;        // [kRing] copies: entry in place
   uint64_t* e_free = e_full + kRing;  // [kRing] MMA: the entry's last reader done
-  uint64_t* s_full = e_free + kRing;  // [2] MMA: S of a block ready
-  uint64_t* p_full = s_full + 2;      // [2] softmax: P of a block in TMEM
-  uint64_t* pv_done = p_full + 2;     // MMA: one more block's P V done
+  uint64_t* s_full = e_free + kRing;  // MMA: S of a block ready
+  uint64_t* p_full = s_full + 1;      // softmax: P of a block in TMEM
+  uint64_t* pv_done = p_full + 1;     // MMA: one more block's P V done
   uint64_t* o_final = pv_done + 1;    // MMA: the last P V done
   uint64_t* fin = o_final + 1;        // MMA: everything issued is done
   volatile uint32_t* tmem_slot = reinterpret_cast<volatile uint32_t*>(fin + 1);
@@ -218,15 +243,13 @@ __global__ void __launch_bounds__(kAttThreads, 1) attend_kernel(AttendArgs a) {
   };
 
   if (tid == 0) {
-    mbar_init(q_full, kProducers);
+    mbar_init(q_full, kProducers + kSoftThreads);
     for (int s = 0; s < kRing; ++s) {
       mbar_init(&e_full[s], kProducers);
       mbar_init(&e_free[s], 1);
     }
-    for (int s = 0; s < 2; ++s) {
-      mbar_init(&s_full[s], 1);
-      mbar_init(&p_full[s], 128);
-    }
+    mbar_init(s_full, 1);
+    mbar_init(p_full, kSoftThreads);
     mbar_init(pv_done, 1);
     mbar_init(o_final, 1);
     mbar_init(fin, 1);
@@ -245,12 +268,39 @@ __global__ void __launch_bounds__(kAttThreads, 1) attend_kernel(AttendArgs a) {
   tc_after();
   const uint32_t tmem = *tmem_slot;
 
+  if (warp >= 4) {
+    // the softmax warps put query slabs 0..kQTmemSlabs-1 of their head into
+    // TMEM, the A operand of those slabs' S MMAs: column 32s + x of lane h
+    // holds elements 64s + 2x and 64s + 2x + 1 of head h.  Warps 4+q and 8+q
+    // (lanes 32q..) take slabs 0-1 and 2-3.
+    const int ch = (warp - 4) >> 2;
+    const uint4* qv = reinterpret_cast<const uint4*>(a.q + (size_t)(qrow0 + 32 * (warp & 3) + lane) * kRow) + 16 * ch;
+    const uint32_t qa = tmem + ((uint32_t)(32 * (warp & 3)) << 16) + kColQ + 64u * (uint32_t)ch;
+#pragma unroll 1
+    for (int c = 0; c < 4; ++c) {
+      uint32_t w[16];
+#pragma unroll
+      for (int q4 = 0; q4 < 4; ++q4) {
+        const uint4 x = __ldg(qv + 4 * c + q4);
+        w[4 * q4] = x.x;
+        w[4 * q4 + 1] = x.y;
+        w[4 * q4 + 2] = x.z;
+        w[4 * q4 + 3] = x.w;
+      }
+      tmem_st16(qa + 16u * (uint32_t)c, w);
+    }
+    tmem_wait_st();
+    tc_before();
+    mbar_arrive(q_full);
+  }
   if (warp < 2) {
-    // ---- copies: the query tile, then every slab of every block ----
+    // ---- copies: query slabs kQTmemSlabs..8, then every slab of every block ----
     const uint8_t* qsrc = reinterpret_cast<const uint8_t*>(a.q) + qrow0 * (kRow * 2);
-    for (int idx = tid; idx < kM * 72; idx += kProducers) {
-      const int r = idx / 72, g = idx - r * 72;
-      cp_async16(swz(sb + kQOff + (uint32_t)(g >> 3) * kQSlab, r, g & 7), qsrc + (size_t)r * (kRow * 2) + g * 16);
+    constexpr int kQChunks = (kSlabs - kQTmemSlabs) * 8;
+    for (int idx = tid; idx < kM * kQChunks; idx += kProducers) {
+      const int r = idx / kQChunks, g = kQTmemSlabs * 8 + (idx - r * kQChunks);
+      cp_async16(swz(sb + kQOff + (uint32_t)((g >> 3) - kQTmemSlabs) * kQSlab, r, g & 7),
+                 qsrc + (size_t)r * (kRow * 2) + g * 16);
     }
     cp_async_commit();
     const uint8_t* ubase = reinterpret_cast<const uint8_t*>(a.hot) + (size_t)u * a.C * (kRow * 2);
@@ -309,27 +359,34 @@ __global__ void __launch_bounds__(kAttThreads, 1) attend_kernel(AttendArgs a) {
     // ---- MMA issue (one thread) ----
     if (lane == 0) {
       constexpr uint32_t kIdQK = idesc_bf16(kM, kBlk, false);
-      constexpr uint32_t kIdPV = idesc_bf16(kM, 64, true);
+      constexpr uint32_t kIdPV = idesc_bf16(kM, kHalfCols, true);
       bool ok = mbar_wait(q_full, 0, a.wait_ns);
-      const uint64_t qdesc = sdesc(sb + kQOff, 16, 1024);
-      int pv_next = 0;  // first block whose P V is not issued yet
-      // O[:, 64v..64v+63] += P V_v for the value slabs v of block jj; each
-      // slab's entry is freed once its MMAs are done
-      auto issue_pv = [&](int jj) -> bool {
-        if (!mbar_wait(&p_full[jj & 1], (jj >> 1) & 1, a.wait_ns)) return false;
-        tc_after();
-        const uint32_t pa = tmem + kColS + (uint32_t)(jj & 1) * kBlk;  // P: first 64 columns of S
-#pragma unroll 1
-        for (int v = 0; v < kVSlabs; ++v) {
-          const int e = jj * kSlabs + (kSlabs - kVSlabs) + v;
-          // MN-major: 64 value columns per row of 128 bytes, 8-row groups 1 KB apart
-          const uint64_t vdesc = sdesc(sb + kROff + (uint32_t)(e % kRing) * kEntry, kEntry, 1024);
+      // entry t always sits in ring slot t: the descriptors are fixed
+      uint64_t kd[kSlabs], qd[kSlabs];
+      uint32_t qa[kSlabs];
 #pragma unroll
-          for (int kk = 0; kk < kBlk / 16; ++kk)
-            mma_ts(tmem + kColO + 64u * (uint32_t)v, pa + 8u * (uint32_t)kk, vdesc + ((uint32_t)kk * 16u * 128u >> 4),
-                   kIdPV, (jj > 0 || kk > 0) ? 1u : 0u);
-          mma_commit(&e_free[e % kRing]);
-        }
+      for (int t = 0; t < kSlabs; ++t) {
+        const int sl = slab_of(t, half);
+        kd[t] = sdesc(sb + kROff + (uint32_t)t * kEntry, 16, 1024);
+        qd[t] = sdesc(sb + kQOff + (uint32_t)(sl < kQTmemSlabs ? 0 : sl - kQTmemSlabs) * kQSlab, 16, 1024);
+        qa[t] = tmem + kColQ + 32u * (uint32_t)(sl < kQTmemSlabs ? sl : 0);
+      }
+      // V: the four value slabs of a block in slots kSlabs-kVSlabs.. are the
+      // four 64-column chunks of one N = 256 MN-major operand (chunk stride:
+      // one ring entry; 8-row groups 1 KB apart)
+      const uint64_t vdesc = sdesc(sb + kROff + (uint32_t)(kSlabs - kVSlabs) * kEntry, kEntry, 1024);
+      int pv_next = 0;  // first block whose P V is not issued yet
+      // O += P V for block jj; the value slabs' entries are freed once done
+      auto issue_pv = [&](int jj) -> bool {
+        if (!mbar_wait(&p_full[0], jj & 1, a.wait_ns)) return false;
+        tc_after();
+        const uint32_t pa = tmem + kColS;  // P: first 64 columns of S
+#pragma unroll
+        for (int kk = 0; kk < kBlk / 16; ++kk)
+          mma_ts(tmem + kColO, pa + 8u * (uint32_t)kk, vdesc + ((uint32_t)kk * 16u * 128u >> 4), kIdPV,
+                 (jj > 0 || kk > 0) ? 1u : 0u);
+#pragma unroll
+        for (int v = 0; v < kVSlabs; ++v) mma_commit(&e_free[kSlabs - kVSlabs + v]);
         mma_commit(pv_done);
         return true;
       };
@@ -339,36 +396,35 @@ __global__ void __launch_bounds__(kAttThreads, 1) attend_kernel(AttendArgs a) {
         return true;
       };
       for (int j = 0; ok && j < nb; ++j) {
-        // S[j & 1] holds P of block j-2 until its P V is issued
-        if (j >= 2 && !flush_pv(j - 2)) {
+        // S holds P of block j-1 until its P V is issued (the tensor pipe runs
+        // MMAs in order, so P is read before this block's S overwrites it);
+        // the same P V frees the value slots this block's entries 5..8 reuse
+        if (j >= 1 && !flush_pv(j - 1)) {
           ok = false;
           break;
         }
-        const uint32_t dS = tmem + kColS + (uint32_t)(j & 1) * kBlk;
+        const uint32_t dS = tmem + kColS;
+#pragma unroll
         for (int t = 0; t < kSlabs; ++t) {
           const int e = j * kSlabs + t;
-          // the slot last held entry e - kRing: a value slab is freed by its P V
-          if (e >= kRing) {
-            const int pj = (e - kRing) / kSlabs, pt = (e - kRing) - pj * kSlabs;
-            if (pt >= kSlabs - kVSlabs && !flush_pv(pj)) {
-              ok = false;
-              break;
-            }
-          }
-          if (*abort_flag || !mbar_wait(&e_full[e % kRing], (e / kRing) & 1, a.wait_ns)) {
+          if (*abort_flag || !mbar_wait(&e_full[t], (e / kRing) & 1, a.wait_ns)) {
             ok = false;
             break;
           }
           tc_after();
-          const uint64_t kdesc = sdesc(sb + kROff + (uint32_t)(e % kRing) * kEntry, 16, 1024);
-          const uint64_t qd = qdesc + (((uint32_t)slab_of(t, half) * kQSlab) >> 4);
+          if (slab_of(t, half) < kQTmemSlabs) {  // A: the query slab in TMEM (8 columns per K step)
 #pragma unroll
-          for (int kk = 0; kk < 4; ++kk)
-            mma_ss(dS, qd + (uint32_t)(kk * 2), kdesc + (uint32_t)(kk * 2), kIdQK, (t > 0 || kk > 0) ? 1u : 0u);
-          if (t < kSlabs - kVSlabs) mma_commit(&e_free[e % kRing]);  // only the scores read this slab
+            for (int kk = 0; kk < 4; ++kk)
+              mma_ts(dS, qa[t] + 8u * (uint32_t)kk, kd[t] + (uint32_t)(kk * 2), kIdQK, (t > 0 || kk > 0) ? 1u : 0u);
+          } else {  // A: from shared memory
+#pragma unroll
+            for (int kk = 0; kk < 4; ++kk)
+              mma_ss(dS, qd[t] + (uint32_t)(kk * 2), kd[t] + (uint32_t)(kk * 2), kIdQK, (t > 0 || kk > 0) ? 1u : 0u);
+          }
+          if (t < kSlabs - kVSlabs) mma_commit(&e_free[t]);  // only the scores read this slab
         }
         if (!ok) break;
-        mma_commit(&s_full[j & 1]);
+        mma_commit(&s_full[0]);
       }
       if (ok && !flush_pv(nb - 1)) ok = false;
       if (ok) mma_commit(o_final);
@@ -378,118 +434,125 @@ __global__ void __launch_bounds__(kAttThreads, 1) attend_kernel(AttendArgs a) {
     }
     __syncwarp();
   } else if (warp >= 4) {
-    // ---- online softmax, one head per thread ----
-    const int h = tid - 128;
-    const uint32_t lane_addr = (uint32_t)(32 * (warp & 3)) << 16;
+    // ---- online softmax: warps 4+q and 8+q share the heads (TMEM lanes)
+    // 32q..32q+31, one thread per head and half (ch) of each block's rows ----
+    const int q = warp & 3, ch = (warp - 4) >> 2;
+    const int h = 32 * q + lane;
+    const uint32_t lane_addr = (uint32_t)(32 * q) << 16;
+    const uint32_t sS = tmem + lane_addr + kColS;
+    // exchange slots: the last two S columns of each half, read by their
+    // owner before the exchange and written by no MMA until P is consumed
+    const uint32_t x_mine = sS + 64u * (uint32_t)ch + 62u, x_peer = sS + 64u * (uint32_t)(1 - ch) + 62u;
     const float sl2 = a.scale_log2;
     float m_run = -INFINITY, l_run = 0.f;
     bool ok = true;
-    // slots of rows 32c + lane of the next block (validity masks), a block ahead
-    int32_t sn[kBlk / 32];
+    // slots of this half's rows 64ch + 32c + lane of the next block (validity masks)
+    int32_t sn[2];
     auto load_valid = [&](int j) {
 #pragma unroll
-      for (int c = 0; c < kBlk / 32; ++c) {
-        const int r = j * kBlk + 32 * c + lane;
+      for (int c = 0; c < 2; ++c) {
+        const int r = j * kBlk + 64 * ch + 32 * c + lane;
         sn[c] = j < nb && r < a.k ? __ldg(a.slots + list + r) : -1;
       }
     };
+    // the partner warps pass (stop flag, value) through TMEM and a named
+    // barrier, so that they take every decision (stop, rescale) together;
+    // every exchange is reached by both (a stop is taken only after one)
+    uint32_t peer_stop, peer_val;
+    auto exchange = [&](bool stop_mine, float val) {
+      tmem_st2(x_mine, stop_mine ? 1u : 0u, __float_as_uint(val));
+      tmem_wait_st();
+      tc_before();
+      named_bar_sync(1 + q, 64);
+      tc_after();
+      tmem_ld2(x_peer, peer_stop, peer_val);
+      tmem_wait_ld();
+    };
     load_valid(0);
     for (int j = 0; j < nb; ++j) {
-      if (__any_sync(kFull, *abort_flag != 0u)) {  // warp-uniform: TMEM access is warp-wide
+      bool stop = __any_sync(kFull, *abort_flag != 0u);
+      if (!stop) stop = !__all_sync(kFull, mbar_wait(&s_full[0], j & 1, a.wait_ns));
+      tc_after();
+      uint32_t vm[2];
+#pragma unroll
+      for (int c = 0; c < 2; ++c) vm[c] = __ballot_sync(kFull, sn[c] >= 0 && sn[c] < a.C);
+      load_valid(j + 1);
+      // this half's 64 scores, log2-scaled, -inf for dropped rows
+      float t[64];
+      tmem_ld32(sS + 64u * (uint32_t)ch, *reinterpret_cast<float(*)[32]>(&t[0]));
+      tmem_ld32(sS + 64u * (uint32_t)ch + 32u, *reinterpret_cast<float(*)[32]>(&t[32]));
+      tmem_wait_ld();
+      float mx = -INFINITY;
+#pragma unroll
+      for (int i = 0; i < 64; ++i) {
+        t[i] = ((vm[i >> 5] >> (i & 31)) & 1u) ? t[i] * sl2 : -INFINITY;
+        mx = fmaxf(mx, t[i]);
+      }
+      exchange(stop, mx);
+      if (__any_sync(kFull, stop || peer_stop != 0u)) {  // warp-uniform, and the same in both partners
         ok = false;
         break;
       }
-      ok = __all_sync(kFull, mbar_wait(&s_full[j & 1], (j >> 1) & 1, a.wait_ns));
-      if (!ok) break;
-      tc_after();
-      uint32_t vm[kBlk / 32];
-#pragma unroll
-      for (int c = 0; c < kBlk / 32; ++c) vm[c] = __ballot_sync(kFull, sn[c] >= 0 && sn[c] < a.C);
-      load_valid(j + 1);
-      const uint32_t sS = tmem + lane_addr + kColS + (uint32_t)(j & 1) * kBlk;
-      // One read of S: the weights against the running maximum go to registers,
-      // and only if some score passes it by more than 2^8 (always on the first
-      // block with a listed row) does the warp rescale and compute them again.
-      uint32_t pk[kBlk / 2];
-      float mx = -INFINITY, ls = 0.f;
-      const float mu0 = m_run == -INFINITY ? 0.f : m_run;
-#pragma unroll
-      for (int c = 0; c < kBlk / 32; ++c) {
-        float v[32];
-        tmem_ld32(sS + 32u * (uint32_t)c, v);
-        tmem_wait_ld();
-#pragma unroll
-        for (int e = 0; e < 16; ++e) {
-          const bool ok0 = (vm[c] >> (2 * e)) & 1u, ok1 = (vm[c] >> (2 * e + 1)) & 1u;
-          const float t0 = ok0 ? v[2 * e] * sl2 : -INFINITY, t1 = ok1 ? v[2 * e + 1] * sl2 : -INFINITY;
-          mx = fmaxf(mx, fmaxf(t0, t1));
-          const __nv_bfloat162 b2 = __floats2bfloat162_rn(ok0 ? exp2f(t0 - mu0) : 0.f, ok1 ? exp2f(t1 - mu0) : 0.f);
-          ls += __low2float(b2) + __high2float(b2);
-          pk[16 * c + e] = *reinterpret_cast<const uint32_t*>(&b2);
-        }
-      }
+      mx = fmaxf(mx, __uint_as_float(peer_val));
+      // the maximum moves only when a score passes it by more than 2^8 (always
+      // on the first block with a listed row); O is then rescaled in TMEM
       if (__any_sync(kFull, mx > m_run + kRescaleLog2)) {
-        // the warp moves its maxima together (TMEM access is warp-wide)
         const float m_new = fmaxf(m_run, mx);
         const float f = m_new == -INFINITY ? 1.f : exp2f(m_run - m_new);
         l_run *= f;
         if (j > 0) {  // O holds P V of blocks 0..j-1
-          ok = __all_sync(kFull, mbar_wait(pv_done, (j - 1) & 1, a.wait_ns));
-          if (!ok) break;
-          tc_after();
+          if (!__all_sync(kFull, mbar_wait(pv_done, (j - 1) & 1, a.wait_ns))) {
+            fail();  // the partner learns of it at the next exchange
+          } else {
+            tc_after();
 #pragma unroll 1
-          for (int c0 = 0; c0 < kHalfCols; c0 += 32) {
-            float o[32];
-            tmem_ld32(tmem + lane_addr + kColO + (uint32_t)c0, o);
-            tmem_wait_ld();
-            uint32_t w[32];
+            for (int c0 = 0; c0 < kHalfCols / 2; c0 += 32) {
+              const uint32_t oa = tmem + lane_addr + kColO + (uint32_t)(kHalfCols / 2 * ch + c0);
+              float o[32];
+              tmem_ld32(oa, o);
+              tmem_wait_ld();
+              uint32_t w[32];
 #pragma unroll
-            for (int c = 0; c < 32; ++c) w[c] = __float_as_uint(o[c] * f);
-            tmem_st32(tmem + lane_addr + kColO + (uint32_t)c0, w);
+              for (int c = 0; c < 32; ++c) w[c] = __float_as_uint(o[c] * f);
+              tmem_st32(oa, w);
+            }
+            tmem_wait_st();
           }
-          tmem_wait_st();
         }
         m_run = m_new;
-        const float mu = m_run == -INFINITY ? 0.f : m_run;
-        ls = 0.f;
-#pragma unroll
-        for (int c = 0; c < kBlk / 32; ++c) {
-          float v[32];
-          tmem_ld32(sS + 32u * (uint32_t)c, v);
-          tmem_wait_ld();
-#pragma unroll
-          for (int e = 0; e < 16; ++e) {
-            const float x0 = ((vm[c] >> (2 * e)) & 1u) ? exp2f(v[2 * e] * sl2 - mu) : 0.f;
-            const float x1 = ((vm[c] >> (2 * e + 1)) & 1u) ? exp2f(v[2 * e + 1] * sl2 - mu) : 0.f;
-            const __nv_bfloat162 b2 = __floats2bfloat162_rn(x0, x1);
-            ls += __low2float(b2) + __high2float(b2);
-            pk[16 * c + e] = *reinterpret_cast<const uint32_t*>(&b2);
-          }
-        }
       }
-      // P (bf16 pairs) over the first 64 columns of this S buffer, all of which
-      // this thread has read
+      const float mu = m_run == -INFINITY ? 0.f : m_run;
+      // P rounded to bf16 over columns 32ch.. of S (every thread has read its
+      // scores: the exchange came after); l sums the rounded weights
+      float ls = 0.f;
 #pragma unroll
-      for (int c = 0; c < kBlk / 32; ++c) {
+      for (int c = 0; c < 2; ++c) {
         uint32_t w[16];
 #pragma unroll
-        for (int e = 0; e < 16; ++e) w[e] = pk[16 * c + e];
-        tmem_st16(sS + 16u * (uint32_t)c, w);
+        for (int e = 0; e < 16; ++e) {
+          const __nv_bfloat162 b2 = __floats2bfloat162_rn(exp2f(t[32 * c + 2 * e] - mu), exp2f(t[32 * c + 2 * e + 1] - mu));
+          ls += __low2float(b2) + __high2float(b2);
+          w[e] = *reinterpret_cast<const uint32_t*>(&b2);
+        }
+        tmem_st16(sS + 32u * (uint32_t)ch + 16u * (uint32_t)c, w);
       }
       tmem_wait_st();
       l_run += ls;
       tc_before();
-      mbar_arrive(&p_full[j & 1]);
+      mbar_arrive(&p_full[0]);
     }
     if (ok) ok = __all_sync(kFull, mbar_wait(o_final, 0, a.wait_ns));
-    if (ok) {
-      tc_after();
-      const float inv = l_run > 0.f ? 1.f / l_run : 0.f;
-      uint16_t* orow = a.out + (size_t)(qrow0 + h) * kVal + (size_t)half * kHalfCols;
+    tc_after();
+    // l of the whole row: both halves' sums (no MMA touches S any more)
+    exchange(!ok, l_run);
+    if (ok && peer_stop == 0u) {
+      const float l = l_run + __uint_as_float(peer_val);
+      const float inv = l > 0.f ? 1.f / l : 0.f;
+      uint16_t* orow = a.out + (size_t)(qrow0 + h) * kVal + (size_t)half * kHalfCols + (size_t)(kHalfCols / 2) * ch;
 #pragma unroll 1
-      for (int c0 = 0; c0 < kHalfCols; c0 += 32) {
+      for (int c0 = 0; c0 < kHalfCols / 2; c0 += 32) {
         float o[32];
-        tmem_ld32(tmem + lane_addr + kColO + (uint32_t)c0, o);
+        tmem_ld32(tmem + lane_addr + kColO + (uint32_t)(kHalfCols / 2 * ch + c0), o);
         tmem_wait_ld();
         uint32_t w[16];
 #pragma unroll
@@ -501,8 +564,8 @@ __global__ void __launch_bounds__(kAttThreads, 1) attend_kernel(AttendArgs a) {
 #pragma unroll
         for (int q4 = 0; q4 < 4; ++q4) dst[q4] = make_uint4(w[4 * q4], w[4 * q4 + 1], w[4 * q4 + 2], w[4 * q4 + 3]);
       }
-      if (half == 0 && a.lse)
-        a.lse[qrow0 + h] = l_run > 0.f ? (m_run + log2f(l_run)) * 0.6931471805599453f : -INFINITY;
+      if (half == 0 && ch == 0 && a.lse)
+        a.lse[qrow0 + h] = l > 0.f ? (m_run + log2f(l)) * 0.6931471805599453f : -INFINITY;
     } else {
       fail();
     }
