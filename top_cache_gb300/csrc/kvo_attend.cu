@@ -11,7 +11,7 @@
 //   lse_h = log sum_i exp(s_i).
 //
 // One CTA per (unit, position, group of 128 heads, half of the 512 value
-// columns); 384 threads.  The list is cut into blocks of 128 rows.  Issuing a
+// columns); 512 threads.  The list is cut into blocks of 128 rows.  Issuing a
 // tcgen05.mma from one thread costs about a hundred cycles whatever N is up to
 // 128, so every MMA is made as wide as the operands allow: S MMAs have N = 128
 // (a block), and one block's P V is eight MMAs of N = 256 (this CTA's value
@@ -21,16 +21,17 @@
 // slab of a block (entry t always holds slab t of the current block), this
 // CTA's four value slabs last and side by side, so that they form the N = 256
 // operand of P V, while the next block's other five slabs stream in:
-//   warps 0-1  copy query slabs 4-8, then every slab of every block with
+//   warps 0-3  copy query slabs 4-8, then every slab of every block with
 //              16-byte cp.async into the 128-byte-swizzled K-major layout the
-//              MMA reads;
-//   warp 2     holds 512 TMEM columns; lane 0 issues every tcgen05.mma:
+//              MMA reads (four warps: the rate at which cp.async goes out
+//              grows with the warps issuing it);
+//   warp 4     holds 512 TMEM columns; lane 0 issues every tcgen05.mma:
 //              S = Q K^T (M 128, N 128, K 64 per slab) into the S buffer;
 //              once P is ready, O += P V (M 128, N 256, K 128), P read from
 //              TMEM, before the next block's S (S is single-buffered);
-//   warps 4-11 put query slabs 0-3 into TMEM, then run the online softmax: a
-//              head (TMEM lane) per thread pair, warp 4+q taking the first 64
-//              rows of a block and warp 8+q the other 64 for heads 32q..;
+//   warps 8-15 put query slabs 0-3 into TMEM, then run the online softmax: a
+//              head (TMEM lane) per thread pair, warp 8+q taking the first 64
+//              rows of a block and warp 12+q the other 64 for heads 32q..;
 //              each reads its scores once, the pair agrees on the block
 //              maximum through TMEM and a named barrier, the running maximum
 //              moves only when it grows by more than 2^8 (O is then rescaled
@@ -57,9 +58,12 @@ constexpr int kVSlabs = 4;                // value slabs of this CTA's half
 constexpr int kRing = kSlabs;             // ring entries: entry t holds slab t of a block
 constexpr int kQTmemSlabs = 4;            // query slabs 0..3 live in TMEM, 4..8 in shared memory
 constexpr int kHalfCols = kVal / 2;       // value columns per CTA
-constexpr int kAttThreads = 384;
-constexpr int kSoftThreads = 256;        // warps 4-11
-constexpr int kProducers = 64;            // warps 0-1
+constexpr int kAttThreads = 512;
+constexpr int kProducers = 128;           // warps 0-3: copies
+constexpr int kMmaWarp = 4;               // TMEM allocation and MMA issue
+constexpr int kSoftWarp0 = 8;             // warps 8-15: softmax
+constexpr int kSoftThreads = 256;
+constexpr int kRowStep = kProducers / 8;  // rows of an entry between one copy thread's chunks
 constexpr uint32_t kQSlab = kM * 128;     // one slab of the query tile
 constexpr uint32_t kEntry = kBlk * 128;   // one slab of a row block
 constexpr uint32_t kQOff = 0;             // query slabs kQTmemSlabs..8
@@ -72,6 +76,7 @@ constexpr uint32_t kColS = 256;  // S: 128 fp32 columns; P (bf16 pairs) over its
 constexpr uint32_t kColQ = 384;  // query slabs 0..3: 128 columns of bf16 pairs (32 per slab)
 constexpr float kRescaleLog2 = 8.f;
 static_assert(kAttSmem <= 232448, "shared memory of one CTA");
+static_assert(kBlk % kRowStep == 0 && kSoftWarp0 % 4 == 0, "copy rows; softmax warps start a TMEM lane quadrant");
 static_assert(kRing == kSlabs, "entry t of the ring holds slab t of the current block");
 static_assert(kColQ + kQTmemSlabs * 32 <= kTmemCols, "TMEM columns");
 
@@ -256,7 +261,7 @@ __global__ void __launch_bounds__(kAttThreads, 1) attend_kernel(AttendArgs a) {
     *abort_flag = 0u;
     fence_mbar_init();
   }
-  if (warp == 2) {
+  if (warp == kMmaWarp) {
     asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
                      smem_u32((const void*)tmem_slot)),
                  "r"(kTmemCols)
@@ -268,12 +273,12 @@ __global__ void __launch_bounds__(kAttThreads, 1) attend_kernel(AttendArgs a) {
   tc_after();
   const uint32_t tmem = *tmem_slot;
 
-  if (warp >= 4) {
+  if (warp >= kSoftWarp0) {
     // the softmax warps put query slabs 0..kQTmemSlabs-1 of their head into
     // TMEM, the A operand of those slabs' S MMAs: column 32s + x of lane h
-    // holds elements 64s + 2x and 64s + 2x + 1 of head h.  Warps 4+q and 8+q
+    // holds elements 64s + 2x and 64s + 2x + 1 of head h.  Warps 8+q and 12+q
     // (lanes 32q..) take slabs 0-1 and 2-3.
-    const int ch = (warp - 4) >> 2;
+    const int ch = (warp - kSoftWarp0) >> 2;
     const uint4* qv = reinterpret_cast<const uint4*>(a.q + (size_t)(qrow0 + 32 * (warp & 3) + lane) * kRow) + 16 * ch;
     const uint32_t qa = tmem + ((uint32_t)(32 * (warp & 3)) << 16) + kColQ + 64u * (uint32_t)ch;
 #pragma unroll 1
@@ -293,7 +298,7 @@ __global__ void __launch_bounds__(kAttThreads, 1) attend_kernel(AttendArgs a) {
     tc_before();
     mbar_arrive(q_full);
   }
-  if (warp < 2) {
+  if (warp < kProducers / 32) {
     // ---- copies: query slabs kQTmemSlabs..8, then every slab of every block ----
     const uint8_t* qsrc = reinterpret_cast<const uint8_t*>(a.q) + qrow0 * (kRow * 2);
     constexpr int kQChunks = (kSlabs - kQTmemSlabs) * 8;
@@ -304,16 +309,16 @@ __global__ void __launch_bounds__(kAttThreads, 1) attend_kernel(AttendArgs a) {
     }
     cp_async_commit();
     const uint8_t* ubase = reinterpret_cast<const uint8_t*>(a.hot) + (size_t)u * a.C * (kRow * 2);
-    // this thread copies chunk csub of rows rsub + 8m (m < 16) of every entry
+    // this thread copies chunk csub of rows rsub + kRowStep m of every entry
     const int rsub = tid >> 3, csub = tid & 7;
-    int32_t rs[kBlk / 8];
+    int32_t rs[kBlk / kRowStep];
     int rs_block = -1;
     auto issue = [&](int e) {
       const int j = e / kSlabs, t = e - j * kSlabs;
       if (j != rs_block) {
 #pragma unroll
-        for (int m = 0; m < kBlk / 8; ++m) {
-          const int r = j * kBlk + rsub + 8 * m;
+        for (int m = 0; m < kBlk / kRowStep; ++m) {
+          const int r = j * kBlk + rsub + kRowStep * m;
           int32_t sl = r < a.k ? __ldg(a.slots + list + r) : -1;
           rs[m] = sl < 0 || sl >= a.C ? 0 : sl;  // a pad reads a valid row; the softmax drops it
         }
@@ -322,18 +327,22 @@ __global__ void __launch_bounds__(kAttThreads, 1) attend_kernel(AttendArgs a) {
       const uint32_t dst = sb + kROff + (uint32_t)(e % kRing) * kEntry;
       const int s = slab_of(t, half);
 #pragma unroll
-      for (int m = 0; m < kBlk / 8; ++m)
-        cp_async16(swz(dst, rsub + 8 * m, csub), ubase + (size_t)rs[m] * (kRow * 2) + s * 128 + csub * 16);
+      for (int m = 0; m < kBlk / kRowStep; ++m)
+        cp_async16(swz(dst, rsub + kRowStep * m, csub), ubase + (size_t)rs[m] * (kRow * 2) + s * 128 + csub * 16);
       cp_async_commit();
     };
-    // Entries go out as soon as their ring slot is free; an entry is announced
-    // once its copies (and all older ones) have landed.  The warp blocks on a
-    // slot only when everything it issued has been announced, so it never
-    // holds back an entry the MMA needs in order to free that slot.
+    // Entries go out as soon as their ring slot is free, but a block's first
+    // entry only once the previous block has landed: the value slabs of a
+    // block are on the critical path (their slots free up only when the last
+    // block's P V is done), and the next block's slabs would share the
+    // copy bandwidth with them.  An entry is announced once its copies (and
+    // all older ones) have landed.  The warp blocks on a slot only when
+    // everything it issued has been announced, so it never holds back an
+    // entry the MMA needs in order to free that slot.
     int issued = 0, arrived = 0;
     while (arrived < ne) {
       if (__any_sync(kFull, *abort_flag != 0u)) break;  // warp-uniform: shuffles follow
-      while (issued < ne && issued - arrived < kRing &&
+      while (issued < ne && issued - arrived < kRing && issued / kSlabs <= arrived / kSlabs &&
              (issued < kRing ||
               __all_sync(kFull, mbar_test(&e_free[issued % kRing], ((issued / kRing) - 1) & 1)))) {
         issue(issued);
@@ -355,7 +364,7 @@ __global__ void __launch_bounds__(kAttThreads, 1) attend_kernel(AttendArgs a) {
       }
     }
     cp_async_wait<0>();
-  } else if (warp == 2) {
+  } else if (warp == kMmaWarp) {
     // ---- MMA issue (one thread) ----
     if (lane == 0) {
       constexpr uint32_t kIdQK = idesc_bf16(kM, kBlk, false);
@@ -433,10 +442,10 @@ __global__ void __launch_bounds__(kAttThreads, 1) attend_kernel(AttendArgs a) {
       if (!mbar_wait(fin, 0, a.wait_ns)) fail();
     }
     __syncwarp();
-  } else if (warp >= 4) {
-    // ---- online softmax: warps 4+q and 8+q share the heads (TMEM lanes)
+  } else if (warp >= kSoftWarp0) {
+    // ---- online softmax: warps 8+q and 12+q share the heads (TMEM lanes)
     // 32q..32q+31, one thread per head and half (ch) of each block's rows ----
-    const int q = warp & 3, ch = (warp - 4) >> 2;
+    const int q = warp & 3, ch = (warp - kSoftWarp0) >> 2;
     const int h = 32 * q + lane;
     const uint32_t lane_addr = (uint32_t)(32 * q) << 16;
     const uint32_t sS = tmem + lane_addr + kColS;
@@ -572,7 +581,7 @@ __global__ void __launch_bounds__(kAttThreads, 1) attend_kernel(AttendArgs a) {
   }
   tc_before();
   __syncthreads();
-  if (warp == 2) {
+  if (warp == kMmaWarp) {
     tc_after();
     asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(kTmemCols) : "memory");
   }
