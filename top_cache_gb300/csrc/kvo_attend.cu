@@ -15,13 +15,14 @@
 // tcgen05.mma from one thread costs about a hundred cycles whatever N is up to
 // 128, so every MMA is made as wide as the operands allow: S MMAs have N = 128
 // (a block), and one block's P V is eight MMAs of N = 256 (this CTA's value
-// columns).  The query tile (128 x 576 bf16) stays on chip: its first four
-// 64-column slabs in TMEM (the A operand of their S MMAs), the other five in
+// columns).  The query tile (128 x 576 bf16) stays on chip: the four
+// 64-column slabs that match this CTA's value slabs in TMEM (the A operand of
+// their S MMAs: issuing an MMA with A in TMEM is cheaper), the other five in
 // shared memory.  That leaves room for a ring of nine 16 KB entries, one per
 // slab of a block (entry t always holds slab t of the current block), this
 // CTA's four value slabs last and side by side, so that they form the N = 256
 // operand of P V, while the next block's other five slabs stream in:
-//   warps 0-3  copy query slabs 4-8, then every slab of every block with
+//   warps 0-3  copy those five query slabs, then every slab of every block with
 //              16-byte cp.async into the 128-byte-swizzled K-major layout the
 //              MMA reads (four warps: the rate at which cp.async goes out
 //              grows with the warps issuing it);
@@ -29,7 +30,7 @@
 //              S = Q K^T (M 128, N 128, K 64 per slab) into the S buffer;
 //              once P is ready, O += P V (M 128, N 256, K 128), P read from
 //              TMEM, before the next block's S (S is single-buffered);
-//   warps 8-15 put query slabs 0-3 into TMEM, then run the online softmax: a
+//   warps 8-15 put the other four into TMEM, then run the online softmax: a
 //              head (TMEM lane) per thread pair, warp 8+q taking the first 64
 //              rows of a block and warp 12+q the other 64 for heads 32q..;
 //              each reads its scores once, the pair agrees on the block
@@ -56,7 +57,7 @@ constexpr int kBlk = 128;                 // rows per block: N of S, K of P V
 constexpr int kSlabs = kRow / 64;         // 128-byte slabs of a row
 constexpr int kVSlabs = 4;                // value slabs of this CTA's half
 constexpr int kRing = kSlabs;             // ring entries: entry t holds slab t of a block
-constexpr int kQTmemSlabs = 4;            // query slabs 0..3 live in TMEM, 4..8 in shared memory
+constexpr int kQTmemSlabs = kVSlabs;      // query slabs in TMEM: this CTA's value slabs (entries 5..8)
 constexpr int kHalfCols = kVal / 2;       // value columns per CTA
 constexpr int kAttThreads = 512;
 constexpr int kProducers = 128;           // warps 0-3: copies
@@ -66,19 +67,20 @@ constexpr int kSoftThreads = 256;
 constexpr int kRowStep = kProducers / 8;  // rows of an entry between one copy thread's chunks
 constexpr uint32_t kQSlab = kM * 128;     // one slab of the query tile
 constexpr uint32_t kEntry = kBlk * 128;   // one slab of a row block
-constexpr uint32_t kQOff = 0;             // query slabs kQTmemSlabs..8
+constexpr uint32_t kQOff = 0;             // the query slabs of entries 0..4, in entry order
 constexpr uint32_t kROff = (kSlabs - kQTmemSlabs) * kQSlab;
 constexpr uint32_t kBarOff = kROff + kRing * kEntry;
 constexpr uint32_t kAttSmem = kBarOff + 256 + 1024;  // barriers, flags, 1 KB alignment slack
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kColO = 0;    // O: 256 fp32 columns
 constexpr uint32_t kColS = 256;  // S: 128 fp32 columns; P (bf16 pairs) over its first 64
-constexpr uint32_t kColQ = 384;  // query slabs 0..3: 128 columns of bf16 pairs (32 per slab)
+constexpr uint32_t kColQ = 384;  // query slabs 4 half + i: 128 columns of bf16 pairs (32 per slab)
 constexpr float kRescaleLog2 = 8.f;
 static_assert(kAttSmem <= 232448, "shared memory of one CTA");
 static_assert(kBlk % kRowStep == 0 && kSoftWarp0 % 4 == 0, "copy rows; softmax warps start a TMEM lane quadrant");
 static_assert(kRing == kSlabs, "entry t of the ring holds slab t of the current block");
 static_assert(kColQ + kQTmemSlabs * 32 <= kTmemCols, "TMEM columns");
+static_assert(kQTmemSlabs == 4, "the softmax warps load four query slabs, two per warp pair member");
 
 // Shared-memory matrix descriptor, 128-byte swizzle (start, leading and stride
 // byte offsets in 16-byte units; descriptor version 1).
@@ -274,12 +276,13 @@ __global__ void __launch_bounds__(kAttThreads, 1) attend_kernel(AttendArgs a) {
   const uint32_t tmem = *tmem_slot;
 
   if (warp >= kSoftWarp0) {
-    // the softmax warps put query slabs 0..kQTmemSlabs-1 of their head into
-    // TMEM, the A operand of those slabs' S MMAs: column 32s + x of lane h
-    // holds elements 64s + 2x and 64s + 2x + 1 of head h.  Warps 8+q and 12+q
-    // (lanes 32q..) take slabs 0-1 and 2-3.
+    // the softmax warps put this CTA's value slabs 4 half + i (i < 4) of
+    // their head's query into TMEM, the A operand of those slabs' S MMAs:
+    // column 32i + x of lane h holds elements 64(4 half + i) + 2x and + 2x + 1
+    // of head h.  Warps 8+q and 12+q (lanes 32q..) take i = 0-1 and 2-3.
     const int ch = (warp - kSoftWarp0) >> 2;
-    const uint4* qv = reinterpret_cast<const uint4*>(a.q + (size_t)(qrow0 + 32 * (warp & 3) + lane) * kRow) + 16 * ch;
+    const uint4* qv =
+        reinterpret_cast<const uint4*>(a.q + (size_t)(qrow0 + 32 * (warp & 3) + lane) * kRow) + 32 * half + 16 * ch;
     const uint32_t qa = tmem + ((uint32_t)(32 * (warp & 3)) << 16) + kColQ + 64u * (uint32_t)ch;
 #pragma unroll 1
     for (int c = 0; c < 4; ++c) {
@@ -299,13 +302,13 @@ __global__ void __launch_bounds__(kAttThreads, 1) attend_kernel(AttendArgs a) {
     mbar_arrive(q_full);
   }
   if (warp < kProducers / 32) {
-    // ---- copies: query slabs kQTmemSlabs..8, then every slab of every block ----
+    // ---- copies: the query slabs of entries 0..4, then every slab of every block ----
     const uint8_t* qsrc = reinterpret_cast<const uint8_t*>(a.q) + qrow0 * (kRow * 2);
     constexpr int kQChunks = (kSlabs - kQTmemSlabs) * 8;
     for (int idx = tid; idx < kM * kQChunks; idx += kProducers) {
-      const int r = idx / kQChunks, g = kQTmemSlabs * 8 + (idx - r * kQChunks);
-      cp_async16(swz(sb + kQOff + (uint32_t)((g >> 3) - kQTmemSlabs) * kQSlab, r, g & 7),
-                 qsrc + (size_t)r * (kRow * 2) + g * 16);
+      const int r = idx / kQChunks, g = idx - r * kQChunks;  // 16-byte chunk g of the smem part
+      cp_async16(swz(sb + kQOff + (uint32_t)(g >> 3) * kQSlab, r, g & 7),
+                 qsrc + (size_t)r * (kRow * 2) + slab_of(g >> 3, half) * 128 + (g & 7) * 16);
     }
     cp_async_commit();
     const uint8_t* ubase = reinterpret_cast<const uint8_t*>(a.hot) + (size_t)u * a.C * (kRow * 2);
@@ -375,10 +378,10 @@ __global__ void __launch_bounds__(kAttThreads, 1) attend_kernel(AttendArgs a) {
       uint32_t qa[kSlabs];
 #pragma unroll
       for (int t = 0; t < kSlabs; ++t) {
-        const int sl = slab_of(t, half);
+        const int tq = t - (kSlabs - kQTmemSlabs);  // >= 0: the query slab is in TMEM
         kd[t] = sdesc(sb + kROff + (uint32_t)t * kEntry, 16, 1024);
-        qd[t] = sdesc(sb + kQOff + (uint32_t)(sl < kQTmemSlabs ? 0 : sl - kQTmemSlabs) * kQSlab, 16, 1024);
-        qa[t] = tmem + kColQ + 32u * (uint32_t)(sl < kQTmemSlabs ? sl : 0);
+        qd[t] = sdesc(sb + kQOff + (uint32_t)(tq < 0 ? t : 0) * kQSlab, 16, 1024);
+        qa[t] = tmem + kColQ + 32u * (uint32_t)(tq < 0 ? 0 : tq);
       }
       // V: the four value slabs of a block in slots kSlabs-kVSlabs.. are the
       // four 64-column chunks of one N = 256 MN-major operand (chunk stride:
@@ -421,7 +424,7 @@ __global__ void __launch_bounds__(kAttThreads, 1) attend_kernel(AttendArgs a) {
             break;
           }
           tc_after();
-          if (slab_of(t, half) < kQTmemSlabs) {  // A: the query slab in TMEM (8 columns per K step)
+          if (t >= kSlabs - kQTmemSlabs) {  // A: the query slab in TMEM (8 columns per K step)
 #pragma unroll
             for (int kk = 0; kk < 4; ++kk)
               mma_ts(dS, qa[t] + 8u * (uint32_t)kk, kd[t] + (uint32_t)(kk * 2), kIdQK, (t > 0 || kk > 0) ? 1u : 0u);
