@@ -128,11 +128,25 @@ def huge_backed_fraction(addr):
     return None
 
 
-def kernel_source_hash():
+# The sources each timed kernel is compiled from (its translation unit and every header it
+# includes): a committed traffic figure stands only while their hash is the one it was taken at.
+KERNEL_SOURCES = {
+    "fused": ["kvo_fused.cu", "kvo_fused_i8.cu", "kvo_fused.cuh", "kvo_device.cuh", "kvo_internal.cuh"],
+    "score": ["kvo_select.cu", "kvo_device.cuh", "kvo_internal.cuh"],
+    "append": ["kvo_residency.cu", "kvo_device.cuh", "kvo_internal.cuh"],
+    "attend": ["kvo_attend.cu", "kvo_internal.cuh"],
+}
+
+
+def kernel_sources(kernel):
+    """Repository paths of the files kernel is compiled from (the C ABI header included)."""
+    return ["top_cache_gb300/csrc/" + f for f in KERNEL_SOURCES[kernel]] + ["include/kvo.h"]
+
+
+def kernel_source_hash(kernel):
     h = hashlib.sha256()
-    csrc = os.path.join(ROOT, "top_cache_gb300", "csrc")
-    for name in sorted(os.listdir(csrc)):
-        with open(os.path.join(csrc, name), "rb") as f:
+    for rel in kernel_sources(kernel):
+        with open(os.path.join(ROOT, rel), "rb") as f:
             h.update(f.read())
     return h.hexdigest()[:16]
 
@@ -143,7 +157,7 @@ def load_traffic(kernel, workload):
         with open(TRAFFIC_FILE) as f:
             t = json.load(f)
         e = t[kernel]
-        if e.get("source_hash") != kernel_source_hash() or e.get("workload") != workload:
+        if e.get("source_hash") != kernel_source_hash(kernel) or e.get("workload") != workload:
             return None
         return float(e["bytes_per_launch"])
     except Exception:
@@ -370,7 +384,8 @@ def run_attention(args, kv, wl, units, device, torch):
         "selections_per_s": round(U / (t * 1e-3), 1),
         "roofline": {"bound": "tensor", "achieved": round(achieved, 1), "peak": peak,
                      "unit": "TFLOP/s", "frac": round(achieved / peak, 4),
-                     "peak_source": "%s bf16 dense (burst)" % src, "traffic": None},
+                     "peak_source": "%s bf16 dense (burst)" % src,
+                     "traffic": load_traffic("attend", wl.name)},
         "flops_per_launch": flops, "executed_tflops": round(flops_exec / (t * 1e-3) / 1e12, 1),
         "rows_listed": n_rows, "l2_to_sm_bytes_per_launch": rows_bytes,
         "l2": "inputs larger than L2: %.2f GB of listed hot rows and queries per launch"
