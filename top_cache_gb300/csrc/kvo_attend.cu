@@ -65,6 +65,7 @@ constexpr int kMmaWarp = 4;               // TMEM allocation and MMA issue
 constexpr int kSoftWarp0 = 8;             // warps 8-15: softmax
 constexpr int kSoftThreads = 256;
 constexpr int kRowStep = kProducers / 8;  // rows of an entry between one copy thread's chunks
+constexpr int kCopyLag = 4;               // entries a copy warp keeps in flight unannounced
 constexpr uint32_t kQSlab = kM * 128;     // one slab of the query tile
 constexpr uint32_t kEntry = kBlk * 128;   // one slab of a row block
 constexpr uint32_t kQOff = 0;             // the query slabs of entries 0..4, in entry order
@@ -78,6 +79,7 @@ constexpr uint32_t kColQ = 384;  // query slabs 4 half + i: 128 columns of bf16 
 constexpr float kRescaleLog2 = 8.f;
 static_assert(kAttSmem <= 232448, "shared memory of one CTA");
 static_assert(kBlk % kRowStep == 0 && kSoftWarp0 % 4 == 0, "copy rows; softmax warps start a TMEM lane quadrant");
+static_assert(kCopyLag >= 1 && kCopyLag <= kRing, "copies in flight");
 static_assert(kRing == kSlabs, "entry t of the ring holds slab t of the current block");
 static_assert(kColQ + kQTmemSlabs * 32 <= kTmemCols, "TMEM columns");
 static_assert(kQTmemSlabs == 4, "the softmax warps load four query slabs, two per warp pair member");
@@ -188,6 +190,13 @@ __device__ __forceinline__ bool mbar_test(uint64_t* bar, uint32_t parity) {
       : "r"(smem_u32(bar)), "r"(parity)
       : "memory");
   return ok != 0;
+}
+// 2^x with the hardware approximation (relative error near 2^-22, far below
+// the bf16 rounding of the weights); 2^-inf = 0, tiny results flush to zero.
+__device__ __forceinline__ float ex2_ftz(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
 }
 // Two consecutive 32-bit columns of this thread's TMEM lane.
 __device__ __forceinline__ void tmem_st2(uint32_t taddr, uint32_t x, uint32_t y) {
@@ -314,18 +323,27 @@ __global__ void __launch_bounds__(kAttThreads, 1) attend_kernel(AttendArgs a) {
     const uint8_t* ubase = reinterpret_cast<const uint8_t*>(a.hot) + (size_t)u * a.C * (kRow * 2);
     // this thread copies chunk csub of rows rsub + kRowStep m of every entry
     const int rsub = tid >> 3, csub = tid & 7;
-    int32_t rs[kBlk / kRowStep];
+    // slots of this thread's rows of the current block (rs) and of the next
+    // (rs_next, loaded a block ahead so that a block's first copies do not
+    // wait for them)
+    int32_t rs[kBlk / kRowStep], rs_next[kBlk / kRowStep];
+    auto load_rows = [&](int j, int32_t (&dst)[kBlk / kRowStep]) {
+#pragma unroll
+      for (int m = 0; m < kBlk / kRowStep; ++m) {
+        const int r = j * kBlk + rsub + kRowStep * m;
+        dst[m] = j < nb && r < a.k ? __ldg(a.slots + list + r) : -1;
+      }
+    };
+    load_rows(0, rs_next);
     int rs_block = -1;
     auto issue = [&](int e) {
       const int j = e / kSlabs, t = e - j * kSlabs;
-      if (j != rs_block) {
+      if (j != rs_block) {  // blocks are issued in order: rs_next holds block j
 #pragma unroll
-        for (int m = 0; m < kBlk / kRowStep; ++m) {
-          const int r = j * kBlk + rsub + kRowStep * m;
-          int32_t sl = r < a.k ? __ldg(a.slots + list + r) : -1;
-          rs[m] = sl < 0 || sl >= a.C ? 0 : sl;  // a pad reads a valid row; the softmax drops it
-        }
+        for (int m = 0; m < kBlk / kRowStep; ++m)  // a pad reads a valid row; the softmax drops it
+          rs[m] = rs_next[m] < 0 || rs_next[m] >= a.C ? 0 : rs_next[m];
         rs_block = j;
+        load_rows(j + 1, rs_next);
       }
       const uint32_t dst = sb + kROff + (uint32_t)(e % kRing) * kEntry;
       const int s = slab_of(t, half);
@@ -339,13 +357,15 @@ __global__ void __launch_bounds__(kAttThreads, 1) attend_kernel(AttendArgs a) {
     // block are on the critical path (their slots free up only when the last
     // block's P V is done), and the next block's slabs would share the
     // copy bandwidth with them.  An entry is announced once its copies (and
-    // all older ones) have landed.  The warp blocks on a slot only when
-    // everything it issued has been announced, so it never holds back an
-    // entry the MMA needs in order to free that slot.
+    // all older ones) have landed; at most kCopyLag entries are in flight
+    // unannounced, so that the warp announces each one soon after it lands
+    // instead of after issuing everything it can.  The warp blocks on a slot
+    // only when everything it issued has been announced, so it never holds
+    // back an entry the MMA needs in order to free that slot.
     int issued = 0, arrived = 0;
     while (arrived < ne) {
       if (__any_sync(kFull, *abort_flag != 0u)) break;  // warp-uniform: shuffles follow
-      while (issued < ne && issued - arrived < kRing && issued / kSlabs <= arrived / kSlabs &&
+      while (issued < ne && issued - arrived < kCopyLag && issued / kSlabs <= arrived / kSlabs &&
              (issued < kRing ||
               __all_sync(kFull, mbar_test(&e_free[issued % kRing], ((issued / kRing) - 1) & 1)))) {
         issue(issued);
@@ -542,7 +562,7 @@ __global__ void __launch_bounds__(kAttThreads, 1) attend_kernel(AttendArgs a) {
         uint32_t w[16];
 #pragma unroll
         for (int e = 0; e < 16; ++e) {
-          const __nv_bfloat162 b2 = __floats2bfloat162_rn(exp2f(t[32 * c + 2 * e] - mu), exp2f(t[32 * c + 2 * e + 1] - mu));
+          const __nv_bfloat162 b2 = __floats2bfloat162_rn(ex2_ftz(t[32 * c + 2 * e] - mu), ex2_ftz(t[32 * c + 2 * e + 1] - mu));
           ls += __low2float(b2) + __high2float(b2);
           w[e] = *reinterpret_cast<const uint32_t*>(&b2);
         }
