@@ -65,7 +65,6 @@ constexpr int kMmaWarp = 4;               // TMEM allocation and MMA issue
 constexpr int kSoftWarp0 = 8;             // warps 8-15: softmax
 constexpr int kSoftThreads = 256;
 constexpr int kRowStep = kProducers / 8;  // rows of an entry between one copy thread's chunks
-constexpr int kCopyLag = 4;               // entries a copy warp keeps in flight unannounced
 constexpr uint32_t kQSlab = kM * 128;     // one slab of the query tile
 constexpr uint32_t kEntry = kBlk * 128;   // one slab of a row block
 constexpr uint32_t kQOff = 0;             // the query slabs of entries 0..4, in entry order
@@ -79,7 +78,6 @@ constexpr uint32_t kColQ = 384;  // query slabs 4 half + i: 128 columns of bf16 
 constexpr float kRescaleLog2 = 8.f;
 static_assert(kAttSmem <= 232448, "shared memory of one CTA");
 static_assert(kBlk % kRowStep == 0 && kSoftWarp0 % 4 == 0, "copy rows; softmax warps start a TMEM lane quadrant");
-static_assert(kCopyLag >= 1 && kCopyLag <= kRing, "copies in flight");
 static_assert(kRing == kSlabs, "entry t of the ring holds slab t of the current block");
 static_assert(kColQ + kQTmemSlabs * 32 <= kTmemCols, "TMEM columns");
 static_assert(kQTmemSlabs == 4, "the softmax warps load four query slabs, two per warp pair member");
@@ -160,36 +158,13 @@ __device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&r)[16
 __device__ __forceinline__ void cp_async16(uint32_t dst, const void* src) {
   asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
 }
-__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
-template <int N>
-__device__ __forceinline__ void cp_async_wait() {
-  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
-}
-// wait until at most n committed groups are pending (n clamped to 0..8)
-__device__ __forceinline__ void cp_async_wait_n(int n) {
-  switch (n <= 0 ? 0 : n >= 8 ? 8 : n) {
-    case 0: cp_async_wait<0>(); break;
-    case 1: cp_async_wait<1>(); break;
-    case 2: cp_async_wait<2>(); break;
-    case 3: cp_async_wait<3>(); break;
-    case 4: cp_async_wait<4>(); break;
-    case 5: cp_async_wait<5>(); break;
-    case 6: cp_async_wait<6>(); break;
-    case 7: cp_async_wait<7>(); break;
-    default: cp_async_wait<8>(); break;
-  }
-}
-// non-blocking test of a phase parity
-__device__ __forceinline__ bool mbar_test(uint64_t* bar, uint32_t parity) {
-  uint32_t ok;
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
-      "selp.u32 %0, 1, 0, p;\n\t}"
-      : "=r"(ok)
-      : "r"(smem_u32(bar)), "r"(parity)
-      : "memory");
-  return ok != 0;
+// Wait for every cp.async this thread has issued.
+__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
+// The barrier counts one arrival once every cp.async this thread has issued
+// so far has landed (its pending count is not raised: the arrival is one of
+// those it was initialised for).
+__device__ __forceinline__ void cp_async_arrive_noinc(uint64_t* bar) {
+  asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(smem_u32(bar)) : "memory");
 }
 // 2^x with the hardware approximation (relative error near 2^-22, far below
 // the bf16 rounding of the weights); 2^-inf = 0, tiny results flush to zero.
@@ -319,7 +294,7 @@ __global__ void __launch_bounds__(kAttThreads, 1) attend_kernel(AttendArgs a) {
       cp_async16(swz(sb + kQOff + (uint32_t)(g >> 3) * kQSlab, r, g & 7),
                  qsrc + (size_t)r * (kRow * 2) + slab_of(g >> 3, half) * 128 + (g & 7) * 16);
     }
-    cp_async_commit();
+    cp_async_arrive_noinc(q_full);
     const uint8_t* ubase = reinterpret_cast<const uint8_t*>(a.hot) + (size_t)u * a.C * (kRow * 2);
     // this thread copies chunk csub of rows rsub + kRowStep m of every entry
     const int rsub = tid >> 3, csub = tid & 7;
@@ -350,49 +325,37 @@ __global__ void __launch_bounds__(kAttThreads, 1) attend_kernel(AttendArgs a) {
 #pragma unroll
       for (int m = 0; m < kBlk / kRowStep; ++m)
         cp_async16(swz(dst, rsub + kRowStep * m, csub), ubase + (size_t)rs[m] * (kRow * 2) + s * 128 + csub * 16);
-      cp_async_commit();
+      cp_async_arrive_noinc(&e_full[e % kRing]);  // counts once this thread's copies have landed
     };
-    // Entries go out as soon as their ring slot is free, but a block's first
-    // entry only once the previous block has landed: the value slabs of a
-    // block are on the critical path (their slots free up only when the last
-    // block's P V is done), and the next block's slabs would share the
-    // copy bandwidth with them.  An entry is announced once its copies (and
-    // all older ones) have landed; at most kCopyLag entries are in flight
-    // unannounced, so that the warp announces each one soon after it lands
-    // instead of after issuing everything it can.  The warp blocks on a slot
-    // only when everything it issued has been announced, so it never holds
-    // back an entry the MMA needs in order to free that slot.
-    int issued = 0, arrived = 0;
-    while (arrived < ne) {
+    // Entries go out in order, each as soon as its ring slot is free; a
+    // block's first entry only once the previous block has landed (its last
+    // entry's barrier has completed): the value slabs of a block are on the
+    // critical path (their slots free up only when the last block's P V is
+    // done), and the next block's slabs would share the copy bandwidth with
+    // them.  Completion is tracked by the entry's barrier itself, so the
+    // warps never wait for their own copies and keep the ring full.
+    for (int e = 0; e < ne; ++e) {
       if (__any_sync(kFull, *abort_flag != 0u)) break;  // warp-uniform: shuffles follow
-      while (issued < ne && issued - arrived < kCopyLag && issued / kSlabs <= arrived / kSlabs &&
-             (issued < kRing ||
-              __all_sync(kFull, mbar_test(&e_free[issued % kRing], ((issued / kRing) - 1) & 1)))) {
-        issue(issued);
-        ++issued;
+      const int j = e / kSlabs, t = e - j * kSlabs;
+      bool ok = true;
+      if (t == 0 && j > 0)
+        ok = __all_sync(kFull, mbar_wait(&e_full[kSlabs - 1], (j - 1) & 1, a.wait_ns));
+      if (ok && e >= kRing)
+        ok = __all_sync(kFull, mbar_wait(&e_free[t], ((e / kRing) - 1) & 1, a.wait_ns));
+      if (!ok) {
+        fail();
+        break;
       }
-      if (arrived < issued) {
-        cp_async_wait_n(issued - 1 - arrived);
-        fence_proxy_async_smem();  // the tensor cores read what cp.async wrote
-        if (arrived == 0) mbar_arrive(q_full);
-        mbar_arrive(&e_full[arrived % kRing]);
-        ++arrived;
-      } else {
-        const bool ok =
-            __all_sync(kFull, mbar_wait(&e_free[issued % kRing], ((issued / kRing) - 1) & 1, a.wait_ns));
-        if (!ok) {
-          fail();
-          break;
-        }
-      }
+      issue(e);
     }
-    cp_async_wait<0>();
+    cp_async_wait_all();
   } else if (warp == kMmaWarp) {
     // ---- MMA issue (one thread) ----
     if (lane == 0) {
       constexpr uint32_t kIdQK = idesc_bf16(kM, kBlk, false);
       constexpr uint32_t kIdPV = idesc_bf16(kM, kHalfCols, true);
       bool ok = mbar_wait(q_full, 0, a.wait_ns);
+      fence_proxy_async_smem();  // the tensor cores read what cp.async wrote (acquired through the barrier)
       // entry t always sits in ring slot t: the descriptors are fixed
       uint64_t kd[kSlabs], qd[kSlabs];
       uint32_t qa[kSlabs];
@@ -443,6 +406,7 @@ __global__ void __launch_bounds__(kAttThreads, 1) attend_kernel(AttendArgs a) {
             ok = false;
             break;
           }
+          fence_proxy_async_smem();  // as for the query slabs
           tc_after();
           if (t >= kSlabs - kQTmemSlabs) {  // A: the query slab in TMEM (8 columns per K step)
 #pragma unroll
