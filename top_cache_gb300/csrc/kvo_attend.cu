@@ -479,10 +479,18 @@ __global__ void __launch_bounds__(kAttThreads, 1) attend_kernel(AttendArgs a) {
       tmem_ld32(sS + 64u * (uint32_t)ch + 32u, *reinterpret_cast<float(*)[32]>(&t[32]));
       tmem_wait_ld();
       float mx = -INFINITY;
+      if ((vm[0] & vm[1]) == kFull) {  // every row listed (the masks are the same in all lanes)
 #pragma unroll
-      for (int i = 0; i < 64; ++i) {
-        t[i] = ((vm[i >> 5] >> (i & 31)) & 1u) ? t[i] * sl2 : -INFINITY;
-        mx = fmaxf(mx, t[i]);
+        for (int i = 0; i < 64; ++i) {
+          t[i] *= sl2;
+          mx = fmaxf(mx, t[i]);
+        }
+      } else {
+#pragma unroll
+        for (int i = 0; i < 64; ++i) {
+          t[i] = ((vm[i >> 5] >> (i & 31)) & 1u) ? t[i] * sl2 : -INFINITY;
+          mx = fmaxf(mx, t[i]);
+        }
       }
       exchange(stop, mx);
       if (__any_sync(kFull, stop || peer_stop != 0u)) {  // warp-uniform, and the same in both partners
