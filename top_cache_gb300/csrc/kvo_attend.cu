@@ -10,39 +10,42 @@
 //   s_i = scale * q_h . row_i,   out_h = sum_i softmax(s)_i * row_i[0:512],
 //   lse_h = log sum_i exp(s_i).
 //
-// One CTA per (unit, position, group of 128 heads, half of the 512 value
-// columns); 512 threads.  The list is cut into blocks of 128 rows.  Issuing a
-// tcgen05.mma from one thread costs about a hundred cycles whatever N is up to
-// 128, so every MMA is made as wide as the operands allow: S MMAs have N = 128
-// (a block), and one block's P V is eight MMAs of N = 256 (this CTA's value
-// columns).  The query tile (128 x 576 bf16) stays on chip: the four
-// 64-column slabs that match this CTA's value slabs in TMEM (the A operand of
-// their S MMAs: issuing an MMA with A in TMEM is cheaper), the other five in
-// shared memory.  That leaves room for a ring of nine 16 KB entries, one per
-// slab of a block (entry t always holds slab t of the current block), this
-// CTA's four value slabs last and side by side, so that they form the N = 256
-// operand of P V, while the next block's other five slabs stream in:
-//   warps 0-3  copy those five query slabs, then every slab of every block with
-//              16-byte cp.async into the 128-byte-swizzled K-major layout the
-//              MMA reads (four warps: the rate at which cp.async goes out
-//              grows with the warps issuing it);
-//   warp 4     holds 512 TMEM columns; lane 0 issues every tcgen05.mma:
-//              S = Q K^T (M 128, N 128, K 64 per slab) into the S buffer;
-//              once P is ready, O += P V (M 128, N 256, K 128), P read from
-//              TMEM, before the next block's S (S is single-buffered);
-//   warps 8-15 put the other four into TMEM, then run the online softmax: a
-//              head (TMEM lane) per thread pair, warp 8+q taking the first 64
-//              rows of a block and warp 12+q the other 64 for heads 32q..;
-//              each reads its scores once, the pair agrees on the block
-//              maximum through TMEM and a named barrier, the running maximum
-//              moves only when it grows by more than 2^8 (O is then rescaled
-//              in TMEM), P is rounded to bf16 and written back over the first
-//              64 columns of S, and l sums the rounded weights so that out is
-//              their exact weighted mean; at the end O / l in bf16 and lse.
-// A ring entry is freed by the MMAs that read it last: the S MMAs for the five
-// slabs only the scores use, the P V MMAs for the value slabs.
+// A cluster of two CTAs per (unit, position, group of 128 heads); CTA c of
+// the pair owns value columns 256c..256c+255 (slabs 4c..4c+3 of a row) and
+// rows 64c..64c+63 of every 128-row block.  The scores are split by slab: CTA
+// c computes the partial S over its own four value slabs, plus the rope slab
+// on the blocks whose index has its parity, so each row slab is copied and
+// multiplied once per pair.  Per block:
+//   - each CTA sends its partial scores of the partner's rows into the
+//     partner's shared memory and adds the partner's partial scores of its
+//     own rows (distributed shared memory, mbarriers with cluster scope);
+//   - the two agree on each head's block maximum the same way;
+//   - each writes P (bf16) of its 64 rows into both CTAs' P tile, and each
+//     computes O[:, own 256 columns] += P V over all 128 rows.
+// Issuing a tcgen05.mma from one thread costs about a hundred cycles whatever
+// N is up to 128, so every MMA is as wide as the operands allow: S MMAs have
+// N = 128, P V is eight MMAs of N = 256.  S is freed as soon as the softmax
+// has read it (P lives in shared memory), so the next block's S overlaps the
+// softmax of this one.
+//   warps 0-1  copy the rope query slab, then this CTA's slabs of every
+//              block with 16-byte cp.async into the 128-byte-swizzled
+//              K-major layout; completion is counted by each ring entry's
+//              mbarrier (cp.async.mbarrier.arrive.noinc), so they never
+//              wait for their own copies.  Ring: nine 16 KB entries, the
+//              value slabs of even blocks in 0-3, of odd blocks in 4-7 (side
+//              by side: the N = 256 operand of P V), the rope slab in 8;
+//   warps 4-7  put this CTA's four query slabs into TMEM, then run the
+//              online softmax, one head (TMEM lane) per thread: the running
+//              maximum moves only when a score passes it by more than 2^8 (O
+//              is then rescaled in TMEM); P is rounded to bf16 and l sums the
+//              rounded weights, so out is their exact weighted mean; at the
+//              end the pair adds its two l, and O / l in bf16 and lse;
+//   warp 2     holds 512 TMEM columns; lane 0 issues every tcgen05.mma:
+//              S(j) (A: query slabs in TMEM, the rope one in shared memory),
+//              then P V of block j-1 (A: P tile, B: value slabs).
 // Every mbarrier wait is bounded: on expiry the CTA sets kErrTimeout in the
-// error word, stops, waits for its own copies and MMAs and frees its TMEM.
+// error word and stops; both CTAs always meet at the final cluster barrier,
+// after which no access to the partner's shared memory is made.
 #include <cuda_bf16.h>
 
 #include "kvo_internal.cuh"
@@ -52,35 +55,39 @@ namespace {
 
 constexpr int kRow = 576;                 // elements per hot row
 constexpr int kVal = 512;                 // value (latent) elements
-constexpr int kM = 128;                   // heads per CTA: M of the MMAs
+constexpr int kM = 128;                   // heads per CTA pair: M of the MMAs
 constexpr int kBlk = 128;                 // rows per block: N of S, K of P V
-constexpr int kSlabs = kRow / 64;         // 128-byte slabs of a row
-constexpr int kVSlabs = 4;                // value slabs of this CTA's half
-constexpr int kRing = kSlabs;             // ring entries: entry t holds slab t of a block
-constexpr int kQTmemSlabs = kVSlabs;      // query slabs in TMEM: this CTA's value slabs (entries 5..8)
+constexpr int kOwnRows = kBlk / 2;        // rows of a block whose softmax this CTA runs
+constexpr int kVSlabs = 4;                // value slabs of one CTA
+constexpr int kRopeSlab = 8;              // slab of the rope key
+constexpr int kRing = 2 * kVSlabs + 1;    // value slabs of two blocks + the rope slab
 constexpr int kHalfCols = kVal / 2;       // value columns per CTA
-constexpr int kAttThreads = 512;
-constexpr int kProducers = 128;           // warps 0-3: copies
-constexpr int kMmaWarp = 4;               // TMEM allocation and MMA issue
-constexpr int kSoftWarp0 = 8;             // warps 8-15: softmax
-constexpr int kSoftThreads = 256;
+constexpr int kAttThreads = 256;
+constexpr int kProducers = 64;            // warps 0-1: copies
+constexpr int kMmaWarp = 2;               // TMEM allocation and MMA issue
+constexpr int kSoftWarp0 = 4;             // warps 4-7: softmax
+constexpr int kSoftThreads = 128;
 constexpr int kRowStep = kProducers / 8;  // rows of an entry between one copy thread's chunks
 constexpr uint32_t kQSlab = kM * 128;     // one slab of the query tile
 constexpr uint32_t kEntry = kBlk * 128;   // one slab of a row block
-constexpr uint32_t kQOff = 0;             // the query slabs of entries 0..4, in entry order
-constexpr uint32_t kROff = (kSlabs - kQTmemSlabs) * kQSlab;
-constexpr uint32_t kBarOff = kROff + kRing * kEntry;
+constexpr uint32_t kPSlab = kM * 128;     // 64 rows of P (K-major, 128-byte swizzled)
+constexpr uint32_t kQOff = 0;                               // rope query slab
+constexpr uint32_t kROff = kQOff + kQSlab;                  // ring
+constexpr uint32_t kPOff = kROff + kRing * kEntry;          // P tile: two slabs
+constexpr uint32_t kXSOff = kPOff + 2 * kPSlab;             // partner's partial scores of own rows
+constexpr uint32_t kXSBytes = kM * kOwnRows * 4;           // partial scores of 64 rows of 128 heads
+constexpr uint32_t kXMOff = kXSOff + kXSBytes;              // partner's block maxima [2][128], then its l
+constexpr uint32_t kBarOff = kXMOff + 2 * kM * 4;
 constexpr uint32_t kAttSmem = kBarOff + 256 + 1024;  // barriers, flags, 1 KB alignment slack
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kColO = 0;    // O: 256 fp32 columns
-constexpr uint32_t kColS = 256;  // S: 128 fp32 columns; P (bf16 pairs) over its first 64
-constexpr uint32_t kColQ = 384;  // query slabs 4 half + i: 128 columns of bf16 pairs (32 per slab)
+constexpr uint32_t kColS = 256;  // S: 128 fp32 columns (this CTA's partial, then read out)
+constexpr uint32_t kColQ = 384;  // query slabs 4c + i: 128 columns of bf16 pairs (32 per slab)
 constexpr float kRescaleLog2 = 8.f;
 static_assert(kAttSmem <= 232448, "shared memory of one CTA");
+static_assert(kROff % 1024 == 0 && kPOff % 1024 == 0, "128-byte-swizzled tiles sit on 1 KB boundaries");
 static_assert(kBlk % kRowStep == 0 && kSoftWarp0 % 4 == 0, "copy rows; softmax warps start a TMEM lane quadrant");
-static_assert(kRing == kSlabs, "entry t of the ring holds slab t of the current block");
-static_assert(kColQ + kQTmemSlabs * 32 <= kTmemCols, "TMEM columns");
-static_assert(kQTmemSlabs == 4, "the softmax warps load four query slabs, two per warp pair member");
+static_assert(kSoftThreads == kM, "one softmax thread per head");
 
 // Shared-memory matrix descriptor, 128-byte swizzle (start, leading and stride
 // byte offsets in 16-byte units; descriptor version 1).
@@ -134,16 +141,15 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32]) {
 #pragma unroll
   for (int c = 0; c < 32; ++c) v[c] = __uint_as_float(r[c]);
 }
-__device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32]) {
+// 16 consecutive 32-bit columns of this thread's TMEM lane.
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&r)[16]) {
   asm volatile(
-      "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, "
-      "%12, %13, %14, %15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, "
-      "%30, %31, %32};" ::"r"(taddr),
-      "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]),
-      "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]),
-      "r"(r[15]), "r"(r[16]), "r"(r[17]), "r"(r[18]), "r"(r[19]), "r"(r[20]), "r"(r[21]),
-      "r"(r[22]), "r"(r[23]), "r"(r[24]), "r"(r[25]), "r"(r[26]), "r"(r[27]), "r"(r[28]),
-      "r"(r[29]), "r"(r[30]), "r"(r[31])
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, "
+      "%12, %13, %14, %15}, [%16];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
+        "=r"(r[14]), "=r"(r[15])
+      : "r"(taddr)
       : "memory");
 }
 __device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&r)[16]) {
@@ -173,50 +179,98 @@ __device__ __forceinline__ float ex2_ftz(float x) {
   asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
   return y;
 }
-// Two consecutive 32-bit columns of this thread's TMEM lane.
-__device__ __forceinline__ void tmem_st2(uint32_t taddr, uint32_t x, uint32_t y) {
-  asm volatile("tcgen05.st.sync.aligned.32x32b.x2.b32 [%0], {%1, %2};" ::"r"(taddr), "r"(x), "r"(y) : "memory");
-}
-__device__ __forceinline__ void tmem_ld2(uint32_t taddr, uint32_t& x, uint32_t& y) {
-  asm volatile("tcgen05.ld.sync.aligned.32x32b.x2.b32 {%0, %1}, [%2];" : "=r"(x), "=r"(y) : "r"(taddr) : "memory");
-}
-// Barrier `id` (1..15) over `threads` threads (whole warps).
-__device__ __forceinline__ void named_bar_sync(int id, int threads) {
-  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(threads) : "memory");
-}
 // 16-byte chunk c (0..7) of row r in a 128-byte-swizzled slab (1 KB aligned).
 __device__ __forceinline__ uint32_t swz(uint32_t slab, int r, int c) {
   return slab + (uint32_t)r * 128u + ((uint32_t)(c ^ (r & 7)) << 4);
 }
 
-// Slab of the row that entry t (0..8) of a block carries: first the five the
-// scores alone use (the other half's value slabs, the rope key), then this
-// CTA's value slabs in column order.
-__device__ __forceinline__ int slab_of(int t, int half) {
-  return t < 4 ? 4 * (1 - half) + t : t == 4 ? 8 : 4 * half + (t - 5);
+// ---- the CTA pair: distributed shared memory and cluster-scope barriers ----
+// Address of the same shared-memory offset in CTA `rank` of the cluster.
+__device__ __forceinline__ uint32_t peer_addr(uint32_t local, uint32_t rank) {
+  uint32_t r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(local), "r"(rank));
+  return r;
+}
+__device__ __forceinline__ void st_local_v4(uint32_t addr, uint32_t x, uint32_t y, uint32_t z, uint32_t w) {
+  asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(x), "r"(y), "r"(z), "r"(w) : "memory");
+}
+__device__ __forceinline__ float4 ld_local_f4(uint32_t addr) {
+  float4 v;
+  asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];" : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w) : "r"(addr)
+               : "memory");
+  return v;
+}
+// Stores into the partner's shared memory whose bytes count down the
+// partner's barrier `peer_bar` (expect-tx) once they have landed.
+__device__ __forceinline__ void st_async_v4(uint32_t addr, uint32_t x, uint32_t y, uint32_t z, uint32_t w,
+                                            uint32_t peer_bar) {
+  asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.v4.b32 [%0], {%1, %2, %3, %4}, [%5];" ::"r"(addr),
+               "r"(x), "r"(y), "r"(z), "r"(w), "r"(peer_bar)
+               : "memory");
+}
+__device__ __forceinline__ void st_async_f32(uint32_t addr, float v, uint32_t peer_bar) {
+  asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.b32 [%0], %1, [%2];" ::"r"(addr),
+               "r"(__float_as_uint(v)), "r"(peer_bar)
+               : "memory");
+}
+__device__ __forceinline__ bool mbar_try_wait_cluster(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+// Bounded wait on a barrier that the partner arrives on (acquire at cluster scope).
+__device__ __forceinline__ bool mbar_wait_cluster(uint64_t* bar, uint32_t parity, uint64_t limit_ns) {
+  if (mbar_try_wait_cluster(bar, parity)) return true;
+  const uint64_t t0 = global_ns();
+  for (uint32_t it = 1;; ++it) {
+    if (mbar_try_wait_cluster(bar, parity)) return true;
+    if ((it & 31u) == 0 && global_ns() - t0 > limit_ns) return false;
+  }
+}
+// MMA completion signalled to the same barrier in both CTAs of the pair.
+__device__ __forceinline__ void mma_commit_pair(uint64_t* bar) {
+  asm volatile(
+      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(
+          smem_u32(bar)),
+      "h"((uint16_t)3)
+      : "memory");
+}
+// Every thread of both CTAs.
+__device__ __forceinline__ void cluster_sync() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
 }
 
-__global__ void __launch_bounds__(kAttThreads, 1) attend_kernel(AttendArgs a) {
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kAttThreads, 1) attend_kernel(AttendArgs a) {
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
-  const uint32_t pad = ((raw + 1023u) & ~1023u) - raw;
+  const uint32_t pad = ((raw + 1023u) & ~1023u) - raw;  // the same in both CTAs
   uint8_t* smem = smem_raw + pad;
   const uint32_t sb = raw + pad;
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kBarOff);
-  uint64_t* q_full = bars;            // copies and softmax warps: query tile in place
+  uint64_t* q_full = bars;            // copies and softmax: query slabs in place
   uint64_t* e_full = bars + 1;        // [kRing] copies: entry in place
   uint64_t* e_free = e_full + kRing;  // [kRing] MMA: the entry's last reader done
-  uint64_t* s_full = e_free + kRing;  // MMA: S of a block ready
-  uint64_t* p_full = s_full + 1;      // softmax: P of a block in TMEM
-  uint64_t* pv_done = p_full + 1;     // MMA: one more block's P V done
-  uint64_t* o_final = pv_done + 1;    // MMA: the last P V done
+  uint64_t* s_full = e_free + kRing;  // MMA: partial S of a block ready
+  uint64_t* s_free = s_full + 1;      // softmax: S read out
+  uint64_t* xs_full = s_free + 1;     // partner: its partial scores of own rows written (expect-tx)
+  uint64_t* xm_full = xs_full + 1;    // partner: its block maxima (at the end its l) written (expect-tx)
+  uint64_t* p_full = xm_full + 1;     // own softmax threads and the partner's P stores: the P tile complete
+  uint64_t* p_free = p_full + 1;      // both CTAs' MMA: P V of a block done
+  uint64_t* o_final = p_free + 1;     // MMA: the last P V done
   uint64_t* fin = o_final + 1;        // MMA: everything issued is done
   volatile uint32_t* tmem_slot = reinterpret_cast<volatile uint32_t*>(fin + 1);
   volatile uint32_t* abort_flag = tmem_slot + 1;
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   int b = blockIdx.x;
-  const int half = b & 1;
+  const int half = b & 1;  // the rank in the cluster
+  const uint32_t peer = (uint32_t)(half ^ 1);
   b >>= 1;
   const int HG = a.H / kM;
   const int hg = b % HG;
@@ -227,7 +281,7 @@ __global__ void __launch_bounds__(kAttThreads, 1) attend_kernel(AttendArgs a) {
   const int64_t list = ((int64_t)i * a.P + p) * a.k;
   const int64_t qrow0 = ((int64_t)i * a.P + p) * a.H + (int64_t)hg * kM;
   const int nb = (a.k + kBlk - 1) / kBlk;
-  const int ne = nb * kSlabs;  // ring entries over the whole list
+  auto own_rope = [&](int j) { return (j & 1) == half; };
   auto fail = [&]() {
     atomicOr(a.err, kErrTimeout);
     *abort_flag = 1u;
@@ -240,10 +294,19 @@ __global__ void __launch_bounds__(kAttThreads, 1) attend_kernel(AttendArgs a) {
       mbar_init(&e_free[s], 1);
     }
     mbar_init(s_full, 1);
-    mbar_init(p_full, kSoftThreads);
-    mbar_init(pv_done, 1);
+    mbar_init(s_free, kSoftThreads);
+    // The exchange barriers complete when the partner's bytes have landed and
+    // one local arrival has announced how many (for the next phase, right
+    // after the current one is seen complete, before the partner can send).
+    mbar_init(xs_full, 1);
+    mbar_init(xm_full, 1);
+    mbar_init(p_full, kSoftThreads + 1);  // this CTA's softmax threads + the partner's half of P
+    mbar_init(p_free, 2);                 // this CTA's P V and the partner's
     mbar_init(o_final, 1);
     mbar_init(fin, 1);
+    mbar_arrive_expect_tx(xs_full, kXSBytes);
+    mbar_arrive_expect_tx(xm_full, kM * 4);
+    mbar_arrive_expect_tx(p_full, kPSlab);
     *abort_flag = 0u;
     fence_mbar_init();
   }
@@ -255,98 +318,61 @@ __global__ void __launch_bounds__(kAttThreads, 1) attend_kernel(AttendArgs a) {
     asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
   }
   tc_before();
-  __syncthreads();
+  cluster_sync();  // both CTAs' barriers exist before either arrives on the other's
   tc_after();
   const uint32_t tmem = *tmem_slot;
 
-  if (warp >= kSoftWarp0) {
-    // the softmax warps put this CTA's value slabs 4 half + i (i < 4) of
-    // their head's query into TMEM, the A operand of those slabs' S MMAs:
-    // column 32i + x of lane h holds elements 64(4 half + i) + 2x and + 2x + 1
-    // of head h.  Warps 8+q and 12+q (lanes 32q..) take i = 0-1 and 2-3.
-    const int ch = (warp - kSoftWarp0) >> 2;
-    const uint4* qv =
-        reinterpret_cast<const uint4*>(a.q + (size_t)(qrow0 + 32 * (warp & 3) + lane) * kRow) + 32 * half + 16 * ch;
-    const uint32_t qa = tmem + ((uint32_t)(32 * (warp & 3)) << 16) + kColQ + 64u * (uint32_t)ch;
-#pragma unroll 1
-    for (int c = 0; c < 4; ++c) {
-      uint32_t w[16];
-#pragma unroll
-      for (int q4 = 0; q4 < 4; ++q4) {
-        const uint4 x = __ldg(qv + 4 * c + q4);
-        w[4 * q4] = x.x;
-        w[4 * q4 + 1] = x.y;
-        w[4 * q4 + 2] = x.z;
-        w[4 * q4 + 3] = x.w;
-      }
-      tmem_st16(qa + 16u * (uint32_t)c, w);
-    }
-    tmem_wait_st();
-    tc_before();
-    mbar_arrive(q_full);
-  }
   if (warp < kProducers / 32) {
-    // ---- copies: the query slabs of entries 0..4, then every slab of every block ----
+    // ---- copies: the rope query slab, then this CTA's slabs of every block ----
     const uint8_t* qsrc = reinterpret_cast<const uint8_t*>(a.q) + qrow0 * (kRow * 2);
-    constexpr int kQChunks = (kSlabs - kQTmemSlabs) * 8;
-    for (int idx = tid; idx < kM * kQChunks; idx += kProducers) {
-      const int r = idx / kQChunks, g = idx - r * kQChunks;  // 16-byte chunk g of the smem part
-      cp_async16(swz(sb + kQOff + (uint32_t)(g >> 3) * kQSlab, r, g & 7),
-                 qsrc + (size_t)r * (kRow * 2) + slab_of(g >> 3, half) * 128 + (g & 7) * 16);
+    for (int idx = tid; idx < kM * 8; idx += kProducers) {
+      const int r = idx >> 3, c = idx & 7;
+      cp_async16(swz(sb + kQOff, r, c), qsrc + (size_t)r * (kRow * 2) + kRopeSlab * 128 + c * 16);
     }
     cp_async_arrive_noinc(q_full);
     const uint8_t* ubase = reinterpret_cast<const uint8_t*>(a.hot) + (size_t)u * a.C * (kRow * 2);
-    // this thread copies chunk csub of rows rsub + kRowStep m of every entry
+    // this thread copies chunk csub of rows rsub + kRowStep m of every entry;
+    // the slots of the next block's rows are read a block ahead
     const int rsub = tid >> 3, csub = tid & 7;
-    // slots of this thread's rows of the current block (rs) and of the next
-    // (rs_next, loaded a block ahead so that a block's first copies do not
-    // wait for them)
     int32_t rs[kBlk / kRowStep], rs_next[kBlk / kRowStep];
-    auto load_rows = [&](int j, int32_t (&dst)[kBlk / kRowStep]) {
+    auto load_rows = [&](int j) {
 #pragma unroll
       for (int m = 0; m < kBlk / kRowStep; ++m) {
         const int r = j * kBlk + rsub + kRowStep * m;
-        dst[m] = j < nb && r < a.k ? __ldg(a.slots + list + r) : -1;
+        rs_next[m] = j < nb && r < a.k ? __ldg(a.slots + list + r) : -1;
       }
     };
-    load_rows(0, rs_next);
-    int rs_block = -1;
-    auto issue = [&](int e) {
-      const int j = e / kSlabs, t = e - j * kSlabs;
-      if (j != rs_block) {  // blocks are issued in order: rs_next holds block j
-#pragma unroll
-        for (int m = 0; m < kBlk / kRowStep; ++m)  // a pad reads a valid row; the softmax drops it
-          rs[m] = rs_next[m] < 0 || rs_next[m] >= a.C ? 0 : rs_next[m];
-        rs_block = j;
-        load_rows(j + 1, rs_next);
-      }
-      const uint32_t dst = sb + kROff + (uint32_t)(e % kRing) * kEntry;
-      const int s = slab_of(t, half);
+    auto issue = [&](int slab, int slot) {
+      const uint32_t dst = sb + kROff + (uint32_t)slot * kEntry;
 #pragma unroll
       for (int m = 0; m < kBlk / kRowStep; ++m)
-        cp_async16(swz(dst, rsub + kRowStep * m, csub), ubase + (size_t)rs[m] * (kRow * 2) + s * 128 + csub * 16);
-      cp_async_arrive_noinc(&e_full[e % kRing]);  // counts once this thread's copies have landed
+        cp_async16(swz(dst, rsub + kRowStep * m, csub), ubase + (size_t)rs[m] * (kRow * 2) + slab * 128 + csub * 16);
+      cp_async_arrive_noinc(&e_full[slot]);  // counts once this thread's copies have landed
     };
-    // Entries go out in order, each as soon as its ring slot is free; a
-    // block's first entry only once the previous block has landed (its last
-    // entry's barrier has completed): the value slabs of a block are on the
-    // critical path (their slots free up only when the last block's P V is
-    // done), and the next block's slabs would share the copy bandwidth with
-    // them.  Completion is tracked by the entry's barrier itself, so the
-    // warps never wait for their own copies and keep the ring full.
-    for (int e = 0; e < ne; ++e) {
+    load_rows(0);
+    // A block's value slabs reuse the slots of block j-2's, freed by its P V;
+    // the rope slot is reused every other block (the blocks of this CTA's parity).
+    for (int j = 0; j < nb; ++j) {
       if (__any_sync(kFull, *abort_flag != 0u)) break;  // warp-uniform: shuffles follow
-      const int j = e / kSlabs, t = e - j * kSlabs;
+      const int vb = kVSlabs * (j & 1);
       bool ok = true;
-      if (t == 0 && j > 0)
-        ok = __all_sync(kFull, mbar_wait(&e_full[kSlabs - 1], (j - 1) & 1, a.wait_ns));
-      if (ok && e >= kRing)
-        ok = __all_sync(kFull, mbar_wait(&e_free[t], ((e / kRing) - 1) & 1, a.wait_ns));
+      if (j >= 2) {
+        const uint32_t par = (uint32_t)((j >> 1) - 1) & 1u;
+#pragma unroll
+        for (int v = 0; v < kVSlabs; ++v) ok = ok && __all_sync(kFull, mbar_wait(&e_free[vb + v], par, a.wait_ns));
+        if (own_rope(j)) ok = ok && __all_sync(kFull, mbar_wait(&e_free[kRing - 1], par, a.wait_ns));
+      }
       if (!ok) {
         fail();
         break;
       }
-      issue(e);
+#pragma unroll
+      for (int m = 0; m < kBlk / kRowStep; ++m)  // a pad reads a valid row; the softmax drops it
+        rs[m] = rs_next[m] < 0 || rs_next[m] >= a.C ? 0 : rs_next[m];
+      load_rows(j + 1);
+      if (own_rope(j)) issue(kRopeSlab, kRing - 1);
+#pragma unroll
+      for (int v = 0; v < kVSlabs; ++v) issue(kVSlabs * half + v, vb + v);
     }
     cp_async_wait_all();
   } else if (warp == kMmaWarp) {
@@ -356,207 +382,267 @@ __global__ void __launch_bounds__(kAttThreads, 1) attend_kernel(AttendArgs a) {
       constexpr uint32_t kIdPV = idesc_bf16(kM, kHalfCols, true);
       bool ok = mbar_wait(q_full, 0, a.wait_ns);
       fence_proxy_async_smem();  // the tensor cores read what cp.async wrote (acquired through the barrier)
-      // entry t always sits in ring slot t: the descriptors are fixed
-      uint64_t kd[kSlabs], qd[kSlabs];
-      uint32_t qa[kSlabs];
+      // ring slot s: kd0 + s * (kEntry >> 4) (the start address field, in 16-byte units)
+      const uint64_t kd0 = sdesc(sb + kROff, 16, 1024);
+      auto kd = [&](int s) { return kd0 + (uint64_t)((uint32_t)s * (kEntry >> 4)); };
+      const uint64_t qd_rope = sdesc(sb + kQOff, 16, 1024);
+      // P tile: K step kk is in slab kk / 4 at byte 32 (kk % 4) of each row
+      uint64_t pd[kBlk / 16];
 #pragma unroll
-      for (int t = 0; t < kSlabs; ++t) {
-        const int tq = t - (kSlabs - kQTmemSlabs);  // >= 0: the query slab is in TMEM
-        kd[t] = sdesc(sb + kROff + (uint32_t)t * kEntry, 16, 1024);
-        qd[t] = sdesc(sb + kQOff + (uint32_t)(tq < 0 ? t : 0) * kQSlab, 16, 1024);
-        qa[t] = tmem + kColQ + 32u * (uint32_t)(tq < 0 ? 0 : tq);
-      }
-      // V: the four value slabs of a block in slots kSlabs-kVSlabs.. are the
-      // four 64-column chunks of one N = 256 MN-major operand (chunk stride:
-      // one ring entry; 8-row groups 1 KB apart)
-      const uint64_t vdesc = sdesc(sb + kROff + (uint32_t)(kSlabs - kVSlabs) * kEntry, kEntry, 1024);
-      int pv_next = 0;  // first block whose P V is not issued yet
-      // O += P V for block jj; the value slabs' entries are freed once done
+      for (int kk = 0; kk < kBlk / 16; ++kk)
+        pd[kk] = sdesc(sb + kPOff + (uint32_t)(kk >> 2) * kPSlab, 16, 1024) + (uint32_t)((kk & 3) * 2);
+      // O += P V for block jj; V: the block's four value slabs side by side, the
+      // four 64-column chunks of one N = 256 MN-major operand (chunk stride one
+      // entry, 8-row groups 1 KB apart)
       auto issue_pv = [&](int jj) -> bool {
-        if (!mbar_wait(&p_full[0], jj & 1, a.wait_ns)) return false;
+        if (!mbar_wait_cluster(p_full, jj & 1, a.wait_ns)) return false;
+        if (jj + 1 < nb) mbar_arrive_expect_tx(p_full, kPSlab);  // the partner's half of the next P
+        fence_proxy_async_smem();  // P was written with ordinary and asynchronous stores
         tc_after();
-        const uint32_t pa = tmem + kColS;  // P: first 64 columns of S
+        const int vb = kVSlabs * (jj & 1);
+        const uint64_t vdesc = sdesc(sb + kROff + (uint32_t)vb * kEntry, kEntry, 1024);
 #pragma unroll
         for (int kk = 0; kk < kBlk / 16; ++kk)
-          mma_ts(tmem + kColO, pa + 8u * (uint32_t)kk, vdesc + ((uint32_t)kk * 16u * 128u >> 4), kIdPV,
-                 (jj > 0 || kk > 0) ? 1u : 0u);
+          mma_ss(tmem + kColO, pd[kk], vdesc + ((uint32_t)kk * 16u * 128u >> 4), kIdPV, (jj > 0 || kk > 0) ? 1u : 0u);
 #pragma unroll
-        for (int v = 0; v < kVSlabs; ++v) mma_commit(&e_free[kSlabs - kVSlabs + v]);
-        mma_commit(pv_done);
+        for (int v = 0; v < kVSlabs; ++v) mma_commit(&e_free[vb + v]);
+        mma_commit_pair(p_free);  // both CTAs learn that this P tile and these slots are free
         return true;
       };
-      auto flush_pv = [&](int upto) -> bool {  // P V of blocks pv_next..upto, in order
-        for (; pv_next <= upto; ++pv_next)
-          if (!issue_pv(pv_next)) return false;
-        return true;
-      };
+      const uint32_t dS = tmem + kColS;
       for (int j = 0; ok && j < nb; ++j) {
-        // S holds P of block j-1 until its P V is issued (the tensor pipe runs
-        // MMAs in order, so P is read before this block's S overwrites it);
-        // the same P V frees the value slots this block's entries 5..8 reuse
-        if (j >= 1 && !flush_pv(j - 1)) {
+        // S(j) overwrites S(j-1) once the softmax has read it out
+        if (j >= 1 && !mbar_wait(s_free, (j - 1) & 1, a.wait_ns)) {
           ok = false;
           break;
         }
-        const uint32_t dS = tmem + kColS;
-#pragma unroll
-        for (int t = 0; t < kSlabs; ++t) {
-          const int e = j * kSlabs + t;
-          if (*abort_flag || !mbar_wait(&e_full[t], (e / kRing) & 1, a.wait_ns)) {
+        tc_after();
+        const uint32_t par = (uint32_t)(j >> 1) & 1u;
+        uint32_t acc = 0u;
+        if (own_rope(j)) {
+          if (*abort_flag || !mbar_wait(&e_full[kRing - 1], par, a.wait_ns)) {
             ok = false;
             break;
           }
-          fence_proxy_async_smem();  // as for the query slabs
+          fence_proxy_async_smem();
           tc_after();
-          if (t >= kSlabs - kQTmemSlabs) {  // A: the query slab in TMEM (8 columns per K step)
 #pragma unroll
-            for (int kk = 0; kk < 4; ++kk)
-              mma_ts(dS, qa[t] + 8u * (uint32_t)kk, kd[t] + (uint32_t)(kk * 2), kIdQK, (t > 0 || kk > 0) ? 1u : 0u);
-          } else {  // A: from shared memory
+          for (int kk = 0; kk < 4; ++kk)
+            mma_ss(dS, qd_rope + (uint32_t)(kk * 2), kd(kRing - 1) + (uint32_t)(kk * 2), kIdQK, (kk > 0) ? 1u : 0u);
+          mma_commit(&e_free[kRing - 1]);
+          acc = 1u;
+        }
+        const int vb = kVSlabs * (j & 1);
 #pragma unroll
-            for (int kk = 0; kk < 4; ++kk)
-              mma_ss(dS, qd[t] + (uint32_t)(kk * 2), kd[t] + (uint32_t)(kk * 2), kIdQK, (t > 0 || kk > 0) ? 1u : 0u);
+        for (int v = 0; v < kVSlabs; ++v) {
+          if (*abort_flag || !mbar_wait(&e_full[vb + v], par, a.wait_ns)) {
+            ok = false;
+            break;
           }
-          if (t < kSlabs - kVSlabs) mma_commit(&e_free[t]);  // only the scores read this slab
+          fence_proxy_async_smem();
+          tc_after();
+#pragma unroll
+          for (int kk = 0; kk < 4; ++kk)
+            mma_ts(dS, tmem + kColQ + 32u * (uint32_t)v + 8u * (uint32_t)kk, kd(vb + v) + (uint32_t)(kk * 2), kIdQK,
+                   (acc || v > 0 || kk > 0) ? 1u : 0u);
         }
         if (!ok) break;
-        mma_commit(&s_full[0]);
+        mma_commit(s_full);
+        if (j >= 1 && !issue_pv(j - 1)) {
+          ok = false;
+          break;
+        }
       }
-      if (ok && !flush_pv(nb - 1)) ok = false;
+      if (ok && !issue_pv(nb - 1)) ok = false;
       if (ok) mma_commit(o_final);
       if (!ok) fail();
       mma_commit(fin);  // everything issued above is complete before TMEM is freed
       if (!mbar_wait(fin, 0, a.wait_ns)) fail();
     }
     __syncwarp();
-  } else if (warp >= kSoftWarp0) {
-    // ---- online softmax: warps 8+q and 12+q share the heads (TMEM lanes)
-    // 32q..32q+31, one thread per head and half (ch) of each block's rows ----
-    const int q = warp & 3, ch = (warp - kSoftWarp0) >> 2;
-    const int h = 32 * q + lane;
-    const uint32_t lane_addr = (uint32_t)(32 * q) << 16;
+  } else if (warp >= kSoftWarp0 && warp < kSoftWarp0 + kSoftThreads / 32) {
+    // ---- online softmax: head hd (TMEM lane hd), rows 64 half.. of each block ----
+    const int hd = tid - kSoftWarp0 * 32;
+    const uint32_t lane_addr = (uint32_t)(32 * (warp & 3)) << 16;
     const uint32_t sS = tmem + lane_addr + kColS;
-    // exchange slots: the last two S columns of each half, read by their
-    // owner before the exchange and written by no MMA until P is consumed
-    const uint32_t x_mine = sS + 64u * (uint32_t)ch + 62u, x_peer = sS + 64u * (uint32_t)(1 - ch) + 62u;
+    {  // this CTA's query slabs 4 half + i into TMEM: column 32i + x holds elements 64(4 half + i) + 2x, + 2x + 1
+      const uint4* qv = reinterpret_cast<const uint4*>(a.q + (size_t)(qrow0 + hd) * kRow) + 32 * half;
+#pragma unroll 1
+      for (int c = 0; c < 8; ++c) {
+        uint32_t w[16];
+#pragma unroll
+        for (int q4 = 0; q4 < 4; ++q4) {
+          const uint4 x = __ldg(qv + 4 * c + q4);
+          w[4 * q4] = x.x;
+          w[4 * q4 + 1] = x.y;
+          w[4 * q4 + 2] = x.z;
+          w[4 * q4 + 3] = x.w;
+        }
+        tmem_st16(tmem + lane_addr + kColQ + 16u * (uint32_t)c, w);
+      }
+      tmem_wait_st();
+      tc_before();
+      mbar_arrive(q_full);
+    }
+    // the partner's shared memory: where this thread's partial scores of its
+    // rows, block maxima and P go, and its barriers
+    const uint32_t xs_peer = peer_addr(sb + kXSOff, peer), xm_peer = peer_addr(sb + kXMOff, peer);
+    const uint32_t p_peer = peer_addr(sb + kPOff, peer);
+    const uint32_t xs_full_peer = peer_addr(smem_u32(xs_full), peer), xm_full_peer = peer_addr(smem_u32(xm_full), peer);
+    const uint32_t p_full_peer = peer_addr(smem_u32(p_full), peer);
+    // partial scores of head hd, rows 4c..4c+3 of the 64: 16-byte cell
+    // (c, hd), so that a warp's stores fill consecutive banks
+    auto xs_off = [&](int c) { return ((uint32_t)c * kM + (uint32_t)hd) * 16u; };
+    // P of head hd, rows 64 half + 8c..: 16-byte chunk c of the head's row in slab `half`
+    const uint32_t p_row = (uint32_t)half * kPSlab + (uint32_t)hd * 128u;
     const float sl2 = a.scale_log2;
     float m_run = -INFINITY, l_run = 0.f;
     bool ok = true;
-    // slots of this half's rows 64ch + 32c + lane of the next block (validity masks)
+    // slots of rows 64 half + 32c + lane of the next block (validity masks)
     int32_t sn[2];
     auto load_valid = [&](int j) {
 #pragma unroll
       for (int c = 0; c < 2; ++c) {
-        const int r = j * kBlk + 64 * ch + 32 * c + lane;
+        const int r = j * kBlk + kOwnRows * half + 32 * c + lane;
         sn[c] = j < nb && r < a.k ? __ldg(a.slots + list + r) : -1;
       }
     };
-    // the partner warps pass (stop flag, value) through TMEM and a named
-    // barrier, so that they take every decision (stop, rescale) together;
-    // every exchange is reached by both (a stop is taken only after one)
-    uint32_t peer_stop, peer_val;
-    auto exchange = [&](bool stop_mine, float val) {
-      tmem_st2(x_mine, stop_mine ? 1u : 0u, __float_as_uint(val));
-      tmem_wait_st();
-      tc_before();
-      named_bar_sync(1 + q, 64);
-      tc_after();
-      tmem_ld2(x_peer, peer_stop, peer_val);
-      tmem_wait_ld();
-    };
     load_valid(0);
     for (int j = 0; j < nb; ++j) {
-      bool stop = __any_sync(kFull, *abort_flag != 0u);
-      if (!stop) stop = !__all_sync(kFull, mbar_wait(&s_full[0], j & 1, a.wait_ns));
+      // every decision below is warp-uniform; the waits are bounded, so a warp
+      // that stops leaves the others and the partner to time out
+      bool f = __any_sync(kFull, *abort_flag != 0u);
+      if (!f) f = !__all_sync(kFull, mbar_wait(s_full, j & 1, a.wait_ns));
+      // the partner has read what this CTA sent for the last block: its block
+      // maximum, which came after, has arrived
+      if (f) {
+        ok = false;
+        break;
+      }
       tc_after();
       uint32_t vm[2];
 #pragma unroll
       for (int c = 0; c < 2; ++c) vm[c] = __ballot_sync(kFull, sn[c] >= 0 && sn[c] < a.C);
       load_valid(j + 1);
-      // this half's 64 scores, log2-scaled, -inf for dropped rows
-      float t[64];
-      tmem_ld32(sS + 64u * (uint32_t)ch, *reinterpret_cast<float(*)[32]>(&t[0]));
-      tmem_ld32(sS + 64u * (uint32_t)ch + 32u, *reinterpret_cast<float(*)[32]>(&t[32]));
-      tmem_wait_ld();
-      float mx = -INFINITY;
-      if ((vm[0] & vm[1]) == kFull) {  // every row listed (the masks are the same in all lanes)
+      // own rows' partial scores to registers; the partner's rows' to its memory
+      float t[kOwnRows];
+      tmem_ld32(sS + (uint32_t)(kOwnRows * half), *reinterpret_cast<float(*)[32]>(&t[0]));
+      tmem_ld32(sS + (uint32_t)(kOwnRows * half) + 32u, *reinterpret_cast<float(*)[32]>(&t[32]));
 #pragma unroll
-        for (int i = 0; i < 64; ++i) {
-          t[i] *= sl2;
-          mx = fmaxf(mx, t[i]);
+      for (int h2 = 0; h2 < 2; ++h2) {
+        float ps[32];
+        tmem_ld32(sS + (uint32_t)(kOwnRows * (int)peer) + 32u * (uint32_t)h2, ps);
+        tmem_wait_ld();
+        if (h2 == 1) {  // S is read out: the next block's S may start
+          tc_before();
+          mbar_arrive(s_free);
         }
-      } else {
 #pragma unroll
-        for (int i = 0; i < 64; ++i) {
-          t[i] = ((vm[i >> 5] >> (i & 31)) & 1u) ? t[i] * sl2 : -INFINITY;
-          mx = fmaxf(mx, t[i]);
-        }
+        for (int c = 0; c < 8; ++c)
+          st_async_v4(xs_peer + xs_off(8 * h2 + c), __float_as_uint(ps[4 * c]), __float_as_uint(ps[4 * c + 1]),
+                      __float_as_uint(ps[4 * c + 2]), __float_as_uint(ps[4 * c + 3]), xs_full_peer);
       }
-      exchange(stop, mx);
-      if (__any_sync(kFull, stop || peer_stop != 0u)) {  // warp-uniform, and the same in both partners
+      if (!__all_sync(kFull, mbar_wait_cluster(xs_full, j & 1, a.wait_ns))) {
         ok = false;
         break;
       }
-      mx = fmaxf(mx, __uint_as_float(peer_val));
-      // the maximum moves only when a score passes it by more than 2^8 (always
-      // on the first block with a listed row); O is then rescaled in TMEM
+      if (hd == 0 && j + 1 < nb) mbar_arrive_expect_tx(xs_full, kXSBytes);
+#pragma unroll
+      for (int c = 0; c < kOwnRows / 4; ++c) {
+        const float4 x = ld_local_f4(sb + kXSOff + xs_off(c));
+        t[4 * c] += x.x;
+        t[4 * c + 1] += x.y;
+        t[4 * c + 2] += x.z;
+        t[4 * c + 3] += x.w;
+      }
+      // log2-scaled scores, -inf for dropped rows, and their maximum
+      float mx = -INFINITY;
+      if ((vm[0] & vm[1]) == kFull) {  // every row listed (the masks are the same in all lanes)
+#pragma unroll
+        for (int r = 0; r < kOwnRows; ++r) {
+          t[r] *= sl2;
+          mx = fmaxf(mx, t[r]);
+        }
+      } else {
+#pragma unroll
+        for (int r = 0; r < kOwnRows; ++r) {
+          t[r] = ((vm[r >> 5] >> (r & 31)) & 1u) ? t[r] * sl2 : -INFINITY;
+          mx = fmaxf(mx, t[r]);
+        }
+      }
+      st_async_f32(xm_peer + (uint32_t)(((j & 1) * kM + hd) * 4), mx, xm_full_peer);
+      if (!__all_sync(kFull, mbar_wait_cluster(xm_full, j & 1, a.wait_ns))) {
+        ok = false;
+        break;
+      }
+      if (hd == 0) mbar_arrive_expect_tx(xm_full, kM * 4);  // the next block's maxima, or at the end the l
+      mx = fmaxf(mx, reinterpret_cast<const float*>(smem + kXMOff)[(j & 1) * kM + hd]);
+      // Both CTAs hold the same maxima and running maximum, so they take the
+      // same decisions.  The running maximum moves only when a score passes it
+      // by more than 2^8 (always on the first block with a listed row); O is
+      // then rescaled, once the last P V is done.
+      bool pv_seen = j == 0;
       if (__any_sync(kFull, mx > m_run + kRescaleLog2)) {
         const float m_new = fmaxf(m_run, mx);
-        const float f = m_new == -INFINITY ? 1.f : exp2f(m_run - m_new);
-        l_run *= f;
-        if (j > 0) {  // O holds P V of blocks 0..j-1
-          if (!__all_sync(kFull, mbar_wait(pv_done, (j - 1) & 1, a.wait_ns))) {
-            fail();  // the partner learns of it at the next exchange
-          } else {
-            tc_after();
-#pragma unroll 1
-            for (int c0 = 0; c0 < kHalfCols / 2; c0 += 32) {
-              const uint32_t oa = tmem + lane_addr + kColO + (uint32_t)(kHalfCols / 2 * ch + c0);
-              float o[32];
-              tmem_ld32(oa, o);
-              tmem_wait_ld();
-              uint32_t w[32];
-#pragma unroll
-              for (int c = 0; c < 32; ++c) w[c] = __float_as_uint(o[c] * f);
-              tmem_st32(oa, w);
-            }
-            tmem_wait_st();
+        const float fac = m_new == -INFINITY ? 1.f : exp2f(m_run - m_new);
+        l_run *= fac;
+        if (j > 0) {
+          if (!__all_sync(kFull, mbar_wait_cluster(p_free, (j - 1) & 1, a.wait_ns))) {
+            ok = false;
+            break;
           }
+          pv_seen = true;
+          tc_after();
+#pragma unroll 1
+          for (int c0 = 0; c0 < kHalfCols; c0 += 16) {
+            uint32_t w[16];
+            tmem_ld16(tmem + lane_addr + kColO + (uint32_t)c0, w);
+            tmem_wait_ld();
+#pragma unroll
+            for (int c = 0; c < 16; ++c) w[c] = __float_as_uint(__uint_as_float(w[c]) * fac);
+            tmem_st16(tmem + lane_addr + kColO + (uint32_t)c0, w);
+          }
+          tmem_wait_st();
         }
         m_run = m_new;
       }
+      // the P tiles are free once both CTAs' P V of the last block is done
+      if (!pv_seen && !__all_sync(kFull, mbar_wait_cluster(p_free, (j - 1) & 1, a.wait_ns))) {
+        ok = false;
+        break;
+      }
       const float mu = m_run == -INFINITY ? 0.f : m_run;
-      // P rounded to bf16 over columns 32ch.. of S (every thread has read its
-      // scores: the exchange came after); l sums the rounded weights
+      // P of the 64 rows (bf16) into both CTAs' P tile; l sums the rounded weights
       float ls = 0.f;
 #pragma unroll
-      for (int c = 0; c < 2; ++c) {
-        uint32_t w[16];
+      for (int c = 0; c < kOwnRows / 8; ++c) {
+        uint32_t w[4];
 #pragma unroll
-        for (int e = 0; e < 16; ++e) {
-          const __nv_bfloat162 b2 = __floats2bfloat162_rn(ex2_ftz(t[32 * c + 2 * e] - mu), ex2_ftz(t[32 * c + 2 * e + 1] - mu));
+        for (int e = 0; e < 4; ++e) {
+          const __nv_bfloat162 b2 = __floats2bfloat162_rn(ex2_ftz(t[8 * c + 2 * e] - mu), ex2_ftz(t[8 * c + 2 * e + 1] - mu));
           ls += __low2float(b2) + __high2float(b2);
           w[e] = *reinterpret_cast<const uint32_t*>(&b2);
         }
-        tmem_st16(sS + 32u * (uint32_t)ch + 16u * (uint32_t)c, w);
+        const uint32_t off = p_row + ((uint32_t)(c ^ (hd & 7)) << 4);
+        st_local_v4(sb + kPOff + off, w[0], w[1], w[2], w[3]);
+        st_async_v4(p_peer + off, w[0], w[1], w[2], w[3], p_full_peer);
       }
-      tmem_wait_st();
       l_run += ls;
-      tc_before();
-      mbar_arrive(&p_full[0]);
+      mbar_arrive(p_full);
     }
     if (ok) ok = __all_sync(kFull, mbar_wait(o_final, 0, a.wait_ns));
     tc_after();
-    // l of the whole row: both halves' sums (no MMA touches S any more)
-    exchange(!ok, l_run);
-    if (ok && peer_stop == 0u) {
-      const float l = l_run + __uint_as_float(peer_val);
+    // l of the whole row: this CTA's rows and the partner's
+    st_async_f32(xm_peer + (uint32_t)(((nb & 1) * kM + hd) * 4), l_run, xm_full_peer);
+    const bool lx = __all_sync(kFull, mbar_wait_cluster(xm_full, nb & 1, a.wait_ns));
+    if (ok && lx) {
+      const float l = l_run + reinterpret_cast<const float*>(smem + kXMOff)[(nb & 1) * kM + hd];
       const float inv = l > 0.f ? 1.f / l : 0.f;
-      uint16_t* orow = a.out + (size_t)(qrow0 + h) * kVal + (size_t)half * kHalfCols + (size_t)(kHalfCols / 2) * ch;
+      uint16_t* orow = a.out + (size_t)(qrow0 + hd) * kVal + (size_t)half * kHalfCols;
 #pragma unroll 1
-      for (int c0 = 0; c0 < kHalfCols / 2; c0 += 32) {
+      for (int c0 = 0; c0 < kHalfCols; c0 += 32) {
         float o[32];
-        tmem_ld32(tmem + lane_addr + kColO + (uint32_t)(kHalfCols / 2 * ch + c0), o);
+        tmem_ld32(tmem + lane_addr + kColO + (uint32_t)c0, o);
         tmem_wait_ld();
         uint32_t w[16];
 #pragma unroll
@@ -568,14 +654,14 @@ __global__ void __launch_bounds__(kAttThreads, 1) attend_kernel(AttendArgs a) {
 #pragma unroll
         for (int q4 = 0; q4 < 4; ++q4) dst[q4] = make_uint4(w[4 * q4], w[4 * q4 + 1], w[4 * q4 + 2], w[4 * q4 + 3]);
       }
-      if (half == 0 && ch == 0 && a.lse)
-        a.lse[qrow0 + h] = l > 0.f ? (m_run + log2f(l)) * 0.6931471805599453f : -INFINITY;
+      if (half == 0 && a.lse)
+        a.lse[qrow0 + hd] = l > 0.f ? (m_run + log2f(l)) * 0.6931471805599453f : -INFINITY;
     } else {
       fail();
     }
   }
   tc_before();
-  __syncthreads();
+  cluster_sync();  // no access to the partner's shared memory after this
   if (warp == kMmaWarp) {
     tc_after();
     asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(kTmemCols) : "memory");
