@@ -27,7 +27,7 @@
 // N = 128, P V is eight MMAs of N = 256.  S is freed as soon as the softmax
 // has read it (P lives in shared memory), so the next block's S overlaps the
 // softmax of this one.
-//   warps 0-1  copy the rope query slab, then this CTA's slabs of every
+//   warps 0-3  copy the rope query slab, then this CTA's slabs of every
 //              block with 16-byte cp.async into the 128-byte-swizzled
 //              K-major layout; completion is counted by each ring entry's
 //              mbarrier (cp.async.mbarrier.arrive.noinc), so they never
@@ -40,7 +40,7 @@
 //              is then rescaled in TMEM); P is rounded to bf16 and l sums the
 //              rounded weights, so out is their exact weighted mean; at the
 //              end the pair adds its two l, and O / l in bf16 and lse;
-//   warp 2     holds 512 TMEM columns; lane 0 issues every tcgen05.mma:
+//   warp 8     holds 512 TMEM columns; lane 0 issues every tcgen05.mma:
 //              S(j) (A: query slabs in TMEM, the rope one in shared memory),
 //              then P V of block j-1 (A: P tile, B: value slabs).
 // Every mbarrier wait is bounded: on expiry the CTA sets kErrTimeout in the
@@ -62,10 +62,10 @@ constexpr int kVSlabs = 4;                // value slabs of one CTA
 constexpr int kRopeSlab = 8;              // slab of the rope key
 constexpr int kRing = 2 * kVSlabs + 1;    // value slabs of two blocks + the rope slab
 constexpr int kHalfCols = kVal / 2;       // value columns per CTA
-constexpr int kAttThreads = 256;
-constexpr int kProducers = 64;            // warps 0-1: copies
-constexpr int kMmaWarp = 2;               // TMEM allocation and MMA issue
+constexpr int kAttThreads = 288;
+constexpr int kProducers = 128;           // warps 0-3: copies
 constexpr int kSoftWarp0 = 4;             // warps 4-7: softmax
+constexpr int kMmaWarp = 8;               // TMEM allocation and MMA issue
 constexpr int kSoftThreads = 128;
 constexpr int kRowStep = kProducers / 8;  // rows of an entry between one copy thread's chunks
 constexpr uint32_t kQSlab = kM * 128;     // one slab of the query tile
@@ -524,24 +524,23 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kAttThreads, 1) atte
 #pragma unroll
       for (int c = 0; c < 2; ++c) vm[c] = __ballot_sync(kFull, sn[c] >= 0 && sn[c] < a.C);
       load_valid(j + 1);
-      // own rows' partial scores to registers; the partner's rows' to its memory
-      float t[kOwnRows];
-      tmem_ld32(sS + (uint32_t)(kOwnRows * half), *reinterpret_cast<float(*)[32]>(&t[0]));
-      tmem_ld32(sS + (uint32_t)(kOwnRows * half) + 32u, *reinterpret_cast<float(*)[32]>(&t[32]));
+      // the partner's rows' partial scores to its memory, then own rows' to registers
 #pragma unroll
       for (int h2 = 0; h2 < 2; ++h2) {
         float ps[32];
         tmem_ld32(sS + (uint32_t)(kOwnRows * (int)peer) + 32u * (uint32_t)h2, ps);
         tmem_wait_ld();
-        if (h2 == 1) {  // S is read out: the next block's S may start
-          tc_before();
-          mbar_arrive(s_free);
-        }
 #pragma unroll
         for (int c = 0; c < 8; ++c)
           st_async_v4(xs_peer + xs_off(8 * h2 + c), __float_as_uint(ps[4 * c]), __float_as_uint(ps[4 * c + 1]),
                       __float_as_uint(ps[4 * c + 2]), __float_as_uint(ps[4 * c + 3]), xs_full_peer);
       }
+      float t[kOwnRows];
+      tmem_ld32(sS + (uint32_t)(kOwnRows * half), *reinterpret_cast<float(*)[32]>(&t[0]));
+      tmem_ld32(sS + (uint32_t)(kOwnRows * half) + 32u, *reinterpret_cast<float(*)[32]>(&t[32]));
+      tmem_wait_ld();
+      tc_before();
+      mbar_arrive(s_free);  // S is read out: the next block's S may start
       if (!__all_sync(kFull, mbar_wait_cluster(xs_full, j & 1, a.wait_ns))) {
         ok = false;
         break;
