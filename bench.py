@@ -343,8 +343,8 @@ def run_attention(args, kv, wl, units, device, torch):
     """Time kvo_attend (decode step 7) on the slots of the last step, on its own.
 
     Algorithmic work per (unit, position): 2 * H * n * (576 + 512) FLOPs for n listed rows
-    (scores over the full row, values over the latent part).  The kernel computes the
-    scores once per half of the value columns, so it executes 2 * H * n * (2 * 576 + 512)."""
+    (scores over the full row, values over the latent part).  The kernel's CTA pair splits
+    the scores by slab, so it executes exactly that."""
     import numpy as np
     import workload as W
     H = args.attend_heads
@@ -373,11 +373,11 @@ def run_attention(args, kv, wl, units, device, torch):
     ms = [ev[2 * i].elapsed_time(ev[2 * i + 1]) for i in range(n_launch)]
     t = statistics.mean(ms)
     flops = 2.0 * H * n_rows * (576 + 512)
-    flops_exec = 2.0 * H * n_rows * (2 * 576 + 512)
+    flops_exec = flops
     peak, src = load_bf16_peak()
     achieved = flops / (t * 1e-3) / 1e12
-    ctas = U * P * (H // 128) * 2
-    rows_bytes = ctas * k * 1152 + U * P * H * 576 * 2
+    # each CTA of a pair reads its own slabs: the pair reads every listed row once
+    rows_bytes = U * P * (H // 128) * k * 1152 + U * P * H * 576 * 2
     return {
         "kernel": "attend_kernel", "heads": H, "scale": round(scale, 6), "launches": n_launch,
         "ms_per_launch": round(t, 4), "ms_min": round(min(ms), 4),
