@@ -18,7 +18,8 @@
 // multiplied once per pair.  Per block:
 //   - each CTA sends its partial scores of the partner's rows into the
 //     partner's shared memory and adds the partner's partial scores of its
-//     own rows (distributed shared memory, mbarriers with cluster scope);
+//     own rows (distributed shared memory: st.async, whose bytes count down
+//     the receiver's expect-tx barrier, so no arrival travels with them);
 //   - the two agree on each head's block maximum the same way;
 //   - each writes P (bf16) of its 64 rows into both CTAs' P tile, and each
 //     computes O[:, own 256 columns] += P V over all 128 rows.
