@@ -98,19 +98,21 @@ def _run(wl, H=128, scales=(SCALE,), steps=None, check_units=None, units_each_st
 
 
 def test_attend_reduced_mtp3():
-    # several 32-row blocks per list, four positions, three steps of a drifting query
+    # two 128-row blocks per list (one for each CTA of a pair's rope turn), four
+    # positions, three steps of a drifting query
     wl = W.Workload("att", 2, 2, 3000, 4, 4, 256, 1100, 3, 0.9, 90)
     assert _run(wl, scales=(SCALE, 0.5, 0.01)) == 2 * 2 * 4 * 3 * 3
 
 
 def test_attend_ragged_list_and_pads():
-    # k = 200 is not a multiple of 32 (last block partial) and the context is shorter
+    # k = 200 is not a multiple of 128 (last block partial) and the context is shorter
     # than k, so every list carries pads (slot -1)
     wl = W.Workload("attpad", 1, 2, 120, 2, 2, 200, 512, 2, 0.5, 91)
     assert _run(wl) > 0
 
 
 def test_attend_two_head_groups():
+    # k = 96: a single, partial block (the rope slab goes to the first CTA of each pair)
     wl = W.Workload("atth", 1, 2, 2000, 2, 2, 96, 400, 2, 0.8, 92)
     assert _run(wl, H=256, scales=(SCALE, 0.3)) > 0
 
@@ -123,6 +125,7 @@ def test_attend_growing_maximum_rescales():
 
 
 def test_attend_unit_subset():
+    # k = 64: a single, partial block
     wl = W.Workload("attsub", 2, 2, 1500, 2, 2, 64, 256, 2, 0.7, 94)
     r = Runner(wl)
     try:
