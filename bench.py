@@ -128,6 +128,48 @@ def huge_backed_fraction(addr):
     return None
 
 
+def numa_spread(addr):
+    """Share of the pages of the mapping that holds host address addr on each NUMA node
+    (from /proc/self/numa_maps), e.g. {"N0": 1.0}, or None when it cannot be read.  Where
+    a pinned pool sits decides how fast the host link can read it."""
+    try:
+        with open("/proc/self/numa_maps") as f:
+            lines = f.read().splitlines()
+    except OSError:
+        return None
+    best = None
+    for line in lines:
+        parts = line.split()
+        try:
+            start = int(parts[0], 16)
+        except (ValueError, IndexError):
+            continue
+        if start <= addr and (best is None or start > best[0]):
+            best = (start, parts)
+    if best is None:
+        return None
+    counts = {}
+    for tok in best[1]:
+        if tok.startswith("N") and "=" in tok and tok[1:tok.index("=")].isdigit():
+            counts[tok[:tok.index("=")]] = int(tok[tok.index("=") + 1:])
+    total = sum(counts.values())
+    return {n: round(c / total, 4) for n, c in sorted(counts.items())} if total else None
+
+
+def gpu_numa_node(index):
+    """NUMA node of GPU `index` from sysfs (via its PCI bus id), or None."""
+    try:
+        out = subprocess.run(["nvidia-smi", "-i", str(index), "--query-gpu=pci.bus_id",
+                              "--format=csv,noheader"], capture_output=True, text=True, timeout=20)
+        bus = out.stdout.strip().lower()
+        dom, rest = bus.split(":", 1)
+        with open("/sys/bus/pci/devices/%s:%s/numa_node" % (dom[-4:], rest)) as f:
+            n = int(f.read().strip())
+        return n if n >= 0 else None
+    except (OSError, ValueError, subprocess.SubprocessError):
+        return None
+
+
 # The sources each timed kernel is compiled from (its translation unit and every header it
 # includes): a committed traffic figure stands only while their hash is the one it was taken at.
 KERNEL_SOURCES = {
@@ -441,6 +483,7 @@ def run_layerwise(args, link, device, torch, log):
             lw.end()
 
         huge_frac = huge_backed_fraction(lw.host_rows_ptr(0))
+        pool_numa = numa_spread(lw.host_rows_ptr(0))
         log("layerwise set-up %.1f s (host pool %.2f GB)" % (time.time() - t0, N * T * row * 2 / 1e9))
         one_pass(L0)  # warm-up pass
         torch.cuda.synchronize(device)
@@ -484,7 +527,7 @@ def run_layerwise(args, link, device, torch, log):
                      "t_roofline_ms": round(t_roof, 4), "frac": round(t_roof / t_pass, 4),
                      "peaks_gbs": {"h2d": round(link["h2d"], 1), "d2h": round(link["d2h"], 1)}},
         "device_buffer_bytes": 4 * T * row * 2, "host_pool_bytes": N * T * row * 2,
-        "host_pool_huge_backed": huge_frac,
+        "host_pool_huge_backed": huge_frac, "host_pool_numa": pool_numa,
     }
 
 
@@ -663,6 +706,9 @@ def run_kvo(args, log):
                    "host_pool_page": kv.get_option(K.KVO_OPT_HOST_HUGE_PAGE) or "base",
                    "host_pool_huge_backed": huge_backed_fraction(
                        kv.host_block(0) if args.host_block_tokens else kv.host_rows(0)),
+                   "host_pool_numa": numa_spread(
+                       kv.host_block(0) if args.host_block_tokens else kv.host_rows(0)),
+                   "gpu_numa_node": gpu_numa_node(device.index if device.index is not None else 0),
                    "host_block_tokens": args.host_block_tokens or None,
                    "gather": "bulk" if path == "fused" else args.gather, "groups": args.groups,
                    "parallelism": "replicas%d" % world,

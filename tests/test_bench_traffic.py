@@ -1,5 +1,5 @@
-"""bench.py's committed DRAM-traffic figures: reported only for the kernel sources they were
-measured on.  Host logic only (no GPU)."""
+"""bench.py host logic: committed DRAM-traffic figures are reported only for the kernel
+sources they were measured on; NUMA placement of host buffers.  No GPU."""
 import json
 import os
 import sys
@@ -47,3 +47,12 @@ def test_committed_entries_name_their_sources():
             continue
         assert e["sources"] == bench.kernel_sources(kernel)
         assert e["bytes_per_launch"] > 0 and len(e["source_hash"]) == 16
+
+
+def test_numa_spread_of_a_host_buffer():
+    import numpy as np
+    buf = np.ones(1 << 20, dtype=np.uint8)
+    spread = bench.numa_spread(buf.ctypes.data)
+    if spread is not None:  # /proc/self/numa_maps readable
+        assert all(k.startswith("N") for k in spread)
+        assert abs(sum(spread.values()) - 1.0) < 1e-3
