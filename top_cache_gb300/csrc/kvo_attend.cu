@@ -514,8 +514,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kAttThreads, 1) atte
       // that stops leaves the others and the partner to time out
       bool f = __any_sync(kFull, *abort_flag != 0u);
       if (!f) f = !__all_sync(kFull, mbar_wait(s_full, j & 1, a.wait_ns));
-      // the partner has read what this CTA sent for the last block: its block
-      // maximum, which came after, has arrived
       if (f) {
         ok = false;
         break;
@@ -525,7 +523,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kAttThreads, 1) atte
 #pragma unroll
       for (int c = 0; c < 2; ++c) vm[c] = __ballot_sync(kFull, sn[c] >= 0 && sn[c] < a.C);
       load_valid(j + 1);
-      // the partner's rows' partial scores to its memory, then own rows' to registers
+      // the partner's rows' partial scores to its memory, then own rows' to
+      // registers.  The partner's buffer is free: the partner sent its block
+      // maximum of the last block after reading what this CTA wrote for it,
+      // and that maximum has arrived (the last iteration waited for it).
 #pragma unroll
       for (int h2 = 0; h2 < 2; ++h2) {
         float ps[32];
