@@ -663,6 +663,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kAttThreads, 1) atte
   }
   tc_before();
   cluster_sync();  // no access to the partner's shared memory after this
+  if (*abort_flag) {
+    // A pair that stopped early may leave an asynchronous store of the
+    // partner's into this CTA's shared memory in flight (it was issued before
+    // the partner reached the barrier): give it time to land before exiting.
+    const uint64_t t0 = global_ns();
+    while (global_ns() - t0 < 20000u) {
+    }
+  }
   if (warp == kMmaWarp) {
     tc_after();
     asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(kTmemCols) : "memory");
