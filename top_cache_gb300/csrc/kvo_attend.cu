@@ -457,8 +457,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kAttThreads, 1) atte
       if (ok && !issue_pv(nb - 1)) ok = false;
       if (ok) mma_commit(o_final);
       if (!ok) fail();
-      mma_commit(fin);  // everything issued above is complete before TMEM is freed
-      if (!mbar_wait(fin, 0, a.wait_ns)) fail();
+      // Everything issued above is complete before TMEM is freed.  The tensor
+      // pipe waits on nothing outside this CTA, so this wait is not cut short
+      // by a small caller's limit: it is bounded by 2 s at least.
+      mma_commit(fin);
+      if (!mbar_wait(fin, 0, a.wait_ns > 2000000000ull ? a.wait_ns : 2000000000ull)) fail();
     }
     __syncwarp();
   } else if (warp >= kSoftWarp0 && warp < kSoftWarp0 + kSoftThreads / 32) {
