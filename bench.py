@@ -875,6 +875,10 @@ def run_reference(args, log):
     per_unit_s = 1.0 / probe["value"]
     budget_s = 90.0
     n_units = int(max(1, min(wl.n_units, budget_s / max(1, args.steps + args.warmup) / per_unit_s)))
+    # Units are independent, so a sample of a few units per core measures the same rate;
+    # the cap also bounds the untimed set-up (generating and loading each unit's prefill
+    # rows, 38 MB per unit on batch16x8_32k_mtp3), which otherwise dominates the run.
+    n_units = min(n_units, max(32, 2 * oracle.threads()))
     units = wl.units_rl()[:n_units]
     S = wl.steps
     tmax = wl.max_tokens(S)
