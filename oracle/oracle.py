@@ -25,24 +25,36 @@ _lock = threading.Lock()
 _lib = None
 
 
+def compile_source(src, out):
+    """Compile an oracle source with plain gcc: no fast-math, no FP contraction."""
+    cmd = ["gcc", "-O2", "-std=c11", "-fPIC", "-shared", "-fopenmp", "-ffp-contract=off",
+           "-fno-fast-math", src, "-o", out, "-lm"]
+    subprocess.run(cmd, check=True)
+
+
 def build(force=False):
-    """Compile the oracle with plain gcc: no fast-math, no FP contraction."""
+    """Compile kvo_oracle.c into libkvo_oracle.so unless it is up to date."""
     if not force and os.path.exists(_SO) and os.path.getmtime(_SO) >= os.path.getmtime(_SRC):
         return _SO
     tmp = _SO + ".tmp%d" % os.getpid()
-    cmd = ["gcc", "-O2", "-std=c11", "-fPIC", "-shared", "-fopenmp", "-ffp-contract=off",
-           "-fno-fast-math", _SRC, "-o", tmp, "-lm"]
-    subprocess.run(cmd, check=True)
+    compile_source(_SRC, tmp)
     os.replace(tmp, _SO)
     return _SO
 
 
 def lib():
+    """The oracle library, built on first use.
+
+    KVO_ORACLE_LIB, when set, names an already compiled copy to load instead: the
+    mutation test uses it to run the pins against copies with a planted mistake.
+    """
     global _lib
     with _lock:
         if _lib is None:
-            build()
-            L = ctypes.CDLL(_SO)
+            path = os.environ.get("KVO_ORACLE_LIB")
+            if not path:
+                path = build()
+            L = ctypes.CDLL(path)
             vp, i32, i64 = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64
             L.oracle_unit_new.restype = vp
             L.oracle_unit_new.argtypes = [i64, i32, i32, i32, i32, i32, i32]
