@@ -587,6 +587,7 @@ int kvo_create(const kvo_config* cfg, kvo_handle** out) {
   }
   cudaError_t e = alloc_host_pool(h, pool_rows * h->R * 2);
   if (e != cudaSuccess) {
+    cudaGetLastError();  // the failed allocation is not left as this thread's last CUDA error
     delete h;
     return fail(KVO_ENOMEM, std::string("pinned host pool: ") + cudaGetErrorString(e));
   }
@@ -659,6 +660,9 @@ int kvo_create(const kvo_config* cfg, kvo_handle** out) {
   if (e != cudaSuccess) {
     free_all(h);
     delete h;
+    // A failed cudaMalloc is also recorded as the thread's last CUDA error; left there,
+    // the caller's next kernel launch check (this library's or PyTorch's) would report it.
+    cudaGetLastError();
     return fail(KVO_ENOMEM, std::string("device allocation: ") + cudaGetErrorString(e));
   }
   // initial state: nothing resident, every slot free, stamps and lengths 0
@@ -1095,7 +1099,10 @@ int kvo_set_option(kvo_handle* h, int32_t key, int64_t value) {
       if (e != cudaSuccess) return cuda_fail(e, "piece_tokens");
       h->piece_tokens = (int)value;
       e = alloc_fused_segments(h);
-      if (e != cudaSuccess) return fail(KVO_ENOMEM, std::string("piece segments: ") + cudaGetErrorString(e));
+      if (e != cudaSuccess) {
+        cudaGetLastError();  // as in kvo_create: not left as the thread's last CUDA error
+        return fail(KVO_ENOMEM, std::string("piece segments: ") + cudaGetErrorString(e));
+      }
       return KVO_OK;
     }
     case KVO_OPT_HOST_HUGE_PAGE:

@@ -163,6 +163,7 @@ int kvo_lw_create(const kvo_lw_config* cfg, kvo_lw** out) {
   if (e == cudaSuccess) e = cudaEventCreateWithFlags(&lw->ev_end, cudaEventDisableTiming);
   if (e != cudaSuccess) {
     release(lw);
+    cudaGetLastError();  // a failed allocation is not left as the thread's last CUDA error
     return e == cudaErrorMemoryAllocation ? kvo::set_error(KVO_ENOMEM, "layerwise buffers")
                                           : kvo::set_cuda_error(e, "layerwise create");
   }
