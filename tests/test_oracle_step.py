@@ -231,3 +231,19 @@ def test_generated_workload_invariants():
             # scores are non-increasing along each list
             assert np.all(np.diff(r.score, axis=1) <= 0)
         assert total_miss < wl.steps * wl.topk  # the walk gives a nontrivial hit rate
+
+
+def test_thousand_random_tiny_shapes():
+    # brute force over many shapes at once: L <= 64, k <= 8, C <= 16, P in 1..4, small
+    # integer values (so ties are frequent), distinct or shared queries across positions
+    for seed in range(1000):
+        rng = np.random.default_rng(50_000 + seed)
+        P = int(rng.integers(1, 5))
+        k = int(rng.integers(1, 9))
+        C = int(rng.integers(k, 17))
+        n_new = int(rng.integers(0, 3))
+        n_steps = int(rng.integers(1, 5))
+        n_init = int(rng.integers(0, 64 - n_steps * n_new + 1))
+        _drive(seed, n_init=n_init, n_steps=n_steps, n_new=n_new, k=k, C=C, P=P,
+               distinct_queries=bool(rng.integers(0, 2)), lo=-1, hi=int(rng.integers(1, 3)),
+               dup_rows=bool(rng.integers(0, 2)))
