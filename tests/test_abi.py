@@ -89,3 +89,22 @@ def test_header_constants_match_binding():
             assert len(kvo.PROF_KINDS) == value
         else:
             assert getattr(kvo, name) == value, name
+
+
+def test_binding_refuses_strided_buffers():
+    # argument marshalling only, but it must not hand a strided view to the C ABI as dense
+    import numpy as np
+    import torch
+    from top_cache_gb300 import kvo
+    a = np.zeros((4, 8), np.int32)
+    assert kvo._ptr(a) == a.ctypes.data
+    assert kvo._ptr(a[1:3]) == a[1:3].ctypes.data  # leading-dimension slices stay dense
+    with pytest.raises(kvo.KvoError) as e:
+        kvo._ptr(a[:, :4])
+    assert e.value.code == kvo.KVO_EINVAL
+    t = torch.zeros((4, 8), dtype=torch.int32)
+    assert kvo._ptr(t[2:]) == t[2:].data_ptr()
+    for bad in (t[:, 1:], t.t()):
+        with pytest.raises(kvo.KvoError):
+            kvo._ptr(bad)
+    assert kvo._ptr(None) is None and kvo._ptr(1234) == 1234

@@ -163,7 +163,9 @@ def test_attend_bad_arguments():
         q = torch.zeros((1, 1, 128, 576), dtype=torch.int16, device="cuda")
         out = torch.zeros((1, 1, 128, 512), dtype=torch.int16, device="cuda")
         with pytest.raises(K.KvoError):
-            r.kv.attend(q[..., :64, :], SCALE, out)  # 64 heads: not a multiple of 128
+            r.kv.attend(q[..., :64, :].contiguous(), SCALE, out)  # 64 heads: not a multiple of 128
+        with pytest.raises(K.KvoError):
+            r.kv.attend(q[..., :64, :], SCALE, out)  # a strided view is refused by the binding
         with pytest.raises(K.KvoError):
             r.kv.attend(q, float("nan"), out)
         qm = torch.zeros(1 * 128 * 576 + 8, dtype=torch.int16, device="cuda")[1:1 + 128 * 576]

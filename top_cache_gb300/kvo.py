@@ -167,13 +167,21 @@ def _check(rc):
 
 
 def _ptr(t):
-    """Device/host address of a tensor or array, or None."""
+    """Device/host address of a tensor or array, or None.
+
+    The C ABI takes dense row-major buffers, so a strided view (a slice along an
+    inner dimension, a transpose) is refused here rather than read as if dense.
+    """
     if t is None:
         return None
     if isinstance(t, int):
         return t
     if isinstance(t, np.ndarray):
+        if not t.flags.c_contiguous:
+            raise KvoError(KVO_EINVAL, "array is not C-contiguous")
         return t.ctypes.data
+    if not t.is_contiguous():
+        raise KvoError(KVO_EINVAL, "tensor is not contiguous")
     return t.data_ptr()
 
 
