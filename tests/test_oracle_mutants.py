@@ -144,3 +144,74 @@ def test_every_planted_mistake_fails_a_pin(tmp_path):
     assert rc0 == 0, "the unchanged oracle fails its pins when compiled for this test:\n" + log0
     survivors = [name for name, rc, _ in results[1:] if rc != 1]
     assert not survivors, "mutants the pins do not catch (or that crash): %s" % survivors
+
+
+# ---------------------------------------------------------------- layerwise oracle
+LW_SRC = os.path.join(ROOT, "oracle", "layerwise.py")
+LW_MUTANTS = [
+    ("round robin by layer index instead of reusable ordinal",
+     "phys[l] = len(ind) + (k % shared)", "phys[l] = len(ind) + (l % shared)"),
+    ("physical buffers I + B instead of I + min(B, R)",
+     "return len(ind) + shared, phys", "return len(ind) + n_shared, phys"),
+    ("independent layers share buffer 0",
+     "        phys[l] = k\n", "        phys[l] = 0\n"),
+    ("digest of signed values",
+     ".astype(np.int64).sum()", ".view(np.int16).astype(np.int64).sum()"),
+    ("compute reads the chunk's own rows too",
+     "digests.append(digest(self.host[l, :self.length]))\n"
+     "            self.host[l, self.length:self.length + c] = chunk[l]",
+     "self.host[l, self.length:self.length + c] = chunk[l]\n"
+     "            digests.append(digest(self.host[l, :self.length + c]))"),
+    ("chunk saved one row late",
+     "self.host[l, self.length:self.length + c] = chunk[l]",
+     "self.host[l, self.length + 1:self.length + 1 + c] = chunk[l][:max(0, self.max_tokens - self.length - 1)]"),
+    ("a pass that exactly fills max_tokens refused",
+     "if self.length + c > self.max_tokens:", "if self.length + c >= self.max_tokens:"),
+    ("length not advanced",
+     "        self.length += c\n", "\n"),
+]
+
+
+def _lw_pin_failures(module):
+    """Run every test of tests/test_oracle_layerwise.py against `module`; count failures."""
+    import importlib
+    pins = importlib.import_module("tests.test_oracle_layerwise")
+    saved = pins.LW
+    pins.LW = module
+    failures = 0
+    try:
+        for name in dir(pins):
+            fn = getattr(pins, name)
+            if not name.startswith("test_") or not callable(fn):
+                continue
+            calls = [()]
+            for mark in getattr(fn, "pytestmark", []):
+                if mark.name == "parametrize":
+                    names = [n.strip() for n in mark.args[0].split(",")]
+                    calls = [tuple(v) if len(names) > 1 else (v,) for v in mark.args[1]]
+            for args in calls:
+                try:
+                    fn(*args)
+                except Exception:
+                    failures += 1
+    finally:
+        pins.LW = saved
+    return failures
+
+
+def _lw_module(text, name):
+    import types
+    m = types.ModuleType(name)
+    exec(compile(text, name, "exec"), m.__dict__)
+    return m
+
+
+def test_every_planted_layerwise_mistake_fails_a_pin():
+    base = open(LW_SRC).read()
+    assert _lw_pin_failures(_lw_module(base, "lw_unchanged")) == 0
+    survivors = []
+    for i, (name, old, new) in enumerate(LW_MUTANTS):
+        assert base.count(old) == 1, "mutation site not unique or missing: %s" % name
+        if _lw_pin_failures(_lw_module(base.replace(old, new), "lw_mutant%d" % i)) == 0:
+            survivors.append(name)
+    assert not survivors, "layerwise mutants the pins do not catch: %s" % survivors
