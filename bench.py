@@ -20,6 +20,7 @@ import argparse
 import hashlib
 import json
 import os
+import re
 import statistics
 import subprocess
 import sys
@@ -185,11 +186,19 @@ def kernel_sources(kernel):
     return ["top_cache_gb300/csrc/" + f for f in KERNEL_SOURCES[kernel]] + ["include/kvo.h"]
 
 
+def code_only(text):
+    """C/C++ source without its comments, trailing blanks and empty lines: what the compiler
+    sees, so that an edit to a comment leaves a traffic figure's hash unchanged."""
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    text = re.sub(r"//[^\n]*", "", text)
+    return "\n".join(line.rstrip() for line in text.splitlines() if line.strip())
+
+
 def kernel_source_hash(kernel):
     h = hashlib.sha256()
     for rel in kernel_sources(kernel):
-        with open(os.path.join(ROOT, rel), "rb") as f:
-            h.update(f.read())
+        with open(os.path.join(ROOT, rel), encoding="utf-8") as f:
+            h.update(code_only(f.read()).encode())
     return h.hexdigest()[:16]
 
 
