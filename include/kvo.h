@@ -332,8 +332,8 @@ int kvo_select_noalloc(const void* keys, int64_t unit_stride, const int32_t* cac
                        void* stream);
 
 /*
- * kvo_attend ([LS] Decode step 7: sparse attention consumes the resident
- * K/V; the pages name an SFA/MLA model without its formula, so this is the
+ * kvo_attend ([LS] Decode step 7: the sparse-attention operator reads the
+ * K/V rows now resident on the device; the pages name an SFA/MLA model without its formula, so this is the
  * absorbed latent attention of the DeepSeek family, reading R13 of the
  * oracle): for each listed unit u, position p and head h, over the hot rows
  * named by that position's top-k slots (slot < 0 or >= hot_capacity: pad,

@@ -58,8 +58,8 @@
  *               rotation, H H = 128 I, so the score estimates q . k); a zero
  *               score is +0.  Keys are quantized when they are appended,
  *               queries at each step; the bf16 keys are kept only for tests.
- *  R13 sparse attention ([LS] Decode step 7, "sparse attention consumes the
- *               resident K/V"; the pages name an SFA/MLA model but give no
+ *  R13 sparse attention ([LS] Decode step 7: attention runs on the rows
+ *               made resident by the step; the pages name an SFA/MLA model but give no
  *               formula, so the absorbed multi-head latent attention of the
  *               DeepSeek family is taken): per unit, position p and head h,
  *               over the tokens t of that position's top-k list (pads

@@ -24,7 +24,7 @@ Readings (choices of this project where the pages leave a step open):
                  is reused only after the save of its previous layer has finished
                  (the reuse invariant), and the load of a layer may start up to
                  `lookahead` layers ahead of its compute.
- R16 stand-in  : the tests' stand-in for "run attention and update KV" reads the
+ R16 stand-in  : the tests' stand-in for the layer's attention and KV update reads the
                  whole cached prefix of the layer and reports its digest, the exact
                  sum of its bf16 bit patterns taken as unsigned 16-bit integers, so
                  that a load that brought the wrong rows, or a buffer overwritten

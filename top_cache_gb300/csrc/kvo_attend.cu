@@ -1,6 +1,6 @@
 // Sparse attention over the hot buffer on the 5th-generation tensor cores:
 // decode step 7 of "Layerwise and Sparse KV Cache Offloading Design"
-// (section 4, "Decode step": sparse attention consumes the resident K/V).
+// (section 4, "Decode step": the attention operator reads the resident rows).
 //
 // Reading R13 of the oracle (the pages name an SFA/MLA sparse-attention model
 // but give no formula): absorbed latent attention.  A hot row is 576 bf16 =

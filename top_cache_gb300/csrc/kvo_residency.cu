@@ -1,13 +1,13 @@
 // Residency update, miss-row fill and new-token append.
 //
 // "Layerwise and Sparse KV Cache Offloading Design", section 4 "Sparse Decode
-// Offload", Decode step: (2) new K/V rows copied to their logical slots in the
-// host pool, (4) the per-layer LRU residency table identifies hits, assigns
-// hot slots to misses and selects eviction slots, (5) only miss rows are
-// copied host -> device, (6) logical top-k positions remapped to physical
+// Offload", Decode step: (2) each new token's K/V row lands at its own logical
+// index of the host pool, (4) a per-layer LRU table tells hits from misses,
+// gives each miss a hot slot and picks the slots to evict, (5) only missed
+// rows cross host -> device, (6) the top-k's logical positions become hot
 // slots.  "FlashOffloading ... What does it mean?", decode paragraphs: the
-// shelf size stays fixed, the MTP3 per-position miss lists are merged and
-// deduplicated before loading, cache_slots maps a token to its slot or -1.
+// shelf has a fixed size, the four MTP3 positions' miss lists become one
+// list without repeats before any load, cache_slots gives a token's slot or -1.
 //
 //  residency_kernel : one CTA per unit; merge + dedup of the P lists, LRU
 //                     victims in (last_use, slot) order, reverse-index
