@@ -700,7 +700,7 @@ def run_kvo(args, log):
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        cpu = run_cpu_baseline(wl, args.cpu_units, args.cpu_steps, log)
+        cpu = run_cpu_baseline(wl, args.cpu_units, min(args.cpu_steps, wl.steps), log)
 
     launches = sum(v[1] for v in prof.values())
     line = {
@@ -835,8 +835,10 @@ def run_e2e(args, kv, inp, wl, U, device, world, torch):
 
 
 # --------------------------------------------------------------------------- CPU oracle
-def run_cpu_baseline(wl, n_units, n_steps, log, units_offset=0):
-    """The CPU oracle, as it stands, on a bounded sample of the same workload."""
+def run_cpu_baseline(wl, n_units, n_steps, log, units_offset=0, max_seconds=30.0):
+    """The CPU oracle, as it stands, on a bounded sample of the same workload: n_units units
+    over up to n_steps steps of the sequence, stopping early once the warm steps have taken
+    max_seconds."""
     import numpy as np
     import oracle
     import workload as W
@@ -853,6 +855,7 @@ def run_cpu_baseline(wl, n_units, n_steps, log, units_offset=0):
         ors.append(o)
     timed = 0.0
     L = wl.context
+    done = 0
     for s in range(n_steps):
         t0 = time.perf_counter()
         for i, o in enumerate(ors):
@@ -860,13 +863,16 @@ def run_cpu_baseline(wl, n_units, n_steps, log, units_offset=0):
         oracle.step_many(ors, q[s])
         dt = time.perf_counter() - t0
         L += wl.n_new
+        done = s + 1
         if s > 0:
             timed += dt
-    n = len(units) * (n_steps - 1)
+            if timed >= max_seconds:
+                break
+    n = len(units) * (done - 1)
     log("cpu oracle: %d unit-steps in %.2f s" % (n, timed))
     return {"value": round(n / timed, 2), "unit": UNIT, "cores": oracle.threads(), "kind": "oracle",
             "sample": "%d of %d units (%s), %d warm steps after one cold step, context %d"
-                      % (len(units), wl.n_units, wl.name, n_steps - 1, wl.context)}
+                      % (len(units), wl.n_units, wl.name, done - 1, wl.context)}
 
 
 def run_reference(args, log):
@@ -980,7 +986,7 @@ def main(argv=None):
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-units", type=int, default=32)
-    ap.add_argument("--cpu-steps", type=int, default=4)
+    ap.add_argument("--cpu-steps", type=int, default=50)  # at most the sequence's own steps
     ap.add_argument("--quiet", action="store_true")
     args = ap.parse_args(argv)
     if args.warmup < 3:
