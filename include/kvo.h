@@ -162,19 +162,23 @@ typedef struct kvo_stats {
  */
 int kvo_create(const kvo_config* cfg, kvo_handle** out);
 
-/* kvo_destroy: synchronise the device and free everything.  NULL is a no-op. */
+/* kvo_destroy: synchronise the device and free everything kvo_create made
+ * (the pages define no teardown; this is the library's own).  NULL is a no-op. */
 int kvo_destroy(kvo_handle* h);
 
 /*
- * kvo_host_rows: host address of row 0 of unit's pool; rows are contiguous,
- * row_elems bf16 each, max_tokens rows.  The caller may write rows [0, n)
+ * kvo_host_rows ([LS] "Memory layout": the full main-KV history of every
+ * unit lives in the pinned host pool): host address of row 0 of unit's pool;
+ * rows are contiguous, row_elems bf16 each, max_tokens rows.  The caller may write rows [0, n)
  * before kvo_prefill(unit, n) (bulk load of a prefilled context; untimed
  * set-up, outside the decode step).  NULL if unit is out of range.
  */
 void* kvo_host_rows(kvo_handle* h, int32_t unit);
 
 /*
- * Paged host pool (config host_block_tokens > 0).  A unit's token t lives in
+ * Paged host pool (config host_block_tokens > 0; "SFA Remote D2H Connector
+ * Design", "Data Ownership": the main KV is addressed by block IDs).  A unit's
+ * token t lives in
  * row t mod B of physical block blocks[t / B] of its block table (B =
  * host_block_tokens); the indexer cache and the hot buffers stay per unit on
  * the device.  kvo_host_rows returns NULL for a paged pool.
@@ -195,7 +199,10 @@ int kvo_set_blocks(kvo_handle* h, int32_t unit, int32_t first_block, int32_t n_b
 void* kvo_host_block(kvo_handle* h, int64_t block);
 
 /*
- * kvo_prefill: set an empty unit's context to n_tokens tokens whose rows are
+ * kvo_prefill ([LS] section 5, "Request flow", steps 1 and 5: the decode
+ * side takes a prefilled request into its main host destination and its
+ * indexer destination): set an empty unit's context to n_tokens tokens whose
+ * rows are
  * already in the host pool; copies idx_keys (bf16 [n_tokens][128], host or
  * device memory) into the indexer cache on the given stream.  Errors:
  * KVO_EINVAL (unit not empty), KVO_ERANGE (unit or n_tokens out of range).
@@ -260,7 +267,8 @@ int kvo_select(const void* keys, int64_t unit_stride, const int32_t* cache_slots
                void* workspace, size_t workspace_bytes, void* stream);
 
 /*
- * kvo_reset: return every listed unit to its first keep_tokens cached tokens
+ * kvo_reset (the pages define no reset; the library's own, for reusing a
+ * unit): return every listed unit to its first keep_tokens cached tokens
  * with an empty hot shelf (cache_slots and slot_token -1, last_use and stamp
  * 0), as when a finished request's unit is reused for a new request whose
  * prefilled context is already in place.  keep_tokens must not exceed any
@@ -271,7 +279,8 @@ int kvo_reset(kvo_handle* h, const int32_t* units, int32_t n_units, int64_t keep
               void* stream);
 
 /*
- * Per-kernel device time, recorded when KVO_OPT_PROFILE is 1: CUDA events on
+ * Per-kernel device time (measurement support; no passage of the pages),
+ * recorded when KVO_OPT_PROFILE is 1: CUDA events on
  * the launching stream bracket every kernel the library launches.
  * kvo_profile_read synchronises those events, adds their durations into
  * ms[kind] and the launch counts into launches[kind] for kind <
@@ -291,18 +300,21 @@ int kvo_reset(kvo_handle* h, const int32_t* units, int32_t n_units, int64_t keep
 #define KVO_PROF_KINDS 11
 int kvo_profile_read(kvo_handle* h, double* ms, uint64_t* launches, int32_t n_kinds);
 
-/* kvo_set_option: KVO_OPT_* above.  KVO_EINVAL on unknown key or value. */
+/* kvo_set_option: KVO_OPT_* above (library tuning; no passage of the pages).
+ * KVO_EINVAL on unknown key or value. */
 int kvo_set_option(kvo_handle* h, int32_t key, int64_t value);
 
 /* kvo_get_option: the current value of KVO_OPT_* key into *value (host
  * memory).  KVO_EINVAL on unknown key or NULL arguments. */
 int kvo_get_option(kvo_handle* h, int32_t key, int64_t* value);
 
-/* kvo_get_stats: synchronises the device, then copies the counters. */
+/* kvo_get_stats (library counters; no passage of the pages): synchronises the
+ * device, then copies the counters. */
 int kvo_get_stats(kvo_handle* h, kvo_stats* out);
 
 /*
- * kvo_export_state: synchronises the device and copies one unit's state to
+ * kvo_export_state (test accessor of the state [LS] "Memory layout" and
+ * Decode step 4 describe): synchronises the device and copies one unit's state to
  * host buffers (any may be NULL): cache_slots [max_tokens] int32,
  * slot_token [hot_capacity] int32, last_use [hot_capacity] uint32, length
  * and stamp scalars, hot_rows [hot_capacity][row_elems] bf16.
@@ -433,7 +445,8 @@ int kvo_lw_end(kvo_lw* lw, void* stream);
 int kvo_lw_stats(kvo_lw* lw, uint64_t* bytes_h2d, uint64_t* bytes_d2h);
 
 /*
- * kvo_wait_selftest: runs, on `device`, one thread through the two bounded
+ * kvo_wait_selftest (failure detection of the library's own bounded waits;
+ * no passage of the pages): runs, on `device`, one thread through the two bounded
  * waits every kernel of the library relies on (a spin on a global flag and an
  * mbarrier phase wait), each on a condition nothing satisfies and limited to
  * limit_ns (1 us .. 10 s).  Both must give up; the call returns KVO_ETIMEOUT
@@ -442,7 +455,8 @@ int kvo_lw_stats(kvo_lw* lw, uint64_t* bytes_h2d, uint64_t* bytes_d2h);
  */
 int kvo_wait_selftest(int32_t device, int64_t limit_ns, int64_t* waited_ns);
 
-/* kvo_last_error: message of the last failing call on this thread ("" if none). */
+/* kvo_last_error (library error reporting; no passage of the pages): message
+ * of the last failing call on this thread ("" if none). */
 const char* kvo_last_error(void);
 
 #ifdef __cplusplus
