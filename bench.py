@@ -6,13 +6,15 @@ tokens (rows to the pinned host pool, keys to the indexer cache), then
 kvo_step (score every cached token, fused top-k with packed payload, MTP
 merge/dedup, LRU residency update, miss-row fill from host, remap).
 
-Workload (default): 16 requests x 8 layers, 32,768-token context, MTP3 (4
-positions, 4 new tokens per step), top-2048 of a 4,096-slot hot shelf, random
-walk queries with drift 0.9, a 50-step decode sequence.  The timed loop
-replays that sequence: after step 49 every unit is returned to its 32,768
-prefilled tokens with an empty shelf (kvo_reset, inside the timed region) and
-the sequence starts again, so cold and warm steps appear in the sequence's
-own mix.  The 1.07 GB of indexer keys read per step exceed the 129 MB L2.
+Workload (default): the largest single-GPU configuration, 32 requests x 16
+layers, 65,536-token context, top-2048 of a 16,384-slot hot shelf (a quarter
+of the context), one query position, random-walk queries with drift 0.95, a
+50-step decode sequence, 38.7 GB of main KV in the pinned host pool.  The
+warm-up steps run the start of the sequence; the timed steps continue it (past
+step 49 every unit is returned to its prefilled tokens with an empty shelf,
+kvo_reset, and the sequence starts again).  The cold step (an empty shelf, every
+selected row a miss) is timed on its own after the timed steps.  The 8.59 GB of
+indexer keys read per step exceed the 129 MB L2.
 
 Prints one JSON line (rank 0).  --impl reference times the CPU oracle instead.
 """
@@ -33,7 +35,7 @@ if ROOT not in sys.path:
 
 METRIC = "decode steps/s (layer·request selections/s) + miss-fill GB/s vs roofline"
 UNIT = "selections/s"
-DEFAULT_WORKLOAD = "batch16x8_32k_mtp3"
+DEFAULT_WORKLOAD = "batch32x16_64k"
 PEAKS_FILE = os.path.join(ROOT, "MEASURED_PEAKS.json")
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "traffic.json")
 FALLBACK_HBM_GBS = 6800.0
@@ -445,6 +447,61 @@ def run_attention(args, kv, wl, units, device, torch):
     }
 
 
+def run_copy_sfa(args, kv, inp, wl, units, device, torch):
+    """Decode step + sparse attention over the whole sequence, two ways: the step fills the
+    miss rows and the attention kernel runs after it ("serial"), or the step leaves them and
+    the attention kernel reads them from the pinned pool itself and writes them to their
+    slots ("deferred", KVO_OPT_DEFER_FILL; the pages' Copy-SFA operator).  Each way replays
+    the sequence from the prefill; the medians of the warm steps are compared.  The
+    fraction of the fill hidden is (serial - deferred) / (step with fill - step without)."""
+    import numpy as np
+    import workload as W
+    from top_cache_gb300 import kvo as K
+    H = args.attend_heads
+    P = wl.n_pos
+    U = len(units)
+    q = W.attention_queries(wl.seed, units, 0, P, H)
+    qd = torch.from_numpy(q.view(np.int16)).to(device)
+    del q
+    out = torch.empty((U, P, H, 512), dtype=torch.bfloat16, device=device)
+    lse = torch.empty((U, P, H), dtype=torch.float32, device=device)
+    scale = 1.0 / (192.0 ** 0.5)
+    stream = torch.cuda.current_stream(device)
+    res = {}
+    for name, defer in (("serial", 0), ("deferred", 1)):
+        kv.set_option(K.KVO_OPT_DEFER_FILL, defer)
+        kv.reset(wl.context)
+        seq = Sequence(kv, inp, wl)
+        n = wl.steps
+        ev = [torch.cuda.Event(enable_timing=True) for _ in range(3 * n)]
+        st0 = kv.stats()
+        for i in range(n):
+            ev[3 * i].record(stream)
+            seq.step()
+            ev[3 * i + 1].record(stream)
+            kv.attend(qd, scale, out, lse)
+            ev[3 * i + 2].record(stream)
+        torch.cuda.synchronize(device)
+        st1 = kv.stats()
+        step = [ev[3 * i].elapsed_time(ev[3 * i + 1]) for i in range(1, n)]
+        att = [ev[3 * i + 1].elapsed_time(ev[3 * i + 2]) for i in range(1, n)]
+        tot = [ev[3 * i].elapsed_time(ev[3 * i + 2]) for i in range(1, n)]
+        res[name] = {"step_ms": round(statistics.median(step), 4), "attend_ms": round(statistics.median(att), 4),
+                     "total_ms": round(statistics.median(tot), 4),
+                     "cold_total_ms": round(ev[0].elapsed_time(ev[2]), 4),
+                     "rows_h2d_per_step": (st1["rows_h2d"] - st0["rows_h2d"]) / n,
+                     "dup_host_bytes_per_step": (st1["fetch_dup_bytes"] - st0["fetch_dup_bytes"]) / n,
+                     "timeouts": st1["timeouts"]}
+    kv.set_option(K.KVO_OPT_DEFER_FILL, 0)
+    kv.reset(wl.context)
+    fill = res["serial"]["step_ms"] - res["deferred"]["step_ms"]
+    saved = res["serial"]["total_ms"] - res["deferred"]["total_ms"]
+    res["fill_ms"] = round(fill, 4)
+    res["hidden_fraction"] = round(saved / fill, 4) if fill > 0 else None
+    res["selections_per_s"] = {k_: round(U / (res[k_]["total_ms"] * 1e-3), 1) for k_ in ("serial", "deferred")}
+    return res
+
+
 # --------------------------------------------------------------------------- layerwise prefill
 def run_layerwise(args, link, device, torch, log):
     """Time prefill passes of the layerwise offload (kvo_lw_*) on their own.
@@ -570,6 +627,12 @@ def run_kvo(args, log):
     seq = Sequence(kv, inp, wl)
     stream = torch.cuda.current_stream(device)
 
+    # the clock sampler starts before the warm-up, so that its start-up (nvidia-smi
+    # initialising NVML) overlaps the warm-up steps rather than the timed ones
+    sampler = ClockSampler(local)
+    t_s = time.time()
+    while not sampler.samples and time.time() - t_s < 5.0:
+        time.sleep(0.05)
     # warm-up (the first step of the sequence is the cold, all-miss step)
     for _ in range(args.warmup):
         seq.step()
@@ -577,8 +640,6 @@ def run_kvo(args, log):
     kv.profile_read()
     kv.set_option(K.KVO_OPT_PROFILE, 1)
     st0 = kv.stats()
-    sampler = ClockSampler(local)
-    time.sleep(0.3)
 
     # ---------------- timed region
     ev = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps + 1)]
@@ -605,6 +666,20 @@ def run_kvo(args, log):
         torch.cuda.synchronize(device)
     sampler.stop()
     clocks = sampler.summary(t_wall0, t_wall1)
+
+    # the cold step on its own: every unit back at its prefilled context with an empty
+    # shelf, then step 0 of the sequence (every selected row a miss), three times
+    cold_ms = []
+    for _ in range(3):
+        kv.reset(wl.context)
+        seq = Sequence(kv, inp, wl)
+        c0, c1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize(device)
+        c0.record(stream)
+        seq.step()
+        c1.record(stream)
+        torch.cuda.synchronize(device)
+        cold_ms.append(c0.elapsed_time(c1))
 
     fused_frac = (st1["fused_steps"] - st0["fused_steps"]) / args.steps
     path = "fused" if fused_frac == 1 else "staged" if fused_frac == 0 else "mixed (%.0f%% fused)" % (100 * fused_frac)
@@ -687,6 +762,7 @@ def run_kvo(args, log):
     attention = None
     if args.attend_heads > 0 and wl.row_elems == 576:
         attention = run_attention(args, kv, wl, units, device, torch)
+        attention["copy_sfa"] = run_copy_sfa(args, kv, inp, wl, units, device, torch)
 
     # ---------------- layerwise prefill offload, timed on its own
     layerwise = None
@@ -736,6 +812,7 @@ def run_kvo(args, log):
                      "p90": round(sorted(step_ms)[int(0.9 * (len(step_ms) - 1))], 4),
                      "warm_median": round(statistics.median(warm), 4) if warm else None,
                      "cold_median": round(statistics.median(cold), 4) if cold else None,
+                     "cold_step_alone_ms": round(statistics.median(cold_ms), 4),
                      "p99": round(sorted(step_ms)[int(0.99 * (len(step_ms) - 1))], 4),
                      "max": round(max(step_ms), 4),
                      # the slowest steps as (position in the sequence, ms): tells a slow
@@ -949,7 +1026,7 @@ def run_reference(args, log):
 def main(argv=None):
     ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=2495)
+    ap.add_argument("--steps", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=("kvo", "reference"), default="kvo")
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD)

@@ -117,6 +117,8 @@ typedef struct kvo_stats {
   uint64_t rescored;        /* units rescored because a speculative threshold was too high */
   uint64_t fused_steps;     /* kvo_step calls that ran as one fused launch (KVO_OPT_FUSED) */
   uint64_t block_errors;    /* paged pool: rows of unmapped blocks skipped by append or gather */
+  uint64_t fetch_dup_bytes; /* deferred fill: host-pool bytes the attention kernel read for a row
+                               part another CTA of the same call was still writing (read twice) */
 } kvo_stats;
 
 /* Options for kvo_set_option. */
@@ -146,9 +148,19 @@ typedef struct kvo_stats {
                                    the others score and join the fill when no piece is left */
 #define KVO_OPT_PIECE_TOKENS 9  /* fused step: tokens per scoring piece, a multiple of 128 in
                                    [128, 2^20] (default 4096); resizes scratch, synchronous */
-#define KVO_OPT_HOST_HUGE_PAGE 10 /* read only (kvo_get_option): page size of the pinned host pool
-                                     when it is backed by transparent huge pages (pools of at
-                                     least four huge pages), 0 when it comes from cudaHostAlloc */
+#define KVO_OPT_HOST_HUGE_PAGE 10 /* read only (kvo_get_option): page size of transparent huge
+                                     pages backing the pinned host pool; always 0 (the pool is
+                                     driver-allocated pinned memory, cudaHostAlloc) */
+#define KVO_OPT_DEFER_FILL 11   /* 1: kvo_step assigns the miss rows' hot slots but leaves the rows
+                                   to the next kvo_attend on the same unit list, which reads them
+                                   from the pinned pool inside the attention kernel and writes them
+                                   to their slots (the Copy-SFA operator of "Layerwise and Sparse KV
+                                   Cache Offloading Design", Chinese edition: misses fetched inside
+                                   sparse attention).  Any other call that needs the hot rows first
+                                   (kvo_step, kvo_reset, kvo_export_state, kvo_attend on another unit
+                                   list) completes the fill with a copy kernel on its stream.
+                                   Requires row_elems == 576; the first 1 allocates 12 bytes per
+                                   hot slot of claim words (synchronous).  Default 0 */
 #define KVO_GATHER_LDG 0  /* miss rows read by 16-byte loads from the mapped host pool */
 #define KVO_GATHER_BULK 1 /* miss rows moved by bulk async copies through shared memory */
 
@@ -258,13 +270,20 @@ int kvo_step(kvo_handle* h, const int32_t* units, int32_t n_units, const void* q
  *   workspace   : device scratch of at least kvo_select_workspace_size()
  *                 bytes, 256-byte aligned, owned by the caller; its contents
  *                 need no initialisation and are not preserved
+ *   status      : device uint32, nullable, 4-byte aligned: set to 0 at the
+ *                 start of the call on the stream; the kernels OR in
+ *                 KVO_SELECT_ERR_TIMEOUT (a bounded wait expired) or
+ *                 KVO_SELECT_ERR_PLAN (an internal consistency check failed);
+ *                 nonzero means the outputs are not valid
  * Errors: KVO_EINVAL, KVO_ECUDA.  Asynchronous on stream.
  */
+#define KVO_SELECT_ERR_TIMEOUT 1u
+#define KVO_SELECT_ERR_PLAN 2u
 size_t kvo_select_workspace_size(int32_t n_units, int32_t n_pos, int32_t k, int32_t device);
 int kvo_select(const void* keys, int64_t unit_stride, const int32_t* cache_slots,
                const int64_t* lengths, int32_t n_units, int32_t n_pos, int32_t k,
                const void* queries, int32_t* tokens, float* scores, int32_t* payload,
-               void* workspace, size_t workspace_bytes, void* stream);
+               void* workspace, size_t workspace_bytes, uint32_t* status, void* stream);
 
 /*
  * kvo_reset (the pages define no reset; the library's own, for reusing a
@@ -336,12 +355,15 @@ int kvo_export_state(kvo_handle* h, int32_t unit, int32_t* cache_slots, int32_t*
  * 16 MiB, else KVO_ERANGE with a message.  All calls share the array: the
  * call clears what must start at zero, but calls that overlap on the GPU race
  * (order them on one stream).  The first call on a device looks up the
- * array's address for that device; make it before any stream capture.
+ * array's address for that device; make it before any stream capture.  That
+ * address is kept until exit, so calls after a cudaDeviceReset of that device
+ * are not supported.  status (device uint32, nullable) reports the kernels'
+ * completion as for kvo_select; without it an expired wait goes unreported.
  */
 int kvo_select_noalloc(const void* keys, int64_t unit_stride, const int32_t* cache_slots,
                        const int64_t* lengths, int32_t n_units, int32_t n_pos, int32_t k,
                        const void* queries, int32_t* tokens, float* scores, int32_t* payload,
-                       void* stream);
+                       uint32_t* status, void* stream);
 
 /*
  * kvo_attend ([LS] Decode step 7: the sparse-attention operator reads the
@@ -355,7 +377,16 @@ int kvo_select_noalloc(const void* keys, int64_t unit_stride, const int32_t* cac
  *   out[u][p][h][d] = sum_i softmax(s)_i * row_i[d]  (d < 512),
  *   lse[u][p][h] = log sum_i exp(s_i)  (-inf when the list has no row).
  * Run it after kvo_step on the same stream with that step's topk_slots: the
- * hot rows it reads are the ones the step made resident.
+ * hot rows it reads are the ones the step made resident.  When that step ran
+ * with KVO_OPT_DEFER_FILL = 1 and this call lists the same units in the same
+ * order, the step's miss rows are not in the hot buffer yet: this kernel reads
+ * each from the pinned pool (the token its packed payload names), uses it, and
+ * writes it to its slot, one CTA per row part (claim words in device memory;
+ * a CTA that finds a part claimed but not yet written reads the pool again),
+ * so that on return the hot buffer is as a filling kvo_step would have left it
+ * (the pages' Copy-SFA operator, Chinese edition of "Layerwise and Sparse KV
+ * Cache Offloading Design": misses copied inside sparse attention).  Those
+ * rows count in kvo_stats.rows_h2d / bytes_h2d, re-reads in fetch_dup_bytes.
  *   units      : host array [n_units] (as kvo_step), or NULL = all units.
  *   queries    : device bf16 [n_units][P][n_heads][576], 16-byte aligned.
  *   n_heads    : a multiple of 128 (one CTA pair per 128 heads).

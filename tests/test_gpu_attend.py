@@ -182,3 +182,106 @@ def test_full_batch16x8_mtp3_attend_sampled():
     # the oracle replays three units
     wl = W.WORKLOADS["batch16x8_32k_mtp3"]
     assert _run(wl, steps=2, check_units=[0, 77, 127]) == 3 * 4 * 2
+
+
+# ---------------------------------------------------------------------------
+# Deferred fill (KVO_OPT_DEFER_FILL): the step assigns the miss rows' slots and the
+# attention kernel reads those rows from the pinned pool itself, uses them and writes
+# them to their hot slots (the pages' Copy-SFA operator: misses fetched inside sparse
+# attention).  After the attention call the state must be exactly the oracle's, hot
+# rows included, and every miss row must have crossed the host link once.
+# ---------------------------------------------------------------------------
+def _run_fetch(wl, H=128, scale=SCALE, steps=None, check_units=None, distinct=False, paged=0, fused=None):
+    opts = {K.KVO_OPT_DEFER_FILL: 1}
+    if fused is not None:
+        opts[K.KVO_OPT_FUSED] = fused
+    r = Runner(wl, steps=steps, check_units=check_units, distinct=distinct, paged=paged, options=opts)
+    try:
+        n = 0
+        for s in range(r.steps):
+            r.append(wl.n_new)
+            st0 = r.kv.stats()
+            res = r.step(s)
+            r.compare(res, state=False)  # outputs only: exporting the state would complete the fill
+            q, out, lse = _attend_gpu(r, s, H, scale)
+            n += _compare(r, res, q, out, lse, scale)
+            st1 = r.kv.stats()
+            misses = st1["misses"] - st0["misses"]
+            # each part of each miss row is claimed and written by exactly one CTA
+            assert st1["bytes_h2d"] - st0["bytes_h2d"] == misses * wl.row_elems * 2
+            assert st1["rows_h2d"] - st0["rows_h2d"] == misses
+            for u in res:
+                r.compare_state(u)  # slot maps, stamps and every occupied hot row
+        return n
+    finally:
+        r.close()
+
+
+def test_fetch_reduced_mtp3():
+    # four positions of one query walk share most rows: the first position's pairs
+    # fetch them, the others find them written (or read the host pool again)
+    wl = W.Workload("attf", 2, 2, 3000, 4, 4, 256, 1100, 3, 0.9, 96)
+    assert _run_fetch(wl) == 2 * 2 * 4 * 3
+
+
+def test_fetch_distinct_queries_staged_and_fused():
+    # positions with their own queries list different rows; both step paths
+    wl = W.Workload("attfd", 2, 3, 2500, 4, 4, 128, 700, 3, 0.6, 97)
+    assert _run_fetch(wl, distinct=True, fused=0) == 2 * 3 * 4 * 3
+    assert _run_fetch(wl, distinct=True, fused=1) == 2 * 3 * 4 * 3
+
+
+def test_fetch_all_misses_and_ragged():
+    # drift 0: nearly every selected row is a miss; k = 200 leaves a partial last block
+    wl = W.Workload("attf0", 3, 2, 2000, 4, 4, 200, 900, 3, 0.0, 98)
+    assert _run_fetch(wl) > 0
+
+
+def test_fetch_paged_pool():
+    # rows reached through scattered 128-row blocks of a paged pool
+    wl = W.Workload("attfp", 2, 2, 1800, 2, 2, 256, 600, 3, 0.8, 99)
+    assert _run_fetch(wl, paged=128) > 0
+
+
+def test_fetch_flushed_when_no_attention_follows():
+    # a deferred step followed by another step, by an export or by attention on another
+    # unit list completes the fill with a copy kernel; the state stays the oracle's
+    wl = W.Workload("attff", 2, 2, 2000, 2, 2, 128, 512, 4, 0.7, 100)
+    r = Runner(wl, options={K.KVO_OPT_DEFER_FILL: 1})
+    try:
+        r.append(wl.n_new)
+        r.compare(r.step(0), state=True)  # export: flushed
+        r.append(wl.n_new)
+        res = r.step(1)
+        r.compare(res, state=False)
+        r.append(wl.n_new)
+        res = r.step(2)  # flushes step 1's rows first
+        r.compare(res, state=False)
+        ids = [1, 3]  # another unit list: flushed, then plain attention
+        slots = torch.stack([r.kv.slots[1], r.kv.slots[3]]).contiguous()
+        q = W.attention_queries(wl.seed, [r.units_rl[u] for u in ids], 2, wl.n_pos, 128)
+        out = torch.zeros((2, wl.n_pos, 128, 512), dtype=torch.int16, device="cuda")
+        lse = torch.zeros((2, wl.n_pos, 128), dtype=torch.float32, device="cuda")
+        r.kv.attend(torch.from_numpy(q.view(np.int16)).cuda(), SCALE, out, lse, slots=slots, units=ids)
+        torch.cuda.synchronize()
+        sub = {u: res[u] for u in ids}
+        assert _compare(r, sub, q, out.cpu().numpy().view(np.uint16), lse.cpu().numpy(), SCALE, ids=ids) == 2 * wl.n_pos
+        for u in range(r.U):
+            r.compare_state(u)
+        r.append(wl.n_new)
+        r.compare(r.step(3), state=True)
+        assert r.kv.stats()["timeouts"] == 0
+    finally:
+        r.close()
+
+
+def test_full_batch16x8_mtp3_fetch_sampled():
+    # the benchmark workload at full size with the fill inside the attention kernel
+    wl = W.WORKLOADS["batch16x8_32k_mtp3"]
+    assert _run_fetch(wl, steps=2, check_units=[0, 77, 127]) == 3 * 4 * 2
+
+
+def test_fetch_sweep_drift0_reduced():
+    # the hit-rate sweep's all-miss point (drift 0), reduced: 32 units
+    wl = W.reduced(W.WORKLOADS["sweep64x4_16k_mtp3"], n_requests=8, drift=0.0, steps=3)
+    assert _run_fetch(wl, check_units=[0, 13, 31]) == 3 * 4 * 3

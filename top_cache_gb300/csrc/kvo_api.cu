@@ -12,7 +12,9 @@
 #include <stdint.h>
 #include <stdio.h>
 #include <string.h>
+#include <stdlib.h>
 #include <sys/mman.h>
+#include <unistd.h>
 
 #include <string>
 #include <vector>
@@ -33,7 +35,7 @@ struct kvo_handle {
   int64_t n_blocks = 0;
   int32_t max_blocks = 0;             // block-table entries per unit
   int32_t* blocks = nullptr;          // [U][max_blocks] block tables (device), -1 = unmapped
-  size_t pool_map_bytes = 0;          // > 0: mmap'ed with transparent huge pages, registered
+  size_t pool_map_bytes = 0;          // always 0: cudaHostAlloc memory
   size_t pool_huge_page = 0;
   uint16_t* idx = nullptr;           // bf16 indexer [U][stride][128]
   int8_t* idx8 = nullptr;            // int8 indexer codes [U][stride][128]
@@ -101,6 +103,15 @@ struct kvo_handle {
   uint32_t* chunk_flag = nullptr;
   int64_t chunk_cap = 0;
   uint32_t epoch = 0;
+  // deferred fill (KVO_OPT_DEFER_FILL): kvo_step assigns the miss rows' slots and
+  // leaves the rows to the next kvo_attend on the same units, which reads them
+  // from the host pool inside the attention kernel and writes them to the hot buffer
+  int defer_fill = 0;
+  bool fill_pending = false;           // a deferred step's rows are not yet in the hot buffer
+  std::vector<int32_t> pending_units;  // its unit list (materialised)
+  const int32_t* pending_du = nullptr; // its device unit list
+  uint32_t* claim = nullptr;           // [U][C][3] claim words of the fetching attention
+  uint32_t fetch_epoch = 0;
   // unit groups: miss-row copies overlap the next group's scoring
   int groups = 1;
   int score_ctas = 0;
@@ -167,7 +178,7 @@ void free_all(kvo_handle* h) {
                  h->tspec, h->fb, h->fb_any, h->tok_bits, h->order, h->order_par, h->seg_keys, h->seg_cnt, h->sel_pay,
                  h->miss_tok, h->miss_slot, h->miss_cnt, h->miss_off, h->done_ctr, h->err,
                  h->stats, h->pbeg, h->pdone, h->ctr, h->plan_flag, h->fseg_keys, h->fseg_cnt, h->chunk_unit,
-                 h->chunk_start, h->chunk_cnt, h->chunk_flag};
+                 h->chunk_start, h->chunk_cnt, h->chunk_flag, h->claim};
   for (void* p : dev)
     if (p) cudaFree(p);
   if (h->bytes_seen) cudaFree(h->bytes_seen);
@@ -182,29 +193,13 @@ size_t residency_smem_bytes(int C, int P, int k) {
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
-// Size of the kernel's transparent huge pages (0 when not offered).
-size_t thp_size() {
-  FILE* f = fopen("/sys/kernel/mm/transparent_hugepage/hpage_pmd_size", "r");
-  if (!f) return 0;
-  unsigned long long v = 0;
-  if (fscanf(f, "%llu", &v) != 1) v = 0;
-  fclose(f);
-  FILE* e = fopen("/sys/kernel/mm/transparent_hugepage/enabled", "r");
-  if (!e) return 0;
-  char buf[128] = {};
-  const size_t n = fread(buf, 1, sizeof(buf) - 1, e);
-  fclose(e);
-  buf[n] = 0;
-  if (strstr(buf, "[never]")) return 0;
-  return (size_t)v;
-}
-
-// The pinned host pool.  Rows are read at random by the GPU over the host
-// link, and with base pages the address translation of a large pool becomes
-// the limit (measured: ~200 GB/s up to ~21 GB of pool, 37-52 GB/s at 43 GB
-// with 64 KB pages, 80 GB/s with 512 MB pages).  Pools of at least four huge
-// pages are therefore mapped with transparent huge pages (madvise) and
-// registered; otherwise, or when that fails, cudaHostAlloc.
+// The pinned host pool: driver-allocated pinned memory (cudaHostAlloc), mapped
+// into the GPU's address space.  An anonymous mapping backed by transparent huge
+// pages and registered with cudaHostRegister gathered faster while its huge pages
+// stayed whole, but the host kernel split some of them while the GPU read the pool
+// (vmstat thp_split_pmd), and each split cost the following steps tens to hundreds
+// of milliseconds of GPU address translation; driver-allocated memory is never
+// split, compacted or migrated.
 cudaError_t alloc_host_pool(kvo_handle* h, size_t bytes) {
   void* p = nullptr;
   cudaError_t e = kvo::alloc_pinned(bytes, &p, &h->pool_map_bytes, &h->pool_huge_page);
@@ -300,6 +295,7 @@ int resolve_units(kvo_handle* h, const int32_t* units, int32_t n_units, cudaStre
   return KVO_OK;
 }
 
+
 cudaEvent_t take_event(kvo_handle* h) {
   if (!h->free_events.empty()) {
     cudaEvent_t e = h->free_events.back();
@@ -321,6 +317,51 @@ cudaError_t timed(kvo_handle* h, int kind, cudaStream_t s, F launch) {
   if (e1) cudaEventRecord(e1, s);
   if (e0 && e1) h->recs.push_back({kind, e0, e1});
   return e;
+}
+
+// The unit list of a call, materialised (NULL = all units in order).
+std::vector<int32_t> unit_list(const kvo_handle* h, const int32_t* units, int32_t n_units) {
+  std::vector<int32_t> v;
+  if (units) {
+    v.assign(units, units + (n_units > 0 ? n_units : 0));
+  } else {
+    v.resize((size_t)h->U);
+    for (int32_t u = 0; u < h->U; ++u) v[(size_t)u] = u;
+  }
+  return v;
+}
+
+// Completes a deferred fill on stream s: the pending step's miss rows are copied
+// into the hot buffer (used when no fetching kvo_attend on the same units follows).
+int flush_pending(kvo_handle* h, cudaStream_t s) {
+  if (!h->fill_pending) return KVO_OK;
+  kvo::GatherArgs ga{};
+  ga.units = h->pending_du;
+  ga.n = (int32_t)h->pending_units.size();
+  ga.row_elems = h->R;
+  ga.C = h->C;
+  ga.stride = h->stride;
+  ga.rows = host_rows_of(h);
+  ga.host_pool = h->host_pool_dev;
+  ga.hot = h->hot;
+  ga.miss_tok = h->miss_tok;
+  ga.miss_slot = h->miss_slot;
+  ga.miss_cnt = h->miss_cnt;
+  ga.pk = h->P * h->k;
+  ga.stats = h->stats;
+  ga.err = h->err;
+  ga.wait_ns = h->wait_ns;
+  cudaError_t e = timed(h, KVO_PROF_GATHER, s, [&] { return kvo::launch_flush_fill(ga, s); });
+  if (e != cudaSuccess) return cuda_fail(e, "deferred fill");
+  h->fill_pending = false;
+  return KVO_OK;
+}
+
+// Records a step whose fill was deferred.
+void set_pending(kvo_handle* h, const int32_t* units, int32_t n_units, const int32_t* du) {
+  h->pending_units = unit_list(h, units, n_units);
+  h->pending_du = du;
+  h->fill_pending = true;
 }
 
 int grid_for(int64_t T, int G_max) {
@@ -458,6 +499,8 @@ int fused_step(kvo_handle* h, const int32_t* du, const int32_t* units, int32_t n
   f.smem_bytes = (int)kvo::fused_smem_bytes(h->P, h->k, h->cap, h->int8);
   f.plan_flag = h->plan_flag;
   f.qdone = h->qdone;
+  f.defer = h->defer_fill;
+  if (f.defer) f.n_gather = 0;  // nothing to fill: every CTA scores
 
   // the plan runs inside the fused launch (its CTA 0)
   cudaError_t e = timed(h, KVO_PROF_FUSED, s, [&] { return kvo::launch_fused(f, h->n_sm, s); });
@@ -479,51 +522,18 @@ namespace kvo {
 int set_error(int code, const char* msg) { return fail(code, msg); }
 int set_cuda_error(cudaError_t e, const char* what) { return cuda_fail(e, what); }
 
-// Pinned, device-mapped host memory.  Rows are read at random by the GPU over
-// the host link, and with base pages the address translation of a large pool
-// becomes the limit (measured: ~200 GB/s up to ~21 GB of pool, 37-52 GB/s at
-// 43 GB with 64 KB pages, 80 GB/s with 512 MB pages).  Allocations of at least
-// four huge pages are therefore mapped with transparent huge pages (madvise)
-// and registered (*map_bytes > 0); otherwise, or when that fails,
-// cudaHostAlloc (*map_bytes = 0).
+// Pinned, device-mapped host memory from the driver (cudaHostAlloc); map_bytes
+// and huge_page are always 0 (no anonymous mapping of this library's own).
 cudaError_t alloc_pinned(size_t bytes, void** out, size_t* map_bytes, size_t* huge_page) {
-  *out = nullptr;
   *map_bytes = 0;
   *huge_page = 0;
-  const size_t huge = thp_size();
-  if (huge >= (2u << 20) && bytes >= 4 * huge) {
-    const size_t len = (bytes + huge - 1) / huge * huge;
-    void* raw = mmap(nullptr, len + huge, PROT_READ | PROT_WRITE, MAP_PRIVATE | MAP_ANONYMOUS | MAP_NORESERVE, -1, 0);
-    if (raw != MAP_FAILED) {
-      const uintptr_t r = reinterpret_cast<uintptr_t>(raw);
-      const uintptr_t a = (r + huge - 1) / huge * huge;
-      if (a > r) munmap(raw, a - r);
-      const size_t tail = (r + len + huge) - (a + len);
-      if (tail) munmap(reinterpret_cast<void*>(a + len), tail);
-      void* p = reinterpret_cast<void*>(a);
-      if (madvise(p, len, MADV_HUGEPAGE) == 0 &&
-          cudaHostRegister(p, len, cudaHostRegisterMapped | cudaHostRegisterPortable) == cudaSuccess) {
-        *out = p;
-        *map_bytes = len;
-        *huge_page = huge;
-        return cudaSuccess;
-      }
-      cudaGetLastError();  // clear a failed registration
-      munmap(p, len);
-    }
-  }
   cudaError_t e = cudaHostAlloc(out, bytes, cudaHostAllocMapped | cudaHostAllocPortable);
   if (e != cudaSuccess) *out = nullptr;
   return e;
 }
 
-void free_pinned(void* p, size_t map_bytes) {
-  if (p && map_bytes) {
-    cudaHostUnregister(p);
-    munmap(p, map_bytes);
-  } else if (p) {
-    cudaFreeHost(p);
-  }
+void free_pinned(void* p, size_t /*map_bytes*/) {
+  if (p) cudaFreeHost(p);
 }
 
 }  // namespace kvo
@@ -832,12 +842,17 @@ int kvo_step(kvo_handle* h, const int32_t* units, int32_t n_units, const void* q
   if (!aligned16(queries)) return fail(KVO_EINVAL, "queries not 16-byte aligned");
   DeviceGuard guard(h->device);
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  const int32_t* du = nullptr;
-  int rc = resolve_units(h, units, n_units, s, &du);
+  int rc = flush_pending(h, s);  // a deferred fill no attention call took up
   if (rc != KVO_OK) return rc;
-  if (use_fused(h, units, n_units))
-    return fused_step(h, du, units, n_units, queries, topk_tokens, topk_slots, topk_scores, topk_payload,
-                      unit_status, s);
+  const int32_t* du = nullptr;
+  rc = resolve_units(h, units, n_units, s, &du);
+  if (rc != KVO_OK) return rc;
+  if (use_fused(h, units, n_units)) {
+    rc = fused_step(h, du, units, n_units, queries, topk_tokens, topk_slots, topk_scores, topk_payload,
+                    unit_status, s);
+    if (rc == KVO_OK && h->defer_fill) set_pending(h, units, n_units, du);
+    return rc;
+  }
   const int PK = h->P * h->k;
   int NG = h->groups < n_units ? h->groups : n_units;
   if (NG < 1) NG = 1;
@@ -958,7 +973,9 @@ int kvo_step(kvo_handle* h, const int32_t* units, int32_t n_units, const void* q
     ga.stats = h->stats;
     ga.err = h->err;
     ga.wait_ns = h->wait_ns;
-    if (NG > 1) {
+    if (h->defer_fill) {
+      // the rows are left for the attention call (or the next call's flush)
+    } else if (NG > 1) {
       if (e == cudaSuccess) e = cudaEventRecord(h->ev_group[g], s);
       if (e == cudaSuccess) e = cudaStreamWaitEvent(h->side, h->ev_group[g], 0);
       if (e == cudaSuccess)
@@ -974,6 +991,7 @@ int kvo_step(kvo_handle* h, const int32_t* units, int32_t n_units, const void* q
   if (e != cudaSuccess) return cuda_fail(e, "step launch");
   ++h->host_steps;
   ++h->planned_steps;
+  if (h->defer_fill) set_pending(h, units, n_units, du);
   return KVO_OK;
 }
 
@@ -990,8 +1008,9 @@ size_t kvo_select_workspace_size(int32_t n_units, int32_t n_pos, int32_t k, int3
 int kvo_select(const void* keys, int64_t unit_stride, const int32_t* cache_slots,
                const int64_t* lengths, int32_t n_units, int32_t n_pos, int32_t k,
                const void* queries, int32_t* tokens, float* scores, int32_t* payload,
-               void* workspace, size_t workspace_bytes, void* stream) {
+               void* workspace, size_t workspace_bytes, uint32_t* status, void* stream) {
   if (!keys || !lengths || !queries || !tokens || !workspace) return fail(KVO_EINVAL, "NULL argument");
+  if (reinterpret_cast<uintptr_t>(status) & 3u) return fail(KVO_EINVAL, "status not 4-byte aligned");
   if (n_units < 1 || n_pos < 1 || n_pos > 8 || k < 1 || k > 4096) return fail(KVO_EINVAL, "size out of range");
   if (unit_stride < 1 || unit_stride >= (int64_t)1 << 31) return fail(KVO_EINVAL, "unit_stride out of range");
   if (!aligned16(keys) || !aligned16(queries)) return fail(KVO_EINVAL, "keys/queries not 16-byte aligned");
@@ -1022,7 +1041,7 @@ int kvo_select(const void* keys, int64_t unit_stride, const int32_t* cache_slots
   uint64_t* d_seg_keys = reinterpret_cast<uint64_t*>(w); w += up(segs * PK * 8);
   int32_t* d_seg_cnt = reinterpret_cast<int32_t*>(w); w += up(segs * n_pos * 4);
   int32_t* d_pay = reinterpret_cast<int32_t*>(w); w += up(n * PK * 4);
-  uint32_t* d_err = reinterpret_cast<uint32_t*>(w);
+  uint32_t* d_err = status ? status : reinterpret_cast<uint32_t*>(w);  // the caller's word when given
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   cudaError_t e = cudaMemcpyAsync(d_units, host.data(), n * 4, cudaMemcpyHostToDevice, s);
   if (e == cudaSuccess) e = cudaMemcpyAsync(d_len, host.data() + n, n * 4, cudaMemcpyHostToDevice, s);
@@ -1107,6 +1126,25 @@ int kvo_set_option(kvo_handle* h, int32_t key, int64_t value) {
     }
     case KVO_OPT_HOST_HUGE_PAGE:
       return fail(KVO_EINVAL, "read-only option");
+    case KVO_OPT_DEFER_FILL: {
+      if (value != 0 && value != 1) return fail(KVO_EINVAL, "defer_fill is 0 or 1");
+      if (value == 1 && h->R != 576) return fail(KVO_EINVAL, "defer_fill needs the attention row (576 elements)");
+      if (value == 1 && !h->claim) {
+        DeviceGuard guard(h->device);
+        const size_t n = (size_t)h->U * (size_t)h->C * 3;
+        cudaError_t e = dalloc(&h->claim, n);
+        if (e == cudaSuccess) e = cudaMemset(h->claim, 0, n * 4);
+        if (e != cudaSuccess) {
+          if (h->claim) cudaFree(h->claim);
+          h->claim = nullptr;
+          cudaGetLastError();  // as in kvo_create: not left as the thread's last CUDA error
+          return fail(KVO_ENOMEM, std::string("claim words: ") + cudaGetErrorString(e));
+        }
+        h->fetch_epoch = 0;
+      }
+      h->defer_fill = (int)value;
+      return KVO_OK;
+    }
     case KVO_OPT_WAIT_LIMIT_NS:
       if (value < 1000) return fail(KVO_EINVAL, "wait limit below 1 us");
       h->wait_ns = (uint64_t)value;
@@ -1129,6 +1167,7 @@ int kvo_get_option(kvo_handle* h, int32_t key, int64_t* value) {
     case KVO_OPT_GATHER_CTAS: *value = h->gather_ctas; return KVO_OK;
     case KVO_OPT_PIECE_TOKENS: *value = h->piece_tokens; return KVO_OK;
     case KVO_OPT_HOST_HUGE_PAGE: *value = (int64_t)h->pool_huge_page; return KVO_OK;
+    case KVO_OPT_DEFER_FILL: *value = h->defer_fill; return KVO_OK;
     default: return fail(KVO_EINVAL, "unknown option");
   }
 }
@@ -1143,8 +1182,10 @@ int kvo_reset(kvo_handle* h, const int32_t* units, int32_t n_units, int64_t keep
     if (u < 0 || u >= h->U) return fail(KVO_ERANGE, "unit id out of range");
     if (h->len_host[(size_t)u] < keep_tokens) return fail(KVO_ERANGE, "keep_tokens beyond a unit's length");
   }
+  int rc = flush_pending(h, s);
+  if (rc != KVO_OK) return rc;
   const int32_t* du = nullptr;
-  int rc = resolve_units(h, units, n_units, s, &du);
+  rc = resolve_units(h, units, n_units, s, &du);
   if (rc != KVO_OK) return rc;
   kvo::ResetArgs a{};
   a.units = du;
@@ -1179,10 +1220,36 @@ int kvo_attend(kvo_handle* h, const int32_t* units, int32_t n_units, const void*
   if (!(scale == scale) || scale > 3.0e38f || scale < -3.0e38f) return fail(KVO_EINVAL, "scale is not finite");
   DeviceGuard guard(h->device);
   cudaStream_t s = static_cast<cudaStream_t>(stream);
+  // After a deferred step on the same units, the attention kernel fills the
+  // step's miss rows itself; any other unit list completes the fill first.
+  bool fetch = false;
+  if (h->fill_pending) {
+    fetch = unit_list(h, units, n_units) == h->pending_units;
+    if (!fetch) {
+      const int rf = flush_pending(h, s);
+      if (rf != KVO_OK) return rf;
+    }
+  }
   const int32_t* du = nullptr;
   int rc = resolve_units(h, units, n_units, s, &du);
   if (rc != KVO_OK) return rc;
   kvo::AttendArgs a{};
+  if (fetch) {
+    if (h->fetch_epoch >= 0x7ffffff0u) {  // 2e + 1 must stay below 2^32: start the claim words again
+      cudaError_t ez = cudaMemsetAsync(h->claim, 0, (size_t)h->U * h->C * 3 * 4, s);
+      if (ez != cudaSuccess) return cuda_fail(ez, "claim words");
+      h->fetch_epoch = 0;
+    }
+    a.pay = h->sel_pay;
+    a.host_pool = h->host_pool_dev;
+    a.hrows = host_rows_of(h);
+    a.hot_w = h->hot;
+    a.claim = h->claim;
+    a.epoch = ++h->fetch_epoch;
+    const int pairs = h->n_sm / 2, per_unit = h->P * (n_heads / 128);
+    a.group = pairs / per_unit > 0 ? pairs / per_unit : 1;
+    a.stats = h->stats;
+  }
   a.units = du;
   a.slots = topk_slots;
   a.q = static_cast<const uint16_t*>(queries);
@@ -1199,6 +1266,7 @@ int kvo_attend(kvo_handle* h, const int32_t* units, int32_t n_units, const void*
   a.wait_ns = h->wait_ns;
   cudaError_t e = timed(h, KVO_PROF_ATTEND, s, [&] { return kvo::launch_attend(a, s); });
   if (e != cudaSuccess) return cuda_fail(e, "attention launch");
+  if (fetch) h->fill_pending = false;
   return KVO_OK;
 }
 
@@ -1256,6 +1324,7 @@ int kvo_get_stats(kvo_handle* h, kvo_stats* out) {
   out->rescored = d.rescored;
   out->fused_steps = h->fused_steps;
   out->block_errors = d.block_errors;
+  out->fetch_dup_bytes = d.fetch_dup_bytes;
   return KVO_OK;
 }
 
@@ -1265,6 +1334,11 @@ int kvo_export_state(kvo_handle* h, int32_t unit, int32_t* cache_slots, int32_t*
   if (unit < 0 || unit >= h->U) return fail(KVO_ERANGE, "unit out of range");
   DeviceGuard guard(h->device);
   cudaError_t e = cudaDeviceSynchronize();
+  if (e == cudaSuccess && h->fill_pending) {  // the state is exported complete
+    const int rf = flush_pending(h, 0);
+    if (rf != KVO_OK) return rf;
+    e = cudaDeviceSynchronize();
+  }
   const size_t S = (size_t)h->stride, C = (size_t)h->C;
   if (e == cudaSuccess && cache_slots)
     e = cudaMemcpy(cache_slots, h->cache_slots + unit * S, (size_t)h->cfg.max_tokens * 4, cudaMemcpyDeviceToHost);

@@ -79,7 +79,10 @@ constexpr uint32_t kXSOff = kPOff + 2 * kPSlab;             // partner's partial
 constexpr uint32_t kXSBytes = kM * kOwnRows * 4;           // partial scores of 64 rows of 128 heads
 constexpr uint32_t kXMOff = kXSOff + kXSBytes;              // partner's block maxima [2][128], then its l
 constexpr uint32_t kBarOff = kXMOff + 2 * kM * 4;
-constexpr uint32_t kAttSmem = kBarOff + 256 + 1024;  // barriers, flags, 1 KB alignment slack
+constexpr uint32_t kFetchOff = kBarOff + 256;        // fetching variant: claim-mask barriers [2], masks [2][2][4]
+constexpr uint32_t kAttSmem = kFetchOff + 128 + 1024;  // barriers, flags, masks, 1 KB alignment slack
+constexpr int kWriterWarp = 9;                        // fetching variant: writes filled rows to the hot buffer
+constexpr int kAttThreadsFetch = kAttThreads + 32;
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kColO = 0;    // O: 256 fp32 columns
 constexpr uint32_t kColS = 256;  // S: 128 fp32 columns (this CTA's partial, then read out)
@@ -180,6 +183,64 @@ __device__ __forceinline__ float ex2_ftz(float x) {
   asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
   return y;
 }
+__device__ __forceinline__ uint4 ld_shared_u4(uint32_t addr) {
+  uint4 v;
+  asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(addr)
+               : "memory");
+  return v;
+}
+__device__ __forceinline__ uint32_t ld_acquire_gpu(const uint32_t* p) {
+  uint32_t v;
+  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+__device__ __forceinline__ void st_release_gpu(uint32_t* p, uint32_t v) {
+  asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+// Source of one part of a miss row in this call (epoch e, e2 = 2e): 0 = the hot
+// buffer (another CTA has written it: 2e + 1), 1 = the host pool, claimed by this
+// CTA (which then writes it to the hot buffer), 2 = the host pool, claimed by
+// another CTA that has not finished writing it (the same bytes, read again).
+__device__ __forceinline__ int claim_part(uint32_t* w, uint32_t e2) {
+  if (ld_acquire_gpu(w) == e2 + 1u) return 0;
+  return atomicMax(w, e2) < e2 ? 1 : 2;
+}
+// The order of the (unit, position) pairs of the fetching variant.  Rounds of G
+// units: round r runs position 0 of units rG.. (their miss rows are fetched
+// and written by these pairs), then positions 1..P-1 of the previous round's
+// units, whose shared miss rows are by then mostly in the hot buffer.  Pair b
+// of n*P -> (list index i, position p).
+__device__ __forceinline__ void pair_order(int b, int n, int P, int G, int& i, int& p) {
+  i = 0;
+  p = 0;
+  if (P == 1 || G <= 0) {
+    i = b / P;
+    p = b % P;
+    return;
+  }
+  const int ng = (n + G - 1) / G;
+  int base = 0;
+  for (int r = 0; r <= ng; ++r) {
+    if (r < ng) {
+      const int g = min(G, n - r * G);
+      if (b < base + g) {
+        i = r * G + (b - base);
+        return;
+      }
+      base += g;
+    }
+    if (r >= 1) {
+      const int g = min(G, n - (r - 1) * G);
+      if (b < base + (P - 1) * g) {
+        const int x = b - base;
+        p = 1 + x / g;
+        i = (r - 1) * G + x % g;
+        return;
+      }
+      base += (P - 1) * g;
+    }
+  }
+}
 // 16-byte chunk c (0..7) of row r in a 128-byte-swizzled slab (1 KB aligned).
 __device__ __forceinline__ uint32_t swz(uint32_t slab, int r, int c) {
   return slab + (uint32_t)r * 128u + ((uint32_t)(c ^ (r & 7)) << 4);
@@ -247,7 +308,9 @@ __device__ __forceinline__ void cluster_sync() {
   asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
 }
 
-__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kAttThreads, 1) attend_kernel(AttendArgs a) {
+template <bool kFetch>
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kFetch ? kAttThreadsFetch : kAttThreads, 1)
+    attend_kernel(AttendArgs a) {
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
   const uint32_t pad = ((raw + 1023u) & ~1023u) - raw;  // the same in both CTAs
@@ -267,6 +330,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kAttThreads, 1) atte
   uint64_t* fin = o_final + 1;        // MMA: everything issued is done
   volatile uint32_t* tmem_slot = reinterpret_cast<volatile uint32_t*>(fin + 1);
   volatile uint32_t* abort_flag = tmem_slot + 1;
+  uint64_t* m_ready = reinterpret_cast<uint64_t*>(smem + kFetchOff);     // [2] copies: a block's claim masks set
+  uint32_t* cmask = reinterpret_cast<uint32_t*>(smem + kFetchOff + 16);  // [block & 1][value, rope][4 words]
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   int b = blockIdx.x;
@@ -276,8 +341,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kAttThreads, 1) atte
   const int HG = a.H / kM;
   const int hg = b % HG;
   b /= HG;
-  const int p = b % a.P;
-  const int i = b / a.P;
+  int p = b % a.P, i = b / a.P;
+  if (kFetch) pair_order(b, a.n, a.P, a.group, i, p);
   const int u = a.units[i];
   const int64_t list = ((int64_t)i * a.P + p) * a.k;
   const int64_t qrow0 = ((int64_t)i * a.P + p) * a.H + (int64_t)hg * kM;
@@ -292,7 +357,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kAttThreads, 1) atte
     mbar_init(q_full, kProducers + kSoftThreads);
     for (int s = 0; s < kRing; ++s) {
       mbar_init(&e_full[s], kProducers);
-      mbar_init(&e_free[s], 1);
+      mbar_init(&e_free[s], kFetch ? 2 : 1);  // fetching: the writer warp has read the entry too
+    }
+    if (kFetch) {
+      mbar_init(&m_ready[0], kProducers / 32);
+      mbar_init(&m_ready[1], kProducers / 32);
+      for (int w = 0; w < 16; ++w) cmask[w] = 0u;
     }
     mbar_init(s_full, 1);
     mbar_init(s_free, kSoftThreads);
@@ -332,24 +402,34 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kAttThreads, 1) atte
     }
     cp_async_arrive_noinc(q_full);
     const uint8_t* ubase = reinterpret_cast<const uint8_t*>(a.hot) + (size_t)u * a.C * (kRow * 2);
+    const uint8_t* hbase = reinterpret_cast<const uint8_t*>(a.host_pool);
     // this thread copies chunk csub of rows rsub + kRowStep m of every entry;
-    // the slots of the next block's rows are read a block ahead
+    // the slots (and, fetching, the payloads) of the next block's rows are read a block ahead
     const int rsub = tid >> 3, csub = tid & 7;
-    int32_t rs[kBlk / kRowStep], rs_next[kBlk / kRowStep];
+    constexpr int kRowsPT = kBlk / kRowStep;
+    int32_t rs[kRowsPT], rs_next[kRowsPT], py_next[kRowsPT];
+    int64_t hrow[kRowsPT];  // fetching: host-pool row of a miss row
     auto load_rows = [&](int j) {
 #pragma unroll
-      for (int m = 0; m < kBlk / kRowStep; ++m) {
+      for (int m = 0; m < kRowsPT; ++m) {
         const int r = j * kBlk + rsub + kRowStep * m;
-        rs_next[m] = j < nb && r < a.k ? __ldg(a.slots + list + r) : -1;
+        const bool in = j < nb && r < a.k;
+        rs_next[m] = in ? __ldg(a.slots + list + r) : -1;
+        if (kFetch) py_next[m] = in ? __ldg(a.pay + list + r) : INT32_MIN;
       }
     };
-    auto issue = [&](int slab, int slot) {
+    // host: bit m set = row m's part comes from the host pool
+    auto issue = [&](int slab, int slot, uint32_t host) {
       const uint32_t dst = sb + kROff + (uint32_t)slot * kEntry;
 #pragma unroll
-      for (int m = 0; m < kBlk / kRowStep; ++m)
-        cp_async16(swz(dst, rsub + kRowStep * m, csub), ubase + (size_t)rs[m] * (kRow * 2) + slab * 128 + csub * 16);
+      for (int m = 0; m < kRowsPT; ++m) {
+        const uint8_t* src = (kFetch && ((host >> m) & 1u)) ? hbase + hrow[m] * (kRow * 2)
+                                                             : ubase + (size_t)rs[m] * (kRow * 2);
+        cp_async16(swz(dst, rsub + kRowStep * m, csub), src + slab * 128 + csub * 16);
+      }
       cp_async_arrive_noinc(&e_full[slot]);  // counts once this thread's copies have landed
     };
+    unsigned long long dup_bytes = 0;
     load_rows(0);
     // A block's value slabs reuse the slots of block j-2's, freed by its P V;
     // the rope slot is reused every other block (the blocks of this CTA's parity).
@@ -367,14 +447,49 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kAttThreads, 1) atte
         fail();
         break;
       }
+      uint32_t host_v = 0u, host_r = 0u;
 #pragma unroll
-      for (int m = 0; m < kBlk / kRowStep; ++m)  // a pad reads a valid row; the softmax drops it
-        rs[m] = rs_next[m] < 0 || rs_next[m] >= a.C ? 0 : rs_next[m];
+      for (int m = 0; m < kRowsPT; ++m) {
+        const int32_t slot = rs_next[m];
+        const bool valid = slot >= 0 && slot < a.C;
+        rs[m] = valid ? slot : 0;  // a pad reads a valid row; the softmax drops it
+        if (kFetch) {
+          // a miss row of the step: its parts come from the host pool unless
+          // another CTA of this call has already written them to the hot buffer
+          const int32_t pay = py_next[m];
+          hrow[m] = -1;
+          int tv = 0, tr = 0;
+          if (valid && pay < 0 && pay != INT32_MIN) {
+            hrow[m] = host_row(a.hrows, u, (int64_t)(-(pay + 1)));
+            if (hrow[m] >= 0 && csub == 0) {  // one lane of the row's eight claims for them
+              uint32_t* w = a.claim + ((size_t)u * a.C + (size_t)slot) * 3;
+              const uint32_t e2 = 2u * a.epoch;
+              tv = claim_part(w + half, e2);
+              if (own_rope(j)) tr = claim_part(w + 2, e2);
+            }
+          }
+          tv = __shfl_sync(kFull, tv, lane & ~7);
+          tr = __shfl_sync(kFull, tr, lane & ~7);
+          if (tv) host_v |= 1u << m;
+          if (tr) host_r |= 1u << m;
+          const int r = rsub + kRowStep * m;
+          if (csub == 0) {
+            if (tv == 1) atomicOr(&cmask[((j & 1) * 2 + 0) * 4 + (r >> 5)], 1u << (r & 31));
+            if (tr == 1) atomicOr(&cmask[((j & 1) * 2 + 1) * 4 + (r >> 5)], 1u << (r & 31));
+            dup_bytes += (tv == 2 ? 512u : 0u) + (tr == 2 ? 128u : 0u);
+          }
+        }
+      }
       load_rows(j + 1);
-      if (own_rope(j)) issue(kRopeSlab, kRing - 1);
+      if (kFetch) {
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&m_ready[j & 1]);  // this warp's claims of block j are in the masks
+      }
+      if (own_rope(j)) issue(kRopeSlab, kRing - 1, host_r);
 #pragma unroll
-      for (int v = 0; v < kVSlabs; ++v) issue(kVSlabs * half + v, vb + v);
+      for (int v = 0; v < kVSlabs; ++v) issue(kVSlabs * half + v, vb + v, host_v);
     }
+    if (kFetch && dup_bytes && a.stats) atomicAdd(&a.stats->fetch_dup_bytes, dup_bytes);
     cp_async_wait_all();
   } else if (warp == kMmaWarp) {
     // ---- MMA issue (one thread) ----
@@ -464,6 +579,86 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kAttThreads, 1) atte
       if (!mbar_wait(fin, 0, a.wait_ns > 2000000000ull ? a.wait_ns : 2000000000ull)) fail();
     }
     __syncwarp();
+  } else if (kFetch && warp == kWriterWarp) {
+    // ---- fetching: the rows this CTA claimed go to their hot slots ----
+    // Once a block's entries have landed, each claimed row part is read from
+    // the ring (un-swizzled) and stored to the row's hot slot; then its claim
+    // word says written (release, after a fence), and the entries are freed.
+    uint8_t* hot_u = reinterpret_cast<uint8_t*>(a.hot_w) + (size_t)u * a.C * (kRow * 2);
+    const uint32_t done = 2u * a.epoch + 1u;
+    unsigned long long bytes = 0, rows = 0;
+    for (int j = 0; j < nb; ++j) {
+      if (__any_sync(kFull, *abort_flag != 0u)) break;
+      const uint32_t par = (uint32_t)(j >> 1) & 1u;
+      const int vb = kVSlabs * (j & 1);
+      const bool rope = own_rope(j);
+      bool ok = __all_sync(kFull, mbar_wait(&m_ready[j & 1], par, a.wait_ns));
+#pragma unroll
+      for (int v = 0; v < kVSlabs; ++v) ok = ok && __all_sync(kFull, mbar_wait(&e_full[vb + v], par, a.wait_ns));
+      if (rope) ok = ok && __all_sync(kFull, mbar_wait(&e_full[kRing - 1], par, a.wait_ns));
+      if (!ok) {
+        fail();
+        break;
+      }
+      uint32_t* mk = cmask + (j & 1) * 8;
+      uint32_t mv[4], mr[4];
+#pragma unroll
+      for (int w = 0; w < 4; ++w) {
+        mv[w] = mk[w];
+        mr[w] = mk[4 + w];
+      }
+      __syncwarp();
+      // cleared for block j + 2, whose claims start after this warp frees block j's entries
+      if (lane < 8) mk[lane] = 0u;
+      const int32_t* bslots = a.slots + list + (int64_t)j * kBlk;
+#pragma unroll 1
+      for (int w = 0; w < 4; ++w) {
+        uint32_t bits = mv[w];
+        while (bits) {  // value part: lane -> slab lane / 8, chunk lane % 8
+          const int r = 32 * w + __ffs(bits) - 1;
+          bits &= bits - 1u;
+          const int32_t slot = __ldg(bslots + r);
+          const int v = lane >> 3, c = lane & 7;
+          const uint4 x = ld_shared_u4(swz(sb + kROff + (uint32_t)(vb + v) * kEntry, r, c));
+          *reinterpret_cast<uint4*>(hot_u + (size_t)slot * (kRow * 2) + half * 512 + v * 128 + c * 16) = x;
+        }
+        bits = mr[w];
+        while (bits) {  // rope part: lanes 0-7, one chunk each
+          const int r = 32 * w + __ffs(bits) - 1;
+          bits &= bits - 1u;
+          if (lane < 8) {
+            const int32_t slot = __ldg(bslots + r);
+            const uint4 x = ld_shared_u4(swz(sb + kROff + (uint32_t)(kRing - 1) * kEntry, r, lane));
+            *reinterpret_cast<uint4*>(hot_u + (size_t)slot * (kRow * 2) + kRopeSlab * 128 + lane * 16) = x;
+          }
+        }
+      }
+      __threadfence();
+      __syncwarp();
+#pragma unroll
+      for (int w = 0; w < 4; ++w) {
+        if ((mv[w] >> lane) & 1u) {
+          const int32_t slot = __ldg(bslots + 32 * w + lane);
+          st_release_gpu(a.claim + ((size_t)u * a.C + (size_t)slot) * 3 + half, done);
+        }
+        if ((mr[w] >> lane) & 1u) {
+          const int32_t slot = __ldg(bslots + 32 * w + lane);
+          st_release_gpu(a.claim + ((size_t)u * a.C + (size_t)slot) * 3 + 2, done);
+        }
+        bytes += (unsigned long long)__popc(mv[w]) * 512u + (unsigned long long)__popc(mr[w]) * 128u;
+        if (half == 0) rows += (unsigned long long)__popc(mv[w]);
+      }
+      __syncwarp();
+      if (lane == 0) {  // the entries may be refilled once the MMAs are done with them too
+#pragma unroll
+        for (int v = 0; v < kVSlabs; ++v) mbar_arrive(&e_free[vb + v]);
+        if (rope) mbar_arrive(&e_free[kRing - 1]);
+      }
+    }
+    if (lane == 0 && a.stats && bytes) {
+      atomicAdd(&a.stats->bytes_h2d, bytes);
+      if (rows) atomicAdd(&a.stats->rows_h2d, rows);
+    }
   } else if (warp >= kSoftWarp0 && warp < kSoftWarp0 + kSoftThreads / 32) {
     // ---- online softmax: head hd (TMEM lane hd), rows 64 half.. of each block ----
     const int hd = tid - kSoftWarp0 * 32;
@@ -686,10 +881,16 @@ size_t attend_smem_bytes() { return kAttSmem; }
 
 cudaError_t launch_attend(const AttendArgs& a, cudaStream_t s) {
   if (a.n <= 0) return cudaSuccess;
-  cudaError_t e = cudaFuncSetAttribute(attend_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kAttSmem);
-  if (e != cudaSuccess) return e;
   const int64_t grid = (int64_t)a.n * a.P * (a.H / kM) * 2;
-  attend_kernel<<<(unsigned)grid, kAttThreads, kAttSmem, s>>>(a);
+  if (a.pay) {
+    cudaError_t e = cudaFuncSetAttribute(attend_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kAttSmem);
+    if (e != cudaSuccess) return e;
+    attend_kernel<true><<<(unsigned)grid, kAttThreadsFetch, kAttSmem, s>>>(a);
+  } else {
+    cudaError_t e = cudaFuncSetAttribute(attend_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kAttSmem);
+    if (e != cudaSuccess) return e;
+    attend_kernel<false><<<(unsigned)grid, kAttThreads, kAttSmem, s>>>(a);
+  }
   return cudaGetLastError();
 }
 

@@ -447,7 +447,7 @@ __device__ __forceinline__ void finish_unit(const FusedArgs& f, const FusedSmem&
   residency_body<kCT>(f.r, i, bitmap, M, V, fs.sm.hist, ctid, [] { consumer_sync(); }, nullptr, [&](uint32_t m) {
     __threadfence();
     consumer_sync();
-    if (ctid < 32) publish_chunks(f, i, m, ctid);
+    if (ctid < 32) publish_chunks(f, i, f.defer ? 0u : m, ctid);  // deferred: the rows stay for the attention call
   });
 }
 

@@ -19,7 +19,7 @@ constexpr uint32_t kErrPlan = 2u;
 // Device-side counters (mirrors kvo_stats).
 struct DevStats {
   unsigned long long steps, unit_steps, capacity_errors, hits, misses, rows_h2d, bytes_h2d,
-      rows_d2h, bytes_d2h, timeouts, rescored, block_errors;
+      rows_d2h, bytes_d2h, timeouts, rescored, block_errors, fetch_dup_bytes;
 };
 
 // Host-pool row of token t of unit u: contiguous per unit (blocks == nullptr),
@@ -277,6 +277,7 @@ struct GatherArgs {
   const int32_t* miss_tok;
   const int32_t* miss_slot;
   const int64_t* miss_off;     // [n+1]
+  const int32_t* miss_cnt;     // [n] (the deferred fill's flush)
   int32_t pk;                  // stride of the miss lists
   DevStats* stats;
   uint32_t* err;
@@ -295,6 +296,17 @@ struct AttendArgs {
   float scale_log2;       // softmax scale * log2(e)
   uint32_t* err;
   uint64_t wait_ns;
+  // In-kernel fill of the step's miss rows (used by the fetching variant only):
+  // an entry whose payload is a miss (pay < 0, not the pad value) names token
+  // -pay-1 of the host pool, read inside the kernel and written to its slot.
+  const int32_t* pay;         // [n][P][k] the step's packed payloads
+  const uint16_t* host_pool;  // device-visible address of the pinned pool
+  HostRows hrows;             // token -> host-pool row
+  uint16_t* hot_w;            // == hot, for the writes of filled rows
+  uint32_t* claim;            // [U][C][3] claim words of (slot, part): 2e claimed, 2e + 1 written
+  uint32_t epoch;             // this call's e (>= 1)
+  int group;                  // units per round of the pair order
+  DevStats* stats;
 };
 
 struct AppendArgs {
@@ -364,6 +376,7 @@ struct FusedArgs {
   int32_t smem_bytes;          // dynamic shared memory of one CTA
   uint32_t* plan_flag;         // == epoch once CTA 0 has run the plan
   uint32_t* qdone;             // CTAs done quantizing queries (int8 indexer); zero between launches
+  int32_t defer;               // 1: the miss rows are left for the attention call (nothing is published)
 };
 
 // Sets the thread-local message returned by kvo_last_error().
@@ -376,8 +389,9 @@ cudaError_t launch_score(const SelectArgs& a, cudaStream_t s);
 cudaError_t launch_select(const SelectArgs& a, cudaStream_t s);
 cudaError_t launch_residency(const ResidencyArgs& a, cudaStream_t s);
 cudaError_t launch_gather(const GatherArgs& a, int n_sm, cudaStream_t s);
+cudaError_t launch_flush_fill(const GatherArgs& a, cudaStream_t s);  // one CTA per listed unit, miss_cnt rows each
 cudaError_t launch_append(const AppendArgs& a, cudaStream_t s);
-cudaError_t launch_attend(const AttendArgs& a, cudaStream_t s);
+cudaError_t launch_attend(const AttendArgs& a, cudaStream_t s);  // a.pay != nullptr: fetching variant
 cudaError_t run_wait_selftest(uint64_t limit_ns, unsigned long long* host_out);  // out[3]
 // host helpers shared by the entry points (kvo_api.cu)
 int set_error(int code, const char* msg);

@@ -21,7 +21,16 @@
 //
 // The first call on a device resolves the array's device address for that
 // device (cudaGetSymbolAddress, with that device current), once per device;
-// make that first call before any stream capture.
+// make that first call before any stream capture.  The address is kept for
+// the life of the process: a cudaDeviceReset on that device ends the module
+// instance it points into, so calls after a reset are not supported (as for
+// every other resource of this library on that device).
+//
+// Completion status: the kernels record an expired bounded wait (bit 1) or a
+// failed internal consistency check (bit 2) in an error word.  A caller that
+// passes `status` (a device word of its own) gets that word there, cleared at
+// the start of the call; nonzero means the outputs are not valid.  Without
+// `status` the word lives in the fixed array and cannot be observed.
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -68,7 +77,7 @@ extern "C" {
 int kvo_select_noalloc(const void* keys, int64_t unit_stride, const int32_t* cache_slots,
                        const int64_t* lengths, int32_t n_units, int32_t n_pos, int32_t k,
                        const void* queries, int32_t* tokens, float* scores, int32_t* payload,
-                       void* stream) {
+                       uint32_t* status, void* stream) {
   if (!keys || !lengths || !queries || !tokens) return noalloc_fail(KVO_EINVAL, "NULL argument");
   if (n_units < 1 || n_pos < 1 || n_pos > 8 || k < 1 || k > 4096)
     return noalloc_fail(KVO_EINVAL, "size out of range");
@@ -78,6 +87,7 @@ int kvo_select_noalloc(const void* keys, int64_t unit_stride, const int32_t* cac
     return noalloc_fail(KVO_EINVAL, "unit_stride out of range");
   if ((reinterpret_cast<uintptr_t>(keys) & 15u) || (reinterpret_cast<uintptr_t>(queries) & 15u))
     return noalloc_fail(KVO_EINVAL, "keys/queries not 16-byte aligned");
+  if (reinterpret_cast<uintptr_t>(status) & 3u) return noalloc_fail(KVO_EINVAL, "status not 4-byte aligned");
   const int cap = kvo::score_cap_for(n_pos, k, false);
   if (cap == 0) return noalloc_fail(KVO_EINVAL, "k too large for n_pos");
   int dev = 0, n_sm = 0;
@@ -108,7 +118,8 @@ int kvo_select_noalloc(const void* keys, int64_t unit_stride, const int32_t* cac
     if (!g_noalloc_ptr[dev]) {
       void* p = nullptr;
       const cudaError_t e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
-      if (e != cudaSuccess || !p) return noalloc_fail(KVO_ECUDA, "cudaGetSymbolAddress of the fixed scratch failed");
+      if (e != cudaSuccess) return kvo::set_cuda_error(e, "cudaGetSymbolAddress of the fixed scratch");
+      if (!p) return noalloc_fail(KVO_ECUDA, "cudaGetSymbolAddress of the fixed scratch returned NULL");
       g_noalloc_ptr[dev] = p;
     }
     base = g_noalloc_ptr[dev];
@@ -122,12 +133,12 @@ int kvo_select_noalloc(const void* keys, int64_t unit_stride, const int32_t* cac
   uint64_t* d_seg_keys = reinterpret_cast<uint64_t*>(w); w += up256(segs * PK * 8);
   int32_t* d_seg_cnt = reinterpret_cast<int32_t*>(w); w += up256(segs * n_pos * 4);
   int32_t* d_pay = reinterpret_cast<int32_t*>(w); w += up256(n * PK * 4);
-  uint32_t* d_err = reinterpret_cast<uint32_t*>(w);
+  uint32_t* d_err = status ? status : reinterpret_cast<uint32_t*>(w);
 
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   noalloc_setup_kernel<<<1, 64, 0, s>>>(lens, d_units, d_len, d_err);
   cudaError_t e = cudaGetLastError();
-  if (e != cudaSuccess) return noalloc_fail(KVO_ECUDA, "set-up launch failed");
+  if (e != cudaSuccess) return kvo::set_cuda_error(e, "no-allocation select set-up launch");
 
   kvo::SelectArgs sa{};
   sa.keys = static_cast<const uint16_t*>(keys);
@@ -157,7 +168,7 @@ int kvo_select_noalloc(const void* keys, int64_t unit_stride, const int32_t* cac
   e = kvo::launch_plan(sa, s);
   if (e == cudaSuccess) e = kvo::launch_score(sa, s);
   if (e == cudaSuccess) e = kvo::launch_select(sa, s);
-  if (e != cudaSuccess) return noalloc_fail(KVO_ECUDA, "select launch failed");
+  if (e != cudaSuccess) return kvo::set_cuda_error(e, "no-allocation select launch");
   return KVO_OK;
 }
 

@@ -328,6 +328,41 @@ cudaError_t launch_residency(const ResidencyArgs& a, cudaStream_t s) {
   return cudaGetLastError();
 }
 
+// A deferred fill completed without the attention call: CTA i copies the
+// miss_cnt[i] rows of listed unit i, 16 bytes per thread and step.
+__global__ void __launch_bounds__(256) flush_fill_kernel(GatherArgs a) {
+  const int i = blockIdx.x;
+  const int64_t u = a.units[i];
+  const int64_t m = a.miss_cnt[i];
+  const int chunks = a.row_elems / 8;
+  unsigned long long rows = 0, bad = 0;
+  for (int64_t e = threadIdx.x; e < m * chunks; e += blockDim.x) {
+    const int64_t r = e / chunks;
+    const int c = (int)(e % chunks);
+    const int32_t t = a.miss_tok[(int64_t)i * a.pk + r];
+    const int32_t s = a.miss_slot[(int64_t)i * a.pk + r];
+    const int64_t hr = host_row(a.rows, u, t);
+    if (hr < 0) {  // unmapped block: the hot row stays as it was
+      bad += c == 0;
+      continue;
+    }
+    const uint4 x = *reinterpret_cast<const uint4*>(a.host_pool + hr * a.row_elems + c * 8);
+    *reinterpret_cast<uint4*>(a.hot + (u * a.C + s) * a.row_elems + c * 8) = x;
+    rows += c == 0;
+  }
+  if (a.stats && rows) {
+    atomicAdd(&a.stats->rows_h2d, rows);
+    atomicAdd(&a.stats->bytes_h2d, rows * (unsigned long long)a.row_elems * 2u);
+  }
+  if (a.stats && bad) atomicAdd(&a.stats->block_errors, bad);
+}
+
+cudaError_t launch_flush_fill(const GatherArgs& a, cudaStream_t s) {
+  if (a.n <= 0) return cudaSuccess;
+  flush_fill_kernel<<<a.n, 256, 0, s>>>(a);
+  return cudaGetLastError();
+}
+
 cudaError_t launch_gather(const GatherArgs& a, int n_sm, cudaStream_t s) {
   if (a.mode == KVO_GATHER_BULK) {
     const uint32_t slot_bytes = ((uint32_t)a.row_elems * 2u + 127u) & ~127u;

@@ -22,6 +22,8 @@ KVO_ECUDA = -4
 KVO_ETIMEOUT = -5
 KVO_ECAPACITY = -6
 KVO_PAD_PAYLOAD = -(2 ** 31)
+KVO_SELECT_ERR_TIMEOUT = 1  # bits of the select calls' status word
+KVO_SELECT_ERR_PLAN = 2
 
 KVO_OPT_GATHER_MODE = 1
 KVO_OPT_WAIT_LIMIT_NS = 2
@@ -33,6 +35,7 @@ KVO_OPT_FUSED = 7
 KVO_OPT_GATHER_CTAS = 8
 KVO_OPT_PIECE_TOKENS = 9
 KVO_OPT_HOST_HUGE_PAGE = 10
+KVO_OPT_DEFER_FILL = 11
 PROF_KINDS = ("append", "plan", "score", "select", "residency", "gather", "reset", "rescore",
               "reselect", "fused", "attend")
 KVO_IDX_BF16 = 0
@@ -68,7 +71,7 @@ class KvoStats(ctypes.Structure):
     _fields_ = [(n, ctypes.c_uint64) for n in
                 ("steps", "unit_steps", "capacity_errors", "hits", "misses", "rows_h2d",
                  "bytes_h2d", "rows_d2h", "bytes_d2h", "timeouts", "rescored", "fused_steps",
-                 "block_errors")]
+                 "block_errors", "fetch_dup_bytes")]
 
 
 class KvoError(RuntimeError):
@@ -111,9 +114,9 @@ def lib():
             L.kvo_select_workspace_size.argtypes = [i32, i32, i32, i32]
             L.kvo_select.restype = ctypes.c_int
             L.kvo_select.argtypes = [vp, i64, vp, vp, i32, i32, i32, vp, vp, vp, vp, vp,
-                                     ctypes.c_size_t, vp]
+                                     ctypes.c_size_t, vp, vp]
             L.kvo_select_noalloc.restype = ctypes.c_int
-            L.kvo_select_noalloc.argtypes = [vp, i64, vp, vp, i32, i32, i32, vp, vp, vp, vp, vp]
+            L.kvo_select_noalloc.argtypes = [vp, i64, vp, vp, i32, i32, i32, vp, vp, vp, vp, vp, vp]
             L.kvo_attend.restype = ctypes.c_int
             L.kvo_attend.argtypes = [vp, vp, i32, vp, i32, ctypes.c_float, vp, vp, vp, vp]
             L.kvo_reset.restype = ctypes.c_int
@@ -252,22 +255,24 @@ def kvo_select_workspace_size(n_units, n_pos, k, device=0):
 
 
 def kvo_select(keys, unit_stride, cache_slots, lengths, n_units, n_pos, k, queries, tokens,
-               scores, payload, workspace, workspace_bytes, stream=None):
+               scores, payload, workspace, workspace_bytes, stream=None, status=None):
     ln = np.ascontiguousarray(lengths, dtype=np.int64)
     return _check(lib().kvo_select(_ptr(keys), unit_stride, _ptr(cache_slots), ln.ctypes.data,
                                    n_units, n_pos, k, _ptr(queries), _ptr(tokens), _ptr(scores),
-                                   _ptr(payload), _ptr(workspace), workspace_bytes,
+                                   _ptr(payload), _ptr(workspace), workspace_bytes, _ptr(status),
                                    _stream(stream)))
 
 
 def kvo_select_noalloc(keys, unit_stride, cache_slots, lengths, n_units, n_pos, k, queries,
-                       tokens, scores, payload, stream=None):
-    """kvo_select without a workspace (fixed scratch inside the library; allocates nothing)."""
+                       tokens, scores, payload, stream=None, status=None):
+    """kvo_select without a workspace (fixed scratch inside the library; allocates nothing).
+    status: optional device uint32 tensor of one element that receives the kernels'
+    completion word (0 = the outputs are valid)."""
     ln = np.ascontiguousarray(lengths, dtype=np.int64)
     return _check(lib().kvo_select_noalloc(_ptr(keys), unit_stride, _ptr(cache_slots),
                                            ln.ctypes.data, n_units, n_pos, k, _ptr(queries),
                                            _ptr(tokens), _ptr(scores), _ptr(payload),
-                                           _stream(stream)))
+                                           _ptr(status), _stream(stream)))
 
 
 def kvo_reset(h, units, n_units, keep_tokens, stream=None):
