@@ -136,7 +136,9 @@ typedef struct kvo_stats {
                                    some units with the select, residency and miss-row fill of
                                    others; 0: one launch per stage; 2 (default): per call, the
                                    fused launch when the configuration fits its layout,
-                                   hot_capacity <= 65536 and the miss rows of the previous step
+                                   hot_capacity <= 65536, the pinned pool is at most 16 GiB
+                                   (the staged gather's fixed unit-to-CTA order reads a larger
+                                   pool faster) and the miss rows of the previous step
                                    amount to at least 1.5% of the indexer key bytes (the staged
                                    step wins when few rows move or the LRU lists are long), else
                                    the staged one.  Both give identical results.  When the

@@ -36,6 +36,7 @@ struct kvo_handle {
   int32_t max_blocks = 0;             // block-table entries per unit
   int32_t* blocks = nullptr;          // [U][max_blocks] block tables (device), -1 = unmapped
   size_t pool_map_bytes = 0;          // always 0: cudaHostAlloc memory
+  size_t pool_bytes = 0;              // size of the pinned pool
   size_t pool_huge_page = 0;
   uint16_t* idx = nullptr;           // bf16 indexer [U][stride][128]
   int8_t* idx8 = nullptr;            // int8 indexer codes [U][stride][128]
@@ -209,6 +210,12 @@ cudaError_t alloc_host_pool(kvo_handle* h, size_t bytes) {
 
 // Largest hot capacity for which kvo_step takes the fused path by default.
 constexpr int kFusedDefaultMaxCapacity = 65536;
+// Largest pinned pool for which kvo_step takes the fused path by default.  The fused
+// fill hands out rows in chunks from a counter, so its CTAs read rows of many units at
+// once and in a different order every step; from a large pool such reads wait for address
+// translations (measured on a 38.7 GB pool: 89-107 GB/s), while the staged gather, whose
+// CTAs keep the same units from step to step, moves the same rows at 203-208 GB/s.
+constexpr size_t kFusedDefaultMaxPoolBytes = (size_t)16 << 30;
 
 // Whether the fused step's shared-memory layout holds this configuration:
 // the finisher's select and residency reuse the candidate buffers.
@@ -381,6 +388,7 @@ bool use_fused(kvo_handle* h, const int32_t* units, int32_t n_units) {
   if (h->fused == 0 || !h->fused_ok) return false;
   if (h->fused == 1) return true;
   if (h->C > kFusedDefaultMaxCapacity) return false;
+  if (h->pool_bytes > kFusedDefaultMaxPoolBytes) return false;
   if (h->planned_steps < 2 || !h->bytes_prev_host) return true;
   int64_t T = 0;
   for (int32_t i = 0; i < n_units; ++i) T += h->len_host[(size_t)(units ? units[i] : i)];
@@ -595,7 +603,8 @@ int kvo_create(const kvo_config* cfg, kvo_handle** out) {
     h->n_blocks = c.host_blocks > 0 ? c.host_blocks : (int64_t)U * h->max_blocks;
     pool_rows = (size_t)h->n_blocks * (size_t)h->block_tokens;
   }
-  cudaError_t e = alloc_host_pool(h, pool_rows * h->R * 2);
+  h->pool_bytes = pool_rows * h->R * 2;
+  cudaError_t e = alloc_host_pool(h, h->pool_bytes);
   if (e != cudaSuccess) {
     cudaGetLastError();  // the failed allocation is not left as this thread's last CUDA error
     delete h;
