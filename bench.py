@@ -179,6 +179,7 @@ KERNEL_SOURCES = {
     "fused": ["kvo_fused.cu", "kvo_fused_i8.cu", "kvo_fused.cuh", "kvo_device.cuh", "kvo_internal.cuh"],
     "score": ["kvo_select.cu", "kvo_device.cuh", "kvo_internal.cuh"],
     "append": ["kvo_residency.cu", "kvo_device.cuh", "kvo_internal.cuh"],
+    "gather": ["kvo_residency.cu", "kvo_device.cuh", "kvo_internal.cuh"],
     "attend": ["kvo_attend.cu", "kvo_internal.cuh"],
 }
 

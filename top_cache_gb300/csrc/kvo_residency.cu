@@ -98,8 +98,13 @@ __global__ void __launch_bounds__(kGatherThreads) gather_ldg_kernel(GatherArgs a
   // in any order that changes between steps, the translations of a 38.7 GB pool are
   // missed again each step and the same copy runs at half the rate (probe: 208 GB/s with
   // a fixed unit-to-CTA assignment, 89-107 GB/s with rows or units claimed dynamically).
-  for (int i = blockIdx.x; i < a.n; i += gridDim.x)
-  for (int64_t b0 = a.miss_off[i]; b0 < a.miss_off[i + 1]; b0 += kGatherRows) {
+  // With fewer units than CTAs, each unit gets k = grid / n CTAs, which take its batches
+  // in turn (again the same CTAs for the same unit in every step).
+  const int k = a.n >= (int)gridDim.x || a.n <= 0 ? 1 : (int)gridDim.x / a.n;
+  const int first = k == 1 ? (int)blockIdx.x : (int)blockIdx.x / k, sub = k == 1 ? 0 : (int)blockIdx.x % k;
+  const int ustep = k == 1 ? (int)gridDim.x : a.n;
+  for (int i = first; i < a.n; i += ustep)
+  for (int64_t b0 = a.miss_off[i] + (int64_t)sub * kGatherRows; b0 < a.miss_off[i + 1]; b0 += (int64_t)k * kGatherRows) {
     const int64_t R_i = a.miss_off[i + 1];
     const int nrow = (int)((R_i - b0) < kGatherRows ? (R_i - b0) : kGatherRows);
     if (tid < nrow) {
