@@ -173,6 +173,15 @@ def gpu_numa_node(index):
         return None
 
 
+# Kernels bracketed with CUDA events inside the timed region: those a roofline is reported for.
+TIMED_KINDS = ("score", "gather", "fused")
+
+
+def _kinds_mask(names):
+    from top_cache_gb300 import kvo as K
+    return sum(1 << K.PROF_KINDS.index(n) for n in names)
+
+
 # The sources each timed kernel is compiled from (its translation unit and every header it
 # includes): a committed traffic figure stands only while their hash is the one it was taken at.
 KERNEL_SOURCES = {
@@ -552,7 +561,11 @@ def run_layerwise(args, link, device, torch, log):
         huge_frac = huge_backed_fraction(lw.host_rows_ptr(0))
         pool_numa = numa_spread(lw.host_rows_ptr(0))
         log("layerwise set-up %.1f s (host pool %.2f GB)" % (time.time() - t0, N * T * row * 2 / 1e9))
-        one_pass(L0)  # warm-up pass
+        # two warm-up passes over the same prefix (the first timed pass after a single one
+        # has been seen to take up to ten times the others, once per process)
+        for _ in range(2):
+            lw.set_length(L0)
+            one_pass(L0)
         torch.cuda.synchronize(device)
         st0 = lw.stats()
         ev = [torch.cuda.Event(enable_timing=True) for _ in range(n_pass + 1)]
@@ -614,8 +627,13 @@ def run_kvo(args, log):
     kv, inp, units = prepare(wl, rank, device, log, args.idx, args.host_block_tokens)
     U, P, k, R = len(units), wl.n_pos, wl.topk, wl.row_elems
     kv.set_option(K.KVO_OPT_GATHER_MODE, K.KVO_GATHER_BULK if args.gather == "bulk" else K.KVO_GATHER_LDG)
-    kv.set_option(K.KVO_OPT_GROUPS, args.groups)
-    kv.set_option(K.KVO_OPT_SCORE_CTAS, args.score_ctas)
+    # options left unset keep the library's per-call choice
+    if args.groups is not None:
+        kv.set_option(K.KVO_OPT_GROUPS, args.groups)
+    if args.score_ctas:
+        kv.set_option(K.KVO_OPT_SCORE_CTAS, args.score_ctas)
+    if args.group_gather_sms is not None:
+        kv.set_option(K.KVO_OPT_GROUP_GATHER_SMS, args.group_gather_sms)
     if args.speculate is not None:
         kv.set_option(K.KVO_OPT_SPECULATE, args.speculate)
     if args.path != "auto":
@@ -639,6 +657,10 @@ def run_kvo(args, log):
         seq.step()
     torch.cuda.synchronize(device)
     kv.profile_read()
+    # in the timed region only the kernels a roofline is reported for are bracketed with
+    # events (each pair adds a few microseconds between launches); the small kernels'
+    # times come from a replay of the same positions afterwards
+    kv.set_option(K.KVO_OPT_PROFILE_KINDS, _kinds_mask(TIMED_KINDS))
     kv.set_option(K.KVO_OPT_PROFILE, 1)
     st0 = kv.stats()
 
@@ -668,6 +690,24 @@ def run_kvo(args, log):
     sampler.stop()
     clocks = sampler.summary(t_wall0, t_wall1)
 
+    # replay of the timed positions with every launch bracketed (the small kernels' times)
+    kv.reset(wl.context)
+    seq = Sequence(kv, inp, wl)
+    for _ in range(args.warmup):
+        seq.step()
+    torch.cuda.synchronize(device)
+    kv.profile_read()
+    kv.set_option(K.KVO_OPT_PROFILE_KINDS, (1 << len(K.PROF_KINDS)) - 1)
+    kv.set_option(K.KVO_OPT_PROFILE, 1)
+    for _ in range(args.steps):
+        seq.step()
+    torch.cuda.synchronize(device)
+    prof_all = kv.profile_read()
+    kv.set_option(K.KVO_OPT_PROFILE, 0)
+    for name, (ms, n) in prof_all.items():
+        if name not in TIMED_KINDS and n:
+            prof[name] = (ms, n)
+
     # the cold step on its own: every unit back at its prefilled context with an empty
     # shelf, then step 0 of the sequence (every selected row a miss), three times
     cold_ms = []
@@ -684,6 +724,11 @@ def run_kvo(args, log):
 
     fused_frac = (st1["fused_steps"] - st0["fused_steps"]) / args.steps
     path = "fused" if fused_frac == 1 else "staged" if fused_frac == 0 else "mixed (%.0f%% fused)" % (100 * fused_frac)
+    split_frac = (st1["split_steps"] - st0["split_steps"]) / args.steps
+    if split_frac == 1:
+        path = "staged, two unit groups (the first group's rows copied inside the second's score launch)"
+    elif split_frac > 0:
+        path += " (%.0f%% in split unit groups)" % (100 * split_frac)
     max_ms = reduce_max(total_ms, world, device)
     value = whole_job_rate(U, args.steps, max_ms, world)
 
@@ -699,21 +744,35 @@ def run_kvo(args, log):
         if n == 0:
             continue
         kernels[name] = {"launches": n, "ms_total": round(ms, 4), "ms_per_launch": round(ms / n, 5),
-                         "share": round(ms / max(1e-9, sum(v[0] for v in prof.values())), 4)}
-    # per-launch bytes: each step's share (a step runs either the staged or the
-    # fused launches; with the per-call choice both can appear in one run)
+                         "share": round(ms / max(1e-9, sum(v[0] for v in prof.values())), 4),
+                         "timed": "in the timed region" if name in TIMED_KINDS
+                                  else "replay of the timed positions"}
+    # per-launch bytes: a step runs either the staged or the fused launches (with the
+    # per-call choice both can appear in one run), and a staged step in unit groups runs
+    # one score and one gather launch per group, each over its own units: the bytes of
+    # all staged steps divided by their launches
     score_step = score_bytes / args.steps
     rows_step = bytes_h2d / args.steps
-    if "score" in kernels:
-        sb = score_step * prof["score"][1]
+    n_fused = prof["fused"][1] if "fused" in prof else 0
+    staged_steps = args.steps - n_fused
+    if "score" in kernels and staged_steps:
+        sb = score_step * staged_steps
         a = sb / (prof["score"][0] / 1e3) / 1e9
-        kernels["score"].update(bound="hbm", bytes_per_launch=score_step,
+        if st1["rows_h2d_in_score"] > st0["rows_h2d_in_score"]:
+            kernels["score"]["note"] = ("%.0f MB of miss rows per step copied by the first CTAs of "
+                                        "the second group's score launch"
+                                        % ((st1["rows_h2d_in_score"] - st0["rows_h2d_in_score"])
+                                           * R * 2 / args.steps / 1e6))
+        kernels["score"].update(bound="hbm", bytes_per_launch=sb / prof["score"][1],
                                 achieved_gbs=round(a, 1), peak_gbs=hbm_peak,
                                 frac=round(a / hbm_peak, 4), peak_source=hbm_src)
-    if "gather" in kernels and bytes_h2d:
-        gb = rows_step * prof["gather"][1]
+    # rows copied by the first CTAs of a score launch (staged step in unit groups) are
+    # not the gather launches' bytes
+    carried_b = (st1["rows_h2d_in_score"] - st0["rows_h2d_in_score"]) * R * 2
+    if "gather" in kernels and bytes_h2d - carried_b > 0 and staged_steps:
+        gb = (bytes_h2d - carried_b) / args.steps * staged_steps
         a = gb / (prof["gather"][0] / 1e3) / 1e9
-        kernels["gather"].update(bound="host-link", bytes_per_launch=rows_step,
+        kernels["gather"].update(bound="host-link", bytes_per_launch=gb / prof["gather"][1],
                                  achieved_gbs=round(a, 1), peak_gbs=round(link["h2d"], 1),
                                  frac=round(a / link["h2d"], 4),
                                  peak_source="measured pinned host->device copy, this run")
@@ -779,7 +838,7 @@ def run_kvo(args, log):
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         cpu = run_cpu_baseline(wl, args.cpu_units, min(args.cpu_steps, wl.steps), log)
 
-    launches = sum(v[1] for v in prof.values())
+    launches = st1["launches"] - st0["launches"]
     line = {
         "metric": METRIC, "value": round(value, 1), "unit": UNIT, "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(max_ms / args.steps, 4),
@@ -796,7 +855,7 @@ def run_kvo(args, log):
                        kv.host_block(0) if args.host_block_tokens else kv.host_rows(0)),
                    "gpu_numa_node": gpu_numa_node(device.index if device.index is not None else 0),
                    "host_block_tokens": args.host_block_tokens or None,
-                   "gather": "bulk" if path == "fused" else args.gather, "groups": args.groups,
+                   "gather": "bulk" if path == "fused" else args.gather, "groups": args.groups if args.groups is not None else "per call",
                    "parallelism": "replicas%d" % world,
                    "l2": "inputs larger than L2: %.2f GB of indexer keys read per step"
                          % (score_bytes / n_steps / 1e9)},
@@ -812,7 +871,9 @@ def run_kvo(args, log):
         "steps_ms": {"median": round(statistics.median(step_ms), 4),
                      "p90": round(sorted(step_ms)[int(0.9 * (len(step_ms) - 1))], 4),
                      "warm_median": round(statistics.median(warm), 4) if warm else None,
-                     "cold_median": round(statistics.median(cold), 4) if cold else None,
+                     # the cold step: from the timed loop when it covered position 0, else
+                     # the step 0 timed on its own after it
+                     "cold_median": round(statistics.median(cold if cold else cold_ms), 4),
                      "cold_step_alone_ms": round(statistics.median(cold_ms), 4),
                      "p99": round(sorted(step_ms)[int(0.99 * (len(step_ms) - 1))], 4),
                      "max": round(max(step_ms), 4),
@@ -1037,9 +1098,11 @@ def main(argv=None):
     ap.add_argument("--drift", type=float, default=None,
                     help="query drift a of the workload (the sweep workload's points: 0, .5, .9, .99, 1)")
     ap.add_argument("--gather", choices=("ldg", "bulk"), default="ldg")
-    ap.add_argument("--groups", type=int, default=1,
+    ap.add_argument("--groups", type=int, default=None,
                     help="unit groups per step; miss-row copies overlap the next group's scoring")
     ap.add_argument("--score-ctas", type=int, default=0, help="cap on scoring CTAs (0 = one per SM)")
+    ap.add_argument("--group-gather-sms", type=int, default=None,
+                    help="staged step in unit groups: CTAs of each score launch that copy the previous group's rows")
     ap.add_argument("--path", choices=("auto", "fused", "staged"), default="auto",
                     help="fused: one cooperative launch per step; staged: one launch per stage; "
                          "auto: the library's default for the configuration")

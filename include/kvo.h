@@ -119,6 +119,11 @@ typedef struct kvo_stats {
   uint64_t block_errors;    /* paged pool: rows of unmapped blocks skipped by append or gather */
   uint64_t fetch_dup_bytes; /* deferred fill: host-pool bytes the attention kernel read for a row
                                part another CTA of the same call was still writing (read twice) */
+  uint64_t split_steps;     /* staged kvo_step calls in unit groups whose row copies ran inside
+                               the next group's score launch (KVO_OPT_GROUP_GATHER_SMS) */
+  uint64_t launches;        /* kernels launched by kvo_append, kvo_step, kvo_reset and kvo_attend */
+  uint64_t rows_h2d_in_score; /* of rows_h2d: rows copied by the first CTAs of a score launch
+                                 (KVO_OPT_GROUP_GATHER_SMS) */
 } kvo_stats;
 
 /* Options for kvo_set_option. */
@@ -141,7 +146,12 @@ typedef struct kvo_stats {
                                    pool faster) and the miss rows of the previous step
                                    amount to at least 1.5% of the indexer key bytes (the staged
                                    step wins when few rows move or the LRU lists are long), else
-                                   the staged one.  Both give identical results.  When the
+                                   the staged one; that staged step runs in two unit groups, the
+                                   first group's rows copied by some CTAs of the second group's
+                                   score launch (KVO_OPT_GROUP_GATHER_SMS, default 4/25 of the
+                                   SMs), when those rows amount to at least 1.5% of the key
+                                   bytes, the call lists at least 64 units and KVO_OPT_GROUPS has
+                                   not been set.  All give identical results.  When the
                                    configuration does not fit the fused layout the default is 0
                                    and setting 1 or 2 returns KVO_EINVAL.  The fused step moves
                                    miss rows with bulk async copies and ignores
@@ -163,6 +173,17 @@ typedef struct kvo_stats {
                                    list) completes the fill with a copy kernel on its stream.
                                    Requires row_elems == 576; the first 1 allocates 12 bytes per
                                    hot slot of claim words (synchronous).  Default 0 */
+#define KVO_OPT_GROUP_GATHER_SMS 12 /* staged step in unit groups: 0 copies each group's miss rows
+                                   on a library stream beside the next group's scoring; s in
+                                   1 .. SMs/2 makes the first s CTAs of group g+1's score launch
+                                   (one per SM) copy group g's rows while the others score, all
+                                   on the caller's stream (the last group's rows use every SM
+                                   after its residency update).  Default 0 with KVO_OPT_GROUPS
+                                   set by the caller, 4/25 of the SMs in the two-group step that
+                                   KVO_OPT_FUSED = 2 chooses */
+#define KVO_OPT_PROFILE_KINDS 13 /* with KVO_OPT_PROFILE 1: bit (1 << KVO_PROF_x) set brackets the
+                                   launches of kind x with events (default every kind); each
+                                   pair of events adds a few microseconds between launches */
 #define KVO_GATHER_LDG 0  /* miss rows read by 16-byte loads from the mapped host pool */
 #define KVO_GATHER_BULK 1 /* miss rows moved by bulk async copies through shared memory */
 

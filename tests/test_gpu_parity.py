@@ -134,6 +134,16 @@ def test_unit_groups_two_streams(groups, path):
     _run(wl, options={K.KVO_OPT_GROUPS: groups})
 
 
+@pytest.mark.parametrize("groups,sms", [(2, 8), (3, 32), (5, 2)])
+def test_unit_groups_split_sms(groups, sms, path):
+    _staged_only(path)
+    # the first `sms` CTAs of each group's score launch copy the previous group's rows
+    # while the others score (KVO_OPT_GROUP_GATHER_SMS): results as without groups
+    wl = W.reduced(W.WORKLOADS["batch16x8_32k_mtp3"], n_requests=3, n_layers=2, context=3001,
+                   topk=256, hot_capacity=600, steps=5)
+    _run(wl, options={K.KVO_OPT_GROUPS: groups, K.KVO_OPT_GROUP_GATHER_SMS: sms})
+
+
 def test_few_score_ctas_long_pieces(path):
     _staged_only(path)
     # a cap on scoring CTAs makes each CTA stream long pieces (many compactions)
@@ -391,6 +401,13 @@ def test_full_batch16x8_mtp3_grouped_sampled(path):
     _staged_only(path)
     wl = W.WORKLOADS["batch16x8_32k_mtp3"]
     _run(wl, steps=20, check_units=[0, 40, 127], count_rows=False, options={K.KVO_OPT_GROUPS: 4})
+
+
+def test_full_batch16x8_mtp3_split_sms_sampled(path):
+    _staged_only(path)
+    wl = W.WORKLOADS["batch16x8_32k_mtp3"]
+    _run(wl, steps=12, check_units=[1, 63, 126], count_rows=False,
+         options={K.KVO_OPT_GROUPS: 2, K.KVO_OPT_GROUP_GATHER_SMS: 32})
 
 
 def test_full_batch16x8_mtp3_int8_sampled():

@@ -86,6 +86,7 @@ struct kvo_handle {
   int fused = 2;                // KVO_OPT_FUSED mode: 0 staged, 1 fused, 2 per call
   int gather_ctas = 8;
   uint64_t fused_steps = 0;
+  uint64_t split_steps = 0;
   unsigned long long* bytes_prev_host = nullptr;  // pinned, mapped: previous step's miss bytes
   unsigned long long* bytes_prev_dev = nullptr;   // its device address
   unsigned long long* bytes_seen = nullptr;       // device
@@ -115,12 +116,16 @@ struct kvo_handle {
   uint32_t fetch_epoch = 0;
   // unit groups: miss-row copies overlap the next group's scoring
   int groups = 1;
+  int group_gather_sms = 0;     // KVO_OPT_GROUP_GATHER_SMS
+  bool groups_set = false, group_gather_sms_set = false;  // set by the caller (else chosen per call)
   int score_ctas = 0;
   cudaStream_t side = nullptr;
   cudaEvent_t ev_fork = nullptr, ev_join = nullptr;
   cudaEvent_t ev_group[16] = {};
   // opt-in launch profiling
   bool profile = false;
+  uint32_t profile_kinds = (1u << KVO_PROF_KINDS) - 1;  // KVO_OPT_PROFILE_KINDS
+  uint64_t launches = 0;  // kernels launched through timed()
   struct Rec {
     int kind;
     cudaEvent_t e0, e1;
@@ -317,7 +322,8 @@ cudaEvent_t take_event(kvo_handle* h) {
 // Runs one launch, bracketed by events when profiling is on.
 template <class F>
 cudaError_t timed(kvo_handle* h, int kind, cudaStream_t s, F launch) {
-  if (!h->profile) return launch();
+  ++h->launches;
+  if (!h->profile || !((h->profile_kinds >> kind) & 1u)) return launch();
   cudaEvent_t e0 = take_event(h), e1 = take_event(h);
   if (e0) cudaEventRecord(e0, s);
   cudaError_t e = launch();
@@ -389,6 +395,21 @@ bool use_fused(kvo_handle* h, const int32_t* units, int32_t n_units) {
   if (h->fused == 1) return true;
   if (h->C > kFusedDefaultMaxCapacity) return false;
   if (h->pool_bytes > kFusedDefaultMaxPoolBytes) return false;
+  if (h->planned_steps < 2 || !h->bytes_prev_host) return true;
+  int64_t T = 0;
+  for (int32_t i = 0; i < n_units; ++i) T += h->len_host[(size_t)(units ? units[i] : i)];
+  const unsigned long long rows = *reinterpret_cast<volatile unsigned long long*>(h->bytes_prev_host);
+  return (double)rows >= 0.015 * (double)T * kvo::kKeyBytes;
+}
+
+// Staged step of the per-call choice (mode 2): two unit groups, the first group's miss
+// rows copied by the first 4/25 of the CTAs of the second group's score launch (24 of 152,
+// one per SM) while its other CTAs score, when the previous step's rows were at least 1.5%
+// of the key bytes and the call lists enough units for two groups.  The copying CTAs keep
+// a fixed unit assignment and start with the launch, on the caller's stream.
+constexpr int kSplitMinUnits = 64;
+bool use_split(kvo_handle* h, const int32_t* units, int32_t n_units) {
+  if (h->fused != 2 || h->groups_set || h->defer_fill || n_units < kSplitMinUnits) return false;
   if (h->planned_steps < 2 || !h->bytes_prev_host) return true;
   int64_t T = 0;
   for (int32_t i = 0; i < n_units; ++i) T += h->len_host[(size_t)(units ? units[i] : i)];
@@ -864,10 +885,21 @@ int kvo_step(kvo_handle* h, const int32_t* units, int32_t n_units, const void* q
   }
   const int PK = h->P * h->k;
   int NG = h->groups < n_units ? h->groups : n_units;
+  int gsm = h->group_gather_sms;
+  if (use_split(h, units, n_units)) {
+    NG = 2;
+    if (!h->group_gather_sms_set) gsm = h->n_sm * 4 / 25 > 0 ? h->n_sm * 4 / 25 : 1;
+  }
   if (NG < 1) NG = 1;
   const int g_max = h->score_ctas > 0 && h->score_ctas < h->G_max ? h->score_ctas : h->G_max;
+  // split: the score launch of group g > 0 carries the copy of group g-1's rows in its
+  // first gsm CTAs (one stream); else each group's copy runs on the side stream
+  const bool split = NG > 1 && gsm > 0 && !h->defer_fill;
+  const bool side = NG > 1 && !split;
+  kvo::GatherArgs ga_prev{};
+  bool have_prev = false;
   cudaError_t e = cudaSuccess;
-  if (NG > 1) {
+  if (side) {
     e = cudaEventRecord(h->ev_fork, s);
     if (e == cudaSuccess) e = cudaStreamWaitEvent(h->side, h->ev_fork, 0);
   }
@@ -895,7 +927,13 @@ int kvo_step(kvo_handle* h, const int32_t* units, int32_t n_units, const void* q
     sa.k = h->k;
     sa.cap = h->cap;
     sa.T = T;
-    sa.G = grid_for(T, g_max);
+    const bool carry = split && have_prev;  // this launch also copies the previous group's rows
+    sa.G = grid_for(T, carry && g_max > h->n_sm - gsm ? h->n_sm - gsm : g_max);
+    if (carry) {
+      sa.gather_ctas = gsm;
+      sa.prev = ga_prev;
+      have_prev = false;
+    }
     sa.off = h->off;
     sa.gthr = h->gthr;
     sa.seg_keys = h->seg_keys;
@@ -931,6 +969,7 @@ int kvo_step(kvo_handle* h, const int32_t* units, int32_t n_units, const void* q
       // units whose speculative threshold was too high are rescored exactly
       kvo::SelectArgs fa = sa;
       fa.fallback = 1;
+      fa.gather_ctas = 0;
       if (e == cudaSuccess) e = timed(h, KVO_PROF_RESCORE, s, [&] { return kvo::launch_score(fa, s); });
       if (e == cudaSuccess) e = timed(h, KVO_PROF_RESELECT, s, [&] { return kvo::launch_select(fa, s); });
     }
@@ -984,7 +1023,10 @@ int kvo_step(kvo_handle* h, const int32_t* units, int32_t n_units, const void* q
     ga.wait_ns = h->wait_ns;
     if (h->defer_fill) {
       // the rows are left for the attention call (or the next call's flush)
-    } else if (NG > 1) {
+    } else if (split && en < n_units) {
+      ga_prev = ga;  // copied by the next group's score launch
+      have_prev = true;
+    } else if (side) {
       if (e == cudaSuccess) e = cudaEventRecord(h->ev_group[g], s);
       if (e == cudaSuccess) e = cudaStreamWaitEvent(h->side, h->ev_group[g], 0);
       if (e == cudaSuccess)
@@ -993,13 +1035,14 @@ int kvo_step(kvo_handle* h, const int32_t* units, int32_t n_units, const void* q
       e = timed(h, KVO_PROF_GATHER, s, [&] { return kvo::launch_gather(ga, h->n_sm, s); });
     }
   }
-  if (NG > 1 && e == cudaSuccess) {
+  if (side && e == cudaSuccess) {
     e = cudaEventRecord(h->ev_join, h->side);
     if (e == cudaSuccess) e = cudaStreamWaitEvent(s, h->ev_join, 0);
   }
   if (e != cudaSuccess) return cuda_fail(e, "step launch");
   ++h->host_steps;
   ++h->planned_steps;
+  if (split) ++h->split_steps;
   if (h->defer_fill) set_pending(h, units, n_units, du);
   return KVO_OK;
 }
@@ -1098,9 +1141,19 @@ int kvo_set_option(kvo_handle* h, int32_t key, int64_t value) {
       if (value != 0 && value != 1) return fail(KVO_EINVAL, "profile is 0 or 1");
       h->profile = value == 1;
       return KVO_OK;
+    case KVO_OPT_PROFILE_KINDS:
+      if (value < 1 || value >= (1 << KVO_PROF_KINDS)) return fail(KVO_EINVAL, "profile kinds: a non-empty mask of KVO_PROF_*");
+      h->profile_kinds = (uint32_t)value;
+      return KVO_OK;
     case KVO_OPT_GROUPS:
       if (value < 1 || value > 16) return fail(KVO_EINVAL, "groups must be in [1, 16]");
       h->groups = (int)value;
+      h->groups_set = true;
+      return KVO_OK;
+    case KVO_OPT_GROUP_GATHER_SMS:
+      if (value < 0 || value > h->n_sm / 2) return fail(KVO_EINVAL, "group_gather_sms must be in [0, SMs/2]");
+      h->group_gather_sms = (int)value;
+      h->group_gather_sms_set = true;
       return KVO_OK;
     case KVO_OPT_SCORE_CTAS:
       if (value < 0 || value > 1 << 20) return fail(KVO_EINVAL, "score_ctas out of range");
@@ -1169,7 +1222,9 @@ int kvo_get_option(kvo_handle* h, int32_t key, int64_t* value) {
     case KVO_OPT_GATHER_MODE: *value = h->gather_mode; return KVO_OK;
     case KVO_OPT_WAIT_LIMIT_NS: *value = (int64_t)h->wait_ns; return KVO_OK;
     case KVO_OPT_PROFILE: *value = h->profile ? 1 : 0; return KVO_OK;
+    case KVO_OPT_PROFILE_KINDS: *value = h->profile_kinds; return KVO_OK;
     case KVO_OPT_GROUPS: *value = h->groups; return KVO_OK;
+    case KVO_OPT_GROUP_GATHER_SMS: *value = h->group_gather_sms; return KVO_OK;
     case KVO_OPT_SCORE_CTAS: *value = h->score_ctas; return KVO_OK;
     case KVO_OPT_SPECULATE: *value = h->speculate; return KVO_OK;
     case KVO_OPT_FUSED: *value = h->fused; return KVO_OK;
@@ -1334,6 +1389,9 @@ int kvo_get_stats(kvo_handle* h, kvo_stats* out) {
   out->fused_steps = h->fused_steps;
   out->block_errors = d.block_errors;
   out->fetch_dup_bytes = d.fetch_dup_bytes;
+  out->split_steps = h->split_steps;
+  out->launches = h->launches;
+  out->rows_h2d_in_score = d.rows_h2d_in_score;
   return KVO_OK;
 }
 

@@ -32,6 +32,7 @@ constexpr int kSelLog2B = 11;               // buckets of the select kernel's bu
 constexpr int kSelMaxSegs = 512;            // segments whose offsets the select kernel holds
 constexpr int kSelSmemBytes = 104 * 1024;   // two CTAs per SM
 constexpr int kMaxK = 4096;
+constexpr int kScoreGatherRows = 90;        // rows per batch of a score launch's copying CTAs (x 72 chunks <= 12 x 544)
 
 __device__ __forceinline__ void consumer_sync() { named_sync(1, kCT); }
 
@@ -743,6 +744,86 @@ __device__ __forceinline__ void issue_tile(const SelectArgs& a, uint8_t* stage, 
     bulk_g2s_hint(stage, a.keys + row * kDim, bytes, full, pol);
   }
 }
+
+// ---------------------------------------------------------------------------
+// Miss-row copy by 16-byte loads from the mapped host pool (zero copy): CTA
+// `cta` of `ncta` CTAs (NT threads each) moves batches of ROWS rows of one unit,
+// each thread with up to U loads in flight.  Used by the gather kernel (every
+// CTA of its launch) and by the first CTAs of a score launch of a staged step
+// in unit groups (the previous group's rows).
+// ---------------------------------------------------------------------------
+template <int NT, int ROWS, int U>
+__device__ __forceinline__ void gather_rows_ldg(const GatherArgs& a, int cta, int ncta, bool in_score = false) {
+  static_assert(ROWS <= NT, "one thread per row of a batch fetches its addresses");
+  __shared__ int64_t src_off[ROWS];
+  __shared__ int64_t dst_off[ROWS];
+  __shared__ unsigned int bad;  // rows of unmapped blocks (paged pool), left as they were
+  const int tid = threadIdx.x;
+  const int cpr = a.row_elems / 8;  // 16-byte chunks per row
+  int64_t moved = 0;
+  if (tid == 0) bad = 0;
+  __syncthreads();
+  // Units are assigned to CTAs by their place in the list (i, i + ncta, ...), the same
+  // in every step: the rows one CTA reads then stay in the same few units' regions of the
+  // pool from step to step, and the GPU keeps those regions' address translations.  Taken
+  // in any order that changes between steps, the translations of a 38.7 GB pool are
+  // missed again each step and the same copy runs at half the rate (probe: 208 GB/s with
+  // a fixed unit-to-CTA assignment, 89-107 GB/s with rows or units claimed dynamically).
+  // With fewer units than CTAs, each unit gets k = ncta / n CTAs, which take its batches
+  // in turn (again the same CTAs for the same unit in every step).
+  const int k = a.n >= ncta || a.n <= 0 ? 1 : ncta / a.n;
+  const int first = k == 1 ? cta : cta / k, sub = k == 1 ? 0 : cta % k;
+  const int ustep = k == 1 ? ncta : a.n;
+  for (int i = first; i < a.n; i += ustep)
+  for (int64_t b0 = a.miss_off[i] + (int64_t)sub * ROWS; b0 < a.miss_off[i + 1]; b0 += (int64_t)k * ROWS) {
+    const int64_t R_i = a.miss_off[i + 1];
+    const int nrow = (int)((R_i - b0) < ROWS ? (R_i - b0) : ROWS);
+    if (tid < nrow) {
+      const int64_t loc = b0 + tid - a.miss_off[i];
+      const int u = a.units[i];
+      const int32_t t = a.miss_tok[(int64_t)i * a.pk + loc];
+      const int32_t s = a.miss_slot[(int64_t)i * a.pk + loc];
+      const int64_t hr = host_row(a.rows, u, t);
+      src_off[tid] = hr < 0 ? -1 : hr * a.row_elems;
+      dst_off[tid] = ((int64_t)u * a.C + s) * a.row_elems;
+      if (hr < 0) atomicAdd(&bad, 1u);
+    }
+    __syncthreads();
+    const int total = nrow * cpr;
+    for (int q0 = tid; q0 < total; q0 += NT * U) {
+      uint4 v[U];
+#pragma unroll
+      for (int x = 0; x < U; ++x) {
+        const int q = q0 + x * NT;
+        if (q < total) {
+          const int row = q / cpr, c = q - row * cpr;
+          if (src_off[row] >= 0) v[x] = *reinterpret_cast<const uint4*>(a.host_pool + src_off[row] + c * 8);
+        }
+      }
+#pragma unroll
+      for (int x = 0; x < U; ++x) {
+        const int q = q0 + x * NT;
+        if (q < total) {
+          const int row = q / cpr, c = q - row * cpr;
+          if (src_off[row] >= 0) *reinterpret_cast<uint4*>(a.hot + dst_off[row] + c * 8) = v[x];
+        }
+      }
+    }
+    moved += nrow;
+    __syncthreads();
+  }
+  __syncthreads();
+  if (tid == 0 && a.stats) {
+    moved -= bad;
+    if (moved) {
+      atomicAdd(&a.stats->rows_h2d, (unsigned long long)moved);
+      atomicAdd(&a.stats->bytes_h2d, (unsigned long long)moved * a.row_elems * 2ull);
+      if (in_score) atomicAdd(&a.stats->rows_h2d_in_score, (unsigned long long)moved);
+    }
+    if (bad) atomicAdd(&a.stats->block_errors, (unsigned long long)bad);
+  }
+}
+
 
 template <int PP, class KF>
 struct ScorerFor {

@@ -19,7 +19,8 @@ constexpr uint32_t kErrPlan = 2u;
 // Device-side counters (mirrors kvo_stats).
 struct DevStats {
   unsigned long long steps, unit_steps, capacity_errors, hits, misses, rows_h2d, bytes_h2d,
-      rows_d2h, bytes_d2h, timeouts, rescored, block_errors, fetch_dup_bytes;
+      rows_d2h, bytes_d2h, timeouts, rescored, block_errors, fetch_dup_bytes,
+      rows_h2d_in_score;  // of rows_h2d: copied by the first CTAs of a score launch
 };
 
 // Host-pool row of token t of unit u: contiguous per unit (blocks == nullptr),
@@ -186,6 +187,23 @@ __device__ __forceinline__ int64_t cta_start(int c, int64_t T, int G) {
 // ---------------------------------------------------------------------------
 // Launch-side structures
 // ---------------------------------------------------------------------------
+struct GatherArgs {
+  const int32_t* units;
+  int32_t n, row_elems, C, mode;
+  int64_t stride;              // host pool rows per unit
+  HostRows rows;               // token -> host-pool row
+  const uint16_t* host_pool;   // device-visible address of the pinned pool
+  uint16_t* hot;               // [U][C][row_elems]
+  const int32_t* miss_tok;
+  const int32_t* miss_slot;
+  const int64_t* miss_off;     // [n+1]
+  const int32_t* miss_cnt;     // [n] (the deferred fill's flush)
+  int32_t pk;                  // stride of the miss lists
+  DevStats* stats;
+  uint32_t* err;
+  uint64_t wait_ns;
+};
+
 struct SelectArgs {
   const uint16_t* keys;        // bf16 [.][stride][128], unit id major (bf16 indexer)
   const int8_t* keys8;         // int8 [.][stride][128] codes (int8 indexer), else nullptr
@@ -200,6 +218,11 @@ struct SelectArgs {
   int32_t n, P, k, cap;        // cap: candidate buffer entries per position
   int64_t T;                   // total cached tokens of the listed units
   int32_t G;                   // score CTAs
+  // Separate score launch of a staged step in unit groups (0: none): the first
+  // gather_ctas CTAs of the launch copy the miss rows of the previous group
+  // (prev) instead of scoring; the G scoring CTAs follow them.
+  int32_t gather_ctas;
+  GatherArgs prev;
   int64_t* off;                // [n+1] flat offsets (scratch, written by plan)
   uint64_t* gthr;              // [n][P] shared lower bounds of each k-th best key (zeroed by plan)
   uint64_t* seg_keys;          // [(G+n)][P][k] candidates per segment
@@ -267,22 +290,6 @@ struct ResidencyArgs {
   int32_t U;
 };
 
-struct GatherArgs {
-  const int32_t* units;
-  int32_t n, row_elems, C, mode;
-  int64_t stride;              // host pool rows per unit
-  HostRows rows;               // token -> host-pool row
-  const uint16_t* host_pool;   // device-visible address of the pinned pool
-  uint16_t* hot;               // [U][C][row_elems]
-  const int32_t* miss_tok;
-  const int32_t* miss_slot;
-  const int64_t* miss_off;     // [n+1]
-  const int32_t* miss_cnt;     // [n] (the deferred fill's flush)
-  int32_t pk;                  // stride of the miss lists
-  DevStats* stats;
-  uint32_t* err;
-  uint64_t wait_ns;
-};
 
 // Sparse attention over the hot buffer (kvo_attend.cu).
 struct AttendArgs {

@@ -86,8 +86,15 @@ __global__ void __launch_bounds__(1024) plan_kernel(SelectArgs a) {
   plan_body<1024>(a, threadIdx.x, warp_sums, &carry);
 }
 
+// The copying CTAs' part of a score launch, a separate function so that its
+// registers (12 loads in flight per thread) do not constrain the scoring code's.
+__device__ __noinline__ void score_launch_copy(const GatherArgs& g, int cta, int ncta) {
+  gather_rows_ldg<kScoreThreads, kScoreGatherRows, 12>(g, cta, ncta, true);
+}
+
 // ---------------------------------------------------------------------------
-// score: one persistent CTA per flat piece of the token range.
+// score: one persistent CTA per flat piece of the token range (after the
+// CTAs, if any, that copy the previous unit group's miss rows).
 // ---------------------------------------------------------------------------
 template <int PP, class KF>
 __global__ void __launch_bounds__(kScoreThreads, 1) score_kernel(SelectArgs a) {
@@ -95,8 +102,13 @@ __global__ void __launch_bounds__(kScoreThreads, 1) score_kernel(SelectArgs a) {
   ScoreSmem sm;
   sm.carve<KF>(smem, a.P, a.cap);
 
+  if ((int)blockIdx.x < a.gather_ctas) {
+    // the previous unit group's miss rows, copied while this group is scored
+    score_launch_copy(a.prev, (int)blockIdx.x, a.gather_ctas);
+    return;
+  }
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int c = blockIdx.x;
+  const int c = (int)blockIdx.x - a.gather_ctas;
   if (a.fallback && *reinterpret_cast<volatile uint32_t*>(a.fb_any) == 0) return;
   const int64_t g0 = cta_start(c, a.T, a.G), g1 = cta_start(c + 1, a.T, a.G);
   const int32_t* only = a.fallback ? a.fb : nullptr;  // rescoring pass: flagged units only
@@ -259,7 +271,7 @@ static cudaError_t launch_score_pp(const SelectArgs& a, cudaStream_t s) {
   cudaError_t e = cudaFuncSetAttribute(score_kernel<PP, KF>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        (int)smem);
   if (e != cudaSuccess) return e;
-  score_kernel<PP, KF><<<a.G, kScoreThreads, smem, s>>>(a);
+  score_kernel<PP, KF><<<a.G + a.gather_ctas, kScoreThreads, smem, s>>>(a);
   return cudaGetLastError();
 }
 

@@ -36,6 +36,8 @@ KVO_OPT_GATHER_CTAS = 8
 KVO_OPT_PIECE_TOKENS = 9
 KVO_OPT_HOST_HUGE_PAGE = 10
 KVO_OPT_DEFER_FILL = 11
+KVO_OPT_GROUP_GATHER_SMS = 12
+KVO_OPT_PROFILE_KINDS = 13
 PROF_KINDS = ("append", "plan", "score", "select", "residency", "gather", "reset", "rescore",
               "reselect", "fused", "attend")
 KVO_IDX_BF16 = 0
@@ -71,7 +73,7 @@ class KvoStats(ctypes.Structure):
     _fields_ = [(n, ctypes.c_uint64) for n in
                 ("steps", "unit_steps", "capacity_errors", "hits", "misses", "rows_h2d",
                  "bytes_h2d", "rows_d2h", "bytes_d2h", "timeouts", "rescored", "fused_steps",
-                 "block_errors", "fetch_dup_bytes")]
+                 "block_errors", "fetch_dup_bytes", "split_steps", "launches", "rows_h2d_in_score")]
 
 
 class KvoError(RuntimeError):
