@@ -74,6 +74,7 @@ struct kvo_handle {
   int32_t* miss_tok = nullptr;
   int32_t* miss_slot = nullptr;
   int32_t* miss_cnt = nullptr;
+  int32_t* claim_batches = nullptr;  // [U] copy batches claimed per unit (staged step in unit groups)
   int64_t* miss_off = nullptr;
   uint32_t* done_ctr = nullptr;
   uint32_t* err = nullptr;
@@ -184,7 +185,7 @@ void free_all(kvo_handle* h) {
                  h->tspec, h->fb, h->fb_any, h->tok_bits, h->order, h->order_par, h->seg_keys, h->seg_cnt, h->sel_pay,
                  h->miss_tok, h->miss_slot, h->miss_cnt, h->miss_off, h->done_ctr, h->err,
                  h->stats, h->pbeg, h->pdone, h->ctr, h->plan_flag, h->fseg_keys, h->fseg_cnt, h->chunk_unit,
-                 h->chunk_start, h->chunk_cnt, h->chunk_flag, h->claim};
+                 h->chunk_start, h->chunk_cnt, h->chunk_flag, h->claim, h->claim_batches};
   for (void* p : dev)
     if (p) cudaFree(p);
   if (h->bytes_seen) cudaFree(h->bytes_seen);
@@ -674,6 +675,7 @@ int kvo_create(const kvo_config* cfg, kvo_handle** out) {
   if (e == cudaSuccess) e = dalloc(&h->miss_tok, U * PK);
   if (e == cudaSuccess) e = dalloc(&h->miss_slot, U * PK);
   if (e == cudaSuccess) e = dalloc(&h->miss_cnt, U);
+  if (e == cudaSuccess) e = dalloc(&h->claim_batches, U);
   if (e == cudaSuccess) e = dalloc(&h->miss_off, U + 16);
   if (e == cudaSuccess) e = dalloc(&h->done_ctr, 16);
   if (e == cudaSuccess) e = cudaStreamCreateWithFlags(&h->side, cudaStreamNonBlocking);
@@ -933,6 +935,8 @@ int kvo_step(kvo_handle* h, const int32_t* units, int32_t n_units, const void* q
       sa.gather_ctas = gsm;
       sa.prev = ga_prev;
       have_prev = false;
+      // the batch counters the copying and helping CTAs claim from start at zero
+      e = cudaMemsetAsync(ga_prev.claim, 0, (size_t)ga_prev.n * sizeof(int32_t), s);
     }
     sa.off = h->off;
     sa.gthr = h->gthr;
@@ -1025,6 +1029,7 @@ int kvo_step(kvo_handle* h, const int32_t* units, int32_t n_units, const void* q
       // the rows are left for the attention call (or the next call's flush)
     } else if (split && en < n_units) {
       ga_prev = ga;  // copied by the next group's score launch
+      ga_prev.claim = h->claim_batches + b;
       have_prev = true;
     } else if (side) {
       if (e == cudaSuccess) e = cudaEventRecord(h->ev_group[g], s);

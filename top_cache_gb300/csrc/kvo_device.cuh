@@ -746,74 +746,80 @@ __device__ __forceinline__ void issue_tile(const SelectArgs& a, uint8_t* stage, 
 }
 
 // ---------------------------------------------------------------------------
-// Miss-row copy by 16-byte loads from the mapped host pool (zero copy): CTA
-// `cta` of `ncta` CTAs (NT threads each) moves batches of ROWS rows of one unit,
-// each thread with up to U loads in flight.  Used by the gather kernel (every
-// CTA of its launch) and by the first CTAs of a score launch of a staged step
-// in unit groups (the previous group's rows).
+// Miss-row copy by 16-byte loads from the mapped host pool (zero copy), NT
+// threads per CTA, batches of up to ROWS rows of one unit, each thread with up
+// to U loads in flight.  Used by the gather kernel (every CTA of its launch)
+// and by a score launch of a staged step in unit groups (the previous group's
+// rows: its first CTAs copy them, its scoring CTAs help once they are done).
 // ---------------------------------------------------------------------------
-template <int NT, int ROWS, int U>
-__device__ __forceinline__ void gather_rows_ldg(const GatherArgs& a, int cta, int ncta, bool in_score = false) {
-  static_assert(ROWS <= NT, "one thread per row of a batch fetches its addresses");
-  __shared__ int64_t src_off[ROWS];
-  __shared__ int64_t dst_off[ROWS];
-  __shared__ unsigned int bad;  // rows of unmapped blocks (paged pool), left as they were
+struct CopyScratch {      // shared memory of a copying CTA
+  int64_t* src_off;       // [ROWS]
+  int64_t* dst_off;       // [ROWS]
+  int32_t* list;          // [NT] (helpers)
+  uint32_t* word;         // [4]: rows of unmapped blocks, claimed batch, list count
+};
+
+// Rows [b0, b0 + nrow) of unit i's miss list (all threads; ends with a barrier).
+template <int NT, int U>
+__device__ __forceinline__ void copy_batch(const GatherArgs& a, int i, int64_t b0, int nrow, const CopyScratch& cs) {
   const int tid = threadIdx.x;
   const int cpr = a.row_elems / 8;  // 16-byte chunks per row
-  int64_t moved = 0;
-  if (tid == 0) bad = 0;
-  __syncthreads();
-  // Units are assigned to CTAs by their place in the list (i, i + ncta, ...), the same
-  // in every step: the rows one CTA reads then stay in the same few units' regions of the
-  // pool from step to step, and the GPU keeps those regions' address translations.  Taken
-  // in any order that changes between steps, the translations of a 38.7 GB pool are
-  // missed again each step and the same copy runs at half the rate (probe: 208 GB/s with
-  // a fixed unit-to-CTA assignment, 89-107 GB/s with rows or units claimed dynamically).
-  // With fewer units than CTAs, each unit gets k = ncta / n CTAs, which take its batches
-  // in turn (again the same CTAs for the same unit in every step).
-  const int k = a.n >= ncta || a.n <= 0 ? 1 : ncta / a.n;
-  const int first = k == 1 ? cta : cta / k, sub = k == 1 ? 0 : cta % k;
-  const int ustep = k == 1 ? ncta : a.n;
-  for (int i = first; i < a.n; i += ustep)
-  for (int64_t b0 = a.miss_off[i] + (int64_t)sub * ROWS; b0 < a.miss_off[i + 1]; b0 += (int64_t)k * ROWS) {
-    const int64_t R_i = a.miss_off[i + 1];
-    const int nrow = (int)((R_i - b0) < ROWS ? (R_i - b0) : ROWS);
-    if (tid < nrow) {
-      const int64_t loc = b0 + tid - a.miss_off[i];
-      const int u = a.units[i];
-      const int32_t t = a.miss_tok[(int64_t)i * a.pk + loc];
-      const int32_t s = a.miss_slot[(int64_t)i * a.pk + loc];
-      const int64_t hr = host_row(a.rows, u, t);
-      src_off[tid] = hr < 0 ? -1 : hr * a.row_elems;
-      dst_off[tid] = ((int64_t)u * a.C + s) * a.row_elems;
-      if (hr < 0) atomicAdd(&bad, 1u);
-    }
-    __syncthreads();
-    const int total = nrow * cpr;
-    for (int q0 = tid; q0 < total; q0 += NT * U) {
-      uint4 v[U];
-#pragma unroll
-      for (int x = 0; x < U; ++x) {
-        const int q = q0 + x * NT;
-        if (q < total) {
-          const int row = q / cpr, c = q - row * cpr;
-          if (src_off[row] >= 0) v[x] = *reinterpret_cast<const uint4*>(a.host_pool + src_off[row] + c * 8);
-        }
-      }
-#pragma unroll
-      for (int x = 0; x < U; ++x) {
-        const int q = q0 + x * NT;
-        if (q < total) {
-          const int row = q / cpr, c = q - row * cpr;
-          if (src_off[row] >= 0) *reinterpret_cast<uint4*>(a.hot + dst_off[row] + c * 8) = v[x];
-        }
-      }
-    }
-    moved += nrow;
-    __syncthreads();
+  if (tid < nrow) {
+    const int64_t loc = b0 + tid - a.miss_off[i];
+    const int u = a.units[i];
+    const int32_t t = a.miss_tok[(int64_t)i * a.pk + loc];
+    const int32_t s = a.miss_slot[(int64_t)i * a.pk + loc];
+    const int64_t hr = host_row(a.rows, u, t);
+    cs.src_off[tid] = hr < 0 ? -1 : hr * a.row_elems;
+    cs.dst_off[tid] = ((int64_t)u * a.C + s) * a.row_elems;
+    if (hr < 0) atomicAdd(&cs.word[0], 1u);
   }
   __syncthreads();
-  if (tid == 0 && a.stats) {
+  const int total = nrow * cpr;
+  for (int q0 = tid; q0 < total; q0 += NT * U) {
+    uint4 v[U];
+#pragma unroll
+    for (int x = 0; x < U; ++x) {
+      const int q = q0 + x * NT;
+      if (q < total) {
+        const int row = q / cpr, c = q - row * cpr;
+        if (cs.src_off[row] >= 0) v[x] = *reinterpret_cast<const uint4*>(a.host_pool + cs.src_off[row] + c * 8);
+      }
+    }
+#pragma unroll
+    for (int x = 0; x < U; ++x) {
+      const int q = q0 + x * NT;
+      if (q < total) {
+        const int row = q / cpr, c = q - row * cpr;
+        if (cs.src_off[row] >= 0) *reinterpret_cast<uint4*>(a.hot + cs.dst_off[row] + c * 8) = v[x];
+      }
+    }
+  }
+  __syncthreads();
+}
+
+// Unit i's batches taken one at a time from its claim counter (shared with the
+// other CTAs that copy or help); returns the rows this CTA copied.
+template <int NT, int ROWS, int U>
+__device__ __forceinline__ int64_t copy_claimed(const GatherArgs& a, int i, const CopyScratch& cs) {
+  const int64_t r0 = a.miss_off[i], r1 = a.miss_off[i + 1];
+  int64_t moved = 0;
+  for (;;) {
+    if (threadIdx.x == 0) cs.word[1] = (uint32_t)atomicAdd(&a.claim[i], 1);
+    __syncthreads();
+    const int64_t b0 = r0 + (int64_t)cs.word[1] * ROWS;
+    __syncthreads();  // every thread has read the claim before the next one is written
+    if (b0 >= r1) return moved;
+    const int nrow = (int)((r1 - b0) < ROWS ? (r1 - b0) : ROWS);
+    copy_batch<NT, U>(a, i, b0, nrow, cs);
+    moved += nrow;
+  }
+}
+
+// Adds a CTA's copied rows to the statistics (thread 0, after a barrier).
+__device__ __forceinline__ void copy_stats(const GatherArgs& a, int64_t moved, const CopyScratch& cs, bool in_score) {
+  if (threadIdx.x == 0 && a.stats) {
+    const uint32_t bad = cs.word[0];
     moved -= bad;
     if (moved) {
       atomicAdd(&a.stats->rows_h2d, (unsigned long long)moved);
@@ -824,6 +830,66 @@ __device__ __forceinline__ void gather_rows_ldg(const GatherArgs& a, int cta, in
   }
 }
 
+// CTA `cta` of `ncta` copying CTAs.  Units are assigned to CTAs by their place in the
+// list (i, i + ncta, ...), the same in every step: the rows one CTA reads then stay in the
+// same few units' regions of the pool from step to step, and the GPU keeps those regions'
+// address translations.  Taken in any order that changes between steps, the translations
+// of a 38.7 GB pool are missed again each step and the same copy runs at half the rate
+// (probe: 208 GB/s with a fixed unit-to-CTA assignment, 89-107 GB/s with rows or units
+// claimed dynamically).  With claim counters (a.claim), a unit's batches are still taken
+// in order by its CTA, but CTAs that help (copy_help) may take the last ones.  Without
+// them and with fewer units than CTAs, each unit gets k = ncta / n CTAs, which take its
+// batches in turn (again the same CTAs for the same unit in every step).
+template <int NT, int ROWS, int U>
+__device__ __forceinline__ void gather_rows_ldg(const GatherArgs& a, int cta, int ncta, const CopyScratch& cs,
+                                                bool in_score = false) {
+  static_assert(ROWS <= NT, "one thread per row of a batch fetches its addresses");
+  const int tid = threadIdx.x;
+  int64_t moved = 0;
+  if (tid == 0) cs.word[0] = 0;
+  __syncthreads();
+  if (a.claim) {
+    for (int i = cta; i < a.n; i += ncta) moved += copy_claimed<NT, ROWS, U>(a, i, cs);
+  } else {
+    const int k = a.n >= ncta || a.n <= 0 ? 1 : ncta / a.n;
+    const int first = k == 1 ? cta : cta / k, sub = k == 1 ? 0 : cta % k;
+    const int ustep = k == 1 ? ncta : a.n;
+    for (int i = first; i < a.n; i += ustep)
+      for (int64_t b0 = a.miss_off[i] + (int64_t)sub * ROWS; b0 < a.miss_off[i + 1]; b0 += (int64_t)k * ROWS) {
+        const int64_t R_i = a.miss_off[i + 1];
+        const int nrow = (int)((R_i - b0) < ROWS ? (R_i - b0) : ROWS);
+        copy_batch<NT, U>(a, i, b0, nrow, cs);
+        moved += nrow;
+      }
+  }
+  __syncthreads();
+  copy_stats(a, moved, cs, in_score);
+}
+
+// A CTA that has finished its own work takes the batches the copying CTAs have not yet
+// claimed, scanning the units from the end of the list (the copying CTAs take theirs
+// from the front).  When the copy keeps pace with the scoring, nothing is left.
+template <int NT, int ROWS, int U>
+__device__ __forceinline__ void copy_help(const GatherArgs& a, const CopyScratch& cs) {
+  const int tid = threadIdx.x;
+  int64_t moved = 0;
+  if (tid == 0) cs.word[0] = 0;
+  for (int base = 0; base < a.n; base += NT) {
+    if (tid == 0) cs.word[2] = 0;
+    __syncthreads();
+    if (base + tid < a.n) {
+      const int i = a.n - 1 - (base + tid);
+      const int64_t rows = a.miss_off[i + 1] - a.miss_off[i];
+      const int nb = (int)((rows + ROWS - 1) / ROWS);
+      if (*reinterpret_cast<const volatile int32_t*>(&a.claim[i]) < nb) cs.list[atomicAdd(&cs.word[2], 1u)] = i;
+    }
+    __syncthreads();
+    const int cnt = (int)cs.word[2];
+    for (int e = 0; e < cnt; ++e) moved += copy_claimed<NT, ROWS, U>(a, cs.list[e], cs);
+    __syncthreads();
+  }
+  copy_stats(a, moved, cs, true);
+}
 
 template <int PP, class KF>
 struct ScorerFor {

@@ -199,6 +199,7 @@ struct GatherArgs {
   const int64_t* miss_off;     // [n+1]
   const int32_t* miss_cnt;     // [n] (the deferred fill's flush)
   int32_t pk;                  // stride of the miss lists
+  int32_t* claim;              // [n] batches claimed per unit (zero before the launch), or nullptr
   DevStats* stats;
   uint32_t* err;
   uint64_t wait_ns;

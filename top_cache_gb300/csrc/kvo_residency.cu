@@ -85,7 +85,11 @@ __global__ void __launch_bounds__(kResThreads) residency_kernel(ResidencyArgs a)
 // gather, 16-byte loads from the mapped host pool (zero copy)
 // ---------------------------------------------------------------------------
 __global__ void __launch_bounds__(kGatherThreads) gather_ldg_kernel(GatherArgs a) {
-  dev::gather_rows_ldg<kGatherThreads, kGatherRows, 8>(a, (int)blockIdx.x, (int)gridDim.x);
+  __shared__ int64_t src_off[kGatherRows];
+  __shared__ int64_t dst_off[kGatherRows];
+  __shared__ uint32_t word[4];
+  const dev::CopyScratch cs{src_off, dst_off, nullptr, word};
+  dev::gather_rows_ldg<kGatherThreads, kGatherRows, 8>(a, (int)blockIdx.x, (int)gridDim.x, cs);
 }
 
 // ---------------------------------------------------------------------------

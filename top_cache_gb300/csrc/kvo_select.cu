@@ -86,10 +86,26 @@ __global__ void __launch_bounds__(1024) plan_kernel(SelectArgs a) {
   plan_body<1024>(a, threadIdx.x, warp_sums, &carry);
 }
 
-// The copying CTAs' part of a score launch, a separate function so that its
-// registers (12 loads in flight per thread) do not constrain the scoring code's.
-__device__ __noinline__ void score_launch_copy(const GatherArgs& g, int cta, int ncta) {
-  gather_rows_ldg<kScoreThreads, kScoreGatherRows, 12>(g, cta, ncta, true);
+// The copying part of a score launch (the previous unit group's miss rows), in
+// separate functions so that their registers (12 loads in flight per thread) do
+// not constrain the scoring code's.  Scratch: the start of the CTA's dynamic
+// shared memory (unused by a copying CTA; a scoring CTA's key ring once it has
+// scored).
+__device__ __forceinline__ CopyScratch copy_scratch(uint8_t* smem) {
+  int64_t* src = reinterpret_cast<int64_t*>(smem);
+  int64_t* dst = src + kScoreGatherRows;
+  int32_t* list = reinterpret_cast<int32_t*>(dst + kScoreGatherRows);
+  return CopyScratch{src, dst, list, reinterpret_cast<uint32_t*>(list + kScoreThreads)};
+}
+__device__ __noinline__ void score_launch_copy(const GatherArgs& g, int cta, int ncta, uint8_t* smem) {
+  gather_rows_ldg<kScoreThreads, kScoreGatherRows, 12>(g, cta, ncta, copy_scratch(smem), true);
+}
+// Every thread of a scoring CTA calls it after its part of the scoring (the
+// producer warp and the consumer warps from different places): the barrier
+// below is where the key ring becomes free (every tile issued has been used).
+__device__ __noinline__ void score_launch_help(const GatherArgs& g, uint8_t* smem) {
+  __syncthreads();
+  copy_help<kScoreThreads, kScoreGatherRows, 12>(g, copy_scratch(smem));
 }
 
 // ---------------------------------------------------------------------------
@@ -104,7 +120,7 @@ __global__ void __launch_bounds__(kScoreThreads, 1) score_kernel(SelectArgs a) {
 
   if ((int)blockIdx.x < a.gather_ctas) {
     // the previous unit group's miss rows, copied while this group is scored
-    score_launch_copy(a.prev, (int)blockIdx.x, a.gather_ctas);
+    score_launch_copy(a.prev, (int)blockIdx.x, a.gather_ctas, smem);
     return;
   }
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -120,7 +136,14 @@ __global__ void __launch_bounds__(kScoreThreads, 1) score_kernel(SelectArgs a) {
     fence_mbar_init();
   }
   __syncthreads();
-  if (g0 >= g1) return;
+  // scoring CTAs of a launch that also copies the previous group's rows take the rows
+  // its copying CTAs have not yet claimed once their own scoring is done
+  // (the condition is read from the kernel parameters where it is used, so that no
+  // register holds it across the scoring loop)
+  if (g0 >= g1) {
+    if (a.gather_ctas > 0 && a.prev.claim) score_launch_help(a.prev, smem);
+    return;
+  }
 
   if (warp == kCW) {
     // ---------------- producer: stream every tile of every piece ----------
@@ -142,6 +165,7 @@ __global__ void __launch_bounds__(kScoreThreads, 1) score_kernel(SelectArgs a) {
         }
       }
     }
+    if (a.gather_ctas > 0 && a.prev.claim) score_launch_help(a.prev, smem);
     return;
   }
 
@@ -177,6 +201,7 @@ __global__ void __launch_bounds__(kScoreThreads, 1) score_kernel(SelectArgs a) {
     }
     piece_end(sm, P, k, cap, gth, (int64_t)c + i, a.seg_keys, a.seg_cnt, ctid);
   }
+  if (a.gather_ctas > 0 && a.prev.claim) score_launch_help(a.prev, smem);
 }
 
 // int8 indexer: rotation and quantization of n keys (one warp per key).
