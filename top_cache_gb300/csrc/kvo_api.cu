@@ -962,7 +962,7 @@ int kvo_step(kvo_handle* h, const int32_t* units, int32_t n_units, const void* q
       sa.bytes_prev = h->bytes_prev_dev;
       sa.bytes_seen = h->bytes_seen;
     }
-    if (sa.q8)  // int8 indexer: this group's queries, one warp each
+    if (sa.q8 && e == cudaSuccess)  // int8 indexer: this group's queries, one warp each
       e = timed(h, KVO_PROF_PLAN, s, [&] {
         return kvo::launch_quant_keys(sa.queries, (int64_t)ng * h->P, sa.q8, sa.qscale, s);
       });
