@@ -134,14 +134,15 @@ def test_unit_groups_two_streams(groups, path):
     _run(wl, options={K.KVO_OPT_GROUPS: groups})
 
 
-@pytest.mark.parametrize("groups,sms", [(2, 8), (3, 32), (5, 2)])
-def test_unit_groups_split_sms(groups, sms, path):
+@pytest.mark.parametrize("groups,sms,int8", [(2, 8, False), (3, 32, False), (5, 2, False), (2, 8, True)])
+def test_unit_groups_split_sms(groups, sms, int8, path):
     _staged_only(path)
     # the first `sms` CTAs of each group's score launch copy the previous group's rows
-    # while the others score (KVO_OPT_GROUP_GATHER_SMS): results as without groups
+    # while the others score, then help with what is left (KVO_OPT_GROUP_GATHER_SMS):
+    # results as without groups, each row copied once
     wl = W.reduced(W.WORKLOADS["batch16x8_32k_mtp3"], n_requests=3, n_layers=2, context=3001,
                    topk=256, hot_capacity=600, steps=5)
-    _run(wl, options={K.KVO_OPT_GROUPS: groups, K.KVO_OPT_GROUP_GATHER_SMS: sms})
+    _run(wl, idx_int8=int8, options={K.KVO_OPT_GROUPS: groups, K.KVO_OPT_GROUP_GATHER_SMS: sms})
 
 
 def test_few_score_ctas_long_pieces(path):
