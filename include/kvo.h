@@ -176,11 +176,13 @@ typedef struct kvo_stats {
 #define KVO_OPT_GROUP_GATHER_SMS 12 /* staged step in unit groups: 0 copies each group's miss rows
                                    on a library stream beside the next group's scoring; s in
                                    1 .. SMs/2 makes the first s CTAs of group g+1's score launch
-                                   (one per SM) copy group g's rows while the others score, all
-                                   on the caller's stream (the last group's rows use every SM
-                                   after its residency update).  Default 0 with KVO_OPT_GROUPS
-                                   set by the caller, 4/25 of the SMs in the two-group step that
-                                   KVO_OPT_FUSED = 2 chooses */
+                                   (one per SM) copy group g's rows while the others score and
+                                   then take the copy batches not yet claimed, all on the
+                                   caller's stream (the last group's rows use every SM after its
+                                   residency update).  Default 0 with KVO_OPT_GROUPS set by the
+                                   caller; the two-group step that KVO_OPT_FUSED = 2 chooses uses
+                                   4/25 of the SMs unless this option was set (kvo_get_option
+                                   returns the value set, 0 if none) */
 #define KVO_OPT_PROFILE_KINDS 13 /* with KVO_OPT_PROFILE 1: bit (1 << KVO_PROF_x) set brackets the
                                    launches of kind x with events (default every kind); each
                                    pair of events adds a few microseconds between launches */
