@@ -61,3 +61,19 @@ def test_numa_spread_of_a_host_buffer():
     if spread is not None:  # /proc/self/numa_maps readable
         assert all(k.startswith("N") for k in spread)
         assert abs(sum(spread.values()) - 1.0) < 1e-3
+
+
+def test_timed_region_profiles_the_roofline_kernels_only():
+    # the kinds bracketed with events inside the timed region are names the library
+    # profiles, and the mask passed to KVO_OPT_PROFILE_KINDS has exactly their bits
+    from top_cache_gb300 import kvo as K
+    for name in bench.TIMED_KINDS:
+        assert name in K.PROF_KINDS
+    mask = bench._kinds_mask(bench.TIMED_KINDS)
+    assert mask == sum(1 << K.PROF_KINDS.index(n) for n in ("score", "gather", "fused"))
+    assert 0 < mask < (1 << len(K.PROF_KINDS))
+    # the committed figures cover the default workload's dominant kernels
+    with open(os.path.join(ROOT, "profiles", "traffic.json")) as f:
+        t = json.load(f)
+    for kernel in ("score", "gather"):
+        assert t[kernel]["workload"] == bench.DEFAULT_WORKLOAD
